@@ -1,0 +1,172 @@
+"""FP64 CPU oracle for the selected-token log-probability path.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The product library
+(``selected_token_logprob_gb300``) never imports it, and the two share no code:
+the oracle is plain C in IEEE double (``logp_oracle.c``), built with gcc, plus
+this ctypes loader that marshals numpy arrays.
+
+What each function computes, and the passage it follows, is stated in the C
+file.  BF16 arrays are passed as ``numpy.uint16`` bit patterns.
+
+Parity status: every oracle function is pinned by CPU tests against closed
+forms, brute force, finite differences or a library routine (see
+``tests/test_oracle_pins.py``); none is "parity unpinned".
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "logp_oracle.c")
+_LIB = os.path.join(_HERE, "liblogp_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_F64P = np.ctypeslib.ndpointer(dtype=np.float64, flags="C_CONTIGUOUS")
+_F32P = np.ctypeslib.ndpointer(dtype=np.float32, flags="C_CONTIGUOUS")
+_U16P = np.ctypeslib.ndpointer(dtype=np.uint16, flags="C_CONTIGUOUS")
+_I64P = np.ctypeslib.ndpointer(dtype=np.int64, flags="C_CONTIGUOUS")
+_I64 = ctypes.c_int64
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (OpenMP, no FP contraction) if stale."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+           "-ffp-contract=off", "-fno-fast-math", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        build()
+        lib = ctypes.CDLL(_LIB)
+        lib.oracle_round_bf16.restype = ctypes.c_uint16
+        lib.oracle_round_bf16.argtypes = [ctypes.c_double]
+        lib.oracle_round_bf16_array.argtypes = [_F64P, _U16P, _I64]
+        lib.oracle_bf16_to_double_array.argtypes = [_U16P, _F64P, _I64]
+        lib.oracle_forward.argtypes = [_U16P, _I64, _I64, _I64, _I64P, _I64, _F64P, _F64P]
+        lib.oracle_backward.argtypes = [_U16P, _I64, _I64, _I64, _I64P, _I64, _F32P, _F64P, _I64]
+        lib.oracle_backward_compare.argtypes = [_U16P, _I64, _I64, _I64, _I64P, _I64, _F32P,
+                                                _U16P, _I64, _F64P, _I64P]
+        lib.oracle_range_partials.argtypes = [_U16P, _I64, _I64, _I64, _I64, _I64, _F64P, _F64P]
+        lib.oracle_merge_partials.argtypes = [_F64P, _F64P, _I64, _I64, _F64P]
+        lib.oracle_num_threads.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _u16(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError("BF16 arrays are passed as uint16 bit patterns")
+    return a
+
+
+def _shape(x: np.ndarray, v: int | None):
+    """(n, v, ld) of a 2-D BF16 bit array whose first v columns are the row."""
+    if x.ndim != 2:
+        raise ValueError("logits must be 2-D")
+    n, ld = x.shape
+    return n, (ld if v is None else v), ld
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def round_bf16(d) -> np.ndarray:
+    """Nearest BF16 (ties to even) of each double, as uint16 bit patterns."""
+    d = np.asarray(d, dtype=np.float64)
+    flat = np.ascontiguousarray(d.reshape(-1))
+    out = np.empty(flat.shape, dtype=np.uint16)
+    _load().oracle_round_bf16_array(flat, out, flat.size)
+    return out.reshape(d.shape)
+
+
+def bf16_to_f64(b) -> np.ndarray:
+    b = np.asarray(b)
+    flat = _u16(b.reshape(-1))
+    out = np.empty(flat.shape, dtype=np.float64)
+    _load().oracle_bf16_to_double_array(flat, out, flat.size)
+    return out.reshape(b.shape)
+
+
+def forward(x, y, ignore_index: int = -100, v: int | None = None):
+    """FP64 (logp[n], lse[n]) of BF16 logits x[n, ld] (first v columns)."""
+    x = _u16(x)
+    n, v, ld = _shape(x, v)
+    y = np.ascontiguousarray(y, dtype=np.int64)
+    logp = np.empty(n, dtype=np.float64)
+    lse = np.empty(n, dtype=np.float64)
+    _load().oracle_forward(x, n, v, ld, y, ignore_index, logp, lse)
+    return logp, lse
+
+
+def backward(x, y, g, ignore_index: int = -100, v: int | None = None) -> np.ndarray:
+    """Dense FP64 gradient d[n, v] (small shapes only)."""
+    x = _u16(x)
+    n, v, ld = _shape(x, v)
+    y = np.ascontiguousarray(y, dtype=np.int64)
+    g = np.ascontiguousarray(g, dtype=np.float32)
+    d = np.empty((n, v), dtype=np.float64)
+    _load().oracle_backward(x, n, v, ld, y, ignore_index, g, d, v)
+    return d
+
+
+def backward_compare(x, y, g, dl, ignore_index: int = -100, v: int | None = None) -> dict:
+    """Stream-compare a BF16 gradient dl[n, ld_out] with the FP64 gradient."""
+    x = _u16(x)
+    dl = _u16(dl)
+    n, v, ld = _shape(x, v)
+    if dl.ndim != 2 or dl.shape[0] != n or dl.shape[1] < v:
+        raise ValueError("dlogits shape mismatch")
+    y = np.ascontiguousarray(y, dtype=np.int64)
+    g = np.ascontiguousarray(g, dtype=np.float32)
+    stats = np.zeros(3, dtype=np.float64)
+    counts = np.zeros(3, dtype=np.int64)
+    _load().oracle_backward_compare(x, n, v, ld, y, ignore_index, g, dl, dl.shape[1],
+                                    stats, counts)
+    return {
+        "max_abs_diff": float(stats[0]),
+        "max_abs_d": float(stats[1]),
+        "max_rounding_gap": float(stats[2]),
+        "n_compared": int(counts[0]),
+        "n_not_correctly_rounded": int(counts[1]),
+        "n_nonfinite": int(counts[2]),
+    }
+
+
+def range_partials(x, w: int, k: int, v: int | None = None):
+    """FP64 (m, s) partials [n, k] over consecutive column ranges of width w."""
+    x = _u16(x)
+    n, v, ld = _shape(x, v)
+    pm = np.empty((n, k), dtype=np.float64)
+    ps = np.empty((n, k), dtype=np.float64)
+    _load().oracle_range_partials(x, n, v, ld, w, k, pm, ps)
+    return pm, ps
+
+
+def merge_partials(pm, ps) -> np.ndarray:
+    """FP64 LSE[n] from partials [n, k] merged in index order."""
+    pm = np.ascontiguousarray(pm, dtype=np.float64)
+    ps = np.ascontiguousarray(ps, dtype=np.float64)
+    n, k = pm.shape
+    lse = np.empty(n, dtype=np.float64)
+    _load().oracle_merge_partials(pm, ps, n, k, lse)
+    return lse

@@ -1,0 +1,398 @@
+"""Pins of the FP64 oracle against facts fixed outside the oracle itself.
+
+Each test is chosen so that a plausible slip in the oracle (a dropped term, a
+wrong sign or index, a missing max shift, a double rounding, a miscounted
+comparison) fails at least one of them:
+
+* closed forms from tests/golden/closed_forms.txt (uniform rows, V = 1, V = 2,
+  masked tails, inactive rows, closed-form gradients);
+* brute-force nearest-BF16 search for the rounding routine;
+* Richardson-extrapolated central differences of the oracle's own forward
+  (gradient sign, the one-hot term, the g scaling);
+* central differences of a library routine (torch float64 log_softmax);
+* a library cross-check of the forward (torch float64 log_softmax + gather);
+* 50-digit decimal brute force for a few tiny rows;
+* invariants: shift and permutation invariance, rows summing to zero, the
+  sharded merge equalling the unsharded log-sum-exp.
+"""
+
+import math
+import struct
+from decimal import Decimal, getcontext
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from golden import closed_forms, to_bf16_bits_exact
+
+IGN = -100
+
+
+def _bits(vals):
+    return to_bf16_bits_exact(vals)
+
+
+def _rand_bf16(rng, n, v, sigma=2.0):
+    f = (rng.standard_normal((n, v)) * sigma).astype(np.float32)
+    return workloads.bf16_bits(torch.from_numpy(f).to(torch.bfloat16))
+
+
+# ---------------------------------------------------------------- rounding
+
+
+def _bf16_value(b):
+    return struct.unpack("<f", struct.pack("<I", (int(b) & 0xFFFF) << 16))[0]
+
+
+def _brute_nearest_bf16(d):
+    """Nearest BF16 by search over all patterns near d's binary32 truncation;
+    ties go to the even pattern."""
+    if math.isnan(d):
+        return None
+    f32 = struct.unpack("<I", struct.pack("<f", np.float32(d)))[0] if abs(d) < 3.4e38 else None
+    if f32 is None:
+        return 0x7F80 | (0x8000 if d < 0 else 0)
+    top = f32 >> 16
+    cands = []
+    for k in range(-3, 4):
+        b = (top + k) & 0xFFFF
+        if (b & 0x7F80) == 0x7F80 and (b & 0x7F):
+            continue  # NaN patterns
+        val = _bf16_value(b)
+        if math.isinf(val) and not math.isinf(d):
+            # inf is the result only when |d| reaches max + half ulp
+            if abs(d) < (2 - 2 ** -8) * 2.0 ** 127:
+                continue
+        cands.append((abs(val - d) if not math.isinf(val) else 0.0, b))
+    best = min(c[0] for c in cands)
+    ties = [b for dist, b in cands if dist == best]
+    # ties: prefer even significand, and among equal values prefer the
+    # pattern whose sign matches d (so -0 rounds to -0)
+    ties.sort(key=lambda b: (b & 1, (b >> 15) != (1 if math.copysign(1, d) < 0 else 0)))
+    return ties[0]
+
+
+def test_round_bf16_known_values():
+    cases = {
+        1.0: 0x3F80,
+        -1.0: 0xBF80,
+        1.0 + 2 ** -8: 0x3F80,          # tie, even stays
+        1.0 + 3 * 2 ** -8: 0x3F82,      # tie, rounds up to even
+        1.0 + 2 ** -8 + 2 ** -30: 0x3F81,  # just above the tie
+        2.0 ** -133: 0x0001,            # smallest subnormal
+        2.0 ** -134: 0x0000,            # tie with zero, even
+        3 * 2.0 ** -134: 0x0002,        # tie, even
+        255 * 2.0 ** 120: 0x7F7F,       # largest finite
+        255.5 * 2.0 ** 120: 0x7F80,     # overflow at max + half ulp
+        -0.0: 0x8000,
+        float("inf"): 0x7F80,
+        float("-inf"): 0xFF80,
+    }
+    for d, want in cases.items():
+        assert int(oracle.round_bf16(d)) == want, (d, hex(int(oracle.round_bf16(d))))
+    assert int(oracle.round_bf16(float("nan"))) & 0x7FFF > 0x7F80
+
+
+def test_round_bf16_matches_brute_force():
+    rng = np.random.default_rng(1)
+    d = np.concatenate([
+        rng.standard_normal(3000) * 10.0 ** rng.integers(-40, 38, 3000),
+        rng.standard_normal(500) * 2.0 ** -128,     # subnormal range
+        (1 + (2 * rng.integers(0, 128, 200) + 1) * 2.0 ** -8) * 2.0 ** rng.integers(-20, 20, 200),  # ties
+    ])
+    got = oracle.round_bf16(d)
+    for di, gi in zip(d, got):
+        assert int(gi) == _brute_nearest_bf16(float(di)), (di, hex(int(gi)))
+
+
+def test_round_bf16_is_not_double_rounding():
+    # d sits just above a BF16 tie, but its binary32 rounding lands exactly on
+    # the tie; rounding via binary32 would then go to even (down).
+    d = 1.0 + 2 ** -8 + 2 ** -40
+    assert int(oracle.round_bf16(d)) == 0x3F81
+
+
+def test_bf16_widening_exact():
+    b = np.arange(0, 65536, dtype=np.uint16)
+    got = oracle.bf16_to_f64(b)
+    want = np.array([_bf16_value(i) for i in range(65536)], dtype=np.float64)
+    finite = ~np.isnan(want)
+    assert np.array_equal(got[finite], want[finite])
+    assert np.all(np.isnan(got[~finite]))
+
+
+# ---------------------------------------------------------------- closed forms
+
+
+@pytest.mark.parametrize("case", closed_forms(), ids=lambda c: c["name"])
+def test_closed_forms(case):
+    x = _bits(case["logits"])[None, :]
+    y = np.array([case["target"]], dtype=np.int64)
+    logp, lse = oracle.forward(x, y, IGN)
+    assert abs(logp[0] - case["logp"]) <= 1e-13 * max(1.0, abs(case["logp"]))
+    assert abs(lse[0] - case["lse"]) <= 1e-13 * max(1.0, abs(case["lse"]))
+    if case["dlogits"] is not None:
+        g = np.array([case["grad"]], dtype=np.float32)
+        d = oracle.backward(x, y, g, IGN)
+        np.testing.assert_allclose(d[0], case["dlogits"], rtol=0, atol=1e-14)
+
+
+def test_inactive_rows_are_exact_zero():
+    rng = np.random.default_rng(2)
+    x = _rand_bf16(rng, 6, 37)
+    y = np.array([-100, 37, 40, -1, 5, 36], dtype=np.int64)
+    g = np.ones(6, dtype=np.float32)
+    logp, _ = oracle.forward(x, y, IGN)
+    d = oracle.backward(x, y, g, IGN)
+    for t in range(4):
+        assert logp[t] == 0.0 and np.all(d[t] == 0.0)
+    assert logp[4] < 0 and np.any(d[4] != 0)
+    # an ignore index inside [0, V) also deactivates its rows
+    logp2, _ = oracle.forward(x, y, 5)
+    assert logp2[4] == 0.0
+
+
+# ---------------------------------------------------------------- library and brute force
+
+
+def test_forward_matches_torch_float64_log_softmax():
+    rng = np.random.default_rng(3)
+    for n, v in [(16, 1), (16, 7), (32, 1031), (4, workloads.QWEN3_VOCAB)]:
+        x = _rand_bf16(rng, n, v, sigma=3.0)
+        y = rng.integers(0, v, n).astype(np.int64)
+        logp, lse = oracle.forward(x, y, IGN)
+        xt = torch.from_numpy(oracle.bf16_to_f64(x))
+        ref_lsm = torch.log_softmax(xt, dim=1)
+        ref_logp = ref_lsm.gather(1, torch.from_numpy(y)[:, None])[:, 0].numpy()
+        ref_lse = torch.logsumexp(xt, dim=1).numpy()
+        np.testing.assert_allclose(logp, ref_logp, rtol=0, atol=1e-11)
+        np.testing.assert_allclose(lse, ref_lse, rtol=1e-13, atol=1e-12)
+
+
+def test_forward_decimal_brute_force():
+    getcontext().prec = 50
+    rng = np.random.default_rng(4)
+    x = _rand_bf16(rng, 5, 9, sigma=4.0)
+    y = np.array([0, 3, 8, 4, 1], dtype=np.int64)
+    logp, lse = oracle.forward(x, y, IGN)
+    xv = oracle.bf16_to_f64(x)
+    for t in range(5):
+        s = sum(Decimal(float(v)).exp() for v in xv[t])
+        want_lse = s.ln()
+        want_logp = Decimal(float(xv[t, y[t]])) - want_lse
+        assert abs(Decimal(lse[t]) - want_lse) < Decimal("1e-14")
+        assert abs(Decimal(logp[t]) - want_logp) < Decimal("1e-14")
+
+
+def test_gradient_against_decimal_softmax():
+    getcontext().prec = 50
+    rng = np.random.default_rng(5)
+    x = _rand_bf16(rng, 3, 6, sigma=2.0)
+    y = np.array([0, 5, 2], dtype=np.int64)
+    g = np.array([1.5, -0.25, 3.0], dtype=np.float32)
+    d = oracle.backward(x, y, g, IGN)
+    xv = oracle.bf16_to_f64(x)
+    for t in range(3):
+        e = [Decimal(float(v)).exp() for v in xv[t]]
+        s = sum(e)
+        for c in range(6):
+            want = Decimal(float(g[t])) * ((1 if c == y[t] else 0) - e[c] / s)
+            assert abs(Decimal(d[t, c]) - want) < Decimal("1e-15")
+
+
+# ---------------------------------------------------------------- finite differences
+
+
+def test_gradient_by_richardson_central_differences_of_oracle_forward():
+    """d logp / d x_v of the oracle's own forward, with perturbations that keep
+    every logit an exact BF16 value: logits are small integers in [2, 4), where
+    x +- 2^-5 and x +- 2^-6 are BF16 numbers."""
+    rng = np.random.default_rng(6)
+    v = 12
+    base = rng.integers(2, 4, v).astype(np.float64) + rng.integers(0, 8, v) * 2.0 ** -3
+    y = np.array([4], dtype=np.int64)
+    g = np.array([1.0], dtype=np.float32)
+    d = oracle.backward(_bits(base)[None, :], y, g, IGN)[0]
+
+    def logp_at(xs):
+        return oracle.forward(_bits(xs)[None, :], y, IGN)[0][0]
+
+    for c in range(v):
+        est = []
+        for h in (2.0 ** -5, 2.0 ** -6):
+            xp, xm = base.copy(), base.copy()
+            xp[c] += h
+            xm[c] -= h
+            est.append((logp_at(xp) - logp_at(xm)) / (2 * h))
+        rich = (4 * est[1] - est[0]) / 3
+        assert abs(rich - d[c]) < 2e-7, (c, rich, d[c])
+
+
+def test_gradient_by_central_differences_of_torch_log_softmax():
+    rng = np.random.default_rng(7)
+    v = 20
+    x = _rand_bf16(rng, 1, v, sigma=1.5)
+    y = np.array([13], dtype=np.int64)
+    g = np.array([-2.5], dtype=np.float32)
+    d = oracle.backward(x, y, g, IGN)[0]
+    xv = torch.from_numpy(oracle.bf16_to_f64(x)[0])
+    h = 1e-6
+    for c in range(v):
+        xp, xm = xv.clone(), xv.clone()
+        xp[c] += h
+        xm[c] -= h
+        fd = (torch.log_softmax(xp, 0)[13] - torch.log_softmax(xm, 0)[13]).item() / (2 * h)
+        assert abs(float(g[0]) * fd - d[c]) < 1e-8
+
+
+# ---------------------------------------------------------------- invariants
+
+
+def test_rows_sum_to_zero_and_uniform_gradient():
+    rng = np.random.default_rng(8)
+    x = _rand_bf16(rng, 8, 1031, sigma=3.0)
+    y = rng.integers(0, 1031, 8).astype(np.int64)
+    g = rng.standard_normal(8).astype(np.float32)
+    d = oracle.backward(x, y, g, IGN)
+    for t in range(8):
+        assert abs(d[t].sum()) <= 1e-12 * max(1.0, abs(float(g[t])))
+        assert np.sign(d[t, y[t]]) == np.sign(g[t]) or g[t] == 0
+        off = np.delete(d[t], y[t])
+        assert np.all(np.sign(off) * np.sign(g[t]) <= 0)
+
+
+def test_shift_invariance():
+    rng = np.random.default_rng(9)
+    # integer-valued logits stay exact BF16 numbers after adding an integer
+    xi = rng.integers(-40, 40, (4, 200)).astype(np.float64)
+    y = rng.integers(0, 200, 4).astype(np.int64)
+    a_logp, a_lse = oracle.forward(_bits(xi), y, IGN)
+    b_logp, b_lse = oracle.forward(_bits(xi + 64.0), y, IGN)
+    np.testing.assert_allclose(a_logp, b_logp, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(b_lse - a_lse, 64.0, rtol=0, atol=1e-12)
+
+
+def test_large_logits_do_not_overflow():
+    # exp(1024) overflows a double: a missing max shift would give inf/nan
+    xi = np.array([[1024.0, 1016.0, 1008.0, 1024.0]])
+    logp, lse = oracle.forward(_bits(xi), np.array([1], dtype=np.int64), IGN)
+    want = -8.0 - math.log(2 + math.exp(-8) + math.exp(-16))
+    assert abs(logp[0] - want) < 1e-13 and math.isfinite(lse[0])
+
+
+def test_permutation_invariance():
+    rng = np.random.default_rng(10)
+    x = _rand_bf16(rng, 3, 300)
+    y = np.array([7, 150, 299], dtype=np.int64)
+    logp, lse = oracle.forward(x, y, IGN)
+    perm = rng.permutation(300)
+    inv = np.argsort(perm)
+    logp2, lse2 = oracle.forward(np.ascontiguousarray(x[:, perm]), inv[y], IGN)
+    np.testing.assert_allclose(logp, logp2, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse2, rtol=1e-14)
+
+
+def test_masked_tail_equals_truncated_row():
+    rng = np.random.default_rng(11)
+    x = _rand_bf16(rng, 2, 100)
+    xm = x.copy()
+    xm[:, 60:] = 0xFF80  # -inf
+    y = np.array([3, 59], dtype=np.int64)
+    g = np.array([1.0, -1.0], dtype=np.float32)
+    logp_m, lse_m = oracle.forward(xm, y, IGN)
+    logp_t, lse_t = oracle.forward(np.ascontiguousarray(x[:, :60]), y, IGN)
+    np.testing.assert_allclose(logp_m, logp_t, rtol=0, atol=1e-13)
+    d = oracle.backward(xm, y, g, IGN)
+    assert np.all(d[:, 60:] == 0.0) and np.all(np.isfinite(d))
+
+
+def test_strided_rows_ignore_padding_columns():
+    rng = np.random.default_rng(12)
+    x = _rand_bf16(rng, 3, 64)
+    y = np.array([1, 2, 3], dtype=np.int64)
+    logp, lse = oracle.forward(np.ascontiguousarray(x[:, :50]), y, IGN)
+    logp2, lse2 = oracle.forward(x, y, IGN, v=50)
+    assert np.array_equal(logp, logp2) and np.array_equal(lse, lse2)
+
+
+# ---------------------------------------------------------------- partials and merge
+
+
+@pytest.mark.parametrize("v,w,k", [(1031, 72, 16), (151936, 9496, 16), (151936, 75968, 2),
+                                   (151936, 37984, 4), (255, 16, 16), (9, 8, 16)])
+def test_merge_of_partials_equals_unsharded_lse(v, w, k):
+    rng = np.random.default_rng(13)
+    n = 3 if v > 10000 else 16
+    x = _rand_bf16(rng, n, v, sigma=2.5)
+    pm, ps = oracle.range_partials(x, w, k)
+    lse = oracle.merge_partials(pm, ps)
+    _, lse_ref = oracle.forward(x, np.zeros(n, dtype=np.int64), IGN)
+    np.testing.assert_allclose(lse, lse_ref, rtol=1e-13, atol=0)
+    xv = oracle.bf16_to_f64(x)
+    for j in range(k):
+        c0, c1 = min(j * w, v), min((j + 1) * w, v)
+        if c0 == c1:
+            assert np.all(pm[:, j] == -np.inf) and np.all(ps[:, j] == 0.0)
+        else:
+            assert np.array_equal(pm[:, j], xv[:, c0:c1].max(axis=1))
+
+
+def test_identity_partials_change_nothing():
+    rng = np.random.default_rng(14)
+    x = _rand_bf16(rng, 4, 500)
+    pm, ps = oracle.range_partials(x, 125, 4)
+    lse = oracle.merge_partials(pm, ps)
+    pm2 = np.concatenate([pm, np.full((4, 3), -np.inf)], axis=1)
+    ps2 = np.concatenate([ps, np.zeros((4, 3))], axis=1)
+    assert np.array_equal(oracle.merge_partials(pm2, ps2), lse)
+    assert np.all(oracle.merge_partials(np.full((2, 3), -np.inf), np.zeros((2, 3))) == -np.inf)
+
+
+def test_single_partial_merge_is_m_plus_log_s():
+    pm = np.array([[3.0], [-2.0]])
+    ps = np.array([[5.0], [1.0]])
+    np.testing.assert_allclose(oracle.merge_partials(pm, ps), [3 + math.log(5.0), -2.0],
+                               rtol=1e-15)
+
+
+# ---------------------------------------------------------------- the comparison routine
+
+
+def test_backward_compare_counts_planted_mistakes():
+    rng = np.random.default_rng(15)
+    n, v = 12, 333
+    x = _rand_bf16(rng, n, v)
+    y = rng.integers(0, v, n).astype(np.int64)
+    y[3] = IGN
+    g = rng.standard_normal(n).astype(np.float32)
+    d = oracle.backward(x, y, g, IGN)
+    cr = oracle.round_bf16(d)
+    st = oracle.backward_compare(x, y, g, cr, IGN)
+    assert st["n_compared"] == n * v
+    assert st["n_not_correctly_rounded"] == 0
+    assert st["max_abs_diff"] == st["max_rounding_gap"]
+    assert st["max_abs_d"] == np.abs(d).max()
+    bad = cr.copy()
+    bad[5, 17] ^= 1          # one ulp off
+    bad[3, 0] = 0x3F80       # an inactive row that is not zero
+    st2 = oracle.backward_compare(x, y, g, bad, IGN)
+    assert st2["n_not_correctly_rounded"] == 2
+    assert st2["max_abs_diff"] >= 1.0
+    # strided output with padding columns
+    wide = np.zeros((n, v + 5), dtype=np.uint16)
+    wide[:, :v] = cr
+    assert oracle.backward_compare(x, y, g, wide, IGN)["n_not_correctly_rounded"] == 0
+
+
+def test_workload_recipe_shapes():
+    x, y, g = workloads.make("tiny")
+    assert x.shape == (64, 1024) and x.dtype == torch.bfloat16
+    assert int((y == IGN).sum()) == 6 and g.dtype == torch.float32
+    x2, y2, g2 = workloads.make("tiny")
+    assert torch.equal(x.view(torch.int16), x2.view(torch.int16)) and torch.equal(y, y2)
+    lw = workloads.WORKLOADS["long"]
+    gl = workloads.grads(64, lw.grad, 0)
+    assert torch.all(gl.abs() == 1.0 / 64)
