@@ -1,0 +1,399 @@
+"""Benchmark of the selected-token log-probability hot path on GB300.
+
+One step = forward (logp, lse) + backward (dlogits) over the long-CoT workload
+(N = 32768 rows, V = 151936, BF16 logits ~ N(0, 2^2) plus a +8 spike per row,
+5% ignore rows, g = +-1/N), inputs resident in HBM.  The logits (9.96 GB) and
+dlogits (9.96 GB) are far larger than L2 (129 MB), so no L2 flush is needed
+between steps.
+
+Metric: effective HBM GB/s of forward + backward, counting the algorithmic
+6 bytes per logit (forward: one 2-byte read; backward: one 2-byte read and one
+2-byte write), plus ms per step.  Prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the FP64 CPU oracle on the host cores (a bounded
+sample of rows per step) on the same metric; under torchrun only rank 0 runs
+it.  For N > 1 (torchrun) every rank runs its own replica of the workload on
+its own GPU (weak scaling, no collective on the data path).
+"""
+
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fwd+bwd ms & HBM GB/s (% roofline) at N=32768, V=151936 BF16"
+UNIT = "GB/s"
+BYTES_PER_LOGIT = 6          # fwd read 2 + bwd read 2 + bwd write 2
+BWD_BYTES_PER_LOGIT = 4
+FWD_BYTES_PER_LOGIT = 2
+FALLBACK_HBM_GBS = 6800.0
+# Pages' fused kernel, forward + backward at 32768 x 151936 (B200, BF16):
+# 27.2 ms (RL-Kernel PR #495, Results table).  Context only: another GPU.
+PAGES_FWD_BWD_MS = 27.2
+WORKLOAD_DESC = ("long-CoT: N=32768, V=151936, BF16 logits ~ N(0,2^2) + 8 spike/row, "
+                 "5% ignore_index, g=+-1/N (synthetic)")
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy)"
+    return FALLBACK_HBM_GBS, "fallback 6.8 TB/s"
+
+
+def _kernel_hash() -> str:
+    h = hashlib.sha256()
+    for fn in ("fused_logp.cu", "logp_kernels.cuh"):
+        with open(os.path.join(ROOT, "selected_token_logprob_gb300", "csrc", fn), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _profiled_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
+    was taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", f"{kernel}_long.md")
+    if not os.path.exists(p):
+        return None
+    txt = open(p).read()
+    m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", txt)
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    if not m_hash or not m_bytes or m_hash.group(1) != _kernel_hash():
+        return None
+    return float(m_bytes.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+        return False
+
+    def summary(self):
+        rows = [r for r in csv.reader(io.StringIO(self.out or "")) if len(r) >= 9]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]
+                          and "Not" not in r[5 + i]})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _max_over_ranks(val: float, world: int, device) -> float:
+    if world == 1:
+        return val
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([val], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def run_ours(args):
+    import torch
+
+    import selected_token_logprob_gb300 as flp
+    import workloads
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    flp._lib.load()
+
+    wl = workloads.WORKLOADS[args.workload]
+    n, v = wl.n, wl.v
+    x, y, g = workloads.make(wl, device=dev, seed=wl.seed + rank)
+    logp = torch.empty(n, dtype=torch.float32, device=dev)
+    lse = torch.empty(n, dtype=torch.float32, device=dev)
+    dl = torch.empty((n, v), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        flp.fused_logp_forward(x, y, logp=logp, lse=lse)
+        flp.fused_logp_backward(x, y, lse, g, dlogits=dl)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    _barrier(world)
+    torch.cuda.synchronize(dev)
+    with sampler:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for k in range(args.steps):
+            ev[k][0].record(stream)
+            flp.fused_logp_forward(x, y, logp=logp, lse=lse)
+            ev[k][1].record(stream)
+            flp.fused_logp_backward(x, y, lse, g, dlogits=dl)
+            ev[k][2].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    _barrier(world)
+    total_ms = _max_over_ranks(t0.elapsed_time(t1), world, dev)
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    ms_per_step = total_ms / args.steps
+    logits_per_rank = n * v
+    value = world * logits_per_rank * BYTES_PER_LOGIT / (ms_per_step * 1e-3) / 1e9
+
+    # end to end through the public API from pinned host buffers
+    e2e = run_e2e(args, flp, x, y, g, dev, stream, world)
+
+    peak, peak_src = _peaks()
+    bwd_avg = statistics.mean(bwd_ms)
+    fwd_avg = statistics.mean(fwd_ms)
+    achieved = logits_per_rank * BWD_BYTES_PER_LOGIT / (bwd_avg * 1e-3) / 1e9
+    clocks = sampler.summary()
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": round(value / (logits_per_rank * BYTES_PER_LOGIT / (PAGES_FWD_BWD_MS * 1e-3) / 1e9), 3)
+        if world == 1 else None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC, "n": n, "v": v, "logits_dtype": "bf16",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs (9.96 GB) exceed the 129 MB L2; no flush"},
+        "fwd_ms": round(fwd_avg, 4), "bwd_ms": round(bwd_avg, 4),
+        "fwd_gbs": round(logits_per_rank * FWD_BYTES_PER_LOGIT / (fwd_avg * 1e-3) / 1e9, 1),
+        "bwd_gbs": round(achieved, 1),
+        "roofline": {"kernel": "k_logp_bwd", "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_source": peak_src,
+                     "traffic": _profiled_traffic("k_logp_bwd"),
+                     "fwd_frac": round(logits_per_rank * FWD_BYTES_PER_LOGIT / (fwd_avg * 1e-3)
+                                       / 1e9 / peak, 4),
+                     "step_frac": round(value / world / peak, 4)},
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+        "vs_baseline_note": "pages' fused kernel 27.2 ms fwd+bwd on one B200 (context only)",
+    }
+    if rank == 0:
+        line["cpu_baseline"] = cpu_baseline(args, x, y, g, v)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def run_e2e(args, flp, x, y, g, dev, stream, world):
+    import torch
+
+    n, v = x.shape
+    hx = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    hx.copy_(x)
+    hy = y.cpu().pin_memory()
+    hg = g.cpu().pin_memory()
+    hlogp = torch.empty(n, dtype=torch.float32).pin_memory()
+    hlse = torch.empty(n, dtype=torch.float32).pin_memory()
+    dx = torch.empty_like(x)
+    dy = torch.empty_like(y)
+    dg = torch.empty_like(g)
+    logp = torch.empty(n, dtype=torch.float32, device=dev)
+    lse = torch.empty(n, dtype=torch.float32, device=dev)
+    dl = torch.empty_like(x)
+
+    def step():
+        dx.copy_(hx, non_blocking=True)
+        dy.copy_(hy, non_blocking=True)
+        dg.copy_(hg, non_blocking=True)
+        flp.fused_logp_forward(dx, dy, logp=logp, lse=lse)
+        flp.fused_logp_backward(dx, dy, lse, dg, dlogits=dl)
+        hlogp.copy_(logp, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+
+    steps = max(1, min(args.steps, args.e2e_steps))
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize(dev)
+    _barrier(world)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = _max_over_ranks(a.elapsed_time(b) / steps, world, dev)
+    del hx
+    return {"value": round(world * n * v * BYTES_PER_LOGIT / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
+            "ms_per_step": round(ms, 3), "steps": steps,
+            "h2d_bytes_per_step": n * v * 2 + n * 8 + n * 4,
+            "d2h_bytes_per_step": n * 4 * 2}
+
+
+def _oracle_sample_rate(x_rows_u16, y_np, g_np, v, seconds: float):
+    """GB/s-equivalent of the FP64 oracle (forward + dense backward) on a
+    cycling row sample, for about `seconds` of wall time."""
+    import numpy as np
+
+    import oracle
+
+    chunk = 64
+    rows_done = 0
+    t0 = time.perf_counter()
+    i = 0
+    nrows = x_rows_u16.shape[0]
+    while True:
+        a = (i * chunk) % nrows
+        xb = np.ascontiguousarray(x_rows_u16[a:a + chunk])
+        yb = y_np[a:a + chunk]
+        gb = g_np[a:a + chunk]
+        oracle.forward(xb, yb)
+        oracle.backward(xb, yb, gb)
+        rows_done += xb.shape[0]
+        i += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return rows_done * v * BYTES_PER_LOGIT / el / 1e9, rows_done, el
+
+
+def cpu_baseline(args, x, y, g, v):
+    import oracle
+    import workloads
+
+    if args.cpu_seconds <= 0:
+        return None
+    rows = min(512, x.shape[0])
+    xs = workloads.bf16_bits(x[:rows])
+    rate, done, el = _oracle_sample_rate(xs, y[:rows].cpu().numpy(), g[:rows].cpu().numpy(), v,
+                                         args.cpu_seconds)
+    return {"value": round(rate, 4), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{done} rows of the long-CoT workload (first {rows} rows, cycled), "
+                      f"FP64 forward + dense backward, {el:.1f} s"}
+
+
+def run_reference(args):
+    """The FP64 CPU oracle as the reference arm (rank 0 only)."""
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    import oracle
+    import workloads
+
+    oracle.build()
+    wl = workloads.WORKLOADS[args.workload]
+    rows = args.ref_rows
+    x, y, g = workloads.make(wl, n=rows)   # same recipe, a bounded row sample, on the host
+    xb = workloads.bf16_bits(x)
+    yn, gn = y.numpy(), g.numpy()
+    for _ in range(args.warmup):
+        oracle.forward(xb, yn)
+        oracle.backward(xb, yn, gn)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.forward(xb, yn)
+        oracle.backward(xb, yn, gn)
+        times.append(time.perf_counter() - t0)
+    sec = statistics.mean(times)
+    value = rows * wl.v * BYTES_PER_LOGIT / sec / 1e9
+    sample = (f"{rows} rows of the long-CoT workload per step (FP64 forward + dense backward); "
+              f"GB/s counts the same 6 B/logit")
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": WORKLOAD_DESC, "n": wl.n, "v": wl.v, "rows_per_step": rows},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="long")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-rows", type=int, default=128)
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

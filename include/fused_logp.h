@@ -1,0 +1,152 @@
+/*
+ * fused_logp.h: C ABI of the GB300 selected-token log-probability library
+ * (libfused_logp.so, sm_103a).
+ *
+ * The operation (RL-Kernel issue #241 "TP-aware deterministic logprob",
+ * Background and Goal): for BF16 logits x[N, V] and int64 targets y[N],
+ *     LSE_t  = log sum_v exp(x[t, v])           (FP32 accumulation)
+ *     logp_t = x[t, y_t] - LSE_t
+ * and its gradient (RL-Kernel PR #495 "zero-workspace fused backward",
+ * Summary item 2) for an upstream gradient g[N]:
+ *     dlogits[t, v] = g_t * (onehot(y_t)[v] - exp(x[t, v] - LSE_t))
+ * written straight to BF16 with no FP32 [N, V] workspace.
+ *
+ * A row is ACTIVE when 0 <= y_t < V and y_t != ignore_index.  Inactive rows
+ * get logp = 0 and an all-zero gradient row (PR #495, Behavior changes:
+ * out-of-range targets); their LSE is still computed.
+ *
+ * Vocabulary tiles.  Each row is cut into FLP_NUM_TILES = 16 fixed tiles of
+ * width W = flp_tile_width(V) = 8 * ceil(V / 128) columns (the last ones
+ * clipped or empty).  Every tile is reduced by the same fixed tree whatever N,
+ * the row's position in the batch, or the shard that holds it; the 16 tile
+ * partials are then merged in tile-index order.  This is the tile-level merge
+ * of RL-Kernel PR #314 ("Deterministic config option", the tensor-parallel
+ * section: fixed tiles reduced as the same shape on any rank, then one fixed
+ * merge order), which makes results bitwise independent of N, of the row's
+ * position and of the shard split.
+ *
+ * Conventions for every entry point:
+ *   - Pointers are DEVICE pointers of one CUDA device, owned and allocated by
+ *     the caller.  The library allocates nothing (no workspace, PR #495
+ *     Summary item 2).  BF16 buffers are passed as void pointers to
+ *     IEEE bfloat16 data.  Row-major with a row stride (ld) in elements.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream)
+ *     and run on the device that holds `logits` (or the first device pointer);
+ *     the caller's current device is restored before returning (the device
+ *     guard of PR #495's review thread).
+ *   - All extents and index arithmetic are int64 (PR #495 review: the
+ *     int32 loop overflow near INT_MAX).
+ *   - n == 0 returns FLP_OK without touching the device (PR #495 Tests:
+ *     empty input).
+ *   - Errors are reported by the return code, before any launch, with a
+ *     thread-local message from flp_last_error().  Nothing traps on the GPU.
+ *   - Results are deterministic: repeated calls give identical bits.
+ */
+#ifndef FUSED_LOGP_H
+#define FUSED_LOGP_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum flp_status {
+    FLP_OK = 0,
+    FLP_EINVAL = 1,        /* null pointer, bad extent or stride, host pointer,
+                              pointers on different devices, bad overlap */
+    FLP_EUNSUPPORTED = 2,  /* shard bounds off the tile grid */
+    FLP_ECUDA = 3          /* a CUDA runtime call or the launch failed */
+} flp_status;
+
+/* Same type as cudaStream_t, declared without CUDA headers. */
+typedef struct CUstream_st* flp_stream_t;
+
+#define FLP_NUM_TILES 16
+
+/* Message of the last failing call on this thread ("" after success). */
+const char* flp_last_error(void);
+
+/* Library version string. */
+const char* flp_version(void);
+
+/* Tile width W for a vocabulary of v columns: 8 * ceil(v / 128); 0 if v < 1. */
+int64_t flp_tile_width(int64_t v);
+
+/*
+ * Forward.  For t in [0, n):
+ *   lse[t]  = M + log S, with (M, S) the index-order merge of the 16 tile
+ *             partials (m_k, s_k), m_k = max over tile k, s_k = sum over tile
+ *             k of exp(x - m_k), all FP32; the final log and add are carried
+ *             in FP64 and rounded once to FP32.
+ *   logp[t] = x[t, y_t] - lse (rounded once from FP64) if the row is active,
+ *             else 0.
+ *   logits   [n, ld] BF16, ld >= v >= 1 (columns >= v are never read)
+ *   targets  [n] int64
+ *   logp     [n] FP32 out
+ *   lse      [n] FP32 out (keep it for the backward)
+ * Any alignment and any ld are accepted; 16-byte aligned rows take the
+ * vector path, others a scalar path with the same arithmetic (same bits).
+ * Errors: FLP_EINVAL for n < 0, v < 1, ld < v, a null or host pointer.
+ */
+flp_status fused_logp_forward(const void* logits, int64_t n, int64_t v, int64_t ld,
+                              const int64_t* targets, int64_t ignore_index,
+                              float* logp, float* lse, flp_stream_t stream);
+
+/*
+ * Backward.  dlogits[t, c] for c in [0, v):
+ *   active row:   g_t * (onehot(y_t)[c] - exp(x[t, c] - lse[t])), rounded
+ *                 to nearest-even BF16 once, from an FP32 computation whose
+ *                 exponent argument is carried with its rounding error;
+ *   inactive row: +0.
+ *   logits   [n, ld] BF16
+ *   targets  [n] int64, lse [n] FP32 (from fused_logp_forward), grad [n] FP32
+ *   dlogits  [n, ld_out] BF16 out, ld_out >= v; columns >= v are untouched.
+ * dlogits may alias logits exactly (same pointer and ld == ld_out: the
+ * gradient then overwrites the logits in place); any other overlap is
+ * FLP_EINVAL.  Elementwise, so batch-invariant by construction.
+ */
+flp_status fused_logp_backward(const void* logits, int64_t n, int64_t v, int64_t ld,
+                               const int64_t* targets, int64_t ignore_index,
+                               const float* lse, const float* grad,
+                               void* dlogits, int64_t ld_out, flp_stream_t stream);
+
+/*
+ * Vocab-shard partials (issue #241 PR 3 and PR 6 bullets; PR #314
+ * ReductionSpec).  A shard holds global columns [vocab_start, vocab_start +
+ * real_width) of a v_total-column vocabulary in its own buffer
+ * shard_logits[n, ld_shard] (ld_shard >= real_width; columns >= real_width
+ * are padding, masked to -inf, never read).  For each global tile k the shard
+ * covers, writes part_max[t, k] and part_sum[t, k] (FP32, [n, 16] row-major),
+ * bitwise equal to the forward's own tile partials.  For each row whose
+ * target falls inside the shard, writes sel[t] = x[t, y_t] (the single-owner
+ * copy of the selected logit); other rows' sel is left untouched.
+ * The shard bounds must lie on the tile grid: vocab_start % W == 0, and
+ * real_width % W == 0 unless the shard ends at v_total; otherwise
+ * FLP_EUNSUPPORTED (the capability gate of issue #241 PR 6).
+ * Columns of part_max/part_sum for tiles outside the shard are untouched.
+ */
+flp_status logp_shard_partials(const void* shard_logits, int64_t n, int64_t ld_shard,
+                               int64_t vocab_start, int64_t real_width, int64_t v_total,
+                               const int64_t* targets, float* part_max, float* part_sum,
+                               float* sel, flp_stream_t stream);
+
+/*
+ * Merge (issue #241 PR 3 bullets: M = max m_l, S = sum s_l exp(m_l - M),
+ * LSE = M + log S in fixed index order).  Folds the tile partials [n, 16]
+ * of tiles 0 .. ceil(v_total / W) - 1 in index order with the same arithmetic
+ * as the forward, then writes lse[t] and logp[t] = sel[t] - lse (active rows)
+ * or 0.  Together with logp_shard_partials over shards that cover
+ * [0, v_total), the results are bitwise equal to fused_logp_forward.
+ * sel is read only for active rows.
+ */
+flp_status logp_merge_partials(const float* part_max, const float* part_sum,
+                               const float* sel, const int64_t* targets,
+                               int64_t ignore_index, int64_t n, int64_t v_total,
+                               float* logp, float* lse, flp_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FUSED_LOGP_H */

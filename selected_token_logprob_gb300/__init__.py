@@ -1,0 +1,212 @@
+"""Selected-token log-probability on GB300 (sm_103a).
+
+Thin Python binding of the C ABI in ``include/fused_logp.h``: argument
+checking and marshalling of torch tensors into pointers, sizes and the current
+CUDA stream.  Every step of the computation runs in the library's CUDA
+kernels; torch only provides device memory and streams.  There is no CPU or
+PyTorch fallback: without the built library every call raises.
+
+Entry points (same names as the C ABI):
+    fused_logp_forward(logits, targets, ignore_index) -> (logp, lse)
+    fused_logp_backward(logits, targets, lse, grad, ignore_index) -> dlogits
+    logp_shard_partials(shard_logits, vocab_start, real_width, v_total, targets,
+                        part_max, part_sum, sel)
+    logp_merge_partials(part_max, part_sum, sel, targets, v_total,
+                        ignore_index) -> (logp, lse)
+and ``FusedLogp``, an autograd function that saves only the O(N) LSE.
+
+Logits are BF16 [N, V] (row stride may exceed V: pass a column slice of a
+wider buffer), targets int64 [N], the upstream gradient FP32 [N]; logp and
+lse are FP32 [N].  ``ignore_index`` defaults to -100.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+from ._lib import FusedLogpError
+
+IGNORE_INDEX = -100
+NUM_TILES = 16
+
+__all__ = [
+    "FusedLogp",
+    "FusedLogpError",
+    "IGNORE_INDEX",
+    "NUM_TILES",
+    "flp_tile_width",
+    "fused_logp",
+    "fused_logp_backward",
+    "fused_logp_forward",
+    "logp_merge_partials",
+    "logp_shard_partials",
+]
+
+
+def _stream(t: torch.Tensor) -> int:
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _rows(x: torch.Tensor, name: str):
+    """(n, v, ld) of a 2-D tensor whose rows are contiguous."""
+    if x.dim() != 2:
+        raise ValueError(f"{name} must be 2-D [N, V], got shape {tuple(x.shape)}")
+    n, v = x.shape
+    if v > 1 and x.stride(1) != 1:
+        raise ValueError(f"{name} rows must be contiguous (stride(1) == 1)")
+    ld = x.stride(0) if n > 1 else max(v, x.stride(0))
+    if ld < v:
+        raise ValueError(f"{name} row stride {ld} is smaller than its width {v}")
+    return n, v, ld
+
+
+def _vec(t: torch.Tensor, name: str, n: int, dtype: torch.dtype) -> None:
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != 1 or t.shape[0] != n:
+        raise ValueError(f"{name} must have shape [{n}], got {tuple(t.shape)}")
+    if n > 1 and t.stride(0) != 1:
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _cuda(*ts) -> None:
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("all tensors must be CUDA tensors")
+
+
+def flp_tile_width(v: int) -> int:
+    """Tile width W = 8 * ceil(v / 128) of a v-column vocabulary."""
+    return int(_lib.load().flp_tile_width(int(v)))
+
+
+def fused_logp_forward(logits: torch.Tensor, targets: torch.Tensor,
+                       ignore_index: int = IGNORE_INDEX,
+                       logp: torch.Tensor | None = None, lse: torch.Tensor | None = None):
+    """(logp, lse), FP32 [N] each, of BF16 logits [N, V]."""
+    n, v, ld = _rows(logits, "logits")
+    if logits.dtype != torch.bfloat16:
+        raise TypeError(f"logits must be torch.bfloat16, got {logits.dtype}")
+    _vec(targets, "targets", n, torch.int64)
+    dev = logits.device
+    logp = torch.empty(n, dtype=torch.float32, device=dev) if logp is None else logp
+    lse = torch.empty(n, dtype=torch.float32, device=dev) if lse is None else lse
+    _vec(logp, "logp", n, torch.float32)
+    _vec(lse, "lse", n, torch.float32)
+    _cuda(logits, targets, logp, lse)
+    if n == 0:
+        return logp, lse
+    st = _lib.load().fused_logp_forward(logits.data_ptr(), n, v, ld, targets.data_ptr(),
+                                        int(ignore_index), logp.data_ptr(), lse.data_ptr(),
+                                        _stream(logits))
+    _lib.check("fused_logp_forward", st)
+    return logp, lse
+
+
+def fused_logp_backward(logits: torch.Tensor, targets: torch.Tensor, lse: torch.Tensor,
+                        grad: torch.Tensor, ignore_index: int = IGNORE_INDEX,
+                        dlogits: torch.Tensor | None = None) -> torch.Tensor:
+    """dlogits BF16 [N, V] = grad * (onehot(targets) - softmax(logits)).
+
+    ``dlogits`` may be ``logits`` itself (in-place gradient)."""
+    n, v, ld = _rows(logits, "logits")
+    if logits.dtype != torch.bfloat16:
+        raise TypeError(f"logits must be torch.bfloat16, got {logits.dtype}")
+    _vec(targets, "targets", n, torch.int64)
+    _vec(lse, "lse", n, torch.float32)
+    _vec(grad, "grad", n, torch.float32)
+    if dlogits is None:
+        dlogits = torch.empty((n, v), dtype=torch.bfloat16, device=logits.device)
+    if dlogits.dtype != torch.bfloat16 or tuple(dlogits.shape) != (n, v):
+        raise ValueError("dlogits must be BF16 with the logits' shape")
+    _, _, ld_out = _rows(dlogits, "dlogits")
+    _cuda(logits, targets, lse, grad, dlogits)
+    if n == 0:
+        return dlogits
+    st = _lib.load().fused_logp_backward(logits.data_ptr(), n, v, ld, targets.data_ptr(),
+                                         int(ignore_index), lse.data_ptr(), grad.data_ptr(),
+                                         dlogits.data_ptr(), ld_out, _stream(logits))
+    _lib.check("fused_logp_backward", st)
+    return dlogits
+
+
+def logp_shard_partials(shard_logits: torch.Tensor, vocab_start: int, real_width: int,
+                        v_total: int, targets: torch.Tensor, part_max: torch.Tensor,
+                        part_sum: torch.Tensor, sel: torch.Tensor) -> None:
+    """Write one vocab shard's tile partials into part_max/part_sum [N, 16]
+    and, for rows whose target it owns, the selected logit into sel [N].
+
+    shard_logits is BF16 [N, W_pad] holding global columns
+    [vocab_start, vocab_start + real_width); columns >= real_width are padding
+    and are never read."""
+    n, wpad, ld = _rows(shard_logits, "shard_logits")
+    if shard_logits.dtype != torch.bfloat16:
+        raise TypeError("shard_logits must be torch.bfloat16")
+    if real_width > wpad:
+        raise ValueError(f"real_width {real_width} exceeds the shard width {wpad}")
+    _vec(targets, "targets", n, torch.int64)
+    for name, t in (("part_max", part_max), ("part_sum", part_sum)):
+        if t.dtype != torch.float32 or tuple(t.shape) != (n, NUM_TILES) or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous FP32 [{n}, {NUM_TILES}] tensor")
+    _vec(sel, "sel", n, torch.float32)
+    _cuda(shard_logits, targets, part_max, part_sum, sel)
+    if n == 0:
+        return
+    st = _lib.load().logp_shard_partials(shard_logits.data_ptr(), n, ld, int(vocab_start),
+                                         int(real_width), int(v_total), targets.data_ptr(),
+                                         part_max.data_ptr(), part_sum.data_ptr(),
+                                         sel.data_ptr(), _stream(shard_logits))
+    _lib.check("logp_shard_partials", st)
+
+
+def logp_merge_partials(part_max: torch.Tensor, part_sum: torch.Tensor, sel: torch.Tensor,
+                        targets: torch.Tensor, v_total: int,
+                        ignore_index: int = IGNORE_INDEX,
+                        logp: torch.Tensor | None = None, lse: torch.Tensor | None = None):
+    """(logp, lse) from the tile partials of shards covering [0, v_total)."""
+    n = targets.shape[0] if targets.dim() == 1 else -1
+    _vec(targets, "targets", n, torch.int64)
+    for name, t in (("part_max", part_max), ("part_sum", part_sum)):
+        if t.dtype != torch.float32 or tuple(t.shape) != (n, NUM_TILES) or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous FP32 [{n}, {NUM_TILES}] tensor")
+    _vec(sel, "sel", n, torch.float32)
+    dev = targets.device
+    logp = torch.empty(n, dtype=torch.float32, device=dev) if logp is None else logp
+    lse = torch.empty(n, dtype=torch.float32, device=dev) if lse is None else lse
+    _vec(logp, "logp", n, torch.float32)
+    _vec(lse, "lse", n, torch.float32)
+    _cuda(part_max, part_sum, sel, targets, logp, lse)
+    if n == 0:
+        return logp, lse
+    st = _lib.load().logp_merge_partials(part_max.data_ptr(), part_sum.data_ptr(),
+                                         sel.data_ptr(), targets.data_ptr(), int(ignore_index),
+                                         n, int(v_total), logp.data_ptr(), lse.data_ptr(),
+                                         _stream(targets))
+    _lib.check("logp_merge_partials", st)
+    return logp, lse
+
+
+class FusedLogp(torch.autograd.Function):
+    """logp = FusedLogp.apply(logits, targets, ignore_index); the backward
+    writes dlogits straight to BF16 from the saved FP32 LSE (O(N) state)."""
+
+    @staticmethod
+    def forward(ctx, logits, targets, ignore_index=IGNORE_INDEX):
+        logp, lse = fused_logp_forward(logits, targets, ignore_index)
+        ctx.save_for_backward(logits, targets, lse)
+        ctx.ignore_index = ignore_index
+        return logp
+
+    @staticmethod
+    def backward(ctx, grad_logp):
+        logits, targets, lse = ctx.saved_tensors
+        g = grad_logp.to(torch.float32).contiguous()
+        d = fused_logp_backward(logits, targets, lse, g, ctx.ignore_index)
+        return d, None, None
+
+
+def fused_logp(logits: torch.Tensor, targets: torch.Tensor,
+               ignore_index: int = IGNORE_INDEX) -> torch.Tensor:
+    """Autograd-aware selected-token logp (FP32 [N])."""
+    return FusedLogp.apply(logits, targets, ignore_index)

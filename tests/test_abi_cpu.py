@@ -1,0 +1,142 @@
+"""The C ABI library builds, loads and exports every symbol its header
+declares, and rejects bad arguments on the host before touching any device.
+These run without a GPU: every call here either returns before its first CUDA
+runtime call or fails that call's pointer check."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import selected_token_logprob_gb300 as flp
+from selected_token_logprob_gb300 import _lib
+from selected_token_logprob_gb300 import build as flp_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+EINVAL, EUNSUP = _lib.FLP_EINVAL, _lib.FLP_EUNSUPPORTED
+
+
+@pytest.fixture(scope="module")
+def lib():
+    flp_build.build()
+    return _lib.load()
+
+
+def _declared_functions():
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for fn in sorted(os.listdir(inc)):
+        if not fn.endswith(".h"):
+            continue
+        src = open(os.path.join(inc, fn)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(",
+                            src, flags=re.M)
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert {"fused_logp_forward", "fused_logp_backward", "logp_shard_partials",
+            "logp_merge_partials", "flp_last_error", "flp_tile_width"} <= set(names)
+    for name in names:
+        assert hasattr(lib, name), name
+    assert set(names) == set(_lib.SIGNATURES), "binding signatures out of sync with the header"
+
+
+def test_version_and_tile_width(lib):
+    assert b"sm_103a" in lib.flp_version()
+    for v, w in [(151936, 9496), (1024, 64), (1, 8), (0, 0), (255, 16), (1031, 72), (128, 8),
+                 (129, 16), (2**40, 2**40 // 16)]:
+        assert lib.flp_tile_width(v) == w, (v, w)
+    assert flp.flp_tile_width(151936) == 9496
+
+
+def test_empty_input_is_ok_without_device(lib):
+    assert lib.fused_logp_forward(None, 0, 10, 10, None, -100, None, None, None) == 0
+    assert lib.flp_last_error() == b""
+    assert lib.fused_logp_backward(None, 0, 10, 10, None, -100, None, None, None, 10, None) == 0
+    assert lib.logp_merge_partials(None, None, None, None, -100, 0, 10, None, None, None) == 0
+
+
+def test_forward_argument_errors(lib):
+    buf = (ctypes.c_char * 64)()
+    p = ctypes.addressof(buf)
+    cases = [
+        dict(n=-1, v=10, ld=10),
+        dict(n=4, v=0, ld=10),
+        dict(n=4, v=10, ld=9),
+        dict(n=2**62, v=2**20, ld=2**20),   # extent overflows int64
+    ]
+    for c in cases:
+        st = lib.fused_logp_forward(p, c["n"], c["v"], c["ld"], p, -100, p, p, None)
+        assert st == EINVAL, c
+        assert lib.flp_last_error()
+    # null pointers
+    assert lib.fused_logp_forward(None, 4, 10, 10, p, -100, p, p, None) == EINVAL
+    assert b"logits" in lib.flp_last_error()
+    # host memory is not accepted as device memory
+    assert lib.fused_logp_forward(p, 4, 10, 10, p, -100, p, p, None) == EINVAL
+
+
+def test_backward_argument_errors(lib):
+    buf = (ctypes.c_char * 64)()
+    p = ctypes.addressof(buf)
+    assert lib.fused_logp_backward(p, 4, 10, 10, p, -100, p, p, p, 9, None) == EINVAL  # ld_out < v
+    assert lib.fused_logp_backward(p, -2, 10, 10, p, -100, p, p, p, 10, None) == EINVAL
+    assert lib.fused_logp_backward(p, 4, 10, 10, p, -100, None, p, p, 10, None) == EINVAL
+
+
+def test_shard_gate(lib):
+    buf = (ctypes.c_char * 64)()
+    p = ctypes.addressof(buf)
+    V, W = 151936, 9496
+    # bounds off the tile grid are refused before any device work
+    assert lib.logp_shard_partials(p, 8, 76032, 100, 75968, V, p, p, p, p, None) == EUNSUP
+    assert lib.logp_shard_partials(p, 8, 76032, 0, 75000, V, p, p, p, p, None) == EUNSUP
+    assert b"tile width" in lib.flp_last_error()
+    # outside the vocabulary / bad widths
+    assert lib.logp_shard_partials(p, 8, 76032, 2 * W, V, V, p, p, p, p, None) == EINVAL
+    assert lib.logp_shard_partials(p, 8, 10, 0, 9496, V, p, p, p, p, None) == EINVAL
+    assert lib.logp_shard_partials(p, 8, 10, 0, 0, V, p, p, p, p, None) == EINVAL
+    # a last shard may be ragged: passes the gate, then fails on host memory
+    assert lib.logp_shard_partials(p, 8, 76032, 15 * W, V - 15 * W, V, p, p, p, p, None) == EINVAL
+    assert b"device memory" in lib.flp_last_error() or b"cudaPointer" in lib.flp_last_error()
+
+
+def test_python_binding_checks_before_calling():
+    x = torch.zeros((4, 10), dtype=torch.float32)
+    y = torch.zeros(4, dtype=torch.int64)
+    with pytest.raises(TypeError):
+        flp.fused_logp_forward(x, y)
+    xb = x.to(torch.bfloat16)
+    with pytest.raises(TypeError):
+        flp.fused_logp_forward(xb, y.to(torch.int32))
+    with pytest.raises(ValueError):
+        flp.fused_logp_forward(xb, torch.zeros(3, dtype=torch.int64))
+    with pytest.raises(ValueError):
+        flp.fused_logp_forward(xb.t(), torch.zeros(10, dtype=torch.int64))
+    with pytest.raises(ValueError):
+        flp.fused_logp_forward(xb, y)  # CPU tensors are refused, no CPU fallback
+    lse = torch.zeros(4)
+    with pytest.raises(TypeError):
+        flp.fused_logp_backward(xb, y, lse, torch.zeros(4, dtype=torch.float64))
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(_lib, "_lib", None)
+    monkeypatch.setattr(flp_build, "LIB", str(tmp_path / "nope.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        _lib.load()
+
+
+def test_package_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "selected_token_logprob_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                src = open(os.path.join(dirpath, fn)).read()
+                assert "oracle" not in src.lower(), fn

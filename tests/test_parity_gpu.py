@@ -1,0 +1,223 @@
+"""GPU parity: the CUDA path (through the C ABI) against the FP64 oracle, on
+the same seeded inputs.  Sizes span several tiles and ragged tails; the
+long-CoT workload runs at full size in the benchmark's launch configuration
+and is checked on sampled rows."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import selected_token_logprob_gb300 as flp
+import workloads
+from golden import closed_forms, to_bf16_bits_exact
+from parity_util import bits, check_backward, check_forward, run
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+IGN = -100
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    flp._lib.load(build_if_missing=True)
+
+
+def _to_dev(*ts):
+    return [t.to(DEV) for t in ts]
+
+
+def test_tiny_full():
+    x, y, g = workloads.make("tiny")
+    xd, yd, gd = _to_dev(x, y, g)
+    logp, lse, dl = run(xd, yd, gd)
+    xb = bits(x)
+    check_forward(xb, y.numpy(), logp, lse)
+    check_backward(xb, y.numpy(), g.numpy(), dl)
+
+
+def test_mid_full():
+    x, y, g = workloads.make("mid", device=DEV)
+    logp, lse, dl = run(x, y, g)
+    xb, yn, gn = bits(x), y.cpu().numpy(), g.cpu().numpy()
+    f = check_forward(xb, yn, logp, lse)
+    b = check_backward(xb, yn, gn, dl)
+    print("mid:", f, b)
+
+
+def test_long_full_size_sampled_rows():
+    """Full 32768 x 151936 launch (the benchmark's configuration); every 16th
+    row and every ignore row are checked against the oracle."""
+    x, y, g = workloads.make("long", device=DEV)
+    logp, lse, dl = run(x, y, g)
+    torch.cuda.synchronize()
+    yn = y.cpu().numpy()
+    rows = np.union1d(np.arange(0, x.shape[0], 16), np.nonzero(yn == IGN)[0])
+    idx = torch.from_numpy(rows).to(DEV)
+    xb = bits(x.index_select(0, idx))
+    f = check_forward(xb, yn[rows], logp[idx], lse[idx])
+    b = check_backward(xb, yn[rows], g.cpu().numpy()[rows], dl.index_select(0, idx))
+    print("long (sampled):", f, b)
+    # every inactive row's gradient is exactly zero over the full tensor
+    inactive = torch.from_numpy(np.nonzero(yn == IGN)[0]).to(DEV)
+    assert int(dl.index_select(0, inactive).view(torch.int16).abs().sum()) == 0
+
+
+@pytest.mark.parametrize("v", [1, 7, 8, 9, 127, 128, 129, 255, 1031, 4097, 9497])
+@pytest.mark.parametrize("n", [1, 3, 33])
+def test_ragged_shapes(n, v):
+    wl = workloads.Workload("edge", n, v, 2.0, 8.0, 0.1, "normal", seed=v + n)
+    x, y, g = workloads.make(wl)
+    xd, yd, gd = _to_dev(x, y, g)
+    logp, lse, dl = run(xd, yd, gd)
+    xb = bits(x)
+    check_forward(xb, y.numpy(), logp, lse)
+    check_backward(xb, y.numpy(), g.numpy(), dl, min_cr=0.999 if n * v < 10000 else 0.9999)
+
+
+@pytest.mark.parametrize("v,ld,offset", [(1031, 1031, 0), (1031, 1040, 0), (1031, 1040, 1),
+                                         (4096, 4100, 3), (151936, 151937, 1)])
+def test_strided_and_misaligned_match_aligned_bitwise(v, ld, offset):
+    """Rows that are not 16-byte aligned take the scalar path; the results are
+    bitwise equal to the aligned vector path and within tolerance of the oracle."""
+    n = 5
+    wl = workloads.Workload("stride", n, v, 2.0, 8.0, 0.0, "normal", seed=ld)
+    x, y, g = workloads.make(wl, device=DEV)
+    big = torch.zeros(n * ld + offset + 8, dtype=torch.bfloat16, device=DEV)
+    xs = big[offset:offset + n * ld].view(n, ld)[:, :v]
+    xs.copy_(x)
+    a_logp, a_lse, a_dl = run(x, y, g)
+    dl_out = torch.zeros(n * ld + offset + 8, dtype=torch.bfloat16, device=DEV)
+    ds = dl_out[offset:offset + n * ld].view(n, ld)[:, :v]
+    s_logp, s_lse = flp.fused_logp_forward(xs, y)
+    flp.fused_logp_backward(xs, y, s_lse, g, dlogits=ds)
+    assert torch.equal(a_logp.view(torch.int32), s_logp.view(torch.int32))
+    assert torch.equal(a_lse.view(torch.int32), s_lse.view(torch.int32))
+    assert torch.equal(a_dl.view(torch.int16), ds.contiguous().view(torch.int16))
+    # padding columns of the strided output are untouched
+    if ld > v:
+        pad = dl_out[offset:offset + n * ld].view(n, ld)[:, v:]
+        assert int(pad.view(torch.int16).abs().sum()) == 0
+    check_forward(bits(x), y.cpu().numpy(), s_logp, s_lse)
+
+
+def test_inactive_targets_and_ignore_index():
+    v = 300
+    x, _, g = workloads.make(workloads.Workload("inact", 8, v, 2.0, 0.0, 0.0, "normal", seed=3))
+    y = torch.tensor([-100, v, v + 5, -5, 0, v - 1, 17, 17], dtype=torch.int64)
+    xd, yd, gd = _to_dev(x, y, g)
+    logp, lse, dl = run(xd, yd, gd)
+    for t in range(4):
+        assert logp[t].item() == 0.0
+        assert int(dl[t].view(torch.int16).abs().sum()) == 0
+    check_forward(bits(x), y.numpy(), logp, lse)
+    check_backward(bits(x), y.numpy(), g.numpy(), dl, min_cr=0.999)
+    # an ignore index inside [0, V) deactivates exactly the rows that hold it
+    logp2, lse2, dl2 = run(xd, yd, gd, ignore_index=17)
+    assert logp2[6].item() == 0.0 and logp2[7].item() == 0.0
+    assert int(dl2[6:].view(torch.int16).abs().sum()) == 0
+    assert torch.equal(dl2[:6].view(torch.int16), dl[:6].view(torch.int16))
+    assert torch.equal(lse2.view(torch.int32), lse.view(torch.int32))
+
+
+def test_all_rows_inactive():
+    x, _, g = workloads.make(workloads.Workload("allin", 4, 2000, 1.0, 0.0, 0.0, "normal"))
+    y = torch.full((4,), IGN, dtype=torch.int64)
+    logp, lse, dl = run(*_to_dev(x, y, g))
+    assert torch.all(logp == 0) and int(dl.view(torch.int16).abs().sum()) == 0
+    check_forward(bits(x), y.numpy(), logp, lse)
+
+
+def test_masked_tail_gives_zero_finite_gradient():
+    v = 5000
+    x, y, g = workloads.make(workloads.Workload("mask", 6, v, 2.0, 0.0, 0.0, "normal", seed=9))
+    x[:, 3000:] = float("-inf")
+    y = torch.randint(0, 3000, (6,), generator=torch.Generator().manual_seed(1))
+    logp, lse, dl = run(*_to_dev(x, y, g))
+    assert torch.isfinite(dl.float()).all()
+    assert torch.all(dl[:, 3000:].float() == 0)
+    check_forward(bits(x), y.numpy(), logp, lse)
+    check_backward(bits(x), y.numpy(), g.numpy(), dl)
+    # equal to the truncated row
+    t_logp, t_lse = flp.fused_logp_forward(x[:, :3000].contiguous().to(DEV), y.to(DEV))
+    assert torch.allclose(t_logp, logp, rtol=0, atol=1e-6)
+
+
+@pytest.mark.parametrize("case", closed_forms(), ids=lambda c: c["name"])
+def test_closed_forms_on_gpu(case):
+    x = torch.from_numpy(to_bf16_bits_exact(case["logits"]).view(np.int16)).view(torch.bfloat16)
+    x = x[None, :].to(DEV)
+    y = torch.tensor([case["target"]], dtype=torch.int64, device=DEV)
+    g = torch.tensor([case["grad"] or 1.0], dtype=torch.float32, device=DEV)
+    logp, lse, dl = run(x, y, g)
+    assert abs(logp.item() - case["logp"]) <= 1e-6 * max(1.0, abs(case["logp"]))
+    assert abs(lse.item() - case["lse"]) <= 1e-6 * max(1.0, abs(case["lse"]))
+    if case["dlogits"] is not None:
+        np.testing.assert_allclose(dl[0].float().cpu().numpy(), case["dlogits"], rtol=0, atol=1e-6)
+
+
+def test_uniform_full_vocab_row():
+    v = workloads.QWEN3_VOCAB
+    x = torch.full((2, v), 1.5, dtype=torch.bfloat16, device=DEV)
+    y = torch.tensor([0, v - 1], device=DEV)
+    g = torch.tensor([1.0, -3.0], device=DEV)
+    logp, lse, dl = run(x, y, g)
+    assert torch.allclose(logp.double().cpu(), torch.full((2,), -np.log(v), dtype=torch.float64),
+                          atol=1e-5, rtol=0)
+    check_backward(bits(x), y.cpu().numpy(), g.cpu().numpy(), dl)
+
+
+def test_large_offsets_do_not_overflow():
+    v = 2048
+    x, y, g = workloads.make(workloads.Workload("off", 4, v, 2.0, 0.0, 0.0, "normal", seed=5))
+    x = (x.float() + 3000.0).to(torch.bfloat16)  # exp(3000) overflows anything
+    logp, lse, dl = run(*_to_dev(x, y, g))
+    assert torch.isfinite(logp).all() and torch.isfinite(dl.float()).all()
+    check_forward(bits(x), y.numpy(), logp, lse)
+
+
+def test_in_place_backward_matches_out_of_place():
+    x, y, g = workloads.make("tiny", device=DEV)
+    logp, lse, dl = run(x, y, g)
+    xi = x.clone()
+    out = flp.fused_logp_backward(xi, y, lse, g, dlogits=xi)
+    assert out.data_ptr() == xi.data_ptr()
+    assert torch.equal(xi.view(torch.int16), dl.view(torch.int16))
+    with pytest.raises(flp.FusedLogpError, match="overlaps"):
+        flp.fused_logp_backward(x[1:], y[1:], lse[1:], g[1:], dlogits=x[:-1])
+
+
+def test_autograd_function():
+    x, y, g = workloads.make("tiny", device=DEV)
+    xr = x.clone().requires_grad_(True)
+    logp = flp.fused_logp(xr, y)
+    (logp * g).sum().backward()
+    _, lse, dl = run(x, y, g)
+    assert torch.equal(xr.grad.view(torch.int16), dl.view(torch.int16))
+
+
+def test_empty_batch():
+    x = torch.empty((0, 128), dtype=torch.bfloat16, device=DEV)
+    y = torch.empty((0,), dtype=torch.int64, device=DEV)
+    g = torch.empty((0,), dtype=torch.float32, device=DEV)
+    logp, lse, dl = run(x, y, g)
+    assert logp.numel() == 0 and dl.shape == (0, 128)
+
+
+def test_device_guard_restores_current_device():
+    x, y, g = workloads.make("tiny", device=DEV)
+    before = torch.cuda.current_device()
+    run(x, y, g)
+    assert torch.cuda.current_device() == before
+
+
+def test_host_pointer_is_rejected():
+    x, y, g = workloads.make("tiny")
+    with pytest.raises(ValueError):
+        flp.fused_logp_forward(x, y)   # binding refuses CPU tensors
+    lib = flp._lib.load()
+    yd = y.to(DEV)
+    out = torch.empty(64, device=DEV)
+    st = lib.fused_logp_forward(x.data_ptr(), 64, 1024, 1024, yd.data_ptr(), IGN,
+                                out.data_ptr(), out.data_ptr(), None)
+    assert st == flp._lib.FLP_EINVAL and b"device memory" in lib.flp_last_error()
