@@ -170,12 +170,13 @@ def run_ours(args):
     x, y, g = workloads.make(wl, device=dev, seed=wl.seed + rank)
     logp = torch.empty(n, dtype=torch.float32, device=dev)
     lse = torch.empty(n, dtype=torch.float32, device=dev)
+    lse_lo = torch.empty(n, dtype=torch.float32, device=dev)
     dl = torch.empty((n, v), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        flp.fused_logp_forward(x, y, logp=logp, lse=lse)
-        flp.fused_logp_backward(x, y, lse, g, dlogits=dl)
+        flp.fused_logp_forward(x, y, logp=logp, lse=lse, lse_lo=lse_lo)
+        flp.fused_logp_backward(x, y, lse, g, dlogits=dl, lse_lo=lse_lo)
 
     for _ in range(args.warmup):
         step()
@@ -191,9 +192,9 @@ def run_ours(args):
         t0.record(stream)
         for k in range(args.steps):
             ev[k][0].record(stream)
-            flp.fused_logp_forward(x, y, logp=logp, lse=lse)
+            flp.fused_logp_forward(x, y, logp=logp, lse=lse, lse_lo=lse_lo)
             ev[k][1].record(stream)
-            flp.fused_logp_backward(x, y, lse, g, dlogits=dl)
+            flp.fused_logp_backward(x, y, lse, g, dlogits=dl, lse_lo=lse_lo)
             ev[k][2].record(stream)
         t1.record(stream)
         torch.cuda.synchronize(dev)
@@ -262,14 +263,15 @@ def run_e2e(args, flp, x, y, g, dev, stream, world):
     dg = torch.empty_like(g)
     logp = torch.empty(n, dtype=torch.float32, device=dev)
     lse = torch.empty(n, dtype=torch.float32, device=dev)
+    lse_lo = torch.empty(n, dtype=torch.float32, device=dev)
     dl = torch.empty_like(x)
 
     def step():
         dx.copy_(hx, non_blocking=True)
         dy.copy_(hy, non_blocking=True)
         dg.copy_(hg, non_blocking=True)
-        flp.fused_logp_forward(dx, dy, logp=logp, lse=lse)
-        flp.fused_logp_backward(dx, dy, lse, dg, dlogits=dl)
+        flp.fused_logp_forward(dx, dy, logp=logp, lse=lse, lse_lo=lse_lo)
+        flp.fused_logp_backward(dx, dy, lse, dg, dlogits=dl, lse_lo=lse_lo)
         hlogp.copy_(logp, non_blocking=True)
         hlse.copy_(lse, non_blocking=True)
 

@@ -85,13 +85,18 @@ int64_t flp_tile_width(int64_t v);
  *   targets  [n] int64
  *   logp     [n] FP32 out
  *   lse      [n] FP32 out (keep it for the backward)
- * Any alignment and any ld are accepted; 16-byte aligned rows take the
- * vector path, others a scalar path with the same arithmetic (same bits).
+ *   lse_lo   [n] FP32 out, or NULL: the FP32 rounding residual of the LSE
+ *            (LSE - lse, |lse_lo| <= half an ulp of lse).  Passing it to the
+ *            backward removes the FP32 quantisation of the LSE from the
+ *            gradient (an addition of this library; the pages store FP32 only).
+ * Any alignment and any ld are accepted.  16-byte aligned rows with ld % 8 == 0
+ * stream through per-warp bulk-copy (TMA) rings in shared memory; other
+ * layouts take a scalar-load path with the same arithmetic (same bits).
  * Errors: FLP_EINVAL for n < 0, v < 1, ld < v, a null or host pointer.
  */
 flp_status fused_logp_forward(const void* logits, int64_t n, int64_t v, int64_t ld,
                               const int64_t* targets, int64_t ignore_index,
-                              float* logp, float* lse, flp_stream_t stream);
+                              float* logp, float* lse, float* lse_lo, flp_stream_t stream);
 
 /*
  * Backward.  dlogits[t, c] for c in [0, v):
@@ -101,14 +106,16 @@ flp_status fused_logp_forward(const void* logits, int64_t n, int64_t v, int64_t 
  *   inactive row: +0.
  *   logits   [n, ld] BF16
  *   targets  [n] int64, lse [n] FP32 (from fused_logp_forward), grad [n] FP32
+ *   lse_lo   [n] FP32 from fused_logp_forward, or NULL (then taken as 0)
  *   dlogits  [n, ld_out] BF16 out, ld_out >= v; columns >= v are untouched.
+ * Gradient values below 2^-126 in magnitude flush to zero.
  * dlogits may alias logits exactly (same pointer and ld == ld_out: the
  * gradient then overwrites the logits in place); any other overlap is
  * FLP_EINVAL.  Elementwise, so batch-invariant by construction.
  */
 flp_status fused_logp_backward(const void* logits, int64_t n, int64_t v, int64_t ld,
                                const int64_t* targets, int64_t ignore_index,
-                               const float* lse, const float* grad,
+                               const float* lse, const float* lse_lo, const float* grad,
                                void* dlogits, int64_t ld_out, flp_stream_t stream);
 
 /*
@@ -138,12 +145,30 @@ flp_status logp_shard_partials(const void* shard_logits, int64_t n, int64_t ld_s
  * as the forward, then writes lse[t] and logp[t] = sel[t] - lse (active rows)
  * or 0.  Together with logp_shard_partials over shards that cover
  * [0, v_total), the results are bitwise equal to fused_logp_forward.
- * sel is read only for active rows.
+ * sel is read only for active rows.  lse_lo (nullable) as in the forward.
  */
 flp_status logp_merge_partials(const float* part_max, const float* part_sum,
                                const float* sel, const int64_t* targets,
                                int64_t ignore_index, int64_t n, int64_t v_total,
-                               float* logp, float* lse, flp_stream_t stream);
+                               float* logp, float* lse, float* lse_lo, flp_stream_t stream);
+
+/*
+ * Health of the device side (no counterpart in the pages: a guard of this
+ * library's own waits).  The bulk-copy forward waits on its own copies with a
+ * bounded wait (about 2 s); if one runs out, the kernel records it in a
+ * sticky device word, stops issuing copies, drains the ones in flight and
+ * returns, so the context stays usable.  flp_device_error synchronises with
+ * `device`, returns that word in *code (0 = no wait ran out) and clears it.
+ */
+flp_status flp_device_error(int device, int* code);
+
+/*
+ * Self-test of the bounded wait: launches one thread on `device` that waits on
+ * a barrier nothing arrives on, with a limit of limit_cycles SM cycles
+ * (at most 1e8), synchronises, and sets *timed_out = 1 if the wait gave up
+ * (it must).  Also sets the sticky word read by flp_device_error.
+ */
+flp_status flp_selftest_wait_timeout(int device, int64_t limit_cycles, int* timed_out);
 
 #ifdef __cplusplus
 }

@@ -8,12 +8,17 @@ PyTorch fallback: without the built library every call raises.
 
 Entry points (same names as the C ABI):
     fused_logp_forward(logits, targets, ignore_index) -> (logp, lse)
-    fused_logp_backward(logits, targets, lse, grad, ignore_index) -> dlogits
+        (with_lse_lo=True also returns lse_lo, the FP32 rounding residual of
+        the LSE, which the backward accepts to avoid the FP32 quantisation)
+    fused_logp_backward(logits, targets, lse, grad, ignore_index, lse_lo=None)
+        -> dlogits
     logp_shard_partials(shard_logits, vocab_start, real_width, v_total, targets,
                         part_max, part_sum, sel)
     logp_merge_partials(part_max, part_sum, sel, targets, v_total,
                         ignore_index) -> (logp, lse)
-and ``FusedLogp``, an autograd function that saves only the O(N) LSE.
+``FusedLogp``, an autograd function that saves only the O(N) LSE (and its
+residual), and ``flp_device_error`` / ``flp_selftest_wait_timeout`` for the
+device-side health word.
 
 Logits are BF16 [N, V] (row stride may exceed V: pass a column slice of a
 wider buffer), targets int64 [N], the upstream gradient FP32 [N]; logp and
@@ -35,6 +40,8 @@ __all__ = [
     "FusedLogpError",
     "IGNORE_INDEX",
     "NUM_TILES",
+    "flp_device_error",
+    "flp_selftest_wait_timeout",
     "flp_tile_width",
     "fused_logp",
     "fused_logp_backward",
@@ -81,10 +88,16 @@ def flp_tile_width(v: int) -> int:
     return int(_lib.load().flp_tile_width(int(v)))
 
 
+def _opt_ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
 def fused_logp_forward(logits: torch.Tensor, targets: torch.Tensor,
                        ignore_index: int = IGNORE_INDEX,
-                       logp: torch.Tensor | None = None, lse: torch.Tensor | None = None):
-    """(logp, lse), FP32 [N] each, of BF16 logits [N, V]."""
+                       logp: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                       lse_lo: torch.Tensor | None = None, with_lse_lo: bool = False):
+    """(logp, lse), FP32 [N] each, of BF16 logits [N, V]; (logp, lse, lse_lo)
+    when ``with_lse_lo`` is true or an ``lse_lo`` buffer is given."""
     n, v, ld = _rows(logits, "logits")
     if logits.dtype != torch.bfloat16:
         raise TypeError(f"logits must be torch.bfloat16, got {logits.dtype}")
@@ -92,30 +105,40 @@ def fused_logp_forward(logits: torch.Tensor, targets: torch.Tensor,
     dev = logits.device
     logp = torch.empty(n, dtype=torch.float32, device=dev) if logp is None else logp
     lse = torch.empty(n, dtype=torch.float32, device=dev) if lse is None else lse
+    want_lo = with_lse_lo or lse_lo is not None
+    if want_lo and lse_lo is None:
+        lse_lo = torch.empty(n, dtype=torch.float32, device=dev)
     _vec(logp, "logp", n, torch.float32)
     _vec(lse, "lse", n, torch.float32)
     _cuda(logits, targets, logp, lse)
-    if n == 0:
-        return logp, lse
-    st = _lib.load().fused_logp_forward(logits.data_ptr(), n, v, ld, targets.data_ptr(),
-                                        int(ignore_index), logp.data_ptr(), lse.data_ptr(),
-                                        _stream(logits))
-    _lib.check("fused_logp_forward", st)
-    return logp, lse
+    if want_lo:
+        _vec(lse_lo, "lse_lo", n, torch.float32)
+        _cuda(lse_lo)
+    if n > 0:
+        st = _lib.load().fused_logp_forward(logits.data_ptr(), n, v, ld, targets.data_ptr(),
+                                            int(ignore_index), logp.data_ptr(), lse.data_ptr(),
+                                            _opt_ptr(lse_lo), _stream(logits))
+        _lib.check("fused_logp_forward", st)
+    return (logp, lse, lse_lo) if want_lo else (logp, lse)
 
 
 def fused_logp_backward(logits: torch.Tensor, targets: torch.Tensor, lse: torch.Tensor,
                         grad: torch.Tensor, ignore_index: int = IGNORE_INDEX,
-                        dlogits: torch.Tensor | None = None) -> torch.Tensor:
+                        dlogits: torch.Tensor | None = None,
+                        lse_lo: torch.Tensor | None = None) -> torch.Tensor:
     """dlogits BF16 [N, V] = grad * (onehot(targets) - softmax(logits)).
 
-    ``dlogits`` may be ``logits`` itself (in-place gradient)."""
+    ``dlogits`` may be ``logits`` itself (in-place gradient).  ``lse_lo`` is
+    the residual returned by the forward with ``with_lse_lo=True``."""
     n, v, ld = _rows(logits, "logits")
     if logits.dtype != torch.bfloat16:
         raise TypeError(f"logits must be torch.bfloat16, got {logits.dtype}")
     _vec(targets, "targets", n, torch.int64)
     _vec(lse, "lse", n, torch.float32)
     _vec(grad, "grad", n, torch.float32)
+    if lse_lo is not None:
+        _vec(lse_lo, "lse_lo", n, torch.float32)
+        _cuda(lse_lo)
     if dlogits is None:
         dlogits = torch.empty((n, v), dtype=torch.bfloat16, device=logits.device)
     if dlogits.dtype != torch.bfloat16 or tuple(dlogits.shape) != (n, v):
@@ -125,8 +148,9 @@ def fused_logp_backward(logits: torch.Tensor, targets: torch.Tensor, lse: torch.
     if n == 0:
         return dlogits
     st = _lib.load().fused_logp_backward(logits.data_ptr(), n, v, ld, targets.data_ptr(),
-                                         int(ignore_index), lse.data_ptr(), grad.data_ptr(),
-                                         dlogits.data_ptr(), ld_out, _stream(logits))
+                                         int(ignore_index), lse.data_ptr(), _opt_ptr(lse_lo),
+                                         grad.data_ptr(), dlogits.data_ptr(), ld_out,
+                                         _stream(logits))
     _lib.check("fused_logp_backward", st)
     return dlogits
 
@@ -163,8 +187,10 @@ def logp_shard_partials(shard_logits: torch.Tensor, vocab_start: int, real_width
 def logp_merge_partials(part_max: torch.Tensor, part_sum: torch.Tensor, sel: torch.Tensor,
                         targets: torch.Tensor, v_total: int,
                         ignore_index: int = IGNORE_INDEX,
-                        logp: torch.Tensor | None = None, lse: torch.Tensor | None = None):
-    """(logp, lse) from the tile partials of shards covering [0, v_total)."""
+                        logp: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                        lse_lo: torch.Tensor | None = None, with_lse_lo: bool = False):
+    """(logp, lse) [or (logp, lse, lse_lo)] from the tile partials of shards
+    covering [0, v_total)."""
     n = targets.shape[0] if targets.dim() == 1 else -1
     _vec(targets, "targets", n, torch.int64)
     for name, t in (("part_max", part_max), ("part_sum", part_sum)):
@@ -174,17 +200,23 @@ def logp_merge_partials(part_max: torch.Tensor, part_sum: torch.Tensor, sel: tor
     dev = targets.device
     logp = torch.empty(n, dtype=torch.float32, device=dev) if logp is None else logp
     lse = torch.empty(n, dtype=torch.float32, device=dev) if lse is None else lse
+    want_lo = with_lse_lo or lse_lo is not None
+    if want_lo and lse_lo is None:
+        lse_lo = torch.empty(n, dtype=torch.float32, device=dev)
     _vec(logp, "logp", n, torch.float32)
     _vec(lse, "lse", n, torch.float32)
     _cuda(part_max, part_sum, sel, targets, logp, lse)
-    if n == 0:
-        return logp, lse
-    st = _lib.load().logp_merge_partials(part_max.data_ptr(), part_sum.data_ptr(),
-                                         sel.data_ptr(), targets.data_ptr(), int(ignore_index),
-                                         n, int(v_total), logp.data_ptr(), lse.data_ptr(),
-                                         _stream(targets))
-    _lib.check("logp_merge_partials", st)
-    return logp, lse
+    if want_lo:
+        _vec(lse_lo, "lse_lo", n, torch.float32)
+        _cuda(lse_lo)
+    if n > 0:
+        st = _lib.load().logp_merge_partials(part_max.data_ptr(), part_sum.data_ptr(),
+                                             sel.data_ptr(), targets.data_ptr(),
+                                             int(ignore_index), n, int(v_total),
+                                             logp.data_ptr(), lse.data_ptr(), _opt_ptr(lse_lo),
+                                             _stream(targets))
+        _lib.check("logp_merge_partials", st)
+    return (logp, lse, lse_lo) if want_lo else (logp, lse)
 
 
 class FusedLogp(torch.autograd.Function):
@@ -193,16 +225,16 @@ class FusedLogp(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, logits, targets, ignore_index=IGNORE_INDEX):
-        logp, lse = fused_logp_forward(logits, targets, ignore_index)
-        ctx.save_for_backward(logits, targets, lse)
+        logp, lse, lse_lo = fused_logp_forward(logits, targets, ignore_index, with_lse_lo=True)
+        ctx.save_for_backward(logits, targets, lse, lse_lo)
         ctx.ignore_index = ignore_index
         return logp
 
     @staticmethod
     def backward(ctx, grad_logp):
-        logits, targets, lse = ctx.saved_tensors
+        logits, targets, lse, lse_lo = ctx.saved_tensors
         g = grad_logp.to(torch.float32).contiguous()
-        d = fused_logp_backward(logits, targets, lse, g, ctx.ignore_index)
+        d = fused_logp_backward(logits, targets, lse, g, ctx.ignore_index, lse_lo=lse_lo)
         return d, None, None
 
 
@@ -210,3 +242,25 @@ def fused_logp(logits: torch.Tensor, targets: torch.Tensor,
                ignore_index: int = IGNORE_INDEX) -> torch.Tensor:
     """Autograd-aware selected-token logp (FP32 [N])."""
     return FusedLogp.apply(logits, targets, ignore_index)
+
+
+def flp_device_error(device: int | torch.device = 0) -> int:
+    """Read and clear the library's sticky device error word (0 = healthy;
+    1 = a bounded wait of a kernel ran out).  Synchronises with the device."""
+    import ctypes
+
+    dev = torch.device(device).index if not isinstance(device, int) else device
+    code = ctypes.c_int(-1)
+    _lib.check("flp_device_error", _lib.load().flp_device_error(int(dev or 0), ctypes.byref(code)))
+    return code.value
+
+
+def flp_selftest_wait_timeout(device: int = 0, limit_cycles: int = 200000) -> int:
+    """Run the bounded-wait self-test (a wait nothing completes); returns 1 if
+    the wait gave up as it must."""
+    import ctypes
+
+    out = ctypes.c_int(-1)
+    _lib.check("flp_selftest_wait_timeout",
+               _lib.load().flp_selftest_wait_timeout(int(device), int(limit_cycles), ctypes.byref(out)))
+    return out.value

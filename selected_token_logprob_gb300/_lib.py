@@ -26,10 +26,12 @@ SIGNATURES = {
     "flp_last_error": (ctypes.c_char_p, []),
     "flp_version": (ctypes.c_char_p, []),
     "flp_tile_width": (_I64, [_I64]),
-    "fused_logp_forward": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P]),
-    "fused_logp_backward": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P, _I64, _P]),
+    "fused_logp_forward": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P, _P]),
+    "fused_logp_backward": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P, _P, _I64, _P]),
     "logp_shard_partials": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
-    "logp_merge_partials": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P]),
+    "logp_merge_partials": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P]),
+    "flp_device_error": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_int)]),
+    "flp_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_int, _I64, ctypes.POINTER(ctypes.c_int)]),
 }
 
 

@@ -105,6 +105,25 @@ flp_status check_launch(const char* what) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 constexpr int64_t kMaxGrid = 2147483647;
+constexpr int kMaxDevices = 64;
+
+// Once per device: allow the bulk-copy forward its dynamic shared memory, and
+// cache the SM count used to size its persistent grid.
+flp_status bulk_forward_setup(int dev, int* sms) {
+    static int sm_count[kMaxDevices];
+    static bool ready[kMaxDevices];
+    if (dev < 0 || dev >= kMaxDevices) return fail(FLP_ECUDA, "device index %d out of range", dev);
+    if (!ready[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(flp::k_logp_fwd_bulk,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             flp::kFwdSmemBytes);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return fail(FLP_ECUDA, "forward setup: %s", cudaGetErrorString(e));
+        ready[dev] = true;
+    }
+    *sms = sm_count[dev];
+    return FLP_OK;
+}
 
 int grid_for(int64_t items) { return (int)(items < kMaxGrid ? items : kMaxGrid); }
 
@@ -120,17 +139,17 @@ int64_t flp_tile_width(int64_t v) { return tile_width(v); }
 
 flp_status fused_logp_forward(const void* logits, int64_t n, int64_t v, int64_t ld,
                               const int64_t* targets, int64_t ignore_index, float* logp,
-                              float* lse, flp_stream_t stream) {
+                              float* lse, float* lse_lo, flp_stream_t stream) {
     if (n < 0) return fail(FLP_EINVAL, "n must be >= 0 (got %lld)", (long long)n);
     if (v < 1) return fail(FLP_EINVAL, "v must be >= 1 (got %lld)", (long long)v);
     if (ld < v) return fail(FLP_EINVAL, "ld (%lld) must be >= v (%lld)", (long long)ld, (long long)v);
     if (n == 0) return ok();
     int64_t bytes;
     if (!span_bytes(n, v, ld, 2, &bytes)) return fail(FLP_EINVAL, "logits extent overflows int64");
-    const void* ptrs[] = {logits, targets, logp, lse};
-    const char* names[] = {"logits", "targets", "logp", "lse"};
+    const void* ptrs[] = {logits, targets, logp, lse, lse_lo ? lse_lo : lse};
+    const char* names[] = {"logits", "targets", "logp", "lse", "lse_lo"};
     int dev;
-    flp_status st = common_device(4, ptrs, names, &dev);
+    flp_status st = common_device(5, ptrs, names, &dev);
     if (st != FLP_OK) return st;
     DeviceGuard guard;
     if ((st = guard.enter(dev)) != FLP_OK) return st;
@@ -138,20 +157,23 @@ flp_status fused_logp_forward(const void* logits, int64_t n, int64_t v, int64_t 
     const int64_t W = tile_width(v);
     const uint16_t* x = static_cast<const uint16_t*>(logits);
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int grid = grid_for(n);
-    if (aligned16(x) && ld % 8 == 0)
-        flp::k_logp_fwd<true><<<grid, flp::kFwdThreads, 0, s>>>(x, n, v, ld, W, targets,
-                                                               ignore_index, logp, lse);
-    else
-        flp::k_logp_fwd<false><<<grid, flp::kFwdThreads, 0, s>>>(x, n, v, ld, W, targets,
-                                                                ignore_index, logp, lse);
+    if (aligned16(x) && ld % 8 == 0) {
+        int sms;
+        if ((st = bulk_forward_setup(dev, &sms)) != FLP_OK) return st;
+        const int grid = grid_for(n < 2 * (int64_t)sms ? n : 2 * (int64_t)sms);
+        flp::k_logp_fwd_bulk<<<grid, flp::kFwdThreads, flp::kFwdSmemBytes, s>>>(
+            x, n, v, ld, W, targets, ignore_index, logp, lse, lse_lo);
+    } else {
+        flp::k_logp_fwd<false><<<grid_for(n), flp::kFwdThreads, 0, s>>>(
+            x, n, v, ld, W, targets, ignore_index, logp, lse, lse_lo);
+    }
     return check_launch("forward");
 }
 
 flp_status fused_logp_backward(const void* logits, int64_t n, int64_t v, int64_t ld,
                                const int64_t* targets, int64_t ignore_index, const float* lse,
-                               const float* grad, void* dlogits, int64_t ld_out,
-                               flp_stream_t stream) {
+                               const float* lse_lo, const float* grad, void* dlogits,
+                               int64_t ld_out, flp_stream_t stream) {
     if (n < 0) return fail(FLP_EINVAL, "n must be >= 0 (got %lld)", (long long)n);
     if (v < 1) return fail(FLP_EINVAL, "v must be >= 1 (got %lld)", (long long)v);
     if (ld < v) return fail(FLP_EINVAL, "ld (%lld) must be >= v (%lld)", (long long)ld, (long long)v);
@@ -161,10 +183,10 @@ flp_status fused_logp_backward(const void* logits, int64_t n, int64_t v, int64_t
     int64_t in_bytes, out_bytes;
     if (!span_bytes(n, v, ld, 2, &in_bytes) || !span_bytes(n, v, ld_out, 2, &out_bytes))
         return fail(FLP_EINVAL, "logits/dlogits extent overflows int64");
-    const void* ptrs[] = {logits, targets, lse, grad, dlogits};
-    const char* names[] = {"logits", "targets", "lse", "grad", "dlogits"};
+    const void* ptrs[] = {logits, targets, lse, grad, dlogits, lse_lo ? lse_lo : lse};
+    const char* names[] = {"logits", "targets", "lse", "grad", "dlogits", "lse_lo"};
     int dev;
-    flp_status st = common_device(5, ptrs, names, &dev);
+    flp_status st = common_device(6, ptrs, names, &dev);
     if (st != FLP_OK) return st;
 
     const uintptr_t xb = reinterpret_cast<uintptr_t>(logits);
@@ -187,7 +209,7 @@ flp_status fused_logp_backward(const void* logits, int64_t n, int64_t v, int64_t
     const bool vout = aligned16(dx) && ld_out % 8 == 0;
 #define FLP_BWD(VI, VO, IP)                                                                   \
     flp::k_logp_bwd<VI, VO, IP><<<grid, flp::kBwdThreads, 0, s>>>(x, n, v, ld, targets,      \
-                                                                  ignore_index, lse, grad, dx, \
+                                                                  ignore_index, lse, lse_lo, grad, dx, \
                                                                   ld_out, segs)
     if (in_place) {
         if (vin) FLP_BWD(true, true, true);
@@ -248,14 +270,15 @@ flp_status logp_shard_partials(const void* shard_logits, int64_t n, int64_t ld_s
 
 flp_status logp_merge_partials(const float* part_max, const float* part_sum, const float* sel,
                                const int64_t* targets, int64_t ignore_index, int64_t n,
-                               int64_t v_total, float* logp, float* lse, flp_stream_t stream) {
+                               int64_t v_total, float* logp, float* lse, float* lse_lo,
+                               flp_stream_t stream) {
     if (n < 0) return fail(FLP_EINVAL, "n must be >= 0 (got %lld)", (long long)n);
     if (v_total < 1) return fail(FLP_EINVAL, "v_total must be >= 1");
     if (n == 0) return ok();
-    const void* ptrs[] = {part_max, part_sum, sel, targets, logp, lse};
-    const char* names[] = {"part_max", "part_sum", "sel", "targets", "logp", "lse"};
+    const void* ptrs[] = {part_max, part_sum, sel, targets, logp, lse, lse_lo ? lse_lo : lse};
+    const char* names[] = {"part_max", "part_sum", "sel", "targets", "logp", "lse", "lse_lo"};
     int dev;
-    flp_status st = common_device(6, ptrs, names, &dev);
+    flp_status st = common_device(7, ptrs, names, &dev);
     if (st != FLP_OK) return st;
     DeviceGuard guard;
     if ((st = guard.enter(dev)) != FLP_OK) return st;
@@ -266,8 +289,38 @@ flp_status logp_merge_partials(const float* part_max, const float* part_sum, con
     const int64_t rows_per_block = 256 / 16;
     const int grid = grid_for(ceil_div(n, rows_per_block));
     flp::k_logp_merge<<<grid, 256, 0, s>>>(part_max, part_sum, sel, targets, ignore_index, n,
-                                           v_total, n_tiles, logp, lse);
+                                           v_total, n_tiles, logp, lse, lse_lo);
     return check_launch("merge");
+}
+
+flp_status flp_device_error(int device, int* code) {
+    if (code == nullptr) return fail(FLP_EINVAL, "code is a null pointer");
+    DeviceGuard guard;
+    flp_status st = guard.enter(device);
+    if (st != FLP_OK) return st;
+    int v = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, flp::g_device_error, sizeof v);
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(flp::g_device_error, &zero, sizeof zero);
+    if (e != cudaSuccess) return fail(FLP_ECUDA, "device error word: %s", cudaGetErrorString(e));
+    *code = v;
+    return ok();
+}
+
+flp_status flp_selftest_wait_timeout(int device, int64_t limit_cycles, int* timed_out) {
+    if (timed_out == nullptr) return fail(FLP_EINVAL, "timed_out is a null pointer");
+    if (limit_cycles < 0 || limit_cycles > 100000000)
+        return fail(FLP_EINVAL, "limit_cycles must be in [0, 1e8]");
+    DeviceGuard guard;
+    flp_status st = guard.enter(device);
+    if (st != FLP_OK) return st;
+    flp::k_wait_timeout_selftest<<<1, 1>>>((long long)limit_cycles);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    int v = -1;
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&v, flp::g_selftest_result, sizeof v);
+    if (e != cudaSuccess) return fail(FLP_ECUDA, "self-test: %s", cudaGetErrorString(e));
+    *timed_out = v;
+    return ok();
 }
 
 }  // extern "C"

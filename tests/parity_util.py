@@ -25,9 +25,14 @@ GRAD_REL = 2e-3
 MIN_CORRECTLY_ROUNDED = 0.9999
 
 
-def run(x, y, g, ignore_index=-100):
-    logp, lse = flp.fused_logp_forward(x, y, ignore_index)
-    dl = flp.fused_logp_backward(x, y, lse, g, ignore_index)
+def run(x, y, g, ignore_index=-100, use_lse_lo=True):
+    """Forward + backward through the C ABI; by default the backward gets the
+    LSE's FP32 rounding residual (the path the autograd wrapper takes)."""
+    if use_lse_lo:
+        logp, lse, lse_lo = flp.fused_logp_forward(x, y, ignore_index, with_lse_lo=True)
+    else:
+        (logp, lse), lse_lo = flp.fused_logp_forward(x, y, ignore_index), None
+    dl = flp.fused_logp_backward(x, y, lse, g, ignore_index, lse_lo=lse_lo)
     return logp, lse, dl
 
 

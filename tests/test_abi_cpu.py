@@ -56,10 +56,12 @@ def test_version_and_tile_width(lib):
 
 
 def test_empty_input_is_ok_without_device(lib):
-    assert lib.fused_logp_forward(None, 0, 10, 10, None, -100, None, None, None) == 0
+    assert lib.fused_logp_forward(None, 0, 10, 10, None, -100, None, None, None, None) == 0
     assert lib.flp_last_error() == b""
-    assert lib.fused_logp_backward(None, 0, 10, 10, None, -100, None, None, None, 10, None) == 0
-    assert lib.logp_merge_partials(None, None, None, None, -100, 0, 10, None, None, None) == 0
+    assert lib.fused_logp_backward(None, 0, 10, 10, None, -100, None, None, None, None, 10,
+                                   None) == 0
+    assert lib.logp_merge_partials(None, None, None, None, -100, 0, 10, None, None, None,
+                                   None) == 0
 
 
 def test_forward_argument_errors(lib):
@@ -72,22 +74,22 @@ def test_forward_argument_errors(lib):
         dict(n=2**62, v=2**20, ld=2**20),   # extent overflows int64
     ]
     for c in cases:
-        st = lib.fused_logp_forward(p, c["n"], c["v"], c["ld"], p, -100, p, p, None)
+        st = lib.fused_logp_forward(p, c["n"], c["v"], c["ld"], p, -100, p, p, None, None)
         assert st == EINVAL, c
         assert lib.flp_last_error()
     # null pointers
-    assert lib.fused_logp_forward(None, 4, 10, 10, p, -100, p, p, None) == EINVAL
+    assert lib.fused_logp_forward(None, 4, 10, 10, p, -100, p, p, None, None) == EINVAL
     assert b"logits" in lib.flp_last_error()
     # host memory is not accepted as device memory
-    assert lib.fused_logp_forward(p, 4, 10, 10, p, -100, p, p, None) == EINVAL
+    assert lib.fused_logp_forward(p, 4, 10, 10, p, -100, p, p, None, None) == EINVAL
 
 
 def test_backward_argument_errors(lib):
     buf = (ctypes.c_char * 64)()
     p = ctypes.addressof(buf)
-    assert lib.fused_logp_backward(p, 4, 10, 10, p, -100, p, p, p, 9, None) == EINVAL  # ld_out < v
-    assert lib.fused_logp_backward(p, -2, 10, 10, p, -100, p, p, p, 10, None) == EINVAL
-    assert lib.fused_logp_backward(p, 4, 10, 10, p, -100, None, p, p, 10, None) == EINVAL
+    assert lib.fused_logp_backward(p, 4, 10, 10, p, -100, p, None, p, p, 9, None) == EINVAL  # ld_out < v
+    assert lib.fused_logp_backward(p, -2, 10, 10, p, -100, p, None, p, p, 10, None) == EINVAL
+    assert lib.fused_logp_backward(p, 4, 10, 10, p, -100, None, None, p, p, 10, None) == EINVAL
 
 
 def test_shard_gate(lib):
@@ -105,6 +107,15 @@ def test_shard_gate(lib):
     # a last shard may be ragged: passes the gate, then fails on host memory
     assert lib.logp_shard_partials(p, 8, 76032, 15 * W, V - 15 * W, V, p, p, p, p, None) == EINVAL
     assert b"device memory" in lib.flp_last_error() or b"cudaPointer" in lib.flp_last_error()
+
+
+def test_device_entry_points_reject_null_outputs(lib):
+    assert lib.flp_device_error(0, None) == EINVAL
+    assert lib.flp_selftest_wait_timeout(0, 1000, None) == EINVAL
+    import ctypes as C
+    out = C.c_int(0)
+    assert lib.flp_selftest_wait_timeout(0, -1, C.byref(out)) == EINVAL
+    assert lib.flp_selftest_wait_timeout(0, 10**9, C.byref(out)) == EINVAL
 
 
 def test_python_binding_checks_before_calling():

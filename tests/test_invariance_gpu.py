@@ -66,8 +66,9 @@ def test_batch_invariance_sweep_2232():
                 save_x, save_y, save_g = F[pos].clone(), fy[pos].clone(), fg[pos].clone()
                 for k in range(8):
                     F[pos].copy_(px[k]); fy[pos] = py[k]; fg[pos] = pg[k]
-                    lp, ls = flp.fused_logp_forward(F[:B], fy[:B])
-                    flp.fused_logp_backward(F[:B], fy[:B], ls, fg[:B], dlogits=dl_buf[:B])
+                    lp, ls, lo = flp.fused_logp_forward(F[:B], fy[:B], with_lse_lo=True)
+                    flp.fused_logp_backward(F[:B], fy[:B], ls, fg[:B], dlogits=dl_buf[:B],
+                                            lse_lo=lo)
                     r_lp, r_ls, r_d = refs[k]
                     same = (torch.equal(_i(lp[pos:pos + 1]), _i(r_lp))
                             and torch.equal(_i(ls[pos:pos + 1]), _i(r_ls))
@@ -103,17 +104,19 @@ def _sharded_forward(shards, y, v_total, order=None):
     for l in (order or range(len(shards))):
         buf, a, w = shards[l]
         flp.logp_shard_partials(buf, a, w, v_total, y, pm, ps, sel)
-    logp, lse = flp.logp_merge_partials(pm, ps, sel, y, v_total)
+    logp, lse, lse_lo = flp.logp_merge_partials(pm, ps, sel, y, v_total, with_lse_lo=True)
+    _sharded_forward.lse_lo = lse_lo
     return logp, lse, pm, ps
 
 
 @pytest.mark.parametrize("S", [1, 2, 4, 8, 16])
 def test_sharded_equals_unsharded_bitwise(S):
     x, y, _ = workloads.make("sharded", device=DEV)
-    logp, lse = flp.fused_logp_forward(x, y)
+    logp, lse, lse_lo = flp.fused_logp_forward(x, y, with_lse_lo=True)
     s_logp, s_lse, pm, ps = _sharded_forward(_shards(x, S), y, V)
     assert torch.equal(_i(s_lse), _i(lse))
     assert torch.equal(_i(s_logp), _i(logp))
+    assert torch.equal(_i(_sharded_forward.lse_lo), _i(lse_lo))
     # the shard launch order does not matter either
     if S > 1:
         r_logp, r_lse, _, _ = _sharded_forward(_shards(x, S), y, V, order=list(range(S))[::-1])
