@@ -90,8 +90,9 @@ int64_t flp_tile_width(int64_t v);
  *            backward removes the FP32 quantisation of the LSE from the
  *            gradient (an addition of this library; the pages store FP32 only).
  * Any alignment and any ld are accepted.  16-byte aligned rows with ld % 8 == 0
- * stream through per-warp bulk-copy (TMA) rings in shared memory; other
- * layouts take a scalar-load path with the same arithmetic (same bits).
+ * (and v < 2^31) stream through per-warp bulk-copy (TMA) rings in shared
+ * memory; other layouts take a scalar-load path with the same arithmetic
+ * (same bits).
  * Errors: FLP_EINVAL for n < 0, v < 1, ld < v, a null or host pointer.
  */
 flp_status fused_logp_forward(const void* logits, int64_t n, int64_t v, int64_t ld,

@@ -157,7 +157,7 @@ flp_status fused_logp_forward(const void* logits, int64_t n, int64_t v, int64_t 
     const int64_t W = tile_width(v);
     const uint16_t* x = static_cast<const uint16_t*>(logits);
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (aligned16(x) && ld % 8 == 0) {
+    if (aligned16(x) && ld % 8 == 0 && v < ((int64_t)1 << 31)) {
         int sms;
         if ((st = bulk_forward_setup(dev, &sms)) != FLP_OK) return st;
         const int grid = grid_for(n < 2 * (int64_t)sms ? n : 2 * (int64_t)sms);

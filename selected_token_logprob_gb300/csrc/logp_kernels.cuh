@@ -98,6 +98,16 @@ __device__ __forceinline__ uint32_t bf2_max(uint32_t a, uint32_t b) {
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 __device__ __forceinline__ u64 bf2_widen(uint32_t w) { return f2(bf_lo(w), bf_hi(w)); }
+// (x_lo - b, x_hi - b) for the two BF16 values of w: each widened exactly and
+// rounded once (mixed-precision subtract, a BF16 operand and a binary32 one).
+__device__ __forceinline__ u64 bf2_sub(uint32_t w, float b) {
+    float lo, hi;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "sub.rn.f32.bf16 %0, l, %3;\n\tsub.rn.f32.bf16 %1, h, %3;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(w), "f"(b));
+    return f2(lo, hi);
+}
 __device__ __forceinline__ uint32_t ldg_u16(const uint16_t* p) {
     return (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(p));
 }
@@ -172,35 +182,38 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         "l"(src), "r"(bytes), "r"(bar)
         : "memory");
 }
+// One probe of phase `parity` of an mbarrier.
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
 // Wait for phase `parity` of an mbarrier, giving up after `limit` cycles.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long limit) {
-    long long t0 = 0;
-    for (uint32_t it = 0;; ++it) {
-        uint32_t done;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(done)
-            : "r"(bar), "r"(parity)
-            : "memory");
-        if (done) return true;
-        if ((it & 31u) == 0) {
-            const long long now = clock64();
-            if (it == 0) t0 = now;
-            else if (now - t0 > limit) return false;
-        }
+    if (mbar_try(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try(bar, parity)) return true;
+        if ((it & 31u) == 0 && clock64() - t0 > limit) return false;
     }
 }
 
 // ---------------------------------------------------------------- forward reduction
 
 // One online step of a lane over kGroup vectors of 8 BF16 (q[u] = the four
-// 32-bit words of vector u, vectors [0, nvalid) hold data, others are -inf):
-// gm = max(m, elements) by packed BF16 maxima; each element's term
-// 2^((x - gm) log2 e) on the special-function unit (x - gm is exact: both are
-// BF16 values); the terms summed by a fixed pairwise tree (word pairs, then
-// vectors: ((w0 + w1) + (w2 + w3)) lane-wise, vectors ((v0 + v1) + (v2 + v3)),
-// then the even and odd lanes); s = s * exp(m - gm) + group sum.
+// 32-bit words of vector u; with kFull all vectors hold data, otherwise
+// vectors [0, nvalid) do and the others are -inf): gm = max(m, elements) by
+// packed BF16 maxima; each element's term 2^((x - gm) log2 e) on the
+// special-function unit (x - gm is exact: both are BF16 values); the terms
+// summed by a fixed pairwise tree (word pairs, then vectors:
+// ((w0 + w1) + (w2 + w3)) lane-wise, vectors ((v0 + v1) + (v2 + v3)), then the
+// even and odd lanes); s = s * exp(m - gm) + group sum.
+template <bool kFull>
 __device__ __forceinline__ void group_update(const uint32_t (&q)[kGroup][4], int nvalid, float& m,
                                              float& s) {
     uint32_t w = bf2_max(bf2_max(q[0][0], q[0][1]), bf2_max(q[0][2], q[0][3]));
@@ -209,17 +222,16 @@ __device__ __forceinline__ void group_update(const uint32_t (&q)[kGroup][4], int
         w = bf2_max(w, bf2_max(bf2_max(q[u][0], q[u][1]), bf2_max(q[u][2], q[u][3])));
     const float gm = fmaxf(m, fmaxf(bf_lo(w), bf_hi(w)));
     if (gm == -INFINITY) return;  // nothing finite seen yet: (m, s) stays (-inf, 0)
-    const u64 neg_gm = f2(-gm, -gm);
     const u64 l2e = f2(kLog2e, kLog2e);
     u64 vsum[kGroup];
 #pragma unroll
     for (int u = 0; u < kGroup; ++u) {
-        if (u < nvalid) {
+        if (kFull || u < nvalid) {
             u64 p[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 float a0, a1;
-                f2_split(f2_mul(f2_add(bf2_widen(q[u][k]), neg_gm), l2e), a0, a1);
+                f2_split(f2_mul(bf2_sub(q[u][k], gm), l2e), a0, a1);
                 p[k] = f2(ex2_ftz(a0), ex2_ftz(a1));
             }
             vsum[u] = f2_add(f2_add(p[0], p[1]), f2_add(p[2], p[3]));
@@ -278,7 +290,8 @@ __device__ __forceinline__ MS tile_scan(const uint16_t* __restrict__ tile, int64
                 q[u][0] = q[u][1] = q[u][2] = q[u][3] = kNegInf2;
             }
         }
-        group_update(q, nvalid, m, s);
+        if (nvalid == kGroup) group_update<true>(q, nvalid, m, s);
+        else group_update<false>(q, nvalid, m, s);
     }
     return MS{m, s};
 }
@@ -385,18 +398,19 @@ k_logp_fwd(const uint16_t* __restrict__ x, int64_t n, int64_t v, int64_t ld, int
     }
 }
 
-// Forward with bulk copies (16-byte aligned rows, ld % 8 == 0).  Persistent
-// CTAs of 16 warps; CTA b takes rows b, b + grid, b + 2 grid, ...  Each warp
-// streams its tile of successive rows through a private ring of kStages
-// shared-memory stages (one 2 KB group each): lane 0 issues cp.async.bulk for
-// group i + kStages as soon as the warp has read group i, so copies of the
-// next row are already in flight while a row is finished.  The lanes read the
-// same words, in the same order, as tile_scan would load them (a ragged last
-// vector is read from global memory), so results are bitwise those of
-// k_logp_fwd.  Tile partials go to a double-buffered shared array; after one
-// barrier per row, warp (row mod 16) merges them and writes the row.
-// A wait that runs out sets g_device_error; the warp then stops issuing
-// copies and skips waits, and drains its copies in flight before exiting.
+// Forward with bulk copies (16-byte aligned rows, ld % 8 == 0, V < 2^31).
+// Persistent CTAs of 16 warps; CTA b takes rows b, b + grid, b + 2 grid, ...
+// Each warp streams its tile of successive rows through a private ring of
+// kStages shared-memory stages (one 2 KB group each): lane 0 issues
+// cp.async.bulk for group i + kStages as soon as the warp has read group i,
+// so copies of the next row are already in flight while a row is finished.
+// The lanes read the same words, in the same order, as tile_scan would load
+// them (a ragged last vector is read from global memory), so results are
+// bitwise those of k_logp_fwd.  Tile partials go to a double-buffered shared
+// array; after one barrier per row, warp (row mod 16) merges them and writes
+// the row.  A wait that runs out sets g_device_error; the warp then stops
+// issuing copies and skips waits, and drains its copies in flight before
+// exiting.
 __global__ void __launch_bounds__(kFwdThreads, 2)
 k_logp_fwd_bulk(const uint16_t* __restrict__ x, int64_t n, int64_t v, int64_t ld, int64_t W,
                 const int64_t* __restrict__ y, int64_t ignore_index, float* __restrict__ logp,
@@ -411,30 +425,33 @@ k_logp_fwd_bulk(const uint16_t* __restrict__ x, int64_t n, int64_t v, int64_t ld
     fence_mbar_init();
     __syncthreads();
 
+    // tile-local extents fit in 32 bits (the host routes V >= 2^31 elsewhere)
     const int64_t c0 = (int64_t)warp * W;
-    const int64_t width = c0 >= v ? 0 : (v - c0 < W ? v - c0 : W);
-    const int64_t nfull = width >> 3, nvec = (width + 7) >> 3;
-    const int64_t G = (nvec + kGroupVecs - 1) / kGroupVecs;      // groups per row
+    const int width = (int)(c0 >= v ? 0 : (v - c0 < W ? v - c0 : W));
+    const int nfull = width >> 3, nvec = (width + 7) >> 3;
+    const int G = (nvec + kGroupVecs - 1) / kGroupVecs;          // groups per row
+    const int Gfull = nfull / kGroupVecs;                        // groups of 128 full vectors
     const int64_t rows = (n > (int64_t)blockIdx.x) ? (n - 1 - blockIdx.x) / gridDim.x + 1 : 0;
     const int64_t jobs = rows * G;
+    const int64_t row_step = (int64_t)gridDim.x * ld;
 
-    // Issuer position (row iteration, group, stage); every lane tracks it, lane 0
-    // issues.  Job order: row iteration major, group minor.
-    int64_t iss_j = 0;
+    // Issuer: group iss_g of the row at iss_row (its first element of this
+    // tile), stage iss_st.  Every lane tracks it; lane 0 issues.
+    const uint16_t* iss_row = x + (int64_t)blockIdx.x * ld + c0;
     int iss_g = 0, iss_st = 0;
     int64_t issued = 0;
     auto issue_next = [&]() {
         if (lane == 0) {
-            const int64_t t = (int64_t)blockIdx.x + iss_j * gridDim.x;
-            const int64_t nv = nfull - (int64_t)iss_g * kGroupVecs;
+            const int nv = nfull - iss_g * kGroupVecs;
             const uint32_t bytes = nv <= 0 ? 0u : (uint32_t)((nv < kGroupVecs ? nv : kGroupVecs) * 16);
             const uint32_t bar = bar0 + iss_st * 8;
             mbar_arrive_expect_tx(bar, bytes);
-            if (bytes)
-                bulk_g2s(stage0 + iss_st * kStageBytes,
-                         x + t * ld + c0 + (int64_t)iss_g * (kGroupVecs * 8), bytes, bar);
+            if (bytes) bulk_g2s(stage0 + iss_st * kStageBytes, iss_row + iss_g * (kGroupVecs * 8), bytes, bar);
         }
-        if (++iss_g == G) { iss_g = 0; ++iss_j; }
+        if (++iss_g == G) {
+            iss_g = 0;
+            iss_row += row_step;
+        }
         if (++iss_st == kStages) iss_st = 0;
         ++issued;
     };
@@ -445,7 +462,6 @@ k_logp_fwd_bulk(const uint16_t* __restrict__ x, int64_t n, int64_t v, int64_t ld
 
     int st = 0;          // stage of the next group to consume
     uint32_t phase = 0;  // its mbarrier parity
-    int64_t consumed = 0;
     for (int64_t j = 0; j < rows; ++j) {
         const int64_t t = (int64_t)blockIdx.x + j * gridDim.x;
         const int folder = (int)(j % kTiles);
@@ -458,36 +474,54 @@ k_logp_fwd_bulk(const uint16_t* __restrict__ x, int64_t n, int64_t v, int64_t ld
         }
         const uint16_t* __restrict__ tile = x + t * ld + c0;
         float m = -INFINITY, s = 0.f;
-        for (int g = 0; g < (int)G; ++g) {
+        for (int g = 0; g < G; ++g) {
             if (ok) {
                 ok = __all_sync(0xffffffffu, mbar_wait(bar0 + st * 8, phase, kWaitLimitCycles));
-                if (!ok) fail_at = consumed;
+                if (!ok) fail_at = j * G + g;
             }
-            const int64_t v0 = (int64_t)g * kGroupVecs;
+            const uint32_t sbase = stage0 + st * kStageBytes + lane * 16;
             uint32_t q[kGroup][4];
-            int nvalid = 0;
+            if (g < Gfull) {
 #pragma unroll
-            for (int u = 0; u < kGroup; ++u) {
-                const int64_t jv = v0 + kWarp * u + lane;
-                if (jv < nfull) {
-                    const uint4 r = lds_v4(stage0 + st * kStageBytes + (kWarp * u + lane) * 16);
+                for (int u = 0; u < kGroup; ++u) {
+                    const uint4 r = lds_v4(sbase + u * (kWarp * 16));
                     q[u][0] = r.x; q[u][1] = r.y; q[u][2] = r.z; q[u][3] = r.w;
-                    nvalid = u + 1;
-                } else if (jv < nvec) {
-                    load_words<false>(tile, jv * 8, width, q[u]);
-                    nvalid = u + 1;
-                } else {
-                    q[u][0] = q[u][1] = q[u][2] = q[u][3] = kNegInf2;
                 }
+                __syncwarp();
+                if (ok && issued < jobs) {
+                    if (lane == 0) fence_proxy_async_smem();
+                    issue_next();
+                }
+                group_update<true>(q, kGroup, m, s);
+            } else {
+                const int v0 = g * kGroupVecs;
+                int nvalid = 0;
+#pragma unroll
+                for (int u = 0; u < kGroup; ++u) {
+                    const int jv = v0 + kWarp * u + lane;
+                    if (jv < nfull) {
+                        const uint4 r = lds_v4(sbase + u * (kWarp * 16));
+                        q[u][0] = r.x; q[u][1] = r.y; q[u][2] = r.z; q[u][3] = r.w;
+                        nvalid = u + 1;
+                    } else if (jv < nvec) {
+                        load_words<false>(tile, (int64_t)jv * 8, width, q[u]);
+                        nvalid = u + 1;
+                    } else {
+                        q[u][0] = q[u][1] = q[u][2] = q[u][3] = kNegInf2;
+                    }
+                }
+                __syncwarp();
+                if (ok && issued < jobs) {
+                    if (lane == 0) fence_proxy_async_smem();
+                    issue_next();
+                }
+                if (nvalid == kGroup) group_update<true>(q, nvalid, m, s);
+                else group_update<false>(q, nvalid, m, s);
             }
-            __syncwarp();
-            if (ok && issued < jobs) {
-                if (lane == 0) fence_proxy_async_smem();
-                issue_next();
+            if (++st == kStages) {
+                st = 0;
+                phase ^= 1u;
             }
-            ++consumed;
-            if (++st == kStages) { st = 0; phase ^= 1u; }
-            group_update(q, nvalid, m, s);
         }
         MS p = warp_merge(MS{m, s});
         if (lane == 0) {
