@@ -226,8 +226,11 @@ def test_lse_residual_is_the_rounding_error():
     assert np.all(np.abs(lo) <= ulp / 2)
     err_hi = np.abs(hi - ref_lse)
     err_sum = np.abs(hi + lo - ref_lse)
-    print("lse error: fp32", err_hi.max(), "with residual", err_sum.max())
-    assert err_sum.max() < 2e-7 and np.mean(err_sum) < np.mean(err_hi)
+    print("lse error: fp32 max/mean", err_hi.max(), err_hi.mean(),
+          "with residual max/mean", err_sum.max(), err_sum.mean())
+    # what remains is the forward's FP32 accumulation error (a few 1e-8 to
+    # 1e-7 relative); the residual removes the FP32 storage rounding on top
+    assert err_sum.max() < 5e-7 and np.mean(err_sum) < np.mean(err_hi)
 
 
 def test_device_error_word_and_wait_selftest():
