@@ -58,17 +58,51 @@ def _load():
         lib = ctypes.CDLL(_LIB)
         lib.oracle_round_bf16.restype = ctypes.c_uint16
         lib.oracle_round_bf16.argtypes = [ctypes.c_double]
+        lib.oracle_round_f16.restype = ctypes.c_uint16
+        lib.oracle_round_f16.argtypes = [ctypes.c_double]
         lib.oracle_round_bf16_array.argtypes = [_F64P, _U16P, _I64]
         lib.oracle_bf16_to_double_array.argtypes = [_U16P, _F64P, _I64]
-        lib.oracle_forward.argtypes = [_U16P, _I64, _I64, _I64, _I64P, _I64, _F64P, _F64P]
-        lib.oracle_backward.argtypes = [_U16P, _I64, _I64, _I64, _I64P, _I64, _F32P, _F64P, _I64]
-        lib.oracle_backward_compare.argtypes = [_U16P, _I64, _I64, _I64, _I64P, _I64, _F32P,
-                                                _U16P, _I64, _F64P, _I64P]
-        lib.oracle_range_partials.argtypes = [_U16P, _I64, _I64, _I64, _I64, _I64, _F64P, _F64P]
+        lib.oracle_round_f16_array.argtypes = [_F64P, _U16P, _I64]
+        lib.oracle_f16_to_double_array.argtypes = [_U16P, _F64P, _I64]
+        V = ctypes.c_void_p
+        I = ctypes.c_int
+        D = ctypes.c_double
+        lib.oracle_forward.argtypes = [V, I, _I64, _I64, _I64, _I64P, _I64, V, D, _F64P, _F64P]
+        lib.oracle_backward.argtypes = [V, I, _I64, _I64, _I64, _I64P, _I64, V, D, _F32P, _F64P, _I64]
+        lib.oracle_backward_compare.argtypes = [V, I, _I64, _I64, _I64, _I64P, _I64, V, D, _F32P,
+                                                V, I, _I64, _F64P, _I64P]
+        lib.oracle_range_partials.argtypes = [V, I, _I64, _I64, _I64, _I64, _I64, D, _F64P, _F64P]
         lib.oracle_merge_partials.argtypes = [_F64P, _F64P, _I64, _I64, _F64P]
         lib.oracle_num_threads.restype = ctypes.c_int
         _lib = lib
         return lib
+
+
+DTYPES = {"bf16": 0, "f16": 1, "f32": 2}
+
+
+def _logits(x, dtype: str | None):
+    """Contiguous array and dtype code: uint16 bits for bf16/f16, float32 for f32."""
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.float32:
+        if dtype not in (None, "f32"):
+            raise TypeError("float32 logits are dtype f32")
+        return x, DTYPES["f32"]
+    if x.dtype != np.uint16:
+        raise TypeError("logits are uint16 bit patterns (bf16/f16) or float32")
+    dtype = dtype or "bf16"
+    if dtype not in ("bf16", "f16"):
+        raise TypeError("uint16 logits are bf16 or f16 bit patterns")
+    return x, DTYPES[dtype]
+
+
+def _mask(mask, n):
+    if mask is None:
+        return None, None
+    m = np.ascontiguousarray(mask, dtype=np.uint8)
+    if m.shape != (n,):
+        raise ValueError("mask must have shape [n]")
+    return m, m.ctypes.data
 
 
 def _u16(a) -> np.ndarray:
@@ -107,41 +141,70 @@ def bf16_to_f64(b) -> np.ndarray:
     return out.reshape(b.shape)
 
 
-def forward(x, y, ignore_index: int = -100, v: int | None = None):
-    """FP64 (logp[n], lse[n]) of BF16 logits x[n, ld] (first v columns)."""
-    x = _u16(x)
+def round_f16(d) -> np.ndarray:
+    """Nearest binary16 (ties to even) of each double, as uint16 bit patterns."""
+    d = np.asarray(d, dtype=np.float64)
+    flat = np.ascontiguousarray(d.reshape(-1))
+    out = np.empty(flat.shape, dtype=np.uint16)
+    _load().oracle_round_f16_array(flat, out, flat.size)
+    return out.reshape(d.shape)
+
+
+def f16_to_f64(b) -> np.ndarray:
+    b = np.asarray(b)
+    flat = _u16(b.reshape(-1))
+    out = np.empty(flat.shape, dtype=np.float64)
+    _load().oracle_f16_to_double_array(flat, out, flat.size)
+    return out.reshape(b.shape)
+
+
+def forward(x, y, ignore_index: int = -100, v: int | None = None, dtype: str | None = None,
+            scale: float = 1.0, mask=None):
+    """FP64 (logp[n], lse[n]) of logits x[n, ld] (first v columns), with the
+    logits scaled by `scale` (1/temperature) and an optional active mask."""
+    x, dt = _logits(x, dtype)
     n, v, ld = _shape(x, v)
     y = np.ascontiguousarray(y, dtype=np.int64)
+    mk, mp = _mask(mask, n)
     logp = np.empty(n, dtype=np.float64)
     lse = np.empty(n, dtype=np.float64)
-    _load().oracle_forward(x, n, v, ld, y, ignore_index, logp, lse)
+    _load().oracle_forward(x.ctypes.data, dt, n, v, ld, y, ignore_index, mp, float(scale), logp, lse)
     return logp, lse
 
 
-def backward(x, y, g, ignore_index: int = -100, v: int | None = None) -> np.ndarray:
-    """Dense FP64 gradient d[n, v] (small shapes only)."""
-    x = _u16(x)
+def backward(x, y, g, ignore_index: int = -100, v: int | None = None, dtype: str | None = None,
+             scale: float = 1.0, mask=None) -> np.ndarray:
+    """Dense FP64 gradient d[n, v] with respect to the unscaled logits (small
+    shapes only)."""
+    x, dt = _logits(x, dtype)
     n, v, ld = _shape(x, v)
     y = np.ascontiguousarray(y, dtype=np.int64)
     g = np.ascontiguousarray(g, dtype=np.float32)
+    mk, mp = _mask(mask, n)
     d = np.empty((n, v), dtype=np.float64)
-    _load().oracle_backward(x, n, v, ld, y, ignore_index, g, d, v)
+    _load().oracle_backward(x.ctypes.data, dt, n, v, ld, y, ignore_index, mp, float(scale), g, d, v)
     return d
 
 
-def backward_compare(x, y, g, dl, ignore_index: int = -100, v: int | None = None) -> dict:
-    """Stream-compare a BF16 gradient dl[n, ld_out] with the FP64 gradient."""
-    x = _u16(x)
-    dl = _u16(dl)
+def backward_compare(x, y, g, dl, ignore_index: int = -100, v: int | None = None,
+                     dtype: str | None = None, scale: float = 1.0, mask=None,
+                     out_dtype: str | None = None) -> dict:
+    """Stream-compare a gradient dl[n, ld_out] (uint16 bits of bf16/f16, or
+    float32) with the FP64 gradient; "correctly rounded" = equal to the nearest
+    value of the output dtype (that of the logits unless out_dtype is given)."""
+    x, dt = _logits(x, dtype)
     n, v, ld = _shape(x, v)
+    dl, odt = _logits(dl, out_dtype if out_dtype is not None else
+                      (None if x.dtype == np.float32 else (dtype or "bf16")))
     if dl.ndim != 2 or dl.shape[0] != n or dl.shape[1] < v:
         raise ValueError("dlogits shape mismatch")
     y = np.ascontiguousarray(y, dtype=np.int64)
     g = np.ascontiguousarray(g, dtype=np.float32)
+    mk, mp = _mask(mask, n)
     stats = np.zeros(3, dtype=np.float64)
     counts = np.zeros(3, dtype=np.int64)
-    _load().oracle_backward_compare(x, n, v, ld, y, ignore_index, g, dl, dl.shape[1],
-                                    stats, counts)
+    _load().oracle_backward_compare(x.ctypes.data, dt, n, v, ld, y, ignore_index, mp, float(scale),
+                                    g, dl.ctypes.data, odt, dl.shape[1], stats, counts)
     return {
         "max_abs_diff": float(stats[0]),
         "max_abs_d": float(stats[1]),
@@ -152,13 +215,15 @@ def backward_compare(x, y, g, dl, ignore_index: int = -100, v: int | None = None
     }
 
 
-def range_partials(x, w: int, k: int, v: int | None = None):
-    """FP64 (m, s) partials [n, k] over consecutive column ranges of width w."""
-    x = _u16(x)
+def range_partials(x, w: int, k: int, v: int | None = None, dtype: str | None = None,
+                   scale: float = 1.0):
+    """FP64 (m, s) partials [n, k] of the scaled logits over consecutive column
+    ranges of width w."""
+    x, dt = _logits(x, dtype)
     n, v, ld = _shape(x, v)
     pm = np.empty((n, k), dtype=np.float64)
     ps = np.empty((n, k), dtype=np.float64)
-    _load().oracle_range_partials(x, n, v, ld, w, k, pm, ps)
+    _load().oracle_range_partials(x.ctypes.data, dt, n, v, ld, w, k, float(scale), pm, ps)
     return pm, ps
 
 

@@ -19,9 +19,19 @@
  *   - PR #314 "Deterministic config option", ReductionSpec text: padded
  *     columns count as -inf, and (-inf, 0) is the identity partial.
  *
- * Everything is computed in IEEE double from the exact BF16 inputs with a
- * plain two-pass log-sum-exp.  Compile with -ffp-contract=off so that x86
- * and Arm hosts round identically.
+ * Everything is computed in IEEE double from the exact inputs with a plain
+ * two-pass log-sum-exp.  Compile with -ffp-contract=off so that x86 and Arm
+ * hosts round identically.
+ *
+ * Variants (the same definitions, generalised):
+ *   - logits in BF16, FP16 or FP32 (PR #495 Tests: accuracy for
+ *     FP32/BF16/FP16 against an FP64 reference), widened exactly;
+ *   - a temperature: the logits are scaled by s = 1/T before the log-softmax
+ *     (PR #495, the provider experiment: rollout logprobs at temperature 1.0
+ *     and 0.7), so LSE = log sum exp(s x), logp = s x_y - LSE and, by the chain
+ *     rule, d = s g (onehot - exp(s x - LSE));
+ *   - an explicit active-row mask (PR #314, MaskMode explicit_active_mask):
+ *     a row is active only if its mask byte is nonzero.
  */
 #include <math.h>
 #include <stdint.h>
@@ -73,103 +83,177 @@ void oracle_bf16_to_double_array(const uint16_t* in, double* out, int64_t count)
     for (int64_t i = 0; i < count; ++i) out[i] = bf16_bits_to_double(in[i]);
 }
 
-/* ---- row log-sum-exp ----------------------------------------------------- */
+/* ---- FP16 and element access by dtype ------------------------------------- */
 
-/* A row is active when its target names a real vocabulary column and is not
- * the ignore index (PR #495, Behavior changes: out-of-range targets). */
-static int row_active(int64_t y, int64_t v, int64_t ignore_index) {
-    return y >= 0 && y < v && y != ignore_index;
+enum { DT_BF16 = 0, DT_F16 = 1, DT_F32 = 2 };
+
+/* IEEE binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits;
+ * subnormals below 2^-14 with spacing 2^-24. */
+static double f16_bits_to_double(uint16_t h) {
+    int sign = (h >> 15) & 1, e = (h >> 10) & 0x1f, f = h & 0x3ff;
+    double v;
+    if (e == 0x1f) v = f ? NAN : INFINITY;
+    else if (e == 0) v = ldexp((double)f, -24);
+    else v = ldexp((double)(f | 0x400), e - 25);
+    return sign ? -v : v;
 }
 
-/* Plain two-pass log-sum-exp over columns [c0, c1) of one row:
- * m = max x, lse = m + log(sum exp(x - m)).  An all -inf range gives
- * m = -inf and lse = -inf (the identity partial's log-sum-exp). */
-static void range_max_sumexp(const uint16_t* xr, int64_t c0, int64_t c1,
-                             double* m_out, double* s_out) {
+/* Round a double to the nearest binary16 (ties to even); overflow to inf at
+ * 65520 = max + half an ulp. */
+uint16_t oracle_round_f16(double d) {
+    if (isnan(d)) return 0x7e00;
+    uint16_t sign = signbit(d) ? 0x8000 : 0;
+    double a = fabs(d);
+    if (isinf(a)) return sign | 0x7c00;
+    if (a == 0.0) return sign;
+    int e;
+    (void)frexp(a, &e);
+    int q = (e - 1) - 10;            /* exponent of one unit in the last place */
+    if (q < -24) q = -24;            /* subnormal spacing */
+    double r = nearbyint(ldexp(a, -q));
+    double val = ldexp(r, q);
+    if (val >= 65520.0) return sign | 0x7c00;
+    /* encode val (exactly representable) */
+    if (val < ldexp(1.0, -14)) return sign | (uint16_t)ldexp(val, 24);
+    int ev;
+    double fr = frexp(val, &ev);     /* val = fr * 2^ev, fr in [0.5, 1) */
+    uint16_t bits = (uint16_t)(((ev - 1 + 15) << 10) | ((uint16_t)ldexp(fr * 2.0 - 1.0, 10)));
+    return sign | bits;
+}
+
+void oracle_round_f16_array(const double* in, uint16_t* out, int64_t count) {
+    for (int64_t i = 0; i < count; ++i) out[i] = oracle_round_f16(in[i]);
+}
+
+void oracle_f16_to_double_array(const uint16_t* in, double* out, int64_t count) {
+    for (int64_t i = 0; i < count; ++i) out[i] = f16_bits_to_double(in[i]);
+}
+
+/* Element c of row t of an [n, ld] logit matrix of the given dtype, exactly. */
+static double elem(const void* x, int dtype, int64_t ld, int64_t t, int64_t c) {
+    int64_t i = t * ld + c;
+    if (dtype == DT_F32) return (double)((const float*)x)[i];
+    if (dtype == DT_F16) return f16_bits_to_double(((const uint16_t*)x)[i]);
+    return bf16_bits_to_double(((const uint16_t*)x)[i]);
+}
+
+/* The value of the output dtype nearest to d (ties to even), as a double. */
+static double round_to(double d, int dtype) {
+    if (dtype == DT_F32) return (double)(float)d;  /* C conversion rounds to nearest even */
+    if (dtype == DT_F16) return f16_bits_to_double(oracle_round_f16(d));
+    return bf16_bits_to_double(oracle_round_bf16(d));
+}
+
+/* ---- row log-sum-exp ----------------------------------------------------- */
+
+/* Plain two-pass log-sum-exp of the scaled row s * x over columns [c0, c1):
+ * m = max s x, sum = sum exp(s x - m).  An all -inf range gives m = -inf and
+ * sum = 0, the identity partial (PR #314, ReductionSpec). */
+static void range_max_sumexp(const void* x, int dtype, int64_t ld, int64_t t, int64_t c0,
+                             int64_t c1, double s, double* m_out, double* s_out) {
     double m = -INFINITY;
     for (int64_t c = c0; c < c1; ++c) {
-        double x = bf16_bits_to_double(xr[c]);
-        if (x > m) m = x;
+        double v = s * elem(x, dtype, ld, t, c);
+        if (v > m) m = v;
     }
-    double s = 0.0;
+    double acc = 0.0;
     if (m != -INFINITY) {
         for (int64_t c = c0; c < c1; ++c) {
-            double x = bf16_bits_to_double(xr[c]);
-            if (x != -INFINITY) s += exp(x - m);
+            double v = s * elem(x, dtype, ld, t, c);
+            if (v != -INFINITY) acc += exp(v - m);
         }
     }
     *m_out = m;
-    *s_out = s;
+    *s_out = acc;
 }
 
-static double row_lse(const uint16_t* xr, int64_t v) {
-    double m, s;
-    range_max_sumexp(xr, 0, v, &m, &s);
+/* LSE = m + log(sum exp(s x - m)) over the whole row (-inf for an all -inf row). */
+static double row_lse(const void* x, int dtype, int64_t ld, int64_t t, int64_t v, double s) {
+    double m, acc;
+    range_max_sumexp(x, dtype, ld, t, 0, v, s, &m, &acc);
     if (m == -INFINITY) return -INFINITY;
-    return m + log(s);
+    return m + log(acc);
 }
 
-/* ---- forward: logp and lse ----------------------------------------------- */
+/* A row is active when its mask byte (if a mask is given) is nonzero and its
+ * target names a real vocabulary column other than the ignore index (PR #495,
+ * Behavior changes: out-of-range targets; PR #314 MaskMode). */
+static int row_active(const int64_t* y, const uint8_t* mask, int64_t t, int64_t v,
+                      int64_t ignore_index) {
+    return (mask == 0 || mask[t] != 0) && y[t] >= 0 && y[t] < v && y[t] != ignore_index;
+}
 
-/* logp[t] = x[t, y_t] - LSE_t for active rows, 0 otherwise; lse[t] = LSE_t
- * for every row (issue #241 Background; PR #495 Behavior changes). */
-void oracle_forward(const uint16_t* x, int64_t n, int64_t v, int64_t ld,
-                    const int64_t* y, int64_t ignore_index,
-                    double* logp, double* lse) {
-#pragma omp parallel for schedule(static)
+/* ---- vocab partials and their merge ---------------------------------------- */
+
+/* Merge of k partials per row in index order (issue #241, PR 3 bullets):
+ * M = max m_l, S = sum s_l exp(m_l - M), LSE = M + log S.  Identity
+ * partials (m = -inf) contribute nothing; a row of identities has LSE -inf. */
+void oracle_merge_partials(const double* pm, const double* ps, int64_t n,
+                           int64_t k, double* lse) {
     for (int64_t t = 0; t < n; ++t) {
-        const uint16_t* xr = x + t * ld;
-        double l = row_lse(xr, v);
-        lse[t] = l;
-        logp[t] = row_active(y[t], v, ignore_index)
-                      ? bf16_bits_to_double(xr[y[t]]) - l
-                      : 0.0;
+        const double* m = pm + t * k;
+        const double* s = ps + t * k;
+        double M = -INFINITY;
+        for (int64_t j = 0; j < k; ++j)
+            if (m[j] > M) M = m[j];
+        if (M == -INFINITY) {
+            lse[t] = -INFINITY;
+            continue;
+        }
+        double S = 0.0;
+        for (int64_t j = 0; j < k; ++j)
+            if (m[j] != -INFINITY) S += s[j] * exp(m[j] - M);
+        lse[t] = M + log(S);
     }
 }
 
-/* ---- backward ------------------------------------------------------------ */
+/* ---- entry points (dtype, scale s = 1/T, active mask) ----------------------- */
 
-/* One gradient element of an active row: d = g * (onehot - softmax), with the
- * softmax taken as exp(x - LSE) (PR #495 Summary item 2).  On the target
- * column 1 - exp(u) is written as -expm1(u), the same quantity without the
- * cancellation when the target's probability is near 1. */
-static double grad_elem(double x, double l, double g, int on_target) {
-    double u = x - l;
-    return on_target ? -g * expm1(u) : -g * exp(u);
-}
-
-/* Dense FP64 gradient for small shapes: d[t*ld_d + c].  Inactive rows are
- * exactly zero. */
-void oracle_backward(const uint16_t* x, int64_t n, int64_t v, int64_t ld,
-                     const int64_t* y, int64_t ignore_index, const float* g,
-                     double* d, int64_t ld_d) {
+/* logp[t] = s x[t, y_t] - LSE_t for active rows (else 0), lse[t] = LSE_t,
+ * LSE_t = log sum_v exp(s x[t, v]). */
+void oracle_forward(const void* x, int dtype, int64_t n, int64_t v, int64_t ld,
+                       const int64_t* y, int64_t ignore_index, const uint8_t* mask, double s,
+                       double* logp, double* lse) {
 #pragma omp parallel for schedule(static)
     for (int64_t t = 0; t < n; ++t) {
-        const uint16_t* xr = x + t * ld;
+        double l = row_lse(x, dtype, ld, t, v, s);
+        lse[t] = l;
+        logp[t] = row_active(y, mask, t, v, ignore_index) ? s * elem(x, dtype, ld, t, y[t]) - l : 0.0;
+    }
+}
+
+/* Dense gradient with respect to the unscaled logits:
+ * d = s g (onehot - exp(s x - LSE)), the target column as -s g expm1(s x_y - LSE). */
+void oracle_backward(const void* x, int dtype, int64_t n, int64_t v, int64_t ld,
+                        const int64_t* y, int64_t ignore_index, const uint8_t* mask, double s,
+                        const float* g, double* d, int64_t ld_d) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < n; ++t) {
         double* dr = d + t * ld_d;
-        if (!row_active(y[t], v, ignore_index)) {
+        if (!row_active(y, mask, t, v, ignore_index)) {
             for (int64_t c = 0; c < v; ++c) dr[c] = 0.0;
             continue;
         }
-        double l = row_lse(xr, v);
-        double gt = (double)g[t];
-        for (int64_t c = 0; c < v; ++c)
-            dr[c] = grad_elem(bf16_bits_to_double(xr[c]), l, gt, c == y[t]);
+        double l = row_lse(x, dtype, ld, t, v, s);
+        double gs = s * (double)g[t];
+        for (int64_t c = 0; c < v; ++c) {
+            double u = s * elem(x, dtype, ld, t, c) - l;
+            dr[c] = (c == y[t]) ? -gs * expm1(u) : -gs * exp(u);
+        }
     }
 }
 
-/* Streaming comparison of a BF16 gradient against the FP64 gradient, one row
- * at a time, never holding an FP64 [n, v] array.  stats (doubles):
- *   [0] max |dl - d64|            [1] max |d64|
- *   [2] max |round_bf16(d64) - d64|   (the error a correctly rounded result has)
- * counts (int64):
- *   [0] elements compared   [1] elements whose bits differ from round_bf16(d64)
- *   [2] elements that are NaN/inf in dl where d64 is finite
- * Values are compared as numbers, so +0 and -0 count as equal. */
-void oracle_backward_compare(const uint16_t* x, int64_t n, int64_t v, int64_t ld,
-                             const int64_t* y, int64_t ignore_index,
-                             const float* g, const uint16_t* dl, int64_t ld_out,
-                             double* stats, int64_t* counts) {
+/* Streaming comparison of a gradient buffer dl[n, ld_out] in dtype out_dtype
+ * with the FP64 gradient, one row at a time, never holding an FP64 [n, v]
+ * array.  stats (doubles): [0] max |dl - d64|, [1] max |d64|,
+ * [2] max |round(d64) - d64| (the error a correctly rounded result has);
+ * counts (int64): [0] elements compared, [1] elements whose value differs from
+ * the nearest out_dtype value of d64, [2] non-finite outputs where d64 is
+ * finite.  Values are compared as numbers (+0 equals -0). */
+void oracle_backward_compare(const void* x, int dtype, int64_t n, int64_t v, int64_t ld,
+                                const int64_t* y, int64_t ignore_index, const uint8_t* mask,
+                                double s, const float* g, const void* dl, int out_dtype,
+                                int64_t ld_out, double* stats, int64_t* counts) {
     double max_diff = 0.0, max_d = 0.0, max_gap = 0.0;
     int64_t n_cmp = 0, n_bad = 0, n_nonfinite = 0;
 #pragma omp parallel
@@ -178,16 +262,17 @@ void oracle_backward_compare(const uint16_t* x, int64_t n, int64_t v, int64_t ld
         int64_t l_cmp = 0, l_bad = 0, l_nf = 0;
 #pragma omp for schedule(static)
         for (int64_t t = 0; t < n; ++t) {
-            const uint16_t* xr = x + t * ld;
-            const uint16_t* gr = dl + t * ld_out;
-            int act = row_active(y[t], v, ignore_index);
-            double l = act ? row_lse(xr, v) : 0.0;
-            double gt = (double)g[t];
+            int act = row_active(y, mask, t, v, ignore_index);
+            double l = act ? row_lse(x, dtype, ld, t, v, s) : 0.0;
+            double gs = s * (double)g[t];
             for (int64_t c = 0; c < v; ++c) {
-                double d64 = act ? grad_elem(bf16_bits_to_double(xr[c]), l, gt, c == y[t]) : 0.0;
-                uint16_t cr = oracle_round_bf16(d64);
-                double crv = bf16_bits_to_double(cr);
-                double got = bf16_bits_to_double(gr[c]);
+                double d64 = 0.0;
+                if (act) {
+                    double u = s * elem(x, dtype, ld, t, c) - l;
+                    d64 = (c == y[t]) ? -gs * expm1(u) : -gs * exp(u);
+                }
+                double crv = round_to(d64, out_dtype);
+                double got = elem(dl, out_dtype, ld_out, t, c);
                 double diff = fabs(got - d64);
                 if (!isfinite(got) && isfinite(d64)) ++l_nf;
                 if (diff > l_diff || isnan(diff)) l_diff = isnan(diff) ? INFINITY : diff;
@@ -215,44 +300,17 @@ void oracle_backward_compare(const uint16_t* x, int64_t n, int64_t v, int64_t ld
     counts[2] = n_nonfinite;
 }
 
-/* ---- vocab partials and their merge ---------------------------------------- */
-
-/* Per-range partials (issue #241, PR 3 bullets): for each row and each of k
- * consecutive column ranges of width w (the last ones clipped at v, empty
- * ones giving the identity (-inf, 0)), m = max x and s = sum exp(x - m). */
-void oracle_range_partials(const uint16_t* x, int64_t n, int64_t v, int64_t ld,
-                           int64_t w, int64_t k, double* pm, double* ps) {
+/* Range partials of the scaled row (m = max s x, s = sum exp(s x - m)). */
+void oracle_range_partials(const void* x, int dtype, int64_t n, int64_t v, int64_t ld,
+                              int64_t w, int64_t k, double s, double* pm, double* ps) {
 #pragma omp parallel for schedule(static)
     for (int64_t t = 0; t < n; ++t) {
-        const uint16_t* xr = x + t * ld;
         for (int64_t j = 0; j < k; ++j) {
             int64_t c0 = j * w, c1 = (j + 1) * w;
             if (c0 > v) c0 = v;
             if (c1 > v) c1 = v;
-            range_max_sumexp(xr, c0, c1, &pm[t * k + j], &ps[t * k + j]);
+            range_max_sumexp(x, dtype, ld, t, c0, c1, s, &pm[t * k + j], &ps[t * k + j]);
         }
-    }
-}
-
-/* Merge of k partials per row in index order (issue #241, PR 3 bullets):
- * M = max m_l, S = sum s_l exp(m_l - M), LSE = M + log S.  Identity
- * partials (m = -inf) contribute nothing; a row of identities has LSE -inf. */
-void oracle_merge_partials(const double* pm, const double* ps, int64_t n,
-                           int64_t k, double* lse) {
-    for (int64_t t = 0; t < n; ++t) {
-        const double* m = pm + t * k;
-        const double* s = ps + t * k;
-        double M = -INFINITY;
-        for (int64_t j = 0; j < k; ++j)
-            if (m[j] > M) M = m[j];
-        if (M == -INFINITY) {
-            lse[t] = -INFINITY;
-            continue;
-        }
-        double S = 0.0;
-        for (int64_t j = 0; j < k; ++j)
-            if (m[j] != -INFINITY) S += s[j] * exp(m[j] - M);
-        lse[t] = M + log(S);
     }
 }
 

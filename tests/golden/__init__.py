@@ -43,6 +43,30 @@ def closed_forms():
     return cases
 
 
+def temperature_forms():
+    """Cases of temperature_forms.txt (as closed_forms, plus "scale")."""
+    cases = []
+    with open(os.path.join(HERE, "temperature_forms.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            name, v, lg, y, sc, g, logp, lse, d = [t.strip() for t in line.split(";")]
+            v = int(v)
+            cases.append({
+                "name": name,
+                "v": v,
+                "logits": np.array(_floats(lg, v), dtype=np.float64),
+                "target": int(y),
+                "scale": float(sc),
+                "grad": None if g == "-" else float(g),
+                "logp": float(logp),
+                "lse": float(lse),
+                "dlogits": None if d == "-" else np.array(_floats(d, v), dtype=np.float64),
+            })
+    return cases
+
+
 def to_bf16_bits_exact(vals) -> np.ndarray:
     """BF16 bit patterns of values that are exactly representable in BF16
     (raises otherwise): the top half of their binary32 encoding."""
@@ -56,4 +80,4 @@ def to_bf16_bits_exact(vals) -> np.ndarray:
     return (u >> 16).astype(np.uint16)
 
 
-__all__ = ["closed_forms", "to_bf16_bits_exact"]
+__all__ = ["closed_forms", "temperature_forms", "to_bf16_bits_exact"]

@@ -396,3 +396,133 @@ def test_workload_recipe_shapes():
     lw = workloads.WORKLOADS["long"]
     gl = workloads.grads(64, lw.grad, 0)
     assert torch.all(gl.abs() == 1.0 / 64)
+
+
+# ---------------------------------------------------------------- variants: FP16 / FP32 logits,
+# temperature, explicit active mask
+
+
+def test_f16_widening_matches_numpy():
+    b = np.arange(0, 65536, dtype=np.uint16)
+    got = oracle.f16_to_f64(b)
+    want = b.view(np.float16).astype(np.float64)
+    finite = ~np.isnan(want)
+    assert np.array_equal(got[finite], want[finite]) and np.all(np.isnan(got[~finite]))
+
+
+def test_round_f16_matches_numpy_and_known_values():
+    rng = np.random.default_rng(20)
+    d = np.concatenate([rng.standard_normal(20000) * 10.0 ** rng.integers(-9, 6, 20000),
+                        (1 + (2 * rng.integers(0, 1024, 500) + 1) * 2.0 ** -11)
+                        * 2.0 ** rng.integers(-14, 15, 500),          # ties
+                        rng.integers(1, 2048, 200) * 2.0 ** -25])      # subnormal ties
+    got = oracle.round_f16(d)
+    with np.errstate(over="ignore"):
+        want = d.astype(np.float16).view(np.uint16)
+    assert np.array_equal(got, want)
+    for val, bits in [(65504.0, 0x7BFF), (65519.99, 0x7BFF), (65520.0, 0x7C00), (2.0 ** -24, 0x0001),
+                      (2.0 ** -25, 0x0000), (3 * 2.0 ** -25, 0x0002), (-1.0, 0xBC00),
+                      (1.0 + 2.0 ** -11, 0x3C00), (1.0 + 3 * 2.0 ** -11, 0x3C02)]:
+        assert int(oracle.round_f16(val)) == bits, (val, hex(int(oracle.round_f16(val))))
+
+
+@pytest.mark.parametrize("dtype", ["f16", "f32"])
+def test_forward_other_dtypes_match_torch(dtype):
+    rng = np.random.default_rng(21)
+    n, v = 12, 1031
+    f = (rng.standard_normal((n, v)) * 3.0).astype(np.float32)
+    x = f.astype(np.float16).view(np.uint16) if dtype == "f16" else f
+    xv = (x.view(np.float16).astype(np.float64) if dtype == "f16" else f.astype(np.float64))
+    y = rng.integers(0, v, n).astype(np.int64)
+    for scale in (1.0, float(np.float32(1 / 0.7))):
+        logp, lse = oracle.forward(x, y, dtype=dtype, scale=scale)
+        t = torch.from_numpy(xv) * scale
+        ref = torch.log_softmax(t, 1).gather(1, torch.from_numpy(y)[:, None])[:, 0].numpy()
+        np.testing.assert_allclose(logp, ref, rtol=0, atol=1e-11)
+        np.testing.assert_allclose(lse, torch.logsumexp(t, 1).numpy(), rtol=1e-13)
+
+
+@pytest.mark.parametrize("case", __import__("golden").temperature_forms(), ids=lambda c: c["name"])
+def test_temperature_closed_forms(case):
+    x = _bits(case["logits"])[None, :]
+    y = np.array([case["target"]], dtype=np.int64)
+    logp, lse = oracle.forward(x, y, IGN, scale=case["scale"])
+    assert abs(logp[0] - case["logp"]) <= 1e-13 * max(1.0, abs(case["logp"]))
+    assert abs(lse[0] - case["lse"]) <= 1e-13 * max(1.0, abs(case["lse"]))
+    if case["dlogits"] is not None:
+        d = oracle.backward(x, y, np.array([case["grad"]], np.float32), IGN, scale=case["scale"])
+        np.testing.assert_allclose(d[0], case["dlogits"], rtol=0, atol=1e-14)
+
+
+def test_temperature_gradient_by_richardson_central_differences():
+    """With a temperature the gradient with respect to the unscaled logits
+    carries the factor s (chain rule); central differences of the oracle's own
+    forward see it."""
+    rng = np.random.default_rng(22)
+    v = 10
+    base = rng.integers(2, 4, v).astype(np.float64) + rng.integers(0, 8, v) * 2.0 ** -3
+    y = np.array([3], dtype=np.int64)
+    g = np.array([1.5], dtype=np.float32)
+    for scale in (0.5, float(np.float32(1 / 0.7)), 3.0):
+        d = oracle.backward(_bits(base)[None, :], y, g, IGN, scale=scale)[0]
+        for c in range(v):
+            est = []
+            for h in (2.0 ** -5, 2.0 ** -6):
+                xp, xm = base.copy(), base.copy()
+                xp[c] += h
+                xm[c] -= h
+                lp = oracle.forward(_bits(xp)[None, :], y, IGN, scale=scale)[0][0]
+                lm = oracle.forward(_bits(xm)[None, :], y, IGN, scale=scale)[0][0]
+                est.append((lp - lm) / (2 * h))
+            rich = (4 * est[1] - est[0]) / 3
+            assert abs(1.5 * rich - d[c]) < 2e-6 * scale ** 3, (scale, c, rich, d[c])
+
+
+def test_active_mask():
+    rng = np.random.default_rng(23)
+    x = _rand_bf16(rng, 6, 50)
+    y = rng.integers(0, 50, 6).astype(np.int64)
+    y[4] = IGN
+    g = np.ones(6, dtype=np.float32)
+    mask = np.array([1, 0, 1, 0, 1, 1], dtype=np.uint8)
+    logp0, lse0 = oracle.forward(x, y, IGN)
+    logp, lse = oracle.forward(x, y, IGN, mask=mask)
+    d0 = oracle.backward(x, y, g, IGN)
+    d = oracle.backward(x, y, g, IGN, mask=mask)
+    for t in range(6):
+        if mask[t] and y[t] != IGN:
+            assert logp[t] == logp0[t] and np.array_equal(d[t], d0[t])
+        else:
+            assert logp[t] == 0.0 and np.all(d[t] == 0.0)
+    assert np.array_equal(lse, lse0)  # the LSE is computed for every row
+
+
+@pytest.mark.parametrize("out_dtype", ["f16", "f32"])
+def test_backward_compare_other_out_dtypes(out_dtype):
+    rng = np.random.default_rng(24)
+    n, v = 6, 200
+    f = (rng.standard_normal((n, v)) * 2).astype(np.float32)
+    x = f.astype(np.float16).view(np.uint16) if out_dtype == "f16" else f
+    y = rng.integers(0, v, n).astype(np.int64)
+    g = rng.standard_normal(n).astype(np.float32)
+    d = oracle.backward(x, y, g, dtype=out_dtype)
+    cr = oracle.round_f16(d) if out_dtype == "f16" else d.astype(np.float32)
+    st = oracle.backward_compare(x, y, g, cr, dtype=out_dtype)
+    assert st["n_not_correctly_rounded"] == 0 and st["n_compared"] == n * v
+    bad = cr.copy()
+    if out_dtype == "f16":
+        bad[2, 5] ^= 1
+    else:
+        bad[2, 5] = np.nextafter(bad[2, 5], np.float32(np.inf))
+    assert oracle.backward_compare(x, y, g, bad, dtype=out_dtype)["n_not_correctly_rounded"] == 1
+
+
+def test_scaled_range_partials_merge_to_scaled_lse():
+    rng = np.random.default_rng(25)
+    x = _rand_bf16(rng, 4, 1031, sigma=3.0)
+    s = float(np.float32(1 / 0.7))
+    pm, ps = oracle.range_partials(x, 72, 16, scale=s)
+    _, lse = oracle.forward(x, np.zeros(4, np.int64), scale=s)
+    np.testing.assert_allclose(oracle.merge_partials(pm, ps), lse, rtol=1e-13)
+    xv = oracle.bf16_to_f64(x)
+    assert np.array_equal(pm[:, 0], (s * xv[:, :72]).max(axis=1))
