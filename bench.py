@@ -59,7 +59,7 @@ def _peaks():
 
 def _kernel_hash() -> str:
     h = hashlib.sha256()
-    for fn in ("fused_logp.cu", "logp_kernels.cuh"):
+    for fn in ("fused_logp.cu", "logp_kernels.cuh", "logp_prims.cuh"):
         with open(os.path.join(ROOT, "selected_token_logprob_gb300", "csrc", fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -167,16 +167,19 @@ def run_ours(args):
 
     wl = workloads.WORKLOADS[args.workload]
     n, v = wl.n, wl.v
-    x, y, g = workloads.make(wl, device=dev, seed=wl.seed + rank)
+    tdt = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[args.dtype]
+    ebytes = 4 if args.dtype == "f32" else 2
+    temp = args.temperature
+    x, y, g = workloads.make(wl, device=dev, seed=wl.seed + rank, dtype=tdt)
     logp = torch.empty(n, dtype=torch.float32, device=dev)
     lse = torch.empty(n, dtype=torch.float32, device=dev)
     lse_lo = torch.empty(n, dtype=torch.float32, device=dev)
-    dl = torch.empty((n, v), dtype=torch.bfloat16, device=dev)
+    dl = torch.empty((n, v), dtype=tdt, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        flp.fused_logp_forward(x, y, logp=logp, lse=lse, lse_lo=lse_lo)
-        flp.fused_logp_backward(x, y, lse, g, dlogits=dl, lse_lo=lse_lo)
+        flp.fused_logp_forward(x, y, logp=logp, lse=lse, lse_lo=lse_lo, temperature=temp)
+        flp.fused_logp_backward(x, y, lse, g, dlogits=dl, lse_lo=lse_lo, temperature=temp)
 
     for _ in range(args.warmup):
         step()
@@ -192,9 +195,9 @@ def run_ours(args):
         t0.record(stream)
         for k in range(args.steps):
             ev[k][0].record(stream)
-            flp.fused_logp_forward(x, y, logp=logp, lse=lse, lse_lo=lse_lo)
+            flp.fused_logp_forward(x, y, logp=logp, lse=lse, lse_lo=lse_lo, temperature=temp)
             ev[k][1].record(stream)
-            flp.fused_logp_backward(x, y, lse, g, dlogits=dl, lse_lo=lse_lo)
+            flp.fused_logp_backward(x, y, lse, g, dlogits=dl, lse_lo=lse_lo, temperature=temp)
             ev[k][2].record(stream)
         t1.record(stream)
         torch.cuda.synchronize(dev)
@@ -204,35 +207,38 @@ def run_ours(args):
     bwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
     ms_per_step = total_ms / args.steps
     logits_per_rank = n * v
-    value = world * logits_per_rank * BYTES_PER_LOGIT / (ms_per_step * 1e-3) / 1e9
+    bpl = BYTES_PER_LOGIT * ebytes // 2              # algorithmic bytes per logit, this dtype
+    value = world * logits_per_rank * bpl / (ms_per_step * 1e-3) / 1e9
 
     # end to end through the public API from pinned host buffers
-    e2e = run_e2e(args, flp, x, y, g, dev, stream, world)
+    e2e = run_e2e(args, flp, x, y, g, dev, stream, world, temp, bpl)
 
     peak, peak_src = _peaks()
     bwd_avg = statistics.mean(bwd_ms)
     fwd_avg = statistics.mean(fwd_ms)
-    achieved = logits_per_rank * BWD_BYTES_PER_LOGIT / (bwd_avg * 1e-3) / 1e9
+    achieved = logits_per_rank * BWD_BYTES_PER_LOGIT * ebytes // 2 / (bwd_avg * 1e-3) / 1e9
     clocks = sampler.summary()
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": round(value / (logits_per_rank * BYTES_PER_LOGIT / (PAGES_FWD_BWD_MS * 1e-3) / 1e9), 3)
-        if world == 1 else None,
+        if world == 1 and args.dtype == "bf16" and temp == 1.0 else None,
         "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD_DESC, "n": n, "v": v, "logits_dtype": "bf16",
+        "config": {"workload": WORKLOAD_DESC if args.workload == "long" else args.workload,
+                   "n": n, "v": v, "logits_dtype": args.dtype, "temperature": temp,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "inputs (9.96 GB) exceed the 129 MB L2; no flush"},
         "fwd_ms": round(fwd_avg, 4), "bwd_ms": round(bwd_avg, 4),
-        "fwd_gbs": round(logits_per_rank * FWD_BYTES_PER_LOGIT / (fwd_avg * 1e-3) / 1e9, 1),
+        "fwd_gbs": round(logits_per_rank * FWD_BYTES_PER_LOGIT * ebytes // 2 / (fwd_avg * 1e-3) / 1e9, 1),
         "bwd_gbs": round(achieved, 1),
         "roofline": {"kernel": "k_logp_bwd", "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": peak_src,
-                     "traffic": _profiled_traffic("k_logp_bwd"),
-                     "fwd_frac": round(logits_per_rank * FWD_BYTES_PER_LOGIT / (fwd_avg * 1e-3)
-                                       / 1e9 / peak, 4),
+                     "traffic": _profiled_traffic("k_logp_bwd")
+                     if args.dtype == "bf16" and args.workload == "long" else None,
+                     "fwd_frac": round(logits_per_rank * FWD_BYTES_PER_LOGIT * ebytes // 2
+                                       / (fwd_avg * 1e-3) / 1e9 / peak, 4),
                      "step_frac": round(value / world / peak, 4)},
         "e2e": e2e,
         "gpu_launches": 2 * args.steps,
@@ -248,7 +254,7 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_e2e(args, flp, x, y, g, dev, stream, world):
+def run_e2e(args, flp, x, y, g, dev, stream, world, temp=1.0, bpl=BYTES_PER_LOGIT):
     import torch
 
     n, v = x.shape
@@ -270,8 +276,8 @@ def run_e2e(args, flp, x, y, g, dev, stream, world):
         dx.copy_(hx, non_blocking=True)
         dy.copy_(hy, non_blocking=True)
         dg.copy_(hg, non_blocking=True)
-        flp.fused_logp_forward(dx, dy, logp=logp, lse=lse, lse_lo=lse_lo)
-        flp.fused_logp_backward(dx, dy, lse, dg, dlogits=dl, lse_lo=lse_lo)
+        flp.fused_logp_forward(dx, dy, logp=logp, lse=lse, lse_lo=lse_lo, temperature=temp)
+        flp.fused_logp_backward(dx, dy, lse, dg, dlogits=dl, lse_lo=lse_lo, temperature=temp)
         hlogp.copy_(logp, non_blocking=True)
         hlse.copy_(lse, non_blocking=True)
 
@@ -289,9 +295,9 @@ def run_e2e(args, flp, x, y, g, dev, stream, world):
     torch.cuda.synchronize(dev)
     ms = _max_over_ranks(a.elapsed_time(b) / steps, world, dev)
     del hx
-    return {"value": round(world * n * v * BYTES_PER_LOGIT / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
+    return {"value": round(world * n * v * bpl / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
             "ms_per_step": round(ms, 3), "steps": steps,
-            "h2d_bytes_per_step": n * v * 2 + n * 8 + n * 4,
+            "h2d_bytes_per_step": n * v * x.element_size() + n * 8 + n * 4,
             "d2h_bytes_per_step": n * 4 * 2}
 
 
@@ -326,7 +332,7 @@ def cpu_baseline(args, x, y, g, v):
     import oracle
     import workloads
 
-    if args.cpu_seconds <= 0:
+    if args.cpu_seconds <= 0 or x.dtype != __import__("torch").bfloat16:
         return None
     rows = min(512, x.shape[0])
     xs = workloads.bf16_bits(x[:rows])
@@ -389,6 +395,9 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-rows", type=int, default=128)
+    ap.add_argument("--dtype", choices=["bf16", "f16", "f32"], default="bf16",
+                    help="logits dtype (the metric is quoted for bf16)")
+    ap.add_argument("--temperature", type=float, default=1.0)
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps
     if args.impl == "reference":

@@ -64,6 +64,12 @@ typedef struct CUstream_st* flp_stream_t;
 
 #define FLP_NUM_TILES 16
 
+/* Logit dtypes of the _ex entry points (the gradient is written in the same
+ * dtype).  PR #495 Tests name FP32/BF16/FP16 logits. */
+#define FLP_DTYPE_BF16 0
+#define FLP_DTYPE_F16 1
+#define FLP_DTYPE_F32 2
+
 /* Message of the last failing call on this thread ("" after success). */
 const char* flp_last_error(void);
 
@@ -152,6 +158,43 @@ flp_status logp_merge_partials(const float* part_max, const float* part_sum,
                                const float* sel, const int64_t* targets,
                                int64_t ignore_index, int64_t n, int64_t v_total,
                                float* logp, float* lse, float* lse_lo, flp_stream_t stream);
+
+/*
+ * Generalised forms (the calls above are these with FLP_DTYPE_BF16, no mask
+ * and inv_temperature = 1).
+ *   dtype           FLP_DTYPE_BF16 / FLP_DTYPE_F16 / FLP_DTYPE_F32: the dtype of
+ *                   logits, shard_logits and dlogits.
+ *   active_mask     [n] uint8 or NULL: a row is active only if its byte is
+ *                   nonzero (and its target is in [0, v) and not ignore_index)
+ *                   (PR #314, MaskMode explicit_active_mask).
+ *   inv_temperature s = 1/T > 0, finite: the logits are scaled by s before the
+ *                   log-softmax, as in rollout logprobs at a temperature (PR
+ *                   #495, provider experiment at T = 1.0 and 0.7):
+ *                   LSE = log sum exp(s x), logp = s x_y - LSE, and the
+ *                   gradient with respect to the unscaled logits is
+ *                   s g (onehot - exp(s x - LSE)).
+ * Shard partials hold m = max x (unscaled) and sum exp(s (x - m)); a merge
+ * must use the same inv_temperature as the partials.  Any other value of
+ * dtype or inv_temperature is FLP_EINVAL.
+ */
+flp_status fused_logp_forward_ex(const void* logits, int dtype, int64_t n, int64_t v, int64_t ld,
+                                 const int64_t* targets, int64_t ignore_index,
+                                 const uint8_t* active_mask, float inv_temperature, float* logp,
+                                 float* lse, float* lse_lo, flp_stream_t stream);
+flp_status fused_logp_backward_ex(const void* logits, int dtype, int64_t n, int64_t v, int64_t ld,
+                                  const int64_t* targets, int64_t ignore_index,
+                                  const uint8_t* active_mask, float inv_temperature,
+                                  const float* lse, const float* lse_lo, const float* grad,
+                                  void* dlogits, int64_t ld_out, flp_stream_t stream);
+flp_status logp_shard_partials_ex(const void* shard_logits, int dtype, int64_t n, int64_t ld_shard,
+                                  int64_t vocab_start, int64_t real_width, int64_t v_total,
+                                  float inv_temperature, const int64_t* targets, float* part_max,
+                                  float* part_sum, float* sel, flp_stream_t stream);
+flp_status logp_merge_partials_ex(const float* part_max, const float* part_sum, const float* sel,
+                                  const int64_t* targets, int64_t ignore_index,
+                                  const uint8_t* active_mask, int64_t n, int64_t v_total,
+                                  float inv_temperature, float* logp, float* lse, float* lse_lo,
+                                  flp_stream_t stream);
 
 /*
  * Health of the device side (no counterpart in the pages: a guard of this

@@ -20,9 +20,13 @@ Entry points (same names as the C ABI):
 residual), and ``flp_device_error`` / ``flp_selftest_wait_timeout`` for the
 device-side health word.
 
-Logits are BF16 [N, V] (row stride may exceed V: pass a column slice of a
-wider buffer), targets int64 [N], the upstream gradient FP32 [N]; logp and
-lse are FP32 [N].  ``ignore_index`` defaults to -100.
+Logits are BF16, FP16 or FP32 [N, V] (row stride may exceed V: pass a column
+slice of a wider buffer), targets int64 [N], the upstream gradient FP32 [N];
+logp and lse are FP32 [N]; the gradient has the logits' dtype.
+``ignore_index`` defaults to -100.  ``temperature`` T scales the logits by
+1/T before the log-softmax (the gradient is with respect to the unscaled
+logits); ``active_mask`` (bool or uint8 [N]) excludes rows explicitly.  The
+shard partials and their merge must use the same temperature.
 """
 
 from __future__ import annotations
@@ -34,6 +38,7 @@ from ._lib import FusedLogpError
 
 IGNORE_INDEX = -100
 NUM_TILES = 16
+_DTYPES = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}
 
 __all__ = [
     "FusedLogp",
@@ -92,15 +97,40 @@ def _opt_ptr(t: torch.Tensor | None) -> int | None:
     return None if t is None else t.data_ptr()
 
 
+def _dtype(x: torch.Tensor, name: str) -> int:
+    if x.dtype not in _DTYPES:
+        raise TypeError(f"{name} must be bfloat16, float16 or float32, got {x.dtype}")
+    return _DTYPES[x.dtype]
+
+
+def _inv_temperature(temperature: float) -> float:
+    t = float(temperature)
+    if not (t > 0.0) or t == float("inf"):
+        raise ValueError(f"temperature must be finite and > 0, got {temperature}")
+    return 1.0 / t   # rounded to binary32 at the C boundary
+
+
+def _mask(active_mask: torch.Tensor | None, n: int) -> int | None:
+    if active_mask is None:
+        return None
+    if active_mask.dtype not in (torch.bool, torch.uint8):
+        raise TypeError("active_mask must be bool or uint8")
+    if active_mask.dim() != 1 or active_mask.shape[0] != n or (n > 1 and active_mask.stride(0) != 1):
+        raise ValueError(f"active_mask must be a contiguous [{n}] tensor")
+    _cuda(active_mask)
+    return active_mask.data_ptr()
+
+
 def fused_logp_forward(logits: torch.Tensor, targets: torch.Tensor,
                        ignore_index: int = IGNORE_INDEX,
                        logp: torch.Tensor | None = None, lse: torch.Tensor | None = None,
-                       lse_lo: torch.Tensor | None = None, with_lse_lo: bool = False):
-    """(logp, lse), FP32 [N] each, of BF16 logits [N, V]; (logp, lse, lse_lo)
+                       lse_lo: torch.Tensor | None = None, with_lse_lo: bool = False,
+                       temperature: float = 1.0, active_mask: torch.Tensor | None = None):
+    """(logp, lse), FP32 [N] each, of logits [N, V]; (logp, lse, lse_lo)
     when ``with_lse_lo`` is true or an ``lse_lo`` buffer is given."""
     n, v, ld = _rows(logits, "logits")
-    if logits.dtype != torch.bfloat16:
-        raise TypeError(f"logits must be torch.bfloat16, got {logits.dtype}")
+    dt = _dtype(logits, "logits")
+    inv_t = _inv_temperature(temperature)
     _vec(targets, "targets", n, torch.int64)
     dev = logits.device
     logp = torch.empty(n, dtype=torch.float32, device=dev) if logp is None else logp
@@ -114,10 +144,11 @@ def fused_logp_forward(logits: torch.Tensor, targets: torch.Tensor,
     if want_lo:
         _vec(lse_lo, "lse_lo", n, torch.float32)
         _cuda(lse_lo)
+    mp = _mask(active_mask, n)
     if n > 0:
-        st = _lib.load().fused_logp_forward(logits.data_ptr(), n, v, ld, targets.data_ptr(),
-                                            int(ignore_index), logp.data_ptr(), lse.data_ptr(),
-                                            _opt_ptr(lse_lo), _stream(logits))
+        st = _lib.load().fused_logp_forward_ex(logits.data_ptr(), dt, n, v, ld, targets.data_ptr(),
+                                               int(ignore_index), mp, inv_t, logp.data_ptr(),
+                                               lse.data_ptr(), _opt_ptr(lse_lo), _stream(logits))
         _lib.check("fused_logp_forward", st)
     return (logp, lse, lse_lo) if want_lo else (logp, lse)
 
@@ -125,14 +156,16 @@ def fused_logp_forward(logits: torch.Tensor, targets: torch.Tensor,
 def fused_logp_backward(logits: torch.Tensor, targets: torch.Tensor, lse: torch.Tensor,
                         grad: torch.Tensor, ignore_index: int = IGNORE_INDEX,
                         dlogits: torch.Tensor | None = None,
-                        lse_lo: torch.Tensor | None = None) -> torch.Tensor:
-    """dlogits BF16 [N, V] = grad * (onehot(targets) - softmax(logits)).
+                        lse_lo: torch.Tensor | None = None, temperature: float = 1.0,
+                        active_mask: torch.Tensor | None = None) -> torch.Tensor:
+    """dlogits [N, V] (the logits' dtype) = grad / T * (onehot(targets) -
+    softmax(logits / T)).
 
     ``dlogits`` may be ``logits`` itself (in-place gradient).  ``lse_lo`` is
     the residual returned by the forward with ``with_lse_lo=True``."""
     n, v, ld = _rows(logits, "logits")
-    if logits.dtype != torch.bfloat16:
-        raise TypeError(f"logits must be torch.bfloat16, got {logits.dtype}")
+    dt = _dtype(logits, "logits")
+    inv_t = _inv_temperature(temperature)
     _vec(targets, "targets", n, torch.int64)
     _vec(lse, "lse", n, torch.float32)
     _vec(grad, "grad", n, torch.float32)
@@ -140,24 +173,26 @@ def fused_logp_backward(logits: torch.Tensor, targets: torch.Tensor, lse: torch.
         _vec(lse_lo, "lse_lo", n, torch.float32)
         _cuda(lse_lo)
     if dlogits is None:
-        dlogits = torch.empty((n, v), dtype=torch.bfloat16, device=logits.device)
-    if dlogits.dtype != torch.bfloat16 or tuple(dlogits.shape) != (n, v):
-        raise ValueError("dlogits must be BF16 with the logits' shape")
+        dlogits = torch.empty((n, v), dtype=logits.dtype, device=logits.device)
+    if dlogits.dtype != logits.dtype or tuple(dlogits.shape) != (n, v):
+        raise ValueError("dlogits must have the logits' dtype and shape")
     _, _, ld_out = _rows(dlogits, "dlogits")
     _cuda(logits, targets, lse, grad, dlogits)
+    mp = _mask(active_mask, n)
     if n == 0:
         return dlogits
-    st = _lib.load().fused_logp_backward(logits.data_ptr(), n, v, ld, targets.data_ptr(),
-                                         int(ignore_index), lse.data_ptr(), _opt_ptr(lse_lo),
-                                         grad.data_ptr(), dlogits.data_ptr(), ld_out,
-                                         _stream(logits))
+    st = _lib.load().fused_logp_backward_ex(logits.data_ptr(), dt, n, v, ld, targets.data_ptr(),
+                                            int(ignore_index), mp, inv_t, lse.data_ptr(),
+                                            _opt_ptr(lse_lo), grad.data_ptr(), dlogits.data_ptr(),
+                                            ld_out, _stream(logits))
     _lib.check("fused_logp_backward", st)
     return dlogits
 
 
 def logp_shard_partials(shard_logits: torch.Tensor, vocab_start: int, real_width: int,
                         v_total: int, targets: torch.Tensor, part_max: torch.Tensor,
-                        part_sum: torch.Tensor, sel: torch.Tensor) -> None:
+                        part_sum: torch.Tensor, sel: torch.Tensor,
+                        temperature: float = 1.0) -> None:
     """Write one vocab shard's tile partials into part_max/part_sum [N, 16]
     and, for rows whose target it owns, the selected logit into sel [N].
 
@@ -165,8 +200,8 @@ def logp_shard_partials(shard_logits: torch.Tensor, vocab_start: int, real_width
     [vocab_start, vocab_start + real_width); columns >= real_width are padding
     and are never read."""
     n, wpad, ld = _rows(shard_logits, "shard_logits")
-    if shard_logits.dtype != torch.bfloat16:
-        raise TypeError("shard_logits must be torch.bfloat16")
+    dt = _dtype(shard_logits, "shard_logits")
+    inv_t = _inv_temperature(temperature)
     if real_width > wpad:
         raise ValueError(f"real_width {real_width} exceeds the shard width {wpad}")
     _vec(targets, "targets", n, torch.int64)
@@ -177,10 +212,11 @@ def logp_shard_partials(shard_logits: torch.Tensor, vocab_start: int, real_width
     _cuda(shard_logits, targets, part_max, part_sum, sel)
     if n == 0:
         return
-    st = _lib.load().logp_shard_partials(shard_logits.data_ptr(), n, ld, int(vocab_start),
-                                         int(real_width), int(v_total), targets.data_ptr(),
-                                         part_max.data_ptr(), part_sum.data_ptr(),
-                                         sel.data_ptr(), _stream(shard_logits))
+    st = _lib.load().logp_shard_partials_ex(shard_logits.data_ptr(), dt, n, ld, int(vocab_start),
+                                            int(real_width), int(v_total), inv_t,
+                                            targets.data_ptr(), part_max.data_ptr(),
+                                            part_sum.data_ptr(), sel.data_ptr(),
+                                            _stream(shard_logits))
     _lib.check("logp_shard_partials", st)
 
 
@@ -188,9 +224,11 @@ def logp_merge_partials(part_max: torch.Tensor, part_sum: torch.Tensor, sel: tor
                         targets: torch.Tensor, v_total: int,
                         ignore_index: int = IGNORE_INDEX,
                         logp: torch.Tensor | None = None, lse: torch.Tensor | None = None,
-                        lse_lo: torch.Tensor | None = None, with_lse_lo: bool = False):
+                        lse_lo: torch.Tensor | None = None, with_lse_lo: bool = False,
+                        temperature: float = 1.0, active_mask: torch.Tensor | None = None):
     """(logp, lse) [or (logp, lse, lse_lo)] from the tile partials of shards
     covering [0, v_total)."""
+    inv_t = _inv_temperature(temperature)
     n = targets.shape[0] if targets.dim() == 1 else -1
     _vec(targets, "targets", n, torch.int64)
     for name, t in (("part_max", part_max), ("part_sum", part_sum)):
@@ -209,12 +247,13 @@ def logp_merge_partials(part_max: torch.Tensor, part_sum: torch.Tensor, sel: tor
     if want_lo:
         _vec(lse_lo, "lse_lo", n, torch.float32)
         _cuda(lse_lo)
+    mp = _mask(active_mask, n)
     if n > 0:
-        st = _lib.load().logp_merge_partials(part_max.data_ptr(), part_sum.data_ptr(),
-                                             sel.data_ptr(), targets.data_ptr(),
-                                             int(ignore_index), n, int(v_total),
-                                             logp.data_ptr(), lse.data_ptr(), _opt_ptr(lse_lo),
-                                             _stream(targets))
+        st = _lib.load().logp_merge_partials_ex(part_max.data_ptr(), part_sum.data_ptr(),
+                                                sel.data_ptr(), targets.data_ptr(),
+                                                int(ignore_index), mp, n, int(v_total), inv_t,
+                                                logp.data_ptr(), lse.data_ptr(), _opt_ptr(lse_lo),
+                                                _stream(targets))
         _lib.check("logp_merge_partials", st)
     return (logp, lse, lse_lo) if want_lo else (logp, lse)
 
@@ -224,24 +263,29 @@ class FusedLogp(torch.autograd.Function):
     writes dlogits straight to BF16 from the saved FP32 LSE (O(N) state)."""
 
     @staticmethod
-    def forward(ctx, logits, targets, ignore_index=IGNORE_INDEX):
-        logp, lse, lse_lo = fused_logp_forward(logits, targets, ignore_index, with_lse_lo=True)
-        ctx.save_for_backward(logits, targets, lse, lse_lo)
+    def forward(ctx, logits, targets, ignore_index=IGNORE_INDEX, temperature=1.0,
+                active_mask=None):
+        logp, lse, lse_lo = fused_logp_forward(logits, targets, ignore_index, with_lse_lo=True,
+                                               temperature=temperature, active_mask=active_mask)
+        ctx.save_for_backward(logits, targets, lse, lse_lo, active_mask)
         ctx.ignore_index = ignore_index
+        ctx.temperature = temperature
         return logp
 
     @staticmethod
     def backward(ctx, grad_logp):
-        logits, targets, lse, lse_lo = ctx.saved_tensors
+        logits, targets, lse, lse_lo, active_mask = ctx.saved_tensors
         g = grad_logp.to(torch.float32).contiguous()
-        d = fused_logp_backward(logits, targets, lse, g, ctx.ignore_index, lse_lo=lse_lo)
-        return d, None, None
+        d = fused_logp_backward(logits, targets, lse, g, ctx.ignore_index, lse_lo=lse_lo,
+                                temperature=ctx.temperature, active_mask=active_mask)
+        return d, None, None, None, None
 
 
 def fused_logp(logits: torch.Tensor, targets: torch.Tensor,
-               ignore_index: int = IGNORE_INDEX) -> torch.Tensor:
+               ignore_index: int = IGNORE_INDEX, temperature: float = 1.0,
+               active_mask: torch.Tensor | None = None) -> torch.Tensor:
     """Autograd-aware selected-token logp (FP32 [N])."""
-    return FusedLogp.apply(logits, targets, ignore_index)
+    return FusedLogp.apply(logits, targets, ignore_index, temperature, active_mask)
 
 
 def flp_device_error(device: int | torch.device = 0) -> int:

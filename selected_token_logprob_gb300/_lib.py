@@ -30,6 +30,14 @@ SIGNATURES = {
     "fused_logp_backward": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P, _P, _I64, _P]),
     "logp_shard_partials": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P]),
     "logp_merge_partials": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _P, _P, _P, _P]),
+    "fused_logp_forward_ex": (ctypes.c_int, [_P, ctypes.c_int, _I64, _I64, _I64, _P, _I64, _P,
+                                             ctypes.c_float, _P, _P, _P, _P]),
+    "fused_logp_backward_ex": (ctypes.c_int, [_P, ctypes.c_int, _I64, _I64, _I64, _P, _I64, _P,
+                                              ctypes.c_float, _P, _P, _P, _P, _I64, _P]),
+    "logp_shard_partials_ex": (ctypes.c_int, [_P, ctypes.c_int, _I64, _I64, _I64, _I64, _I64,
+                                              ctypes.c_float, _P, _P, _P, _P, _P]),
+    "logp_merge_partials_ex": (ctypes.c_int, [_P, _P, _P, _P, _I64, _P, _I64, _I64,
+                                              ctypes.c_float, _P, _P, _P, _P]),
     "flp_device_error": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_int)]),
     "flp_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_int, _I64, ctypes.POINTER(ctypes.c_int)]),
 }

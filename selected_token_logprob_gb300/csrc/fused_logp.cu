@@ -3,6 +3,7 @@
 // include/fused_logp.h.  All checks run on the host before any launch and
 // report through the return code (no device-side traps).
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdarg.h>
 #include <stdint.h>
 #include <stdio.h>
@@ -35,6 +36,8 @@ int64_t tile_width(int64_t v) {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+int elem_bytes(int dtype) { return dtype == FLP_DTYPE_F32 ? 4 : 2; }
+
 // Bytes spanned by an [n, ld] matrix whose rows use the first `v` columns.
 bool span_bytes(int64_t n, int64_t v, int64_t ld, int64_t elem, int64_t* out) {
     int64_t a, b;
@@ -51,8 +54,7 @@ flp_status device_of(const void* p, const char* name, int* dev) {
     const cudaError_t e = cudaPointerGetAttributes(&a, p);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
-        return fail(FLP_EINVAL, "%s: cudaPointerGetAttributes failed (%s)", name,
-                    cudaGetErrorString(e));
+        return fail(FLP_EINVAL, "%s: cudaPointerGetAttributes failed (%s)", name, cudaGetErrorString(e));
     }
     if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged)
         return fail(FLP_EINVAL, "%s must point to device memory", name);
@@ -60,18 +62,23 @@ flp_status device_of(const void* p, const char* name, int* dev) {
     return FLP_OK;
 }
 
-// All pointers must be device memory of one device; returns that device.
+// Every required pointer, and every optional one that is not null, must be
+// device memory of one device; returns that device.
 flp_status common_device(int count, const void* const* ptrs, const char* const* names,
-                         int* dev) {
+                         const bool* optional, int* dev) {
     int d0 = -1;
+    const char* first = nullptr;
     for (int i = 0; i < count; ++i) {
+        if (optional && optional[i] && ptrs[i] == nullptr) continue;
         int d;
         const flp_status st = device_of(ptrs[i], names[i], &d);
         if (st != FLP_OK) return st;
-        if (i == 0) d0 = d;
-        else if (d != d0)
-            return fail(FLP_EINVAL, "%s is on device %d but %s is on device %d", names[i], d,
-                        names[0], d0);
+        if (!first) {
+            d0 = d;
+            first = names[i];
+        } else if (d != d0) {
+            return fail(FLP_EINVAL, "%s is on device %d but %s is on device %d", names[i], d, first, d0);
+        }
     }
     *dev = d0;
     return FLP_OK;
@@ -104,28 +111,157 @@ flp_status check_launch(const char* what) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Rows start on 16-byte boundaries: base aligned and the byte stride a
+// multiple of 16.
+bool rows_aligned16(const void* p, int64_t ld, int dtype) {
+    return aligned16(p) && (ld * elem_bytes(dtype)) % 16 == 0;
+}
+
 constexpr int64_t kMaxGrid = 2147483647;
 constexpr int kMaxDevices = 64;
 
-// Once per device: allow the bulk-copy forward its dynamic shared memory, and
-// cache the SM count used to size its persistent grid.
-flp_status bulk_forward_setup(int dev, int* sms) {
-    static int sm_count[kMaxDevices];
-    static bool ready[kMaxDevices];
-    if (dev < 0 || dev >= kMaxDevices) return fail(FLP_ECUDA, "device index %d out of range", dev);
-    if (!ready[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(flp::k_logp_fwd_bulk,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             flp::kFwdSmemBytes);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return fail(FLP_ECUDA, "forward setup: %s", cudaGetErrorString(e));
-        ready[dev] = true;
-    }
-    *sms = sm_count[dev];
+int grid_for(int64_t items) { return (int)(items < kMaxGrid ? items : kMaxGrid); }
+
+flp_status check_dtype(int dtype) {
+    if (dtype != FLP_DTYPE_BF16 && dtype != FLP_DTYPE_F16 && dtype != FLP_DTYPE_F32)
+        return fail(FLP_EINVAL, "dtype must be FLP_DTYPE_BF16, FLP_DTYPE_F16 or FLP_DTYPE_F32 (got %d)", dtype);
     return FLP_OK;
 }
 
-int grid_for(int64_t items) { return (int)(items < kMaxGrid ? items : kMaxGrid); }
+flp_status check_scale(float s) {
+    if (!(s > 0.f) || !isfinite(s))
+        return fail(FLP_EINVAL, "inv_temperature must be finite and > 0 (got %g)", (double)s);
+    return FLP_OK;
+}
+
+// s and s log2(e) as a two-float, from the double value of log2(e).
+flp::Scale make_scale(float s) {
+    const double c = (double)s * 1.4426950408889634073599246810019;
+    const float hi = (float)c;
+    return flp::Scale{s, hi, (float)(c - (double)hi)};
+}
+
+int sm_count(int dev) {
+    static int count[kMaxDevices];
+    if (count[dev] == 0) {
+        int c = 0;
+        if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        count[dev] = c;
+    }
+    return count[dev];
+}
+
+// Once per device and kernel: allow the bulk-copy forward its dynamic shared
+// memory (idempotent, so a race between threads is harmless).
+template <flp::Dt D, bool kScaled>
+flp_status bulk_setup(int dev) {
+    static bool ready[kMaxDevices];
+    if (!ready[dev]) {
+        const cudaError_t e = cudaFuncSetAttribute(flp::k_logp_fwd_bulk<D, kScaled>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   flp::kFwdSmemBytes<D>);
+        if (e != cudaSuccess) return fail(FLP_ECUDA, "forward setup: %s", cudaGetErrorString(e));
+        ready[dev] = true;
+    }
+    return FLP_OK;
+}
+
+struct FwdArgs {
+    const void* x;
+    int64_t n, v, ld, W;
+    const int64_t* y;
+    int64_t ii;
+    const uint8_t* mask;
+    flp::Scale sc;
+    float *logp, *lse, *lse_lo;
+    cudaStream_t s;
+    int dev;
+    bool bulk;
+};
+
+template <flp::Dt D, bool kScaled>
+flp_status launch_forward(const FwdArgs& a) {
+    if (a.bulk) {
+        flp_status st = bulk_setup<D, kScaled>(a.dev);
+        if (st != FLP_OK) return st;
+        const int sms = sm_count(a.dev);
+        if (sms <= 0) return fail(FLP_ECUDA, "could not read the SM count of device %d", a.dev);
+        const int64_t ctas = (int64_t)flp::kFwdMinBlocks<D> * sms;
+        const int grid = grid_for(a.n < ctas ? a.n : ctas);
+        flp::k_logp_fwd_bulk<D, kScaled><<<grid, flp::kFwdThreads, flp::kFwdSmemBytes<D>, a.s>>>(
+            a.x, a.n, a.v, a.ld, a.W, a.y, a.ii, a.mask, a.sc, a.logp, a.lse, a.lse_lo);
+    } else {
+        flp::k_logp_fwd<D, kScaled><<<grid_for(a.n), flp::kFwdThreads, 0, a.s>>>(
+            a.x, a.n, a.v, a.ld, a.W, a.y, a.ii, a.mask, a.sc, a.logp, a.lse, a.lse_lo);
+    }
+    return check_launch("forward");
+}
+
+template <flp::Dt D>
+flp_status launch_forward_d(const FwdArgs& a) {
+    return a.sc.s == 1.f ? launch_forward<D, false>(a) : launch_forward<D, true>(a);
+}
+
+struct BwdArgs {
+    const void* x;
+    int64_t n, v, ld;
+    const int64_t* y;
+    int64_t ii;
+    const uint8_t* mask;
+    float s;
+    const float *lse, *lse_lo, *g;
+    void* dx;
+    int64_t ld_out, segs;
+    cudaStream_t st;
+    bool vin, vout, in_place;
+};
+
+template <flp::Dt D, bool VI, bool VO, bool IP>
+void launch_bwd(const BwdArgs& a, int grid) {
+    flp::k_logp_bwd<D, VI, VO, IP><<<grid, flp::kBwdThreads, 0, a.st>>>(
+        a.x, a.n, a.v, a.ld, a.y, a.ii, a.mask, a.s, a.lse, a.lse_lo, a.g, a.dx, a.ld_out, a.segs);
+}
+
+template <flp::Dt D>
+void launch_backward_d(const BwdArgs& a, int grid) {
+    if (a.in_place) {
+        if (a.vin) launch_bwd<D, true, true, true>(a, grid);
+        else launch_bwd<D, false, false, true>(a, grid);
+    } else if (a.vin && a.vout) launch_bwd<D, true, true, false>(a, grid);
+    else if (a.vin) launch_bwd<D, true, false, false>(a, grid);
+    else if (a.vout) launch_bwd<D, false, true, false>(a, grid);
+    else launch_bwd<D, false, false, false>(a, grid);
+}
+
+struct PartArgs {
+    const void* xs;
+    int64_t n, ld, real_width, W;
+    int tile0, ntile;
+    int64_t vocab_start;
+    const int64_t* y;
+    flp::Scale sc;
+    float *pm, *ps, *sel;
+    cudaStream_t s;
+    bool vec;
+};
+
+template <flp::Dt D, bool V, bool S>
+void launch_part(const PartArgs& a) {
+    flp::k_logp_partials<D, V, S><<<grid_for(a.n), a.ntile * flp::kWarp, 0, a.s>>>(
+        a.xs, a.n, a.ld, a.real_width, a.W, a.tile0, a.vocab_start, a.y, a.sc, a.pm, a.ps, a.sel);
+}
+
+template <flp::Dt D>
+void launch_partials_d(const PartArgs& a) {
+    const bool scaled = a.sc.s != 1.f;
+    if (a.vec) {
+        if (scaled) launch_part<D, true, true>(a);
+        else launch_part<D, true, false>(a);
+    } else {
+        if (scaled) launch_part<D, false, true>(a);
+        else launch_part<D, false, false>(a);
+    }
+}
 
 }  // namespace
 
@@ -133,61 +269,72 @@ extern "C" {
 
 const char* flp_last_error(void) { return g_msg; }
 
-const char* flp_version(void) { return "fused_logp 0.1 (sm_103a)"; }
+const char* flp_version(void) { return "fused_logp 0.2 (sm_103a)"; }
 
 int64_t flp_tile_width(int64_t v) { return tile_width(v); }
 
-flp_status fused_logp_forward(const void* logits, int64_t n, int64_t v, int64_t ld,
-                              const int64_t* targets, int64_t ignore_index, float* logp,
-                              float* lse, float* lse_lo, flp_stream_t stream) {
+flp_status fused_logp_forward_ex(const void* logits, int dtype, int64_t n, int64_t v, int64_t ld,
+                                 const int64_t* targets, int64_t ignore_index,
+                                 const uint8_t* active_mask, float inv_temperature, float* logp,
+                                 float* lse, float* lse_lo, flp_stream_t stream) {
+    flp_status st;
+    if ((st = check_dtype(dtype)) != FLP_OK) return st;
+    if ((st = check_scale(inv_temperature)) != FLP_OK) return st;
     if (n < 0) return fail(FLP_EINVAL, "n must be >= 0 (got %lld)", (long long)n);
     if (v < 1) return fail(FLP_EINVAL, "v must be >= 1 (got %lld)", (long long)v);
     if (ld < v) return fail(FLP_EINVAL, "ld (%lld) must be >= v (%lld)", (long long)ld, (long long)v);
     if (n == 0) return ok();
     int64_t bytes;
-    if (!span_bytes(n, v, ld, 2, &bytes)) return fail(FLP_EINVAL, "logits extent overflows int64");
-    const void* ptrs[] = {logits, targets, logp, lse, lse_lo ? lse_lo : lse};
-    const char* names[] = {"logits", "targets", "logp", "lse", "lse_lo"};
+    if (!span_bytes(n, v, ld, elem_bytes(dtype), &bytes))
+        return fail(FLP_EINVAL, "logits extent overflows int64");
+    const void* ptrs[] = {logits, targets, logp, lse, lse_lo, active_mask};
+    const char* names[] = {"logits", "targets", "logp", "lse", "lse_lo", "active_mask"};
+    const bool optional[] = {false, false, false, false, true, true};
     int dev;
-    flp_status st = common_device(5, ptrs, names, &dev);
-    if (st != FLP_OK) return st;
+    if ((st = common_device(6, ptrs, names, optional, &dev)) != FLP_OK) return st;
+    if (dev < 0 || dev >= kMaxDevices) return fail(FLP_ECUDA, "device index %d out of range", dev);
     DeviceGuard guard;
     if ((st = guard.enter(dev)) != FLP_OK) return st;
 
-    const int64_t W = tile_width(v);
-    const uint16_t* x = static_cast<const uint16_t*>(logits);
-    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (aligned16(x) && ld % 8 == 0 && v < ((int64_t)1 << 31)) {
-        int sms;
-        if ((st = bulk_forward_setup(dev, &sms)) != FLP_OK) return st;
-        const int grid = grid_for(n < 2 * (int64_t)sms ? n : 2 * (int64_t)sms);
-        flp::k_logp_fwd_bulk<<<grid, flp::kFwdThreads, flp::kFwdSmemBytes, s>>>(
-            x, n, v, ld, W, targets, ignore_index, logp, lse, lse_lo);
-    } else {
-        flp::k_logp_fwd<false><<<grid_for(n), flp::kFwdThreads, 0, s>>>(
-            x, n, v, ld, W, targets, ignore_index, logp, lse, lse_lo);
-    }
-    return check_launch("forward");
+    const FwdArgs a{logits, n, v, ld, tile_width(v), targets, ignore_index, active_mask,
+                    make_scale(inv_temperature), logp, lse, lse_lo,
+                    reinterpret_cast<cudaStream_t>(stream), dev,
+                    rows_aligned16(logits, ld, dtype) && v < ((int64_t)1 << 31)};
+    if (dtype == FLP_DTYPE_BF16) return launch_forward_d<flp::Dt::BF16>(a);
+    if (dtype == FLP_DTYPE_F16) return launch_forward_d<flp::Dt::F16>(a);
+    return launch_forward_d<flp::Dt::F32>(a);
 }
 
-flp_status fused_logp_backward(const void* logits, int64_t n, int64_t v, int64_t ld,
-                               const int64_t* targets, int64_t ignore_index, const float* lse,
-                               const float* lse_lo, const float* grad, void* dlogits,
-                               int64_t ld_out, flp_stream_t stream) {
+flp_status fused_logp_forward(const void* logits, int64_t n, int64_t v, int64_t ld,
+                              const int64_t* targets, int64_t ignore_index, float* logp,
+                              float* lse, float* lse_lo, flp_stream_t stream) {
+    return fused_logp_forward_ex(logits, FLP_DTYPE_BF16, n, v, ld, targets, ignore_index, nullptr,
+                                 1.f, logp, lse, lse_lo, stream);
+}
+
+flp_status fused_logp_backward_ex(const void* logits, int dtype, int64_t n, int64_t v, int64_t ld,
+                                  const int64_t* targets, int64_t ignore_index,
+                                  const uint8_t* active_mask, float inv_temperature,
+                                  const float* lse, const float* lse_lo, const float* grad,
+                                  void* dlogits, int64_t ld_out, flp_stream_t stream) {
+    flp_status st;
+    if ((st = check_dtype(dtype)) != FLP_OK) return st;
+    if ((st = check_scale(inv_temperature)) != FLP_OK) return st;
     if (n < 0) return fail(FLP_EINVAL, "n must be >= 0 (got %lld)", (long long)n);
     if (v < 1) return fail(FLP_EINVAL, "v must be >= 1 (got %lld)", (long long)v);
     if (ld < v) return fail(FLP_EINVAL, "ld (%lld) must be >= v (%lld)", (long long)ld, (long long)v);
     if (ld_out < v)
         return fail(FLP_EINVAL, "ld_out (%lld) must be >= v (%lld)", (long long)ld_out, (long long)v);
     if (n == 0) return ok();
+    const int eb = elem_bytes(dtype);
     int64_t in_bytes, out_bytes;
-    if (!span_bytes(n, v, ld, 2, &in_bytes) || !span_bytes(n, v, ld_out, 2, &out_bytes))
+    if (!span_bytes(n, v, ld, eb, &in_bytes) || !span_bytes(n, v, ld_out, eb, &out_bytes))
         return fail(FLP_EINVAL, "logits/dlogits extent overflows int64");
-    const void* ptrs[] = {logits, targets, lse, grad, dlogits, lse_lo ? lse_lo : lse};
-    const char* names[] = {"logits", "targets", "lse", "grad", "dlogits", "lse_lo"};
+    const void* ptrs[] = {logits, targets, lse, grad, dlogits, lse_lo, active_mask};
+    const char* names[] = {"logits", "targets", "lse", "grad", "dlogits", "lse_lo", "active_mask"};
+    const bool optional[] = {false, false, false, false, false, true, true};
     int dev;
-    flp_status st = common_device(6, ptrs, names, &dev);
-    if (st != FLP_OK) return st;
+    if ((st = common_device(7, ptrs, names, optional, &dev)) != FLP_OK) return st;
 
     const uintptr_t xb = reinterpret_cast<uintptr_t>(logits);
     const uintptr_t db = reinterpret_cast<uintptr_t>(dlogits);
@@ -198,41 +345,41 @@ flp_status fused_logp_backward(const void* logits, int64_t n, int64_t v, int64_t
     DeviceGuard guard;
     if ((st = guard.enter(dev)) != FLP_OK) return st;
 
-    const uint16_t* x = static_cast<const uint16_t*>(logits);
-    uint16_t* dx = static_cast<uint16_t*>(dlogits);
-    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int64_t segs = ceil_div(v, flp::kBwdSegCols);
     int64_t items;
     if (__builtin_mul_overflow(n, segs, &items)) return fail(FLP_EINVAL, "n * segments overflows");
+    const BwdArgs a{logits, n, v, ld, targets, ignore_index, active_mask, inv_temperature, lse,
+                    lse_lo, grad, dlogits, ld_out, segs, reinterpret_cast<cudaStream_t>(stream),
+                    rows_aligned16(logits, ld, dtype), rows_aligned16(dlogits, ld_out, dtype),
+                    in_place};
     const int grid = grid_for(items);
-    const bool vin = aligned16(x) && ld % 8 == 0;
-    const bool vout = aligned16(dx) && ld_out % 8 == 0;
-#define FLP_BWD(VI, VO, IP)                                                                   \
-    flp::k_logp_bwd<VI, VO, IP><<<grid, flp::kBwdThreads, 0, s>>>(x, n, v, ld, targets,      \
-                                                                  ignore_index, lse, lse_lo, grad, dx, \
-                                                                  ld_out, segs)
-    if (in_place) {
-        if (vin) FLP_BWD(true, true, true);
-        else FLP_BWD(false, false, true);
-    } else if (vin && vout) FLP_BWD(true, true, false);
-    else if (vin) FLP_BWD(true, false, false);
-    else if (vout) FLP_BWD(false, true, false);
-    else FLP_BWD(false, false, false);
-#undef FLP_BWD
+    if (dtype == FLP_DTYPE_BF16) launch_backward_d<flp::Dt::BF16>(a, grid);
+    else if (dtype == FLP_DTYPE_F16) launch_backward_d<flp::Dt::F16>(a, grid);
+    else launch_backward_d<flp::Dt::F32>(a, grid);
     return check_launch("backward");
 }
 
-flp_status logp_shard_partials(const void* shard_logits, int64_t n, int64_t ld_shard,
-                               int64_t vocab_start, int64_t real_width, int64_t v_total,
-                               const int64_t* targets, float* part_max, float* part_sum,
-                               float* sel, flp_stream_t stream) {
+flp_status fused_logp_backward(const void* logits, int64_t n, int64_t v, int64_t ld,
+                               const int64_t* targets, int64_t ignore_index, const float* lse,
+                               const float* lse_lo, const float* grad, void* dlogits,
+                               int64_t ld_out, flp_stream_t stream) {
+    return fused_logp_backward_ex(logits, FLP_DTYPE_BF16, n, v, ld, targets, ignore_index, nullptr,
+                                  1.f, lse, lse_lo, grad, dlogits, ld_out, stream);
+}
+
+flp_status logp_shard_partials_ex(const void* shard_logits, int dtype, int64_t n, int64_t ld_shard,
+                                  int64_t vocab_start, int64_t real_width, int64_t v_total,
+                                  float inv_temperature, const int64_t* targets, float* part_max,
+                                  float* part_sum, float* sel, flp_stream_t stream) {
+    flp_status st;
+    if ((st = check_dtype(dtype)) != FLP_OK) return st;
+    if ((st = check_scale(inv_temperature)) != FLP_OK) return st;
     if (n < 0) return fail(FLP_EINVAL, "n must be >= 0 (got %lld)", (long long)n);
     if (v_total < 1) return fail(FLP_EINVAL, "v_total must be >= 1");
     if (real_width < 1) return fail(FLP_EINVAL, "real_width must be >= 1");
     if (vocab_start < 0 || vocab_start + real_width > v_total)
         return fail(FLP_EINVAL, "shard [%lld, %lld) is outside the vocabulary [0, %lld)",
-                    (long long)vocab_start, (long long)(vocab_start + real_width),
-                    (long long)v_total);
+                    (long long)vocab_start, (long long)(vocab_start + real_width), (long long)v_total);
     if (ld_shard < real_width) return fail(FLP_EINVAL, "ld_shard must be >= real_width");
     const int64_t W = tile_width(v_total);
     if (vocab_start % W != 0)
@@ -244,42 +391,48 @@ flp_status logp_shard_partials(const void* shard_logits, int64_t n, int64_t ld_s
                     "does not end the vocabulary", (long long)real_width, (long long)W);
     if (n == 0) return ok();
     int64_t bytes;
-    if (!span_bytes(n, real_width, ld_shard, 2, &bytes))
+    if (!span_bytes(n, real_width, ld_shard, elem_bytes(dtype), &bytes))
         return fail(FLP_EINVAL, "shard extent overflows int64");
     const void* ptrs[] = {shard_logits, targets, part_max, part_sum, sel};
     const char* names[] = {"shard_logits", "targets", "part_max", "part_sum", "sel"};
     int dev;
-    flp_status st = common_device(5, ptrs, names, &dev);
-    if (st != FLP_OK) return st;
+    if ((st = common_device(5, ptrs, names, nullptr, &dev)) != FLP_OK) return st;
     DeviceGuard guard;
     if ((st = guard.enter(dev)) != FLP_OK) return st;
 
-    const int tile0 = (int)(vocab_start / W);
-    const int ntile = (int)ceil_div(real_width, W);
-    const uint16_t* xs = static_cast<const uint16_t*>(shard_logits);
-    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int grid = grid_for(n);
-    if (aligned16(xs) && ld_shard % 8 == 0)
-        flp::k_logp_partials<true><<<grid, ntile * flp::kWarp, 0, s>>>(
-            xs, n, ld_shard, real_width, W, tile0, vocab_start, targets, part_max, part_sum, sel);
-    else
-        flp::k_logp_partials<false><<<grid, ntile * flp::kWarp, 0, s>>>(
-            xs, n, ld_shard, real_width, W, tile0, vocab_start, targets, part_max, part_sum, sel);
+    const PartArgs a{shard_logits, n, ld_shard, real_width, W, (int)(vocab_start / W),
+                     (int)ceil_div(real_width, W), vocab_start, targets, make_scale(inv_temperature),
+                     part_max, part_sum, sel, reinterpret_cast<cudaStream_t>(stream),
+                     rows_aligned16(shard_logits, ld_shard, dtype)};
+    if (dtype == FLP_DTYPE_BF16) launch_partials_d<flp::Dt::BF16>(a);
+    else if (dtype == FLP_DTYPE_F16) launch_partials_d<flp::Dt::F16>(a);
+    else launch_partials_d<flp::Dt::F32>(a);
     return check_launch("shard partials");
 }
 
-flp_status logp_merge_partials(const float* part_max, const float* part_sum, const float* sel,
-                               const int64_t* targets, int64_t ignore_index, int64_t n,
-                               int64_t v_total, float* logp, float* lse, float* lse_lo,
-                               flp_stream_t stream) {
+flp_status logp_shard_partials(const void* shard_logits, int64_t n, int64_t ld_shard,
+                               int64_t vocab_start, int64_t real_width, int64_t v_total,
+                               const int64_t* targets, float* part_max, float* part_sum,
+                               float* sel, flp_stream_t stream) {
+    return logp_shard_partials_ex(shard_logits, FLP_DTYPE_BF16, n, ld_shard, vocab_start,
+                                  real_width, v_total, 1.f, targets, part_max, part_sum, sel, stream);
+}
+
+flp_status logp_merge_partials_ex(const float* part_max, const float* part_sum, const float* sel,
+                                  const int64_t* targets, int64_t ignore_index,
+                                  const uint8_t* active_mask, int64_t n, int64_t v_total,
+                                  float inv_temperature, float* logp, float* lse, float* lse_lo,
+                                  flp_stream_t stream) {
+    flp_status st;
+    if ((st = check_scale(inv_temperature)) != FLP_OK) return st;
     if (n < 0) return fail(FLP_EINVAL, "n must be >= 0 (got %lld)", (long long)n);
     if (v_total < 1) return fail(FLP_EINVAL, "v_total must be >= 1");
     if (n == 0) return ok();
-    const void* ptrs[] = {part_max, part_sum, sel, targets, logp, lse, lse_lo ? lse_lo : lse};
-    const char* names[] = {"part_max", "part_sum", "sel", "targets", "logp", "lse", "lse_lo"};
+    const void* ptrs[] = {part_max, part_sum, sel, targets, logp, lse, lse_lo, active_mask};
+    const char* names[] = {"part_max", "part_sum", "sel", "targets", "logp", "lse", "lse_lo", "active_mask"};
+    const bool optional[] = {false, false, false, false, false, false, true, true};
     int dev;
-    flp_status st = common_device(7, ptrs, names, &dev);
-    if (st != FLP_OK) return st;
+    if ((st = common_device(8, ptrs, names, optional, &dev)) != FLP_OK) return st;
     DeviceGuard guard;
     if ((st = guard.enter(dev)) != FLP_OK) return st;
 
@@ -287,10 +440,18 @@ flp_status logp_merge_partials(const float* part_max, const float* part_sum, con
     const int n_tiles = (int)ceil_div(v_total, W);
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int64_t rows_per_block = 256 / 16;
-    const int grid = grid_for(ceil_div(n, rows_per_block));
-    flp::k_logp_merge<<<grid, 256, 0, s>>>(part_max, part_sum, sel, targets, ignore_index, n,
-                                           v_total, n_tiles, logp, lse, lse_lo);
+    flp::k_logp_merge<<<grid_for(ceil_div(n, rows_per_block)), 256, 0, s>>>(
+        part_max, part_sum, sel, targets, ignore_index, active_mask, n, v_total, n_tiles,
+        inv_temperature, logp, lse, lse_lo);
     return check_launch("merge");
+}
+
+flp_status logp_merge_partials(const float* part_max, const float* part_sum, const float* sel,
+                               const int64_t* targets, int64_t ignore_index, int64_t n,
+                               int64_t v_total, float* logp, float* lse, float* lse_lo,
+                               flp_stream_t stream) {
+    return logp_merge_partials_ex(part_max, part_sum, sel, targets, ignore_index, nullptr, n,
+                                  v_total, 1.f, logp, lse, lse_lo, stream);
 }
 
 flp_status flp_device_error(int device, int* code) {

@@ -1,46 +1,46 @@
 // Device code of the selected-token log-probability path for sm_103a.
 //
 // Forward (RL-Kernel issue #241 "TP-aware deterministic logprob", Background
-// and PR 3 bullets): LSE_t = log sum_v exp(x[t, v]) with FP32 accumulation,
-// logp_t = x[t, y_t] - LSE_t.  Every row is cut into 16 fixed vocabulary tiles
-// of width W = 8 * ceil(V / 128); one warp reduces one tile: each lane keeps
-// an online (max, sumexp) pair over its fixed share of the tile, the warp
-// merges the 32 pairs with a fixed xor butterfly, and a half warp merges the
-// 16 tile partials with a fixed pairwise tree in tile-index order (RL-Kernel
-// PR #314, Tensor Parallel section: fixed tiles, one fixed merge order).
-// Nothing in this order depends on N, on the row's position or on the grid, so
-// every row's bits are batch-invariant, and a vocab shard that reduces its own
-// tiles with the same functions reproduces the same partials bit for bit.
+// and PR 3 bullets): LSE_t = log sum_v exp(s x[t, v]) with FP32 accumulation,
+// logp_t = s x[t, y_t] - LSE_t, where s = 1/T is the inverse temperature
+// (s = 1 unless rollout logprobs at a temperature are asked for, PR #495
+// provider experiment).  Every row is cut into 16 fixed vocabulary tiles of
+// width W = 8 * ceil(V / 128); one warp reduces one tile: each lane keeps an
+// online (max, sumexp) pair over its fixed share of the tile, the warp merges
+// the 32 pairs with a fixed xor butterfly, and a half warp merges the 16 tile
+// partials with a fixed pairwise tree in tile-index order (RL-Kernel PR #314,
+// Tensor Parallel section: fixed tiles, one fixed merge order).  Nothing in
+// this order depends on N, on the row's position or on the grid, so every
+// row's bits are batch-invariant, and a vocab shard that reduces its own tiles
+// with the same functions reproduces the same partials bit for bit.
 //
 // Backward (RL-Kernel PR #495 "zero-workspace fused backward", Summary item
-// 2): dlogits = g * (onehot - exp(x - LSE)) from the saved LSE, one read and
-// one write per logit, elementwise.
+// 2): dlogits = s g (onehot - exp(s x - LSE)) from the saved LSE, one read
+// and one write per logit, elementwise, written in the logits' dtype.
 //
-// Arithmetic on pairs uses the packed binary32 instructions of sm_100+
-// (add/mul/fma .f32x2, each lane an ordinary IEEE round-to-nearest operation)
-// and the packed BF16 maximum; every rounding is explicit, so the full and the
-// shard kernels cannot differ by a contraction.  All index arithmetic is
-// 64-bit.  The only waits are bounded waits of a warp on its own bulk copies.
+// Logits may be BF16, FP16 or FP32 (PR #495 Tests: FP32/BF16/FP16).  A
+// "unit" is 8 consecutive elements of a row (16 bytes for 16-bit types, 32 for
+// FP32); lane j of a warp owns units j, j + 32, ... of its tile.  Rows may be
+// excluded by an explicit active mask (PR #314, MaskMode).  All index
+// arithmetic is 64-bit except tile-local indices of the bulk forward.  The
+// only waits are bounded waits of a warp on its own bulk copies.
 #pragma once
 
-#include <cuda_bf16.h>
-#include <cuda_runtime.h>
-#include <stdint.h>
+#include "logp_prims.cuh"
 
 namespace flp {
 
-constexpr int kTiles = 16;                  // vocabulary tiles per row (K)
+enum class Dt : int { BF16 = 0, F16 = 1, F32 = 2 };
+
+constexpr int kTiles = 16;                   // vocabulary tiles per row (K)
 constexpr int kWarp = 32;
-constexpr int kFwdThreads = kTiles * kWarp; // one warp per tile
-constexpr int kGroup = 4;                   // 16-byte vectors per lane per online step
-constexpr int kGroupVecs = kWarp * kGroup;  // vectors of a tile per group (128)
-constexpr int kStages = 3;                  // bulk-copy ring depth per warp
-constexpr int kStageBytes = kGroupVecs * 16;
-constexpr int kFwdSmemBytes = kTiles * kStages * kStageBytes + kTiles * kStages * 8;
+constexpr int kFwdThreads = kTiles * kWarp;  // one warp per tile
+constexpr int kGroup = 4;                    // units per lane per online step
+constexpr int kGroupUnits = kWarp * kGroup;  // units of a tile per group (128)
+constexpr int kStages = 3;                   // bulk-copy ring depth per warp
 constexpr int kBwdThreads = 256;
-constexpr int kBwdVecPerThread = 4;
-constexpr int64_t kBwdSegCols = (int64_t)kBwdThreads * kBwdVecPerThread * 8;
-constexpr uint32_t kNegInf2 = 0xff80ff80u;  // two BF16 -inf
+constexpr int kBwdUnitsPerThread = 4;
+constexpr int64_t kBwdSegCols = (int64_t)kBwdThreads * kBwdUnitsPerThread * 8;
 // Bounded waits give up after this many SM cycles (about 2 s at 2 GHz).
 constexpr long long kWaitLimitCycles = 4000000000LL;
 
@@ -57,172 +57,155 @@ constexpr float kLog2e = (float)(1.0 / kLn2);
 __device__ int g_device_error;
 
 struct MS {
-    float m;  // running maximum (always the value of an input element, or -inf)
-    float s;  // sum of exp(x - m) over the elements seen
+    float m;  // running maximum of the raw logits (an input element, or -inf)
+    float s;  // sum of exp(s (x - m)) over the elements seen
 };
 
-typedef unsigned long long u64;
+// Inverse temperature s and s log2(e) as a two-float (hi + lo).
+struct Scale {
+    float s, hi, lo;
+};
 
-// ---------------------------------------------------------------- packed arithmetic
+// ---------------------------------------------------------------- units by dtype
 
-__device__ __forceinline__ u64 f2(float lo, float hi) {
-    u64 r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ void f2_split(u64 v, float& lo, float& hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ u64 f2_add(u64 a, u64 b) {
-    u64 r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ u64 f2_mul(u64 a, u64 b) {
-    u64 r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ __forceinline__ u64 f2_fma(u64 a, u64 b, u64 c) {
-    u64 r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
-__device__ __forceinline__ uint32_t bf2_max(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-    return r;
-}
+template <Dt D>
+struct Unit {
+    static constexpr int kWords = (D == Dt::F32) ? 8 : 4;
+    static constexpr int kBytes = kWords * 4;
+    static constexpr int kElemBytes = (D == Dt::F32) ? 4 : 2;
+    static constexpr uint32_t kNegInfBits = (D == Dt::BF16) ? 0xff80u : (D == Dt::F16) ? 0xfc00u : 0xff800000u;
+    uint32_t w[kWords];
+};
 
-// A BF16 value is the top half of a binary32: widening is a shift or a mask.
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-__device__ __forceinline__ u64 bf2_widen(uint32_t w) { return f2(bf_lo(w), bf_hi(w)); }
-// (x_lo - b, x_hi - b) for the two BF16 values of w: each widened exactly and
-// rounded once (mixed-precision subtract, a BF16 operand and a binary32 one).
-__device__ __forceinline__ u64 bf2_sub(uint32_t w, float b) {
-    float lo, hi;
-    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
-        "sub.rn.f32.bf16 %0, l, %3;\n\tsub.rn.f32.bf16 %1, h, %3;\n\t}"
-        : "=f"(lo), "=f"(hi)
-        : "r"(w), "f"(b));
-    return f2(lo, hi);
-}
-__device__ __forceinline__ uint32_t ldg_u16(const uint16_t* p) {
-    return (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(p));
-}
-__device__ __forceinline__ float bf_scalar(const uint16_t* p) { return __uint_as_float(ldg_u16(p) << 16); }
+template <Dt D>
+constexpr int kStageBytes = kGroupUnits * Unit<D>::kBytes;
+template <Dt D>
+constexpr int kFwdSmemBytes = kTiles * kStages * kStageBytes<D> + kTiles * kStages * 8;
+template <Dt D>
+constexpr int kFwdMinBlocks = (D == Dt::F32) ? 1 : 2;
 
-// Two binary32 -> packed BF16 pair, round to nearest even (lo in bits 0..15).
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
+template <Dt D>
+__device__ __forceinline__ uint32_t elem_bits(const void* base, int64_t i) {
+    if constexpr (D == Dt::F32) return __ldg(reinterpret_cast<const unsigned int*>(base) + i);
+    else return (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(base) + i);
+}
+template <Dt D>
+__device__ __forceinline__ uint32_t elem_bits_plain(const void* base, int64_t i) {
+    if constexpr (D == Dt::F32) return reinterpret_cast<const unsigned int*>(base)[i];
+    else return (uint32_t)reinterpret_cast<const unsigned short*>(base)[i];
+}
+template <Dt D>
+__device__ __forceinline__ float bits_value(uint32_t b) {
+    if constexpr (D == Dt::BF16) return __uint_as_float(b << 16);
+    else if constexpr (D == Dt::F16) return __half2float(__ushort_as_half((unsigned short)b));
+    else return __uint_as_float(b);
+}
+template <Dt D>
+__device__ __forceinline__ float elem_value(const void* base, int64_t i) {
+    return bits_value<D>(elem_bits<D>(base, i));
 }
 
-// 2^a on the special-function unit; results below 2^-126 flush to zero.
-__device__ __forceinline__ float ex2_ftz(float a) {
-    float r;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(a));
-    return r;
+template <Dt D>
+__device__ __forceinline__ void unit_fill_neg_inf(Unit<D>& u) {
+    constexpr uint32_t w = (D == Dt::F32) ? Unit<D>::kNegInfBits : (Unit<D>::kNegInfBits * 0x10001u);
+#pragma unroll
+    for (int k = 0; k < Unit<D>::kWords; ++k) u.w[k] = w;
 }
 
-// ---------------------------------------------------------------- memory access
-
-__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
-    uint4 r;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-        : "l"(p));
-    return r;
-}
-__device__ __forceinline__ uint4 ld_v4(const void* p) {
-    uint4 r;
-    asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p)
-                 : "memory");
-    return r;
-}
-__device__ __forceinline__ void st_cs_v4(void* p, uint4 v) {
-    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};"
-                 :
-                 : "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                 : "memory");
-}
-__device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
-    uint4 r;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "r"(addr)
-                 : "memory");
-    return r;
-}
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-// mbarrier and bulk-copy (TMA, non-tensor) primitives.
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void fence_mbar_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-        "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
-// One probe of phase `parity` of an mbarrier.
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return done != 0;
-}
-// Wait for phase `parity` of an mbarrier, giving up after `limit` cycles.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long limit) {
-    if (mbar_try(bar, parity)) return true;
-    const long long t0 = clock64();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try(bar, parity)) return true;
-        if ((it & 31u) == 0 && clock64() - t0 > limit) return false;
+// The unit of the 8 columns [col, col + 8) of a tile; columns >= width read
+// as -inf (padded columns are masked, PR #314 ReductionSpec).  The vector path
+// needs a 16-byte aligned tile; both paths give the same words.
+template <Dt D, bool kVec>
+__device__ __forceinline__ void unit_load(const void* __restrict__ tile, int64_t col, int64_t width,
+                                          Unit<D>& u) {
+    constexpr uint32_t NI = Unit<D>::kNegInfBits;
+    if (kVec && col + 8 <= width) {
+        const char* p = reinterpret_cast<const char*>(tile) + col * Unit<D>::kElemBytes;
+        const uint4 a = ld_nc_v4(p);
+        u.w[0] = a.x; u.w[1] = a.y; u.w[2] = a.z; u.w[3] = a.w;
+        if constexpr (D == Dt::F32) {
+            const uint4 b = ld_nc_v4(p + 16);
+            u.w[4] = b.x; u.w[5] = b.y; u.w[6] = b.z; u.w[7] = b.w;
+        }
+    } else if constexpr (D == Dt::F32) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) u.w[j] = (col + j < width) ? elem_bits<D>(tile, col + j) : NI;
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t lo = (col + 2 * k < width) ? elem_bits<D>(tile, col + 2 * k) : NI;
+            const uint32_t hi = (col + 2 * k + 1 < width) ? elem_bits<D>(tile, col + 2 * k + 1) : NI;
+            u.w[k] = lo | (hi << 16);
+        }
     }
+}
+
+template <Dt D>
+__device__ __forceinline__ void unit_load_shared(uint32_t addr, Unit<D>& u) {
+    const uint4 a = lds_v4(addr);
+    u.w[0] = a.x; u.w[1] = a.y; u.w[2] = a.z; u.w[3] = a.w;
+    if constexpr (D == Dt::F32) {
+        const uint4 b = lds_v4(addr + 16);
+        u.w[4] = b.x; u.w[5] = b.y; u.w[6] = b.z; u.w[7] = b.w;
+    }
+}
+
+// max(m, all elements of the group's units), by packed 16-bit maxima.
+template <Dt D>
+__device__ __forceinline__ float group_max(const Unit<D> (&q)[kGroup], float m) {
+    if constexpr (D == Dt::F32) {
+        float r = m;
+#pragma unroll
+        for (int u = 0; u < kGroup; ++u)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) r = fmaxf(r, __uint_as_float(q[u].w[j]));
+        return r;
+    } else {
+        auto mx = [](uint32_t a, uint32_t b) { return D == Dt::BF16 ? bf2_max(a, b) : h2_max(a, b); };
+        uint32_t w = mx(mx(q[0].w[0], q[0].w[1]), mx(q[0].w[2], q[0].w[3]));
+#pragma unroll
+        for (int u = 1; u < kGroup; ++u) w = mx(w, mx(mx(q[u].w[0], q[u].w[1]), mx(q[u].w[2], q[u].w[3])));
+        const float lo = (D == Dt::BF16) ? bf_lo(w) : h_lo(w);
+        const float hi = (D == Dt::BF16) ? bf_hi(w) : h_hi(w);
+        return fmaxf(m, fmaxf(lo, hi));
+    }
+}
+
+// (x_{2k} - b, x_{2k+1} - b) of a unit, each rounded once.
+template <Dt D>
+__device__ __forceinline__ u64 pair_sub(const Unit<D>& u, int k, float b) {
+    if constexpr (D == Dt::BF16) return bf2_sub(u.w[k], b);
+    else if constexpr (D == Dt::F16) return h2_sub(u.w[k], b);
+    else return f2_add(f2(__uint_as_float(u.w[2 * k]), __uint_as_float(u.w[2 * k + 1])), f2(-b, -b));
+}
+
+// t log2(e) s: one product when s = 1, else against the two-float s log2(e).
+template <bool kScaled>
+__device__ __forceinline__ u64 to_log2(u64 t, const Scale& sc) {
+    if constexpr (kScaled) return f2_fma(t, f2(sc.hi, sc.hi), f2_mul(t, f2(sc.lo, sc.lo)));
+    else return f2_mul(t, f2(kLog2e, kLog2e));
+}
+template <bool kScaled>
+__device__ __forceinline__ float to_log2_1(float t, const Scale& sc) {
+    if constexpr (kScaled) return __fmaf_rn(t, sc.hi, __fmul_rn(t, sc.lo));
+    else return __fmul_rn(t, kLog2e);
 }
 
 // ---------------------------------------------------------------- forward reduction
 
-// One online step of a lane over kGroup vectors of 8 BF16 (q[u] = the four
-// 32-bit words of vector u; with kFull all vectors hold data, otherwise
-// vectors [0, nvalid) do and the others are -inf): gm = max(m, elements) by
-// packed BF16 maxima; each element's term 2^((x - gm) log2 e) on the
-// special-function unit (x - gm is exact: both are BF16 values); the terms
-// summed by a fixed pairwise tree (word pairs, then vectors:
-// ((w0 + w1) + (w2 + w3)) lane-wise, vectors ((v0 + v1) + (v2 + v3)), then the
-// even and odd lanes); s = s * exp(m - gm) + group sum.
-template <bool kFull>
-__device__ __forceinline__ void group_update(const uint32_t (&q)[kGroup][4], int nvalid, float& m,
-                                             float& s) {
-    uint32_t w = bf2_max(bf2_max(q[0][0], q[0][1]), bf2_max(q[0][2], q[0][3]));
-#pragma unroll
-    for (int u = 1; u < kGroup; ++u)
-        w = bf2_max(w, bf2_max(bf2_max(q[u][0], q[u][1]), bf2_max(q[u][2], q[u][3])));
-    const float gm = fmaxf(m, fmaxf(bf_lo(w), bf_hi(w)));
+// One online step of a lane over kGroup units (with kFull all hold data,
+// otherwise units [0, nvalid) do and the others are -inf).  Maxima are kept in
+// units of the raw logits x; the scale enters only the exponent:
+// gm = max(m, elements); each element's term 2^((x - gm) s log2 e) on the
+// special-function unit (x - gm is exact for 16-bit inputs); the terms summed
+// by a fixed pairwise tree (element pairs ((p0 + p1) + (p2 + p3)) lane-wise,
+// units ((u0 + u1) + (u2 + u3)), then the even and odd lanes);
+// s_acc = s_acc * exp(s (m - gm)) + group sum.
+template <Dt D, bool kFull, bool kScaled>
+__device__ __forceinline__ void group_update(const Unit<D> (&q)[kGroup], int nvalid, float& m,
+                                             float& s, const Scale& sc) {
+    const float gm = group_max<D>(q, m);
     if (gm == -INFINITY) return;  // nothing finite seen yet: (m, s) stays (-inf, 0)
-    const u64 l2e = f2(kLog2e, kLog2e);
     u64 vsum[kGroup];
 #pragma unroll
     for (int u = 0; u < kGroup; ++u) {
@@ -231,7 +214,7 @@ __device__ __forceinline__ void group_update(const uint32_t (&q)[kGroup][4], int
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 float a0, a1;
-                f2_split(f2_mul(bf2_sub(q[u][k], gm), l2e), a0, a1);
+                f2_split(to_log2<kScaled>(pair_sub<D>(q[u], k, gm), sc), a0, a1);
                 p[k] = f2(ex2_ftz(a0), ex2_ftz(a1));
             }
             vsum[u] = f2_add(f2_add(p[0], p[1]), f2_add(p[2], p[3]));
@@ -239,67 +222,49 @@ __device__ __forceinline__ void group_update(const uint32_t (&q)[kGroup][4], int
             vsum[u] = 0ull;
         }
     }
-    static_assert(kGroup == 4, "the group tree is written for four vectors");
+    static_assert(kGroup == 4, "the group tree is written for four units");
     float e, o;
     f2_split(f2_add(f2_add(vsum[0], vsum[1]), f2_add(vsum[2], vsum[3])), e, o);
     const float gs = __fadd_rn(e, o);
-    const float r = (m == gm) ? 1.f : ex2_ftz(__fmul_rn(__fsub_rn(m, gm), kLog2e));
+    const float r = (m == gm) ? 1.f : ex2_ftz(to_log2_1<kScaled>(__fsub_rn(m, gm), sc));
     s = __fmaf_rn(s, r, gs);
     m = gm;
 }
 
-// The four words of the 8 columns [col, col + 8) of a tile; columns >= width
-// read as -inf (padded columns are masked, PR #314 ReductionSpec).  The vector
-// path needs a 16-byte aligned tile; both paths give the same words.
-template <bool kVec>
-__device__ __forceinline__ void load_words(const uint16_t* __restrict__ tile, int64_t col,
-                                           int64_t width, uint32_t (&w)[4]) {
-    if (kVec && col + 8 <= width) {
-        const uint4 q = ld_nc_v4(tile + col);
-        w[0] = q.x; w[1] = q.y; w[2] = q.z; w[3] = q.w;
-    } else {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const uint32_t lo = (col + 2 * k < width) ? ldg_u16(tile + col + 2 * k) : 0xff80u;
-            const uint32_t hi = (col + 2 * k + 1 < width) ? ldg_u16(tile + col + 2 * k + 1) : 0xff80u;
-            w[k] = lo | (hi << 16);
-        }
-    }
-}
-
-// Online (max, sumexp) of one lane over a tile of `width` columns: 16-byte
-// vector j of the tile belongs to lane j mod 32, and the lane visits its
-// vectors in increasing j, kGroup at a time (vectors v0 + 32u + lane of group
-// v0 / 128).  Plain loads; the bulk-copy forward feeds group_update with the
-// same words in the same order.
-template <bool kVec>
-__device__ __forceinline__ MS tile_scan(const uint16_t* __restrict__ tile, int64_t width,
-                                        int lane) {
-    const int64_t nvec = (width + 7) >> 3;
+// Online (max, sumexp) of one lane over a tile of `width` columns with plain
+// loads: unit j of the tile belongs to lane j mod 32, visited in increasing j,
+// kGroup at a time (units v0 + 32u + lane of group v0 / 128).  The bulk-copy
+// forward feeds group_update with the same words in the same order.
+template <Dt D, bool kVec, bool kScaled>
+__device__ __forceinline__ MS tile_scan(const void* __restrict__ tile, int64_t width, int lane,
+                                        const Scale& sc) {
+    const int64_t nunit = (width + 7) >> 3;
     float m = -INFINITY, s = 0.f;
-    for (int64_t v0 = 0; v0 < nvec; v0 += kGroupVecs) {
-        uint32_t q[kGroup][4];
+    for (int64_t v0 = 0; v0 < nunit; v0 += kGroupUnits) {
+        Unit<D> q[kGroup];
         int nvalid = 0;
 #pragma unroll
         for (int u = 0; u < kGroup; ++u) {
             const int64_t j = v0 + (int64_t)kWarp * u + lane;
-            if (j < nvec) {
-                load_words<kVec>(tile, j * 8, width, q[u]);
+            if (j < nunit) {
+                unit_load<D, kVec>(tile, j * 8, width, q[u]);
                 nvalid = u + 1;
             } else {
-                q[u][0] = q[u][1] = q[u][2] = q[u][3] = kNegInf2;
+                unit_fill_neg_inf<D>(q[u]);
             }
         }
-        if (nvalid == kGroup) group_update<true>(q, nvalid, m, s);
-        else group_update<false>(q, nvalid, m, s);
+        if (nvalid == kGroup) group_update<D, true, kScaled>(q, nvalid, m, s, sc);
+        else group_update<D, false, kScaled>(q, nvalid, m, s, sc);
     }
     return MS{m, s};
 }
 
 // Merge of two (max, sumexp) pairs: the pair holding the larger max keeps its
-// sum, the other is scaled by exp(m_small - M).  Symmetric in its arguments
-// (IEEE addition commutes), so both lanes of a butterfly get the same bits.
-__device__ __forceinline__ MS ms_merge(MS a, MS b) {
+// sum, the other is scaled by exp(s (m_small - M)).  Symmetric in its
+// arguments (IEEE addition commutes), so both lanes of a butterfly get the
+// same bits.
+template <bool kScaled>
+__device__ __forceinline__ MS ms_merge(MS a, MS b, const Scale& sc) {
     const bool a_big = a.m >= b.m;
     const float M = a_big ? a.m : b.m;
     const float m_small = a_big ? b.m : a.m;
@@ -308,82 +273,86 @@ __device__ __forceinline__ MS ms_merge(MS a, MS b) {
     float r;
     if (m_small == -INFINITY) r = 0.f;
     else if (m_small == M) r = 1.f;
-    else r = ex2_ftz(__fmul_rn(__fsub_rn(m_small, M), kLog2e));
+    else r = ex2_ftz(to_log2_1<kScaled>(__fsub_rn(m_small, M), sc));
     return MS{M, __fmaf_rn(s_small, r, s_big)};
 }
 
 // Fixed xor butterfly over the 32 lanes of a warp (offsets 16, 8, 4, 2, 1);
 // every lane ends with the same pair.
-__device__ __forceinline__ MS warp_merge(MS p) {
+template <bool kScaled>
+__device__ __forceinline__ MS warp_merge(MS p, const Scale& sc) {
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) {
         MS o;
         o.m = __shfl_xor_sync(0xffffffffu, p.m, off);
         o.s = __shfl_xor_sync(0xffffffffu, p.s, off);
-        p = ms_merge(p, o);
+        p = ms_merge<kScaled>(p, o, sc);
     }
     return p;
 }
 
 // Merge of the 16 tile partials of one row held by a 16-lane half warp
 // (lane k of the half holds tile k; tiles beyond the vocabulary hold the
-// identity (-inf, 0)).  M = max m_k; S = sum_k s_k exp(m_k - M) summed as a
-// fixed pairwise tree in tile-index order (issue #241 PR 3 merge formula).
-// m_k - M is exact; exp is the accurate library expf.  All 32 lanes call this
-// together; every lane gets (M, S) of its half.
-__device__ __forceinline__ MS tile_fold16(MS p) {
+// identity (-inf, 0)).  M = max m_k; S = sum_k s_k exp(s (m_k - M)) summed as
+// a fixed pairwise tree in tile-index order (issue #241 PR 3 merge formula).
+// m_k - M is exact for 16-bit inputs; exp is the accurate library expf.  All
+// 32 lanes call this together; every lane gets (M, S) of its half.
+__device__ __forceinline__ MS tile_fold16(MS p, float s) {
     float M = p.m;
 #pragma unroll
     for (int off = 8; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off, 16));
-    float term = (p.m == -INFINITY) ? 0.f : __fmul_rn(p.s, expf(__fsub_rn(p.m, M)));
+    float term = (p.m == -INFINITY) ? 0.f : __fmul_rn(p.s, expf(__fmul_rn(s, __fsub_rn(p.m, M))));
 #pragma unroll
     for (int off = 1; off <= 8; off <<= 1)
         term = __fadd_rn(term, __shfl_xor_sync(0xffffffffu, term, off, 16));
     return MS{M, term};
 }
 
-// LSE = M + log S and logp = x_y - LSE, the log and the subtractions carried
-// in double and each output rounded once to binary32 (the "downcast at final
-// write" of issue #241 Goal).  lse_lo, when given, receives the binary32
+// LSE = s M + log S and logp = s x_y - LSE, carried in double (s M and s x_y
+// are exact there) and each output rounded once to binary32 (the "downcast at
+// final write" of issue #241 Goal).  lse_lo, when given, receives the binary32
 // rounding residual of the LSE (LSE - lse), so that lse + lse_lo carries the
 // LSE to about 2^-48 relative for the backward.
-__device__ __forceinline__ void finalize_row(MS f, bool active, float x_y, float* logp_out,
+__device__ __forceinline__ void finalize_row(MS f, bool active, float x_y, float s, float* logp_out,
                                              float* lse_out, float* lse_lo_out) {
-    const double l = (f.m == -INFINITY) ? -(double)INFINITY : (double)f.m + log((double)f.s);
+    const double l = (f.m == -INFINITY) ? -(double)INFINITY
+                                        : (double)s * (double)f.m + log((double)f.s);
     const float lf = __double2float_rn(l);
     *lse_out = lf;
     if (lse_lo_out) *lse_lo_out = isfinite(lf) ? __double2float_rn(l - (double)lf) : 0.f;
-    *logp_out = active ? __double2float_rn((double)x_y - l) : 0.f;
+    *logp_out = active ? __double2float_rn((double)s * (double)x_y - l) : 0.f;
 }
 
-__device__ __forceinline__ bool row_active(int64_t y, int64_t v, int64_t ignore_index) {
-    return y >= 0 && y < v && y != ignore_index;
+__device__ __forceinline__ bool row_active(const uint8_t* mask, int64_t t, int64_t y, int64_t v,
+                                           int64_t ignore_index) {
+    return (mask == nullptr || __ldg(mask + t) != 0) && y >= 0 && y < v && y != ignore_index;
 }
 
 // ---------------------------------------------------------------- forward kernels
 
 // Forward with plain loads (any alignment): one CTA of 16 warps per row, warp
 // k reduces tile k.
-template <bool kVec>
+template <Dt D, bool kScaled>
 __global__ void __launch_bounds__(kFwdThreads)
-k_logp_fwd(const uint16_t* __restrict__ x, int64_t n, int64_t v, int64_t ld, int64_t W,
-           const int64_t* __restrict__ y, int64_t ignore_index, float* __restrict__ logp,
-           float* __restrict__ lse, float* __restrict__ lse_lo) {
+k_logp_fwd(const void* __restrict__ x, int64_t n, int64_t v, int64_t ld, int64_t W,
+           const int64_t* __restrict__ y, int64_t ignore_index, const uint8_t* __restrict__ mask,
+           Scale sc, float* __restrict__ logp, float* __restrict__ lse, float* __restrict__ lse_lo) {
     __shared__ float sh_m[kTiles], sh_s[kTiles];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int EB = Unit<D>::kElemBytes;
     for (int64_t t = blockIdx.x; t < n; t += gridDim.x) {
-        const uint16_t* __restrict__ xr = x + t * ld;
+        const char* xr = reinterpret_cast<const char*>(x) + t * ld * EB;
         bool act = false;
         float x_y = 0.f;
         if (threadIdx.x == 0) {
             const int64_t yt = __ldg(y + t);
-            act = row_active(yt, v, ignore_index);
-            if (act) x_y = bf_scalar(xr + yt);
+            act = row_active(mask, t, yt, v, ignore_index);
+            if (act) x_y = elem_value<D>(xr, yt);
         }
         const int64_t c0 = (int64_t)warp * W;
         const int64_t width = c0 >= v ? 0 : (v - c0 < W ? v - c0 : W);
-        MS p = tile_scan<kVec>(xr + c0, width, lane);
-        p = warp_merge(p);
+        MS p = tile_scan<D, false, kScaled>(xr + c0 * EB, width, lane, sc);
+        p = warp_merge<kScaled>(p, sc);
         if (lane == 0) {
             sh_m[warp] = p.m;
             sh_s[warp] = p.s;
@@ -391,62 +360,67 @@ k_logp_fwd(const uint16_t* __restrict__ x, int64_t n, int64_t v, int64_t ld, int
         __syncthreads();
         if (warp == 0) {
             const int k = lane & 15;
-            const MS f = tile_fold16(MS{sh_m[k], sh_s[k]});
-            if (lane == 0) finalize_row(f, act, x_y, logp + t, lse + t, lse_lo ? lse_lo + t : nullptr);
+            const MS f = tile_fold16(MS{sh_m[k], sh_s[k]}, sc.s);
+            if (lane == 0)
+                finalize_row(f, act, x_y, sc.s, logp + t, lse + t, lse_lo ? lse_lo + t : nullptr);
         }
         __syncthreads();
     }
 }
 
-// Forward with bulk copies (16-byte aligned rows, ld % 8 == 0, V < 2^31).
-// Persistent CTAs of 16 warps; CTA b takes rows b, b + grid, b + 2 grid, ...
-// Each warp streams its tile of successive rows through a private ring of
-// kStages shared-memory stages (one 2 KB group each): lane 0 issues
-// cp.async.bulk for group i + kStages as soon as the warp has read group i,
-// so copies of the next row are already in flight while a row is finished.
-// The lanes read the same words, in the same order, as tile_scan would load
-// them (a ragged last vector is read from global memory), so results are
-// bitwise those of k_logp_fwd.  Tile partials go to a double-buffered shared
-// array; after one barrier per row, warp (row mod 16) merges them and writes
-// the row.  A wait that runs out sets g_device_error; the warp then stops
-// issuing copies and skips waits, and drains its copies in flight before
-// exiting.
-__global__ void __launch_bounds__(kFwdThreads, 2)
-k_logp_fwd_bulk(const uint16_t* __restrict__ x, int64_t n, int64_t v, int64_t ld, int64_t W,
-                const int64_t* __restrict__ y, int64_t ignore_index, float* __restrict__ logp,
-                float* __restrict__ lse, float* __restrict__ lse_lo) {
+// Forward with bulk copies (16-byte aligned rows whose byte stride is a
+// multiple of 16, V < 2^31).  Persistent CTAs of 16 warps; CTA b takes rows
+// b, b + grid, b + 2 grid, ...  Each warp streams its tile of successive rows
+// through a private ring of kStages shared-memory stages (one group of 128
+// units each): lane 0 issues cp.async.bulk for group i + kStages as soon as the
+// warp has read group i, so copies of the next row are already in flight while
+// a row is finished.  The lanes read the same words, in the same order, as
+// tile_scan would load them (a ragged last unit is read from global memory),
+// so results are bitwise those of k_logp_fwd.  Tile partials go to a
+// double-buffered shared array; after one barrier per row, warp (row mod 16)
+// merges them and writes the row.  A wait that runs out sets g_device_error;
+// the warp then stops issuing copies and skips waits, and drains its copies in
+// flight before exiting.
+template <Dt D, bool kScaled>
+__global__ void __launch_bounds__(kFwdThreads, kFwdMinBlocks<D>)
+k_logp_fwd_bulk(const void* __restrict__ x, int64_t n, int64_t v, int64_t ld, int64_t W,
+                const int64_t* __restrict__ y, int64_t ignore_index, const uint8_t* __restrict__ mask,
+                Scale sc, float* __restrict__ logp, float* __restrict__ lse,
+                float* __restrict__ lse_lo) {
+    constexpr int EB = Unit<D>::kElemBytes;
+    constexpr int UB = Unit<D>::kBytes;
+    constexpr int SB = kStageBytes<D>;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float sh_m[2][kTiles], sh_s[2][kTiles];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t stage0 = smem_u32(smem + warp * kStages * kStageBytes);
-    const uint32_t bar0 = smem_u32(smem + kTiles * kStages * kStageBytes) + warp * kStages * 8;
-    if (threadIdx.x < kTiles * kStages)
-        mbar_init(smem_u32(smem + kTiles * kStages * kStageBytes) + threadIdx.x * 8, 1);
+    const uint32_t stage0 = smem_u32(smem + warp * kStages * SB);
+    const uint32_t bar0 = smem_u32(smem + kTiles * kStages * SB) + warp * kStages * 8;
+    if (threadIdx.x < kTiles * kStages) mbar_init(smem_u32(smem + kTiles * kStages * SB) + threadIdx.x * 8, 1);
     fence_mbar_init();
     __syncthreads();
 
     // tile-local extents fit in 32 bits (the host routes V >= 2^31 elsewhere)
     const int64_t c0 = (int64_t)warp * W;
     const int width = (int)(c0 >= v ? 0 : (v - c0 < W ? v - c0 : W));
-    const int nfull = width >> 3, nvec = (width + 7) >> 3;
-    const int G = (nvec + kGroupVecs - 1) / kGroupVecs;          // groups per row
-    const int Gfull = nfull / kGroupVecs;                        // groups of 128 full vectors
+    const int nfull = width >> 3, nunit = (width + 7) >> 3;
+    const int G = (nunit + kGroupUnits - 1) / kGroupUnits;       // groups per row
+    const int Gfull = nfull / kGroupUnits;                       // groups of 128 full units
     const int64_t rows = (n > (int64_t)blockIdx.x) ? (n - 1 - blockIdx.x) / gridDim.x + 1 : 0;
     const int64_t jobs = rows * G;
-    const int64_t row_step = (int64_t)gridDim.x * ld;
+    const int64_t row_step = (int64_t)gridDim.x * ld * EB;      // bytes
 
-    // Issuer: group iss_g of the row at iss_row (its first element of this
-    // tile), stage iss_st.  Every lane tracks it; lane 0 issues.
-    const uint16_t* iss_row = x + (int64_t)blockIdx.x * ld + c0;
+    // Issuer: group iss_g of the row at iss_row (its first byte of this tile),
+    // stage iss_st.  Every lane tracks it; lane 0 issues.
+    const char* iss_row = reinterpret_cast<const char*>(x) + ((int64_t)blockIdx.x * ld + c0) * EB;
     int iss_g = 0, iss_st = 0;
     int64_t issued = 0;
     auto issue_next = [&]() {
         if (lane == 0) {
-            const int nv = nfull - iss_g * kGroupVecs;
-            const uint32_t bytes = nv <= 0 ? 0u : (uint32_t)((nv < kGroupVecs ? nv : kGroupVecs) * 16);
+            const int nv = nfull - iss_g * kGroupUnits;
+            const uint32_t bytes = nv <= 0 ? 0u : (uint32_t)((nv < kGroupUnits ? nv : kGroupUnits) * UB);
             const uint32_t bar = bar0 + iss_st * 8;
             mbar_arrive_expect_tx(bar, bytes);
-            if (bytes) bulk_g2s(stage0 + iss_st * kStageBytes, iss_row + iss_g * (kGroupVecs * 8), bytes, bar);
+            if (bytes) bulk_g2s(stage0 + iss_st * SB, iss_row + (int64_t)iss_g * SB, bytes, bar);
         }
         if (++iss_g == G) {
             iss_g = 0;
@@ -465,49 +439,46 @@ k_logp_fwd_bulk(const uint16_t* __restrict__ x, int64_t n, int64_t v, int64_t ld
     for (int64_t j = 0; j < rows; ++j) {
         const int64_t t = (int64_t)blockIdx.x + j * gridDim.x;
         const int folder = (int)(j % kTiles);
+        const char* xr = reinterpret_cast<const char*>(x) + t * ld * EB;
         bool act = false;
         float x_y = 0.f;
         if (warp == folder && lane == 0) {
             const int64_t yt = __ldg(y + t);
-            act = row_active(yt, v, ignore_index);
-            if (act) x_y = bf_scalar(x + t * ld + yt);
+            act = row_active(mask, t, yt, v, ignore_index);
+            if (act) x_y = elem_value<D>(xr, yt);
         }
-        const uint16_t* __restrict__ tile = x + t * ld + c0;
+        const char* tile = xr + c0 * EB;
         float m = -INFINITY, s = 0.f;
         for (int g = 0; g < G; ++g) {
             if (ok) {
                 ok = __all_sync(0xffffffffu, mbar_wait(bar0 + st * 8, phase, kWaitLimitCycles));
                 if (!ok) fail_at = j * G + g;
             }
-            const uint32_t sbase = stage0 + st * kStageBytes + lane * 16;
-            uint32_t q[kGroup][4];
+            const uint32_t sbase = stage0 + st * SB + lane * UB;
+            Unit<D> q[kGroup];
             if (g < Gfull) {
 #pragma unroll
-                for (int u = 0; u < kGroup; ++u) {
-                    const uint4 r = lds_v4(sbase + u * (kWarp * 16));
-                    q[u][0] = r.x; q[u][1] = r.y; q[u][2] = r.z; q[u][3] = r.w;
-                }
+                for (int u = 0; u < kGroup; ++u) unit_load_shared<D>(sbase + u * (kWarp * UB), q[u]);
                 __syncwarp();
                 if (ok && issued < jobs) {
                     if (lane == 0) fence_proxy_async_smem();
                     issue_next();
                 }
-                group_update<true>(q, kGroup, m, s);
+                group_update<D, true, kScaled>(q, kGroup, m, s, sc);
             } else {
-                const int v0 = g * kGroupVecs;
+                const int v0 = g * kGroupUnits;
                 int nvalid = 0;
 #pragma unroll
                 for (int u = 0; u < kGroup; ++u) {
                     const int jv = v0 + kWarp * u + lane;
                     if (jv < nfull) {
-                        const uint4 r = lds_v4(sbase + u * (kWarp * 16));
-                        q[u][0] = r.x; q[u][1] = r.y; q[u][2] = r.z; q[u][3] = r.w;
+                        unit_load_shared<D>(sbase + u * (kWarp * UB), q[u]);
                         nvalid = u + 1;
-                    } else if (jv < nvec) {
-                        load_words<false>(tile, (int64_t)jv * 8, width, q[u]);
+                    } else if (jv < nunit) {
+                        unit_load<D, false>(tile, (int64_t)jv * 8, width, q[u]);
                         nvalid = u + 1;
                     } else {
-                        q[u][0] = q[u][1] = q[u][2] = q[u][3] = kNegInf2;
+                        unit_fill_neg_inf<D>(q[u]);
                     }
                 }
                 __syncwarp();
@@ -515,15 +486,15 @@ k_logp_fwd_bulk(const uint16_t* __restrict__ x, int64_t n, int64_t v, int64_t ld
                     if (lane == 0) fence_proxy_async_smem();
                     issue_next();
                 }
-                if (nvalid == kGroup) group_update<true>(q, nvalid, m, s);
-                else group_update<false>(q, nvalid, m, s);
+                if (nvalid == kGroup) group_update<D, true, kScaled>(q, nvalid, m, s, sc);
+                else group_update<D, false, kScaled>(q, nvalid, m, s, sc);
             }
             if (++st == kStages) {
                 st = 0;
                 phase ^= 1u;
             }
         }
-        MS p = warp_merge(MS{m, s});
+        MS p = warp_merge<kScaled>(MS{m, s}, sc);
         if (lane == 0) {
             sh_m[j & 1][warp] = p.m;
             sh_s[j & 1][warp] = p.s;
@@ -531,8 +502,9 @@ k_logp_fwd_bulk(const uint16_t* __restrict__ x, int64_t n, int64_t v, int64_t ld
         __syncthreads();
         if (warp == folder) {
             const int k = lane & 15;
-            const MS f = tile_fold16(MS{sh_m[j & 1][k], sh_s[j & 1][k]});
-            if (lane == 0) finalize_row(f, act, x_y, logp + t, lse + t, lse_lo ? lse_lo + t : nullptr);
+            const MS f = tile_fold16(MS{sh_m[j & 1][k], sh_s[j & 1][k]}, sc.s);
+            if (lane == 0)
+                finalize_row(f, act, x_y, sc.s, logp + t, lse + t, lse_lo ? lse_lo + t : nullptr);
         }
     }
     if (!ok) {
@@ -545,23 +517,24 @@ k_logp_fwd_bulk(const uint16_t* __restrict__ x, int64_t n, int64_t v, int64_t ld
 
 // Shard partials: one CTA per row, warp w reduces the shard's local tile w
 // (global tile tile0 + w) with the same tile_scan/warp_merge as the forward.
-template <bool kVec>
+template <Dt D, bool kVec, bool kScaled>
 __global__ void __launch_bounds__(kFwdThreads)
-k_logp_partials(const uint16_t* __restrict__ xs, int64_t n, int64_t ld, int64_t real_width,
-                int64_t W, int tile0, int64_t vocab_start, const int64_t* __restrict__ y,
+k_logp_partials(const void* __restrict__ xs, int64_t n, int64_t ld, int64_t real_width, int64_t W,
+                int tile0, int64_t vocab_start, const int64_t* __restrict__ y, Scale sc,
                 float* __restrict__ pm, float* __restrict__ ps, float* __restrict__ sel) {
+    constexpr int EB = Unit<D>::kElemBytes;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int64_t t = blockIdx.x; t < n; t += gridDim.x) {
-        const uint16_t* __restrict__ xr = xs + t * ld;
+        const char* xr = reinterpret_cast<const char*>(xs) + t * ld * EB;
         if (threadIdx.x == 0) {
             const int64_t yt = __ldg(y + t);
             if (yt >= vocab_start && yt < vocab_start + real_width)
-                sel[t] = bf_scalar(xr + (yt - vocab_start));
+                sel[t] = elem_value<D>(xr, yt - vocab_start);
         }
         const int64_t c0 = (int64_t)warp * W;
         const int64_t width = real_width - c0 < W ? real_width - c0 : W;
-        MS p = tile_scan<kVec>(xr + c0, width, lane);
-        p = warp_merge(p);
+        MS p = tile_scan<D, kVec, kScaled>(xr + c0 * EB, width, lane, sc);
+        p = warp_merge<kScaled>(p, sc);
         if (lane == 0) {
             pm[t * kTiles + tile0 + warp] = p.m;
             ps[t * kTiles + tile0 + warp] = p.s;
@@ -573,8 +546,8 @@ k_logp_partials(const uint16_t* __restrict__ xs, int64_t n, int64_t ld, int64_t 
 // finalize_row as the forward.
 __global__ void __launch_bounds__(256)
 k_logp_merge(const float* __restrict__ pm, const float* __restrict__ ps,
-             const float* __restrict__ sel, const int64_t* __restrict__ y,
-             int64_t ignore_index, int64_t n, int64_t v, int n_tiles,
+             const float* __restrict__ sel, const int64_t* __restrict__ y, int64_t ignore_index,
+             const uint8_t* __restrict__ mask, int64_t n, int64_t v, int n_tiles, float s,
              float* __restrict__ logp, float* __restrict__ lse, float* __restrict__ lse_lo) {
     const int lane = threadIdx.x & 31, k = lane & 15;
     const int64_t warp_g = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -587,12 +560,12 @@ k_logp_merge(const float* __restrict__ pm, const float* __restrict__ ps,
             p.m = __ldg(pm + t * kTiles + k);
             p.s = __ldg(ps + t * kTiles + k);
         }
-        const MS f = tile_fold16(p);
+        const MS f = tile_fold16(p, s);
         if (valid && k == 0) {
             const int64_t yt = __ldg(y + t);
-            const bool act = row_active(yt, v, ignore_index);
+            const bool act = row_active(mask, t, yt, v, ignore_index);
             const float x_y = act ? __ldg(sel + t) : 0.f;
-            finalize_row(f, act, x_y, logp + t, lse + t, lse_lo ? lse_lo + t : nullptr);
+            finalize_row(f, act, x_y, s, logp + t, lse + t, lse_lo ? lse_lo + t : nullptr);
         }
     }
 }
@@ -601,134 +574,190 @@ k_logp_merge(const float* __restrict__ pm, const float* __restrict__ ps,
 
 // Per-row constants of the backward (see k_logp_bwd).
 struct BwdRow {
-    u64 neg_lr;   // (-lse_r, -lse_r)
-    u64 coef2;    // (coef, coef), coef = -g (1 - delta)
-    uint32_t floor_w;
-    float lr, delta, g;
+    u64 neg_lr;        // (-lse_r, -lse_r)
+    u64 s2;            // (s, s)
+    u64 coef2;         // (coef, coef), coef = -s g (1 - delta)
+    uint32_t floor_w;  // BF16: packed floor for the raw logits
+    float floor_f;     // FP16/FP32: floor for the raw logits
+    float lr, delta, gs, s;
 };
 
-// Gradient of one vector of 8 columns (words w, output words o), target
-// column jt (or outside [0, 8)).
-__device__ __forceinline__ void bwd_vector(const uint32_t (&w)[4], const BwdRow& r, int64_t jt,
-                                           uint32_t (&o)[4]) {
+// The pair (x_{2k}, x_{2k+1}) of a unit widened to binary32 and raised to the
+// row's floor.
+template <Dt D>
+__device__ __forceinline__ u64 bwd_pair(const Unit<D>& u, int k, const BwdRow& r) {
+    if constexpr (D == Dt::BF16) {
+        const uint32_t w = bf2_max(u.w[k], r.floor_w);
+        return f2(bf_lo(w), bf_hi(w));
+    } else if constexpr (D == Dt::F16) {
+        return f2(fmaxf(h_lo(u.w[k]), r.floor_f), fmaxf(h_hi(u.w[k]), r.floor_f));
+    } else {
+        return f2(fmaxf(__uint_as_float(u.w[2 * k]), r.floor_f),
+                  fmaxf(__uint_as_float(u.w[2 * k + 1]), r.floor_f));
+    }
+}
+
+// Gradient of one unit (8 columns) into output words o, target column jt (or
+// outside [0, 8)).
+template <Dt D>
+__device__ __forceinline__ void bwd_unit(const Unit<D>& u, const BwdRow& r, int64_t jt,
+                                         uint32_t (&o)[Unit<D>::kWords]) {
     const u64 l2e = f2(kLog2e, kLog2e);
     const u64 nln2hi = f2(-kLn2Hi, -kLn2Hi), nln2lo = f2(-kLn2Lo, -kLn2Lo);
+    float d[8];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        const u64 tt = f2_add(bf2_widen(bf2_max(w[k], r.floor_w)), r.neg_lr);
+        const u64 tt = f2_fma(bwd_pair<D>(u, k, r), r.s2, r.neg_lr);
         const u64 a = f2_mul(tt, l2e);
         const u64 c = f2_fma(a, nln2lo, f2_fma(a, nln2hi, tt));
         float a0, a1;
         f2_split(a, a0, a1);
         const u64 q = f2_mul(f2(ex2_ftz(a0), ex2_ftz(a1)), r.coef2);
-        float d0, d1;
-        f2_split(f2_fma(q, c, q), d0, d1);
-        o[k] = pack_bf16x2(d0, d1);
+        f2_split(f2_fma(q, c, q), d[2 * k], d[2 * k + 1]);
     }
     if (jt >= 0 && jt < 8) {
-        // target column: g * (1 - p) without cancellation
-        const int kt = (int)(jt >> 1);
-        uint32_t wk = 0;
+        // target column: s g (1 - p) without cancellation (one call site, the
+        // element picked by unrolled selects)
+        float xt = 0.f;
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-            if (k == kt) wk = w[k];
-        wk = bf2_max(wk, r.floor_w);
-        const float xt = (jt & 1) ? bf_hi(wk) : bf_lo(wk);
-        const float dt = __fmul_rn(-r.g, expm1f(__fsub_rn(__fsub_rn(xt, r.lr), r.delta)));
-        const uint32_t bt = pack_bf16x2(dt, dt) & 0xffffu;
+        for (int k = 0; k < 4; ++k) {
+            float lo, hi;
+            f2_split(bwd_pair<D>(u, k, r), lo, hi);
+            if (k == (int)(jt >> 1)) xt = (jt & 1) ? hi : lo;
+        }
+        const float dt = __fmul_rn(-r.gs, expm1f(__fsub_rn(__fmaf_rn(r.s, xt, -r.lr), r.delta)));
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-            if (k == kt) o[k] = (jt & 1) ? ((o[k] & 0xffffu) | (bt << 16)) : ((o[k] & 0xffff0000u) | bt);
+        for (int j = 0; j < 8; ++j)
+            if (j == (int)jt) d[j] = dt;
+    }
+    if constexpr (D == Dt::BF16) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) o[k] = pack_bf16x2(d[2 * k], d[2 * k + 1]);
+    } else if constexpr (D == Dt::F16) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) o[k] = pack_f16x2(d[2 * k], d[2 * k + 1]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) o[j] = __float_as_uint(d[j]);
     }
 }
 
-template <bool kVecIn, bool kInPlace>
-__device__ __forceinline__ void bwd_load(const uint16_t* xr, int64_t col, int64_t v, uint32_t (&w)[4]) {
+template <Dt D, bool kVecIn, bool kInPlace>
+__device__ __forceinline__ void bwd_load(const char* xr, int64_t col, int64_t v, Unit<D>& u) {
+    constexpr int EB = Unit<D>::kElemBytes;
     if (kVecIn && col + 8 <= v) {
-        const uint4 q = kInPlace ? ld_v4(xr + col) : ld_nc_v4(xr + col);
-        w[0] = q.x; w[1] = q.y; w[2] = q.z; w[3] = q.w;
+        const char* p = xr + col * EB;
+        const uint4 a = kInPlace ? ld_v4(p) : ld_nc_v4(p);
+        u.w[0] = a.x; u.w[1] = a.y; u.w[2] = a.z; u.w[3] = a.w;
+        if constexpr (D == Dt::F32) {
+            const uint4 b = kInPlace ? ld_v4(p + 16) : ld_nc_v4(p + 16);
+            u.w[4] = b.x; u.w[5] = b.y; u.w[6] = b.z; u.w[7] = b.w;
+        }
+    } else if constexpr (D == Dt::F32) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            u.w[j] = (col + j < v) ? (kInPlace ? elem_bits_plain<D>(xr, col + j) : elem_bits<D>(xr, col + j)) : 0u;
     } else {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             uint32_t lo = 0, hi = 0;
-            if (col + 2 * k < v) lo = kInPlace ? xr[col + 2 * k] : ldg_u16(xr + col + 2 * k);
-            if (col + 2 * k + 1 < v) hi = kInPlace ? xr[col + 2 * k + 1] : ldg_u16(xr + col + 2 * k + 1);
-            w[k] = lo | (hi << 16);
+            if (col + 2 * k < v)
+                lo = kInPlace ? elem_bits_plain<D>(xr, col + 2 * k) : elem_bits<D>(xr, col + 2 * k);
+            if (col + 2 * k + 1 < v)
+                hi = kInPlace ? elem_bits_plain<D>(xr, col + 2 * k + 1) : elem_bits<D>(xr, col + 2 * k + 1);
+            u.w[k] = lo | (hi << 16);
         }
     }
 }
 
-template <bool kVecOut>
-__device__ __forceinline__ void bwd_store(uint16_t* dr, int64_t col, int64_t v, const uint32_t (&o)[4]) {
+template <Dt D, bool kVecOut>
+__device__ __forceinline__ void bwd_store(char* dr, int64_t col, int64_t v,
+                                          const uint32_t (&o)[Unit<D>::kWords]) {
+    constexpr int EB = Unit<D>::kElemBytes;
     if (kVecOut && col + 8 <= v) {
-        st_cs_v4(dr + col, make_uint4(o[0], o[1], o[2], o[3]));
+        st_cs_v4(dr + col * EB, make_uint4(o[0], o[1], o[2], o[3]));
+        if constexpr (D == Dt::F32) st_cs_v4(dr + col * EB + 16, make_uint4(o[4], o[5], o[6], o[7]));
+    } else if constexpr (D == Dt::F32) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (col + j < v) reinterpret_cast<uint32_t*>(dr)[col + j] = o[j];
     } else {
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-            if (col + j < v) dr[col + j] = (uint16_t)((j & 1) ? (o[j >> 1] >> 16) : (o[j >> 1] & 0xffffu));
+            if (col + j < v)
+                reinterpret_cast<uint16_t*>(dr)[col + j] =
+                    (uint16_t)((j & 1) ? (o[j >> 1] >> 16) : (o[j >> 1] & 0xffffu));
     }
 }
 
 // Backward: one CTA per (row, segment of kBwdSegCols columns), elementwise.
 // Per active row: LSE = lse (+ lse_lo) is split as lse_r + delta with lse_r
-// on a 2^-16 grid, so that t = x - lse_r is exact for the bulk of BF16
-// logits; exp(t) = 2^a (1 + c) with a = t log2 e rounded and c = t - a ln 2
-// recovered by two fused multiply-adds against a two-float ln 2 (the rounding
-// error of a, carried to first order); coef = -g (1 - delta) ~ -g exp(-delta)
-// folds g and delta in once per row.  Logits below LSE - 200 are raised to
-// that bound first (their exp is below 2^-288, zero in binary32), which also
-// keeps a -inf logit from producing inf - inf.  The target column is
-// g * (1 - p) = -g * expm1(x - LSE), without cancellation.  Values below
-// 2^-126 flush to zero.  Each thread loads its four vectors before computing
-// any, so four 16-byte loads are in flight per thread.
-template <bool kVecIn, bool kVecOut, bool kInPlace>
+// on a 2^-16 grid, so that t = s x - lse_r is exact for the bulk of BF16
+// logits at s = 1 (one rounding otherwise); exp(t) = 2^a (1 + c) with
+// a = t log2 e rounded and c = t - a ln 2 recovered by two fused multiply-adds
+// against a two-float ln 2 (the rounding error of a, carried to first order);
+// coef = -s g (1 - delta) ~ -s g exp(-delta) folds s, g and delta in once per
+// row.  Logits below (LSE - 200) / s are raised to that bound first (their exp
+// is below e^-200, zero in binary32), which also keeps a -inf logit from
+// producing inf - inf.  The target column is s g (1 - p) = -s g expm1(s x - LSE),
+// without cancellation.  Values below 2^-126 flush to zero.  Each thread loads
+// its four units before computing any, so four (FP32: eight) 16-byte loads are
+// in flight per thread.
+template <Dt D, bool kVecIn, bool kVecOut, bool kInPlace>
 __global__ void __launch_bounds__(kBwdThreads)
-k_logp_bwd(const uint16_t* x, int64_t n, int64_t v, int64_t ld, const int64_t* __restrict__ y,
-           int64_t ignore_index, const float* __restrict__ lse, const float* __restrict__ lse_lo,
-           const float* __restrict__ g, uint16_t* dx, int64_t ld_out, int64_t segs) {
+k_logp_bwd(const void* x, int64_t n, int64_t v, int64_t ld, const int64_t* __restrict__ y,
+           int64_t ignore_index, const uint8_t* __restrict__ mask, float s,
+           const float* __restrict__ lse, const float* __restrict__ lse_lo,
+           const float* __restrict__ g, void* dx, int64_t ld_out, int64_t segs) {
+    constexpr int EB = Unit<D>::kElemBytes;
+    constexpr int NW = Unit<D>::kWords;
     const int64_t items = n * segs;
     for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
         const int64_t t = item / segs;
         const int64_t col0 = (item - t * segs) * kBwdSegCols + (int64_t)threadIdx.x * 8;
-        const uint16_t* xr = x + t * ld;
-        uint16_t* dr = dx + t * ld_out;
+        const char* xr = reinterpret_cast<const char*>(x) + t * ld * EB;
+        char* dr = reinterpret_cast<char*>(dx) + t * ld_out * EB;
         const int64_t yt = __ldg(y + t);
-        if (!row_active(yt, v, ignore_index)) {
-            const uint32_t z[4] = {0u, 0u, 0u, 0u};
+        const int64_t cs = (int64_t)kBwdThreads * 8;
+        if (!row_active(mask, t, yt, v, ignore_index)) {
+            uint32_t z[NW];
 #pragma unroll
-            for (int u = 0; u < kBwdVecPerThread; ++u) {
-                const int64_t col = col0 + (int64_t)u * kBwdThreads * 8;
-                if (col < v) bwd_store<kVecOut>(dr, col, v, z);
-            }
+            for (int k = 0; k < NW; ++k) z[k] = 0u;
+#pragma unroll
+            for (int u = 0; u < kBwdUnitsPerThread; ++u)
+                if (col0 + u * cs < v) bwd_store<D, kVecOut>(dr, col0 + u * cs, v, z);
             continue;
         }
         BwdRow r;
         const float l = __ldg(lse + t);
         const float l_lo = lse_lo ? __ldg(lse_lo + t) : 0.f;
-        r.g = __ldg(g + t);
+        r.s = s;
+        r.gs = __fmul_rn(s, __ldg(g + t));
         r.lr = (fabsf(l) < 8388608.f) ? __fmul_rn(rintf(__fmul_rn(l, 65536.f)), 1.f / 65536.f) : l;
-        r.delta = __fadd_rn(__fsub_rn(l, r.lr), l_lo);          // l - lr is exact
-        const float coef = __fmaf_rn(r.g, r.delta, -r.g);        // -g (1 - delta)
-        r.floor_w = kNegInf2;
-        if (fabsf(l) < 1048576.f) {
-            const uint32_t b = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rd(__fsub_rn(l, 200.f)));
+        r.delta = __fadd_rn(__fsub_rn(l, r.lr), l_lo);           // l - lr is exact
+        const float coef = __fmaf_rn(r.gs, r.delta, -r.gs);       // -s g (1 - delta)
+        const float fl = __fdiv_rn(__fsub_rn(l, 200.f), s);       // (LSE - 200) / s
+        r.floor_f = fl;
+        r.floor_w = 0xff80ff80u;
+        if constexpr (D == Dt::BF16) {
+            const uint32_t b = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rd(fl));
             r.floor_w = b | (b << 16);
         }
         r.neg_lr = f2(-r.lr, -r.lr);
+        r.s2 = f2(s, s);
         r.coef2 = f2(coef, coef);
 
-        uint32_t w0[4], w1[4], w2[4], w3[4];
-        static_assert(kBwdVecPerThread == 4, "four vectors per thread");
-        const int64_t cs = (int64_t)kBwdThreads * 8;
-        if (col0 < v) bwd_load<kVecIn, kInPlace>(xr, col0, v, w0);
-        if (col0 + cs < v) bwd_load<kVecIn, kInPlace>(xr, col0 + cs, v, w1);
-        if (col0 + 2 * cs < v) bwd_load<kVecIn, kInPlace>(xr, col0 + 2 * cs, v, w2);
-        if (col0 + 3 * cs < v) bwd_load<kVecIn, kInPlace>(xr, col0 + 3 * cs, v, w3);
-        uint32_t o[4];
-        if (col0 < v) { bwd_vector(w0, r, yt - col0, o); bwd_store<kVecOut>(dr, col0, v, o); }
-        if (col0 + cs < v) { bwd_vector(w1, r, yt - (col0 + cs), o); bwd_store<kVecOut>(dr, col0 + cs, v, o); }
-        if (col0 + 2 * cs < v) { bwd_vector(w2, r, yt - (col0 + 2 * cs), o); bwd_store<kVecOut>(dr, col0 + 2 * cs, v, o); }
-        if (col0 + 3 * cs < v) { bwd_vector(w3, r, yt - (col0 + 3 * cs), o); bwd_store<kVecOut>(dr, col0 + 3 * cs, v, o); }
+        Unit<D> w0, w1, w2, w3;
+        static_assert(kBwdUnitsPerThread == 4, "four units per thread");
+        if (col0 < v) bwd_load<D, kVecIn, kInPlace>(xr, col0, v, w0);
+        if (col0 + cs < v) bwd_load<D, kVecIn, kInPlace>(xr, col0 + cs, v, w1);
+        if (col0 + 2 * cs < v) bwd_load<D, kVecIn, kInPlace>(xr, col0 + 2 * cs, v, w2);
+        if (col0 + 3 * cs < v) bwd_load<D, kVecIn, kInPlace>(xr, col0 + 3 * cs, v, w3);
+        uint32_t o[NW];
+        if (col0 < v) { bwd_unit<D>(w0, r, yt - col0, o); bwd_store<D, kVecOut>(dr, col0, v, o); }
+        if (col0 + cs < v) { bwd_unit<D>(w1, r, yt - (col0 + cs), o); bwd_store<D, kVecOut>(dr, col0 + cs, v, o); }
+        if (col0 + 2 * cs < v) { bwd_unit<D>(w2, r, yt - (col0 + 2 * cs), o); bwd_store<D, kVecOut>(dr, col0 + 2 * cs, v, o); }
+        if (col0 + 3 * cs < v) { bwd_unit<D>(w3, r, yt - (col0 + 3 * cs), o); bwd_store<D, kVecOut>(dr, col0 + 3 * cs, v, o); }
     }
 }
 

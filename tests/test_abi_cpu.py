@@ -109,6 +109,22 @@ def test_shard_gate(lib):
     assert b"device memory" in lib.flp_last_error() or b"cudaPointer" in lib.flp_last_error()
 
 
+def test_ex_entry_points_reject_bad_dtype_and_temperature(lib):
+    buf = (ctypes.c_char * 64)()
+    p = ctypes.addressof(buf)
+    assert lib.fused_logp_forward_ex(p, 3, 4, 10, 10, p, -100, None, 1.0, p, p, None, None) == EINVAL
+    assert b"dtype" in lib.flp_last_error()
+    for bad in (0.0, -1.0, float("inf"), float("nan")):
+        assert lib.fused_logp_forward_ex(p, 0, 4, 10, 10, p, -100, None, bad, p, p, None, None) == EINVAL
+        assert lib.fused_logp_backward_ex(p, 0, 4, 10, 10, p, -100, None, bad, p, None, p, p, 10,
+                                          None) == EINVAL
+        assert lib.logp_merge_partials_ex(p, p, p, p, -100, None, 4, 10, bad, p, p, None, None) == EINVAL
+    assert lib.logp_shard_partials_ex(p, 7, 4, 10, 0, 10, 10, 1.0, p, p, p, p, None) == EINVAL
+    # FP32 shard bounds are checked on the same tile grid
+    assert lib.logp_shard_partials_ex(p, 2, 8, 76032, 100, 75968, 151936, 1.0, p, p, p, p,
+                                      None) == EUNSUP
+
+
 def test_device_entry_points_reject_null_outputs(lib):
     assert lib.flp_device_error(0, None) == EINVAL
     assert lib.flp_selftest_wait_timeout(0, 1000, None) == EINVAL
@@ -119,11 +135,15 @@ def test_device_entry_points_reject_null_outputs(lib):
 
 
 def test_python_binding_checks_before_calling():
-    x = torch.zeros((4, 10), dtype=torch.float32)
+    x = torch.zeros((4, 10), dtype=torch.float64)
     y = torch.zeros(4, dtype=torch.int64)
     with pytest.raises(TypeError):
         flp.fused_logp_forward(x, y)
     xb = x.to(torch.bfloat16)
+    with pytest.raises(ValueError):
+        flp.fused_logp_forward(xb, y, temperature=0.0)
+    with pytest.raises(ValueError):
+        flp.fused_logp_forward(xb, y, temperature=float("inf"))
     with pytest.raises(TypeError):
         flp.fused_logp_forward(xb, y.to(torch.int32))
     with pytest.raises(ValueError):

@@ -1,0 +1,187 @@
+"""GPU parity of the variants on the same kernels: FP16 and FP32 logits, a
+temperature (rollout logprobs at T = 0.7, RL-Kernel PR #495 provider
+experiment) and an explicit active-row mask (PR #314 MaskMode), against the
+FP64 oracle with the same dtype, scale and mask; plus the bitwise properties
+(aligned = misaligned, sharded = unsharded, batch invariance) for each.
+
+Tolerances: logp |d| <= 1e-4 (as for BF16).  BF16/FP16 gradients: max error
+no worse than max(2e-3 max|d|, the correctly rounded result's own gap) and at
+least 99.99% correctly rounded.  FP32 gradients: max |error| <= 1e-6 max|d|
+(the FP32 arithmetic carries ~1e-7 relative error on exp(x - LSE), a few ulp
+of binary32, so "correctly rounded" is not the criterion there)."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import selected_token_logprob_gb300 as flp
+import workloads
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+V = workloads.QWEN3_VOCAB
+DTYPES = [torch.bfloat16, torch.float16, torch.float32]
+T07 = 0.7
+S07 = float(np.float32(1.0 / T07))   # the binary32 inverse temperature the library uses
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    flp._lib.load(build_if_missing=True)
+
+
+def _i(t):
+    """Integer view for bitwise comparison."""
+    return t.view(torch.int32 if t.dtype == torch.float32 else torch.int16)
+
+
+def run(x, y, g, temperature=1.0, mask=None, ignore_index=-100):
+    logp, lse, lo = flp.fused_logp_forward(x, y, ignore_index, with_lse_lo=True,
+                                           temperature=temperature, active_mask=mask)
+    d = flp.fused_logp_backward(x, y, lse, g, ignore_index, lse_lo=lo, temperature=temperature,
+                                active_mask=mask)
+    return logp, lse, d
+
+
+def check(x, y, g, logp, lse, d, scale, mask=None, ignore_index=-100):
+    xa, dt = workloads.host_array(x)
+    yn, gn = y.cpu().numpy(), g.cpu().numpy()
+    mk = None if mask is None else mask.cpu().numpy().astype(np.uint8)
+    ref_logp, ref_lse = oracle.forward(xa, yn, ignore_index, dtype=dt, scale=scale, mask=mk)
+    e_logp = float(np.max(np.abs(logp.double().cpu().numpy() - ref_logp)))
+    lse_tol = 1e-4 + np.spacing(np.abs(ref_lse).astype(np.float32)).astype(np.float64)
+    assert e_logp <= 1e-4, e_logp
+    assert np.all(np.abs(lse.double().cpu().numpy() - ref_lse) <= lse_tol)
+    da, _ = workloads.host_array(d)
+    st = oracle.backward_compare(xa, yn, gn, da, ignore_index, dtype=dt, scale=scale, mask=mk)
+    cr = 1 - st["n_not_correctly_rounded"] / st["n_compared"]
+    st["correctly_rounded"] = cr
+    st["max_abs_logp_err"] = e_logp
+    assert st["n_nonfinite"] == 0, st
+    if dt == "f32":
+        assert st["max_abs_diff"] <= 1e-6 * st["max_abs_d"], st
+    else:
+        assert st["max_abs_diff"] <= max(2e-3 * st["max_abs_d"], st["max_rounding_gap"]), st
+        assert cr >= 0.9999, st
+    return st
+
+
+@pytest.mark.parametrize("temperature", [1.0, T07])
+@pytest.mark.parametrize("dtype", DTYPES, ids=["bf16", "f16", "f32"])
+def test_dtype_and_temperature_parity(dtype, temperature):
+    x, y, g = workloads.make("mid", device=DEV, n=256, dtype=dtype)
+    logp, lse, d = run(x, y, g, temperature)
+    st = check(x, y, g, logp, lse, d, 1.0 if temperature == 1.0 else S07)
+    print(f"{dtype} T={temperature}:", st)
+
+
+@pytest.mark.parametrize("dtype", DTYPES, ids=["bf16", "f16", "f32"])
+@pytest.mark.parametrize("v", [1, 9, 255, 1031, 4097])
+def test_ragged_shapes_other_dtypes(dtype, v):
+    wl = workloads.Workload("edge", 5, v, 2.0, 8.0, 0.2, "normal", seed=v)
+    x, y, g = workloads.make(wl, device=DEV, dtype=dtype)
+    logp, lse, d = run(x, y, g, T07)
+    xa, dt = workloads.host_array(x)
+    ref_logp, _ = oracle.forward(xa, y.cpu().numpy(), dtype=dt, scale=S07)
+    assert np.max(np.abs(logp.double().cpu().numpy() - ref_logp)) <= 1e-4
+    da, _ = workloads.host_array(d)
+    st = oracle.backward_compare(xa, y.cpu().numpy(), g.cpu().numpy(), da, dtype=dt, scale=S07)
+    assert st["n_nonfinite"] == 0
+    bound = 1e-6 * st["max_abs_d"] if dt == "f32" else max(2e-3 * st["max_abs_d"], st["max_rounding_gap"])
+    assert st["max_abs_diff"] <= bound + 1e-30, st
+
+
+@pytest.mark.parametrize("dtype", DTYPES, ids=["bf16", "f16", "f32"])
+def test_misaligned_rows_match_bulk_path_bitwise(dtype):
+    n, v = 6, 151936
+    x, y, g = workloads.make(workloads.Workload("al", n, v, 2.0, 8.0, 0.0, "normal", seed=4),
+                             device=DEV, dtype=dtype)
+    ld = v + 1
+    big = torch.zeros(n * ld + 2, dtype=dtype, device=DEV)
+    xs = big[1:1 + n * ld].view(n, ld)[:, :v]
+    xs.copy_(x)
+    for temperature in (1.0, T07):
+        a = run(x, y, g, temperature)
+        b = run(xs, y, g, temperature)
+        for u, w in zip(a, b):
+            assert torch.equal(_i(u.contiguous()), _i(w.contiguous()))
+
+
+def test_active_mask_rows():
+    x, y, g = workloads.make("mid", device=DEV, n=128)
+    mask = torch.ones(128, dtype=torch.bool, device=DEV)
+    mask[::3] = False
+    logp0, lse0, d0 = run(x, y, g)
+    logp, lse, d = run(x, y, g, mask=mask)
+    off = ~mask
+    assert torch.all(logp[off] == 0) and int(d[off].view(torch.int16).abs().sum()) == 0
+    assert torch.equal(_i(logp[mask]), _i(logp0[mask])) and torch.equal(_i(d[mask]), _i(d0[mask]))
+    assert torch.equal(_i(lse), _i(lse0))
+    check(x, y, g, logp, lse, d, 1.0, mask=mask)
+
+
+@pytest.mark.parametrize("dtype", DTYPES, ids=["bf16", "f16", "f32"])
+def test_sharded_equals_unsharded_with_temperature(dtype):
+    n = 512
+    x, y, _ = workloads.make("sharded", device=DEV, n=n, dtype=dtype)
+    mask = (torch.arange(n, device=DEV) % 5 != 0)
+    logp, lse, lo = flp.fused_logp_forward(x, y, with_lse_lo=True, temperature=T07, active_mask=mask)
+    for S in (2, 4):
+        pm = torch.full((n, 16), float("nan"), device=DEV)
+        ps = torch.full((n, 16), float("nan"), device=DEV)
+        sel = torch.full((n,), float("nan"), device=DEV)
+        for l in range(S):
+            a, b = l * V // S, (l + 1) * V // S
+            w = b - a
+            wpad = -(-w // 128) * 128
+            buf = torch.full((n, wpad), float("-inf"), dtype=dtype, device=DEV)
+            buf[:, :w] = x[:, a:b]
+            flp.logp_shard_partials(buf, a, w, V, y, pm, ps, sel, temperature=T07)
+        s_logp, s_lse, s_lo = flp.logp_merge_partials(pm, ps, sel, y, V, with_lse_lo=True,
+                                                      temperature=T07, active_mask=mask)
+        assert torch.equal(_i(s_lse), _i(lse)) and torch.equal(_i(s_logp), _i(logp))
+        assert torch.equal(_i(s_lo), _i(lo))
+
+
+@pytest.mark.parametrize("dtype", DTYPES, ids=["bf16", "f16", "f32"])
+def test_batch_invariance_other_dtypes(dtype):
+    probes, py, pg = workloads.make(workloads.Workload("p", 4, V, 3.0, 0.0, 0.0, "normal", seed=7),
+                                    device=DEV, dtype=dtype)
+    filler, fy, fg = workloads.make(workloads.Workload("f", 257, V, 3.0, 0.0, 0.0, "normal", seed=8),
+                                    device=DEV, dtype=dtype)
+    for k in range(4):
+        ref = run(probes[k:k + 1], py[k:k + 1], pg[k:k + 1], T07)
+        for B in (2, 17, 64, 257):
+            for pos in (0, B // 2, B - 1):
+                xb, yb, gb = filler[:B].clone(), fy[:B].clone(), fg[:B].clone()
+                xb[pos], yb[pos], gb[pos] = probes[k], py[k], pg[k]
+                out = run(xb, yb, gb, T07)
+                for r, o in zip(ref, out):
+                    assert torch.equal(_i(r[0:1].contiguous()), _i(o[pos:pos + 1].contiguous()))
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.float32], ids=["f16", "f32"])
+def test_in_place_other_dtypes(dtype):
+    x, y, g = workloads.make("tiny", device=DEV, dtype=dtype)
+    logp, lse, lo = flp.fused_logp_forward(x, y, with_lse_lo=True)
+    d = flp.fused_logp_backward(x, y, lse, g, lse_lo=lo)
+    xi = x.clone()
+    flp.fused_logp_backward(xi, y, lse, g, lse_lo=lo, dlogits=xi)
+    assert torch.equal(_i(xi), _i(d))
+
+
+def test_autograd_with_temperature_and_mask():
+    x, y, g = workloads.make("tiny", device=DEV, dtype=torch.float32)
+    mask = torch.arange(64, device=DEV) % 4 != 1
+    xr = x.clone().requires_grad_(True)
+    (flp.fused_logp(xr, y, temperature=T07, active_mask=mask) * g).sum().backward()
+    _, _, d = run(x, y, g, T07, mask=mask)
+    assert torch.equal(xr.grad.view(torch.int32), d.view(torch.int32))
+    # against torch's own autograd of log_softmax(x / T) in float64
+    xd = x.double().requires_grad_(True)
+    lp = torch.log_softmax(xd * S07, dim=1)
+    act = (y >= 0) & mask
+    sel = lp.gather(1, y.clamp(min=0)[:, None])[:, 0] * act
+    (sel * g.double()).sum().backward()
+    assert torch.allclose(xr.grad.double(), xd.grad, rtol=0, atol=1e-6 * xd.grad.abs().max().item())

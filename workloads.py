@@ -64,10 +64,12 @@ def _gen(device, seed: int, stream: int) -> torch.Generator:
 
 
 def logits(n: int, v: int, sigma: float, spike: float, seed: int, device="cpu",
-           ld: int | None = None, block_rows: int = 1024) -> torch.Tensor:
-    """BF16 [n, ld] (ld >= v; padding columns are 0) ~ N(0, sigma^2) + spike."""
+           ld: int | None = None, block_rows: int = 1024,
+           dtype: torch.dtype = torch.bfloat16) -> torch.Tensor:
+    """[n, ld] (ld >= v; padding columns are 0) ~ N(0, sigma^2) + spike, drawn in
+    FP32 and cast once (round to nearest even) to `dtype`."""
     ld = v if ld is None else ld
-    out = torch.zeros((n, ld), dtype=torch.bfloat16, device=device)
+    out = torch.zeros((n, ld), dtype=dtype, device=device)
     gl = _gen(device, seed, _S_LOGITS)
     gs = _gen(device, seed, _S_SPIKE)
     for r0 in range(0, n, block_rows):
@@ -78,7 +80,7 @@ def logits(n: int, v: int, sigma: float, spike: float, seed: int, device="cpu",
         if spike:
             cols = torch.randint(0, v, (r1 - r0,), generator=gs, device=device)
             blk[torch.arange(r1 - r0, device=device), cols] += spike
-        out[r0:r1, :v] = blk.to(torch.bfloat16)
+        out[r0:r1, :v] = blk.to(dtype)
         del blk
     return out
 
@@ -106,12 +108,12 @@ def grads(n: int, kind: str, seed: int, device="cpu") -> torch.Tensor:
 
 
 def make(name_or_wl, device="cpu", n: int | None = None, seed: int | None = None,
-         ld: int | None = None):
-    """(logits bf16 [n, ld], targets int64 [n], grad fp32 [n]) of a workload."""
+         ld: int | None = None, dtype: torch.dtype = torch.bfloat16):
+    """(logits [n, ld] in `dtype`, targets int64 [n], grad fp32 [n]) of a workload."""
     wl = WORKLOADS[name_or_wl] if isinstance(name_or_wl, str) else name_or_wl
     n = wl.n if n is None else n
     seed = wl.seed if seed is None else seed
-    x = logits(n, wl.v, wl.sigma, wl.spike, seed, device=device, ld=ld)
+    x = logits(n, wl.v, wl.sigma, wl.spike, seed, device=device, ld=ld, dtype=dtype)
     y = targets(n, wl.v, wl.ignore_frac, seed, device=device)
     g = grads(n, wl.grad, seed, device=device)
     return x, y, g
@@ -130,5 +132,14 @@ def sweep_rows(count: int, v: int, sigma: float, seed: int, stream: int, device=
 
 
 def bf16_bits(t: torch.Tensor):
-    """numpy uint16 view of a CPU BF16 tensor (for the oracle)."""
+    """numpy uint16 view of a BF16 (or FP16) tensor (for the oracle)."""
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view("uint16")
+
+
+def host_array(t: torch.Tensor):
+    """(numpy array, dtype name) of a logits/gradient tensor for the oracle:
+    uint16 bit patterns for bf16/f16, float32 values for f32."""
+    if t.dtype == torch.float32:
+        return t.detach().cpu().contiguous().numpy(), "f32"
+    name = {torch.bfloat16: "bf16", torch.float16: "f16"}[t.dtype]
+    return bf16_bits(t), name
