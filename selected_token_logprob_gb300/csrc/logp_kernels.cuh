@@ -597,6 +597,17 @@ __device__ __forceinline__ u64 bwd_pair(const Unit<D>& u, int k, const BwdRow& r
     }
 }
 
+// Output word(s) of a gradient pair in dtype D (for FP32 two words).
+template <Dt D>
+__device__ __forceinline__ void put_pair(uint32_t (&o)[Unit<D>::kWords], int k, float d0, float d1) {
+    if constexpr (D == Dt::BF16) o[k] = pack_bf16x2(d0, d1);
+    else if constexpr (D == Dt::F16) o[k] = pack_f16x2(d0, d1);
+    else {
+        o[2 * k] = __float_as_uint(d0);
+        o[2 * k + 1] = __float_as_uint(d1);
+    }
+}
+
 // Gradient of one unit (8 columns) into output words o, target column jt (or
 // outside [0, 8)).
 template <Dt D>
@@ -604,41 +615,45 @@ __device__ __forceinline__ void bwd_unit(const Unit<D>& u, const BwdRow& r, int6
                                          uint32_t (&o)[Unit<D>::kWords]) {
     const u64 l2e = f2(kLog2e, kLog2e);
     const u64 nln2hi = f2(-kLn2Hi, -kLn2Hi), nln2lo = f2(-kLn2Lo, -kLn2Lo);
-    float d[8];
+    float xt = 0.f;
+    const int kt = (int)(jt >> 1);
+    const bool has_t = jt >= 0 && jt < 8;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        const u64 tt = f2_fma(bwd_pair<D>(u, k, r), r.s2, r.neg_lr);
+        const u64 xp = bwd_pair<D>(u, k, r);
+        if (k == kt) {
+            float lo, hi;
+            f2_split(xp, lo, hi);
+            xt = (jt & 1) ? hi : lo;
+        }
+        const u64 tt = f2_fma(xp, r.s2, r.neg_lr);
         const u64 a = f2_mul(tt, l2e);
         const u64 c = f2_fma(a, nln2lo, f2_fma(a, nln2hi, tt));
         float a0, a1;
         f2_split(a, a0, a1);
         const u64 q = f2_mul(f2(ex2_ftz(a0), ex2_ftz(a1)), r.coef2);
-        f2_split(f2_fma(q, c, q), d[2 * k], d[2 * k + 1]);
+        float d0, d1;
+        f2_split(f2_fma(q, c, q), d0, d1);
+        put_pair<D>(o, k, d0, d1);
     }
-    if (jt >= 0 && jt < 8) {
-        // target column: s g (1 - p) without cancellation (one call site, the
-        // element picked by unrolled selects)
-        float xt = 0.f;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            float lo, hi;
-            f2_split(bwd_pair<D>(u, k, r), lo, hi);
-            if (k == (int)(jt >> 1)) xt = (jt & 1) ? hi : lo;
-        }
+    if (has_t) {
+        // target column: s g (1 - p) without cancellation, patched into its word
         const float dt = __fmul_rn(-r.gs, expm1f(__fsub_rn(__fmaf_rn(r.s, xt, -r.lr), r.delta)));
+        if constexpr (D == Dt::F32) {
+            // blend by masks (a predicated store per word would be folded into
+            // one store at a run-time index, which needs local memory)
+            const uint32_t bits = __float_as_uint(dt);
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if (j == (int)jt) d[j] = dt;
-    }
-    if constexpr (D == Dt::BF16) {
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t msk = 0u - (uint32_t)(j == (int)jt);
+                o[j] = (o[j] & ~msk) | (bits & msk);
+            }
+        } else {
+            const uint32_t bt = ((D == Dt::BF16) ? pack_bf16x2(dt, dt) : pack_f16x2(dt, dt)) & 0xffffu;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) o[k] = pack_bf16x2(d[2 * k], d[2 * k + 1]);
-    } else if constexpr (D == Dt::F16) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) o[k] = pack_f16x2(d[2 * k], d[2 * k + 1]);
-    } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) o[j] = __float_as_uint(d[j]);
+            for (int k = 0; k < 4; ++k)
+                if (k == kt) o[k] = (jt & 1) ? ((o[k] & 0xffffu) | (bt << 16)) : ((o[k] & 0xffff0000u) | bt);
+        }
     }
 }
 
