@@ -208,22 +208,22 @@ struct BwdArgs {
     const int64_t* y;
     int64_t ii;
     const uint8_t* mask;
-    float s;
+    float s, inv_s;
     const float *lse, *lse_lo, *g;
     void* dx;
-    int64_t ld_out, segs;
+    int64_t ld_out;
     cudaStream_t st;
     bool vin, vout, in_place;
 };
 
 template <flp::Dt D, bool VI, bool VO, bool IP>
-void launch_bwd(const BwdArgs& a, int grid) {
+void launch_bwd(const BwdArgs& a, dim3 grid) {
     flp::k_logp_bwd<D, VI, VO, IP><<<grid, flp::kBwdThreads, 0, a.st>>>(
-        a.x, a.n, a.v, a.ld, a.y, a.ii, a.mask, a.s, a.lse, a.lse_lo, a.g, a.dx, a.ld_out, a.segs);
+        a.x, a.n, a.v, a.ld, a.y, a.ii, a.mask, a.s, a.inv_s, a.lse, a.lse_lo, a.g, a.dx, a.ld_out);
 }
 
 template <flp::Dt D>
-void launch_backward_d(const BwdArgs& a, int grid) {
+void launch_backward_d(const BwdArgs& a, dim3 grid) {
     if (a.in_place) {
         if (a.vin) launch_bwd<D, true, true, true>(a, grid);
         else launch_bwd<D, false, false, true>(a, grid);
@@ -346,13 +346,12 @@ flp_status fused_logp_backward_ex(const void* logits, int dtype, int64_t n, int6
     if ((st = guard.enter(dev)) != FLP_OK) return st;
 
     const int64_t segs = ceil_div(v, flp::kBwdSegCols);
-    int64_t items;
-    if (__builtin_mul_overflow(n, segs, &items)) return fail(FLP_EINVAL, "n * segments overflows");
-    const BwdArgs a{logits, n, v, ld, targets, ignore_index, active_mask, inv_temperature, lse,
-                    lse_lo, grad, dlogits, ld_out, segs, reinterpret_cast<cudaStream_t>(stream),
-                    rows_aligned16(logits, ld, dtype), rows_aligned16(dlogits, ld_out, dtype),
-                    in_place};
-    const int grid = grid_for(items);
+    if (segs > kMaxGrid) return fail(FLP_EINVAL, "v too large for the backward grid");
+    const BwdArgs a{logits, n, v, ld, targets, ignore_index, active_mask, inv_temperature,
+                    1.f / inv_temperature, lse, lse_lo, grad, dlogits, ld_out,
+                    reinterpret_cast<cudaStream_t>(stream), rows_aligned16(logits, ld, dtype),
+                    rows_aligned16(dlogits, ld_out, dtype), in_place};
+    const dim3 grid((unsigned)segs, (unsigned)(n < 65535 ? n : 65535));
     if (dtype == FLP_DTYPE_BF16) launch_backward_d<flp::Dt::BF16>(a, grid);
     else if (dtype == FLP_DTYPE_F16) launch_backward_d<flp::Dt::F16>(a, grid);
     else launch_backward_d<flp::Dt::F32>(a, grid);

@@ -83,6 +83,9 @@ template <Dt D>
 constexpr int kFwdSmemBytes = kTiles * kStages * kStageBytes<D> + kTiles * kStages * 8;
 template <Dt D>
 constexpr int kFwdMinBlocks = (D == Dt::F32) ? 1 : 2;
+// backward CTAs of 256 threads per SM: register caps 48 (16-bit) and 64 (FP32)
+template <Dt D>
+constexpr int kBwdMinBlocks = (D == Dt::F32) ? 4 : 5;
 
 template <Dt D>
 __device__ __forceinline__ uint32_t elem_bits(const void* base, int64_t i) {
@@ -615,18 +618,9 @@ __device__ __forceinline__ void bwd_unit(const Unit<D>& u, const BwdRow& r, int6
                                          uint32_t (&o)[Unit<D>::kWords]) {
     const u64 l2e = f2(kLog2e, kLog2e);
     const u64 nln2hi = f2(-kLn2Hi, -kLn2Hi), nln2lo = f2(-kLn2Lo, -kLn2Lo);
-    float xt = 0.f;
-    const int kt = (int)(jt >> 1);
-    const bool has_t = jt >= 0 && jt < 8;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        const u64 xp = bwd_pair<D>(u, k, r);
-        if (k == kt) {
-            float lo, hi;
-            f2_split(xp, lo, hi);
-            xt = (jt & 1) ? hi : lo;
-        }
-        const u64 tt = f2_fma(xp, r.s2, r.neg_lr);
+        const u64 tt = f2_fma(bwd_pair<D>(u, k, r), r.s2, r.neg_lr);
         const u64 a = f2_mul(tt, l2e);
         const u64 c = f2_fma(a, nln2lo, f2_fma(a, nln2hi, tt));
         float a0, a1;
@@ -636,8 +630,17 @@ __device__ __forceinline__ void bwd_unit(const Unit<D>& u, const BwdRow& r, int6
         f2_split(f2_fma(q, c, q), d0, d1);
         put_pair<D>(o, k, d0, d1);
     }
-    if (has_t) {
+    if (jt >= 0 && jt < 8) {
         // target column: s g (1 - p) without cancellation, patched into its word
+        // (the element is picked by unrolled selects: no run-time index)
+        const int kt = (int)(jt >> 1);
+        float xt = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float lo, hi;
+            f2_split(bwd_pair<D>(u, k, r), lo, hi);
+            if (k == kt) xt = (jt & 1) ? hi : lo;
+        }
         const float dt = __fmul_rn(-r.gs, expm1f(__fsub_rn(__fmaf_rn(r.s, xt, -r.lr), r.delta)));
         if constexpr (D == Dt::F32) {
             // blend by masks (a predicated store per word would be folded into
@@ -705,31 +708,31 @@ __device__ __forceinline__ void bwd_store(char* dr, int64_t col, int64_t v,
     }
 }
 
-// Backward: one CTA per (row, segment of kBwdSegCols columns), elementwise.
+// Backward: one CTA per (segment of kBwdSegCols columns, row), elementwise.
 // Per active row: LSE = lse (+ lse_lo) is split as lse_r + delta with lse_r
 // on a 2^-16 grid, so that t = s x - lse_r is exact for the bulk of BF16
 // logits at s = 1 (one rounding otherwise); exp(t) = 2^a (1 + c) with
 // a = t log2 e rounded and c = t - a ln 2 recovered by two fused multiply-adds
 // against a two-float ln 2 (the rounding error of a, carried to first order);
 // coef = -s g (1 - delta) ~ -s g exp(-delta) folds s, g and delta in once per
-// row.  Logits below (LSE - 200) / s are raised to that bound first (their exp
-// is below e^-200, zero in binary32), which also keeps a -inf logit from
+// row.  Logits below about (LSE - 200) / s are raised to that bound first (their
+// exp is below e^-199, zero in binary32), which also keeps a -inf logit from
 // producing inf - inf.  The target column is s g (1 - p) = -s g expm1(s x - LSE),
 // without cancellation.  Values below 2^-126 flush to zero.  Each thread loads
 // its four units before computing any, so four (FP32: eight) 16-byte loads are
 // in flight per thread.
 template <Dt D, bool kVecIn, bool kVecOut, bool kInPlace>
-__global__ void __launch_bounds__(kBwdThreads)
+__global__ void __launch_bounds__(kBwdThreads, kBwdMinBlocks<D>)
 k_logp_bwd(const void* x, int64_t n, int64_t v, int64_t ld, const int64_t* __restrict__ y,
-           int64_t ignore_index, const uint8_t* __restrict__ mask, float s,
+           int64_t ignore_index, const uint8_t* __restrict__ mask, float s, float inv_s,
            const float* __restrict__ lse, const float* __restrict__ lse_lo,
-           const float* __restrict__ g, void* dx, int64_t ld_out, int64_t segs) {
+           const float* __restrict__ g, void* dx, int64_t ld_out) {
     constexpr int EB = Unit<D>::kElemBytes;
     constexpr int NW = Unit<D>::kWords;
-    const int64_t items = n * segs;
-    for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
-        const int64_t t = item / segs;
-        const int64_t col0 = (item - t * segs) * kBwdSegCols + (int64_t)threadIdx.x * 8;
+    // grid: x = segment of the row, y = row (strided when n > gridDim.y)
+    const int64_t col0 = (int64_t)blockIdx.x * kBwdSegCols + (int64_t)threadIdx.x * 8;
+#pragma unroll 1
+    for (int64_t t = blockIdx.y; t < n; t += gridDim.y) {
         const char* xr = reinterpret_cast<const char*>(x) + t * ld * EB;
         char* dr = reinterpret_cast<char*>(dx) + t * ld_out * EB;
         const int64_t yt = __ldg(y + t);
@@ -751,7 +754,7 @@ k_logp_bwd(const void* x, int64_t n, int64_t v, int64_t ld, const int64_t* __res
         r.lr = (fabsf(l) < 8388608.f) ? __fmul_rn(rintf(__fmul_rn(l, 65536.f)), 1.f / 65536.f) : l;
         r.delta = __fadd_rn(__fsub_rn(l, r.lr), l_lo);           // l - lr is exact
         const float coef = __fmaf_rn(r.gs, r.delta, -r.gs);       // -s g (1 - delta)
-        const float fl = __fdiv_rn(__fsub_rn(l, 200.f), s);       // (LSE - 200) / s
+        const float fl = __fmul_rn(__fsub_rn(l, 200.f), inv_s);   // ~ (LSE - 200) / s
         r.floor_f = fl;
         r.floor_w = 0xff80ff80u;
         if constexpr (D == Dt::BF16) {
