@@ -73,6 +73,8 @@ def _load():
                                                 V, I, _I64, _F64P, _I64P]
         lib.oracle_range_partials.argtypes = [V, I, _I64, _I64, _I64, _I64, _I64, D, _F64P, _F64P]
         lib.oracle_merge_partials.argtypes = [_F64P, _F64P, _I64, _I64, _F64P]
+        lib.oracle_grpo_loss.argtypes = [_F64P, _F64P, V, _F64P, V, V, _I64, _I64, I, D, D, D, D,
+                                         _F64P, _F64P]
         lib.oracle_num_threads.restype = ctypes.c_int
         _lib = lib
         return lib
@@ -235,3 +237,27 @@ def merge_partials(pm, ps) -> np.ndarray:
     lse = np.empty(n, dtype=np.float64)
     _load().oracle_merge_partials(pm, ps, n, k, lse)
     return lse
+
+
+GRPO_MODES = {"token_mean": 0, "seq_mean_token_mean": 1, "seq_mean_token_sum": 2}
+
+
+def grpo_loss(logp, old_logp, advantages, ref_logp=None, mask=None, cu_seqlens=None,
+              mode: str = "token_mean", eps_lo: float = 0.2, eps_hi: float = 0.2,
+              beta: float = 0.0, normalizer: float = 0.0):
+    """FP64 (loss, g[n]) of the clipped-surrogate GRPO loss on per-token logp
+    (definitions in logp_oracle.c, oracle_grpo_loss)."""
+    lp = np.ascontiguousarray(logp, dtype=np.float64)
+    n = lp.shape[0]
+    old = np.ascontiguousarray(old_logp, dtype=np.float64)
+    adv = np.ascontiguousarray(advantages, dtype=np.float64)
+    ref = None if ref_logp is None else np.ascontiguousarray(ref_logp, dtype=np.float64)
+    mk, mp = _mask(mask, n)
+    cu = None if cu_seqlens is None else np.ascontiguousarray(cu_seqlens, dtype=np.int64)
+    loss = np.zeros(1, dtype=np.float64)
+    g = np.empty(n, dtype=np.float64)
+    _load().oracle_grpo_loss(lp, old, None if ref is None else ref.ctypes.data, adv, mp,
+                             None if cu is None else cu.ctypes.data,
+                             0 if cu is None else cu.shape[0] - 1, n, GRPO_MODES[mode],
+                             float(eps_lo), float(eps_hi), float(beta), float(normalizer), loss, g)
+    return float(loss[0]), g

@@ -314,6 +314,82 @@ void oracle_range_partials(const void* x, int dtype, int64_t n, int64_t v, int64
     }
 }
 
+/* ---- GRPO loss on the logp path -------------------------------------------- */
+
+/* Issue #241 PR 5 names the objective (ratio, clip, KL, advantage) and three
+ * normalisers without formulas; this is the standard clipped-surrogate form:
+ * per active token t (mask byte nonzero, or every token when mask is NULL)
+ *   r_t  = exp(logp_t - old_t)
+ *   pg_t = max(-A_t r_t, -A_t clip(r_t, 1 - eps_lo, 1 + eps_hi))
+ *   kl_t = exp(ref_t - logp_t) - (ref_t - logp_t) - 1   (only if ref != NULL)
+ *   l_t  = pg_t + beta kl_t
+ * and the loss over sequences s = [cu[s], cu[s+1]) (n_s active tokens,
+ * S' = sequences with n_s > 0):
+ *   mode 0 token mean:               L = sum_t l_t / D,  D = sum_s n_s
+ *   mode 1 sequence mean of token means: L = (1/S') sum_s (sum_{t in s} l_t) / n_s
+ *   mode 2 sequence mean of token sums:  L = (1/S') sum_s sum_{t in s} l_t
+ * A positive `normalizer` replaces D (mode 0) or S' (modes 1, 2), as when the
+ * count is global across micro-batches.  With cu == NULL the whole batch is
+ * one sequence.  The gradient with respect to logp_t is
+ *   g_t = w_t (dpg_t + beta (1 - exp(ref_t - logp_t))),
+ *   dpg_t = -A_t r_t when the unclipped term is the max (ties included), else 0,
+ *   w_t = 1/D, 1/(S' n_s) or 1/S'; 0 for inactive tokens.
+ * Everything in double. */
+void oracle_grpo_loss(const double* logp, const double* old, const double* ref,
+                      const double* adv, const uint8_t* mask, const int64_t* cu, int64_t nseq,
+                      int64_t n, int mode, double eps_lo, double eps_hi, double beta,
+                      double normalizer, double* loss, double* g) {
+    int64_t one_cu[2] = {0, n};
+    if (cu == 0) {
+        cu = one_cu;
+        nseq = 1;
+    }
+    double tot = 0.0, d_tok = 0.0, s_act = 0.0, seq_terms = 0.0;
+    for (int64_t s = 0; s < nseq; ++s) {
+        double sum = 0.0, cnt = 0.0;
+        for (int64_t t = cu[s]; t < cu[s + 1]; ++t) {
+            if (mask && !mask[t]) continue;
+            double r = exp(logp[t] - old[t]);
+            double rc = r < 1.0 - eps_lo ? 1.0 - eps_lo : (r > 1.0 + eps_hi ? 1.0 + eps_hi : r);
+            double p1 = -adv[t] * r, p2 = -adv[t] * rc;
+            double l = p1 >= p2 ? p1 : p2;
+            if (ref) {
+                double dlt = ref[t] - logp[t];
+                l += beta * (exp(dlt) - dlt - 1.0);
+            }
+            sum += l;
+            cnt += 1.0;
+        }
+        tot += sum;
+        d_tok += cnt;
+        if (cnt > 0) {
+            s_act += 1.0;
+            seq_terms += (mode == 1) ? sum / cnt : sum;
+        }
+    }
+    double den = (mode == 0) ? d_tok : s_act;
+    if (normalizer > 0) den = normalizer;
+    double num = (mode == 0) ? tot : seq_terms;
+    *loss = den > 0 ? num / den : 0.0;
+    for (int64_t s = 0; s < nseq; ++s) {
+        double cnt = 0.0;
+        for (int64_t t = cu[s]; t < cu[s + 1]; ++t) cnt += (mask && !mask[t]) ? 0.0 : 1.0;
+        for (int64_t t = cu[s]; t < cu[s + 1]; ++t) {
+            if ((mask && !mask[t]) || den <= 0) {
+                g[t] = 0.0;
+                continue;
+            }
+            double w = (mode == 1) ? 1.0 / (den * cnt) : 1.0 / den;
+            double r = exp(logp[t] - old[t]);
+            double rc = r < 1.0 - eps_lo ? 1.0 - eps_lo : (r > 1.0 + eps_hi ? 1.0 + eps_hi : r);
+            double p1 = -adv[t] * r, p2 = -adv[t] * rc;
+            double d = p1 >= p2 ? -adv[t] * r : 0.0;
+            if (ref) d += beta * (1.0 - exp(ref[t] - logp[t]));
+            g[t] = w * d;
+        }
+    }
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

@@ -526,3 +526,103 @@ def test_scaled_range_partials_merge_to_scaled_lse():
     np.testing.assert_allclose(oracle.merge_partials(pm, ps), lse, rtol=1e-13)
     xv = oracle.bf16_to_f64(x)
     assert np.array_equal(pm[:, 0], (s * xv[:, :72]).max(axis=1))
+
+
+# ---------------------------------------------------------------- GRPO loss on the logp path
+
+
+def _grpo_case(rng, n=12):
+    lp = -rng.uniform(0.5, 6.0, n)
+    old = lp + rng.uniform(-0.6, 0.6, n)
+    ref = lp + rng.uniform(-0.5, 0.5, n)
+    adv = rng.standard_normal(n)
+    return lp, old, ref, adv
+
+
+def test_grpo_kl_zero_identity():
+    """logp == old_logp: every ratio is exactly 1, the clipped and unclipped
+    terms agree, pg = -A exactly and the gradient is -A times the weight."""
+    rng = np.random.default_rng(30)
+    lp, _, _, adv = _grpo_case(rng)
+    cu = np.array([0, 5, 12])
+    for mode, w in [("token_mean", np.full(12, 1 / 12)),
+                    ("seq_mean_token_mean", np.r_[np.full(5, 1 / 10), np.full(7, 1 / 14)]),
+                    ("seq_mean_token_sum", np.full(12, 1 / 2))]:
+        loss, g = oracle.grpo_loss(lp, lp, adv, cu_seqlens=cu, mode=mode)
+        assert np.array_equal(g, -adv * w)
+        assert abs(loss - np.sum(-adv * w)) < 1e-15
+
+
+def test_grpo_clip_branches_closed_forms():
+    eps = 0.2
+    cases = [  # (ratio, A, loss, dloss/dlogp)
+        (1.5, 2.0, -2.0 * 1.2, 0.0),          # clipped above: constant
+        (1.5, -2.0, 2.0 * 1.5, 2.0 * 1.5),    # negative advantage: unclipped term is the max
+        (0.5, 2.0, -2.0 * 0.5, -2.0 * 0.5),   # below 1 - eps with A > 0: unclipped is the max
+        (0.5, -2.0, 2.0 * 0.8, 0.0),          # below 1 - eps with A < 0: clipped, constant
+        (1.1, 3.0, -3.0 * 1.1, -3.0 * 1.1),   # inside the trust region
+    ]
+    for r, a, want_l, want_g in cases:
+        old = np.array([-2.0])
+        lp = old + math.log(r)
+        loss, g = oracle.grpo_loss(lp, old, np.array([a]), eps_lo=eps, eps_hi=eps)
+        assert abs(loss - want_l) < 1e-12 and abs(g[0] - want_g) < 1e-12, (r, a, loss, g)
+
+
+def test_grpo_kl_closed_form():
+    lp = np.array([-1.0, -2.0, -3.0])
+    d = np.array([0.0, 0.3, -0.4])
+    loss, g = oracle.grpo_loss(lp, lp, np.zeros(3), ref_logp=lp + d, beta=0.5)
+    kl = np.exp(d) - d - 1
+    assert abs(loss - 0.5 * kl.mean()) < 1e-15
+    np.testing.assert_allclose(g, 0.5 * (1 - np.exp(d)) / 3, rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("mode", ["token_mean", "seq_mean_token_mean", "seq_mean_token_sum"])
+def test_grpo_gradient_by_richardson_central_differences(mode):
+    rng = np.random.default_rng(31)
+    lp, old, ref, adv = _grpo_case(rng)
+    cu = np.array([0, 4, 4, 12])              # includes an empty sequence
+    mask = np.ones(12, np.uint8)
+    mask[[2, 9]] = 0
+    kw = dict(ref_logp=ref, mask=mask, cu_seqlens=cu, mode=mode, eps_lo=0.2, eps_hi=0.28,
+              beta=0.05)
+    _, g = oracle.grpo_loss(lp, old, adv, **kw)
+    r = np.exp(lp - old)
+    for t in range(12):
+        if min(abs(r[t] - 0.8), abs(r[t] - 1.28)) < 1e-3:
+            continue   # at a clip kink the derivative is one-sided
+        est = []
+        for h in (1e-4, 5e-5):
+            p, m = lp.copy(), lp.copy()
+            p[t] += h
+            m[t] -= h
+            est.append((oracle.grpo_loss(p, old, adv, **kw)[0] - oracle.grpo_loss(m, old, adv, **kw)[0])
+                       / (2 * h))
+        rich = (4 * est[1] - est[0]) / 3
+        assert abs(rich - g[t]) < 1e-9, (mode, t, rich, g[t])
+    assert g[2] == 0 and g[9] == 0
+
+
+def test_grpo_reduction_invariants():
+    rng = np.random.default_rng(32)
+    lp, old, ref, adv = _grpo_case(rng, n=12)
+    cu = np.array([0, 4, 8, 12])              # equal lengths
+    l0, g0 = oracle.grpo_loss(lp, old, adv, ref_logp=ref, beta=0.1, cu_seqlens=cu)
+    l1, g1 = oracle.grpo_loss(lp, old, adv, ref_logp=ref, beta=0.1, cu_seqlens=cu,
+                              mode="seq_mean_token_mean")
+    l2, g2 = oracle.grpo_loss(lp, old, adv, ref_logp=ref, beta=0.1, cu_seqlens=cu,
+                              mode="seq_mean_token_sum")
+    assert abs(l0 - l1) < 1e-14 and np.allclose(g0, g1, rtol=1e-14, atol=0)
+    assert abs(l2 - 4 * l0) < 1e-13 and np.allclose(g2, 4 * g0, rtol=1e-14, atol=0)
+    # a masked token is the same as a removed one
+    mask = np.ones(12, np.uint8)
+    mask[5] = 0
+    lm, gm = oracle.grpo_loss(lp, old, adv, mask=mask)
+    keep = np.arange(12) != 5
+    lr, gr = oracle.grpo_loss(lp[keep], old[keep], adv[keep])
+    assert abs(lm - lr) < 1e-15 and np.allclose(gm[keep], gr, rtol=1e-14, atol=0) and gm[5] == 0
+    # a global normaliser rescales
+    ln, gn = oracle.grpo_loss(lp, old, adv, normalizer=48.0)
+    la, ga = oracle.grpo_loss(lp, old, adv)
+    assert abs(ln - la / 4) < 1e-15 and np.allclose(gn, ga / 4, rtol=1e-14, atol=0)
