@@ -197,6 +197,46 @@ flp_status logp_merge_partials_ex(const float* part_max, const float* part_sum, 
                                   flp_stream_t stream);
 
 /*
+ * GRPO loss on the logp path (issue #241 PR 5: ratio, clip, KL, advantage,
+ * a declared normaliser and a fixed summation order; the pages name these
+ * terms, the formulas below are the standard clipped-surrogate form).
+ * Per active token t (active_mask byte nonzero, or all when NULL):
+ *   r = exp(logp - old_logp),
+ *   pg = max(-A r, -A clip(r, 1 - eps_lo, 1 + eps_hi)),
+ *   kl = exp(ref - logp) - (ref - logp) - 1 (only if ref_logp != NULL),
+ *   l = pg + beta kl.
+ * mode FLP_GRPO_TOKEN_MEAN:          loss = sum_t l / D (D = active tokens)
+ *      FLP_GRPO_SEQ_MEAN_TOKEN_MEAN: loss = mean over non-empty sequences of
+ *                                    the sequence's mean l
+ *      FLP_GRPO_SEQ_MEAN_TOKEN_SUM:  loss = mean over non-empty sequences of
+ *                                    the sequence's summed l
+ * Sequences are [cu_seqlens[s], cu_seqlens[s+1]) for s < num_seqs (int64 on
+ * the device; bounds are clamped to [0, n]); with cu_seqlens == NULL the whole
+ * batch is one sequence.  normalizer > 0 replaces D (token mean) or the
+ * sequence count, e.g. by a count global to all micro-batches.
+ *   loss       [1] FP32 out
+ *   grad       [n] FP32 out: d loss / d logp (the unclipped term's -A r when
+ *              it is the max, ties included, else 0; plus beta (1 - e^(ref -
+ *              logp)); times the token's normaliser weight; 0 when inactive)
+ *              -- the upstream gradient for fused_logp_backward.
+ *   token_loss [n] FP32 out or NULL: l per token (0 when inactive).
+ * Deterministic: one CTA, fixed xor trees within sequences and a fixed fold
+ * over warps; with logp == old_logp the ratio is exactly 1 and
+ * grad = -A times the weight (the KL = 0 identity of PR 5).
+ * Errors: FLP_EINVAL for a bad mode, eps_lo outside [0, 1), a negative or
+ * non-finite eps_hi, beta or normalizer, or a sequence mode without
+ * sequences.
+ */
+#define FLP_GRPO_TOKEN_MEAN 0
+#define FLP_GRPO_SEQ_MEAN_TOKEN_MEAN 1
+#define FLP_GRPO_SEQ_MEAN_TOKEN_SUM 2
+flp_status logp_grpo_loss(const float* logp, const float* old_logp, const float* ref_logp,
+                          const float* advantages, const uint8_t* active_mask,
+                          const int64_t* cu_seqlens, int64_t num_seqs, int64_t n, int mode,
+                          float eps_lo, float eps_hi, float beta, float normalizer, float* loss,
+                          float* grad, float* token_loss, flp_stream_t stream);
+
+/*
  * Health of the device side (no counterpart in the pages: a guard of this
  * library's own waits).  The bulk-copy forward waits on its own copies with a
  * bounded wait (about 2 s); if one runs out, the kernel records it in a

@@ -51,9 +51,11 @@ __all__ = [
     "fused_logp",
     "fused_logp_backward",
     "fused_logp_forward",
+    "logp_grpo_loss",
     "logp_merge_partials",
     "logp_shard_partials",
 ]
+GRPO_MODES = {"token_mean": 0, "seq_mean_token_mean": 1, "seq_mean_token_sum": 2}
 
 
 def _stream(t: torch.Tensor) -> int:
@@ -256,6 +258,42 @@ def logp_merge_partials(part_max: torch.Tensor, part_sum: torch.Tensor, sel: tor
                                                 _stream(targets))
         _lib.check("logp_merge_partials", st)
     return (logp, lse, lse_lo) if want_lo else (logp, lse)
+
+
+def logp_grpo_loss(logp: torch.Tensor, old_logp: torch.Tensor, advantages: torch.Tensor,
+                   ref_logp: torch.Tensor | None = None, active_mask: torch.Tensor | None = None,
+                   cu_seqlens: torch.Tensor | None = None, mode: str = "token_mean",
+                   eps_lo: float = 0.2, eps_hi: float = 0.2, beta: float = 0.0,
+                   normalizer: float = 0.0, token_loss: bool = False):
+    """GRPO clipped-surrogate loss of per-token logp: (loss FP32 [1], grad
+    FP32 [N] = d loss / d logp) [+ per-token loss FP32 [N] if token_loss].
+    ``grad`` is the upstream gradient for ``fused_logp_backward``."""
+    n = logp.shape[0] if logp.dim() == 1 else -1
+    for name, t in (("logp", logp), ("old_logp", old_logp), ("advantages", advantages)):
+        _vec(t, name, n, torch.float32)
+        _cuda(t)
+    if ref_logp is not None:
+        _vec(ref_logp, "ref_logp", n, torch.float32)
+        _cuda(ref_logp)
+    mp = _mask(active_mask, n)
+    nseq = 0
+    if cu_seqlens is not None:
+        if cu_seqlens.dtype != torch.int64 or cu_seqlens.dim() != 1 or cu_seqlens.shape[0] < 1:
+            raise ValueError("cu_seqlens must be an int64 [S + 1] tensor")
+        _cuda(cu_seqlens)
+        cu_seqlens = cu_seqlens.contiguous()
+        nseq = cu_seqlens.shape[0] - 1
+    dev = logp.device
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    grad = torch.empty(n, dtype=torch.float32, device=dev)
+    tl = torch.empty(n, dtype=torch.float32, device=dev) if token_loss else None
+    st = _lib.load().logp_grpo_loss(logp.data_ptr(), old_logp.data_ptr(), _opt_ptr(ref_logp),
+                                    advantages.data_ptr(), mp, _opt_ptr(cu_seqlens), nseq, n,
+                                    GRPO_MODES[mode], float(eps_lo), float(eps_hi), float(beta),
+                                    float(normalizer), loss.data_ptr(), grad.data_ptr(),
+                                    _opt_ptr(tl), _stream(logp))
+    _lib.check("logp_grpo_loss", st)
+    return (loss, grad, tl) if token_loss else (loss, grad)
 
 
 class FusedLogp(torch.autograd.Function):

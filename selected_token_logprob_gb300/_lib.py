@@ -38,6 +38,9 @@ SIGNATURES = {
                                               ctypes.c_float, _P, _P, _P, _P, _P]),
     "logp_merge_partials_ex": (ctypes.c_int, [_P, _P, _P, _P, _I64, _P, _I64, _I64,
                                               ctypes.c_float, _P, _P, _P, _P]),
+    "logp_grpo_loss": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, ctypes.c_int,
+                                      ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                      ctypes.c_float, _P, _P, _P, _P]),
     "flp_device_error": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_int)]),
     "flp_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_int, _I64, ctypes.POINTER(ctypes.c_int)]),
 }

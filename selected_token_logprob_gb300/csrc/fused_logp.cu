@@ -9,6 +9,7 @@
 #include <stdio.h>
 
 #include "fused_logp.h"
+#include "grpo_kernels.cuh"
 #include "logp_kernels.cuh"
 
 namespace {
@@ -197,9 +198,11 @@ flp_status launch_forward(const FwdArgs& a) {
     return check_launch("forward");
 }
 
+// The exponent argument always uses the two-float s log2(e) (also at s = 1,
+// where it removes the rounding of log2(e) to binary32 from every term).
 template <flp::Dt D>
 flp_status launch_forward_d(const FwdArgs& a) {
-    return a.sc.s == 1.f ? launch_forward<D, false>(a) : launch_forward<D, true>(a);
+    return launch_forward<D, true>(a);
 }
 
 struct BwdArgs {
@@ -253,14 +256,8 @@ void launch_part(const PartArgs& a) {
 
 template <flp::Dt D>
 void launch_partials_d(const PartArgs& a) {
-    const bool scaled = a.sc.s != 1.f;
-    if (a.vec) {
-        if (scaled) launch_part<D, true, true>(a);
-        else launch_part<D, true, false>(a);
-    } else {
-        if (scaled) launch_part<D, false, true>(a);
-        else launch_part<D, false, false>(a);
-    }
+    if (a.vec) launch_part<D, true, true>(a);
+    else launch_part<D, false, true>(a);
 }
 
 }  // namespace
@@ -451,6 +448,42 @@ flp_status logp_merge_partials(const float* part_max, const float* part_sum, con
                                flp_stream_t stream) {
     return logp_merge_partials_ex(part_max, part_sum, sel, targets, ignore_index, nullptr, n,
                                   v_total, 1.f, logp, lse, lse_lo, stream);
+}
+
+flp_status logp_grpo_loss(const float* logp, const float* old_logp, const float* ref_logp,
+                          const float* advantages, const uint8_t* active_mask,
+                          const int64_t* cu_seqlens, int64_t num_seqs, int64_t n, int mode,
+                          float eps_lo, float eps_hi, float beta, float normalizer, float* loss,
+                          float* grad, float* token_loss, flp_stream_t stream) {
+    flp_status st;
+    if (n < 0) return fail(FLP_EINVAL, "n must be >= 0 (got %lld)", (long long)n);
+    if (mode < FLP_GRPO_TOKEN_MEAN || mode > FLP_GRPO_SEQ_MEAN_TOKEN_SUM)
+        return fail(FLP_EINVAL, "mode must be 0, 1 or 2 (got %d)", mode);
+    if (!(eps_lo >= 0.f && eps_lo < 1.f) || !(eps_hi >= 0.f) || !isfinite(eps_hi))
+        return fail(FLP_EINVAL, "clip range needs 0 <= eps_lo < 1 and finite eps_hi >= 0");
+    if (!isfinite(beta) || !isfinite(normalizer) || normalizer < 0.f)
+        return fail(FLP_EINVAL, "beta and normalizer must be finite, normalizer >= 0");
+    if (cu_seqlens && num_seqs < 0) return fail(FLP_EINVAL, "num_seqs must be >= 0");
+    if (!cu_seqlens && mode != FLP_GRPO_TOKEN_MEAN && num_seqs != 0 && num_seqs != 1)
+        return fail(FLP_EINVAL, "sequence normalisers need cu_seqlens (or the whole batch as one sequence)");
+    const void* ptrs[] = {logp, old_logp, advantages, loss, grad, ref_logp, active_mask, cu_seqlens, token_loss};
+    const char* names[] = {"logp", "old_logp", "advantages", "loss", "grad", "ref_logp", "active_mask",
+                           "cu_seqlens", "token_loss"};
+    const bool optional[] = {false, false, false, false, false, true, true, true, true};
+    const int count = n == 0 ? 4 : 9;   // with n == 0 only the loss is written
+    const void* ptrs0[] = {loss};
+    const char* names0[] = {"loss"};
+    int dev;
+    if ((st = n == 0 ? common_device(1, ptrs0, names0, nullptr, &dev)
+                     : common_device(count, ptrs, names, optional, &dev)) != FLP_OK)
+        return st;
+    DeviceGuard guard;
+    if ((st = guard.enter(dev)) != FLP_OK) return st;
+    const flp::GrpoArgs a{logp, old_logp, ref_logp, advantages, active_mask, cu_seqlens,
+                          cu_seqlens ? num_seqs : 0, n, mode, eps_lo, eps_hi, beta, normalizer,
+                          loss, grad, token_loss};
+    flp::k_grpo_loss<<<1, flp::kGrpoThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a);
+    return check_launch("grpo loss");
 }
 
 flp_status flp_device_error(int device, int* code) {

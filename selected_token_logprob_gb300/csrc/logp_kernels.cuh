@@ -38,8 +38,8 @@ constexpr int kFwdThreads = kTiles * kWarp;  // one warp per tile
 constexpr int kGroup = 4;                    // units per lane per online step
 constexpr int kGroupUnits = kWarp * kGroup;  // units of a tile per group (128)
 constexpr int kStages = 3;                   // bulk-copy ring depth per warp
-constexpr int kBwdThreads = 256;
-constexpr int kBwdUnitsPerThread = 4;
+constexpr int kBwdThreads = 128;
+constexpr int kBwdUnitsPerThread = 8;
 constexpr int64_t kBwdSegCols = (int64_t)kBwdThreads * kBwdUnitsPerThread * 8;
 // Bounded waits give up after this many SM cycles (about 2 s at 2 GHz).
 constexpr long long kWaitLimitCycles = 4000000000LL;
@@ -83,9 +83,9 @@ template <Dt D>
 constexpr int kFwdSmemBytes = kTiles * kStages * kStageBytes<D> + kTiles * kStages * 8;
 template <Dt D>
 constexpr int kFwdMinBlocks = (D == Dt::F32) ? 1 : 2;
-// backward CTAs of 256 threads per SM: register caps 48 (16-bit) and 64 (FP32)
+// backward CTAs of 128 threads per SM: register caps 64 (16-bit) and 96 (FP32)
 template <Dt D>
-constexpr int kBwdMinBlocks = (D == Dt::F32) ? 4 : 5;
+constexpr int kBwdMinBlocks = (D == Dt::F32) ? 5 : 8;
 
 template <Dt D>
 __device__ __forceinline__ uint32_t elem_bits(const void* base, int64_t i) {
@@ -719,8 +719,8 @@ __device__ __forceinline__ void bwd_store(char* dr, int64_t col, int64_t v,
 // exp is below e^-199, zero in binary32), which also keeps a -inf logit from
 // producing inf - inf.  The target column is s g (1 - p) = -s g expm1(s x - LSE),
 // without cancellation.  Values below 2^-126 flush to zero.  Each thread loads
-// its four units before computing any, so four (FP32: eight) 16-byte loads are
-// in flight per thread.
+// its eight units before computing any, so eight (FP32: sixteen) 16-byte loads
+// are in flight per thread.
 template <Dt D, bool kVecIn, bool kVecOut, bool kInPlace>
 __global__ void __launch_bounds__(kBwdThreads, kBwdMinBlocks<D>)
 k_logp_bwd(const void* x, int64_t n, int64_t v, int64_t ld, const int64_t* __restrict__ y,
@@ -765,17 +765,18 @@ k_logp_bwd(const void* x, int64_t n, int64_t v, int64_t ld, const int64_t* __res
         r.s2 = f2(s, s);
         r.coef2 = f2(coef, coef);
 
-        Unit<D> w0, w1, w2, w3;
-        static_assert(kBwdUnitsPerThread == 4, "four units per thread");
-        if (col0 < v) bwd_load<D, kVecIn, kInPlace>(xr, col0, v, w0);
-        if (col0 + cs < v) bwd_load<D, kVecIn, kInPlace>(xr, col0 + cs, v, w1);
-        if (col0 + 2 * cs < v) bwd_load<D, kVecIn, kInPlace>(xr, col0 + 2 * cs, v, w2);
-        if (col0 + 3 * cs < v) bwd_load<D, kVecIn, kInPlace>(xr, col0 + 3 * cs, v, w3);
-        uint32_t o[NW];
-        if (col0 < v) { bwd_unit<D>(w0, r, yt - col0, o); bwd_store<D, kVecOut>(dr, col0, v, o); }
-        if (col0 + cs < v) { bwd_unit<D>(w1, r, yt - (col0 + cs), o); bwd_store<D, kVecOut>(dr, col0 + cs, v, o); }
-        if (col0 + 2 * cs < v) { bwd_unit<D>(w2, r, yt - (col0 + 2 * cs), o); bwd_store<D, kVecOut>(dr, col0 + 2 * cs, v, o); }
-        if (col0 + 3 * cs < v) { bwd_unit<D>(w3, r, yt - (col0 + 3 * cs), o); bwd_store<D, kVecOut>(dr, col0 + 3 * cs, v, o); }
+        Unit<D> w[kBwdUnitsPerThread];
+#pragma unroll
+        for (int u = 0; u < kBwdUnitsPerThread; ++u)
+            if (col0 + u * cs < v) bwd_load<D, kVecIn, kInPlace>(xr, col0 + u * cs, v, w[u]);
+#pragma unroll
+        for (int u = 0; u < kBwdUnitsPerThread; ++u) {
+            if (col0 + u * cs < v) {
+                uint32_t o[NW];
+                bwd_unit<D>(w[u], r, yt - (col0 + u * cs), o);
+                bwd_store<D, kVecOut>(dr, col0 + u * cs, v, o);
+            }
+        }
     }
 }
 
