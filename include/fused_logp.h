@@ -254,6 +254,17 @@ flp_status flp_device_error(int device, int* code);
  */
 flp_status flp_selftest_wait_timeout(int device, int64_t limit_cycles, int* timed_out);
 
+/*
+ * Self-test of the exp2 bias correction (no counterpart in the pages).  The
+ * forward sums terms 2^a from the special-function unit's ex2.approx, whose
+ * results are low by a nearly constant ~5e-8 relative; each tile sum is
+ * scaled by (1 + c) to remove it.  This measures the mean relative error of
+ * ex2.approx over 2^20 arguments in [-24, 0) on `device` (synchronising) and
+ * returns it with the compiled-in c, so a test can check that c still
+ * matches the hardware (mean_rel_err ~ -c).
+ */
+flp_status flp_selftest_ex2_bias(int device, double* mean_rel_err, double* compensation);
+
 #ifdef __cplusplus
 }
 #endif

@@ -46,6 +46,7 @@ __all__ = [
     "IGNORE_INDEX",
     "NUM_TILES",
     "flp_device_error",
+    "flp_selftest_ex2_bias",
     "flp_selftest_wait_timeout",
     "flp_tile_width",
     "fused_logp",
@@ -346,3 +347,14 @@ def flp_selftest_wait_timeout(device: int = 0, limit_cycles: int = 200000) -> in
     _lib.check("flp_selftest_wait_timeout",
                _lib.load().flp_selftest_wait_timeout(int(device), int(limit_cycles), ctypes.byref(out)))
     return out.value
+
+
+def flp_selftest_ex2_bias(device: int = 0):
+    """(measured mean relative error of the hardware exp2 approximation, the
+    compiled-in compensation); the compensation is right when they cancel."""
+    import ctypes
+
+    m, c = ctypes.c_double(0.0), ctypes.c_double(0.0)
+    _lib.check("flp_selftest_ex2_bias",
+               _lib.load().flp_selftest_ex2_bias(int(device), ctypes.byref(m), ctypes.byref(c)))
+    return m.value, c.value

@@ -43,6 +43,8 @@ SIGNATURES = {
                                       ctypes.c_float, _P, _P, _P, _P]),
     "flp_device_error": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_int)]),
     "flp_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_int, _I64, ctypes.POINTER(ctypes.c_int)]),
+    "flp_selftest_ex2_bias": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_double),
+                                             ctypes.POINTER(ctypes.c_double)]),
 }
 
 

@@ -499,6 +499,23 @@ flp_status flp_device_error(int device, int* code) {
     return ok();
 }
 
+flp_status flp_selftest_ex2_bias(int device, double* mean_rel_err, double* compensation) {
+    if (mean_rel_err == nullptr || compensation == nullptr)
+        return fail(FLP_EINVAL, "output pointers must not be null");
+    DeviceGuard guard;
+    flp_status st = guard.enter(device);
+    if (st != FLP_OK) return st;
+    flp::k_ex2_bias_selftest<<<1, 1024>>>();
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    double v = 0.0;
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&v, flp::g_ex2_bias, sizeof v);
+    if (e != cudaSuccess) return fail(FLP_ECUDA, "self-test: %s", cudaGetErrorString(e));
+    *mean_rel_err = v;
+    *compensation = (double)flp::kEx2BiasComp;
+    return ok();
+}
+
 flp_status flp_selftest_wait_timeout(int device, int64_t limit_cycles, int* timed_out) {
     if (timed_out == nullptr) return fail(FLP_EINVAL, "timed_out is a null pointer");
     if (limit_cycles < 0 || limit_cycles > 100000000)

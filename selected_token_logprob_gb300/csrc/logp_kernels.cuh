@@ -52,6 +52,12 @@ constexpr float kLn2Hi = (float)kLn2;
 constexpr float kLn2Lo = (float)(kLn2 - (double)kLn2Hi);
 constexpr float kLog2e = (float)(1.0 / kLn2);
 
+// Mean relative error of ex2.approx.ftz.f32 on this GPU family: -4.95e-8
+// (measured over 4M arguments in [-24, 0]; flat in the argument; re-measured
+// by flp_selftest_ex2_bias).  Every tile sum is built from such terms, so it
+// is scaled by (1 + kEx2BiasComp) once, in tile_partial.
+constexpr float kEx2BiasComp = 4.95e-8f;
+
 // Sticky device error word: 1 = a bounded wait ran out.  Read and cleared by
 // flp_device_error().
 __device__ int g_device_error;
@@ -294,6 +300,17 @@ __device__ __forceinline__ MS warp_merge(MS p, const Scale& sc) {
     return p;
 }
 
+// The partial of a whole tile: the warp butterfly of the lane pairs, with the
+// sum corrected for the mean bias of the special-function unit's exp2 (one
+// fused multiply-add).  Every path (forward, plain forward, shard partials)
+// forms tile partials here, so they stay bitwise equal.
+template <bool kScaled>
+__device__ __forceinline__ MS tile_partial(MS lane_pair, const Scale& sc) {
+    MS p = warp_merge<kScaled>(lane_pair, sc);
+    p.s = __fmaf_rn(p.s, kEx2BiasComp, p.s);
+    return p;
+}
+
 // Merge of the 16 tile partials of one row held by a 16-lane half warp
 // (lane k of the half holds tile k; tiles beyond the vocabulary hold the
 // identity (-inf, 0)).  M = max m_k; S = sum_k s_k exp(s (m_k - M)) summed as
@@ -354,8 +371,7 @@ k_logp_fwd(const void* __restrict__ x, int64_t n, int64_t v, int64_t ld, int64_t
         }
         const int64_t c0 = (int64_t)warp * W;
         const int64_t width = c0 >= v ? 0 : (v - c0 < W ? v - c0 : W);
-        MS p = tile_scan<D, false, kScaled>(xr + c0 * EB, width, lane, sc);
-        p = warp_merge<kScaled>(p, sc);
+        const MS p = tile_partial<kScaled>(tile_scan<D, false, kScaled>(xr + c0 * EB, width, lane, sc), sc);
         if (lane == 0) {
             sh_m[warp] = p.m;
             sh_s[warp] = p.s;
@@ -497,7 +513,7 @@ k_logp_fwd_bulk(const void* __restrict__ x, int64_t n, int64_t v, int64_t ld, in
                 phase ^= 1u;
             }
         }
-        MS p = warp_merge<kScaled>(MS{m, s}, sc);
+        const MS p = tile_partial<kScaled>(MS{m, s}, sc);
         if (lane == 0) {
             sh_m[j & 1][warp] = p.m;
             sh_s[j & 1][warp] = p.s;
@@ -536,8 +552,7 @@ k_logp_partials(const void* __restrict__ xs, int64_t n, int64_t ld, int64_t real
         }
         const int64_t c0 = (int64_t)warp * W;
         const int64_t width = real_width - c0 < W ? real_width - c0 : W;
-        MS p = tile_scan<D, kVec, kScaled>(xr + c0 * EB, width, lane, sc);
-        p = warp_merge<kScaled>(p, sc);
+        const MS p = tile_partial<kScaled>(tile_scan<D, kVec, kScaled>(xr + c0 * EB, width, lane, sc), sc);
         if (lane == 0) {
             pm[t * kTiles + tile0 + warp] = p.m;
             ps[t * kTiles + tile0 + warp] = p.s;
@@ -715,7 +730,7 @@ __device__ __forceinline__ void bwd_store(char* dr, int64_t col, int64_t v,
 // a = t log2 e rounded and c = t - a ln 2 recovered by two fused multiply-adds
 // against a two-float ln 2 (the rounding error of a, carried to first order);
 // coef = -s g (1 - delta) ~ -s g exp(-delta) folds s, g and delta in once per
-// row.  Logits below about (LSE - 200) / s are raised to that bound first (their
+// row, with the exp2 bias correction.  Logits below about (LSE - 200) / s are raised to that bound first (their
 // exp is below e^-199, zero in binary32), which also keeps a -inf logit from
 // producing inf - inf.  The target column is s g (1 - p) = -s g expm1(s x - LSE),
 // without cancellation.  Values below 2^-126 flush to zero.  Each thread loads
@@ -753,7 +768,8 @@ k_logp_bwd(const void* x, int64_t n, int64_t v, int64_t ld, const int64_t* __res
         r.gs = __fmul_rn(s, __ldg(g + t));
         r.lr = (fabsf(l) < 8388608.f) ? __fmul_rn(rintf(__fmul_rn(l, 65536.f)), 1.f / 65536.f) : l;
         r.delta = __fadd_rn(__fsub_rn(l, r.lr), l_lo);           // l - lr is exact
-        const float coef = __fmaf_rn(r.gs, r.delta, -r.gs);       // -s g (1 - delta)
+        // -s g (1 - delta), times (1 + b) for the mean bias b of ex2.approx
+        const float coef = __fmaf_rn(r.gs, __fsub_rn(r.delta, kEx2BiasComp), -r.gs);
         const float fl = __fmul_rn(__fsub_rn(l, 200.f), inv_s);   // ~ (LSE - 200) / s
         r.floor_f = fl;
         r.floor_w = 0xff80ff80u;
@@ -777,6 +793,28 @@ k_logp_bwd(const void* x, int64_t n, int64_t v, int64_t ld, const int64_t* __res
                 bwd_store<D, kVecOut>(dr, col0 + u * cs, v, o);
             }
         }
+    }
+}
+
+// Mean relative error of ex2.approx.ftz.f32 against the double exp2 over a
+// fixed grid of 2^20 arguments in [-24, 0) (one CTA; fixed reduction order).
+__device__ double g_ex2_bias;
+__global__ void __launch_bounds__(1024) k_ex2_bias_selftest() {
+    __shared__ double sh[32];
+    double acc = 0.0;
+    for (int i = threadIdx.x; i < (1 << 20); i += 1024) {
+        const float a = -24.0f * (float)i / (float)(1 << 20) - 1.0e-6f * (float)(i & 1023);
+        const double ref = exp2((double)a);
+        acc += ((double)ex2_ftz(a) - ref) / ref;
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double t = 0.0;
+        for (int w = 0; w < 32; ++w) t += sh[w];
+        g_ex2_bias = t / (double)(1 << 20);
     }
 }
 

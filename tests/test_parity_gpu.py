@@ -233,6 +233,14 @@ def test_lse_residual_is_the_rounding_error():
     assert err_sum.max() < 5e-7 and np.mean(err_sum) < np.mean(err_hi)
 
 
+def test_ex2_bias_compensation_matches_hardware():
+    """The forward's tile sums are scaled by (1 + c) to undo the mean bias of
+    the hardware exp2 approximation; c must still match this GPU."""
+    mean_rel, comp = flp.flp_selftest_ex2_bias(0)
+    print("ex2.approx mean relative error", mean_rel, "compensation", comp)
+    assert abs(mean_rel + comp) < 1.5e-8, (mean_rel, comp)
+
+
 def test_device_error_word_and_wait_selftest():
     x, y, g = workloads.make("mid", device=DEV, n=64)
     run(x, y, g)
