@@ -75,6 +75,8 @@ def _load():
         lib.oracle_merge_partials.argtypes = [_F64P, _F64P, _I64, _I64, _F64P]
         lib.oracle_grpo_loss.argtypes = [_F64P, _F64P, V, _F64P, V, V, _I64, _I64, I, D, D, D, D,
                                          _F64P, _F64P]
+        lib.oracle_linear_logp.argtypes = [_U16P, _I64, _U16P, _I64, _I64, _I64, _I64, _I64P, _I64,
+                                           V, D, _F64P, _F64P, V]
         lib.oracle_num_threads.restype = ctypes.c_int
         _lib = lib
         return lib
@@ -215,6 +217,31 @@ def backward_compare(x, y, g, dl, ignore_index: int = -100, v: int | None = None
         "n_not_correctly_rounded": int(counts[1]),
         "n_nonfinite": int(counts[2]),
     }
+
+
+def linear_logp(h, w, y, ignore_index: int = -100, d: int | None = None, scale: float = 1.0,
+                mask=None, with_bound: bool = False):
+    """FP64 (logp[n], lse[n]) of the logits z = h[:, :d] @ w[:, :d].T (h [n, ldh]
+    and w [v, ldw] as BF16 bit patterns), scaled by `scale` (1/temperature);
+    with `with_bound`, also max_j sum_k |h_k w_jk| per row."""
+    h, w = _u16(h), _u16(w)
+    if h.ndim != 2 or w.ndim != 2:
+        raise ValueError("hidden and weight must be 2-D")
+    n, ldh = h.shape
+    v, ldw = w.shape
+    d = min(ldh, ldw) if d is None else int(d)
+    if d > ldh or d > ldw:
+        raise ValueError("d exceeds a row stride")
+    y = np.ascontiguousarray(y, dtype=np.int64)
+    if y.shape != (n,):
+        raise ValueError("targets must have shape [n]")
+    mk, mp = _mask(mask, n)
+    logp = np.empty(n, dtype=np.float64)
+    lse = np.empty(n, dtype=np.float64)
+    bound = np.empty(n, dtype=np.float64) if with_bound else None
+    _load().oracle_linear_logp(h, ldh, w, ldw, n, d, v, y, ignore_index, mp, float(scale), logp, lse,
+                               bound.ctypes.data if with_bound else None)
+    return (logp, lse, bound) if with_bound else (logp, lse)
 
 
 def range_partials(x, w: int, k: int, v: int | None = None, dtype: str | None = None,

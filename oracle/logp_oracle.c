@@ -31,10 +31,13 @@
  *     and 0.7), so LSE = log sum exp(s x), logp = s x_y - LSE and, by the chain
  *     rule, d = s g (onehot - exp(s x - LSE));
  *   - an explicit active-row mask (PR #314, MaskMode explicit_active_mask):
- *     a row is active only if its mask byte is nonzero.
+ *     a row is active only if its mask byte is nonzero;
+ *   - the fused LM head (linear_logp): the logits are formed from hidden
+ *     states and weight rows first (oracle_linear_logp).
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 #ifdef _OPENMP
 #include <omp.h>
@@ -311,6 +314,51 @@ void oracle_range_partials(const void* x, int dtype, int64_t n, int64_t v, int64
             if (c1 > v) c1 = v;
             range_max_sumexp(x, dtype, ld, t, c0, c1, s, &pm[t * k + j], &ps[t * k + j]);
         }
+    }
+}
+
+/* ---- fused LM head + logp ------------------------------------------------- */
+
+/* linear_logp (named in RL-Kernel PR #495, Summary, among the ops that PR
+ * leaves alone; the pages give no formula): the logits are the LM-head
+ * contraction z[t, j] = sum_k h[t, k] w[j, k] of the BF16 hidden states
+ * h [n, d] (row stride ldh) with the BF16 weight rows w [v, d] (row stride
+ * ldw), and the selected-token logprob of issue #241 (Background, Goal) is
+ * taken of s z.  Per row, in double: every z_j (a product of two BF16 values
+ * is exact in double), then the plain two-pass LSE = M + log sum exp(s z_j - M),
+ * logp = s z_y - LSE for active rows, else 0.  bound[t] (if not NULL) is
+ * max_j sum_k |h[t, k] w[j, k]|: the scale of the rounding error of any
+ * binary32 evaluation of the row's logits, for the tests' tolerance. */
+void oracle_linear_logp(const uint16_t* h, int64_t ldh, const uint16_t* w, int64_t ldw,
+                        int64_t n, int64_t d, int64_t v, const int64_t* y, int64_t ignore_index,
+                        const uint8_t* mask, double s, double* logp, double* lse, double* bound) {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t t = 0; t < n; ++t) {
+        double* hz = (double*)malloc(sizeof(double) * (size_t)(d + v));
+        double* z = hz + d;
+        for (int64_t k = 0; k < d; ++k) hz[k] = bf16_bits_to_double(h[t * ldh + k]);
+        double babs = 0.0;
+        for (int64_t j = 0; j < v; ++j) {
+            const uint16_t* wj = w + j * ldw;
+            double acc = 0.0, aabs = 0.0;
+            for (int64_t k = 0; k < d; ++k) {
+                const double p = hz[k] * bf16_bits_to_double(wj[k]);
+                acc += p;
+                aabs += fabs(p);
+            }
+            z[j] = acc;
+            if (aabs > babs) babs = aabs;
+        }
+        double m = -INFINITY;
+        for (int64_t j = 0; j < v; ++j)
+            if (s * z[j] > m) m = s * z[j];
+        double acc = 0.0;
+        for (int64_t j = 0; j < v; ++j) acc += exp(s * z[j] - m);
+        const double l = m + log(acc);
+        lse[t] = l;
+        logp[t] = row_active(y, mask, t, v, ignore_index) ? s * z[y[t]] - l : 0.0;
+        if (bound) bound[t] = babs;
+        free(hz);
     }
 }
 

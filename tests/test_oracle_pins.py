@@ -13,7 +13,10 @@ comparison) fails at least one of them:
 * a library cross-check of the forward (torch float64 log_softmax + gather);
 * 50-digit decimal brute force for a few tiny rows;
 * invariants: shift and permutation invariance, rows summing to zero, the
-  sharded merge equalling the unsharded log-sum-exp.
+  sharded merge equalling the unsharded log-sum-exp;
+* for the fused LM head: numpy float64 matmul + torch float64 log_softmax,
+  one-hot weight rows reducing to the logits oracle, equal rows giving
+  -log V, a hand-worked two-column example.
 """
 
 import math
@@ -626,3 +629,84 @@ def test_grpo_reduction_invariants():
     ln, gn = oracle.grpo_loss(lp, old, adv, normalizer=48.0)
     la, ga = oracle.grpo_loss(lp, old, adv)
     assert abs(ln - la / 4) < 1e-15 and np.allclose(gn, ga / 4, rtol=1e-14, atol=0)
+
+
+# ---- fused LM head + logp (linear_logp) -------------------------------------
+
+def _bf16_of(a):
+    return workloads.bf16_bits(torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16))
+
+
+def test_linear_logp_matches_numpy_matmul_and_torch_log_softmax():
+    """A library chain: numpy float64 matmul of the widened BF16 operands, then
+    torch float64 log_softmax / logsumexp of s z; non-square shapes (a
+    transposed operand fails), ragged d, padded row strides, temperature, mask,
+    ignore and out-of-range targets."""
+    rng = np.random.default_rng(11)
+    n, d, v = 7, 72, 333
+    h = _bf16_of(rng.standard_normal((n, d + 8)))
+    w = _bf16_of(rng.standard_normal((v, d + 24)) * 0.1)
+    h[:, d:] = 0x7F7F   # padding columns hold huge values: must be ignored
+    w[:, d:] = 0xFF7F
+    y = np.array([0, 5, IGN, v - 1, 17, v, 200], dtype=np.int64)
+    mask = np.array([1, 1, 1, 1, 0, 1, 1], dtype=np.uint8)
+    s = float(np.float32(1 / 0.7))
+    lp, lse, bound = oracle.linear_logp(h, w, y, d=d, scale=s, mask=mask, with_bound=True)
+    hd = oracle.bf16_to_f64(h)[:, :d]
+    wd = oracle.bf16_to_f64(w)[:, :d]
+    z = torch.from_numpy(hd @ wd.T) * s
+    ref_lse = torch.logsumexp(z, dim=1).numpy()
+    ls = torch.log_softmax(z, dim=1).numpy()
+    act = (mask != 0) & (y >= 0) & (y < v)
+    ref_lp = np.where(act, ls[np.arange(n), np.clip(y, 0, v - 1)], 0.0)
+    np.testing.assert_allclose(lse, ref_lse, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lp, ref_lp, rtol=0, atol=1e-12)
+    assert np.all(lp[~act] == 0.0)
+    np.testing.assert_allclose(bound, np.max(np.abs(hd) @ np.abs(wd).T, axis=1), rtol=1e-13)
+
+
+def test_linear_logp_one_hot_weights_select_hidden_columns():
+    """Weight rows e_{p(j)}: the logits are the hidden columns p(j) exactly, so
+    the result equals the (separately pinned) logits oracle on those columns."""
+    rng = np.random.default_rng(12)
+    n, d, v = 9, 64, 48
+    h = _bf16_of(rng.standard_normal((n, d)) * 2)
+    p = rng.permutation(d)[:v]
+    w = np.zeros((v, d), dtype=np.uint16)
+    w[np.arange(v), p] = 0x3F80          # BF16 1.0
+    y = rng.integers(0, v, n)
+    y[3] = IGN
+    for s in (1.0, float(np.float32(1 / 0.7))):
+        lp, lse = oracle.linear_logp(h, w, y, scale=s)
+        cols = np.ascontiguousarray(h[:, p])
+        want_lp, want_lse = oracle.forward(cols, y, scale=s)
+        np.testing.assert_allclose(lp, want_lp, rtol=0, atol=1e-15)
+        np.testing.assert_allclose(lse, want_lse, rtol=0, atol=1e-15)
+
+
+def test_linear_logp_equal_weight_rows_give_minus_log_v():
+    """All weight rows equal: every logit of a row is the same, logp = -log V
+    and LSE = z + log V (closed form)."""
+    rng = np.random.default_rng(13)
+    n, d, v = 5, 40, 1000
+    h = _bf16_of(rng.standard_normal((n, d)))
+    row = _bf16_of(rng.standard_normal((1, d)) * 0.3)
+    w = np.repeat(row, v, axis=0)
+    y = rng.integers(0, v, n)
+    lp, lse = oracle.linear_logp(h, w, y)
+    z = oracle.bf16_to_f64(h) @ oracle.bf16_to_f64(row)[0]
+    np.testing.assert_allclose(lp, -math.log(v), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, z + math.log(v), rtol=0, atol=1e-12)
+
+
+def test_linear_logp_hand_example():
+    """h = (1, -2); weight rows (3, 4) and (0.5, 0.25): z = (-5, 0), so
+    logp(y=0) = -log(1 + e^5), logp(y=1) = -log(1 + e^-5), LSE = log(1 + e^-5),
+    and the bound is max(3 + 8, 0.5 + 0.5) = 11."""
+    h = _bits([[1.0, -2.0], [1.0, -2.0]])
+    w = _bits([[3.0, 4.0], [0.5, 0.25]])
+    lp, lse, b = oracle.linear_logp(h, w, np.array([0, 1]), with_bound=True)
+    assert lp[0] == pytest.approx(-math.log1p(math.exp(5.0)), abs=1e-14)
+    assert lp[1] == pytest.approx(-math.log1p(math.exp(-5.0)), abs=1e-14)
+    assert lse[0] == pytest.approx(math.log1p(math.exp(-5.0)), abs=1e-14)
+    assert b[0] == 11.0 and b[1] == 11.0
