@@ -197,6 +197,39 @@ flp_status logp_merge_partials_ex(const float* part_max, const float* part_sum, 
                                   flp_stream_t stream);
 
 /*
+ * Fused LM head + logp (linear_logp, named in RL-Kernel PR #495 Summary; the
+ * pages give no formula or design).  The logits z = H W^T of BF16 hidden
+ * states and BF16 LM-head weight rows are formed on the tensor cores and
+ * reduced where they are formed; they never reach memory.  Then, as for
+ * fused_logp_forward_ex on logits s z:
+ *   lse[t]  = log sum_j exp(s z[t, j]),  logp[t] = s z[t, y_t] - lse[t]
+ * (0 for inactive rows), lse_lo[t] the FP32 rounding residual of the LSE.
+ *   hidden    [n, ld_h] BF16 device, row-major; the first d columns are used
+ *   weight    [v, ld_w] BF16 device, row-major (one row per vocabulary entry)
+ *   targets   [n] int64; ignore_index and active_mask as for the forward
+ *   inv_temperature  s = 1/T (> 0, finite)
+ *   workspace device scratch of at least fused_linear_logp_workspace_size
+ *             bytes (16-byte aligned), owned by the caller; contents on
+ *             return are unspecified.  Layout: FP32 tile maxima [ceil(v/256),
+ *             n], tile sums [ceil(v/256), n], selected logits [n].
+ *   logp, lse [n] FP32 out; lse_lo [n] FP32 out or NULL
+ * Accumulation: FP32 on the tensor cores (BF16 products exact), 128 x 256
+ * tiles, K in increasing order; each row's result is independent of n, of
+ * its position in the batch and of the grid (deterministic, batch-invariant).
+ * Requirements: hidden and weight 16-byte aligned, ld_h and ld_w multiples
+ * of 8 (16-byte row strides for the tensor-map copies), n, v, d < 2^31;
+ * otherwise FLP_EUNSUPPORTED.  FLP_EINVAL for negative sizes, ld < d, a null
+ * or small workspace, pointers on different devices.  n == 0 is a no-op.
+ * Asynchronous on `stream`; the library allocates nothing.
+ */
+flp_status fused_linear_logp_workspace_size(int64_t n, int64_t v, int64_t* bytes);
+flp_status fused_linear_logp_forward(const void* hidden, int64_t n, int64_t d, int64_t ld_h,
+                                     const void* weight, int64_t v, int64_t ld_w, const int64_t* targets,
+                                     int64_t ignore_index, const uint8_t* active_mask, float inv_temperature,
+                                     void* workspace, int64_t workspace_bytes, float* logp, float* lse,
+                                     float* lse_lo, flp_stream_t stream);
+
+/*
  * GRPO loss on the logp path (issue #241 PR 5: ratio, clip, KL, advantage,
  * a declared normaliser and a fixed summation order; the pages name these
  * terms, the formulas below are the standard clipped-surrogate form).

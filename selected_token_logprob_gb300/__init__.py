@@ -52,6 +52,8 @@ __all__ = [
     "fused_logp",
     "fused_logp_backward",
     "fused_logp_forward",
+    "fused_linear_logp_forward",
+    "fused_linear_logp_workspace_size",
     "logp_grpo_loss",
     "logp_merge_partials",
     "logp_shard_partials",
@@ -295,6 +297,64 @@ def logp_grpo_loss(logp: torch.Tensor, old_logp: torch.Tensor, advantages: torch
                                     _opt_ptr(tl), _stream(logp))
     _lib.check("logp_grpo_loss", st)
     return (loss, grad, tl) if token_loss else (loss, grad)
+
+
+def fused_linear_logp_workspace_size(n: int, v: int) -> int:
+    """Bytes of device scratch that fused_linear_logp_forward needs for n rows
+    and a v-entry vocabulary."""
+    import ctypes
+
+    b = ctypes.c_int64(0)
+    _lib.check("fused_linear_logp_workspace_size",
+               _lib.load().fused_linear_logp_workspace_size(int(n), int(v), ctypes.byref(b)))
+    return int(b.value)
+
+
+def fused_linear_logp_forward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
+                              ignore_index: int = IGNORE_INDEX,
+                              logp: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                              lse_lo: torch.Tensor | None = None, with_lse_lo: bool = False,
+                              temperature: float = 1.0, active_mask: torch.Tensor | None = None,
+                              workspace: torch.Tensor | None = None):
+    """(logp, lse) FP32 [N] of the logits hidden @ weight.T (BF16 hidden
+    [N, D], BF16 LM-head weight [V, D]) without materialising the logits;
+    (logp, lse, lse_lo) when ``with_lse_lo`` or an ``lse_lo`` buffer is given.
+    ``workspace`` (a CUDA byte tensor of at least
+    ``fused_linear_logp_workspace_size(N, V)`` bytes) is allocated when not
+    given."""
+    n, d, ld_h = _rows(hidden, "hidden")
+    v, d_w, ld_w = _rows(weight, "weight")
+    if hidden.dtype != torch.bfloat16 or weight.dtype != torch.bfloat16:
+        raise TypeError("hidden and weight must be bfloat16")
+    if d_w != d:
+        raise ValueError(f"hidden has {d} columns but weight has {d_w}")
+    inv_t = _inv_temperature(temperature)
+    _vec(targets, "targets", n, torch.int64)
+    dev = hidden.device
+    logp = torch.empty(n, dtype=torch.float32, device=dev) if logp is None else logp
+    lse = torch.empty(n, dtype=torch.float32, device=dev) if lse is None else lse
+    want_lo = with_lse_lo or lse_lo is not None
+    if want_lo and lse_lo is None:
+        lse_lo = torch.empty(n, dtype=torch.float32, device=dev)
+    _vec(logp, "logp", n, torch.float32)
+    _vec(lse, "lse", n, torch.float32)
+    _cuda(hidden, weight, targets, logp, lse)
+    if want_lo:
+        _vec(lse_lo, "lse_lo", n, torch.float32)
+        _cuda(lse_lo)
+    mp = _mask(active_mask, n)
+    if n > 0:
+        need = fused_linear_logp_workspace_size(n, v)
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        _cuda(workspace)
+        wbytes = workspace.numel() * workspace.element_size()
+        st = _lib.load().fused_linear_logp_forward(
+            hidden.data_ptr(), n, d, ld_h, weight.data_ptr(), v, ld_w, targets.data_ptr(),
+            int(ignore_index), mp, inv_t, workspace.data_ptr(), wbytes, logp.data_ptr(),
+            lse.data_ptr(), _opt_ptr(lse_lo), _stream(hidden))
+        _lib.check("fused_linear_logp_forward", st)
+    return (logp, lse, lse_lo) if want_lo else (logp, lse)
 
 
 class FusedLogp(torch.autograd.Function):

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libfused_logp.so")
 SOURCES = [os.path.join(CSRC, "fused_logp.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("logp_kernels.cuh", "logp_prims.cuh",
-                                                  "grpo_kernels.cuh")] + [os.path.join(INCLUDE, "fused_logp.h")]
+                                                  "grpo_kernels.cuh", "linear_logp.cuh")] + [os.path.join(INCLUDE, "fused_logp.h")]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 

@@ -10,6 +10,7 @@
 
 #include "fused_logp.h"
 #include "grpo_kernels.cuh"
+#include "linear_logp.cuh"
 #include "logp_kernels.cuh"
 
 namespace {
@@ -135,11 +136,16 @@ flp_status check_scale(float s) {
     return FLP_OK;
 }
 
-// s and s log2(e) as a two-float, from the double value of log2(e).
+// s and s log2(e) as a two-float hi + lo, from the double value of log2(e).
+// hi is rounded down and lo kept strictly positive, so that t hi + t lo is
+// -inf (never -inf + inf = NaN) for a -inf logit difference t.
 flp::Scale make_scale(float s) {
     const double c = (double)s * 1.4426950408889634073599246810019;
-    const float hi = (float)c;
-    return flp::Scale{s, hi, (float)(c - (double)hi)};
+    float hi = (float)c;
+    if ((double)hi > c) hi = nextafterf(hi, 0.f);
+    float lo = (float)(c - (double)hi);
+    if (!(lo > 0.f)) lo = 1e-30f;
+    return flp::Scale{s, hi, lo};
 }
 
 int sm_count(int dev) {
@@ -258,6 +264,73 @@ template <flp::Dt D>
 void launch_partials_d(const PartArgs& a) {
     if (a.vec) launch_part<D, true, true>(a);
     else launch_part<D, false, true>(a);
+}
+
+// ---- fused LM head: tensor maps and launch setup
+
+// cuTensorMapEncodeTiled from the driver, found once through the runtime (no
+// link against the driver library).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static const EncodeTiledFn fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            (void)cudaGetLastError();
+            return (EncodeTiledFn) nullptr;
+        }
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+
+// Tensor map of a BF16 row-major [rows, ld] matrix whose first `cols` columns
+// are used: boxes of 64 columns (128 bytes) x box_rows rows, 128-byte swizzle,
+// zero fill outside the matrix.
+flp_status make_tmap_bf16(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t ld,
+                          uint32_t box_rows, const char* name) {
+    const EncodeTiledFn fn = encode_tiled();
+    if (!fn) return fail(FLP_ECUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)flp::kLinBK, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(FLP_EINVAL, "tensor map of %s rejected by the driver (error %d)", name, (int)r);
+    return FLP_OK;
+}
+
+flp_status linear_setup(int dev) {
+    static bool ready[kMaxDevices];
+    if (!ready[dev]) {
+        const cudaError_t e = cudaFuncSetAttribute(flp::k_linear_logp_tiles,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)flp::kLinSmemBytes);
+        if (e != cudaSuccess) return fail(FLP_ECUDA, "linear logp setup: %s", cudaGetErrorString(e));
+        ready[dev] = true;
+    }
+    return FLP_OK;
+}
+
+int64_t linear_vocab_tiles(int64_t v) { return ceil_div(v, flp::kLinBN); }
+
+// Workspace: tile maxima [nvt, n], tile sums [nvt, n], selected logits [n]
+// (binary32), rounded up to 256 bytes; false on overflow.
+bool linear_workspace_bytes(int64_t n, int64_t v, int64_t* out) {
+    int64_t a, b;
+    if (__builtin_mul_overflow(linear_vocab_tiles(v), n, &a)) return false;
+    if (__builtin_mul_overflow(a, (int64_t)2, &a)) return false;
+    if (__builtin_add_overflow(a, n, &b)) return false;
+    if (__builtin_mul_overflow(b, (int64_t)4, &b)) return false;
+    *out = ceil_div(b, 256) * 256;
+    return true;
 }
 
 }  // namespace
@@ -448,6 +521,85 @@ flp_status logp_merge_partials(const float* part_max, const float* part_sum, con
                                flp_stream_t stream) {
     return logp_merge_partials_ex(part_max, part_sum, sel, targets, ignore_index, nullptr, n,
                                   v_total, 1.f, logp, lse, lse_lo, stream);
+}
+
+flp_status fused_linear_logp_workspace_size(int64_t n, int64_t v, int64_t* bytes) {
+    if (bytes == nullptr) return fail(FLP_EINVAL, "bytes is a null pointer");
+    if (n < 0) return fail(FLP_EINVAL, "n must be >= 0 (got %lld)", (long long)n);
+    if (v < 1) return fail(FLP_EINVAL, "v must be >= 1 (got %lld)", (long long)v);
+    if (!linear_workspace_bytes(n, v, bytes)) return fail(FLP_EINVAL, "workspace size overflows int64");
+    return ok();
+}
+
+flp_status fused_linear_logp_forward(const void* hidden, int64_t n, int64_t d, int64_t ld_h,
+                                     const void* weight, int64_t v, int64_t ld_w, const int64_t* targets,
+                                     int64_t ignore_index, const uint8_t* active_mask, float inv_temperature,
+                                     void* workspace, int64_t workspace_bytes, float* logp, float* lse,
+                                     float* lse_lo, flp_stream_t stream) {
+    flp_status st;
+    if ((st = check_scale(inv_temperature)) != FLP_OK) return st;
+    if (n < 0) return fail(FLP_EINVAL, "n must be >= 0 (got %lld)", (long long)n);
+    if (d < 1) return fail(FLP_EINVAL, "d must be >= 1 (got %lld)", (long long)d);
+    if (v < 1) return fail(FLP_EINVAL, "v must be >= 1 (got %lld)", (long long)v);
+    if (ld_h < d || ld_w < d)
+        return fail(FLP_EINVAL, "ld_h (%lld) and ld_w (%lld) must be >= d (%lld)", (long long)ld_h,
+                    (long long)ld_w, (long long)d);
+    if (n == 0) return ok();
+    const int64_t kMaxDim = ((int64_t)1 << 31) - 1;
+    if (n > kMaxDim || v > kMaxDim || d > kMaxDim)
+        return fail(FLP_EUNSUPPORTED, "n, v and d must be below 2^31");
+    if (!aligned16(hidden) || !aligned16(weight) || (ld_h % 8) != 0 || (ld_w % 8) != 0)
+        return fail(FLP_EUNSUPPORTED,
+                    "hidden and weight must start on 16-byte boundaries with row strides a multiple of 8 elements");
+    int64_t bytes_h, bytes_w, need;
+    if (!span_bytes(n, d, ld_h, 2, &bytes_h) || !span_bytes(v, d, ld_w, 2, &bytes_w))
+        return fail(FLP_EINVAL, "hidden or weight extent overflows int64");
+    if (!linear_workspace_bytes(n, v, &need)) return fail(FLP_EINVAL, "workspace size overflows int64");
+    if (workspace_bytes < need)
+        return fail(FLP_EINVAL, "workspace_bytes (%lld) is below the %lld bytes needed", (long long)workspace_bytes,
+                    (long long)need);
+    if (!aligned16(workspace)) return fail(FLP_EINVAL, "workspace must start on a 16-byte boundary");
+    const void* ptrs[] = {hidden, weight, targets, workspace, logp, lse, lse_lo, active_mask};
+    const char* names[] = {"hidden", "weight", "targets", "workspace", "logp", "lse", "lse_lo", "active_mask"};
+    const bool optional[] = {false, false, false, false, false, false, true, true};
+    int dev;
+    if ((st = common_device(8, ptrs, names, optional, &dev)) != FLP_OK) return st;
+    if (dev < 0 || dev >= kMaxDevices) return fail(FLP_ECUDA, "device index %d out of range", dev);
+    DeviceGuard guard;
+    if ((st = guard.enter(dev)) != FLP_OK) return st;
+    if ((st = linear_setup(dev)) != FLP_OK) return st;
+
+    CUtensorMap tm_h, tm_w;
+    if ((st = make_tmap_bf16(&tm_h, hidden, n, d, ld_h, flp::kLinBM, "hidden")) != FLP_OK) return st;
+    if ((st = make_tmap_bf16(&tm_w, weight, v, d, ld_w, flp::kLinBN, "weight")) != FLP_OK) return st;
+
+    const int64_t nvt = linear_vocab_tiles(v);
+    const int64_t nrb = ceil_div(n, flp::kLinBM);
+    float* ws = static_cast<float*>(workspace);
+    flp::LinArgs a;
+    a.n = n;
+    a.v = v;
+    a.nrb = (int)nrb;
+    a.nvt = (int)nvt;
+    a.nkb = (int)ceil_div(d, flp::kLinBK);
+    a.y = targets;
+    a.ignore_index = ignore_index;
+    a.mask = active_mask;
+    a.sc = make_scale(inv_temperature);
+    a.pm = ws;
+    a.ps = ws + nvt * n;
+    a.xsel = ws + 2 * nvt * n;
+    const int sms = sm_count(dev);
+    if (sms <= 0) return fail(FLP_ECUDA, "cannot read the SM count of device %d", dev);
+    const int64_t ntiles = nrb * nvt;
+    const int grid = (int)(ntiles < sms ? ntiles : sms);
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    flp::k_linear_logp_tiles<<<grid, flp::kLinThreads, flp::kLinSmemBytes, s>>>(tm_h, tm_w, a);
+    if ((st = check_launch("linear logp tiles")) != FLP_OK) return st;
+    flp::k_linear_logp_merge<<<grid_for(ceil_div(n, flp::kLinMergeThreads)), flp::kLinMergeThreads, 0, s>>>(
+        a.pm, a.ps, a.xsel, n, (int)nvt, v, targets, ignore_index, active_mask, inv_temperature, logp, lse,
+        lse_lo);
+    return check_launch("linear logp merge");
 }
 
 flp_status logp_grpo_loss(const float* logp, const float* old_logp, const float* ref_logp,

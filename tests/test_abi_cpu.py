@@ -171,3 +171,50 @@ def test_package_does_not_import_the_oracle():
             if fn.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 src = open(os.path.join(dirpath, fn)).read()
                 assert "oracle" not in src.lower(), fn
+
+
+def test_linear_logp_host_checks(lib):
+    b = ctypes.c_int64(0)
+    assert lib.fused_linear_logp_workspace_size(2048, 151936, ctypes.byref(b)) == 0
+    nvt = -(-151936 // 256)
+    assert b.value == -(-(2 * nvt * 2048 + 2048) * 4 // 256) * 256
+    assert lib.fused_linear_logp_workspace_size(-1, 10, ctypes.byref(b)) == EINVAL
+    assert lib.fused_linear_logp_workspace_size(4, 0, ctypes.byref(b)) == EINVAL
+    assert lib.fused_linear_logp_workspace_size(4, 10, None) == EINVAL
+    assert flp.fused_linear_logp_workspace_size(0, 7) == 0
+
+    def call(n=256, d=512, ld_h=512, ptr_h=1 << 20, v=5000, ld_w=512, ptr_w=1 << 21, s=1.0,
+             ws=1 << 22, ws_bytes=1 << 30):
+        return lib.fused_linear_logp_forward(ptr_h, n, d, ld_h, ptr_w, v, ld_w, 1 << 23, -100, None, s,
+                                             ws, ws_bytes, 1 << 24, 1 << 25, None, None)
+
+    assert call(n=0) == 0                                   # empty: no device touched
+    assert call(n=-1) == EINVAL
+    assert call(d=0) == EINVAL
+    assert call(v=0) == EINVAL
+    assert call(ld_h=500) == EINVAL and b"ld_h" in lib.flp_last_error()
+    assert call(ld_w=256) == EINVAL
+    assert call(s=0.0) == EINVAL
+    assert call(s=float("inf")) == EINVAL
+    assert call(ld_h=516) == EUNSUP                         # row stride not 16-byte
+    assert call(ptr_h=(1 << 20) + 8) == EUNSUP              # base not 16-byte aligned
+    assert call(ptr_w=(1 << 21) + 2) == EUNSUP
+    assert call(n=1 << 31) == EUNSUP
+    assert call(ws_bytes=1000) == EINVAL and b"workspace" in lib.flp_last_error()
+    assert call(ws=(1 << 22) + 4) == EINVAL
+    # pointer checks come last: host pointers are not device memory
+    assert call() == EINVAL
+
+
+def test_linear_logp_binding_checks_before_calling():
+    h = torch.zeros(4, 64, dtype=torch.bfloat16)
+    w = torch.zeros(10, 64, dtype=torch.bfloat16)
+    y = torch.zeros(4, dtype=torch.int64)
+    with pytest.raises(TypeError):
+        flp.fused_linear_logp_forward(h.float(), w, y)
+    with pytest.raises(ValueError):
+        flp.fused_linear_logp_forward(h, w[:, :32], y)
+    with pytest.raises(ValueError):
+        flp.fused_linear_logp_forward(h, w, y, temperature=0.0)
+    with pytest.raises(ValueError):
+        flp.fused_linear_logp_forward(h, w, y)               # CPU tensors

@@ -1,0 +1,177 @@
+"""GPU parity of the fused LM head + logp (linear_logp, RL-Kernel PR #495
+Summary names it; the pages give no formula) against the FP64 oracle, plus
+batch invariance and determinism.
+
+Tolerance, derived from the arithmetic.  The tensor cores form each logit
+z = sum_k h_k w_k from exact BF16 products, 16 products per instruction,
+accumulated in binary32 over ceil(D/16) instructions.  Bounding each
+instruction's error by one binary32 rounding of the running sum plus an
+alignment loss of 16 * 2^-24 of its own terms gives, with A = sum_k |h_k w_k|,
+    |dz| <= E = (ceil(D/16) * 2^-23 + 2^-20) * A.
+LSE is a convex combination in z, so |dLSE| <= s E; logp = s z_y - LSE, so
+|dlogp| <= 2 s E, plus 1e-6 (1 + |LSE|) for the exp2 approximation, the
+final binary32 roundings and the partial merge.  The oracle returns
+max_j A_j per row.  The measured errors are printed (they sit far below E);
+the tests also hold the logp error to the 1e-4 absolute bar of the logits
+path for D <= 4096."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import selected_token_logprob_gb300 as flp
+import workloads
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    flp._lib.load(build_if_missing=True)
+
+
+def _i(t):
+    return t.view(torch.int32)
+
+
+def _tol(d, bound, lse, s):
+    e = (math.ceil(d / 16) * 2.0 ** -23 + 2.0 ** -20) * bound
+    return 2 * s * e + 1e-6 * (1 + np.abs(lse)), s * e + 1e-6 * (1 + np.abs(lse))
+
+
+def _check(h, w, y, d, logp, lse, rows=None, s=1.0, mask=None, label=""):
+    """Compare rows (all if None) with the oracle; returns max errors."""
+    rows = np.arange(h.shape[0]) if rows is None else np.asarray(rows)
+    hb = workloads.bf16_bits(h[torch.as_tensor(rows, device=h.device)])
+    wb = workloads.bf16_bits(w)
+    yn = y.cpu().numpy()[rows]
+    mk = None if mask is None else mask.cpu().numpy().astype(np.uint8)[rows]
+    ref_lp, ref_lse, bound = oracle.linear_logp(hb, wb, yn, d=d, scale=s, mask=mk, with_bound=True)
+    got_lp = logp.double().cpu().numpy()[rows]
+    got_lse = lse.double().cpu().numpy()[rows]
+    tol_lp, tol_lse = _tol(d, bound, ref_lse, s)
+    e_lp, e_lse = np.abs(got_lp - ref_lp), np.abs(got_lse - ref_lse)
+    print(f"{label}: max |dlogp| {e_lp.max():.3e} (bound {tol_lp.min():.3e}), "
+          f"max |dLSE| {e_lse.max():.3e}, mean dlogp {np.mean(got_lp - ref_lp):+.3e}")
+    assert np.all(e_lp <= tol_lp), (e_lp.max(), tol_lp.min())
+    assert np.all(e_lse <= tol_lse), (e_lse.max(), tol_lse.min())
+    act = (yn >= 0) & (yn < w.shape[0]) & (yn != workloads.IGNORE_INDEX)
+    if mk is not None:
+        act &= mk != 0
+    assert np.all(got_lp[~act] == 0)
+    if d <= 4096:
+        assert e_lp.max() <= 1e-4, e_lp.max()
+    return e_lp.max(), e_lse.max()
+
+
+def _padded(x, ld, fill):
+    """Copy of x in a row-padded buffer whose padding holds `fill`."""
+    buf = torch.full((x.shape[0], ld), fill, dtype=x.dtype, device=x.device)
+    buf[:, :x.shape[1]] = x
+    return buf[:, :x.shape[1]]
+
+
+@pytest.mark.parametrize("temperature", [1.0, 0.7])
+def test_small_ragged_against_oracle(temperature):
+    """Ragged in every dimension: 200 rows (a partial row block), D = 520 (a
+    partial K block), V = 5000 (a partial vocabulary tile); padded row strides
+    whose padding is NaN (must never be read); ignore, out-of-range and masked
+    rows."""
+    n, d, v = 200, 520, 5000
+    h, w, y = workloads.linear(n, d, v, seed=1, device=DEV)
+    h = _padded(h, d + 8, float("nan"))
+    w = _padded(w, d + 24, float("nan"))
+    y[3] = v
+    y[4] = -5
+    mask = torch.ones(n, dtype=torch.bool, device=DEV)
+    mask[10::17] = False
+    logp, lse, lo = flp.fused_linear_logp_forward(h, w, y, with_lse_lo=True, temperature=temperature,
+                                                  active_mask=mask)
+    s = float(np.float32(1.0 / temperature))
+    _check(h, w, y, d, logp, lse, s=s, mask=mask, label=f"small T={temperature}")
+    off = (~mask) | (y < 0) | (y >= v)
+    assert torch.all(logp[off] == 0)
+    # lse_lo is the binary32 rounding residual of the LSE
+    spacing = torch.from_numpy(np.spacing(np.abs(lse.cpu().numpy()))).to(DEV)
+    assert torch.all(lo.abs() <= spacing / 2)
+
+
+@pytest.mark.parametrize("n,d,v", [(1, 8, 1), (3, 64, 255), (129, 72, 257), (128, 4096, 512),
+                                   (64, 16, 151936)])
+def test_edge_shapes(n, d, v):
+    h, w, y = workloads.linear(n, d, v, seed=2, device=DEV, ignore_frac=0.0)
+    logp, lse = flp.fused_linear_logp_forward(h, w, y)
+    _check(h, w, y, d, logp, lse, label=f"n={n} d={d} v={v}")
+
+
+def test_all_rows_inactive_and_empty():
+    h, w, y = workloads.linear(40, 64, 300, seed=3, device=DEV)
+    y[:] = -100
+    logp, lse = flp.fused_linear_logp_forward(h, w, y)
+    assert torch.all(logp == 0) and torch.isfinite(lse).all()
+    e = flp.fused_linear_logp_forward(h[:0], w, y[:0])
+    assert e[0].numel() == 0
+
+
+def test_full_size_sampled_rows():
+    """The benchmark's configuration (N = 32768, D = 4096, V = 151936, one
+    launch as timed), 48 sampled rows against the oracle; every row finite."""
+    n, d, v = workloads.LINEAR_LONG
+    h, w, y = workloads.linear(n, d, v, seed=0, device=DEV)
+    logp, lse = flp.fused_linear_logp_forward(h, w, y)
+    assert torch.isfinite(logp).all() and torch.isfinite(lse).all()
+    assert torch.all(logp <= 0)
+    g = np.random.default_rng(5)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, n - 1], g.integers(0, n, 43)]))
+    _check(h, w, y, d, logp, lse, rows=rows, label="long (sampled)")
+    assert torch.all(logp[y < 0] == 0)
+
+
+def test_batch_invariance_and_determinism():
+    """A row's bits do not depend on the batch around it or on its position."""
+    d, v = 1024, 20000
+    probes, w, py = workloads.linear(4, d, v, seed=7, device=DEV, ignore_frac=0.0)
+    filler, _, fy = workloads.linear(300, d, v, seed=8, device=DEV, ignore_frac=0.0)
+    ref = [flp.fused_linear_logp_forward(probes[k:k + 1], w, py[k:k + 1], with_lse_lo=True)
+           for k in range(4)]
+    again = flp.fused_linear_logp_forward(probes, w, py, with_lse_lo=True)
+    for k in range(4):
+        for r, a in zip(ref[k], again):
+            assert torch.equal(_i(r[0:1]), _i(a[k:k + 1]))
+    for B in (2, 127, 128, 129, 300):
+        for pos in (0, B // 2, B - 1):
+            hb, yb = filler[:B].clone(), fy[:B].clone()
+            k = (B + pos) % 4
+            hb[pos], yb[pos] = probes[k], py[k]
+            out = flp.fused_linear_logp_forward(hb, w, yb, with_lse_lo=True)
+            for r, o in zip(ref[k], out):
+                assert torch.equal(_i(r[0:1]), _i(o[pos:pos + 1])), (B, pos)
+    x1 = flp.fused_linear_logp_forward(filler, w, fy)
+    x2 = flp.fused_linear_logp_forward(filler, w, fy)
+    assert all(torch.equal(_i(a), _i(b)) for a, b in zip(x1, x2))
+
+
+def test_matches_materialised_logits_path():
+    """The fused path and the logits path (FP32 logits from a plain FP32
+    matmul, then the fused logp forward) agree within the contraction's own
+    rounding error."""
+    n, d, v = 256, 2048, 30000
+    h, w, y = workloads.linear(n, d, v, seed=9, device=DEV)
+    logp, lse = flp.fused_linear_logp_forward(h, w, y)
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        z = h.float() @ w.float().T
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+    logp2, lse2 = flp.fused_logp_forward(z, y)
+    assert torch.max(torch.abs(logp - logp2)).item() <= 1e-4
+    assert torch.max(torch.abs(lse - lse2)).item() <= 1e-4
+
+
+def test_no_device_error():
+    assert flp.flp_device_error(0) == 0

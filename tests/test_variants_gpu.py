@@ -185,3 +185,21 @@ def test_autograd_with_temperature_and_mask():
     sel = lp.gather(1, y.clamp(min=0)[:, None])[:, 0] * act
     (sel * g.double()).sum().backward()
     assert torch.allclose(xr.grad.double(), xd.grad, rtol=0, atol=1e-6 * xd.grad.abs().max().item())
+
+
+@pytest.mark.parametrize("dtype", DTYPES, ids=["bf16", "f16", "f32"])
+@pytest.mark.parametrize("temperature", [1.0, T07, 0.8])
+def test_minus_inf_logits_at_any_temperature(dtype, temperature):
+    """-inf logits (a masked part of the vocabulary) contribute exp(-inf) = 0
+    at every temperature; 0.8 is a temperature whose binary32 s log2(e) rounds
+    up to nearest, the case where a naive two-float product gives -inf + inf."""
+    x, y, g = workloads.make("mid", device=DEV, n=64, dtype=dtype)
+    x[:, 1000:5000] = float("-inf")
+    x[::7, 20000:] = float("-inf")
+    for t in range(64):                       # a -inf target logit is unsupported: retarget those rows
+        if 1000 <= int(y[t]) < 5000 or (t % 7 == 0 and int(y[t]) >= 20000):
+            y[t] = 7
+    logp, lse, d = run(x, y, g, temperature)
+    assert torch.isfinite(logp).all() and torch.isfinite(lse).all()
+    assert torch.isfinite(d.float()).all()
+    check(x, y, g, logp, lse, d, float(np.float32(1.0 / temperature)))

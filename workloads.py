@@ -17,6 +17,12 @@ Recipe (all draws in FP32, then ONE round-to-nearest-even cast to BF16):
   sweep    V=151936, x ~ N(0,3^2); probe and filler rows from separate
            streams.
   sharded  N=8192,  V=151936, x ~ N(0,2^2); targets uniform; no ignore rows.
+  linear   fused LM head: hidden H [N, D] ~ N(0,1), weight W [V, D] ~
+           N(0, (2/sqrt(D))^2) (so the logits H W^T have standard deviation
+           about 2, like the logits workloads), both drawn like the logits
+           (FP32, one cast to BF16) from their own seeds; targets as above
+           with 5% ignore.  Long: N=32768, D=4096 (a Qwen3-8B-sized hidden
+           state; the pages name no hidden size), V=151936.
 Targets are uniform in [0, V); exactly floor(p*N) rows, chosen by a seeded
 permutation, get the ignore index -100.  Each random stream has its own
 generator seeded from (seed, stream id), so changing one never shifts another.
@@ -117,6 +123,20 @@ def make(name_or_wl, device="cpu", n: int | None = None, seed: int | None = None
     y = targets(n, wl.v, wl.ignore_frac, seed, device=device)
     g = grads(n, wl.grad, seed, device=device)
     return x, y, g
+
+
+LINEAR_LONG = (32768, 4096, QWEN3_VOCAB)   # (N, D, V) of the fused LM-head workload
+
+
+def linear(n: int, d: int, v: int, seed: int = 0, device="cpu", ld_h: int | None = None,
+           ld_w: int | None = None, ignore_frac: float = 0.05):
+    """(hidden [n, ld_h] BF16, weight [v, ld_w] BF16, targets int64 [n]) of the
+    fused LM-head workload; padding columns are 0."""
+    base = 1_000 + 3 * int(seed)
+    h = logits(n, d, 1.0, 0.0, base, device=device, ld=ld_h)
+    w = logits(v, d, 2.0 / d ** 0.5, 0.0, base + 1, device=device, ld=ld_w, block_rows=4096)
+    y = targets(n, v, ignore_frac, base + 2, device=device)
+    return h, w, y
 
 
 def sweep_rows(count: int, v: int, sigma: float, seed: int, stream: int, device="cpu"):
