@@ -230,6 +230,41 @@ flp_status fused_linear_logp_forward(const void* hidden, int64_t n, int64_t d, i
                                      float* lse_lo, flp_stream_t stream);
 
 /*
+ * Fused LM head + logp with no allocation and no workspace argument.  The
+ * pages have no counterpart: this is a convenience of this library.
+ *
+ * Some callers cannot allocate device memory at all: a plugin that a host
+ * application hands only its input and output buffers, code running under an
+ * application-wide memory pool that owns all device memory and forbids direct
+ * cudaMalloc calls, or a tight loop where a cudaMalloc/cudaFree pair would
+ * synchronise the device.  For them this entry point computes exactly what
+ * fused_linear_logp_forward computes (same arguments minus the workspace;
+ * identical bits) and takes its scratch from a fixed 16 MiB array in the
+ * library's static device memory.  It calls no allocator.
+ *   Limit: the scratch needed, fused_linear_logp_workspace_size(n, v), must
+ *   be at most 16 MiB (16777216 bytes): up to 3527 rows per call at
+ *   v = 151936.  Larger calls return FLP_EUNSUPPORTED with a message naming
+ *   the sizes; split the rows, or use fused_linear_logp_forward.
+ *   Memory: every GPU that loads the library holds the 16 MiB until the
+ *   process exits.
+ *   First call per device: looks up the array's device address
+ *   (cudaGetSymbolAddress) and caches it; make that first call before any
+ *   stream capture.
+ *   Sharing: all calls in the process use the same array.  Calls whose work
+ *   can overlap on a GPU (different streams, or different host threads
+ *   without ordering) race on it and give wrong results; order them, e.g. on
+ *   one stream.  The array keeps the previous call's contents, and nothing in
+ *   it needs to start at zero: every element a call reads was written
+ *   earlier in that same call.
+ * Errors: as fused_linear_logp_forward, plus FLP_EUNSUPPORTED above the limit.
+ */
+flp_status fused_linear_logp_forward_noalloc(const void* hidden, int64_t n, int64_t d, int64_t ld_h,
+                                             const void* weight, int64_t v, int64_t ld_w,
+                                             const int64_t* targets, int64_t ignore_index,
+                                             const uint8_t* active_mask, float inv_temperature, float* logp,
+                                             float* lse, float* lse_lo, flp_stream_t stream);
+
+/*
  * GRPO loss on the logp path (issue #241 PR 5: ratio, clip, KL, advantage,
  * a declared normaliser and a fixed summation order; the pages name these
  * terms, the formulas below are the standard clipped-surrogate form).

@@ -53,6 +53,7 @@ __all__ = [
     "fused_logp_backward",
     "fused_logp_forward",
     "fused_linear_logp_forward",
+    "fused_linear_logp_forward_noalloc",
     "fused_linear_logp_workspace_size",
     "logp_grpo_loss",
     "logp_merge_partials",
@@ -355,6 +356,36 @@ def fused_linear_logp_forward(hidden: torch.Tensor, weight: torch.Tensor, target
             lse.data_ptr(), _opt_ptr(lse_lo), _stream(hidden))
         _lib.check("fused_linear_logp_forward", st)
     return (logp, lse, lse_lo) if want_lo else (logp, lse)
+
+
+def fused_linear_logp_forward_noalloc(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
+                                      logp: torch.Tensor, lse: torch.Tensor,
+                                      lse_lo: torch.Tensor | None = None,
+                                      ignore_index: int = IGNORE_INDEX, temperature: float = 1.0,
+                                      active_mask: torch.Tensor | None = None):
+    """fused_linear_logp_forward for callers that cannot allocate: the caller
+    passes the outputs, and the library uses its fixed 16 MiB static scratch
+    instead of a workspace (at most 3527 rows per call at V = 151936; calls
+    must not overlap on the GPU).  Nothing is allocated here."""
+    n, d, ld_h = _rows(hidden, "hidden")
+    v, d_w, ld_w = _rows(weight, "weight")
+    if hidden.dtype != torch.bfloat16 or weight.dtype != torch.bfloat16:
+        raise TypeError("hidden and weight must be bfloat16")
+    if d_w != d:
+        raise ValueError(f"hidden has {d} columns but weight has {d_w}")
+    inv_t = _inv_temperature(temperature)
+    _vec(targets, "targets", n, torch.int64)
+    _vec(logp, "logp", n, torch.float32)
+    _vec(lse, "lse", n, torch.float32)
+    _cuda(hidden, weight, targets, logp, lse)
+    if lse_lo is not None:
+        _vec(lse_lo, "lse_lo", n, torch.float32)
+        _cuda(lse_lo)
+    mp = _mask(active_mask, n)
+    st = _lib.load().fused_linear_logp_forward_noalloc(
+        hidden.data_ptr(), n, d, ld_h, weight.data_ptr(), v, ld_w, targets.data_ptr(), int(ignore_index),
+        mp, inv_t, logp.data_ptr(), lse.data_ptr(), _opt_ptr(lse_lo), _stream(hidden))
+    _lib.check("fused_linear_logp_forward_noalloc", st)
 
 
 class FusedLogp(torch.autograd.Function):

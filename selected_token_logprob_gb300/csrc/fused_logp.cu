@@ -13,6 +13,15 @@
 #include "linear_logp.cuh"
 #include "logp_kernels.cuh"
 
+// Fixed device scratch of fused_linear_logp_forward_noalloc, for callers that
+// cannot allocate device memory.  It lives in the module's static device
+// memory: every GPU that loads this library holds these 16 MiB until the
+// process exits.  Host code must not pass this name to a kernel (on the host
+// it names a stand-in object, not device memory); it looks up the device
+// address once per device with cudaGetSymbolAddress.
+constexpr int64_t kNoAllocScratchBytes = (int64_t)16 << 20;
+static __device__ __align__(256) float g_linear_noalloc_scratch[kNoAllocScratchBytes / 4];
+
 namespace {
 
 thread_local char g_msg[512] = "";
@@ -333,6 +342,23 @@ bool linear_workspace_bytes(int64_t n, int64_t v, int64_t* out) {
     return true;
 }
 
+// Device address of g_linear_noalloc_scratch on `dev` (which must be
+// current), looked up on the first call for that device and cached.
+flp_status noalloc_scratch_address(int dev, void** out) {
+    static void* addr[kMaxDevices];
+    if (addr[dev] == nullptr) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_linear_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr) {
+            (void)cudaGetLastError();
+            return fail(FLP_ECUDA, "address of the static scratch on device %d: %s", dev, cudaGetErrorString(e));
+        }
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return FLP_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -600,6 +626,37 @@ flp_status fused_linear_logp_forward(const void* hidden, int64_t n, int64_t d, i
         a.pm, a.ps, a.xsel, n, (int)nvt, v, targets, ignore_index, active_mask, inv_temperature, logp, lse,
         lse_lo);
     return check_launch("linear logp merge");
+}
+
+flp_status fused_linear_logp_forward_noalloc(const void* hidden, int64_t n, int64_t d, int64_t ld_h,
+                                             const void* weight, int64_t v, int64_t ld_w,
+                                             const int64_t* targets, int64_t ignore_index,
+                                             const uint8_t* active_mask, float inv_temperature, float* logp,
+                                             float* lse, float* lse_lo, flp_stream_t stream) {
+    // empty or malformed sizes: the same answers as the workspace entry point
+    if (n <= 0 || v < 1 || d < 1)
+        return fused_linear_logp_forward(hidden, n, d, ld_h, weight, v, ld_w, targets, ignore_index, active_mask,
+                                         inv_temperature, nullptr, 0, logp, lse, lse_lo, stream);
+    int64_t need;
+    if (!linear_workspace_bytes(n, v, &need)) return fail(FLP_EINVAL, "scratch size overflows int64");
+    if (need > kNoAllocScratchBytes)
+        return fail(FLP_EUNSUPPORTED,
+                    "fused_linear_logp_forward_noalloc: %lld rows with a %lld-entry vocabulary need %lld bytes of "
+                    "scratch, more than its fixed %lld bytes; pass fewer rows per call or use "
+                    "fused_linear_logp_forward with a workspace",
+                    (long long)n, (long long)v, (long long)need, (long long)kNoAllocScratchBytes);
+    flp_status st;
+    int dev;
+    if ((st = device_of(hidden, "hidden", &dev)) != FLP_OK) return st;
+    if (dev < 0 || dev >= kMaxDevices) return fail(FLP_ECUDA, "device index %d out of range", dev);
+    void* scratch = nullptr;
+    {
+        DeviceGuard guard;
+        if ((st = guard.enter(dev)) != FLP_OK) return st;
+        if ((st = noalloc_scratch_address(dev, &scratch)) != FLP_OK) return st;
+    }
+    return fused_linear_logp_forward(hidden, n, d, ld_h, weight, v, ld_w, targets, ignore_index, active_mask,
+                                     inv_temperature, scratch, kNoAllocScratchBytes, logp, lse, lse_lo, stream);
 }
 
 flp_status logp_grpo_loss(const float* logp, const float* old_logp, const float* ref_logp,

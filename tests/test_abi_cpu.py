@@ -218,3 +218,19 @@ def test_linear_logp_binding_checks_before_calling():
         flp.fused_linear_logp_forward(h, w, y, temperature=0.0)
     with pytest.raises(ValueError):
         flp.fused_linear_logp_forward(h, w, y)               # CPU tensors
+
+
+def test_linear_logp_noalloc_host_checks(lib):
+    """The no-allocation variant refuses, before touching any device, a call
+    whose scratch would exceed its fixed 16 MiB, and names the sizes."""
+    def call(n, v=151936, d=4096):
+        return lib.fused_linear_logp_forward_noalloc(1 << 20, n, d, d, 1 << 21, v, d, 1 << 22, -100, None,
+                                                     1.0, 1 << 23, 1 << 24, None, None)
+
+    assert call(0) == 0
+    assert call(-1) == EINVAL
+    assert call(3528) == EUNSUP
+    msg = lib.flp_last_error()
+    assert b"3528 rows" in msg and b"16777216" in msg
+    assert call(3527) == EINVAL          # within the limit: reaches the pointer checks
+    assert b"hidden" in lib.flp_last_error()
