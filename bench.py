@@ -11,6 +11,12 @@ Metric: effective HBM GB/s of forward + backward, counting the algorithmic
 2-byte write), plus ms per step.  Prints one JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py --path linear      # fused LM head + logp forward (tensor cores)
+
+--path linear times the fused LM-head forward instead (BF16 hidden states
+[32768, 4096] against BF16 LM-head weights [151936, 4096], logits never
+materialised) and reports dense TFLOP/s (2 N V D per call) against the
+measured bf16 tensor peak.
 
 --impl reference times the FP64 CPU oracle on the host cores (a bounded
 sample of rows per step) on the same metric; under torchrun only rank 0 runs
@@ -41,6 +47,11 @@ BYTES_PER_LOGIT = 6          # fwd read 2 + bwd read 2 + bwd write 2
 BWD_BYTES_PER_LOGIT = 4
 FWD_BYTES_PER_LOGIT = 2
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
+LIN_METRIC = "fused LM-head + logp forward TFLOP/s at N=32768, D=4096, V=151936 BF16"
+LIN_DESC = ("fused LM head: hidden [N, D] BF16 ~ N(0,1), weight [V, D] BF16 ~ N(0,(2/sqrt D)^2), "
+            "targets uniform, 5% ignore_index (synthetic)")
 # Pages' fused kernel, forward + backward at 32768 x 151936 (B200, BF16):
 # 27.2 ms (RL-Kernel PR #495, Results table).  Context only: another GPU.
 PAGES_FWD_BWD_MS = 27.2
@@ -57,9 +68,29 @@ def _peaks():
     return FALLBACK_HBM_GBS, "fallback 6.8 TB/s"
 
 
-def _kernel_hash() -> str:
+def _tensor_peaks():
+    """(burst, sustained, source) dense bf16 TFLOP/s."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return (float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "measured (MEASURED_PEAKS.json bf16_tflops, cuBLAS burst)")
+    return FALLBACK_BF16_TFLOPS, FALLBACK_BF16_TFLOPS_SUSTAINED, "fallback 1.9 PFLOP/s"
+
+
+# Device sources of each profiled kernel (a profile's traffic is reported only
+# while these files are unchanged since its capture).
+KERNEL_SOURCES = {
+    "k_logp_bwd": ("logp_kernels.cuh", "logp_prims.cuh"),
+    "k_logp_fwd_bulk": ("logp_kernels.cuh", "logp_prims.cuh"),
+    "k_linear_logp_tiles": ("linear_logp.cuh", "logp_kernels.cuh", "logp_prims.cuh"),
+}
+
+
+def _kernel_hash(kernel: str = "k_logp_bwd") -> str:
     h = hashlib.sha256()
-    for fn in ("fused_logp.cu", "logp_kernels.cuh", "logp_prims.cuh"):
+    for fn in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "selected_token_logprob_gb300", "csrc", fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -74,7 +105,7 @@ def _profiled_traffic(kernel: str):
     txt = open(p).read()
     m_hash = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", txt)
     m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
-    if not m_hash or not m_bytes or m_hash.group(1) != _kernel_hash():
+    if not m_hash or not m_bytes or m_hash.group(1) != _kernel_hash(kernel):
         return None
     return float(m_bytes.group(1))
 
@@ -254,6 +285,155 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_linear(args):
+    """The fused LM-head forward: one step = one fused_linear_logp_forward
+    call (contraction kernel + partial merge) over the whole batch."""
+    import torch
+
+    import selected_token_logprob_gb300 as flp
+    import workloads
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    flp._lib.load()
+    n, d, v = args.linear_n, args.linear_d, workloads.QWEN3_VOCAB
+    h, w, y = workloads.linear(n, d, v, seed=rank, device=dev)
+    ws = torch.empty(flp.fused_linear_logp_workspace_size(n, v), dtype=torch.uint8, device=dev)
+    logp = torch.empty(n, dtype=torch.float32, device=dev)
+    lse = torch.empty(n, dtype=torch.float32, device=dev)
+    lse_lo = torch.empty(n, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        flp.fused_linear_logp_forward(h, w, y, logp=logp, lse=lse, lse_lo=lse_lo, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    _barrier(world)
+    torch.cuda.synchronize(dev)
+    with sampler:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for k in range(args.steps):
+            ev[k][0].record(stream)
+            step()
+            ev[k][1].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    _barrier(world)
+    total_ms = _max_over_ranks(t0.elapsed_time(t1), world, dev)
+    ms_per_step = total_ms / args.steps
+    flops = 2.0 * n * v * d
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    call_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    achieved = flops / (call_ms * 1e-3) / 1e12
+    burst, sustained, src = _tensor_peaks()
+    e2e = _linear_e2e(args, flp, h, w, y, ws, dev, stream, world)
+    line = {
+        "metric": LIN_METRIC if (n, d) == (32768, 4096) else f"fused LM-head + logp forward TFLOP/s "
+                                                            f"at N={n}, D={d}, V={v} BF16",
+        "value": round(value, 1), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": LIN_DESC, "n": n, "d": d, "v": v,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"inputs ({(n + v) * d * 2 / 1e9:.2f} GB) exceed the 129 MB L2; no flush"},
+        "roofline": {"kernel": "k_linear_logp_tiles (+ k_linear_logp_merge in the timed call)",
+                     "bound": "tensor", "achieved": round(achieved, 1), "peak": burst, "unit": "TFLOP/s",
+                     "frac": round(achieved / burst, 4), "peak_source": src,
+                     "frac_of_sustained": round(achieved / sustained, 4),
+                     "traffic": _profiled_traffic("k_linear_logp_tiles")
+                     if (n, d) == (32768, 4096) else None},
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "clocks": sampler.summary(),
+    }
+    if rank == 0:
+        line["cpu_baseline"] = _linear_cpu_baseline(args, h, w, y, v, d)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def _linear_e2e(args, flp, h, w, y, ws, dev, stream, world):
+    """Through the public API with every input copied from pinned host memory
+    each step (hidden, targets and the LM-head weight) and logp/lse read back."""
+    import torch
+
+    n, d = h.shape
+    v = w.shape[0]
+    hh = torch.empty(h.shape, dtype=h.dtype, pin_memory=True)
+    hh.copy_(h)
+    hw = torch.empty(w.shape, dtype=w.dtype, pin_memory=True)
+    hw.copy_(w)
+    hy = y.cpu().pin_memory()
+    hlogp = torch.empty(n, dtype=torch.float32).pin_memory()
+    hlse = torch.empty(n, dtype=torch.float32).pin_memory()
+    dh, dw, dy = torch.empty_like(h), torch.empty_like(w), torch.empty_like(y)
+    logp = torch.empty(n, dtype=torch.float32, device=dev)
+    lse = torch.empty(n, dtype=torch.float32, device=dev)
+
+    def step():
+        dh.copy_(hh, non_blocking=True)
+        dw.copy_(hw, non_blocking=True)
+        dy.copy_(hy, non_blocking=True)
+        flp.fused_linear_logp_forward(dh, dw, dy, logp=logp, lse=lse, workspace=ws)
+        hlogp.copy_(logp, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+
+    steps = max(1, min(args.steps, args.e2e_steps))
+    step()
+    torch.cuda.synchronize(dev)
+    _barrier(world)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = _max_over_ranks(a.elapsed_time(b) / steps, world, dev)
+    return {"value": round(world * 2.0 * n * v * d / (ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 3), "steps": steps,
+            "h2d_bytes_per_step": (n + v) * d * 2 + n * 8, "d2h_bytes_per_step": n * 4 * 2}
+
+
+def _linear_cpu_baseline(args, h, w, y, v, d):
+    """The FP64 oracle on a bounded row sample of the same workload."""
+    import oracle
+    import workloads
+
+    if args.cpu_seconds <= 0:
+        return None
+    wb = workloads.bf16_bits(w)
+    hb = workloads.bf16_bits(h[:64])
+    yn = y[:64].cpu().numpy()
+    rows, t0 = 0, time.perf_counter()
+    while True:
+        k = 16
+        a = rows % 64
+        oracle.linear_logp(hb[a:a + k], wb, yn[a:a + k], d=d)
+        rows += k
+        el = time.perf_counter() - t0
+        if el >= args.cpu_seconds:
+            break
+    return {"value": round(2.0 * rows * v * d / el / 1e12, 5), "unit": "TFLOP/s",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{rows} rows of the fused LM-head workload (first rows of the batch, full "
+                      f"V x D contraction per row in FP64), {el:.1f} s"}
+
+
 def run_e2e(args, flp, x, y, g, dev, stream, world, temp=1.0, bpl=BYTES_PER_LOGIT):
     import torch
 
@@ -352,6 +532,8 @@ def run_reference(args):
     import workloads
 
     oracle.build()
+    if args.path == "linear":
+        return _run_reference_linear(args, world)
     wl = workloads.WORKLOADS[args.workload]
     rows = args.ref_rows
     x, y, g = workloads.make(wl, n=rows)   # same recipe, a bounded row sample, on the host
@@ -385,6 +567,40 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def _run_reference_linear(args, world):
+    """The FP64 oracle of the fused LM head on a bounded row sample."""
+    import oracle
+    import workloads
+
+    n, d, v = args.linear_n, args.linear_d, workloads.QWEN3_VOCAB
+    rows = max(1, min(args.ref_rows // 8, n))
+    h, w, y = workloads.linear(rows, d, v, seed=0)      # the recipe's first rows, on the host
+    hb, wb, yn = workloads.bf16_bits(h), workloads.bf16_bits(w), y.numpy()
+    for _ in range(min(args.warmup, 1)):
+        oracle.linear_logp(hb, wb, yn, d=d)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.linear_logp(hb, wb, yn, d=d)
+        times.append(time.perf_counter() - t0)
+    sec = statistics.mean(times)
+    value = 2.0 * rows * v * d / sec / 1e12
+    sample = f"{rows} rows of the fused LM-head workload per step (FP64 contraction + log-softmax)"
+    line = {
+        "metric": LIN_METRIC, "value": round(value, 5), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": LIN_DESC, "n": n, "d": d, "v": v, "rows_per_step": rows},
+        "cpu_baseline": {"value": round(value, 5), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 5), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -398,10 +614,17 @@ def main(argv=None):
     ap.add_argument("--dtype", choices=["bf16", "f16", "f32"], default="bf16",
                     help="logits dtype (the metric is quoted for bf16)")
     ap.add_argument("--temperature", type=float, default=1.0)
+    ap.add_argument("--path", choices=["logits", "linear"], default="logits",
+                    help="logits: logp fwd+bwd over BF16 logits (the headline); "
+                         "linear: fused LM head + logp forward")
+    ap.add_argument("--linear-n", type=int, default=32768)
+    ap.add_argument("--linear-d", type=int, default=4096)
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps
     if args.impl == "reference":
         run_reference(args)
+    elif args.path == "linear":
+        run_linear(args)
     else:
         run_ours(args)
 

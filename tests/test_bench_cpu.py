@@ -44,7 +44,7 @@ def test_profiled_traffic_requires_current_kernel_hash(tmp_path, monkeypatch):
     prof = tmp_path / "profiles"
     prof.mkdir()
     (tmp_path / "selected_token_logprob_gb300" / "csrc").mkdir(parents=True)
-    for fn in ("fused_logp.cu", "logp_kernels.cuh", "logp_prims.cuh"):
+    for fn in ("logp_kernels.cuh", "logp_prims.cuh"):
         src = os.path.join(bench.ROOT, "selected_token_logprob_gb300", "csrc", fn)
         (tmp_path / "selected_token_logprob_gb300" / "csrc" / fn).write_bytes(open(src, "rb").read())
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
