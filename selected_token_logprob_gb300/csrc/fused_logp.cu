@@ -299,8 +299,9 @@ EncodeTiledFn encode_tiled() {
 }
 
 // Tensor map of a BF16 row-major [rows, ld] matrix whose first `cols` columns
-// are used: boxes of 64 columns (128 bytes) x box_rows rows, 128-byte swizzle,
-// zero fill outside the matrix.
+// are used: boxes of kLinBK columns (one swizzle span) x box_rows rows, the
+// swizzle the contraction kernel's descriptors expect, zero fill outside the
+// matrix.
 flp_status make_tmap_bf16(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t ld,
                           uint32_t box_rows, const char* name) {
     const EncodeTiledFn fn = encode_tiled();
@@ -310,7 +311,8 @@ flp_status make_tmap_bf16(CUtensorMap* m, const void* ptr, int64_t rows, int64_t
     const cuuint32_t box[2] = {(cuuint32_t)flp::kLinBK, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          flp::kLinRowBytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(FLP_EINVAL, "tensor map of %s rejected by the driver (error %d)", name, (int)r);
     return FLP_OK;

@@ -12,8 +12,11 @@
 // Contraction kernel, one persistent CTA per SM, 6 warps:
 //   warp 0      TMA producer: for each tile and each 64-wide K block, one
 //               tensor-map copy of the H block (128 x 64) and one of the W
-//               block (256 x 64) into a 4-stage shared-memory ring, both with
-//               128-byte swizzle, completing on the stage's mbarrier;
+//               block (256 x 64) into a 4-stage shared-memory ring (192 KB in
+//               flight: the L2 latency under load is what the ring covers),
+//               both with 128-byte swizzle, completing on the stage's mbarrier
+//               (64-byte swizzle with 32-wide K blocks and 9 stages measured
+//               slower: the tensor pipe reads those operands more slowly);
 //   warp 1      allocates 512 TMEM columns (two 128 x 256 FP32 accumulators),
 //               and one elected lane issues tcgen05.mma (kind::f16, BF16 in,
 //               FP32 accumulate, M = 128, N = 256, K = 16), four per K block,
@@ -26,9 +29,10 @@
 //               accuracy) and, in the tile that holds the row's target, the
 //               selected logit; the accumulator is released as soon as it is
 //               read, so the epilogue of tile i overlaps the MMAs of tile i+1.
-// Tiles are visited in groups of 16 row blocks (vocabulary tiles outer, row
+// Tiles are visited in groups of 32 row blocks (vocabulary tiles outer, row
 // blocks inner) so that the CTAs running at one time share their W and H
-// blocks in L2.  A row's partials do not depend on which CTA, in which order,
+// blocks in L2 and the weight is read from DRAM once per group (a sweep of 16
+// to 64 measured 32 and 48 fastest; 64 thrashes L2).  A row's partials do not depend on which CTA, in which order,
 // computed them: each logit is one tensor-core dot product over K in a fixed
 // order, so the result is batch-invariant and deterministic.
 //
@@ -48,15 +52,22 @@ constexpr int kLinBM = 128;                 // rows (tokens) per tile: UMMA M
 constexpr int kLinBN = 256;                 // vocabulary columns per tile: UMMA N
 constexpr int kLinBK = 64;                  // K per stage: one 128-byte swizzle row of BF16
 constexpr int kLinUmmaK = 16;               // K of one tcgen05.mma kind::f16
-constexpr int kLinStages = 4;
+constexpr int kLinStages = 4;               // 4 x 48 KB in flight per SM
 constexpr int kLinThreads = 192;            // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
-constexpr int kLinGroupRows = 16;           // row blocks per raster group
+constexpr int kLinGroupRows = 32;           // row blocks per raster group (swept: 16-64)
 constexpr uint32_t kLinABytes = kLinBM * kLinBK * 2;
 constexpr uint32_t kLinBBytes = kLinBN * kLinBK * 2;
 constexpr uint32_t kLinStageBytes = kLinABytes + kLinBBytes;
 constexpr uint32_t kLinTmemCols = 2 * kLinBN;   // two accumulators
 constexpr uint32_t kLinBarBytes = 256;
 constexpr size_t kLinSmemBytes = 1024 + (size_t)kLinStages * kLinStageBytes + kLinBarBytes;
+// Swizzle of the staged operands: the K extent of a stage row, in bytes (64:
+// 64-byte swizzle, 128: 128-byte swizzle), and its 8-row repeat.
+constexpr uint32_t kLinRowBytes = kLinBK * 2;
+constexpr uint32_t kLinAtomBytes = 8 * kLinRowBytes;
+static_assert(kLinRowBytes == 64 || kLinRowBytes == 128, "stage rows must be one swizzle span");
+static_assert(kLinSmemBytes <= 232448, "shared memory per CTA");
+static_assert(2 * kLinStages * 8 + 48 <= kLinBarBytes, "barrier block");
 constexpr int kLinMergeThreads = 256;
 
 // Instruction descriptor of tcgen05.mma kind::f16: D in FP32 (bits 4-5 = 1),
@@ -65,16 +76,17 @@ constexpr int kLinMergeThreads = 256;
 constexpr uint32_t kLinIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
                                ((uint32_t)(kLinBN >> 3) << 17) | ((uint32_t)(kLinBM >> 4) << 24);
 
-// Shared-memory matrix descriptor of a K-major operand stored as rows of 128
-// bytes with the 128-byte swizzle (the layout the tensor-map copy writes):
-// start address >> 4 in bits 0-13, leading byte offset (unused for this
-// layout; 16 B) in bits 16-29, stride byte offset = 1024 B (8 rows of 128 B)
-// in bits 32-45, the descriptor version 1 in bits 46-47, swizzle mode 2
-// (128 B) in bits 61-63.  The buffer is 1024-byte aligned; the K step of 16
-// BF16 (32 B) inside the swizzle row advances the start address.
-__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
+// Shared-memory matrix descriptor of a K-major operand stored as rows of
+// kLinRowBytes with the matching swizzle (the layout the tensor-map copy
+// writes): start address >> 4 in bits 0-13, leading byte offset (unused for
+// this layout; 16 B) in bits 16-29, stride byte offset = 8 rows in bits
+// 32-45, the descriptor version 1 in bits 46-47, the swizzle mode in bits
+// 61-63 (2: 128-byte, 4: 64-byte).  The buffer is 1024-byte aligned; the K
+// step of 16 BF16 (32 B) inside the swizzle row advances the start address.
+__device__ __forceinline__ uint64_t umma_desc_swz(uint32_t saddr) {
+    constexpr uint64_t mode = (kLinRowBytes == 128) ? 2 : 4;
     return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) |
-           ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+           ((uint64_t)(kLinAtomBytes >> 4) << 32) | ((uint64_t)1 << 46) | (mode << 61);
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
@@ -306,8 +318,8 @@ k_linear_logp_tiles(const __grid_constant__ CUtensorMap tm_h, const __grid_const
                     }
                     tc_fence_after();
                     const uint32_t a_addr = base + stage * kLinStageBytes;
-                    const uint64_t a_desc = umma_desc_sw128(a_addr);
-                    const uint64_t b_desc = umma_desc_sw128(a_addr + kLinABytes);
+                    const uint64_t a_desc = umma_desc_swz(a_addr);
+                    const uint64_t b_desc = umma_desc_swz(a_addr + kLinABytes);
 #pragma unroll
                     for (int k = 0; k < kLinBK / kLinUmmaK; ++k) {
                         // K step of 16 BF16 = 32 bytes = 2 units of the 16-byte address field
