@@ -435,6 +435,12 @@ def _linear_cpu_baseline(args, h, w, y, v, d):
 
 
 def run_e2e(args, flp, x, y, g, dev, stream, world, temp=1.0, bpl=BYTES_PER_LOGIT):
+    """End to end through the public API: every step copies that step's
+    logits, targets and upstream gradients from pinned host memory and reads
+    logp and lse back.  The copy goes in row chunks on two copy streams, and
+    each chunk's forward + backward starts as soon as its rows have landed
+    (rows are independent and every row's result is batch-invariant, so the
+    chunked step gives the same bits as one call over all rows)."""
     import torch
 
     n, v = x.shape
@@ -451,13 +457,27 @@ def run_e2e(args, flp, x, y, g, dev, stream, world, temp=1.0, bpl=BYTES_PER_LOGI
     lse = torch.empty(n, dtype=torch.float32, device=dev)
     lse_lo = torch.empty(n, dtype=torch.float32, device=dev)
     dl = torch.empty_like(x)
+    chunks = max(1, min(args.e2e_chunks, n))
+    per = -(-n // chunks)
+    ranges = [(a, min(n, a + per)) for a in range(0, n, per)]
+    copy_streams = [torch.cuda.Stream(dev) for _ in range(2)]
+    landed = [torch.cuda.Event() for _ in ranges]
 
     def step():
-        dx.copy_(hx, non_blocking=True)
-        dy.copy_(hy, non_blocking=True)
-        dg.copy_(hg, non_blocking=True)
-        flp.fused_logp_forward(dx, dy, logp=logp, lse=lse, lse_lo=lse_lo, temperature=temp)
-        flp.fused_logp_backward(dx, dy, lse, dg, dlogits=dl, lse_lo=lse_lo, temperature=temp)
+        for k, (a, b) in enumerate(ranges):
+            cs = copy_streams[k % 2]
+            cs.wait_stream(stream)          # the previous step is done with these rows
+            with torch.cuda.stream(cs):
+                dx[a:b].copy_(hx[a:b], non_blocking=True)
+                dy[a:b].copy_(hy[a:b], non_blocking=True)
+                dg[a:b].copy_(hg[a:b], non_blocking=True)
+                landed[k].record(cs)
+        for k, (a, b) in enumerate(ranges):
+            stream.wait_event(landed[k])
+            flp.fused_logp_forward(dx[a:b], dy[a:b], logp=logp[a:b], lse=lse[a:b], lse_lo=lse_lo[a:b],
+                                   temperature=temp)
+            flp.fused_logp_backward(dx[a:b], dy[a:b], lse[a:b], dg[a:b], dlogits=dl[a:b],
+                                    lse_lo=lse_lo[a:b], temperature=temp)
         hlogp.copy_(logp, non_blocking=True)
         hlse.copy_(lse, non_blocking=True)
 
@@ -466,20 +486,20 @@ def run_e2e(args, flp, x, y, g, dev, stream, world, temp=1.0, bpl=BYTES_PER_LOGI
         step()
     torch.cuda.synchronize(dev)
     _barrier(world)
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
+    a_ev = torch.cuda.Event(enable_timing=True)
+    b_ev = torch.cuda.Event(enable_timing=True)
+    a_ev.record(stream)
     for _ in range(steps):
         step()
-    b.record(stream)
+    b_ev.record(stream)
     torch.cuda.synchronize(dev)
-    ms = _max_over_ranks(a.elapsed_time(b) / steps, world, dev)
+    ms = _max_over_ranks(a_ev.elapsed_time(b_ev) / steps, world, dev)
     del hx
     return {"value": round(world * n * v * bpl / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
             "ms_per_step": round(ms, 3), "steps": steps,
             "h2d_bytes_per_step": n * v * x.element_size() + n * 8 + n * 4,
-            "d2h_bytes_per_step": n * 4 * 2}
-
+            "d2h_bytes_per_step": n * 4 * 2,
+            "pipeline": f"{len(ranges)} row chunks, 2 copy streams overlapping the compute"}
 
 def _oracle_sample_rate(x_rows_u16, y_np, g_np, v, seconds: float):
     """GB/s-equivalent of the FP64 oracle (forward + dense backward) on a
@@ -609,6 +629,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="long")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-chunks", type=int, default=8,
+                    help="row chunks of the end-to-end step (host copies overlap the compute)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-rows", type=int, default=128)
     ap.add_argument("--dtype", choices=["bf16", "f16", "f32"], default="bf16",
