@@ -111,15 +111,18 @@ def _profiled_traffic(kernel: str):
 
 
 class ClockSampler:
-    """nvidia-smi samples (200 ms) during the timed region."""
+    """nvidia-smi samples (every 200 ms) kept only when their timestamp falls
+    inside the timed region (mark() is called at its start and end)."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
+        self.out = ""
+        self.window = None
 
     def __enter__(self):
         try:
@@ -127,9 +130,15 @@ class ClockSampler:
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.5)                  # let it start sampling before the timed region
         except (OSError, ValueError):
             self.proc = None
         return self
+
+    def mark(self):
+        """Call at the start and at the end of the timed region."""
+        now = time.time()
+        self.window = (now, None) if self.window is None or self.window[1] is not None else (self.window[0], now)
 
     def __exit__(self, *exc):
         self.out = ""
@@ -142,19 +151,32 @@ class ClockSampler:
                 self.out, _ = self.proc.communicate()
         return False
 
+    @staticmethod
+    def _stamp(text: str):
+        import datetime
+
+        try:
+            return datetime.datetime.strptime(text.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
     def summary(self):
-        rows = [r for r in csv.reader(io.StringIO(self.out or "")) if len(r) >= 9]
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
-        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
-        smax = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        rows = [r for r in csv.reader(io.StringIO(self.out or "")) if len(r) >= 10]
+        if self.window and self.window[1] is not None:
+            t0, t1 = self.window
+            inside = [r for r in rows if (ts := self._stamp(r[0])) is not None and t0 <= ts <= t1]
+        else:
+            inside = rows
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        sm = [float(r[2]) for r in inside if r[2].strip().replace(".", "").isdigit()]
+        smax = [float(r[3]) for r in inside if r[3].strip().replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i]
-                          and "Not" not in r[5 + i]})
+        reasons = sorted({names[i] for r in inside for i in range(4) if "Active" in r[6 + i]
+                          and "Not" not in r[6 + i]})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "reasons": reasons, "samples": len(rows)}
-
+                "reasons": reasons, "samples": len(inside)}
 
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -223,6 +245,7 @@ def run_ours(args):
     with sampler:
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
+        sampler.mark()
         t0.record(stream)
         for k in range(args.steps):
             ev[k][0].record(stream)
@@ -232,6 +255,7 @@ def run_ours(args):
             ev[k][2].record(stream)
         t1.record(stream)
         torch.cuda.synchronize(dev)
+        sampler.mark()
     _barrier(world)
     total_ms = _max_over_ranks(t0.elapsed_time(t1), world, dev)
     fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
@@ -322,6 +346,7 @@ def run_linear(args):
     with sampler:
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
+        sampler.mark()
         t0.record(stream)
         for k in range(args.steps):
             ev[k][0].record(stream)
@@ -329,6 +354,7 @@ def run_linear(args):
             ev[k][1].record(stream)
         t1.record(stream)
         torch.cuda.synchronize(dev)
+        sampler.mark()
     _barrier(world)
     total_ms = _max_over_ranks(t0.elapsed_time(t1), world, dev)
     ms_per_step = total_ms / args.steps
@@ -624,7 +650,8 @@ def _run_reference_linear(args, world):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200,
+                    help="timed steps (200 x 4.3 ms: long enough for several clock samples)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="long")

@@ -30,12 +30,22 @@ def test_reference_arm_json_line():
 
 def test_clock_summary_parsing():
     s = bench.ClockSampler(0)
-    s.out = ("0, 1980, 2070, 900.1, 0x0000000000000004, Not Active, Not Active, Not Active, Active\n"
-             "0, 1990, 2070, 950.0, 0x0, Not Active, Not Active, Not Active, Not Active\n"
-             "0, 2000, 2070, 980.5, 0x0, Not Active, Not Active, Not Active, Not Active\n")
-    c = s.summary()
+    s.out = ("2026/12/02 10:00:00.100, 0, 1500, 2070, 300.0, 0x0, Not Active, Not Active, Not Active, Not Active\n"
+             "2026/12/02 10:00:00.300, 0, 1980, 2070, 900.1, 0x0000000000000004, Not Active, Not Active, Not Active, Active\n"
+             "2026/12/02 10:00:00.500, 0, 1990, 2070, 950.0, 0x0, Not Active, Not Active, Not Active, Not Active\n"
+             "2026/12/02 10:00:00.700, 0, 2000, 2070, 980.5, 0x0, Not Active, Not Active, Not Active, Not Active\n"
+             "2026/12/02 10:00:00.900, 0, 900, 2070, 200.5, 0x0, Not Active, Active, Not Active, Not Active\n")
+    c = s.summary()                      # no window marked: every sample
+    assert c["samples"] == 5 and "hw_thermal_slowdown" in c["reasons"]
+    t = bench.ClockSampler._stamp
+    s.window = (t("2026/12/02 10:00:00.250"), t("2026/12/02 10:00:00.750"))
+    c = s.summary()                      # only the samples inside the timed region
     assert c["sm_mhz"] == 1990 and c["sm_max_mhz"] == 2070
     assert c["reasons"] == ["sw_power_cap"] and c["samples"] == 3
+    s.window = None
+    s.mark()
+    s.mark()
+    assert s.window[0] <= s.window[1]
     s.out = ""
     assert s.summary()["reasons"] == ["unavailable"]
 
