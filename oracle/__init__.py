@@ -77,6 +77,8 @@ def _load():
                                          _F64P, _F64P]
         lib.oracle_linear_logp.argtypes = [_U16P, _I64, _U16P, _I64, _I64, _I64, _I64, _I64P, _I64,
                                            V, D, _F64P, _F64P, V]
+        lib.oracle_linear_backward.argtypes = [_U16P, _I64, _U16P, _I64, _I64, _I64, _I64, _I64P, _I64,
+                                               V, D, _F32P, I, V, _F64P, _F64P]
         lib.oracle_num_threads.restype = ctypes.c_int
         _lib = lib
         return lib
@@ -242,6 +244,28 @@ def linear_logp(h, w, y, ignore_index: int = -100, d: int | None = None, scale: 
     _load().oracle_linear_logp(h, ldh, w, ldw, n, d, v, y, ignore_index, mp, float(scale), logp, lse,
                                bound.ctypes.data if with_bound else None)
     return (logp, lse, bound) if with_bound else (logp, lse)
+
+
+def linear_backward(h, w, y, g, ignore_index: int = -100, d: int | None = None, scale: float = 1.0,
+                    mask=None, round_dz: bool = True, with_dz: bool = False):
+    """FP64 (dH [n, d], dW [v, d]) of sum_t g_t logp_t of the fused LM head,
+    through dZ rounded to BF16 when `round_dz` (as the method writes dlogits);
+    with `with_dz`, also dZ [n, v]."""
+    h, w = _u16(h), _u16(w)
+    n, ldh = h.shape
+    v, ldw = w.shape
+    d = min(ldh, ldw) if d is None else int(d)
+    y = np.ascontiguousarray(y, dtype=np.int64)
+    g = np.ascontiguousarray(g, dtype=np.float32)
+    if y.shape != (n,) or g.shape != (n,):
+        raise ValueError("targets and grad must have shape [n]")
+    mk, mp = _mask(mask, n)
+    dh = np.empty((n, d), dtype=np.float64)
+    dw = np.empty((v, d), dtype=np.float64)
+    dz = np.empty((n, v), dtype=np.float64) if with_dz else None
+    _load().oracle_linear_backward(h, ldh, w, ldw, n, d, v, y, ignore_index, mp, float(scale), g,
+                                   int(bool(round_dz)), dz.ctypes.data if with_dz else None, dh, dw)
+    return (dh, dw, dz) if with_dz else (dh, dw)
 
 
 def range_partials(x, w: int, k: int, v: int | None = None, dtype: str | None = None,

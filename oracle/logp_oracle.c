@@ -362,6 +362,69 @@ void oracle_linear_logp(const uint16_t* h, int64_t ldh, const uint16_t* w, int64
     }
 }
 
+/* Backward of the fused LM head: the gradient of sum_t g_t logp_t through
+ * z = H W^T, i.e. the backward of RL-Kernel PR #495 (Summary item 2),
+ * dZ[t, j] = s g_t (onehot(y_t)[j] - exp(s z_tj - LSE_t)) for active rows
+ * (0 otherwise; the target column as -s g_t expm1(s z_ty - LSE_t)), followed
+ * by the chain rule through the contraction: dH = dZ W, dW = dZ^T H.  With
+ * round_dz, every dZ value is first rounded to BF16, as the method writes
+ * dlogits in BF16.  dz [n, v] (optional), dh [n, d], dw [v, d] are dense
+ * row-major doubles; everything is computed in double. */
+void oracle_linear_backward(const uint16_t* h, int64_t ldh, const uint16_t* w, int64_t ldw,
+                            int64_t n, int64_t d, int64_t v, const int64_t* y, int64_t ignore_index,
+                            const uint8_t* mask, double s, const float* g, int round_dz,
+                            double* dz_out, double* dh, double* dw) {
+    double* dz = dz_out ? dz_out : (double*)malloc(sizeof(double) * (size_t)(n * v));
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t t = 0; t < n; ++t) {
+        double* row = dz + t * v;
+        if (!row_active(y, mask, t, v, ignore_index)) {
+            for (int64_t j = 0; j < v; ++j) row[j] = 0.0;
+            continue;
+        }
+        double* hz = (double*)malloc(sizeof(double) * (size_t)d);
+        for (int64_t k = 0; k < d; ++k) hz[k] = bf16_bits_to_double(h[t * ldh + k]);
+        for (int64_t j = 0; j < v; ++j) {
+            const uint16_t* wj = w + j * ldw;
+            double acc = 0.0;
+            for (int64_t k = 0; k < d; ++k) acc += hz[k] * bf16_bits_to_double(wj[k]);
+            row[j] = s * acc;                         /* s z */
+        }
+        double m = -INFINITY;
+        for (int64_t j = 0; j < v; ++j)
+            if (row[j] > m) m = row[j];
+        double sum = 0.0;
+        for (int64_t j = 0; j < v; ++j) sum += exp(row[j] - m);
+        const double l = m + log(sum);
+        const double sg = s * (double)g[t];
+        for (int64_t j = 0; j < v; ++j)
+            row[j] = (j == y[t]) ? -sg * expm1(row[j] - l) : -sg * exp(row[j] - l);
+        if (round_dz)
+            for (int64_t j = 0; j < v; ++j) row[j] = bf16_bits_to_double(oracle_round_bf16(row[j]));
+        free(hz);
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < n; ++t) {
+        for (int64_t k = 0; k < d; ++k) dh[t * d + k] = 0.0;
+        for (int64_t j = 0; j < v; ++j) {
+            const double z = dz[t * v + j];
+            if (z == 0.0) continue;
+            const uint16_t* wj = w + j * ldw;
+            for (int64_t k = 0; k < d; ++k) dh[t * d + k] += z * bf16_bits_to_double(wj[k]);
+        }
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t j = 0; j < v; ++j) {
+        for (int64_t k = 0; k < d; ++k) dw[j * d + k] = 0.0;
+        for (int64_t t = 0; t < n; ++t) {
+            const double z = dz[t * v + j];
+            if (z == 0.0) continue;
+            for (int64_t k = 0; k < d; ++k) dw[j * d + k] += z * bf16_bits_to_double(h[t * ldh + k]);
+        }
+    }
+    if (!dz_out) free(dz);
+}
+
 /* ---- GRPO loss on the logp path -------------------------------------------- */
 
 /* Issue #241 PR 5 names the objective (ratio, clip, KL, advantage) and three

@@ -16,7 +16,9 @@ comparison) fails at least one of them:
   sharded merge equalling the unsharded log-sum-exp;
 * for the fused LM head: numpy float64 matmul + torch float64 log_softmax,
   one-hot weight rows reducing to the logits oracle, equal rows giving
-  -log V, a hand-worked two-column example.
+  -log V, a hand-worked two-column example; its backward against torch
+  float64 autograd, Richardson central differences of the forward, and the
+  BF16-rounded dZ times the operands by numpy matmul.
 """
 
 import math
@@ -710,3 +712,84 @@ def test_linear_logp_hand_example():
     assert lp[1] == pytest.approx(-math.log1p(math.exp(-5.0)), abs=1e-14)
     assert lse[0] == pytest.approx(math.log1p(math.exp(-5.0)), abs=1e-14)
     assert b[0] == 11.0 and b[1] == 11.0
+
+
+def _torch_linear_grads(h, w, y, g, s, mask=None):
+    """torch float64 autograd of sum_t g_t logp_t through z = H W^T."""
+    H = torch.from_numpy(oracle.bf16_to_f64(h)).requires_grad_(True)
+    W = torch.from_numpy(oracle.bf16_to_f64(w)).requires_grad_(True)
+    ls = torch.log_softmax(s * (H @ W.T), dim=1)
+    v = w.shape[0]
+    act = (y >= 0) & (y < v)
+    if mask is not None:
+        act &= mask != 0
+    sel = ls[torch.arange(len(y)), torch.from_numpy(np.clip(y, 0, v - 1))]
+    F = (sel * torch.from_numpy(g.astype(np.float64)) * torch.from_numpy(act.astype(np.float64))).sum()
+    F.backward()
+    return H.grad.numpy(), W.grad.numpy()
+
+
+def test_linear_backward_matches_torch_autograd():
+    """The unrounded oracle gradient equals torch float64 autograd of
+    sum g logp through H W^T (non-square shapes, temperature, mask, ignore)."""
+    rng = np.random.default_rng(31)
+    n, d, v = 6, 40, 97
+    h = _bf16_of(rng.standard_normal((n, d)))
+    w = _bf16_of(rng.standard_normal((v, d)) * 0.3)
+    y = np.array([0, 96, IGN, 5, 50, 200], dtype=np.int64)
+    g = rng.standard_normal(n).astype(np.float32)
+    mask = np.array([1, 1, 1, 0, 1, 1], dtype=np.uint8)
+    s = float(np.float32(1 / 0.7))
+    dh, dw = oracle.linear_backward(h, w, y, g, scale=s, mask=mask, round_dz=False)
+    th, tw = _torch_linear_grads(h, w, y, g, s, mask)
+    np.testing.assert_allclose(dh, th, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dw, tw, rtol=0, atol=1e-12)
+    assert np.all(dh[[2, 3, 5]] == 0)
+
+
+def test_linear_backward_by_central_differences():
+    """d/dH and d/dW of sum g logp (the oracle's forward) by Richardson-
+    extrapolated central differences on BF16-exact perturbations."""
+    rng = np.random.default_rng(32)
+    n, d, v = 3, 16, 11
+    h = _bf16_of(rng.uniform(0.5, 1.0, (n, d)))
+    w = _bf16_of(rng.uniform(0.5, 1.0, (v, d)))
+    y = np.array([1, 7, 10], dtype=np.int64)
+    g = np.array([0.5, -1.5, 2.0], dtype=np.float32)
+    dh, dw = oracle.linear_backward(h, w, y, g, round_dz=False)
+
+    def F(hh, ww):
+        lp, _ = oracle.linear_logp(hh, ww, y)
+        return float(np.dot(lp, g.astype(np.float64)))
+
+    def bump(a, idx, k):       # add k BF16 units in the last place (values in [0.5, 1): 2^-8)
+        b = a.copy()
+        b[idx] = _bf16_of(np.array([oracle.bf16_to_f64(a[idx]) + k * 2.0 ** -8]))[0]
+        return b
+
+    for arr, which, idx, ref in ((h, 0, (1, 3), dh[1, 3]), (w, 1, (7, 5), dw[7, 5]), (w, 1, (2, 0), dw[2, 0])):
+        def Fk(k):
+            hh, ww = (bump(h, idx, k), w) if which == 0 else (h, bump(w, idx, k))
+            return F(hh, ww)
+        e = 2.0 ** -8
+        c1 = (Fk(1) - Fk(-1)) / (2 * e)
+        c2 = (Fk(2) - Fk(-2)) / (4 * e)
+        rich = (4 * c1 - c2) / 3
+        assert rich == pytest.approx(ref, rel=1e-5, abs=1e-8), (which, idx, rich, ref)
+
+
+def test_linear_backward_rounded_dz_equals_bf16_dz_times_weights():
+    """round_dz: dH and dW are the BF16-rounded dZ times W and H exactly (numpy
+    float64 matmul), and dZ rows sum to ~0 for active rows."""
+    rng = np.random.default_rng(33)
+    n, d, v = 5, 24, 300
+    h = _bf16_of(rng.standard_normal((n, d)))
+    w = _bf16_of(rng.standard_normal((v, d)) * 0.2)
+    y = rng.integers(0, v, n)
+    g = rng.standard_normal(n).astype(np.float32)
+    dh, dw, dz = oracle.linear_backward(h, w, y, g, with_dz=True)
+    _, _, dz0 = oracle.linear_backward(h, w, y, g, round_dz=False, with_dz=True)
+    assert np.array_equal(dz, oracle.bf16_to_f64(oracle.round_bf16(dz0)))
+    np.testing.assert_allclose(dh, dz @ oracle.bf16_to_f64(w), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dw, dz.T @ oracle.bf16_to_f64(h), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dz0.sum(axis=1), 0.0, atol=1e-12)
