@@ -230,6 +230,40 @@ flp_status fused_linear_logp_forward(const void* hidden, int64_t n, int64_t d, i
                                      float* lse_lo, flp_stream_t stream);
 
 /*
+ * Backward of the fused LM head (no counterpart in the pages beyond the name
+ * linear_logp; the method's backward, PR #495 Summary item 2, taken through
+ * the contraction): for the loss sum_t grad[t] logp[t],
+ *   dZ[t, j] = s grad[t] (onehot(y_t)[j] - exp(s z[t, j] - LSE_t)),
+ *   dhidden = dZ W   [n, d],   dweight = dZ^T H   [v, d],
+ * with dZ recomputed on the tensor cores from hidden and weight and the
+ * forward's lse (+ lse_lo) and written in BF16 (as the method writes dlogits)
+ * one chunk of 2048 rows at a time into the workspace, never as an [n, v]
+ * tensor; the two products are plain GEMMs on the GPU's GEMM library (FP32
+ * accumulation, no atomic split-K reduction: deterministic).
+ *   hidden, weight, targets, ignore_index, active_mask, inv_temperature: as
+ *             for fused_linear_logp_forward (the same call's arguments)
+ *   lse       [n] FP32, lse_lo [n] FP32 or NULL: the forward's outputs
+ *   grad      [n] FP32 d loss / d logp (0 for inactive rows by definition)
+ *   workspace device scratch of fused_linear_logp_backward_workspace_size
+ *             bytes (256-byte aligned), caller-owned: dZ [2048, ceil(v/8)*8]
+ *             BF16, a [2048, d] FP32 block, 32 MiB for the GEMM library
+ *   dhidden   [n, ld_dh] FP32 out; dweight [v, ld_dw] FP32 out (overwritten,
+ *             not accumulated; all zero when n == 0)
+ * Every chunk has the same shape (the last one padded with zero-gradient
+ * rows), so a row's dhidden does not depend on n or on its position.
+ * Requirements and errors as for the forward, plus ld_dh, ld_dw >= d.
+ * Asynchronous on `stream`; the library allocates no device memory (the GEMM
+ * library's handle is created once per device).
+ */
+flp_status fused_linear_logp_backward_workspace_size(int64_t d, int64_t v, int64_t* bytes);
+flp_status fused_linear_logp_backward(const void* hidden, int64_t n, int64_t d, int64_t ld_h, const void* weight,
+                                      int64_t v, int64_t ld_w, const int64_t* targets, int64_t ignore_index,
+                                      const uint8_t* active_mask, float inv_temperature, const float* lse,
+                                      const float* lse_lo, const float* grad, void* workspace,
+                                      int64_t workspace_bytes, float* dhidden, int64_t ld_dh, float* dweight,
+                                      int64_t ld_dw, flp_stream_t stream);
+
+/*
  * Fused LM head + logp with no allocation and no workspace argument.  The
  * pages have no counterpart: this is a convenience of this library.
  *

@@ -52,6 +52,8 @@ __all__ = [
     "fused_logp",
     "fused_logp_backward",
     "fused_logp_forward",
+    "fused_linear_logp_backward",
+    "fused_linear_logp_backward_workspace_size",
     "fused_linear_logp_forward",
     "fused_linear_logp_forward_noalloc",
     "fused_linear_logp_workspace_size",
@@ -356,6 +358,64 @@ def fused_linear_logp_forward(hidden: torch.Tensor, weight: torch.Tensor, target
             lse.data_ptr(), _opt_ptr(lse_lo), _stream(hidden))
         _lib.check("fused_linear_logp_forward", st)
     return (logp, lse, lse_lo) if want_lo else (logp, lse)
+
+
+def fused_linear_logp_backward_workspace_size(d: int, v: int) -> int:
+    """Bytes of device scratch that fused_linear_logp_backward needs."""
+    import ctypes
+
+    b = ctypes.c_int64(0)
+    _lib.check("fused_linear_logp_backward_workspace_size",
+               _lib.load().fused_linear_logp_backward_workspace_size(int(d), int(v), ctypes.byref(b)))
+    return int(b.value)
+
+
+def fused_linear_logp_backward(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
+                               lse: torch.Tensor, grad: torch.Tensor, ignore_index: int = IGNORE_INDEX,
+                               lse_lo: torch.Tensor | None = None, temperature: float = 1.0,
+                               active_mask: torch.Tensor | None = None,
+                               dhidden: torch.Tensor | None = None, dweight: torch.Tensor | None = None,
+                               workspace: torch.Tensor | None = None):
+    """(dhidden [N, D], dweight [V, D]) FP32 of sum_t grad[t] logp[t] for the
+    fused LM head, from the forward's lse (and lse_lo); dZ is recomputed on
+    the tensor cores in 2048-row chunks and never stored for all rows."""
+    n, d, ld_h = _rows(hidden, "hidden")
+    v, d_w, ld_w = _rows(weight, "weight")
+    if hidden.dtype != torch.bfloat16 or weight.dtype != torch.bfloat16:
+        raise TypeError("hidden and weight must be bfloat16")
+    if d_w != d:
+        raise ValueError(f"hidden has {d} columns but weight has {d_w}")
+    inv_t = _inv_temperature(temperature)
+    _vec(targets, "targets", n, torch.int64)
+    _vec(lse, "lse", n, torch.float32)
+    _vec(grad, "grad", n, torch.float32)
+    dev = hidden.device
+    if lse_lo is not None:
+        _vec(lse_lo, "lse_lo", n, torch.float32)
+        _cuda(lse_lo)
+    if dhidden is None:
+        dhidden = torch.empty((n, d), dtype=torch.float32, device=dev)
+    if dweight is None:
+        dweight = torch.empty((v, d), dtype=torch.float32, device=dev)
+    if dhidden.dtype != torch.float32 or tuple(dhidden.shape) != (n, d):
+        raise ValueError("dhidden must be float32 [N, D]")
+    if dweight.dtype != torch.float32 or tuple(dweight.shape) != (v, d):
+        raise ValueError("dweight must be float32 [V, D]")
+    _, _, ld_dh = _rows(dhidden, "dhidden")
+    _, _, ld_dw = _rows(dweight, "dweight")
+    _cuda(hidden, weight, targets, lse, grad, dhidden, dweight)
+    mp = _mask(active_mask, n)
+    need = fused_linear_logp_backward_workspace_size(d, v)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    _cuda(workspace)
+    st = _lib.load().fused_linear_logp_backward(
+        hidden.data_ptr(), n, d, ld_h, weight.data_ptr(), v, ld_w, targets.data_ptr(), int(ignore_index), mp,
+        inv_t, lse.data_ptr(), _opt_ptr(lse_lo), grad.data_ptr(), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), dhidden.data_ptr(), ld_dh, dweight.data_ptr(), ld_dw,
+        _stream(hidden))
+    _lib.check("fused_linear_logp_backward", st)
+    return dhidden, dweight
 
 
 def fused_linear_logp_forward_noalloc(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,

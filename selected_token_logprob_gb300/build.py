@@ -31,7 +31,7 @@ def nvcc() -> str:
 
 def command(out: str) -> list[str]:
     return [nvcc(), ARCH, "-lineinfo", "-O3", "-std=c++17", "-Xptxas", "-v",
-            "-I" + INCLUDE, "-Xcompiler", "-fPIC", "-shared", *SOURCES, "-o", out]
+            "-I" + INCLUDE, "-Xcompiler", "-fPIC", "-shared", *SOURCES, "-o", out, "-lcublasLt"]
 
 
 def stale() -> bool:

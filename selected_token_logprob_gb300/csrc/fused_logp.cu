@@ -2,6 +2,7 @@
 // configuration and the extern "C" entry points declared in
 // include/fused_logp.h.  All checks run on the host before any launch and
 // report through the return code (no device-side traps).
+#include <cublasLt.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdarg.h>
@@ -321,12 +322,96 @@ flp_status make_tmap_bf16(CUtensorMap* m, const void* ptr, int64_t rows, int64_t
 flp_status linear_setup(int dev) {
     static bool ready[kMaxDevices];
     if (!ready[dev]) {
-        const cudaError_t e = cudaFuncSetAttribute(flp::k_linear_logp_tiles,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   (int)flp::kLinSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(flp::k_linear_logp_tiles<false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)flp::kLinSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(flp::k_linear_logp_tiles<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)flp::kLinSmemBytes);
         if (e != cudaSuccess) return fail(FLP_ECUDA, "linear logp setup: %s", cudaGetErrorString(e));
         ready[dev] = true;
     }
+    return FLP_OK;
+}
+
+// ---- fused LM head backward: row chunks and the two plain GEMMs
+
+// Rows per chunk of the backward: every chunk (the last one padded with zero
+// gradient rows) has this shape, so a row's dH does not depend on the batch.
+constexpr int64_t kLinGradChunk = 2048;
+constexpr int64_t kLtWorkspaceBytes = (int64_t)32 << 20;
+
+int64_t align256(int64_t b) { return ceil_div(b, 256) * 256; }
+
+// Backward workspace: dZ [chunk, ld_dz] BF16, a dH chunk [chunk, d] FP32 for
+// the last (padded) chunk, and the GEMM library's workspace.
+bool linear_grad_workspace(int64_t d, int64_t v, int64_t* ld_dz, int64_t* off_dh, int64_t* off_lt,
+                           int64_t* total) {
+    const int64_t ld = ceil_div(v, 8) * 8;
+    int64_t a, b;
+    if (__builtin_mul_overflow(kLinGradChunk, ld, &a) || __builtin_mul_overflow(a, (int64_t)2, &a)) return false;
+    if (__builtin_mul_overflow(kLinGradChunk, d, &b) || __builtin_mul_overflow(b, (int64_t)4, &b)) return false;
+    *ld_dz = ld;
+    *off_dh = align256(a);
+    *off_lt = *off_dh + align256(b);
+    *total = *off_lt + kLtWorkspaceBytes;
+    return true;
+}
+
+cublasLtHandle_t lt_handle(int dev) {
+    static cublasLtHandle_t handles[kMaxDevices];
+    if (handles[dev] == nullptr) {
+        cublasLtHandle_t h = nullptr;
+        if (cublasLtCreate(&h) != CUBLAS_STATUS_SUCCESS) return nullptr;
+        handles[dev] = h;
+    }
+    return handles[dev];
+}
+
+// C (m x n, FP32, column-major, ldc) = op(A) op(B) + beta C with A, B BF16
+// column-major: a plain GEMM on the library, FP32 accumulation, no in-place
+// (atomic) split-K reduction, so the result is deterministic.
+flp_status lt_gemm(cublasLtHandle_t lt, cublasOperation_t opa, cublasOperation_t opb, int64_t m, int64_t n,
+                   int64_t k, const void* A, int64_t lda, const void* B, int64_t ldb, float beta, float* C,
+                   int64_t ldc, void* ws, cudaStream_t stream, const char* what) {
+    cublasLtMatmulDesc_t op = nullptr;
+    cublasLtMatrixLayout_t la = nullptr, lb = nullptr, lc = nullptr;
+    cublasLtMatmulPreference_t pref = nullptr;
+    cublasStatus_t st = cublasLtMatmulDescCreate(&op, CUBLAS_COMPUTE_32F, CUDA_R_32F);
+    if (st == CUBLAS_STATUS_SUCCESS)
+        st = cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSA, &opa, sizeof opa);
+    if (st == CUBLAS_STATUS_SUCCESS)
+        st = cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSB, &opb, sizeof opb);
+    if (st == CUBLAS_STATUS_SUCCESS)
+        st = cublasLtMatrixLayoutCreate(&la, CUDA_R_16BF, opa == CUBLAS_OP_N ? m : k, opa == CUBLAS_OP_N ? k : m,
+                                        lda);
+    if (st == CUBLAS_STATUS_SUCCESS)
+        st = cublasLtMatrixLayoutCreate(&lb, CUDA_R_16BF, opb == CUBLAS_OP_N ? k : n, opb == CUBLAS_OP_N ? n : k,
+                                        ldb);
+    if (st == CUBLAS_STATUS_SUCCESS) st = cublasLtMatrixLayoutCreate(&lc, CUDA_R_32F, m, n, ldc);
+    if (st == CUBLAS_STATUS_SUCCESS) st = cublasLtMatmulPreferenceCreate(&pref);
+    const uint64_t wsb = (uint64_t)kLtWorkspaceBytes;
+    const uint32_t schemes = CUBLASLT_REDUCTION_SCHEME_NONE | CUBLASLT_REDUCTION_SCHEME_COMPUTE_TYPE |
+                             CUBLASLT_REDUCTION_SCHEME_OUTPUT_TYPE;
+    if (st == CUBLAS_STATUS_SUCCESS)
+        st = cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES, &wsb, sizeof wsb);
+    if (st == CUBLAS_STATUS_SUCCESS)
+        st = cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_REDUCTION_SCHEME_MASK, &schemes,
+                                                  sizeof schemes);
+    cublasLtMatmulHeuristicResult_t heur{};
+    int found = 0;
+    if (st == CUBLAS_STATUS_SUCCESS)
+        st = cublasLtMatmulAlgoGetHeuristic(lt, op, la, lb, lc, lc, pref, 1, &heur, &found);
+    if (st == CUBLAS_STATUS_SUCCESS && found < 1) st = CUBLAS_STATUS_NOT_SUPPORTED;
+    const float alpha = 1.f;
+    if (st == CUBLAS_STATUS_SUCCESS)
+        st = cublasLtMatmul(lt, op, &alpha, A, la, B, lb, &beta, C, lc, C, lc, &heur.algo, ws, kLtWorkspaceBytes,
+                            stream);
+    if (pref) cublasLtMatmulPreferenceDestroy(pref);
+    if (lc) cublasLtMatrixLayoutDestroy(lc);
+    if (lb) cublasLtMatrixLayoutDestroy(lb);
+    if (la) cublasLtMatrixLayoutDestroy(la);
+    if (op) cublasLtMatmulDescDestroy(op);
+    if (st != CUBLAS_STATUS_SUCCESS) return fail(FLP_ECUDA, "%s: GEMM library status %d", what, (int)st);
     return FLP_OK;
 }
 
@@ -617,17 +702,143 @@ flp_status fused_linear_logp_forward(const void* hidden, int64_t n, int64_t d, i
     a.pm = ws;
     a.ps = ws + nvt * n;
     a.xsel = ws + 2 * nvt * n;
+    a.n_valid = n;
+    a.lse = nullptr;
+    a.lse_lo = nullptr;
+    a.g = nullptr;
+    a.inv_s = 0.f;
+    a.dz = nullptr;
+    a.ld_dz = 0;
     const int sms = sm_count(dev);
     if (sms <= 0) return fail(FLP_ECUDA, "cannot read the SM count of device %d", dev);
     const int64_t ntiles = nrb * nvt;
     const int grid = (int)(ntiles < sms ? ntiles : sms);
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    flp::k_linear_logp_tiles<<<grid, flp::kLinThreads, flp::kLinSmemBytes, s>>>(tm_h, tm_w, a);
+    flp::k_linear_logp_tiles<false><<<grid, flp::kLinThreads, flp::kLinSmemBytes, s>>>(tm_h, tm_w, a);
     if ((st = check_launch("linear logp tiles")) != FLP_OK) return st;
     flp::k_linear_logp_merge<<<grid_for(ceil_div(n, flp::kLinMergeThreads)), flp::kLinMergeThreads, 0, s>>>(
         a.pm, a.ps, a.xsel, n, (int)nvt, v, targets, ignore_index, active_mask, inv_temperature, logp, lse,
         lse_lo);
     return check_launch("linear logp merge");
+}
+
+flp_status fused_linear_logp_backward_workspace_size(int64_t d, int64_t v, int64_t* bytes) {
+    if (bytes == nullptr) return fail(FLP_EINVAL, "bytes is a null pointer");
+    if (d < 1 || v < 1) return fail(FLP_EINVAL, "d and v must be >= 1");
+    int64_t ld, off_dh, off_lt;
+    if (!linear_grad_workspace(d, v, &ld, &off_dh, &off_lt, bytes))
+        return fail(FLP_EINVAL, "workspace size overflows int64");
+    return ok();
+}
+
+flp_status fused_linear_logp_backward(const void* hidden, int64_t n, int64_t d, int64_t ld_h, const void* weight,
+                                      int64_t v, int64_t ld_w, const int64_t* targets, int64_t ignore_index,
+                                      const uint8_t* active_mask, float inv_temperature, const float* lse,
+                                      const float* lse_lo, const float* grad, void* workspace,
+                                      int64_t workspace_bytes, float* dhidden, int64_t ld_dh, float* dweight,
+                                      int64_t ld_dw, flp_stream_t stream) {
+    flp_status st;
+    if ((st = check_scale(inv_temperature)) != FLP_OK) return st;
+    if (n < 0) return fail(FLP_EINVAL, "n must be >= 0 (got %lld)", (long long)n);
+    if (d < 1) return fail(FLP_EINVAL, "d must be >= 1 (got %lld)", (long long)d);
+    if (v < 1) return fail(FLP_EINVAL, "v must be >= 1 (got %lld)", (long long)v);
+    if (ld_h < d || ld_w < d || ld_dh < d || ld_dw < d)
+        return fail(FLP_EINVAL, "ld_h, ld_w, ld_dh and ld_dw must be >= d (%lld)", (long long)d);
+    const int64_t kMaxDim = ((int64_t)1 << 31) - 1;
+    if (n > kMaxDim || v > kMaxDim || d > kMaxDim || ld_w > kMaxDim || ld_h > kMaxDim || ld_dh > kMaxDim ||
+        ld_dw > kMaxDim)
+        return fail(FLP_EUNSUPPORTED, "sizes and strides must be below 2^31");
+    if (!aligned16(hidden) || !aligned16(weight) || (ld_h % 8) != 0 || (ld_w % 8) != 0)
+        return fail(FLP_EUNSUPPORTED,
+                    "hidden and weight must start on 16-byte boundaries with row strides a multiple of 8 elements");
+    int64_t ld_dz, off_dh, off_lt, need;
+    if (!linear_grad_workspace(d, v, &ld_dz, &off_dh, &off_lt, &need))
+        return fail(FLP_EINVAL, "workspace size overflows int64");
+    if (workspace_bytes < need)
+        return fail(FLP_EINVAL, "workspace_bytes (%lld) is below the %lld bytes needed", (long long)workspace_bytes,
+                    (long long)need);
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(FLP_EINVAL, "workspace must start on a 256-byte boundary");
+    if (n == 0) {   // no rows: dW = 0
+        int dev0;
+        if ((st = device_of(dweight, "dweight", &dev0)) != FLP_OK) return st;
+        DeviceGuard g0;
+        if ((st = g0.enter(dev0)) != FLP_OK) return st;
+        const cudaError_t e = cudaMemset2DAsync(dweight, (size_t)ld_dw * 4, 0, (size_t)d * 4, (size_t)v,
+                                                reinterpret_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return fail(FLP_ECUDA, "clearing dweight: %s", cudaGetErrorString(e));
+        return ok();
+    }
+    const void* ptrs[] = {hidden, weight, targets, lse, grad, workspace, dhidden, dweight, lse_lo, active_mask};
+    const char* names[] = {"hidden", "weight", "targets", "lse", "grad", "workspace", "dhidden", "dweight",
+                           "lse_lo", "active_mask"};
+    const bool optional[] = {false, false, false, false, false, false, false, false, true, true};
+    int dev;
+    if ((st = common_device(10, ptrs, names, optional, &dev)) != FLP_OK) return st;
+    if (dev < 0 || dev >= kMaxDevices) return fail(FLP_ECUDA, "device index %d out of range", dev);
+    DeviceGuard guard;
+    if ((st = guard.enter(dev)) != FLP_OK) return st;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if ((st = linear_setup(dev)) != FLP_OK) return st;
+    cublasLtHandle_t lt = lt_handle(dev);
+    if (lt == nullptr) return fail(FLP_ECUDA, "cannot create a GEMM library handle on device %d", dev);
+    const int sms = sm_count(dev);
+    if (sms <= 0) return fail(FLP_ECUDA, "cannot read the SM count of device %d", dev);
+
+    CUtensorMap tm_w;
+    if ((st = make_tmap_bf16(&tm_w, weight, v, d, ld_w, flp::kLinBN, "weight")) != FLP_OK) return st;
+    char* ws = static_cast<char*>(workspace);
+    uint16_t* dz = reinterpret_cast<uint16_t*>(ws);
+    float* dh_pad = reinterpret_cast<float*>(ws + off_dh);
+    void* lt_ws = ws + off_lt;
+    const int64_t nvt = linear_vocab_tiles(v);
+    const int64_t nrb = kLinGradChunk / flp::kLinBM;
+    const int64_t ntiles = nrb * nvt;
+    const int grid = (int)(ntiles < sms ? ntiles : sms);
+    const char* hb = static_cast<const char*>(hidden);
+    for (int64_t start = 0; start < n; start += kLinGradChunk) {
+        const int64_t rows = (n - start < kLinGradChunk) ? n - start : kLinGradChunk;
+        const void* h_chunk = hb + start * ld_h * 2;
+        CUtensorMap tm_h;
+        if ((st = make_tmap_bf16(&tm_h, h_chunk, rows, d, ld_h, flp::kLinBM, "hidden")) != FLP_OK) return st;
+        flp::LinArgs a;
+        a.n = kLinGradChunk;
+        a.v = v;
+        a.nrb = (int)nrb;
+        a.nvt = (int)nvt;
+        a.nkb = (int)ceil_div(d, flp::kLinBK);
+        a.y = targets + start;
+        a.ignore_index = ignore_index;
+        a.mask = active_mask ? active_mask + start : nullptr;
+        a.sc = make_scale(inv_temperature);
+        a.pm = a.ps = a.xsel = nullptr;
+        a.n_valid = rows;
+        a.lse = lse + start;
+        a.lse_lo = lse_lo ? lse_lo + start : nullptr;
+        a.g = grad + start;
+        a.inv_s = 1.f / inv_temperature;
+        a.dz = dz;
+        a.ld_dz = ld_dz;
+        flp::k_linear_logp_tiles<true><<<grid, flp::kLinThreads, flp::kLinSmemBytes, s>>>(tm_h, tm_w, a);
+        if ((st = check_launch("linear logp gradient tiles")) != FLP_OK) return st;
+        // dH rows = dZ W: column-major dH^T [d x chunk] = W^T [d x v] dZ^T [v x chunk], always a full chunk
+        const bool full = rows == kLinGradChunk;
+        float* dh_out = full ? dhidden + start * ld_dh : dh_pad;
+        if ((st = lt_gemm(lt, CUBLAS_OP_N, CUBLAS_OP_N, d, kLinGradChunk, v, weight, ld_w, dz, ld_dz, 0.f, dh_out,
+                          full ? ld_dh : d, lt_ws, s, "dhidden")) != FLP_OK)
+            return st;
+        if (!full) {
+            const cudaError_t e = cudaMemcpy2DAsync(dhidden + start * ld_dh, (size_t)ld_dh * 4, dh_pad,
+                                                    (size_t)d * 4, (size_t)d * 4, (size_t)rows,
+                                                    cudaMemcpyDeviceToDevice, s);
+            if (e != cudaSuccess) return fail(FLP_ECUDA, "copying dhidden: %s", cudaGetErrorString(e));
+        }
+        // dW (+)= dZ^T H: column-major dW^T [d x v] = H^T [d x rows] (dZ^T [v x rows])^T
+        if ((st = lt_gemm(lt, CUBLAS_OP_N, CUBLAS_OP_T, d, v, rows, h_chunk, ld_h, dz, ld_dz,
+                          start == 0 ? 0.f : 1.f, dweight, ld_dw, lt_ws, s, "dweight")) != FLP_OK)
+            return st;
+    }
+    return ok();
 }
 
 flp_status fused_linear_logp_forward_noalloc(const void* hidden, int64_t n, int64_t d, int64_t ld_h,

@@ -188,7 +188,64 @@ struct LinArgs {
     float* pm;     // [nvt, n] tile maxima
     float* ps;     // [nvt, n] tile sums
     float* xsel;   // [n] selected logit z[t, y_t] (active rows)
+    // gradient mode: rows [n_valid, n) are padding and get zero gradients
+    int64_t n_valid;
+    const float* lse;
+    const float* lse_lo;   // nullable
+    const float* g;
+    float inv_s;
+    uint16_t* dz;          // [n, ld_dz] BF16 dZ; columns [v, ld_dz) are written as 0
+    int64_t ld_dz;
 };
+
+// Per-row constants of dZ = s g (onehot - exp(s z - LSE)), split like the
+// logits backward: LSE (+ its residual) = lr + delta with lr on a 2^-16 grid,
+// coef = -s g (1 - delta + b) with b the mean exp2 bias, and logits below
+// (LSE - 200) / s raised to that bound (their exp is 0 in binary32).
+struct LinGradRow {
+    float s, lr, delta, gs, coef, floor_f;
+};
+
+__device__ __forceinline__ LinGradRow lin_grad_row(float l, float l_lo, float g, float s, float inv_s) {
+    LinGradRow r;
+    r.s = s;
+    r.gs = __fmul_rn(s, g);
+    r.lr = (fabsf(l) < 8388608.f) ? __fmul_rn(rintf(__fmul_rn(l, 65536.f)), 1.f / 65536.f) : l;
+    r.delta = __fadd_rn(__fsub_rn(l, r.lr), l_lo);                // l - lr is exact
+    r.coef = __fmaf_rn(r.gs, __fsub_rn(r.delta, kEx2BiasComp), -r.gs);
+    r.floor_f = __fmul_rn(__fsub_rn(l, 200.f), inv_s);
+    return r;
+}
+
+// dZ of one 32-column chunk of a row as 16 BF16 pairs: exp(t) = 2^a (1 + c)
+// with t = s z - lr, a = t log2 e rounded, c = t - a ln 2 by two fused
+// multiply-adds against a two-float ln 2; the target column jt (if in
+// [0, 32)) as -s g expm1(s z - LSE); columns at or beyond nvalid are 0.
+__device__ __forceinline__ void lin_grad_chunk(const uint32_t (&r)[32], const LinGradRow& g, int jt, int nvalid,
+                                               uint32_t (&o)[16]) {
+    float d[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const float z = fmaxf(__uint_as_float(r[j]), g.floor_f);
+        const float t = __fmaf_rn(z, g.s, -g.lr);
+        const float a = __fmul_rn(t, kLog2e);
+        const float c = __fmaf_rn(a, -kLn2Lo, __fmaf_rn(a, -kLn2Hi, t));
+        const float q = __fmul_rn(ex2_ftz(a), g.coef);
+        d[j] = (j < nvalid) ? __fmaf_rn(q, c, q) : 0.f;
+    }
+    if (jt >= 0 && jt < 32) {
+        float zt = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (j == jt) zt = __uint_as_float(r[j]);
+        const float dt = __fmul_rn(-g.gs, expm1f(__fsub_rn(__fmaf_rn(g.s, zt, -g.lr), g.delta)));
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (j == jt) d[j] = dt;
+    }
+#pragma unroll
+    for (int k = 0; k < 16; ++k) o[k] = pack_bf16x2(d[2 * k], d[2 * k + 1]);
+}
 
 // Reduce one 32-column chunk of a row into (m, s): columns at or beyond
 // `nvalid` are not part of the vocabulary.
@@ -222,6 +279,10 @@ __device__ __forceinline__ void lin_chunk(const uint32_t (&r)[32], int nvalid, c
     s = __fadd_rn(s, e[0]);
 }
 
+// kGrad = false: tile partials of the forward.  kGrad = true: the same
+// contraction with an epilogue that writes dZ in BF16 (the backward's
+// recomputation of the logits, which never reach memory in FP32).
+template <bool kGrad>
 __global__ void __launch_bounds__(kLinThreads, 1)
 k_linear_logp_tiles(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
                     LinArgs p) {
@@ -356,6 +417,50 @@ k_linear_logp_tiles(const __grid_constant__ CUtensorMap tm_h, const __grid_const
             tc_fence_after();
             const int64_t t = (int64_t)tl.rb * kLinBM + row;
             const int64_t col0 = (int64_t)tl.vt * kLinBN;
+            if constexpr (kGrad) {
+                bool act = false;
+                int64_t jt = -1;
+                LinGradRow gr{};
+                if (t < p.n_valid) {
+                    const int64_t yt = __ldg(p.y + t);
+                    act = row_active(p.mask, t, yt, p.v, p.ignore_index);
+                    if (act) {
+                        gr = lin_grad_row(__ldg(p.lse + t), p.lse_lo ? __ldg(p.lse_lo + t) : 0.f, __ldg(p.g + t),
+                                          p.sc.s, p.inv_s);
+                        if (yt >= col0 && yt < col0 + kLinBN) jt = yt - col0;
+                    }
+                }
+                const int nreal = (p.v - col0 < kLinBN) ? (int)(p.v - col0) : kLinBN;
+                uint16_t* drow = p.dz + t * p.ld_dz;
+#pragma unroll 1
+                for (int c = 0; c < kLinBN / 32; ++c) {
+                    const int64_t c0 = col0 + c * 32;
+                    if (c0 >= p.ld_dz) break;  // uniform over the CTA
+                    __syncwarp();
+                    uint32_t r[32];
+                    tmem_ld32(lane_addr + (uint32_t)(acc * kLinBN + c * 32), r);
+                    uint32_t o[16];
+                    if (act) {
+                        lin_grad_chunk(r, gr, (int)(jt - c * 32), nreal - c * 32, o);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) o[k] = 0u;
+                    }
+                    if (t < p.n) {
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4)
+                            if (c0 + 8 * q4 < p.ld_dz)
+                                st_cs_v4(drow + c0 + 8 * q4, make_uint4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]));
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(tempty0 + 8 * acc);
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+                continue;
+            }
             int64_t jt = -1;  // target column inside this tile, if the row is active
             if (t < p.n) {
                 const int64_t yt = __ldg(p.y + t);

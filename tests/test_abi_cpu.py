@@ -234,3 +234,23 @@ def test_linear_logp_noalloc_host_checks(lib):
     assert b"3528 rows" in msg and b"16777216" in msg
     assert call(3527) == EINVAL          # within the limit: reaches the pointer checks
     assert b"hidden" in lib.flp_last_error()
+
+
+def test_linear_backward_host_checks(lib):
+    b = ctypes.c_int64(0)
+    assert lib.fused_linear_logp_backward_workspace_size(4096, 151936, ctypes.byref(b)) == 0
+    assert b.value >= 2048 * 151936 * 2 + 2048 * 4096 * 4
+    assert lib.fused_linear_logp_backward_workspace_size(0, 10, ctypes.byref(b)) == EINVAL
+
+    def call(n=16, d=64, ld_h=64, v=100, ld_w=64, ws=1 << 20, ws_bytes=1 << 40, ld_dh=64, ld_dw=64, s=1.0):
+        return lib.fused_linear_logp_backward(1 << 20, n, d, ld_h, 1 << 21, v, ld_w, 1 << 22, -100, None, s,
+                                              1 << 23, None, 1 << 24, ws, ws_bytes, 1 << 25, ld_dh, 1 << 26,
+                                              ld_dw, None)
+
+    assert call(n=-1) == EINVAL
+    assert call(ld_dh=32) == EINVAL and call(ld_dw=8) == EINVAL
+    assert call(ld_h=68) == EUNSUP
+    assert call(ws_bytes=100) == EINVAL
+    assert call(ws=(1 << 20) + 16) == EINVAL          # not 256-byte aligned
+    assert call(s=-1.0) == EINVAL
+    assert call() == EINVAL                            # host pointers are not device memory

@@ -175,3 +175,144 @@ def test_matches_materialised_logits_path():
 
 def test_no_device_error():
     assert flp.flp_device_error(0) == 0
+
+
+# ---- backward ----------------------------------------------------------------
+#
+# dZ is checked against the oracle's correctly rounded BF16 dZ, read from the
+# documented workspace layout for a one-chunk call: every value within one
+# BF16 unit, and >= 99.9% equal.  Unlike the logits path (whose logits are
+# exact BF16 inputs, bar 99.99%), each logit here carries the FP32
+# contraction's error dz ~ 1e-6..1e-5: a value within that relative distance
+# r of a BF16 rounding boundary may round to its neighbour, a fraction of
+# about 2 r / 2^-8 = 512 r of the values (~0.05% at r ~ 1e-6); 99.9% leaves
+# twice the margin.
+# dhidden and dweight are checked against the oracle's FP64 products of its
+# rounded dZ with the operands; tolerance per element, with A = sum |dz| |op|
+# the absolute products and M = max |dz| |op| the largest single one:
+#     ceil(K/16) 2^-23 A  (FP32 accumulation, as in the forward's bound)
+#   + 3 * 2^-8 M          (up to three dZ values one BF16 unit off).
+
+def _grad_tol(dz, op, k):
+    adz, aop = np.abs(dz), np.abs(op)
+    A = adz @ aop
+    M = np.empty_like(A)          # largest single |dz_j op_jk| per output element
+    step = max(1, int(2e7 // (adz.shape[0] * adz.shape[1])))
+    for c in range(0, aop.shape[1], step):
+        M[:, c:c + step] = np.max(adz[:, :, None] * aop[None, :, c:c + step], axis=1)
+    return math.ceil(k / 16) * 2.0 ** -23 * A + 3 * 2.0 ** -8 * M
+
+
+def _backward_case(n, d, v, seed, temperature=1.0, mask=None, pad=0):
+    h, w, y = workloads.linear(n, d, v, seed=seed, device=DEV)
+    if pad:
+        h = _padded(h, d + pad, float("nan"))
+        w = _padded(w, d + pad, float("nan"))
+    g = torch.randn(n, generator=torch.Generator().manual_seed(seed)).to(DEV)
+    logp, lse, lo = flp.fused_linear_logp_forward(h, w, y, with_lse_lo=True, temperature=temperature,
+                                                  active_mask=mask)
+    ws = torch.empty(flp.fused_linear_logp_backward_workspace_size(d, v), dtype=torch.uint8, device=DEV)
+    dh, dw = flp.fused_linear_logp_backward(h, w, y, lse, g, lse_lo=lo, temperature=temperature,
+                                            active_mask=mask, workspace=ws)
+    torch.cuda.synchronize()
+    return h, w, y, g, dh, dw, ws
+
+
+@pytest.mark.parametrize("temperature", [1.0, 0.7])
+def test_backward_small_against_oracle(temperature):
+    n, d, v = 200, 520, 5000
+    mask = torch.ones(n, dtype=torch.bool, device=DEV)
+    mask[7::13] = False
+    h, w, y, g, dh, dw, ws = _backward_case(n, d, v, 41, temperature, mask=mask, pad=8)
+    y_np = y.cpu().numpy()
+    s = float(np.float32(1.0 / temperature))
+    hb, wb = workloads.bf16_bits(h), workloads.bf16_bits(w)
+    mk = mask.cpu().numpy().astype(np.uint8)
+    ref_dh, ref_dw, ref_dz = oracle.linear_backward(hb, wb, y_np, g.cpu().numpy(), d=d, scale=s, mask=mk,
+                                                    with_dz=True)
+    # dZ of the (single) chunk from the workspace: [2048, ceil(v/8)*8] BF16
+    ld_dz = -(-v // 8) * 8
+    dz_bits = ws[:n * ld_dz * 2].view(torch.int16).view(n, ld_dz)[:, :v].cpu().numpy().view(np.uint16)
+    got_dz = oracle.bf16_to_f64(dz_bits)
+    neq = int(np.sum(got_dz != ref_dz))
+    gap = np.spacing(np.abs(ref_dz).astype(np.float32)).astype(np.float64) * 2.0 ** 16
+    cr = 1 - neq / ref_dz.size
+    print(f"T={temperature}: dZ correctly rounded {100 * cr:.5f}% ({neq} of {ref_dz.size})")
+    assert cr >= 0.999
+    assert np.all(np.abs(got_dz - ref_dz) <= gap)
+    hd, wd = oracle.bf16_to_f64(hb)[:, :d], oracle.bf16_to_f64(wb)[:, :d]
+    e_dh = np.abs(dh.double().cpu().numpy() - ref_dh)
+    e_dw = np.abs(dw.double().cpu().numpy() - ref_dw)
+    tol_dh = _grad_tol(ref_dz, wd, v)
+    tol_dw = _grad_tol(ref_dz.T, hd, n)
+    print(f"T={temperature}: max |d dH| {e_dh.max():.3e} (max |dH| {np.abs(ref_dh).max():.3e}), "
+          f"max |d dW| {e_dw.max():.3e} (max |dW| {np.abs(ref_dw).max():.3e})")
+    assert np.all(e_dh <= tol_dh)
+    assert np.all(e_dw <= tol_dw)
+    off = (~mask.cpu().numpy()) | (y_np < 0)
+    assert np.all(dh.cpu().numpy()[off] == 0)
+
+
+def test_backward_two_chunks_against_oracle():
+    """2100 rows: a full chunk plus a padded one; dweight sums both."""
+    n, d, v = 2100, 128, 2000
+    h, w, y, g, dh, dw, _ = _backward_case(n, d, v, 42)
+    hb, wb = workloads.bf16_bits(h), workloads.bf16_bits(w)
+    ref_dh, ref_dw, ref_dz = oracle.linear_backward(hb, wb, y.cpu().numpy(), g.cpu().numpy(), with_dz=True)
+    hd, wd = oracle.bf16_to_f64(hb), oracle.bf16_to_f64(wb)
+    e_dh = np.abs(dh.double().cpu().numpy() - ref_dh)
+    e_dw = np.abs(dw.double().cpu().numpy() - ref_dw)
+    print(f"two chunks: max |d dH| {e_dh.max():.3e}, max |d dW| {e_dw.max():.3e}")
+    assert np.all(e_dh <= _grad_tol(ref_dz, wd, v))
+    assert np.all(e_dw <= _grad_tol(ref_dz.T, hd, n))
+
+
+def test_backward_full_size_sampled_rows_and_invariants():
+    """The benchmark's configuration: dhidden of sampled rows against the
+    oracle; dweight's columns sum to ~0 over the vocabulary (dZ rows sum to 0)."""
+    n, d, v = workloads.LINEAR_LONG
+    h, w, y = workloads.linear(n, d, v, seed=0, device=DEV)
+    g = (torch.randint(0, 2, (n,), generator=torch.Generator().manual_seed(3)).float() * 2 - 1).to(DEV) / n
+    logp, lse, lo = flp.fused_linear_logp_forward(h, w, y, with_lse_lo=True)
+    dh, dw = flp.fused_linear_logp_backward(h, w, y, lse, g, lse_lo=lo)
+    torch.cuda.synchronize()
+    assert torch.isfinite(dh).all() and torch.isfinite(dw).all()
+    rows = np.array([0, 2047, 2048, n - 1, 12345, 30000])
+    hb = workloads.bf16_bits(h[torch.as_tensor(rows, device=DEV)])
+    wb = workloads.bf16_bits(w)
+    ref_dh, _, ref_dz = oracle.linear_backward(hb, wb, y.cpu().numpy()[rows], g.cpu().numpy()[rows],
+                                               with_dz=True)
+    got = dh[torch.as_tensor(rows, device=DEV)].double().cpu().numpy()
+    e = np.abs(got - ref_dh)
+    A = np.abs(ref_dz) @ np.abs(oracle.bf16_to_f64(wb))
+    tol = math.ceil(v / 16) * 2.0 ** -23 * A + 3 * 2.0 ** -8 * A
+    print(f"long: max |d dH| {e.max():.3e} (max |dH| {np.abs(ref_dh).max():.3e})")
+    assert np.all(e <= tol)
+    colsum = dw.double().sum(dim=0).abs()
+    colabs = dw.double().abs().sum(dim=0)
+    assert torch.all(colsum <= 1e-3 * colabs + 1e-12)
+
+
+def test_backward_deterministic_and_batch_invariant():
+    d, v = 256, 3000
+    probes, w, py = workloads.linear(3, d, v, seed=51, device=DEV, ignore_frac=0.0)
+    filler, _, fy = workloads.linear(300, d, v, seed=52, device=DEV, ignore_frac=0.0)
+    gp = torch.tensor([0.5, -1.0, 2.0], device=DEV)
+    gf = torch.randn(300, generator=torch.Generator().manual_seed(53)).to(DEV)
+
+    def dh_rows(hh, yy, gg):
+        _, lse, lo = flp.fused_linear_logp_forward(hh, w, yy, with_lse_lo=True)
+        return flp.fused_linear_logp_backward(hh, w, yy, lse, gg, lse_lo=lo)
+
+    ref = [dh_rows(probes[k:k + 1], py[k:k + 1], gp[k:k + 1])[0] for k in range(3)]
+    for B, pos in ((2, 1), (129, 128), (300, 150)):
+        hb, yb, gb = filler[:B].clone(), fy[:B].clone(), gf[:B].clone()
+        k = B % 3
+        hb[pos], yb[pos], gb[pos] = probes[k], py[k], gp[k]
+        out = dh_rows(hb, yb, gb)[0]
+        assert torch.equal(out[pos:pos + 1].view(torch.int32), ref[k].view(torch.int32)), (B, pos)
+    a = dh_rows(filler, fy, gf)
+    b = dh_rows(filler, fy, gf)
+    assert torch.equal(a[0].view(torch.int32), b[0].view(torch.int32))
+    assert torch.equal(a[1].view(torch.int32), b[1].view(torch.int32))
+    assert flp.flp_device_error(0) == 0
