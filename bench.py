@@ -364,6 +364,7 @@ def run_linear(args):
     achieved = flops / (call_ms * 1e-3) / 1e12
     burst, sustained, src = _tensor_peaks()
     e2e = _linear_e2e(args, flp, h, w, y, ws, dev, stream, world)
+    bwd = _linear_backward_timing(args, flp, h, w, y, lse, lse_lo, dev, stream)
     line = {
         "metric": LIN_METRIC if (n, d) == (32768, 4096) else f"fused LM-head + logp forward TFLOP/s "
                                                             f"at N={n}, D={d}, V={v} BF16",
@@ -382,6 +383,7 @@ def run_linear(args):
         "e2e": e2e,
         "gpu_launches": 2 * args.steps,
         "clocks": sampler.summary(),
+        "backward": bwd,
     }
     if rank == 0:
         line["cpu_baseline"] = _linear_cpu_baseline(args, h, w, y, v, d)
@@ -390,6 +392,42 @@ def run_linear(args):
         import torch.distributed as dist
 
         dist.destroy_process_group()
+
+
+def _linear_backward_timing(args, flp, h, w, y, lse, lse_lo, dev, stream):
+    """The fused LM-head backward (dZ recomputed on the tensor cores per
+    2048-row chunk, dH and dW as two library GEMMs): 3 contractions of 2 N V D
+    FLOP each, timed separately from the forward's metric."""
+    import torch
+
+    n, d = h.shape
+    v = w.shape[0]
+    if args.linear_bwd_steps <= 0:
+        return None
+    g = torch.full((n,), 1.0 / n, dtype=torch.float32, device=dev)
+    wsb = torch.empty(flp.fused_linear_logp_backward_workspace_size(d, v), dtype=torch.uint8, device=dev)
+    dh = torch.empty((n, d), dtype=torch.float32, device=dev)
+    dw = torch.empty((v, d), dtype=torch.float32, device=dev)
+
+    def call():
+        flp.fused_linear_logp_backward(h, w, y, lse, g, lse_lo=lse_lo, dhidden=dh, dweight=dw, workspace=wsb)
+
+    call()
+    torch.cuda.synchronize(dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.linear_bwd_steps):
+        call()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / args.linear_bwd_steps
+    burst, sustained, _ = _tensor_peaks()
+    tf = 3 * 2.0 * n * v * d / (ms * 1e-3) / 1e12
+    return {"ms": round(ms, 3), "tflops": round(tf, 1), "frac": round(tf / burst, 4),
+            "frac_of_sustained": round(tf / sustained, 4), "steps": args.linear_bwd_steps,
+            "flop_per_call": 3 * 2.0 * n * v * d,
+            "kernels": "k_linear_logp_tiles<grad> (dZ, BF16) + 2 library GEMMs per 2048-row chunk"}
 
 
 def _linear_e2e(args, flp, h, w, y, ws, dev, stream, world):
@@ -668,6 +706,8 @@ def main(argv=None):
                          "linear: fused LM head + logp forward")
     ap.add_argument("--linear-n", type=int, default=32768)
     ap.add_argument("--linear-d", type=int, default=4096)
+    ap.add_argument("--linear-bwd-steps", type=int, default=5,
+                    help="timed calls of the fused LM-head backward (0: skip)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps
     if args.impl == "reference":
