@@ -396,7 +396,7 @@ def run_linear(args):
 
 def _linear_backward_timing(args, flp, h, w, y, lse, lse_lo, dev, stream):
     """The fused LM-head backward (dZ recomputed on the tensor cores per
-    2048-row chunk, dH and dW as two library GEMMs): 3 contractions of 2 N V D
+    4096-row chunk, dH and dW as two library GEMMs): 3 contractions of 2 N V D
     FLOP each, timed separately from the forward's metric."""
     import torch
 
@@ -427,7 +427,7 @@ def _linear_backward_timing(args, flp, h, w, y, lse, lse_lo, dev, stream):
     return {"ms": round(ms, 3), "tflops": round(tf, 1), "frac": round(tf / burst, 4),
             "frac_of_sustained": round(tf / sustained, 4), "steps": args.linear_bwd_steps,
             "flop_per_call": 3 * 2.0 * n * v * d,
-            "kernels": "k_linear_logp_tiles<grad> (dZ, BF16) + 2 library GEMMs per 2048-row chunk"}
+            "kernels": "k_linear_logp_tiles<grad> (dZ, BF16) + 2 library GEMMs per 4096-row chunk"}
 
 
 def _linear_e2e(args, flp, h, w, y, ws, dev, stream, world):

@@ -237,7 +237,7 @@ flp_status fused_linear_logp_forward(const void* hidden, int64_t n, int64_t d, i
  *   dhidden = dZ W   [n, d],   dweight = dZ^T H   [v, d],
  * with dZ recomputed on the tensor cores from hidden and weight and the
  * forward's lse (+ lse_lo) and written in BF16 (as the method writes dlogits)
- * one chunk of 2048 rows at a time into the workspace, never as an [n, v]
+ * one chunk of 4096 rows at a time into the workspace, never as an [n, v]
  * tensor; the two products are plain GEMMs on the GPU's GEMM library (FP32
  * accumulation, no atomic split-K reduction: deterministic).
  *   hidden, weight, targets, ignore_index, active_mask, inv_temperature: as
@@ -245,8 +245,8 @@ flp_status fused_linear_logp_forward(const void* hidden, int64_t n, int64_t d, i
  *   lse       [n] FP32, lse_lo [n] FP32 or NULL: the forward's outputs
  *   grad      [n] FP32 d loss / d logp (0 for inactive rows by definition)
  *   workspace device scratch of fused_linear_logp_backward_workspace_size
- *             bytes (256-byte aligned), caller-owned: dZ [2048, ceil(v/8)*8]
- *             BF16, a [2048, d] FP32 block, 32 MiB for the GEMM library
+ *             bytes (256-byte aligned), caller-owned: dZ [4096, ceil(v/8)*8]
+ *             BF16, a [4096, d] FP32 block, 32 MiB for the GEMM library
  *   dhidden   [n, ld_dh] FP32 out; dweight [v, ld_dw] FP32 out (overwritten,
  *             not accumulated; all zero when n == 0)
  * Every chunk has the same shape (the last one padded with zero-gradient

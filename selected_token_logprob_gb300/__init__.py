@@ -378,7 +378,7 @@ def fused_linear_logp_backward(hidden: torch.Tensor, weight: torch.Tensor, targe
                                workspace: torch.Tensor | None = None):
     """(dhidden [N, D], dweight [V, D]) FP32 of sum_t grad[t] logp[t] for the
     fused LM head, from the forward's lse (and lse_lo); dZ is recomputed on
-    the tensor cores in 2048-row chunks and never stored for all rows."""
+    the tensor cores in 4096-row chunks and never stored for all rows."""
     n, d, ld_h = _rows(hidden, "hidden")
     v, d_w, ld_w = _rows(weight, "weight")
     if hidden.dtype != torch.bfloat16 or weight.dtype != torch.bfloat16:

@@ -337,7 +337,7 @@ flp_status linear_setup(int dev) {
 
 // Rows per chunk of the backward: every chunk (the last one padded with zero
 // gradient rows) has this shape, so a row's dH does not depend on the batch.
-constexpr int64_t kLinGradChunk = 2048;
+constexpr int64_t kLinGradChunk = 4096;
 constexpr int64_t kLtWorkspaceBytes = (int64_t)32 << 20;
 
 int64_t align256(int64_t b) { return ceil_div(b, 256) * 256; }

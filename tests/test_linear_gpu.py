@@ -230,7 +230,7 @@ def test_backward_small_against_oracle(temperature):
     mk = mask.cpu().numpy().astype(np.uint8)
     ref_dh, ref_dw, ref_dz = oracle.linear_backward(hb, wb, y_np, g.cpu().numpy(), d=d, scale=s, mask=mk,
                                                     with_dz=True)
-    # dZ of the (single) chunk from the workspace: [2048, ceil(v/8)*8] BF16
+    # dZ of the (single) chunk from the workspace: [4096, ceil(v/8)*8] BF16
     ld_dz = -(-v // 8) * 8
     dz_bits = ws[:n * ld_dz * 2].view(torch.int16).view(n, ld_dz)[:, :v].cpu().numpy().view(np.uint16)
     got_dz = oracle.bf16_to_f64(dz_bits)
@@ -254,8 +254,8 @@ def test_backward_small_against_oracle(temperature):
 
 
 def test_backward_two_chunks_against_oracle():
-    """2100 rows: a full chunk plus a padded one; dweight sums both."""
-    n, d, v = 2100, 128, 2000
+    """4148 rows: a full 4096-row chunk plus a padded one; dweight sums both."""
+    n, d, v = 4148, 64, 1500
     h, w, y, g, dh, dw, _ = _backward_case(n, d, v, 42)
     hb, wb = workloads.bf16_bits(h), workloads.bf16_bits(w)
     ref_dh, ref_dw, ref_dz = oracle.linear_backward(hb, wb, y.cpu().numpy(), g.cpu().numpy(), with_dz=True)
@@ -277,7 +277,7 @@ def test_backward_full_size_sampled_rows_and_invariants():
     dh, dw = flp.fused_linear_logp_backward(h, w, y, lse, g, lse_lo=lo)
     torch.cuda.synchronize()
     assert torch.isfinite(dh).all() and torch.isfinite(dw).all()
-    rows = np.array([0, 2047, 2048, n - 1, 12345, 30000])
+    rows = np.array([0, 4095, 4096, n - 1, 12345, 30000])
     hb = workloads.bf16_bits(h[torch.as_tensor(rows, device=DEV)])
     wb = workloads.bf16_bits(w)
     ref_dh, _, ref_dz = oracle.linear_backward(hb, wb, y.cpu().numpy()[rows], g.cpu().numpy()[rows],
