@@ -41,6 +41,7 @@ NUM_TILES = 16
 _DTYPES = {torch.bfloat16: 0, torch.float16: 1, torch.float32: 2}
 
 __all__ = [
+    "FusedLinearLogp",
     "FusedLogp",
     "FusedLogpError",
     "IGNORE_INDEX",
@@ -52,6 +53,7 @@ __all__ = [
     "fused_logp",
     "fused_logp_backward",
     "fused_logp_forward",
+    "fused_linear_logp",
     "fused_linear_logp_backward",
     "fused_linear_logp_backward_workspace_size",
     "fused_linear_logp_forward",
@@ -476,6 +478,43 @@ def fused_logp(logits: torch.Tensor, targets: torch.Tensor,
                active_mask: torch.Tensor | None = None) -> torch.Tensor:
     """Autograd-aware selected-token logp (FP32 [N])."""
     return FusedLogp.apply(logits, targets, ignore_index, temperature, active_mask)
+
+
+class FusedLinearLogp(torch.autograd.Function):
+    """logp = FusedLinearLogp.apply(hidden, weight, targets, ...): the fused
+    LM head + logp; the logits never exist.  The backward recomputes dZ on the
+    tensor cores from the saved LSE (O(N) state) and returns dhidden and
+    dweight in the dtypes of hidden and weight."""
+
+    @staticmethod
+    def forward(ctx, hidden, weight, targets, ignore_index=IGNORE_INDEX, temperature=1.0,
+                active_mask=None):
+        logp, lse, lse_lo = fused_linear_logp_forward(hidden, weight, targets, ignore_index,
+                                                      with_lse_lo=True, temperature=temperature,
+                                                      active_mask=active_mask)
+        ctx.save_for_backward(hidden, weight, targets, lse, lse_lo, active_mask)
+        ctx.ignore_index = ignore_index
+        ctx.temperature = temperature
+        return logp
+
+    @staticmethod
+    def backward(ctx, grad_logp):
+        hidden, weight, targets, lse, lse_lo, active_mask = ctx.saved_tensors
+        g = grad_logp.to(torch.float32).contiguous()
+        dh, dw = fused_linear_logp_backward(hidden, weight, targets, lse, g, ctx.ignore_index,
+                                            lse_lo=lse_lo, temperature=ctx.temperature,
+                                            active_mask=active_mask)
+        dh = dh if hidden.dtype == torch.float32 else dh.to(hidden.dtype)
+        dw = dw if weight.dtype == torch.float32 else dw.to(weight.dtype)
+        return dh, dw, None, None, None, None
+
+
+def fused_linear_logp(hidden: torch.Tensor, weight: torch.Tensor, targets: torch.Tensor,
+                      ignore_index: int = IGNORE_INDEX, temperature: float = 1.0,
+                      active_mask: torch.Tensor | None = None) -> torch.Tensor:
+    """Autograd-aware fused LM head + selected-token logp (FP32 [N]) of
+    hidden [N, D] @ weight[V, D].T, both BF16."""
+    return FusedLinearLogp.apply(hidden, weight, targets, ignore_index, temperature, active_mask)
 
 
 def flp_device_error(device: int | torch.device = 0) -> int:

@@ -316,3 +316,51 @@ def test_backward_deterministic_and_batch_invariant():
     assert torch.equal(a[0].view(torch.int32), b[0].view(torch.int32))
     assert torch.equal(a[1].view(torch.int32), b[1].view(torch.int32))
     assert flp.flp_device_error(0) == 0
+
+
+def test_autograd_wrapper_matches_explicit_calls():
+    n, d, v = 300, 256, 3000
+    h, w, y = workloads.linear(n, d, v, seed=61, device=DEV)
+    hh = h.clone().requires_grad_(True)
+    ww = w.clone().requires_grad_(True)
+    g = torch.randn(n, generator=torch.Generator().manual_seed(62)).to(DEV)
+    logp = flp.fused_linear_logp(hh, ww, y, temperature=0.7)
+    (logp * g).sum().backward()
+    lp2, lse, lo = flp.fused_linear_logp_forward(h, w, y, with_lse_lo=True, temperature=0.7)
+    dh, dw = flp.fused_linear_logp_backward(h, w, y, lse, g, lse_lo=lo, temperature=0.7)
+    assert torch.equal(logp.detach().view(torch.int32), lp2.view(torch.int32))
+    assert hh.grad.dtype == torch.bfloat16 and ww.grad.dtype == torch.bfloat16
+    assert torch.equal(hh.grad, dh.to(torch.bfloat16)) and torch.equal(ww.grad, dw.to(torch.bfloat16))
+
+
+def test_rl_step_through_the_fused_lm_head_against_fp64():
+    """hidden -> fused logp -> GRPO loss and d loss / d logp -> fused LM-head
+    backward, against the same chain in FP64 (oracle forward, GRPO, backward)."""
+    n, d, v = 512, 256, 4000
+    h, w, y = workloads.linear(n, d, v, seed=63, device=DEV)
+    gen = torch.Generator().manual_seed(64)
+    adv = torch.randn(n, generator=gen)
+    shift_old = (torch.rand(n, generator=gen) - 0.5) * 0.6
+    cu = torch.tensor([0, 100, 250, 251, 512], dtype=torch.int64)
+    logp, lse, lo = flp.fused_linear_logp_forward(h, w, y, with_lse_lo=True)
+    old = logp + shift_old.to(DEV)
+    act = (y >= 0).to(torch.uint8)
+    loss, g = flp.logp_grpo_loss(logp, old, adv.to(DEV), active_mask=act, cu_seqlens=cu.to(DEV),
+                                 mode="seq_mean_token_mean")
+    dh, dw = flp.fused_linear_logp_backward(h, w, y, lse, g, lse_lo=lo)
+    torch.cuda.synchronize()
+
+    hb, wb, yn = workloads.bf16_bits(h), workloads.bf16_bits(w), y.cpu().numpy()
+    lp64, _ = oracle.linear_logp(hb, wb, yn)
+    old64 = lp64 + shift_old.double().numpy()
+    l64, g64 = oracle.grpo_loss(lp64, old64, adv.double().numpy(), mask=act.cpu().numpy(),
+                                cu_seqlens=cu.numpy(), mode="seq_mean_token_mean")
+    assert abs(loss.item() - l64) <= 1e-4 * abs(l64) + 1e-6
+    ref_dh, ref_dw, ref_dz = oracle.linear_backward(hb, wb, yn, g64.astype(np.float32), with_dz=True)
+    # the GPU's upstream gradient differs from the FP64 one by ~1e-6 relative:
+    # the per-element bounds above plus that relative difference
+    e_dh = np.abs(dh.double().cpu().numpy() - ref_dh)
+    e_dw = np.abs(dw.double().cpu().numpy() - ref_dw)
+    hd, wd = oracle.bf16_to_f64(hb), oracle.bf16_to_f64(wb)
+    assert np.all(e_dh <= _grad_tol(ref_dz, wd, v) + 1e-5 * np.abs(ref_dh))
+    assert np.all(e_dw <= _grad_tol(ref_dz.T, hd, n) + 1e-5 * np.abs(ref_dw))
