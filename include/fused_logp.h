@@ -248,7 +248,8 @@ flp_status fused_linear_logp_forward(const void* hidden, int64_t n, int64_t d, i
  *             bytes (256-byte aligned), caller-owned: dZ [4096, ceil(v/8)*8]
  *             BF16, a [4096, d] FP32 block, 32 MiB for the GEMM library
  *   dhidden   [n, ld_dh] FP32 out; dweight [v, ld_dw] FP32 out (overwritten,
- *             not accumulated; all zero when n == 0)
+ *             not accumulated; all zero when n == 0, in which case only
+ *             dweight is touched and the workspace may be NULL)
  * Every chunk has the same shape (the last one padded with zero-gradient
  * rows), so a row's dhidden does not depend on n or on its position.
  * Requirements and errors as for the forward, plus ld_dh, ld_dw >= d.

@@ -407,15 +407,17 @@ def fused_linear_logp_backward(hidden: torch.Tensor, weight: torch.Tensor, targe
     _, _, ld_dw = _rows(dweight, "dweight")
     _cuda(hidden, weight, targets, lse, grad, dhidden, dweight)
     mp = _mask(active_mask, n)
-    need = fused_linear_logp_backward_workspace_size(d, v)
+    if workspace is None and n > 0:
+        workspace = torch.empty(fused_linear_logp_backward_workspace_size(d, v), dtype=torch.uint8, device=dev)
     if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
-    _cuda(workspace)
+        wptr, wbytes = None, 0
+    else:
+        _cuda(workspace)
+        wptr, wbytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     st = _lib.load().fused_linear_logp_backward(
         hidden.data_ptr(), n, d, ld_h, weight.data_ptr(), v, ld_w, targets.data_ptr(), int(ignore_index), mp,
-        inv_t, lse.data_ptr(), _opt_ptr(lse_lo), grad.data_ptr(), workspace.data_ptr(),
-        workspace.numel() * workspace.element_size(), dhidden.data_ptr(), ld_dh, dweight.data_ptr(), ld_dw,
-        _stream(hidden))
+        inv_t, lse.data_ptr(), _opt_ptr(lse_lo), grad.data_ptr(), wptr, wbytes, dhidden.data_ptr(), ld_dh,
+        dweight.data_ptr(), ld_dw, _stream(hidden))
     _lib.check("fused_linear_logp_backward", st)
     return dhidden, dweight
 

@@ -751,15 +751,11 @@ flp_status fused_linear_logp_backward(const void* hidden, int64_t n, int64_t d, 
     if (!aligned16(hidden) || !aligned16(weight) || (ld_h % 8) != 0 || (ld_w % 8) != 0)
         return fail(FLP_EUNSUPPORTED,
                     "hidden and weight must start on 16-byte boundaries with row strides a multiple of 8 elements");
-    int64_t ld_dz, off_dh, off_lt, need;
-    if (!linear_grad_workspace(d, v, &ld_dz, &off_dh, &off_lt, &need))
-        return fail(FLP_EINVAL, "workspace size overflows int64");
-    if (workspace_bytes < need)
-        return fail(FLP_EINVAL, "workspace_bytes (%lld) is below the %lld bytes needed", (long long)workspace_bytes,
-                    (long long)need);
-    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-        return fail(FLP_EINVAL, "workspace must start on a 256-byte boundary");
-    if (n == 0) {   // no rows: dW = 0
+    int64_t span;
+    if (!span_bytes(v, d, ld_w, 2, &span) || !span_bytes(v, d, ld_dw, 4, &span) ||
+        (n > 0 && (!span_bytes(n, d, ld_h, 2, &span) || !span_bytes(n, d, ld_dh, 4, &span))))
+        return fail(FLP_EINVAL, "an operand's extent overflows int64");
+    if (n == 0) {   // no rows: dW = 0, nothing else is read
         int dev0;
         if ((st = device_of(dweight, "dweight", &dev0)) != FLP_OK) return st;
         DeviceGuard g0;
@@ -769,6 +765,14 @@ flp_status fused_linear_logp_backward(const void* hidden, int64_t n, int64_t d, 
         if (e != cudaSuccess) return fail(FLP_ECUDA, "clearing dweight: %s", cudaGetErrorString(e));
         return ok();
     }
+    int64_t ld_dz, off_dh, off_lt, need;
+    if (!linear_grad_workspace(d, v, &ld_dz, &off_dh, &off_lt, &need))
+        return fail(FLP_EINVAL, "workspace size overflows int64");
+    if (workspace_bytes < need)
+        return fail(FLP_EINVAL, "workspace_bytes (%lld) is below the %lld bytes needed", (long long)workspace_bytes,
+                    (long long)need);
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(FLP_EINVAL, "workspace must start on a 256-byte boundary");
     const void* ptrs[] = {hidden, weight, targets, lse, grad, workspace, dhidden, dweight, lse_lo, active_mask};
     const char* names[] = {"hidden", "weight", "targets", "lse", "grad", "workspace", "dhidden", "dweight",
                            "lse_lo", "active_mask"};

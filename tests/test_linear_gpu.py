@@ -364,3 +364,14 @@ def test_rl_step_through_the_fused_lm_head_against_fp64():
     hd, wd = oracle.bf16_to_f64(hb), oracle.bf16_to_f64(wb)
     assert np.all(e_dh <= _grad_tol(ref_dz, wd, v) + 1e-5 * np.abs(ref_dh))
     assert np.all(e_dw <= _grad_tol(ref_dz.T, hd, n) + 1e-5 * np.abs(ref_dw))
+
+
+def test_backward_empty_batch_zeroes_dweight():
+    d, v = 64, 300
+    _, w, _ = workloads.linear(1, d, v, seed=71, device=DEV)
+    h0 = torch.empty((0, d), dtype=torch.bfloat16, device=DEV)
+    e = torch.empty(0, device=DEV)
+    dw = torch.full((v, d), 7.0, device=DEV)
+    dh, dw2 = flp.fused_linear_logp_backward(h0, w, torch.empty(0, dtype=torch.int64, device=DEV), e, e,
+                                             dweight=dw)
+    assert dh.shape == (0, d) and dw2 is dw and torch.all(dw == 0)
