@@ -210,8 +210,8 @@ flp_status logp_merge_partials_ex(const float* part_max, const float* part_sum, 
  *   inv_temperature  s = 1/T (> 0, finite)
  *   workspace device scratch of at least fused_linear_logp_workspace_size
  *             bytes (16-byte aligned), owned by the caller; contents on
- *             return are unspecified.  Layout: FP32 tile maxima [ceil(v/256),
- *             n], tile sums [ceil(v/256), n], selected logits [n].
+ *             return are unspecified.  Layout: FP32 tile maxima [n,
+ *             ceil(v/256)], tile sums [n, ceil(v/256)], selected logits [n].
  *   logp, lse [n] FP32 out; lse_lo [n] FP32 out or NULL
  * Accumulation: FP32 on the tensor cores (BF16 products exact), 128 x 256
  * tiles, K in increasing order; each row's result is independent of n, of

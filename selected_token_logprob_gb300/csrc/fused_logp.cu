@@ -417,7 +417,7 @@ flp_status lt_gemm(cublasLtHandle_t lt, cublasOperation_t opa, cublasOperation_t
 
 int64_t linear_vocab_tiles(int64_t v) { return ceil_div(v, flp::kLinBN); }
 
-// Workspace: tile maxima [nvt, n], tile sums [nvt, n], selected logits [n]
+// Workspace: tile maxima [n, nvt], tile sums [n, nvt], selected logits [n]
 // (binary32), rounded up to 256 bytes; false on overflow.
 bool linear_workspace_bytes(int64_t n, int64_t v, int64_t* out) {
     int64_t a, b;
@@ -716,7 +716,10 @@ flp_status fused_linear_logp_forward(const void* hidden, int64_t n, int64_t d, i
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     flp::k_linear_logp_tiles<false><<<grid, flp::kLinThreads, flp::kLinSmemBytes, s>>>(tm_h, tm_w, a);
     if ((st = check_launch("linear logp tiles")) != FLP_OK) return st;
-    flp::k_linear_logp_merge<<<grid_for(ceil_div(n, flp::kLinMergeThreads)), flp::kLinMergeThreads, 0, s>>>(
+    // one warp per row, at most 16 resident CTAs of 256 threads per SM
+    const int64_t merge_ctas = ceil_div(n * 32, flp::kLinMergeThreads);
+    flp::k_linear_logp_merge<<<(int)(merge_ctas < (int64_t)sms * 16 ? merge_ctas : (int64_t)sms * 16),
+                               flp::kLinMergeThreads, 0, s>>>(
         a.pm, a.ps, a.xsel, n, (int)nvt, v, targets, ignore_index, active_mask, inv_temperature, logp, lse,
         lse_lo);
     return check_launch("linear logp merge");

@@ -185,8 +185,8 @@ struct LinArgs {
     int64_t ignore_index;
     const uint8_t* mask;
     Scale sc;
-    float* pm;     // [nvt, n] tile maxima
-    float* ps;     // [nvt, n] tile sums
+    float* pm;     // [n, nvt] tile maxima (row-major: a row's partials are contiguous)
+    float* ps;     // [n, nvt] tile sums
     float* xsel;   // [n] selected logit z[t, y_t] (active rows)
     // gradient mode: rows [n_valid, n) are padding and get zero gradients
     int64_t n_valid;
@@ -490,8 +490,8 @@ k_linear_logp_tiles(const __grid_constant__ CUtensorMap tm_h, const __grid_const
                 acc_phase ^= 1u;
             }
             if (t < p.n) {
-                p.pm[(int64_t)tl.vt * p.n + t] = m;
-                p.ps[(int64_t)tl.vt * p.n + t] = __fmaf_rn(s, kEx2BiasComp, s);
+                p.pm[t * p.nvt + tl.vt] = m;
+                p.ps[t * p.nvt + tl.vt] = __fmaf_rn(s, kEx2BiasComp, s);
                 if (jt >= 0) p.xsel[t] = xs;
             }
         }
@@ -504,30 +504,42 @@ k_linear_logp_tiles(const __grid_constant__ CUtensorMap tm_h, const __grid_const
     }
 }
 
-// Merge of the nvt tile partials of each row in tile order (one thread per
-// row): M = max_k m_k, S = sum_k s_k exp(s (m_k - M)) with the accurate expf,
-// then LSE = s M + log S and logp = s z_y - LSE in double (finalize_row).
+// Merge of the nvt tile partials of each row, one warp per row (rows strided
+// over the grid): lane j folds partials j, j + 32, ... in that order, then the
+// lanes combine with a fixed xor butterfly — M = max_k m_k first, then
+// S = sum_k s_k exp(s (m_k - M)) with the accurate expf — and lane 0 finishes
+// LSE = s M + log S and logp = s z_y - LSE in double (finalize_row).  The
+// order depends only on nvt, never on n or on the grid.
 __global__ void __launch_bounds__(kLinMergeThreads)
 k_linear_logp_merge(const float* __restrict__ pm, const float* __restrict__ ps, const float* __restrict__ xsel,
                     int64_t n, int nvt, int64_t v, const int64_t* __restrict__ y, int64_t ignore_index,
                     const uint8_t* __restrict__ mask, float s, float* __restrict__ logp, float* __restrict__ lse,
                     float* __restrict__ lse_lo) {
-    const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (t >= n) return;
-    float M = -INFINITY;
-    for (int k = 0; k < nvt; ++k) M = fmaxf(M, __ldg(pm + (int64_t)k * n + t));
-    float S = 0.f;
-    if (M != -INFINITY) {
-        for (int k = 0; k < nvt; ++k) {
-            const float mk = __ldg(pm + (int64_t)k * n + t);
-            if (mk != -INFINITY)
-                S = __fmaf_rn(__ldg(ps + (int64_t)k * n + t), expf(__fmul_rn(s, __fsub_rn(mk, M))), S);
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < n; t += warps) {
+        const float* rm = pm + t * nvt;
+        const float* rs = ps + t * nvt;
+        float M = -INFINITY;
+        for (int k = lane; k < nvt; k += 32) M = fmaxf(M, __ldg(rm + k));
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        float S = 0.f;
+        if (M != -INFINITY) {
+            for (int k = lane; k < nvt; k += 32) {
+                const float mk = __ldg(rm + k);
+                if (mk != -INFINITY) S = __fmaf_rn(__ldg(rs + k), expf(__fmul_rn(s, __fsub_rn(mk, M))), S);
+            }
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) S = __fadd_rn(S, __shfl_xor_sync(0xffffffffu, S, off));
+        if (lane == 0) {
+            const int64_t yt = __ldg(y + t);
+            const bool act = row_active(mask, t, yt, v, ignore_index);
+            const float x_y = act ? __ldg(xsel + t) : 0.f;
+            finalize_row(MS{M, S}, act, x_y, s, logp + t, lse + t, lse_lo ? lse_lo + t : nullptr);
         }
     }
-    const int64_t yt = __ldg(y + t);
-    const bool act = row_active(mask, t, yt, v, ignore_index);
-    const float x_y = act ? __ldg(xsel + t) : 0.f;
-    finalize_row(MS{M, S}, act, x_y, s, logp + t, lse + t, lse_lo ? lse_lo + t : nullptr);
 }
 
 }  // namespace flp
