@@ -238,6 +238,18 @@ def run_ours(args):
         step()
     torch.cuda.synchronize(dev)
 
+    # peak memory of a step beyond the resident inputs and outputs (the
+    # library allocates nothing; the target is logits + dlogits + O(N))
+    base = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    step()
+    torch.cuda.synchronize(dev)
+    step_extra = torch.cuda.max_memory_allocated(dev) - base
+    memory = {"logits_bytes": x.numel() * x.element_size(), "dlogits_bytes": dl.numel() * dl.element_size(),
+              "per_row_bytes": n * (8 + 4 + 4 + 4 + 4), "step_extra_bytes": int(step_extra),
+              "note": "logits, dlogits, targets, grad, logp, lse, lse_lo resident before the step; "
+                      "step_extra = max_memory_allocated during one step minus memory_allocated before it"}
+
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     sampler = ClockSampler(local)
     _barrier(world)
@@ -298,6 +310,7 @@ def run_ours(args):
         "e2e": e2e,
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
+        "memory": memory,
         "vs_baseline_note": "pages' fused kernel 27.2 ms fwd+bwd on one B200 (context only)",
     }
     if rank == 0:

@@ -270,3 +270,23 @@ def test_host_pointer_is_rejected():
     st = lib.fused_logp_forward(x.data_ptr(), 64, 1024, 1024, yd.data_ptr(), IGN,
                                 out.data_ptr(), out.data_ptr(), None, None)
     assert st == flp._lib.FLP_EINVAL and b"device memory" in lib.flp_last_error()
+
+
+def test_step_allocates_nothing_beyond_its_outputs():
+    """Peak memory of forward + backward with caller-provided outputs: the
+    library allocates no device memory (logits + dlogits + O(N) in total)."""
+    x, y, g = workloads.make("mid", device=DEV, n=512)
+    n, v = x.shape
+    logp = torch.empty(n, device=DEV)
+    lse = torch.empty(n, device=DEV)
+    lo = torch.empty(n, device=DEV)
+    dl = torch.empty_like(x)
+    flp.fused_logp_forward(x, y, logp=logp, lse=lse, lse_lo=lo)
+    flp.fused_logp_backward(x, y, lse, g, dlogits=dl, lse_lo=lo)
+    torch.cuda.synchronize()
+    base = torch.cuda.memory_allocated()
+    torch.cuda.reset_peak_memory_stats()
+    flp.fused_logp_forward(x, y, logp=logp, lse=lse, lse_lo=lo)
+    flp.fused_logp_backward(x, y, lse, g, dlogits=dl, lse_lo=lo)
+    torch.cuda.synchronize()
+    assert torch.cuda.max_memory_allocated() - base == 0
