@@ -247,9 +247,12 @@ flp_status fused_linear_logp_forward(const void* hidden, int64_t n, int64_t d, i
  *   workspace device scratch of fused_linear_logp_backward_workspace_size
  *             bytes (256-byte aligned), caller-owned: dZ [4096, ceil(v/8)*8]
  *             BF16, a [4096, d] FP32 block, 32 MiB for the GEMM library
- *   dhidden   [n, ld_dh] FP32 out; dweight [v, ld_dw] FP32 out (overwritten,
- *             not accumulated; all zero when n == 0, in which case only
- *             dweight is touched and the workspace may be NULL)
+ *   dhidden   [n, ld_dh] FP32 out
+ *   dweight   [v, ld_dw] FP32: overwritten with dZ^T H when
+ *             accumulate_dweight == 0 (all zero when n == 0), or with
+ *             dweight + dZ^T H when it is nonzero (gradient accumulation over
+ *             micro-batches; unchanged when n == 0).  With n == 0 only dweight
+ *             is touched and the workspace may be NULL.
  * Every chunk has the same shape (the last one padded with zero-gradient
  * rows), so a row's dhidden does not depend on n or on its position.
  * Requirements and errors as for the forward, plus ld_dh, ld_dw >= d.
@@ -262,7 +265,7 @@ flp_status fused_linear_logp_backward(const void* hidden, int64_t n, int64_t d, 
                                       const uint8_t* active_mask, float inv_temperature, const float* lse,
                                       const float* lse_lo, const float* grad, void* workspace,
                                       int64_t workspace_bytes, float* dhidden, int64_t ld_dh, float* dweight,
-                                      int64_t ld_dw, flp_stream_t stream);
+                                      int64_t ld_dw, int accumulate_dweight, flp_stream_t stream);
 
 /*
  * Fused LM head + logp with no allocation and no workspace argument.  The

@@ -377,10 +377,12 @@ def fused_linear_logp_backward(hidden: torch.Tensor, weight: torch.Tensor, targe
                                lse_lo: torch.Tensor | None = None, temperature: float = 1.0,
                                active_mask: torch.Tensor | None = None,
                                dhidden: torch.Tensor | None = None, dweight: torch.Tensor | None = None,
-                               workspace: torch.Tensor | None = None):
+                               workspace: torch.Tensor | None = None, accumulate_dweight: bool = False):
     """(dhidden [N, D], dweight [V, D]) FP32 of sum_t grad[t] logp[t] for the
     fused LM head, from the forward's lse (and lse_lo); dZ is recomputed on
-    the tensor cores in 4096-row chunks and never stored for all rows."""
+    the tensor cores in 4096-row chunks and never stored for all rows.  With
+    ``accumulate_dweight`` the given ``dweight`` is added to, not overwritten
+    (gradient accumulation over micro-batches)."""
     n, d, ld_h = _rows(hidden, "hidden")
     v, d_w, ld_w = _rows(weight, "weight")
     if hidden.dtype != torch.bfloat16 or weight.dtype != torch.bfloat16:
@@ -398,6 +400,8 @@ def fused_linear_logp_backward(hidden: torch.Tensor, weight: torch.Tensor, targe
     if dhidden is None:
         dhidden = torch.empty((n, d), dtype=torch.float32, device=dev)
     if dweight is None:
+        if accumulate_dweight:
+            raise ValueError("accumulate_dweight needs a dweight tensor to add to")
         dweight = torch.empty((v, d), dtype=torch.float32, device=dev)
     if dhidden.dtype != torch.float32 or tuple(dhidden.shape) != (n, d):
         raise ValueError("dhidden must be float32 [N, D]")
@@ -417,7 +421,7 @@ def fused_linear_logp_backward(hidden: torch.Tensor, weight: torch.Tensor, targe
     st = _lib.load().fused_linear_logp_backward(
         hidden.data_ptr(), n, d, ld_h, weight.data_ptr(), v, ld_w, targets.data_ptr(), int(ignore_index), mp,
         inv_t, lse.data_ptr(), _opt_ptr(lse_lo), grad.data_ptr(), wptr, wbytes, dhidden.data_ptr(), ld_dh,
-        dweight.data_ptr(), ld_dw, _stream(hidden))
+        dweight.data_ptr(), ld_dw, int(bool(accumulate_dweight)), _stream(hidden))
     _lib.check("fused_linear_logp_backward", st)
     return dhidden, dweight
 

@@ -49,7 +49,7 @@ SIGNATURES = {
     "fused_linear_logp_backward_workspace_size": (ctypes.c_int, [_I64, _I64, ctypes.POINTER(_I64)]),
     "fused_linear_logp_backward": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _I64, _P,
                                                   ctypes.c_float, _P, _P, _P, _P, _I64, _P, _I64, _P, _I64,
-                                                  _P]),
+                                                  ctypes.c_int, _P]),
     "flp_device_error": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_int)]),
     "flp_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_int, _I64, ctypes.POINTER(ctypes.c_int)]),
     "flp_selftest_ex2_bias": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_double),

@@ -739,7 +739,7 @@ flp_status fused_linear_logp_backward(const void* hidden, int64_t n, int64_t d, 
                                       const uint8_t* active_mask, float inv_temperature, const float* lse,
                                       const float* lse_lo, const float* grad, void* workspace,
                                       int64_t workspace_bytes, float* dhidden, int64_t ld_dh, float* dweight,
-                                      int64_t ld_dw, flp_stream_t stream) {
+                                      int64_t ld_dw, int accumulate_dweight, flp_stream_t stream) {
     flp_status st;
     if ((st = check_scale(inv_temperature)) != FLP_OK) return st;
     if (n < 0) return fail(FLP_EINVAL, "n must be >= 0 (got %lld)", (long long)n);
@@ -758,6 +758,7 @@ flp_status fused_linear_logp_backward(const void* hidden, int64_t n, int64_t d, 
     if (!span_bytes(v, d, ld_w, 2, &span) || !span_bytes(v, d, ld_dw, 4, &span) ||
         (n > 0 && (!span_bytes(n, d, ld_h, 2, &span) || !span_bytes(n, d, ld_dh, 4, &span))))
         return fail(FLP_EINVAL, "an operand's extent overflows int64");
+    if (n == 0 && accumulate_dweight) return ok();   // no rows add nothing
     if (n == 0) {   // no rows: dW = 0, nothing else is read
         int dev0;
         if ((st = device_of(dweight, "dweight", &dev0)) != FLP_OK) return st;
@@ -842,7 +843,8 @@ flp_status fused_linear_logp_backward(const void* hidden, int64_t n, int64_t d, 
         }
         // dW (+)= dZ^T H: column-major dW^T [d x v] = H^T [d x rows] (dZ^T [v x rows])^T
         if ((st = lt_gemm(lt, CUBLAS_OP_N, CUBLAS_OP_T, d, v, rows, h_chunk, ld_h, dz, ld_dz,
-                          start == 0 ? 0.f : 1.f, dweight, ld_dw, lt_ws, s, "dweight")) != FLP_OK)
+                          (start == 0 && !accumulate_dweight) ? 0.f : 1.f, dweight, ld_dw, lt_ws, s,
+                          "dweight")) != FLP_OK)
             return st;
     }
     return ok();

@@ -245,7 +245,7 @@ def test_linear_backward_host_checks(lib):
     def call(n=16, d=64, ld_h=64, v=100, ld_w=64, ws=1 << 20, ws_bytes=1 << 40, ld_dh=64, ld_dw=64, s=1.0):
         return lib.fused_linear_logp_backward(1 << 20, n, d, ld_h, 1 << 21, v, ld_w, 1 << 22, -100, None, s,
                                               1 << 23, None, 1 << 24, ws, ws_bytes, 1 << 25, ld_dh, 1 << 26,
-                                              ld_dw, None)
+                                              ld_dw, 0, None)
 
     assert call(n=-1) == EINVAL
     assert call(ld_dh=32) == EINVAL and call(ld_dw=8) == EINVAL

@@ -375,3 +375,24 @@ def test_backward_empty_batch_zeroes_dweight():
     dh, dw2 = flp.fused_linear_logp_backward(h0, w, torch.empty(0, dtype=torch.int64, device=DEV), e, e,
                                              dweight=dw)
     assert dh.shape == (0, d) and dw2 is dw and torch.all(dw == 0)
+
+
+def test_backward_accumulates_dweight_over_micro_batches():
+    """Two micro-batches with accumulate_dweight give dweight of one call over
+    both (up to FP32 summation order), and dhidden rows unchanged bitwise."""
+    d, v = 128, 2500
+    h, w, y = workloads.linear(700, d, v, seed=81, device=DEV)
+    g = torch.randn(700, generator=torch.Generator().manual_seed(82)).to(DEV)
+    _, lse, lo = flp.fused_linear_logp_forward(h, w, y, with_lse_lo=True)
+    dh_all, dw_all = flp.fused_linear_logp_backward(h, w, y, lse, g, lse_lo=lo)
+    dw = torch.zeros((v, d), device=DEV)
+    parts = []
+    for a, b in ((0, 300), (300, 700)):
+        dh, _ = flp.fused_linear_logp_backward(h[a:b], w, y[a:b], lse[a:b], g[a:b], lse_lo=lo[a:b],
+                                               dweight=dw, accumulate_dweight=True)
+        parts.append(dh)
+    assert torch.equal(torch.cat(parts).view(torch.int32), dh_all.view(torch.int32))
+    assert torch.max(torch.abs(dw - dw_all)).item() <= 1e-5 * torch.max(torch.abs(dw_all)).item()
+    keep = dw.clone()
+    flp.fused_linear_logp_backward(h[:0], w, y[:0], lse[:0], g[:0], dweight=dw, accumulate_dweight=True)
+    assert torch.equal(dw, keep)
