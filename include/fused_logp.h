@@ -230,6 +230,38 @@ flp_status fused_linear_logp_forward(const void* hidden, int64_t n, int64_t d, i
                                      float* lse_lo, flp_stream_t stream);
 
 /*
+ * Vocabulary-sharded fused LM head on one GPU (issue #241 PR 3 and PR 6: a
+ * shard emits (max, sumexp) partials of the tiles it holds plus the selected
+ * logit it owns; one fixed-order merge; PR #314 Tensor Parallel section: the
+ * tile grid makes every shard count give the same bits).  The weight rows of
+ * a vocabulary-parallel LM head are split into shards; shard l holds global
+ * columns [vocab_start, vocab_start + real_width) as its own [real_width,
+ * ld_w] BF16 buffer.
+ *   fused_linear_logp_shard_partials writes that shard's tile partials into
+ *     `workspace` (the layout of fused_linear_logp_forward's workspace for n
+ *     rows and v_total columns: FP32 [n, ceil(v_total/256)] maxima and sums,
+ *     [n] selected logits) and the selected logit of every row whose target
+ *     is in the shard.  vocab_start must be a multiple of 256 (the tile
+ *     grid), else FLP_EUNSUPPORTED; [vocab_start, vocab_start + real_width)
+ *     must lie in [0, v_total).
+ *   fused_linear_logp_merge merges, in tile order, the partials of all tiles
+ *     of [0, v_total) into logp, lse (and lse_lo), as the forward does.
+ * The shards must together cover [0, v_total) (the merge reads every tile's
+ * partial).  With that, the result is bitwise equal to
+ * fused_linear_logp_forward on the unsharded weight, for any shard count.
+ * All calls asynchronous on `stream`; the library allocates nothing.
+ */
+flp_status fused_linear_logp_shard_partials(const void* hidden, int64_t n, int64_t d, int64_t ld_h,
+                                            const void* weight_shard, int64_t real_width, int64_t ld_w,
+                                            int64_t vocab_start, int64_t v_total, const int64_t* targets,
+                                            float inv_temperature, void* workspace, int64_t workspace_bytes,
+                                            flp_stream_t stream);
+flp_status fused_linear_logp_merge(const void* workspace, int64_t workspace_bytes, int64_t n, int64_t v_total,
+                                   const int64_t* targets, int64_t ignore_index, const uint8_t* active_mask,
+                                   float inv_temperature, float* logp, float* lse, float* lse_lo,
+                                   flp_stream_t stream);
+
+/*
  * Backward of the fused LM head (no counterpart in the pages beyond the name
  * linear_logp; the method's backward, PR #495 Summary item 2, taken through
  * the contraction): for the loss sum_t grad[t] logp[t],

@@ -58,6 +58,8 @@ __all__ = [
     "fused_linear_logp_backward_workspace_size",
     "fused_linear_logp_forward",
     "fused_linear_logp_forward_noalloc",
+    "fused_linear_logp_merge",
+    "fused_linear_logp_shard_partials",
     "fused_linear_logp_workspace_size",
     "logp_grpo_loss",
     "logp_merge_partials",
@@ -484,6 +486,48 @@ def fused_logp(logits: torch.Tensor, targets: torch.Tensor,
                active_mask: torch.Tensor | None = None) -> torch.Tensor:
     """Autograd-aware selected-token logp (FP32 [N])."""
     return FusedLogp.apply(logits, targets, ignore_index, temperature, active_mask)
+
+
+def fused_linear_logp_shard_partials(hidden: torch.Tensor, weight_shard: torch.Tensor, vocab_start: int,
+                                     v_total: int, targets: torch.Tensor, workspace: torch.Tensor,
+                                     temperature: float = 1.0) -> None:
+    """Tile partials of one vocabulary shard of the LM head (global columns
+    [vocab_start, vocab_start + weight_shard.shape[0]), vocab_start a multiple
+    of 256) into `workspace` (a byte tensor of
+    fused_linear_logp_workspace_size(N, v_total) bytes shared by all shards)."""
+    n, d, ld_h = _rows(hidden, "hidden")
+    w, d_w, ld_w = _rows(weight_shard, "weight_shard")
+    if hidden.dtype != torch.bfloat16 or weight_shard.dtype != torch.bfloat16:
+        raise TypeError("hidden and weight_shard must be bfloat16")
+    if d_w != d:
+        raise ValueError(f"hidden has {d} columns but weight_shard has {d_w}")
+    _vec(targets, "targets", n, torch.int64)
+    _cuda(hidden, weight_shard, targets, workspace)
+    st = _lib.load().fused_linear_logp_shard_partials(
+        hidden.data_ptr(), n, d, ld_h, weight_shard.data_ptr(), w, ld_w, int(vocab_start), int(v_total),
+        targets.data_ptr(), _inv_temperature(temperature), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream(hidden))
+    _lib.check("fused_linear_logp_shard_partials", st)
+
+
+def fused_linear_logp_merge(workspace: torch.Tensor, v_total: int, targets: torch.Tensor,
+                            ignore_index: int = IGNORE_INDEX, with_lse_lo: bool = False,
+                            temperature: float = 1.0, active_mask: torch.Tensor | None = None):
+    """(logp, lse[, lse_lo]) FP32 [N] from the shards' partials in `workspace`."""
+    n = targets.shape[0]
+    _vec(targets, "targets", n, torch.int64)
+    dev = targets.device
+    logp = torch.empty(n, dtype=torch.float32, device=dev)
+    lse = torch.empty(n, dtype=torch.float32, device=dev)
+    lse_lo = torch.empty(n, dtype=torch.float32, device=dev) if with_lse_lo else None
+    _cuda(workspace, targets)
+    mp = _mask(active_mask, n)
+    st = _lib.load().fused_linear_logp_merge(
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), n, int(v_total), targets.data_ptr(),
+        int(ignore_index), mp, _inv_temperature(temperature), logp.data_ptr(), lse.data_ptr(), _opt_ptr(lse_lo),
+        _stream(targets))
+    _lib.check("fused_linear_logp_merge", st)
+    return (logp, lse, lse_lo) if with_lse_lo else (logp, lse)
 
 
 class FusedLinearLogp(torch.autograd.Function):

@@ -446,6 +446,69 @@ flp_status noalloc_scratch_address(int dev, void** out) {
     return FLP_OK;
 }
 
+// Tile partials of rows [0, n) against `weight` (w rows: global vocabulary
+// columns [vocab_start, vocab_start + w), vocab_start on the 256-column tile
+// grid) into the [n, ceil(v_total / 256)] partial buffers of `ws`, and the
+// selected logit of every row whose target falls in those columns.
+flp_status linear_partials_launch(int dev, const void* hidden, int64_t n, int64_t d, int64_t ld_h,
+                                  const void* weight, int64_t w, int64_t ld_w, int64_t vocab_start, int64_t v_total,
+                                  const int64_t* targets, int64_t ignore_index, const uint8_t* mask, float inv_s,
+                                  float* ws, cudaStream_t stream) {
+    flp_status st;
+    if ((st = linear_setup(dev)) != FLP_OK) return st;
+    CUtensorMap tm_h, tm_w;
+    if ((st = make_tmap_bf16(&tm_h, hidden, n, d, ld_h, flp::kLinBM, "hidden")) != FLP_OK) return st;
+    if ((st = make_tmap_bf16(&tm_w, weight, w, d, ld_w, flp::kLinBN, "weight")) != FLP_OK) return st;
+    const int64_t nvt = linear_vocab_tiles(w);
+    const int64_t nvt_total = linear_vocab_tiles(v_total);
+    const int64_t nrb = ceil_div(n, flp::kLinBM);
+    flp::LinArgs a;
+    a.n = n;
+    a.v = w;
+    a.nrb = (int)nrb;
+    a.nvt = (int)nvt;
+    a.nkb = (int)ceil_div(d, flp::kLinBK);
+    a.vocab_start = vocab_start;
+    a.v_total = v_total;
+    a.vt0 = (int)(vocab_start / flp::kLinBN);
+    a.nvt_total = (int)nvt_total;
+    a.y = targets;
+    a.ignore_index = ignore_index;
+    a.mask = mask;
+    a.sc = make_scale(inv_s);
+    a.pm = ws;
+    a.ps = ws + nvt_total * n;
+    a.xsel = ws + 2 * nvt_total * n;
+    a.n_valid = n;
+    a.lse = nullptr;
+    a.lse_lo = nullptr;
+    a.g = nullptr;
+    a.inv_s = 0.f;
+    a.dz = nullptr;
+    a.ld_dz = 0;
+    const int sms = sm_count(dev);
+    if (sms <= 0) return fail(FLP_ECUDA, "cannot read the SM count of device %d", dev);
+    const int64_t ntiles = nrb * nvt;
+    const int grid = (int)(ntiles < sms ? ntiles : sms);
+    flp::k_linear_logp_tiles<false><<<grid, flp::kLinThreads, flp::kLinSmemBytes, stream>>>(tm_h, tm_w, a);
+    return check_launch("linear logp tiles");
+}
+
+// The fixed-order merge of the [n, ceil(v_total / 256)] partials in `ws`.
+flp_status linear_merge_launch(int dev, const float* ws, int64_t n, int64_t v_total, const int64_t* targets,
+                               int64_t ignore_index, const uint8_t* mask, float inv_s, float* logp, float* lse,
+                               float* lse_lo, cudaStream_t stream) {
+    const int64_t nvt_total = linear_vocab_tiles(v_total);
+    const int sms = sm_count(dev);
+    if (sms <= 0) return fail(FLP_ECUDA, "cannot read the SM count of device %d", dev);
+    // one warp per row, at most 16 resident CTAs of 256 threads per SM
+    const int64_t ctas = ceil_div(n * 32, flp::kLinMergeThreads);
+    flp::k_linear_logp_merge<<<(int)(ctas < (int64_t)sms * 16 ? ctas : (int64_t)sms * 16), flp::kLinMergeThreads,
+                               0, stream>>>(ws, ws + nvt_total * n, ws + 2 * nvt_total * n, n, (int)nvt_total,
+                                            v_total, targets, ignore_index, mask, inv_s, logp, lse, lse_lo);
+    return check_launch("linear logp merge");
+}
+
 }  // namespace
 
 extern "C" {
@@ -680,49 +743,85 @@ flp_status fused_linear_logp_forward(const void* hidden, int64_t n, int64_t d, i
     if (dev < 0 || dev >= kMaxDevices) return fail(FLP_ECUDA, "device index %d out of range", dev);
     DeviceGuard guard;
     if ((st = guard.enter(dev)) != FLP_OK) return st;
-    if ((st = linear_setup(dev)) != FLP_OK) return st;
-
-    CUtensorMap tm_h, tm_w;
-    if ((st = make_tmap_bf16(&tm_h, hidden, n, d, ld_h, flp::kLinBM, "hidden")) != FLP_OK) return st;
-    if ((st = make_tmap_bf16(&tm_w, weight, v, d, ld_w, flp::kLinBN, "weight")) != FLP_OK) return st;
-
-    const int64_t nvt = linear_vocab_tiles(v);
-    const int64_t nrb = ceil_div(n, flp::kLinBM);
-    float* ws = static_cast<float*>(workspace);
-    flp::LinArgs a;
-    a.n = n;
-    a.v = v;
-    a.nrb = (int)nrb;
-    a.nvt = (int)nvt;
-    a.nkb = (int)ceil_div(d, flp::kLinBK);
-    a.y = targets;
-    a.ignore_index = ignore_index;
-    a.mask = active_mask;
-    a.sc = make_scale(inv_temperature);
-    a.pm = ws;
-    a.ps = ws + nvt * n;
-    a.xsel = ws + 2 * nvt * n;
-    a.n_valid = n;
-    a.lse = nullptr;
-    a.lse_lo = nullptr;
-    a.g = nullptr;
-    a.inv_s = 0.f;
-    a.dz = nullptr;
-    a.ld_dz = 0;
-    const int sms = sm_count(dev);
-    if (sms <= 0) return fail(FLP_ECUDA, "cannot read the SM count of device %d", dev);
-    const int64_t ntiles = nrb * nvt;
-    const int grid = (int)(ntiles < sms ? ntiles : sms);
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    flp::k_linear_logp_tiles<false><<<grid, flp::kLinThreads, flp::kLinSmemBytes, s>>>(tm_h, tm_w, a);
-    if ((st = check_launch("linear logp tiles")) != FLP_OK) return st;
-    // one warp per row, at most 16 resident CTAs of 256 threads per SM
-    const int64_t merge_ctas = ceil_div(n * 32, flp::kLinMergeThreads);
-    flp::k_linear_logp_merge<<<(int)(merge_ctas < (int64_t)sms * 16 ? merge_ctas : (int64_t)sms * 16),
-                               flp::kLinMergeThreads, 0, s>>>(
-        a.pm, a.ps, a.xsel, n, (int)nvt, v, targets, ignore_index, active_mask, inv_temperature, logp, lse,
-        lse_lo);
-    return check_launch("linear logp merge");
+    float* ws = static_cast<float*>(workspace);
+    if ((st = linear_partials_launch(dev, hidden, n, d, ld_h, weight, v, ld_w, 0, v, targets, ignore_index,
+                                     active_mask, inv_temperature, ws, s)) != FLP_OK)
+        return st;
+    return linear_merge_launch(dev, ws, n, v, targets, ignore_index, active_mask, inv_temperature, logp, lse,
+                               lse_lo, s);
+}
+
+flp_status fused_linear_logp_shard_partials(const void* hidden, int64_t n, int64_t d, int64_t ld_h,
+                                            const void* weight_shard, int64_t real_width, int64_t ld_w,
+                                            int64_t vocab_start, int64_t v_total, const int64_t* targets,
+                                            float inv_temperature, void* workspace, int64_t workspace_bytes,
+                                            flp_stream_t stream) {
+    flp_status st;
+    if ((st = check_scale(inv_temperature)) != FLP_OK) return st;
+    if (n < 0) return fail(FLP_EINVAL, "n must be >= 0 (got %lld)", (long long)n);
+    if (d < 1) return fail(FLP_EINVAL, "d must be >= 1 (got %lld)", (long long)d);
+    if (real_width < 1 || vocab_start < 0 || v_total < 1 || vocab_start + real_width > v_total)
+        return fail(FLP_EINVAL, "the shard [%lld, %lld) must lie inside [0, %lld)", (long long)vocab_start,
+                    (long long)(vocab_start + real_width), (long long)v_total);
+    if (ld_h < d || ld_w < d) return fail(FLP_EINVAL, "ld_h and ld_w must be >= d (%lld)", (long long)d);
+    if (vocab_start % flp::kLinBN != 0)
+        return fail(FLP_EUNSUPPORTED, "vocab_start (%lld) must be a multiple of the %d-column tile",
+                    (long long)vocab_start, flp::kLinBN);
+    if (n == 0) return ok();
+    const int64_t kMaxDim = ((int64_t)1 << 31) - 1;
+    if (n > kMaxDim || v_total > kMaxDim || d > kMaxDim)
+        return fail(FLP_EUNSUPPORTED, "n, v_total and d must be below 2^31");
+    if (!aligned16(hidden) || !aligned16(weight_shard) || (ld_h % 8) != 0 || (ld_w % 8) != 0)
+        return fail(FLP_EUNSUPPORTED,
+                    "hidden and weight must start on 16-byte boundaries with row strides a multiple of 8 elements");
+    int64_t span, need;
+    if (!span_bytes(n, d, ld_h, 2, &span) || !span_bytes(real_width, d, ld_w, 2, &span))
+        return fail(FLP_EINVAL, "hidden or weight extent overflows int64");
+    if (!linear_workspace_bytes(n, v_total, &need)) return fail(FLP_EINVAL, "workspace size overflows int64");
+    if (workspace_bytes < need)
+        return fail(FLP_EINVAL, "workspace_bytes (%lld) is below the %lld bytes needed", (long long)workspace_bytes,
+                    (long long)need);
+    if (!aligned16(workspace)) return fail(FLP_EINVAL, "workspace must start on a 16-byte boundary");
+    const void* ptrs[] = {hidden, weight_shard, targets, workspace};
+    const char* names[] = {"hidden", "weight_shard", "targets", "workspace"};
+    int dev;
+    if ((st = common_device(4, ptrs, names, nullptr, &dev)) != FLP_OK) return st;
+    if (dev < 0 || dev >= kMaxDevices) return fail(FLP_ECUDA, "device index %d out of range", dev);
+    DeviceGuard guard;
+    if ((st = guard.enter(dev)) != FLP_OK) return st;
+    // the merge decides which rows are active; every in-shard target's logit is kept
+    return linear_partials_launch(dev, hidden, n, d, ld_h, weight_shard, real_width, ld_w, vocab_start, v_total,
+                                  targets, -1, nullptr, inv_temperature, static_cast<float*>(workspace),
+                                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+flp_status fused_linear_logp_merge(const void* workspace, int64_t workspace_bytes, int64_t n, int64_t v_total,
+                                   const int64_t* targets, int64_t ignore_index, const uint8_t* active_mask,
+                                   float inv_temperature, float* logp, float* lse, float* lse_lo,
+                                   flp_stream_t stream) {
+    flp_status st;
+    if ((st = check_scale(inv_temperature)) != FLP_OK) return st;
+    if (n < 0) return fail(FLP_EINVAL, "n must be >= 0 (got %lld)", (long long)n);
+    if (v_total < 1) return fail(FLP_EINVAL, "v_total must be >= 1 (got %lld)", (long long)v_total);
+    if (n == 0) return ok();
+    int64_t need;
+    if (!linear_workspace_bytes(n, v_total, &need)) return fail(FLP_EINVAL, "workspace size overflows int64");
+    if (workspace_bytes < need)
+        return fail(FLP_EINVAL, "workspace_bytes (%lld) is below the %lld bytes needed", (long long)workspace_bytes,
+                    (long long)need);
+    if (!aligned16(workspace)) return fail(FLP_EINVAL, "workspace must start on a 16-byte boundary");
+    const void* ptrs[] = {workspace, targets, logp, lse, lse_lo, active_mask};
+    const char* names[] = {"workspace", "targets", "logp", "lse", "lse_lo", "active_mask"};
+    const bool optional[] = {false, false, false, false, true, true};
+    int dev;
+    if ((st = common_device(6, ptrs, names, optional, &dev)) != FLP_OK) return st;
+    if (dev < 0 || dev >= kMaxDevices) return fail(FLP_ECUDA, "device index %d out of range", dev);
+    DeviceGuard guard;
+    if ((st = guard.enter(dev)) != FLP_OK) return st;
+    return linear_merge_launch(dev, static_cast<const float*>(workspace), n, v_total, targets, ignore_index,
+                               active_mask, inv_temperature, logp, lse, lse_lo,
+                               reinterpret_cast<cudaStream_t>(stream));
 }
 
 flp_status fused_linear_logp_backward_workspace_size(int64_t d, int64_t v, int64_t* bytes) {
@@ -815,6 +914,10 @@ flp_status fused_linear_logp_backward(const void* hidden, int64_t n, int64_t d, 
         a.nrb = (int)nrb;
         a.nvt = (int)nvt;
         a.nkb = (int)ceil_div(d, flp::kLinBK);
+        a.vocab_start = 0;
+        a.v_total = v;
+        a.vt0 = 0;
+        a.nvt_total = (int)nvt;
         a.y = targets + start;
         a.ignore_index = ignore_index;
         a.mask = active_mask ? active_mask + start : nullptr;

@@ -179,8 +179,14 @@ __device__ __forceinline__ LinTile lin_tile(int64_t i, int nrb, int nvt) {
 }
 
 struct LinArgs {
-    int64_t n, v;
-    int nrb, nvt, nkb;
+    int64_t n, v;           // rows; vocabulary columns held by this call's weight rows
+    int nrb, nvt, nkb;      // row blocks, vocabulary tiles of this call, K blocks
+    // vocabulary sharding: this call's weight rows are global columns
+    // [vocab_start, vocab_start + v) of a v_total-column vocabulary whose
+    // partials are laid out [n, nvt_total]; this call's tiles are global tiles
+    // [vt0, vt0 + nvt).  Unsharded: vocab_start = vt0 = 0, v_total = v.
+    int64_t vocab_start, v_total;
+    int vt0, nvt_total;
     const int64_t* y;
     int64_t ignore_index;
     const uint8_t* mask;
@@ -423,7 +429,7 @@ k_linear_logp_tiles(const __grid_constant__ CUtensorMap tm_h, const __grid_const
                 LinGradRow gr{};
                 if (t < p.n_valid) {
                     const int64_t yt = __ldg(p.y + t);
-                    act = row_active(p.mask, t, yt, p.v, p.ignore_index);
+                    act = row_active(p.mask, t, yt, p.v_total, p.ignore_index);
                     if (act) {
                         gr = lin_grad_row(__ldg(p.lse + t), p.lse_lo ? __ldg(p.lse_lo + t) : 0.f, __ldg(p.g + t),
                                           p.sc.s, p.inv_s);
@@ -464,8 +470,9 @@ k_linear_logp_tiles(const __grid_constant__ CUtensorMap tm_h, const __grid_const
             int64_t jt = -1;  // target column inside this tile, if the row is active
             if (t < p.n) {
                 const int64_t yt = __ldg(p.y + t);
-                if (row_active(p.mask, t, yt, p.v, p.ignore_index) && yt >= col0 && yt < col0 + kLinBN)
-                    jt = yt - col0;
+                const int64_t yl = yt - p.vocab_start;   // target column in this call's weight rows
+                if (row_active(p.mask, t, yt, p.v_total, p.ignore_index) && yl >= col0 && yl < col0 + kLinBN)
+                    jt = yl - col0;
             }
             const int nreal = (p.v - col0 < kLinBN) ? (int)(p.v - col0) : kLinBN;
             float m = -INFINITY, s = 0.f, xs = 0.f;
@@ -490,8 +497,8 @@ k_linear_logp_tiles(const __grid_constant__ CUtensorMap tm_h, const __grid_const
                 acc_phase ^= 1u;
             }
             if (t < p.n) {
-                p.pm[t * p.nvt + tl.vt] = m;
-                p.ps[t * p.nvt + tl.vt] = __fmaf_rn(s, kEx2BiasComp, s);
+                p.pm[t * p.nvt_total + p.vt0 + tl.vt] = m;
+                p.ps[t * p.nvt_total + p.vt0 + tl.vt] = __fmaf_rn(s, kEx2BiasComp, s);
                 if (jt >= 0) p.xsel[t] = xs;
             }
         }

@@ -254,3 +254,18 @@ def test_linear_backward_host_checks(lib):
     assert call(ws=(1 << 20) + 16) == EINVAL          # not 256-byte aligned
     assert call(s=-1.0) == EINVAL
     assert call() == EINVAL                            # host pointers are not device memory
+
+
+def test_linear_shard_host_checks(lib):
+    def call(n=16, w=512, start=256, v_total=2000, ld=64):
+        return lib.fused_linear_logp_shard_partials(1 << 20, n, 64, ld, 1 << 21, w, ld, start, v_total,
+                                                    1 << 22, 1.0, 1 << 23, 1 << 30, None)
+
+    assert call(start=100) == EUNSUP and b"multiple" in lib.flp_last_error()
+    assert call(start=1792) == EINVAL                 # [1792, 2304) is not inside [0, 2000)
+    assert call(start=-256) == EINVAL
+    assert call(n=0) == 0
+    assert call() == EINVAL                           # host pointers are not device memory
+    assert lib.fused_linear_logp_merge(None, 0, 0, 10, None, -100, None, 1.0, None, None, None, None) == 0
+    assert lib.fused_linear_logp_merge(1 << 20, 10, 16, 2000, 1 << 21, -100, None, 1.0, 1 << 22, 1 << 23,
+                                       None, None) == EINVAL   # workspace too small

@@ -396,3 +396,36 @@ def test_backward_accumulates_dweight_over_micro_batches():
     keep = dw.clone()
     flp.fused_linear_logp_backward(h[:0], w, y[:0], lse[:0], g[:0], dweight=dw, accumulate_dweight=True)
     assert torch.equal(dw, keep)
+
+
+@pytest.mark.parametrize("bounds", [(0, 10240, 20000), (0, 5120, 12800, 20000), (0, 256, 512, 19968, 20000)])
+def test_vocab_sharded_equals_unsharded_bitwise(bounds):
+    """Shards of the LM-head weight (separate buffers, bounds on the 256-column
+    tile grid) give the unsharded forward's logp, lse and lse_lo bit for bit,
+    with temperature and a mask."""
+    n, d, v = 300, 512, 20000
+    h, w, y = workloads.linear(n, d, v, seed=91, device=DEV)
+    mask = (torch.arange(n, device=DEV) % 7 != 3)
+    ref = flp.fused_linear_logp_forward(h, w, y, with_lse_lo=True, temperature=0.7, active_mask=mask)
+    ws = torch.full((flp.fused_linear_logp_workspace_size(n, v),), 0xFF, dtype=torch.uint8, device=DEV)
+    for a, b in zip(bounds[:-1], bounds[1:]):
+        shard = w[a:b].clone()
+        flp.fused_linear_logp_shard_partials(h, shard, a, v, y, ws, temperature=0.7)
+    out = flp.fused_linear_logp_merge(ws, v, y, with_lse_lo=True, temperature=0.7, active_mask=mask)
+    for r, o in zip(ref, out):
+        assert torch.equal(_i(r), _i(o))
+
+
+def test_vocab_sharded_full_vocabulary_and_gate():
+    n, d, v = 256, 1024, workloads.QWEN3_VOCAB
+    h, w, y = workloads.linear(n, d, v, seed=92, device=DEV)
+    ref = flp.fused_linear_logp_forward(h, w, y)
+    ws = torch.empty(flp.fused_linear_logp_workspace_size(n, v), dtype=torch.uint8, device=DEV)
+    half = 296 * 256                      # 75776: the tile boundary nearest V / 2
+    flp.fused_linear_logp_shard_partials(h, w[:half], 0, v, y, ws)
+    flp.fused_linear_logp_shard_partials(h, w[half:], half, v, y, ws)
+    out = flp.fused_linear_logp_merge(ws, v, y)
+    for r, o in zip(ref, out):
+        assert torch.equal(_i(r), _i(o))
+    with pytest.raises(flp.FusedLogpError, match="multiple"):
+        flp.fused_linear_logp_shard_partials(h, w[100:], 100, v, y, ws)
