@@ -300,6 +300,31 @@ flp_status fused_linear_logp_backward(const void* hidden, int64_t n, int64_t d, 
                                       int64_t ld_dw, int accumulate_dweight, flp_stream_t stream);
 
 /*
+ * Backward of one vocabulary shard of the fused LM head (the shard layout of
+ * fused_linear_logp_shard_partials; lse and lse_lo are the merged, global
+ * values): dZ for the shard's columns, its rows of dweight, and its term of
+ * dhidden = sum over shards of dZ_shard W_shard.
+ *   dhidden           [n, ld_dh] FP32: overwritten with this shard's term,
+ *                     or added to when accumulate_dhidden is nonzero (call
+ *                     the shards in a fixed order, the first without it)
+ *   dweight_shard     [real_width, ld_dw] FP32 (overwritten, or added to with
+ *                     accumulate_dweight)
+ *   workspace         fused_linear_logp_backward_workspace_size(d, real_width)
+ * vocab_start must be a multiple of 256, else FLP_EUNSUPPORTED.  The
+ * summed dhidden is deterministic for a fixed shard layout; it is not bitwise
+ * equal to the unsharded backward's (the sum over the vocabulary is split).
+ * Other arguments and errors as for fused_linear_logp_backward.
+ */
+flp_status fused_linear_logp_shard_backward(const void* hidden, int64_t n, int64_t d, int64_t ld_h,
+                                            const void* weight_shard, int64_t real_width, int64_t ld_w,
+                                            int64_t vocab_start, int64_t v_total, const int64_t* targets,
+                                            int64_t ignore_index, const uint8_t* active_mask, float inv_temperature,
+                                            const float* lse, const float* lse_lo, const float* grad,
+                                            void* workspace, int64_t workspace_bytes, float* dhidden,
+                                            int64_t ld_dh, int accumulate_dhidden, float* dweight_shard,
+                                            int64_t ld_dw, int accumulate_dweight, flp_stream_t stream);
+
+/*
  * Fused LM head + logp with no allocation and no workspace argument.  The
  * pages have no counterpart: this is a convenience of this library.
  *

@@ -59,6 +59,7 @@ __all__ = [
     "fused_linear_logp_forward",
     "fused_linear_logp_forward_noalloc",
     "fused_linear_logp_merge",
+    "fused_linear_logp_shard_backward",
     "fused_linear_logp_shard_partials",
     "fused_linear_logp_workspace_size",
     "logp_grpo_loss",
@@ -528,6 +529,53 @@ def fused_linear_logp_merge(workspace: torch.Tensor, v_total: int, targets: torc
         _stream(targets))
     _lib.check("fused_linear_logp_merge", st)
     return (logp, lse, lse_lo) if with_lse_lo else (logp, lse)
+
+
+def fused_linear_logp_shard_backward(hidden: torch.Tensor, weight_shard: torch.Tensor, vocab_start: int,
+                                     v_total: int, targets: torch.Tensor, lse: torch.Tensor, grad: torch.Tensor,
+                                     dhidden: torch.Tensor, accumulate_dhidden: bool,
+                                     ignore_index: int = IGNORE_INDEX, lse_lo: torch.Tensor | None = None,
+                                     temperature: float = 1.0, active_mask: torch.Tensor | None = None,
+                                     dweight_shard: torch.Tensor | None = None, accumulate_dweight: bool = False,
+                                     workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """One vocabulary shard's backward: writes (or, with accumulate_dhidden,
+    adds) its term of dhidden [N, D] FP32 and returns its dweight rows
+    [real_width, D] FP32.  lse / lse_lo are the merged forward's."""
+    n, d, ld_h = _rows(hidden, "hidden")
+    w, d_w, ld_w = _rows(weight_shard, "weight_shard")
+    if hidden.dtype != torch.bfloat16 or weight_shard.dtype != torch.bfloat16:
+        raise TypeError("hidden and weight_shard must be bfloat16")
+    if d_w != d:
+        raise ValueError(f"hidden has {d} columns but weight_shard has {d_w}")
+    _vec(targets, "targets", n, torch.int64)
+    _vec(lse, "lse", n, torch.float32)
+    _vec(grad, "grad", n, torch.float32)
+    if lse_lo is not None:
+        _vec(lse_lo, "lse_lo", n, torch.float32)
+    dev = hidden.device
+    if dweight_shard is None:
+        if accumulate_dweight:
+            raise ValueError("accumulate_dweight needs a dweight_shard tensor to add to")
+        dweight_shard = torch.empty((w, d), dtype=torch.float32, device=dev)
+    if dhidden.dtype != torch.float32 or tuple(dhidden.shape) != (n, d):
+        raise ValueError("dhidden must be float32 [N, D]")
+    if dweight_shard.dtype != torch.float32 or tuple(dweight_shard.shape) != (w, d):
+        raise ValueError("dweight_shard must be float32 [real_width, D]")
+    _, _, ld_dh = _rows(dhidden, "dhidden")
+    _, _, ld_dw = _rows(dweight_shard, "dweight_shard")
+    _cuda(hidden, weight_shard, targets, lse, grad, dhidden, dweight_shard)
+    mp = _mask(active_mask, n)
+    if workspace is None and n > 0:
+        workspace = torch.empty(fused_linear_logp_backward_workspace_size(d, w), dtype=torch.uint8, device=dev)
+    wptr, wbytes = (None, 0) if workspace is None else (workspace.data_ptr(),
+                                                        workspace.numel() * workspace.element_size())
+    st = _lib.load().fused_linear_logp_shard_backward(
+        hidden.data_ptr(), n, d, ld_h, weight_shard.data_ptr(), w, ld_w, int(vocab_start), int(v_total),
+        targets.data_ptr(), int(ignore_index), mp, _inv_temperature(temperature), lse.data_ptr(), _opt_ptr(lse_lo),
+        grad.data_ptr(), wptr, wbytes, dhidden.data_ptr(), ld_dh, int(bool(accumulate_dhidden)),
+        dweight_shard.data_ptr(), ld_dw, int(bool(accumulate_dweight)), _stream(hidden))
+    _lib.check("fused_linear_logp_shard_backward", st)
+    return dweight_shard
 
 
 class FusedLinearLogp(torch.autograd.Function):

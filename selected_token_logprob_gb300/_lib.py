@@ -50,6 +50,9 @@ SIGNATURES = {
                                                         ctypes.c_float, _P, _I64, _P]),
     "fused_linear_logp_merge": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I64, _P, ctypes.c_float, _P, _P, _P,
                                                _P]),
+    "fused_linear_logp_shard_backward": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I64, _I64, _I64, _I64, _P,
+                                                        _I64, _P, ctypes.c_float, _P, _P, _P, _P, _I64, _P, _I64,
+                                                        ctypes.c_int, _P, _I64, ctypes.c_int, _P]),
     "fused_linear_logp_backward_workspace_size": (ctypes.c_int, [_I64, _I64, ctypes.POINTER(_I64)]),
     "fused_linear_logp_backward": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _I64, _P,
                                                   ctypes.c_float, _P, _P, _P, _P, _I64, _P, _I64, _P, _I64,

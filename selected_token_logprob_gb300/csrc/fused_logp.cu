@@ -833,12 +833,19 @@ flp_status fused_linear_logp_backward_workspace_size(int64_t d, int64_t v, int64
     return ok();
 }
 
-flp_status fused_linear_logp_backward(const void* hidden, int64_t n, int64_t d, int64_t ld_h, const void* weight,
-                                      int64_t v, int64_t ld_w, const int64_t* targets, int64_t ignore_index,
-                                      const uint8_t* active_mask, float inv_temperature, const float* lse,
-                                      const float* lse_lo, const float* grad, void* workspace,
-                                      int64_t workspace_bytes, float* dhidden, int64_t ld_dh, float* dweight,
-                                      int64_t ld_dw, int accumulate_dweight, flp_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The backward for weight rows = global vocabulary columns [vocab_start,
+// vocab_start + v) of a v_total-column vocabulary (the whole head: 0, v).
+flp_status linear_backward_impl(const void* hidden, int64_t n, int64_t d, int64_t ld_h, const void* weight,
+                                int64_t v, int64_t ld_w, int64_t vocab_start, int64_t v_total,
+                                const int64_t* targets, int64_t ignore_index, const uint8_t* active_mask,
+                                float inv_temperature, const float* lse, const float* lse_lo, const float* grad,
+                                void* workspace, int64_t workspace_bytes, float* dhidden, int64_t ld_dh,
+                                int accumulate_dhidden, float* dweight, int64_t ld_dw, int accumulate_dweight,
+                                flp_stream_t stream) {
     flp_status st;
     if ((st = check_scale(inv_temperature)) != FLP_OK) return st;
     if (n < 0) return fail(FLP_EINVAL, "n must be >= 0 (got %lld)", (long long)n);
@@ -857,6 +864,12 @@ flp_status fused_linear_logp_backward(const void* hidden, int64_t n, int64_t d, 
     if (!span_bytes(v, d, ld_w, 2, &span) || !span_bytes(v, d, ld_dw, 4, &span) ||
         (n > 0 && (!span_bytes(n, d, ld_h, 2, &span) || !span_bytes(n, d, ld_dh, 4, &span))))
         return fail(FLP_EINVAL, "an operand's extent overflows int64");
+    if (vocab_start < 0 || vocab_start + v > v_total)
+        return fail(FLP_EINVAL, "the weight rows [%lld, %lld) must lie inside [0, %lld)", (long long)vocab_start,
+                    (long long)(vocab_start + v), (long long)v_total);
+    if (vocab_start % flp::kLinBN != 0)
+        return fail(FLP_EUNSUPPORTED, "vocab_start (%lld) must be a multiple of the %d-column tile",
+                    (long long)vocab_start, flp::kLinBN);
     if (n == 0 && accumulate_dweight) return ok();   // no rows add nothing
     if (n == 0) {   // no rows: dW = 0, nothing else is read
         int dev0;
@@ -914,10 +927,10 @@ flp_status fused_linear_logp_backward(const void* hidden, int64_t n, int64_t d, 
         a.nrb = (int)nrb;
         a.nvt = (int)nvt;
         a.nkb = (int)ceil_div(d, flp::kLinBK);
-        a.vocab_start = 0;
-        a.v_total = v;
-        a.vt0 = 0;
-        a.nvt_total = (int)nvt;
+        a.vocab_start = vocab_start;
+        a.v_total = v_total;
+        a.vt0 = (int)(vocab_start / flp::kLinBN);
+        a.nvt_total = (int)linear_vocab_tiles(v_total);
         a.y = targets + start;
         a.ignore_index = ignore_index;
         a.mask = active_mask ? active_mask + start : nullptr;
@@ -933,12 +946,15 @@ flp_status fused_linear_logp_backward(const void* hidden, int64_t n, int64_t d, 
         flp::k_linear_logp_tiles<true><<<grid, flp::kLinThreads, flp::kLinSmemBytes, s>>>(tm_h, tm_w, a);
         if ((st = check_launch("linear logp gradient tiles")) != FLP_OK) return st;
         // dH rows = dZ W: column-major dH^T [d x chunk] = W^T [d x v] dZ^T [v x chunk], always a full chunk
+        // (a padded last chunk goes through a scratch block), or added to dhidden when accumulating
         const bool full = rows == kLinGradChunk;
-        float* dh_out = full ? dhidden + start * ld_dh : dh_pad;
-        if ((st = lt_gemm(lt, CUBLAS_OP_N, CUBLAS_OP_N, d, kLinGradChunk, v, weight, ld_w, dz, ld_dz, 0.f, dh_out,
-                          full ? ld_dh : d, lt_ws, s, "dhidden")) != FLP_OK)
+        const bool direct = full || accumulate_dhidden;
+        float* dh_out = direct ? dhidden + start * ld_dh : dh_pad;
+        if ((st = lt_gemm(lt, CUBLAS_OP_N, CUBLAS_OP_N, d, direct ? rows : kLinGradChunk, v, weight, ld_w, dz,
+                          ld_dz, accumulate_dhidden ? 1.f : 0.f, dh_out, direct ? ld_dh : d, lt_ws, s,
+                          "dhidden")) != FLP_OK)
             return st;
-        if (!full) {
+        if (!direct) {
             const cudaError_t e = cudaMemcpy2DAsync(dhidden + start * ld_dh, (size_t)ld_dh * 4, dh_pad,
                                                     (size_t)d * 4, (size_t)d * 4, (size_t)rows,
                                                     cudaMemcpyDeviceToDevice, s);
@@ -951,6 +967,36 @@ flp_status fused_linear_logp_backward(const void* hidden, int64_t n, int64_t d, 
             return st;
     }
     return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+flp_status fused_linear_logp_backward(const void* hidden, int64_t n, int64_t d, int64_t ld_h, const void* weight,
+                                      int64_t v, int64_t ld_w, const int64_t* targets, int64_t ignore_index,
+                                      const uint8_t* active_mask, float inv_temperature, const float* lse,
+                                      const float* lse_lo, const float* grad, void* workspace,
+                                      int64_t workspace_bytes, float* dhidden, int64_t ld_dh, float* dweight,
+                                      int64_t ld_dw, int accumulate_dweight, flp_stream_t stream) {
+    return linear_backward_impl(hidden, n, d, ld_h, weight, v, ld_w, 0, v, targets, ignore_index, active_mask,
+                                inv_temperature, lse, lse_lo, grad, workspace, workspace_bytes, dhidden, ld_dh, 0,
+                                dweight, ld_dw, accumulate_dweight, stream);
+}
+
+flp_status fused_linear_logp_shard_backward(const void* hidden, int64_t n, int64_t d, int64_t ld_h,
+                                            const void* weight_shard, int64_t real_width, int64_t ld_w,
+                                            int64_t vocab_start, int64_t v_total, const int64_t* targets,
+                                            int64_t ignore_index, const uint8_t* active_mask, float inv_temperature,
+                                            const float* lse, const float* lse_lo, const float* grad,
+                                            void* workspace, int64_t workspace_bytes, float* dhidden,
+                                            int64_t ld_dh, int accumulate_dhidden, float* dweight_shard,
+                                            int64_t ld_dw, int accumulate_dweight, flp_stream_t stream) {
+    if (real_width < 1) return fail(FLP_EINVAL, "real_width must be >= 1 (got %lld)", (long long)real_width);
+    return linear_backward_impl(hidden, n, d, ld_h, weight_shard, real_width, ld_w, vocab_start, v_total, targets,
+                                ignore_index, active_mask, inv_temperature, lse, lse_lo, grad, workspace,
+                                workspace_bytes, dhidden, ld_dh, accumulate_dhidden, dweight_shard, ld_dw,
+                                accumulate_dweight, stream);
 }
 
 flp_status fused_linear_logp_forward_noalloc(const void* hidden, int64_t n, int64_t d, int64_t ld_h,

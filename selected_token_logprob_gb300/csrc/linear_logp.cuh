@@ -433,7 +433,8 @@ k_linear_logp_tiles(const __grid_constant__ CUtensorMap tm_h, const __grid_const
                     if (act) {
                         gr = lin_grad_row(__ldg(p.lse + t), p.lse_lo ? __ldg(p.lse_lo + t) : 0.f, __ldg(p.g + t),
                                           p.sc.s, p.inv_s);
-                        if (yt >= col0 && yt < col0 + kLinBN) jt = yt - col0;
+                        const int64_t yl = yt - p.vocab_start;   // target column in this call's rows
+                        if (yl >= col0 && yl < col0 + kLinBN) jt = yl - col0;
                     }
                 }
                 const int nreal = (p.v - col0 < kLinBN) ? (int)(p.v - col0) : kLinBN;

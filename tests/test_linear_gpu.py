@@ -429,3 +429,33 @@ def test_vocab_sharded_full_vocabulary_and_gate():
         assert torch.equal(_i(r), _i(o))
     with pytest.raises(flp.FusedLogpError, match="multiple"):
         flp.fused_linear_logp_shard_partials(h, w[100:], 100, v, y, ws)
+
+
+def test_vocab_sharded_backward_against_oracle():
+    """Three shards (bounds on the tile grid, one padded chunk of rows): the
+    shards' dhidden terms summed in shard order and each shard's dweight rows
+    meet the same per-element bounds against the FP64 oracle as the unsharded
+    backward, with temperature and a mask."""
+    n, d, v = 300, 256, 6000
+    bounds = (0, 1536, 4096, 6000)
+    h, w, y = workloads.linear(n, d, v, seed=95, device=DEV)
+    mask = (torch.arange(n, device=DEV) % 5 != 2)
+    g = torch.randn(n, generator=torch.Generator().manual_seed(96)).to(DEV)
+    ws = torch.empty(flp.fused_linear_logp_workspace_size(n, v), dtype=torch.uint8, device=DEV)
+    for a, b in zip(bounds[:-1], bounds[1:]):
+        flp.fused_linear_logp_shard_partials(h, w[a:b].clone(), a, v, y, ws, temperature=0.7)
+    logp, lse, lo = flp.fused_linear_logp_merge(ws, v, y, with_lse_lo=True, temperature=0.7, active_mask=mask)
+    dh = torch.empty((n, d), device=DEV)
+    dws = []
+    for k, (a, b) in enumerate(zip(bounds[:-1], bounds[1:])):
+        dws.append(flp.fused_linear_logp_shard_backward(h, w[a:b].clone(), a, v, y, lse, g, dh, k > 0, lse_lo=lo,
+                                                        temperature=0.7, active_mask=mask))
+    dw = torch.cat(dws)
+    torch.cuda.synchronize()
+    s = float(np.float32(1 / 0.7))
+    hb, wb = workloads.bf16_bits(h), workloads.bf16_bits(w)
+    ref_dh, ref_dw, ref_dz = oracle.linear_backward(hb, wb, y.cpu().numpy(), g.cpu().numpy(), scale=s,
+                                                    mask=mask.cpu().numpy().astype(np.uint8), with_dz=True)
+    hd, wd = oracle.bf16_to_f64(hb), oracle.bf16_to_f64(wb)
+    assert np.all(np.abs(dh.double().cpu().numpy() - ref_dh) <= _grad_tol(ref_dz, wd, v))
+    assert np.all(np.abs(dw.double().cpu().numpy() - ref_dw) <= _grad_tol(ref_dz.T, hd, n))
