@@ -445,7 +445,11 @@ def _linear_backward_timing(args, flp, h, w, y, lse, lse_lo, dev, stream):
 
 def _linear_e2e(args, flp, h, w, y, ws, dev, stream, world):
     """Through the public API with every input copied from pinned host memory
-    each step (hidden, targets and the LM-head weight) and logp/lse read back."""
+    each step (hidden, targets and the LM-head weight) and logp/lse read back.
+    The weight goes over in vocabulary slices on the tile grid, on two copy
+    streams, and each slice's tile partials are computed as soon as it lands
+    (the vocabulary-sharded entry points: bitwise the same result as one call);
+    the fixed-order merge follows."""
     import torch
 
     n, d = h.shape
@@ -458,14 +462,31 @@ def _linear_e2e(args, flp, h, w, y, ws, dev, stream, world):
     hlogp = torch.empty(n, dtype=torch.float32).pin_memory()
     hlse = torch.empty(n, dtype=torch.float32).pin_memory()
     dh, dw, dy = torch.empty_like(h), torch.empty_like(w), torch.empty_like(y)
-    logp = torch.empty(n, dtype=torch.float32, device=dev)
-    lse = torch.empty(n, dtype=torch.float32, device=dev)
+    tiles = -(-v // 256)
+    slices = max(1, min(args.e2e_chunks, tiles))
+    per = -(-tiles // slices) * 256
+    bounds = [(a, min(v, a + per)) for a in range(0, v, per)]
+    copy_streams = [torch.cuda.Stream(dev) for _ in range(2)]
+    h_landed = torch.cuda.Event()
+    landed = [torch.cuda.Event() for _ in bounds]
 
     def step():
-        dh.copy_(hh, non_blocking=True)
-        dw.copy_(hw, non_blocking=True)
-        dy.copy_(hy, non_blocking=True)
-        flp.fused_linear_logp_forward(dh, dw, dy, logp=logp, lse=lse, workspace=ws)
+        for cs in copy_streams:
+            cs.wait_stream(stream)             # the previous step is done with these buffers
+        with torch.cuda.stream(copy_streams[0]):
+            dh.copy_(hh, non_blocking=True)
+            dy.copy_(hy, non_blocking=True)
+            h_landed.record(copy_streams[0])
+        for k, (a, b) in enumerate(bounds):
+            cs = copy_streams[k % 2]
+            with torch.cuda.stream(cs):
+                dw[a:b].copy_(hw[a:b], non_blocking=True)
+                landed[k].record(cs)
+        stream.wait_event(h_landed)
+        for k, (a, b) in enumerate(bounds):
+            stream.wait_event(landed[k])
+            flp.fused_linear_logp_shard_partials(dh, dw[a:b], a, v, dy, ws)
+        logp, lse = flp.fused_linear_logp_merge(ws, v, dy)
         hlogp.copy_(logp, non_blocking=True)
         hlse.copy_(lse, non_blocking=True)
 
@@ -473,18 +494,19 @@ def _linear_e2e(args, flp, h, w, y, ws, dev, stream, world):
     step()
     torch.cuda.synchronize(dev)
     _barrier(world)
-    a = torch.cuda.Event(enable_timing=True)
-    b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
+    a_ev = torch.cuda.Event(enable_timing=True)
+    b_ev = torch.cuda.Event(enable_timing=True)
+    a_ev.record(stream)
     for _ in range(steps):
         step()
-    b.record(stream)
+    b_ev.record(stream)
     torch.cuda.synchronize(dev)
-    ms = _max_over_ranks(a.elapsed_time(b) / steps, world, dev)
+    ms = _max_over_ranks(a_ev.elapsed_time(b_ev) / steps, world, dev)
     return {"value": round(world * 2.0 * n * v * d / (ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 3), "steps": steps,
-            "h2d_bytes_per_step": (n + v) * d * 2 + n * 8, "d2h_bytes_per_step": n * 4 * 2}
-
+            "h2d_bytes_per_step": (n + v) * d * 2 + n * 8, "d2h_bytes_per_step": n * 4 * 2,
+            "pipeline": f"weight in {len(bounds)} vocabulary slices on 2 copy streams, each slice's tile "
+                        f"partials computed as it lands, then the merge"}
 
 def _linear_cpu_baseline(args, h, w, y, v, d):
     """The FP64 oracle on a bounded row sample of the same workload."""
