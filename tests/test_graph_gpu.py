@@ -1,0 +1,78 @@
+"""The entry points only enqueue work on the caller's stream (no allocation,
+no synchronisation inside a call), so a training step built from them can be
+captured once as a CUDA graph and replayed: the replays give the eager
+results bit for bit."""
+
+import pytest
+import torch
+
+import selected_token_logprob_gb300 as flp
+import workloads
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    flp._lib.load(build_if_missing=True)
+
+
+def _i(t):
+    return t.view(torch.int32) if t.dtype == torch.float32 else t.view(torch.int16)
+
+
+def test_logits_step_replays_bitwise():
+    x, y, g = workloads.make("mid", device=DEV, n=256)
+    n, v = x.shape
+    logp, lse, lo = (torch.empty(n, device=DEV) for _ in range(3))
+    dl = torch.empty_like(x)
+
+    def step():
+        flp.fused_logp_forward(x, y, logp=logp, lse=lse, lse_lo=lo)
+        flp.fused_logp_backward(x, y, lse, g, dlogits=dl, lse_lo=lo)
+
+    step()                                   # one-time set-up happens outside the capture
+    torch.cuda.synchronize()
+    want = [t.clone() for t in (logp, lse, lo, dl)]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            step()
+    torch.cuda.current_stream().wait_stream(s)
+    for t in (logp, lse, lo, dl):
+        t.zero_()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    for got, ref in zip((logp, lse, lo, dl), want):
+        assert torch.equal(_i(got), _i(ref))
+    assert flp.flp_device_error(0) == 0
+
+
+def test_linear_forward_replays_bitwise():
+    n, d, v = 300, 512, 8000
+    h, w, y = workloads.linear(n, d, v, seed=101, device=DEV)
+    ws = torch.empty(flp.fused_linear_logp_workspace_size(n, v), dtype=torch.uint8, device=DEV)
+    logp, lse = torch.empty(n, device=DEV), torch.empty(n, device=DEV)
+
+    def step():
+        flp.fused_linear_logp_forward(h, w, y, logp=logp, lse=lse, workspace=ws)
+
+    step()
+    torch.cuda.synchronize()
+    want = [logp.clone(), lse.clone()]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            step()
+    torch.cuda.current_stream().wait_stream(s)
+    logp.zero_()
+    lse.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(_i(logp), _i(want[0])) and torch.equal(_i(lse), _i(want[1]))
