@@ -38,6 +38,8 @@ import subprocess
 import sys
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
@@ -407,6 +409,170 @@ def run_linear(args):
         dist.destroy_process_group()
 
 
+GRPO_METRIC = "GRPO loss + d loss / d logp GB/s (% HBM roofline) at N=16777216 tokens, 16384 sequences"
+
+
+def _grpo_inputs(n, nseq, seed, device):
+    """Seeded GRPO inputs: logp in (-6, 0), old and ref near it, N(0,1)
+    advantages, 10% inactive tokens, nseq packed sequences of random lengths."""
+    import torch
+
+    g = torch.Generator().manual_seed(seed)
+    lp = -torch.rand(n, generator=g) * 6 - 0.05
+    old = lp + (torch.rand(n, generator=g) - 0.5) * 1.2
+    ref = lp + (torch.rand(n, generator=g) - 0.5) * 1.0
+    adv = torch.randn(n, generator=g)
+    mask = (torch.rand(n, generator=g) > 0.1).to(torch.uint8)
+    cuts = torch.sort(torch.randint(0, n + 1, (nseq - 1,), generator=g)).values
+    cu = torch.cat([torch.zeros(1, dtype=torch.int64), cuts, torch.full((1,), n, dtype=torch.int64)])
+    return [t.to(device) for t in (lp, old, ref, adv, mask, cu)]
+
+
+def run_grpo(args):
+    """The GRPO loss on the logp path over a large RL batch: one call = the
+    per-token terms with per-chunk sums, the sequences' folds, the
+    fixed-order reduction, the per-sequence weights."""
+    import torch
+
+    import selected_token_logprob_gb300 as flp
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    flp._lib.load()
+    n, nseq = args.grpo_n, args.grpo_seqs
+    lp, old, ref, adv, mask, cu = _grpo_inputs(n, nseq, 1 + rank, dev)
+    ws = torch.empty(flp.logp_grpo_loss_workspace_size(n, nseq), dtype=torch.uint8, device=dev)
+    kw = dict(ref_logp=ref, active_mask=mask, cu_seqlens=cu, mode="seq_mean_token_mean", eps_lo=0.2,
+              eps_hi=0.28, beta=0.04, workspace=ws)
+
+    def step():
+        return flp.logp_grpo_loss(lp, old, adv, **kw)
+
+    stream = torch.cuda.current_stream(dev)
+    w0 = torch.cuda.Event(enable_timing=True)
+    w1 = torch.cuda.Event(enable_timing=True)
+    w0.record(stream)
+    for _ in range(args.warmup):
+        step()
+    w1.record(stream)
+    torch.cuda.synchronize(dev)
+    # a call takes well under a millisecond: time at least a second of them so
+    # that the clock sampler (every 200 ms) sees the timed region
+    steps = max(args.steps, int(1.0 / max(w0.elapsed_time(w1) / max(args.warmup, 1) * 1e-3, 1e-6)))
+    sampler = ClockSampler(local)
+    with sampler:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        sampler.mark()
+        t0.record(stream)
+        for _ in range(steps):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        sampler.mark()
+    ms = t0.elapsed_time(t1) / steps
+    bpt = 4 * 4 + 1 + 4              # logp, old, ref, adv read + mask read + grad written
+    alg = n * bpt + (nseq + 1) * 8
+    gbs = alg / (ms * 1e-3) / 1e9
+    peak, src = _peaks()
+    # token mean with the caller's normaliser (e.g. a count over all
+    # micro-batches): the weight is known up front, no scale pass
+    kw_tm = dict(ref_logp=ref, active_mask=mask, cu_seqlens=cu, mode="token_mean", eps_lo=0.2, eps_hi=0.28,
+                 beta=0.04, normalizer=float(n), workspace=ws)
+    for _ in range(3):
+        flp.logp_grpo_loss(lp, old, adv, **kw_tm)
+    a_ = torch.cuda.Event(enable_timing=True)
+    b_ = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    a_.record(stream)
+    for _ in range(args.steps):
+        flp.logp_grpo_loss(lp, old, adv, **kw_tm)
+    b_.record(stream)
+    torch.cuda.synchronize(dev)
+    tm_ms = a_.elapsed_time(b_) / args.steps
+    # latency at the logits workloads' size (32768 tokens, 256 sequences)
+    lp2, old2, ref2, adv2, mask2, cu2 = _grpo_inputs(32768, 256, 7, dev)
+    for _ in range(3):
+        flp.logp_grpo_loss(lp2, old2, adv2, ref_logp=ref2, active_mask=mask2, cu_seqlens=cu2,
+                           mode="seq_mean_token_mean", beta=0.04)
+    torch.cuda.synchronize(dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    ws2 = torch.empty(flp.logp_grpo_loss_workspace_size(32768, 256), dtype=torch.uint8, device=dev)
+    a.record(stream)
+    for _ in range(20):
+        flp.logp_grpo_loss(lp2, old2, adv2, ref_logp=ref2, active_mask=mask2, cu_seqlens=cu2,
+                           mode="seq_mean_token_mean", beta=0.04, workspace=ws2)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    small_us = a.elapsed_time(b) / 20 * 1e3
+    # end to end: the step's inputs from pinned host memory, the loss read back
+    host = [t.cpu().pin_memory() for t in (lp, old, ref, adv, mask, cu)]
+    devs = [torch.empty_like(t) for t in (lp, old, ref, adv, mask, cu)]
+    hloss = torch.empty(1, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        for d_, h_ in zip(devs, host):
+            d_.copy_(h_, non_blocking=True)
+        loss, _ = flp.logp_grpo_loss(devs[0], devs[1], devs[3], ref_logp=devs[2], active_mask=devs[4],
+                                     cu_seqlens=devs[5], mode="seq_mean_token_mean", eps_lo=0.2, eps_hi=0.28,
+                                     beta=0.04, workspace=ws)
+        hloss.copy_(loss, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    a.record(stream)
+    for _ in range(max(1, args.e2e_steps)):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = a.elapsed_time(b) / max(1, args.e2e_steps)
+    h2d = sum(t.numel() * t.element_size() for t in host)
+    line = {
+        "metric": GRPO_METRIC if (n, nseq) == (16777216, 16384) else f"GRPO loss GB/s at N={n}, {nseq} sequences",
+        "value": round(gbs, 1), "unit": "GB/s", "n_gpus": 1, "steps": steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"GRPO clipped surrogate + k3 KL (beta 0.04), seq_mean_token_mean, {n} tokens in "
+                               f"{nseq} packed sequences of random lengths, 10% inactive (synthetic)",
+                   "n": n, "num_seqs": nseq, "parallelism": "single GPU",
+                   "l2": f"inputs {n * 17 / 1e6:.0f} MB per step against a 129 MB L2 (no flush)"},
+        "roofline": {"kernel": "k_grpo_terms + k_grpo_segments + k_grpo_reduce + k_grpo_scale (the whole call)",
+                     "bound": "hbm",
+                     "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4),
+                     "peak_source": src, "bytes_per_token": bpt, "traffic": None},
+        "small_call_us": {"n": 32768, "num_seqs": 256, "us": round(small_us, 2)},
+        "token_mean_with_normalizer": {"ms_per_step": round(tm_ms, 4),
+                                       "GB/s": round(alg / (tm_ms * 1e-3) / 1e9, 1),
+                                       "frac": round(alg / (tm_ms * 1e-3) / 1e9 / peak, 4)},
+        "e2e": {"value": round(alg / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 3),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4},
+        "gpu_launches": 4 * steps,
+        "clocks": sampler.summary(),
+    }
+    if rank == 0 and args.cpu_seconds > 0:
+        import oracle
+
+        rows = min(n, 1 << 20)
+        hl = [t[:rows].double().cpu().numpy() for t in (lp, old, ref, adv)]
+        hm = mask[:rows].cpu().numpy()
+        cut = cu.cpu().numpy()
+        cut = np.concatenate([cut[cut < rows], [rows]])
+        t_start, done = time.perf_counter(), 0
+        while True:
+            oracle.grpo_loss(hl[0], hl[1], hl[3], ref_logp=hl[2], mask=hm, cu_seqlens=cut,
+                             mode="seq_mean_token_mean", eps_lo=0.2, eps_hi=0.28, beta=0.04)
+            done += 1
+            el = time.perf_counter() - t_start
+            if el >= min(args.cpu_seconds, 5.0):
+                break
+        line["cpu_baseline"] = {"value": round(done * (rows * bpt) / el / 1e9, 3), "unit": "GB/s",
+                                "cores": oracle.num_threads(), "kind": "oracle",
+                                "sample": f"{done} x {rows} tokens (the first {rows} of the batch), FP64, {el:.1f} s"}
+    print(json.dumps(line), flush=True)
+
+
 def _linear_backward_timing(args, flp, h, w, y, lse, lse_lo, dev, stream):
     """The fused LM-head backward (dZ recomputed on the tensor cores per
     4096-row chunk, dH and dW as two library GEMMs): 3 contractions of 2 N V D
@@ -736,11 +902,13 @@ def main(argv=None):
     ap.add_argument("--dtype", choices=["bf16", "f16", "f32"], default="bf16",
                     help="logits dtype (the metric is quoted for bf16)")
     ap.add_argument("--temperature", type=float, default=1.0)
-    ap.add_argument("--path", choices=["logits", "linear"], default="logits",
+    ap.add_argument("--path", choices=["logits", "linear", "grpo"], default="logits",
                     help="logits: logp fwd+bwd over BF16 logits (the headline); "
                          "linear: fused LM head + logp forward")
     ap.add_argument("--linear-n", type=int, default=32768)
     ap.add_argument("--linear-d", type=int, default=4096)
+    ap.add_argument("--grpo-n", type=int, default=16777216)
+    ap.add_argument("--grpo-seqs", type=int, default=16384)
     ap.add_argument("--linear-bwd-steps", type=int, default=5,
                     help="timed calls of the fused LM-head backward (0: skip)")
     args = ap.parse_args(argv)
@@ -749,6 +917,8 @@ def main(argv=None):
         run_reference(args)
     elif args.path == "linear":
         run_linear(args)
+    elif args.path == "grpo":
+        run_grpo(args)
     else:
         run_ours(args)
 

@@ -456,6 +456,8 @@ void oracle_grpo_loss(const double* logp, const double* old, const double* ref,
         nseq = 1;
     }
     double tot = 0.0, d_tok = 0.0, s_act = 0.0, seq_terms = 0.0;
+    /* a token in no sequence takes part in no term: gradient 0 */
+    for (int64_t t = 0; t < n; ++t) g[t] = 0.0;
     for (int64_t s = 0; s < nseq; ++s) {
         double sum = 0.0, cnt = 0.0;
         for (int64_t t = cu[s]; t < cu[s + 1]; ++t) {

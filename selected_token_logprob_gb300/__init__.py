@@ -63,6 +63,7 @@ __all__ = [
     "fused_linear_logp_shard_partials",
     "fused_linear_logp_workspace_size",
     "logp_grpo_loss",
+    "logp_grpo_loss_workspace_size",
     "logp_merge_partials",
     "logp_shard_partials",
 ]
@@ -275,10 +276,13 @@ def logp_grpo_loss(logp: torch.Tensor, old_logp: torch.Tensor, advantages: torch
                    ref_logp: torch.Tensor | None = None, active_mask: torch.Tensor | None = None,
                    cu_seqlens: torch.Tensor | None = None, mode: str = "token_mean",
                    eps_lo: float = 0.2, eps_hi: float = 0.2, beta: float = 0.0,
-                   normalizer: float = 0.0, token_loss: bool = False):
+                   normalizer: float = 0.0, token_loss: bool = False,
+                   workspace: torch.Tensor | None = None):
     """GRPO clipped-surrogate loss of per-token logp: (loss FP32 [1], grad
     FP32 [N] = d loss / d logp) [+ per-token loss FP32 [N] if token_loss].
-    ``grad`` is the upstream gradient for ``fused_logp_backward``."""
+    ``grad`` is the upstream gradient for ``fused_logp_backward``.
+    ``workspace`` (a CUDA byte tensor of logp_grpo_loss_workspace_size(N, S)
+    bytes) is allocated when not given."""
     n = logp.shape[0] if logp.dim() == 1 else -1
     for name, t in (("logp", logp), ("old_logp", old_logp), ("advantages", advantages)):
         _vec(t, name, n, torch.float32)
@@ -298,13 +302,27 @@ def logp_grpo_loss(logp: torch.Tensor, old_logp: torch.Tensor, advantages: torch
     loss = torch.empty(1, dtype=torch.float32, device=dev)
     grad = torch.empty(n, dtype=torch.float32, device=dev)
     tl = torch.empty(n, dtype=torch.float32, device=dev) if token_loss else None
+    if workspace is None:
+        workspace = torch.empty(logp_grpo_loss_workspace_size(n, nseq), dtype=torch.uint8, device=dev)
+    _cuda(workspace)
     st = _lib.load().logp_grpo_loss(logp.data_ptr(), old_logp.data_ptr(), _opt_ptr(ref_logp),
                                     advantages.data_ptr(), mp, _opt_ptr(cu_seqlens), nseq, n,
                                     GRPO_MODES[mode], float(eps_lo), float(eps_hi), float(beta),
-                                    float(normalizer), loss.data_ptr(), grad.data_ptr(),
-                                    _opt_ptr(tl), _stream(logp))
+                                    float(normalizer), workspace.data_ptr(),
+                                    workspace.numel() * workspace.element_size(), loss.data_ptr(),
+                                    grad.data_ptr(), _opt_ptr(tl), _stream(logp))
     _lib.check("logp_grpo_loss", st)
     return (loss, grad, tl) if token_loss else (loss, grad)
+
+
+def logp_grpo_loss_workspace_size(n: int, num_seqs: int = 0) -> int:
+    """Bytes of device scratch that logp_grpo_loss needs."""
+    import ctypes
+
+    b = ctypes.c_int64(0)
+    _lib.check("logp_grpo_loss_workspace_size",
+               _lib.load().logp_grpo_loss_workspace_size(int(n), int(num_seqs), ctypes.byref(b)))
+    return int(b.value)
 
 
 def fused_linear_logp_workspace_size(n: int, v: int) -> int:

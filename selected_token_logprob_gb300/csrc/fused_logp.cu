@@ -509,6 +509,17 @@ flp_status linear_merge_launch(int dev, const float* ws, int64_t n, int64_t v_to
     return check_launch("linear logp merge");
 }
 
+// GRPO workspace: 32 bytes of normaliser words and the fold's ticket, the
+// fold's per-CTA partials (32 bytes each), per 256-token chunk a two-float
+// sum and a count, and with sequences per (sequence, chunk) piece
+// slot the same, per sequence a two-float mean and a count, and per 256-token
+// chunk its first sequence; rounded up to 256 bytes.
+int64_t grpo_workspace_bytes(int64_t n, int64_t nseq) {
+    const int64_t nchunks = ceil_div(n, flp::kGrpoChunk);
+    const int64_t seq_part = nseq > 0 ? 16 * (nseq + nchunks) + 16 * nseq + 8 * nchunks : 0;
+    return ceil_div(32 + 32 * flp::kGrpoReduceCtas + 16 * nchunks + seq_part, 256) * 256;
+}
+
 }  // namespace
 
 extern "C" {
@@ -1030,11 +1041,19 @@ flp_status fused_linear_logp_forward_noalloc(const void* hidden, int64_t n, int6
                                      inv_temperature, scratch, kNoAllocScratchBytes, logp, lse, lse_lo, stream);
 }
 
+flp_status logp_grpo_loss_workspace_size(int64_t n, int64_t num_seqs, int64_t* bytes) {
+    if (bytes == nullptr) return fail(FLP_EINVAL, "bytes is a null pointer");
+    if (n < 0 || num_seqs < 0) return fail(FLP_EINVAL, "n and num_seqs must be >= 0");
+    *bytes = grpo_workspace_bytes(n, num_seqs);
+    return ok();
+}
+
 flp_status logp_grpo_loss(const float* logp, const float* old_logp, const float* ref_logp,
                           const float* advantages, const uint8_t* active_mask,
                           const int64_t* cu_seqlens, int64_t num_seqs, int64_t n, int mode,
-                          float eps_lo, float eps_hi, float beta, float normalizer, float* loss,
-                          float* grad, float* token_loss, flp_stream_t stream) {
+                          float eps_lo, float eps_hi, float beta, float normalizer, void* workspace,
+                          int64_t workspace_bytes, float* loss, float* grad, float* token_loss,
+                          flp_stream_t stream) {
     flp_status st;
     if (n < 0) return fail(FLP_EINVAL, "n must be >= 0 (got %lld)", (long long)n);
     if (mode < FLP_GRPO_TOKEN_MEAN || mode > FLP_GRPO_SEQ_MEAN_TOKEN_SUM)
@@ -1043,27 +1062,85 @@ flp_status logp_grpo_loss(const float* logp, const float* old_logp, const float*
         return fail(FLP_EINVAL, "clip range needs 0 <= eps_lo < 1 and finite eps_hi >= 0");
     if (!isfinite(beta) || !isfinite(normalizer) || normalizer < 0.f)
         return fail(FLP_EINVAL, "beta and normalizer must be finite, normalizer >= 0");
-    if (cu_seqlens && num_seqs < 0) return fail(FLP_EINVAL, "num_seqs must be >= 0");
+    if (cu_seqlens && (num_seqs < 0 || num_seqs >= INT32_MAX))
+        return fail(FLP_EINVAL, "num_seqs must be in [0, 2^31 - 1)");
     if (!cu_seqlens && mode != FLP_GRPO_TOKEN_MEAN && num_seqs != 0 && num_seqs != 1)
         return fail(FLP_EINVAL, "sequence normalisers need cu_seqlens (or the whole batch as one sequence)");
-    const void* ptrs[] = {logp, old_logp, advantages, loss, grad, ref_logp, active_mask, cu_seqlens, token_loss};
-    const char* names[] = {"logp", "old_logp", "advantages", "loss", "grad", "ref_logp", "active_mask",
-                           "cu_seqlens", "token_loss"};
-    const bool optional[] = {false, false, false, false, false, true, true, true, true};
-    const int count = n == 0 ? 4 : 9;   // with n == 0 only the loss is written
-    const void* ptrs0[] = {loss};
-    const char* names0[] = {"loss"};
+    const int64_t nseq = cu_seqlens ? num_seqs : 0;
+    const int64_t need = grpo_workspace_bytes(n, nseq);
+    if (workspace_bytes < need)
+        return fail(FLP_EINVAL, "workspace_bytes (%lld) is below the %lld bytes needed", (long long)workspace_bytes,
+                    (long long)need);
+    if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0)
+        return fail(FLP_EINVAL, "workspace must start on a 16-byte boundary");
+    const void* ptrs[] = {loss, workspace, logp, old_logp, advantages, grad, ref_logp, active_mask, cu_seqlens,
+                          token_loss};
+    const char* names[] = {"loss", "workspace", "logp", "old_logp", "advantages", "grad", "ref_logp",
+                           "active_mask", "cu_seqlens", "token_loss"};
+    const bool optional[] = {false, false, false, false, false, false, true, true, true, true};
     int dev;
-    if ((st = n == 0 ? common_device(1, ptrs0, names0, nullptr, &dev)
-                     : common_device(count, ptrs, names, optional, &dev)) != FLP_OK)
-        return st;
+    // with n == 0 only the loss (and the workspace's two normaliser words) are written
+    if ((st = common_device(n == 0 ? 2 : 10, ptrs, names, optional, &dev)) != FLP_OK) return st;
+    if (dev < 0 || dev >= kMaxDevices) return fail(FLP_ECUDA, "device index %d out of range", dev);
     DeviceGuard guard;
     if ((st = guard.enter(dev)) != FLP_OK) return st;
-    const flp::GrpoArgs a{logp, old_logp, ref_logp, advantages, active_mask, cu_seqlens,
-                          cu_seqlens ? num_seqs : 0, n, mode, eps_lo, eps_hi, beta, normalizer,
-                          loss, grad, token_loss};
-    flp::k_grpo_loss<<<1, flp::kGrpoThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a);
-    return check_launch("grpo loss");
+    // with a caller's normaliser the token mean and the sequence mean of sums
+    // have one weight known now: pass 1 applies it and the scale pass is skipped
+    const float prescale =
+        (normalizer > 0.f && mode != FLP_GRPO_SEQ_MEAN_TOKEN_MEAN) ? (float)(1.0 / (double)normalizer) : 0.f;
+    const flp::GrpoArgs a{logp, old_logp, ref_logp, advantages, active_mask, cu_seqlens, nseq, n, mode,
+                          eps_lo, eps_hi, beta, normalizer, prescale, loss, grad, token_loss};
+    const int64_t nchunks = ceil_div(n, flp::kGrpoChunk);
+    const int64_t slots = nseq > 0 ? nseq + nchunks : 0;
+    char* base = static_cast<char*>(workspace);
+    flp::GrpoWork wk;
+    wk.den = reinterpret_cast<double*>(base);
+    wk.wt = reinterpret_cast<float*>(base + 16);
+    wk.ticket = reinterpret_cast<unsigned*>(base + 20);
+    wk.part_t = reinterpret_cast<flp::FF*>(base + 32);
+    wk.part_q = wk.part_t + flp::kGrpoReduceCtas;
+    wk.part_c = reinterpret_cast<int64_t*>(wk.part_q + flp::kGrpoReduceCtas);
+    wk.part_a = wk.part_c + flp::kGrpoReduceCtas;
+    wk.chunk_sum = reinterpret_cast<flp::FF*>(wk.part_a + flp::kGrpoReduceCtas);
+    wk.chunk_cnt = reinterpret_cast<int64_t*>(wk.chunk_sum + nchunks);
+    wk.piece = reinterpret_cast<flp::FF*>(wk.chunk_cnt + nchunks);
+    wk.piece_cnt = reinterpret_cast<int64_t*>(wk.piece + slots);
+    wk.seg_mean = reinterpret_cast<flp::FF*>(wk.piece_cnt + slots);
+    wk.seg_cnt = reinterpret_cast<int64_t*>(wk.seg_mean + (nseq > 0 ? nseq : 0));
+    wk.chunk_first = wk.seg_cnt + (nseq > 0 ? nseq : 0);
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int sms = sm_count(dev);
+    if (sms <= 0) return fail(FLP_ECUDA, "cannot read the SM count of device %d", dev);
+    const int64_t cap = (int64_t)sms * 8;
+    const int64_t tok_ctas = ceil_div(nchunks, flp::kGrpoPassThreads / 32);
+    const int tok_grid = (int)(tok_ctas < cap ? (tok_ctas < 1 ? 1 : tok_ctas) : cap);
+    auto al = [](const void* q, uintptr_t m) { return (reinterpret_cast<uintptr_t>(q) & (m - 1)) == 0; };
+    const bool vec = al(logp, 16) && al(old_logp, 16) && al(advantages, 16) && al(grad, 16) && al(ref_logp, 16) &&
+                     al(token_loss, 16) && al(active_mask, 4);
+    if (n > 0) {
+        if (vec)
+            flp::k_grpo_terms<true><<<tok_grid, flp::kGrpoPassThreads, 0, s>>>(a, wk);
+        else
+            flp::k_grpo_terms<false><<<tok_grid, flp::kGrpoPassThreads, 0, s>>>(a, wk);
+        if ((st = check_launch("grpo terms")) != FLP_OK) return st;
+        if (cu_seqlens && mode != FLP_GRPO_TOKEN_MEAN && nseq > 0) {
+            const int64_t ctas = ceil_div(nseq, flp::kGrpoPassThreads);
+            flp::k_grpo_segments<<<(int)(ctas < cap ? ctas : cap), flp::kGrpoPassThreads, 0, s>>>(a, wk);
+            if ((st = check_launch("grpo segments")) != FLP_OK) return st;
+        }
+    }
+    // the fold's first level has a fixed CTA count (its order depends on it);
+    // with no tokens there is nothing to fold and one CTA writes the result
+    flp::k_grpo_reduce<<<n > 0 ? flp::kGrpoReduceCtas : 1, flp::kGrpoReduceThreads, 0, s>>>(a, wk);
+    if ((st = check_launch("grpo reduce")) != FLP_OK) return st;
+    if (n > 0 && prescale == 0.f) {
+        if (vec)
+            flp::k_grpo_scale<true><<<tok_grid, flp::kGrpoPassThreads, 0, s>>>(a, wk);
+        else
+            flp::k_grpo_scale<false><<<tok_grid, flp::kGrpoPassThreads, 0, s>>>(a, wk);
+        if ((st = check_launch("grpo scale")) != FLP_OK) return st;
+    }
+    return ok();
 }
 
 flp_status flp_device_error(int device, int* code) {

@@ -11,23 +11,45 @@
 //              + beta (1 - exp(ref - logp)).
 // Normalisers: 0 token mean (sum l / D), 1 sequence mean of token means,
 // 2 sequence mean of token sums; a positive `normalizer` replaces D or the
-// number of non-empty sequences.
+// number of non-empty sequences.  Tokens outside every sequence count as
+// inactive (l = 0, gradient 0).
 //
-// One CTA of 32 warps.  Segment s (a sequence [cu[s], cu[s+1]), or a chunk of
-// 1024 tokens of the single whole-batch sequence when cu is NULL) belongs to
-// warp s mod 32; a warp walks its segments in increasing s, its lanes walk a
-// segment's tokens with stride 32, and every sum is a fixed xor butterfly over
-// the lanes followed by a left fold over the warps in warp order.  The result
-// depends only on the inputs and the segment layout, never on timing.
+// The batch is cut into fixed chunks of 256 tokens (one warp each),
+// independent of the sequence layout, so the work per warp is the same
+// whatever the sequence lengths:
+//   1. k_grpo_terms: a warp loads its chunk (8 tokens per lane in two
+//      groups of 4, 16-byte accesses when the arrays allow), finds the
+//      sequences that cross it (a 32-ary search over cu_seqlens, overlapped
+//      with the loads), and for each such run (sequence s within chunk w)
+//      sums l and counts the active tokens; the run's sums go to piece slot
+//      s + w (slots of distinct runs never collide: a later sequence only
+//      meets later chunks).  Each token's unnormalised gradient (or, when
+//      the weight is uniform and known up front, the final one) and loss are
+//      written, with the chunk's loss sum, active count and first sequence;
+//   2. k_grpo_segments (sequence normalisers): each sequence's pieces are
+//      folded into its active count and mean;
+//   3. k_grpo_reduce: 128 CTAs each fold a fixed share of the chunk totals
+//      and of the sequences; the CTA that finishes last folds the 128
+//      partials in order into the loss and the weight;
+//   4. k_grpo_scale (when the weight was not known up front): the chunks, in
+//      reverse order (the gradients written last are the likeliest still in
+//      L2), multiply each token's gradient by its sequence's weight.
+// Sums are two-float (hi + lo) compensated sums in FP32 (Knuth's TwoSum per
+// addition; the pair carries about 44 significant bits): the FP64 unit of
+// this GPU is far too slow to accumulate per token.  Token counts are
+// integers.  Every fold has an order fixed by the token positions and the
+// sequence layout, never by the grid or by timing.
 #pragma once
 
 #include "logp_prims.cuh"
 
 namespace flp {
 
-constexpr int kGrpoThreads = 1024;
+constexpr int kGrpoThreads = 1024;                                   // the single-CTA fold
 constexpr int kGrpoWarps = kGrpoThreads / 32;
-constexpr int64_t kGrpoChunk = 1024;
+constexpr int kGrpoPassThreads = 256;                                // token passes: 8 warps per CTA
+constexpr int kGrpoLaneTokens = 8;
+constexpr int64_t kGrpoChunk = 32 * kGrpoLaneTokens;                 // 256 tokens per warp
 
 struct GrpoArgs {
     const float* logp;
@@ -39,126 +61,543 @@ struct GrpoArgs {
     int64_t nseq, n;
     int mode;
     float eps_lo, eps_hi, beta, normalizer;
+    float prescale;             // > 0: the uniform weight, applied by pass 1 (no pass 4)
     float* loss;                // [1]
     float* grad;                // [n]
     float* token_loss;          // nullable [n]
 };
 
-__device__ __forceinline__ double warp_sum_d(double v) {
+// Two-float sum: value = hi + lo.
+struct FF {
+    float hi, lo;
+};
+
+// Knuth's TwoSum: s + e == a + b exactly (s = fl(a + b)).
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+__device__ __forceinline__ FF ff_add(FF x, float y) {
+    float s, e;
+    two_sum(x.hi, y, s, e);
+    return {s, __fadd_rn(x.lo, e)};
+}
+__device__ __forceinline__ FF ff_add(FF x, FF y) {
+    float s, e;
+    two_sum(x.hi, y.hi, s, e);
+    return {s, __fadd_rn(__fadd_rn(x.lo, y.lo), e)};
+}
+// Lane 0 holds the sum over the warp (fixed xor butterfly).
+__device__ __forceinline__ FF ff_warp_sum(FF v) {
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        const FF o{__shfl_xor_sync(0xffffffffu, v.hi, off), __shfl_xor_sync(0xffffffffu, v.lo, off)};
+        v = ff_add(v, o);
+    }
+    return v;
+}
+// An infinite or NaN hi makes lo meaningless (inf - inf): keep hi alone.
+__device__ __forceinline__ double ff_value(FF v) {
+    return isfinite(v.hi) ? (double)v.hi + (double)v.lo : (double)v.hi;
+}
+__device__ __forceinline__ int64_t warp_sum_i64(int64_t v) {
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
     return v;
 }
 
-// [a, b) of segment s, clamped to [0, n] and made non-decreasing.
-__device__ __forceinline__ void grpo_segment(const GrpoArgs& p, int64_t s, int64_t& a, int64_t& b) {
-    if (p.cu) {
-        a = __ldg(p.cu + s);
-        b = __ldg(p.cu + s + 1);
-        a = a < 0 ? 0 : (a > p.n ? p.n : a);
-        b = b < a ? a : (b > p.n ? p.n : b);
-    } else {
-        a = s * kGrpoChunk;
-        b = a + kGrpoChunk < p.n ? a + kGrpoChunk : p.n;
+constexpr int kGrpoReduceCtas = 128;     // first level of the fold: fixed, so the order is too
+constexpr int kGrpoReduceThreads = 256;
+static_assert(kGrpoReduceCtas <= kGrpoReduceThreads, "the last CTA takes one partial per thread");
+
+// e^x as 2^(x log2 e), the power of two from the special-function unit
+// (ex2.approx, flushing subnormal results to 0): within a few ulp for
+// |x| <~ 1, the error growing by about |x| 2^-24 from rounding x log2 e.
+__device__ __forceinline__ float grpo_exp(float x) { return ex2_ftz(__fmul_rn(x, 1.4426950408889634f)); }
+
+struct GrpoWork {
+    double* den;          // [2]: the normaliser, the number of active tokens
+    float* wt;            // [1]: the uniform weight (token mean, sequence mean of sums, or one sequence)
+    unsigned* ticket;     // [1]: CTAs of the fold that are done (zeroed by pass 1, reset by the last CTA)
+    FF* part_t;           // [kGrpoReduceCtas]: per fold CTA, loss sum
+    FF* part_q;           //   sum of sequence means
+    int64_t* part_c;      //   active tokens
+    int64_t* part_a;      //   sequences with an active token
+    FF* chunk_sum;        // [nchunks]: loss sum of each 256-token chunk
+    int64_t* chunk_cnt;   // [nchunks]: its active tokens
+    FF* piece;            // [nseq + nchunks]: loss sum of sequence s within chunk w, at s + w
+    int64_t* piece_cnt;
+    FF* seg_mean;         // [nseq]: mean loss of each sequence (mode 1)
+    int64_t* seg_cnt;     // [nseq]: active tokens of each sequence
+    int64_t* chunk_first; // [nchunks]: the first sequence that may meet each chunk
+};
+
+__device__ __forceinline__ int64_t grpo_chunks(int64_t n) { return (n + kGrpoChunk - 1) / kGrpoChunk; }
+
+// cu_seqlens[s] clamped to [0, n].
+__device__ __forceinline__ int64_t grpo_cu(const GrpoArgs& p, int64_t s) {
+    const int64_t v = __ldg(p.cu + s);
+    return v < 0 ? 0 : (v > p.n ? p.n : v);
+}
+
+// The largest s in [0, nseq] with cu[s] <= x, or -1: a 32-ary search by the
+// whole warp (each step probes the last entry of 32 equal blocks and keeps
+// the first block whose last entry is above x).  All lanes must call it.
+__device__ __forceinline__ int64_t grpo_find(const GrpoArgs& p, int64_t x, int lane) {
+    int lo = 0, hi = (int)p.nseq + 1;   // entries before lo are <= x; [lo, hi) undecided (nseq < 2^31 - 1)
+    while (lo < hi) {
+        const int step = (hi - lo + 31) >> 5;
+        const int first = lo + lane * step;
+        const int end = min(first + step, hi);
+        const bool le = first < hi && grpo_cu(p, end - 1) <= x;
+        const int k = __popc(__ballot_sync(0xffffffffu, le));
+        const int nlo = min(lo + k * step, hi);
+        hi = nlo < hi ? min(lo + (k + 1) * step, hi) - 1 : hi;   // block k's last entry is above x
+        lo = nlo;
+    }
+    return (int64_t)lo - 1;
+}
+
+// The sequences that meet the chunk starting at token c0: the first one
+// (found by the search, or recorded by pass 1) and the next 32 boundaries,
+// fetched by the lanes as chunk-local offsets clamped to [0, 256].  Taken
+// before the chunk's tokens are used, so that these L2 round trips overlap
+// the tokens' loads from HBM.
+struct GrpoRuns {
+    int64_t s;     // the first sequence that may meet the chunk
+    int bnd;       // lane j: cu[s + j] - c0 clamped to [0, 256] (256 past cu[nseq])
+    int64_t aux;   // lane j: aux[s + j] when an aux array is given (s + j < nseq), else 0
+};
+
+__device__ __forceinline__ GrpoRuns grpo_runs_at(const GrpoArgs& p, int64_t s, int64_t c0, int lane,
+                                                 const int64_t* aux) {
+    GrpoRuns r{s < 0 ? 0 : s, (int)kGrpoChunk, 0};
+    const int64_t idx = r.s + lane;
+    if (idx <= p.nseq) {
+        const int64_t d = grpo_cu(p, idx) - c0;
+        r.bnd = d < 0 ? 0 : (d > kGrpoChunk ? (int)kGrpoChunk : (int)d);
+    }
+    if (aux && idx < p.nseq) r.aux = aux[idx];
+    return r;
+}
+__device__ __forceinline__ GrpoRuns grpo_runs_begin(const GrpoArgs& p, int64_t c0, int lane) {
+    if (p.cu == nullptr) return GrpoRuns{0, 0, 0};
+    return grpo_runs_at(p, grpo_find(p, c0, lane), c0, lane, nullptr);
+}
+
+// Calls f(s, ua, ub, aux_s) for each sequence s whose tokens meet the chunk
+// of nv tokens from c0, in sequence order, with [ua, ub) the chunk-local
+// indices of its tokens there (never empty).  Warp-uniform; boundaries are
+// fetched 32 at a time.  kAux: pass the aux value (else 0, no shuffle).
+template <bool kAux, class F>
+__device__ __forceinline__ void grpo_runs(const GrpoArgs& p, GrpoRuns r, int64_t c0, int nv, int lane,
+                                          const int64_t* aux, F&& f) {
+    if (p.cu == nullptr) {
+        f((int64_t)0, 0, nv, (int64_t)0);   // one sequence: the whole batch
+        return;
+    }
+    while (r.s < p.nseq) {
+        for (int j = 0; j < 31; ++j) {
+            const int a = __shfl_sync(0xffffffffu, r.bnd, j);
+            if (r.s + j >= p.nseq || a >= nv) return;
+            const int b = min(__shfl_sync(0xffffffffu, r.bnd, j + 1), nv);
+            const int64_t x = kAux ? __shfl_sync(0xffffffffu, r.aux, j) : 0;
+            if (a < b) f(r.s + j, a, b, x);
+        }
+        r = grpo_runs_at(p, r.s + 31, c0, lane, aux);
     }
 }
 
-__global__ void __launch_bounds__(kGrpoThreads, 1) k_grpo_loss(GrpoArgs p) {
-    __shared__ double sh[kGrpoWarps][4];
-    __shared__ double sh_den;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t nseg = p.cu ? p.nseq : (p.n + kGrpoChunk - 1) / kGrpoChunk;
-    const float lo = 1.f - p.eps_lo, hi = 1.f + p.eps_hi;
-
-    // pass 1: per-token loss and unnormalised gradient, per-segment sums
-    double tot = 0.0, cnt = 0.0, seqterm = 0.0, sact = 0.0;
-    for (int64_t s = warp; s < nseg; s += kGrpoWarps) {
-        int64_t a, b;
-        grpo_segment(p, s, a, b);
-        double lsum = 0.0, lcnt = 0.0;
-        for (int64_t t = a + lane; t < b; t += 32) {
-            float l = 0.f, dl = 0.f;
-            if (p.mask == nullptr || __ldg(p.mask + t) != 0) {
-                const float lp = __ldg(p.logp + t);
-                const float A = __ldg(p.adv + t);
-                const float r = expf(__fsub_rn(lp, __ldg(p.old_logp + t)));
-                const float rc = fminf(fmaxf(r, lo), hi);
-                const float p1 = __fmul_rn(-A, r), p2 = __fmul_rn(-A, rc);
-                const bool unclipped = p1 >= p2;
-                l = unclipped ? p1 : p2;
-                dl = unclipped ? p1 : 0.f;
-                if (p.ref_logp) {
-                    const float d = __fsub_rn(__ldg(p.ref_logp + t), lp);
-                    const float e = expf(d);
-                    l = __fmaf_rn(p.beta, __fsub_rn(__fsub_rn(e, d), 1.f), l);
-                    dl = __fmaf_rn(p.beta, __fsub_rn(1.f, e), dl);
-                }
-                lsum += (double)l;
-                lcnt += 1.0;
-            }
-            p.grad[t] = dl;
-            if (p.token_loss) p.token_loss[t] = l;
-        }
-        const double ssum = warp_sum_d(lsum), scnt = warp_sum_d(lcnt);
-        tot += ssum;
-        cnt += scnt;
-        if (scnt > 0) {
-            sact += 1.0;
-            seqterm += (p.mode == 1) ? ssum / scnt : ssum;
+// Token layout of a chunk: lane L holds tokens u = 128 i + 4 L + e (i < 2,
+// e < 4) at index q = 4 i + e, so each 16-byte access of the warp covers 512
+// contiguous bytes.  kVec: the arrays are 16-byte aligned (the mask 4-byte),
+// whole groups of 4 use vector accesses; otherwise every access is scalar.
+template <bool kVec>
+__device__ __forceinline__ void grpo_ld8(const float* base, int lane, int nvalid, float (&v)[kGrpoLaneTokens]) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int u = 128 * i + 4 * lane;
+        if (kVec && u + 4 <= nvalid) {
+            const float4 x = __ldg(reinterpret_cast<const float4*>(base + u));
+            v[4 * i] = x.x;
+            v[4 * i + 1] = x.y;
+            v[4 * i + 2] = x.z;
+            v[4 * i + 3] = x.w;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[4 * i + e] = u + e < nvalid ? __ldg(base + u + e) : 0.f;
         }
     }
+}
+template <bool kVec>
+__device__ __forceinline__ void grpo_st8(float* base, int lane, int nvalid, const float (&v)[kGrpoLaneTokens]) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int u = 128 * i + 4 * lane;
+        if (kVec && u + 4 <= nvalid) {
+            *reinterpret_cast<float4*>(base + u) = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (u + e < nvalid) base[u + e] = v[4 * i + e];
+        }
+    }
+}
+// Bit q set: token q of the lane exists (u < nvalid) and its mask byte is nonzero.
+template <bool kVec>
+__device__ __forceinline__ uint32_t grpo_active8(const uint8_t* mask, int lane, int nvalid) {
+    uint32_t act = 0;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int u = 128 * i + 4 * lane;
+        if (mask == nullptr) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (u + e < nvalid) act |= 1u << (4 * i + e);
+        } else if (kVec && u + 4 <= nvalid) {
+            // bytes != 0 -> 1 in each byte, then the four bits gathered by a multiply
+            const uint32_t m = __vcmpne4(__ldg(reinterpret_cast<const unsigned int*>(mask + u)), 0u) & 0x01010101u;
+            act |= ((m * 0x01020408u) >> 24) << (4 * i);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (u + e < nvalid && __ldg(mask + u + e) != 0) act |= 1u << (4 * i + e);
+        }
+    }
+    return act;
+}
+// Bits of the lane's tokens with chunk index u in [ua, ub).
+__device__ __forceinline__ uint32_t grpo_in8(int lane, int ua, int ub) {
+    uint32_t in = 0;
+#pragma unroll
+    for (int q = 0; q < kGrpoLaneTokens; ++q) {
+        const int u = 128 * (q >> 2) + 4 * lane + (q & 3);
+        if (u >= ua && u < ub) in |= 1u << q;
+    }
+    return in;
+}
+
+template <bool kVec>
+__global__ void __launch_bounds__(kGrpoPassThreads, 4) k_grpo_terms(GrpoArgs p, GrpoWork wk) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nchunks = grpo_chunks(p.n);
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const float clo = 1.f - p.eps_lo, chi = 1.f + p.eps_hi;
+    if (blockIdx.x == 0 && threadIdx.x == 0) *wk.ticket = 0u;
+    for (int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < nchunks; w += nwarps) {
+        const int64_t c0 = w * kGrpoChunk;
+        const int nv = (int)(p.n - c0 < kGrpoChunk ? p.n - c0 : kGrpoChunk);   // tokens in the chunk
+        float lp[kGrpoLaneTokens], od[kGrpoLaneTokens], av[kGrpoLaneTokens], rf[kGrpoLaneTokens];
+        grpo_ld8<kVec>(p.logp + c0, lane, nv, lp);
+        grpo_ld8<kVec>(p.old_logp + c0, lane, nv, od);
+        grpo_ld8<kVec>(p.adv + c0, lane, nv, av);
+        if (p.ref_logp) grpo_ld8<kVec>(p.ref_logp + c0, lane, nv, rf);
+        const uint32_t act = grpo_active8<kVec>(p.mask ? p.mask + c0 : nullptr, lane, nv);
+        const GrpoRuns runs = grpo_runs_begin(p, c0, lane);   // overlaps the loads above
+        if (p.cu && p.mode == 1 && lane == 0) wk.chunk_first[w] = runs.s;
+        float l[kGrpoLaneTokens], dl[kGrpoLaneTokens];
+#pragma unroll
+        for (int q = 0; q < kGrpoLaneTokens; ++q) {
+            const float r = grpo_exp(__fsub_rn(lp[q], od[q]));
+            const float rc = fminf(fmaxf(r, clo), chi);
+            const float p1 = __fmul_rn(-av[q], r), p2 = __fmul_rn(-av[q], rc);
+            const bool unclipped = p1 >= p2;
+            l[q] = unclipped ? p1 : p2;
+            dl[q] = unclipped ? p1 : 0.f;
+            if (p.ref_logp) {
+                const float d = __fsub_rn(rf[q], lp[q]);
+                const float e = grpo_exp(d);
+                l[q] = __fmaf_rn(p.beta, __fsub_rn(__fsub_rn(e, d), 1.f), l[q]);
+                dl[q] = __fmaf_rn(p.beta, __fsub_rn(1.f, e), dl[q]);
+            }
+            // inactive tokens: 0 (their inputs may be anything)
+            const bool on = (act >> q) & 1u;
+            l[q] = on ? l[q] : 0.f;
+            dl[q] = on ? dl[q] : 0.f;
+        }
+        FF tot{0.f, 0.f};
+        int64_t tcnt = 0;
+        uint32_t inseq = 0;
+        grpo_runs<false>(p, runs, c0, nv, lane, nullptr, [&](int64_t s, int ua, int ub, int64_t) {
+            FF rs{0.f, 0.f};
+            uint32_t in;
+            if (ua == 0 && ub == nv) {   // the whole chunk: no membership tests
+                in = 0xffu;
+#pragma unroll
+                for (int q = 0; q < kGrpoLaneTokens; ++q) rs = ff_add(rs, l[q]);
+            } else {
+                in = grpo_in8(lane, ua, ub);
+#pragma unroll
+                for (int q = 0; q < kGrpoLaneTokens; ++q) rs = ff_add(rs, ((in >> q) & 1u) ? l[q] : 0.f);
+            }
+            inseq |= in;
+            rs = ff_warp_sum(rs);
+            const int cnt = __reduce_add_sync(0xffffffffu, __popc(in & act));
+            if (p.cu && p.mode != 0 && lane == 0) {
+                wk.piece[s + w] = rs;
+                wk.piece_cnt[s + w] = cnt;
+            }
+            tot = ff_add(tot, rs);
+            tcnt += cnt;
+        });
+        if (p.cu && inseq != 0xffu) {   // tokens outside every sequence
+#pragma unroll
+            for (int q = 0; q < kGrpoLaneTokens; ++q) {
+                const bool in = (inseq >> q) & 1u;
+                l[q] = in ? l[q] : 0.f;
+                dl[q] = in ? dl[q] : 0.f;
+            }
+        }
+        if (p.prescale > 0.f) {
+#pragma unroll
+            for (int q = 0; q < kGrpoLaneTokens; ++q) dl[q] = __fmul_rn(dl[q], p.prescale);
+        }
+        grpo_st8<kVec>(p.grad + c0, lane, nv, dl);
+        if (p.token_loss) grpo_st8<kVec>(p.token_loss + c0, lane, nv, l);
+        if (lane == 0) {
+            wk.chunk_sum[w] = tot;
+            wk.chunk_cnt[w] = tcnt;
+        }
+    }
+}
+
+// The mean of a sequence as two floats: sum / cnt, with the remainder of the
+// high quotient carried into the low part.
+__device__ __forceinline__ FF ff_div_count(FF s, int64_t cnt) {
+    const float c = (float)cnt;
+    const float q = __fdiv_rn(s.hi, c);
+    const float r = __fmaf_rn(-q, c, s.hi);   // s.hi - q c, exact for a correctly rounded q (c < 2^24)
+    return {q, __fdiv_rn(__fadd_rn(r, s.lo), c)};
+}
+
+// Folds v over the CTA: the fixed butterfly in each warp, then warp order
+// (thread 0 gets the result; every thread must call it).
+template <int kWarps>
+__device__ __forceinline__ FF cta_fold(FF v, int64_t& c, FF* sh_v, int64_t* sh_c) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    v = ff_warp_sum(v);
+    c = warp_sum_i64(c);
+    __syncthreads();   // the shared slots may still be read by a previous fold
     if (lane == 0) {
-        sh[warp][0] = tot;
-        sh[warp][1] = cnt;
-        sh[warp][2] = seqterm;
-        sh[warp][3] = sact;
+        sh_v[warp] = v;
+        sh_c[warp] = c;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        double T = 0.0, C = 0.0, Q = 0.0, A = 0.0;
-        for (int w = 0; w < kGrpoWarps; ++w) {
-            T += sh[w][0];
-            C += sh[w][1];
-            Q += sh[w][2];
-            A += sh[w][3];
+        v = FF{0.f, 0.f};
+        c = 0;
+        for (int w = 0; w < kWarps; ++w) {
+            v = ff_add(v, sh_v[w]);
+            c += sh_c[w];
         }
-        if (!p.cu) {  // the whole batch is one sequence
-            A = C > 0 ? 1.0 : 0.0;
-            Q = (p.mode == 1) ? (C > 0 ? T / C : 0.0) : T;
-        }
-        double den = (p.mode == 0) ? C : A;
-        if (p.normalizer > 0.f) den = (double)p.normalizer;
-        const double num = (p.mode == 0) ? T : Q;
-        p.loss[0] = den > 0 ? __double2float_rn(num / den) : 0.f;
-        sh_den = den;
-        sh[0][1] = C;   // total active tokens, for the single-sequence weights
     }
-    __syncthreads();
-    const double den = sh_den, total_cnt = sh[0][1];
+    return v;
+}
 
-    // pass 2: weights
-    for (int64_t s = warp; s < nseg; s += kGrpoWarps) {
-        int64_t a, b;
-        grpo_segment(p, s, a, b);
-        double w;
-        if (den <= 0) {
-            w = 0.0;
-        } else if (p.mode == 1) {
-            double n_s;
-            if (p.cu) {
-                double c = 0.0;
-                for (int64_t t = a + lane; t < b; t += 32)
-                    c += (p.mask == nullptr || __ldg(p.mask + t) != 0) ? 1.0 : 0.0;
-                n_s = warp_sum_d(c);
-            } else {
-                n_s = total_cnt;
+constexpr int64_t kGrpoLongPieces = 64;   // sequences with more pieces are folded by a whole warp
+
+// Per sequence s (sequence normalisers): its active-token count and, for
+// mode 1, its mean, from its chunk pieces (chunks floor(a / 256) ..
+// floor((b - 1) / 256), at slots s + chunk).  One lane per sequence folds up
+// to 64 pieces in piece order; a longer sequence is folded by its whole warp
+// (lane-strided, fixed butterfly).  Which of the two a sequence takes depends
+// only on its length, so the result does not depend on the grid.
+__global__ void __launch_bounds__(kGrpoPassThreads) k_grpo_segments(GrpoArgs p, GrpoWork wk) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t base = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31); base < p.nseq; base += nthreads) {
+        const int64_t s = base + lane;
+        int64_t j0 = 0, j1 = -1;
+        if (s < p.nseq) {
+            const int64_t a = grpo_cu(p, s), e = grpo_cu(p, s + 1);
+            if (e > a) {
+                j0 = s + a / kGrpoChunk;
+                j1 = s + (e - 1) / kGrpoChunk;
             }
-            w = n_s > 0 ? 1.0 / (den * n_s) : 0.0;
-        } else {
-            w = 1.0 / den;
         }
-        const float wf = __double2float_rn(w);
-        for (int64_t t = a + lane; t < b; t += 32) p.grad[t] = __fmul_rn(p.grad[t], wf);
+        const bool is_long = j1 - j0 + 1 > kGrpoLongPieces;
+        FF sum{0.f, 0.f};
+        int64_t cnt = 0;
+        if (!is_long) {
+            int64_t j = j0;
+            for (; j + 3 <= j1; j += 4) {   // four loads in flight, added in order
+                FF v[4];
+                int64_t c[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    v[u] = wk.piece[j + u];
+                    c[u] = wk.piece_cnt[j + u];
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    sum = ff_add(sum, v[u]);
+                    cnt += c[u];
+                }
+            }
+            for (; j <= j1; ++j) {
+                sum = ff_add(sum, wk.piece[j]);
+                cnt += wk.piece_cnt[j];
+            }
+        }
+        // the warp's long sequences, one at a time in lane order
+        for (uint32_t m = __ballot_sync(0xffffffffu, is_long); m != 0; m &= m - 1) {
+            const int src = __ffs(m) - 1;
+            const int64_t k0 = __shfl_sync(0xffffffffu, j0, src), k1 = __shfl_sync(0xffffffffu, j1, src);
+            FF ws{0.f, 0.f};
+            int64_t wc = 0;
+            for (int64_t j = k0 + lane; j <= k1; j += 32) {
+                ws = ff_add(ws, wk.piece[j]);
+                wc += wk.piece_cnt[j];
+            }
+            ws = ff_warp_sum(ws);
+            wc = warp_sum_i64(wc);
+            const FF w0{__shfl_sync(0xffffffffu, ws.hi, 0), __shfl_sync(0xffffffffu, ws.lo, 0)};
+            wc = __shfl_sync(0xffffffffu, wc, 0);
+            if (lane == src) {
+                sum = w0;
+                cnt = wc;
+            }
+        }
+        if (s < p.nseq) {
+            wk.seg_cnt[s] = cnt;
+            if (p.mode == 1) wk.seg_mean[s] = cnt > 0 ? ff_div_count(sum, cnt) : FF{0.f, 0.f};
+        }
+    }
+}
+
+// The fold of the loss and the normaliser.  kGrpoReduceCtas CTAs (1 when
+// n == 0): CTA b takes the b-th equal share of the chunk totals and,
+// for the sequence normalisers, of the sequences' counts and means.  Each
+// CTA writes its partials; the CTA that finishes last (an atomic ticket, no
+// waiting) folds the partials in CTA order and writes the loss, the
+// normaliser and the uniform weight.
+__global__ void __launch_bounds__(kGrpoReduceThreads) k_grpo_reduce(GrpoArgs p, GrpoWork wk) {
+    constexpr int kW = kGrpoReduceThreads / 32;
+    __shared__ FF sh_v[kW];
+    __shared__ int64_t sh_c[kW];
+    __shared__ bool last;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = gridDim.x, b = blockIdx.x;
+    const int64_t nchunks = grpo_chunks(p.n);
+    const bool seqs = p.cu != nullptr && p.mode != 0 && p.n > 0;
+    // chunk totals [b ps, (b + 1) ps)
+    const int64_t ps = (nchunks + G - 1) / G;
+    const int64_t k1 = (b + 1) * ps < nchunks ? (b + 1) * ps : nchunks;
+    FF T{0.f, 0.f};
+    int64_t C = 0;
+    for (int64_t k = b * ps + threadIdx.x; k < k1; k += kGrpoReduceThreads) {
+        T = ff_add(T, wk.chunk_sum[k]);
+        C += wk.chunk_cnt[k];
+    }
+    T = cta_fold<kW>(T, C, sh_v, sh_c);
+    FF Q{0.f, 0.f};
+    int64_t A = 0;
+    if (seqs) {   // the sequences [b qs, (b + 1) qs): counts and means
+        const int64_t qs = (p.nseq + G - 1) / G;
+        const int64_t s1 = (b + 1) * qs < p.nseq ? (b + 1) * qs : p.nseq;
+        for (int64_t s = b * qs + threadIdx.x; s < s1; s += kGrpoReduceThreads) {
+            if (wk.seg_cnt[s] > 0) {
+                ++A;
+                if (p.mode == 1) Q = ff_add(Q, wk.seg_mean[s]);
+            }
+        }
+        Q = cta_fold<kW>(Q, A, sh_v, sh_c);
+    }
+    if (G == 1) {
+        if (threadIdx.x == 0) {
+            wk.part_t[0] = T;
+            wk.part_q[0] = Q;
+            wk.part_c[0] = C;
+            wk.part_a[0] = A;
+        }
+    } else {
+        if (threadIdx.x == 0) {
+            wk.part_t[b] = T;
+            wk.part_q[b] = Q;
+            wk.part_c[b] = C;
+            wk.part_a[b] = A;
+            __threadfence();
+            last = atomicAdd(wk.ticket, 1u) == (unsigned)(G - 1);
+        }
+        __syncthreads();
+        if (!last) return;
+        __threadfence();
+    }
+    // the last CTA: thread i takes partial i; the CTA fold combines them (a
+    // fixed butterfly per warp, then warp order)
+    FF t{0.f, 0.f}, q{0.f, 0.f};
+    int64_t c = 0, a = 0;
+    if ((int)threadIdx.x < G) {
+        const float2 tv = __ldcg(reinterpret_cast<const float2*>(wk.part_t) + threadIdx.x);
+        const float2 qv = __ldcg(reinterpret_cast<const float2*>(wk.part_q) + threadIdx.x);
+        t = FF{tv.x, tv.y};
+        q = FF{qv.x, qv.y};
+        c = __ldcg(reinterpret_cast<const long long*>(wk.part_c) + threadIdx.x);
+        a = __ldcg(reinterpret_cast<const long long*>(wk.part_a) + threadIdx.x);
+    }
+    t = cta_fold<kW>(t, c, sh_v, sh_c);
+    q = cta_fold<kW>(q, a, sh_v, sh_c);
+    if (threadIdx.x == 0) {
+        const double tt = ff_value(t), cnt = (double)c;
+        double qq = ff_value(q), aa = (double)a;
+        if (!seqs) {   // the whole batch is one sequence (or token mean)
+            aa = c > 0 ? 1.0 : 0.0;
+            qq = c > 0 ? tt / cnt : 0.0;
+        }
+        double den = (p.mode == 0) ? cnt : aa;
+        if (p.normalizer > 0.f) den = (double)p.normalizer;
+        const double num = (p.mode == 1) ? qq : tt;
+        p.loss[0] = den > 0 ? __double2float_rn(num / den) : 0.f;
+        wk.den[0] = den;
+        wk.den[1] = cnt;
+        double w = 0.0;
+        if (den > 0) w = (p.mode == 1 && p.cu == nullptr) ? (c > 0 ? 1.0 / (den * cnt) : 0.0) : 1.0 / den;
+        wk.wt[0] = __double2float_rn(w);
+        if (G > 1) *wk.ticket = 0u;
+    }
+}
+
+// Each token's gradient times its weight: 1 / den, or for the sequence mean
+// of token means with sequences 1 / (den n_s), n_s the sequence's active
+// tokens (formed in FP32: den n_s rounded, then its correctly rounded
+// reciprocal).
+template <bool kVec>
+__global__ void __launch_bounds__(kGrpoPassThreads, 4) k_grpo_scale(GrpoArgs p, GrpoWork wk) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nchunks = grpo_chunks(p.n);
+    const double den = wk.den[0];
+    if (!(den > 0)) return;   // no active token: every gradient is already 0
+    const float wu = wk.wt[0];
+    const bool per_seq = p.mode == 1 && p.cu != nullptr;
+    const float denf = (float)den;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t ww = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; ww < nchunks; ww += nwarps) {
+        const int64_t w = nchunks - 1 - ww;
+        const int64_t c0 = w * kGrpoChunk;
+        const int nv = (int)(p.n - c0 < kGrpoChunk ? p.n - c0 : kGrpoChunk);
+        float g[kGrpoLaneTokens];
+        grpo_ld8<kVec>(p.grad + c0, lane, nv, g);
+        if (per_seq) {
+            // the first sequence recorded by pass 1; boundaries and counts in one trip
+            const GrpoRuns runs = grpo_runs_at(p, wk.chunk_first[w], c0, lane, wk.seg_cnt);
+            float wt[kGrpoLaneTokens];
+#pragma unroll
+            for (int q = 0; q < kGrpoLaneTokens; ++q) wt[q] = 0.f;
+            grpo_runs<true>(p, runs, c0, nv, lane, wk.seg_cnt, [&](int64_t, int ua, int ub, int64_t c) {
+                const float ws = c > 0 ? __frcp_rn(__fmul_rn(denf, (float)c)) : 0.f;
+                const uint32_t in = grpo_in8(lane, ua, ub);
+#pragma unroll
+                for (int q = 0; q < kGrpoLaneTokens; ++q)
+                    if ((in >> q) & 1u) wt[q] = ws;
+            });
+#pragma unroll
+            for (int q = 0; q < kGrpoLaneTokens; ++q) g[q] = __fmul_rn(g[q], wt[q]);
+        } else {
+#pragma unroll
+            for (int q = 0; q < kGrpoLaneTokens; ++q) g[q] = __fmul_rn(g[q], wu);
+        }
+        grpo_st8<kVec>(p.grad + c0, lane, nv, g);
     }
 }
 

@@ -269,3 +269,25 @@ def test_linear_shard_host_checks(lib):
     assert lib.fused_linear_logp_merge(None, 0, 0, 10, None, -100, None, 1.0, None, None, None, None) == 0
     assert lib.fused_linear_logp_merge(1 << 20, 10, 16, 2000, 1 << 21, -100, None, 1.0, 1 << 22, 1 << 23,
                                        None, None) == EINVAL   # workspace too small
+
+
+def test_grpo_host_checks(lib):
+    b = ctypes.c_int64(0)
+    # 32 bytes of normaliser words, 128 fold partials of 32 bytes, 16 per
+    # 256-token chunk, and with S sequences 16 per piece slot (S + chunks), 16
+    # per sequence and 8 per chunk; rounded up to 256:
+    # 32 + 4096 + 16*128 = 6176 -> 6400;  + 16*228 + 16*100 + 8*128 -> 12544
+    assert lib.logp_grpo_loss_workspace_size(32768, 0, ctypes.byref(b)) == 0 and b.value == 6400
+    assert lib.logp_grpo_loss_workspace_size(32768, 100, ctypes.byref(b)) == 0 and b.value == 12544
+    assert lib.logp_grpo_loss_workspace_size(0, 0, ctypes.byref(b)) == 0 and b.value == 4352
+    assert lib.logp_grpo_loss_workspace_size(-1, 0, ctypes.byref(b)) == EINVAL
+
+    def call(mode=0, ws=1 << 20, ws_bytes=1 << 20, n=1000, eps_lo=0.2):
+        return lib.logp_grpo_loss(1 << 21, 1 << 22, None, 1 << 23, None, None, 0, n, mode, eps_lo, 0.2, 0.0,
+                                  0.0, ws, ws_bytes, 1 << 24, 1 << 25, None, None)
+
+    assert call(mode=3) == EINVAL and b"mode" in lib.flp_last_error()
+    assert call(eps_lo=1.5) == EINVAL
+    assert call(ws_bytes=8) == EINVAL and b"workspace" in lib.flp_last_error()
+    assert call(ws=(1 << 20) + 8) == EINVAL
+    assert call() == EINVAL                            # host pointers are not device memory

@@ -107,7 +107,7 @@ def test_grpo_edge_cases():
     assert abs(loss.item() - want_l) <= 1e-5 * abs(want_l) + 1e-7
     with pytest.raises(flp.FusedLogpError, match="mode"):
         flp._lib.check("logp_grpo_loss", flp._lib.load().logp_grpo_loss(
-            None, None, None, None, None, None, 0, 0, 7, 0.2, 0.2, 0.0, 0.0, None, None, None, None))
+            None, None, None, None, None, None, 0, 0, 7, 0.2, 0.2, 0.0, 0.0, None, 0, None, None, None, None))
 
 
 def test_rl_step_chain_against_fp64():
@@ -135,3 +135,121 @@ def test_rl_step_chain_against_fp64():
     # the GPU's upstream gradient differs from the FP64 one by ~1e-6 relative,
     # so the bound is the plain max-error bound (not the correctly rounded count)
     assert st["max_abs_diff"] <= max(2e-3 * st["max_abs_d"], 2 * st["max_rounding_gap"]), st
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_grpo_many_segments_against_oracle(mode):
+    """A million tokens in 3000 packed sequences (many CTAs in the terms and
+    scale passes) and the whole-batch form (1024 chunks), against FP64."""
+    n = 1 << 20
+    lp, old, ref, adv, mask, cu = _case(n, 11, nseq=3000)
+    for cuv in (cu, None):
+        if cuv is None and mode != "token_mean":
+            continue
+        kw = dict(mode=mode, eps_lo=0.2, eps_hi=0.28, beta=0.02)
+        loss, grad = flp.logp_grpo_loss(*_dev(lp, old, adv), ref_logp=_dev(ref)[0], active_mask=_dev(mask)[0],
+                                        cu_seqlens=None if cuv is None else _dev(cuv)[0], **kw)
+        want_l, want_g = oracle.grpo_loss(lp.double().numpy(), old.double().numpy(), adv.double().numpy(),
+                                          ref_logp=ref.double().numpy(), mask=mask.numpy(),
+                                          cu_seqlens=None if cuv is None else cuv.numpy(), **kw)
+        got_g = grad.double().cpu().numpy()
+        assert abs(loss.item() - want_l) <= 1e-5 * abs(want_l) + 1e-7, (loss.item(), want_l)
+        assert np.max(np.abs(got_g - want_g)) <= 1e-5 * np.max(np.abs(want_g))
+        again = flp.logp_grpo_loss(*_dev(lp, old, adv), ref_logp=_dev(ref)[0], active_mask=_dev(mask)[0],
+                                   cu_seqlens=None if cuv is None else _dev(cuv)[0], **kw)
+        assert torch.equal(again[0].view(torch.int32), loss.view(torch.int32))
+        assert torch.equal(again[1].view(torch.int32), grad.view(torch.int32))
+
+
+def _layout(n, seed):
+    """cu_seqlens that leave 37 tokens uncovered in front and 123 behind, with
+    900 sequences of 0..3 tokens (so one 256-token chunk meets well over 31
+    sequences), one sequence of 20000 tokens (about 80 chunks) and random
+    lengths up to 700 after it."""
+    g = torch.Generator().manual_seed(seed)
+    lens = torch.randint(0, 4, (900,), generator=g).tolist() + [20000]
+    pos = 37 + sum(lens)
+    while True:
+        ln = int(torch.randint(1, 700, (1,), generator=g))
+        if pos + ln > n - 123:
+            break
+        lens.append(ln)
+        pos += ln
+    return torch.cumsum(torch.tensor([37] + lens, dtype=torch.int64), 0)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_grpo_uncovered_tiny_and_long_sequences(mode):
+    n = 60000
+    lp, old, ref, adv, mask, _ = _case(n, 21)
+    cu = _layout(n, 22)
+    cover = torch.zeros(n, dtype=torch.bool)
+    cover[int(cu[0]):int(cu[-1])] = True
+    for norm in (0.0, 777.0):
+        kw = dict(mode=mode, eps_lo=0.2, eps_hi=0.28, beta=0.03, normalizer=norm)
+        loss, grad, tl = flp.logp_grpo_loss(*_dev(lp, old, adv), ref_logp=_dev(ref)[0], active_mask=_dev(mask)[0],
+                                            cu_seqlens=_dev(cu)[0], token_loss=True, **kw)
+        want_l, want_g = oracle.grpo_loss(lp.double().numpy(), old.double().numpy(), adv.double().numpy(),
+                                          ref_logp=ref.double().numpy(), mask=mask.numpy(), cu_seqlens=cu.numpy(),
+                                          **kw)
+        got_g = grad.double().cpu().numpy()
+        assert abs(loss.item() - want_l) <= 1e-5 * abs(want_l) + 1e-7, (norm, loss.item(), want_l)
+        assert np.max(np.abs(got_g - want_g)) <= 1e-5 * np.max(np.abs(want_g)), norm
+        out = ~cover.numpy()
+        assert np.all(got_g[out] == 0) and torch.all(tl.cpu()[~cover] == 0)
+
+
+def test_grpo_one_long_sequence_mean_of_means():
+    """One sequence of 300000 tokens given by cu_seqlens (its 1172 chunk
+    pieces folded by one warp) equals the whole-batch form."""
+    n = 300000
+    lp, old, ref, adv, mask, _ = _case(n, 23)
+    cu = torch.tensor([0, n], dtype=torch.int64)
+    kw = dict(mode="seq_mean_token_mean", beta=0.01)
+    a = flp.logp_grpo_loss(*_dev(lp, old, adv), ref_logp=_dev(ref)[0], active_mask=_dev(mask)[0],
+                           cu_seqlens=_dev(cu)[0], **kw)
+    b = flp.logp_grpo_loss(*_dev(lp, old, adv), ref_logp=_dev(ref)[0], active_mask=_dev(mask)[0], **kw)
+    want_l, want_g = oracle.grpo_loss(lp.double().numpy(), old.double().numpy(), adv.double().numpy(),
+                                      ref_logp=ref.double().numpy(), mask=mask.numpy(), **kw)
+    for loss, grad in (a, b):
+        assert abs(loss.item() - want_l) <= 1e-5 * abs(want_l) + 1e-7
+        assert np.max(np.abs(grad.double().cpu().numpy() - want_g)) <= 1e-5 * np.max(np.abs(want_g))
+
+
+def test_grpo_first_pass_weight_equals_scale_pass():
+    """A normaliser equal to the active-token count makes the weight known up
+    front (applied by the first pass, no scale pass): loss and gradient are
+    bitwise those of the two-step form that derives the count on the device."""
+    n = 100000
+    lp, old, ref, adv, mask, cu = _case(n, 24, nseq=333)
+    d = float(int(mask.sum()))
+    for mode, den in (("token_mean", d), ("seq_mean_token_sum", None)):
+        cnt = d
+        if den is None:   # the number of sequences with an active token
+            cnt = float(sum(int(mask[int(cu[s]):int(cu[s + 1])].sum()) > 0 for s in range(333)))
+        kw = dict(ref_logp=_dev(ref)[0], active_mask=_dev(mask)[0], cu_seqlens=_dev(cu)[0], mode=mode, beta=0.02)
+        a = flp.logp_grpo_loss(*_dev(lp, old, adv), **kw)
+        b = flp.logp_grpo_loss(*_dev(lp, old, adv), normalizer=cnt, **kw)
+        assert torch.equal(a[0].view(torch.int32), b[0].view(torch.int32)), mode
+        assert torch.equal(a[1].view(torch.int32), b[1].view(torch.int32)), mode
+
+
+def test_grpo_unaligned_arrays_bitwise_equal():
+    """Arrays that start 4 bytes past a 16-byte boundary take the scalar-access
+    variant of the token passes; it computes the same tokens in the same
+    order, so loss, gradient and token loss are bitwise those of aligned
+    copies."""
+    n = 70001
+    lp, old, ref, adv, mask, cu = _case(n, 25, nseq=97)
+    big = [torch.empty(n + 1, dtype=t.dtype, device=DEV) for t in (lp, old, ref, adv, mask)]
+    views = []
+    for b, t in zip(big, (lp, old, ref, adv, mask)):
+        b[1:].copy_(t)
+        views.append(b[1:])
+    for mode in MODES:
+        kw = dict(cu_seqlens=_dev(cu)[0], mode=mode, beta=0.05, token_loss=True)
+        a = flp.logp_grpo_loss(*_dev(lp, old, adv), ref_logp=_dev(ref)[0], active_mask=_dev(mask)[0], **kw)
+        b = flp.logp_grpo_loss(views[0], views[1], views[3], ref_logp=views[2], active_mask=views[4], **kw)
+        assert views[0].data_ptr() % 16 == 4
+        for u, v in zip(a, b):
+            assert torch.equal(u.view(torch.int32), v.view(torch.int32)), mode

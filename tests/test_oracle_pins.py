@@ -633,6 +633,27 @@ def test_grpo_reduction_invariants():
     assert abs(ln - la / 4) < 1e-15 and np.allclose(gn, ga / 4, rtol=1e-14, atol=0)
 
 
+def test_grpo_tokens_outside_sequences_are_inactive():
+    """Sequences covering [3, 9) of 12 tokens: the loss equals the loss of the
+    covered slice alone, the uncovered tokens' gradients are exactly 0 (the
+    same as masking them out)."""
+    rng = np.random.default_rng(33)
+    lp, old, ref, adv = _grpo_case(rng, n=12)
+    for mode in ("token_mean", "seq_mean_token_mean", "seq_mean_token_sum"):
+        kw = dict(ref_logp=ref, beta=0.1, mode=mode)
+        lo_, g = oracle.grpo_loss(lp, old, adv, cu_seqlens=np.array([3, 5, 9]), **kw)
+        kw_s = dict(kw, ref_logp=ref[3:9])
+        ls, gs = oracle.grpo_loss(lp[3:9], old[3:9], adv[3:9], cu_seqlens=np.array([0, 2, 6]), **kw_s)
+        assert abs(lo_ - ls) < 1e-15 and np.array_equal(g[3:9], gs)
+        assert np.all(g[:3] == 0) and np.all(g[9:] == 0)
+        mask = np.zeros(12, np.uint8)
+        mask[3:9] = 1
+        # masking [0, 3) and [9, 12) inside sequences [0, 5), [5, 12) leaves the
+        # same active tokens per sequence: the same loss and gradient
+        lm, gm = oracle.grpo_loss(lp, old, adv, mask=mask, cu_seqlens=np.array([0, 5, 12]), **kw)
+        assert abs(lm - lo_) < 1e-15 and np.array_equal(gm, g)
+
+
 # ---- fused LM head + logp (linear_logp) -------------------------------------
 
 def _bf16_of(a):
