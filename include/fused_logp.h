@@ -385,24 +385,25 @@ flp_status fused_linear_logp_forward_noalloc(const void* hidden, int64_t n, int6
  *   token_loss [n] FP32 out or NULL: l per token (0 when inactive).
  *   workspace  device scratch of logp_grpo_loss_workspace_size(n, num_seqs)
  *              bytes (16-byte aligned), caller-owned, no initial contents
- *              needed: 32 bytes of normaliser words, 4 KB of the fold's
+ *              needed: 32 bytes of normaliser words, 32 KB for the fold's
  *              partials, a two-float sum and a count per 256-token chunk,
- *              and with sequences the same per (sequence,
- *              256-token chunk) piece slot (num_seqs + ceil(n / 256) slots),
- *              a two-float mean and a count per sequence and a sequence
- *              index per chunk; rounded up to 256 bytes.  One workspace serves one call at a time.
+ *              and with sequences the same per (sequence, chunk) piece slot
+ *              (num_seqs + ceil(n / 256) slots), a count per sequence and a
+ *              sequence index per chunk; rounded up to 256 bytes.  One
+ *              workspace serves one call at a time.
  * Tokens outside every sequence (before cu_seqlens[0] or from
  * cu_seqlens[num_seqs] on) are inactive: l = 0, grad 0.  cu_seqlens must be
  * non-decreasing; for one that is not, the result is unspecified, but every
  * access stays inside the arrays.
  * Deterministic: the batch is cut into fixed 256-token chunks (one warp
  * each) whatever the sequence lengths; each sequence's sums are a fold of its
- * chunk pieces in a fixed order, and the fold of the chunk totals has a fixed
- * shape (128 shares, then the shares in order); the weights are applied last
- * (by the first pass when normalizer > 0 makes the weight uniform).  Sums are
- * compensated two-float sums in FP32.  The result does not depend on the
- * grid or on timing.  With logp == old_logp the ratio is exactly 1 and
- * grad = -A times the weight (the KL = 0 identity of PR 5).
+ * chunk pieces in a fixed order, and the fold of the chunk totals has a shape
+ * fixed by the sequence count (G shares, then the shares in order); the
+ * weights are applied last (by the first pass when normalizer > 0 makes the
+ * weight uniform).  Sums are plain FP32 within a 256-token chunk and
+ * compensated two-float sums in FP32 from there on.  The result does not
+ * depend on the grid or on timing.  With logp == old_logp the ratio is
+ * exactly 1 and grad = -A times the weight (the KL = 0 identity of PR 5).
  * Errors: FLP_EINVAL for a bad mode, eps_lo outside [0, 1), a negative or
  * non-finite eps_hi, beta or normalizer, a sequence mode without sequences,
  * or num_seqs >= 2^31 - 1.

@@ -509,15 +509,36 @@ flp_status linear_merge_launch(int dev, const float* ws, int64_t n, int64_t v_to
     return check_launch("linear logp merge");
 }
 
-// GRPO workspace: 32 bytes of normaliser words and the fold's ticket, the
-// fold's per-CTA partials (32 bytes each), per 256-token chunk a two-float
-// sum and a count, and with sequences per (sequence, chunk) piece
-// slot the same, per sequence a two-float mean and a count, and per 256-token
-// chunk its first sequence; rounded up to 256 bytes.
+// Launches kern<<<grid, block, 0, s>>>(args...) with programmatic stream
+// serialization: the kernel may start while the previous work on s runs and
+// waits for it with griddepcontrol.wait.
+template <class... Args>
+flp_status launch_dependent(const char* what, void (*kern)(Args...), int grid, int block, cudaStream_t s,
+                            Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)block);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+    if (e != cudaSuccess) return fail(FLP_ECUDA, "%s launch: %s", what, cudaGetErrorString(e));
+    return ok();
+}
+
+// GRPO workspace: 32 bytes of normaliser words and the fold's ticket, room
+// for the fold's per-CTA partials (32 bytes each, up to 1024 CTAs), per
+// 256-token chunk a two-float sum and a count, and with sequences per
+// (sequence, chunk) piece slot the same, per sequence a count and per chunk
+// its first sequence; rounded up to 256 bytes.
 int64_t grpo_workspace_bytes(int64_t n, int64_t nseq) {
     const int64_t nchunks = ceil_div(n, flp::kGrpoChunk);
-    const int64_t seq_part = nseq > 0 ? 16 * (nseq + nchunks) + 16 * nseq + 8 * nchunks : 0;
-    return ceil_div(32 + 32 * flp::kGrpoReduceCtas + 16 * nchunks + seq_part, 256) * 256;
+    const int64_t seq_part = nseq > 0 ? 16 * (nseq + nchunks) + 8 * nseq + 8 * nchunks : 0;
+    return ceil_div(32 + 32 * flp::kGrpoFoldMaxCtas + 16 * nchunks + seq_part, 256) * 256;
 }
 
 }  // namespace
@@ -1098,15 +1119,14 @@ flp_status logp_grpo_loss(const float* logp, const float* old_logp, const float*
     wk.wt = reinterpret_cast<float*>(base + 16);
     wk.ticket = reinterpret_cast<unsigned*>(base + 20);
     wk.part_t = reinterpret_cast<flp::FF*>(base + 32);
-    wk.part_q = wk.part_t + flp::kGrpoReduceCtas;
-    wk.part_c = reinterpret_cast<int64_t*>(wk.part_q + flp::kGrpoReduceCtas);
-    wk.part_a = wk.part_c + flp::kGrpoReduceCtas;
-    wk.chunk_sum = reinterpret_cast<flp::FF*>(wk.part_a + flp::kGrpoReduceCtas);
+    wk.part_q = wk.part_t + flp::kGrpoFoldMaxCtas;
+    wk.part_c = reinterpret_cast<int64_t*>(wk.part_q + flp::kGrpoFoldMaxCtas);
+    wk.part_a = wk.part_c + flp::kGrpoFoldMaxCtas;
+    wk.chunk_sum = reinterpret_cast<flp::FF*>(wk.part_a + flp::kGrpoFoldMaxCtas);
     wk.chunk_cnt = reinterpret_cast<int64_t*>(wk.chunk_sum + nchunks);
     wk.piece = reinterpret_cast<flp::FF*>(wk.chunk_cnt + nchunks);
     wk.piece_cnt = reinterpret_cast<int64_t*>(wk.piece + slots);
-    wk.seg_mean = reinterpret_cast<flp::FF*>(wk.piece_cnt + slots);
-    wk.seg_cnt = reinterpret_cast<int64_t*>(wk.seg_mean + (nseq > 0 ? nseq : 0));
+    wk.seg_cnt = wk.piece_cnt + slots;
     wk.chunk_first = wk.seg_cnt + (nseq > 0 ? nseq : 0);
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int sms = sm_count(dev);
@@ -1123,22 +1143,21 @@ flp_status logp_grpo_loss(const float* logp, const float* old_logp, const float*
         else
             flp::k_grpo_terms<false><<<tok_grid, flp::kGrpoPassThreads, 0, s>>>(a, wk);
         if ((st = check_launch("grpo terms")) != FLP_OK) return st;
-        if (cu_seqlens && mode != FLP_GRPO_TOKEN_MEAN && nseq > 0) {
-            const int64_t ctas = ceil_div(nseq, flp::kGrpoPassThreads);
-            flp::k_grpo_segments<<<(int)(ctas < cap ? ctas : cap), flp::kGrpoPassThreads, 0, s>>>(a, wk);
-            if ((st = check_launch("grpo segments")) != FLP_OK) return st;
-        }
     }
-    // the fold's first level has a fixed CTA count (its order depends on it);
-    // with no tokens there is nothing to fold and one CTA writes the result
-    flp::k_grpo_reduce<<<n > 0 ? flp::kGrpoReduceCtas : 1, flp::kGrpoReduceThreads, 0, s>>>(a, wk);
-    if ((st = check_launch("grpo reduce")) != FLP_OK) return st;
+    // the fold's first level: a CTA count fixed by the sequence count (its
+    // order depends on it); with no tokens one CTA writes the result
+    int64_t fold_ctas = ceil_div(nseq, 256);
+    fold_ctas = fold_ctas < flp::kGrpoFoldMinCtas ? flp::kGrpoFoldMinCtas
+                                                   : (fold_ctas > flp::kGrpoFoldMaxCtas ? flp::kGrpoFoldMaxCtas : fold_ctas);
+    // the fold and the scale pass overlap their launch with the predecessor
+    // (programmatic dependent launch; they wait for it on the device)
+    if ((st = launch_dependent("grpo reduce", flp::k_grpo_reduce, n > 0 ? (int)fold_ctas : 1,
+                               flp::kGrpoReduceThreads, s, a, wk)) != FLP_OK)
+        return st;
     if (n > 0 && prescale == 0.f) {
-        if (vec)
-            flp::k_grpo_scale<true><<<tok_grid, flp::kGrpoPassThreads, 0, s>>>(a, wk);
-        else
-            flp::k_grpo_scale<false><<<tok_grid, flp::kGrpoPassThreads, 0, s>>>(a, wk);
-        if ((st = check_launch("grpo scale")) != FLP_OK) return st;
+        if ((st = launch_dependent("grpo scale", vec ? flp::k_grpo_scale<true> : flp::k_grpo_scale<false>,
+                                   tok_grid, flp::kGrpoPassThreads, s, a, wk)) != FLP_OK)
+            return st;
     }
     return ok();
 }

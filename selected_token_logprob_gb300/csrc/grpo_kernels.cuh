@@ -26,18 +26,20 @@
 //      meets later chunks).  Each token's unnormalised gradient (or, when
 //      the weight is uniform and known up front, the final one) and loss are
 //      written, with the chunk's loss sum, active count and first sequence;
-//   2. k_grpo_segments (sequence normalisers): each sequence's pieces are
-//      folded into its active count and mean;
-//   3. k_grpo_reduce: 128 CTAs each fold a fixed share of the chunk totals
-//      and of the sequences; the CTA that finishes last folds the 128
-//      partials in order into the loss and the weight;
-//   4. k_grpo_scale (when the weight was not known up front): the chunks, in
+//   2. k_grpo_reduce: G CTAs (G fixed by the sequence count) each fold a
+//      fixed share of the chunk totals and of the sequences (each sequence's
+//      pieces give its active count and mean); the CTA that finishes last
+//      folds the G partials in order into the loss and the weight;
+//   3. k_grpo_scale (when the weight was not known up front): the chunks, in
 //      reverse order (the gradients written last are the likeliest still in
 //      L2), multiply each token's gradient by its sequence's weight.
-// Sums are two-float (hi + lo) compensated sums in FP32 (Knuth's TwoSum per
-// addition; the pair carries about 44 significant bits): the FP64 unit of
-// this GPU is far too slow to accumulate per token.  Token counts are
-// integers.  Every fold has an order fixed by the token positions and the
+// Within a 256-token chunk the sums are plain FP32 (each lane's 8 tokens in
+// order, then the xor butterfly: an error of at most about 12 u times the
+// chunk's sum of |l|); from the chunk level up they are two-float (hi + lo)
+// compensated sums in FP32 (Knuth's TwoSum per addition; the pair carries
+// about 44 significant bits), so the error does not grow with the batch: the
+// FP64 unit of this GPU is far too slow to accumulate per token.  Token
+// counts are integers.  Every fold has an order fixed by the token positions and the
 // sequence layout, never by the grid or by timing.
 #pragma once
 
@@ -107,9 +109,12 @@ __device__ __forceinline__ int64_t warp_sum_i64(int64_t v) {
     return v;
 }
 
-constexpr int kGrpoReduceCtas = 128;     // first level of the fold: fixed, so the order is too
+// The fold's first level has G CTAs, G a function of the sequence count
+// only (so the fold order is fixed by the layout): about 256 sequences per
+// CTA, at least 256 and at most 1024 CTAs.
+constexpr int kGrpoFoldMinCtas = 256;
+constexpr int kGrpoFoldMaxCtas = 1024;
 constexpr int kGrpoReduceThreads = 256;
-static_assert(kGrpoReduceCtas <= kGrpoReduceThreads, "the last CTA takes one partial per thread");
 
 // e^x as 2^(x log2 e), the power of two from the special-function unit
 // (ex2.approx, flushing subnormal results to 0): within a few ulp for
@@ -120,7 +125,7 @@ struct GrpoWork {
     double* den;          // [2]: the normaliser, the number of active tokens
     float* wt;            // [1]: the uniform weight (token mean, sequence mean of sums, or one sequence)
     unsigned* ticket;     // [1]: CTAs of the fold that are done (zeroed by pass 1, reset by the last CTA)
-    FF* part_t;           // [kGrpoReduceCtas]: per fold CTA, loss sum
+    FF* part_t;           // [kGrpoFoldMaxCtas]: per fold CTA, loss sum
     FF* part_q;           //   sum of sequence means
     int64_t* part_c;      //   active tokens
     int64_t* part_a;      //   sequences with an active token
@@ -128,7 +133,6 @@ struct GrpoWork {
     int64_t* chunk_cnt;   // [nchunks]: its active tokens
     FF* piece;            // [nseq + nchunks]: loss sum of sequence s within chunk w, at s + w
     int64_t* piece_cnt;
-    FF* seg_mean;         // [nseq]: mean loss of each sequence (mode 1)
     int64_t* seg_cnt;     // [nseq]: active tokens of each sequence
     int64_t* chunk_first; // [nchunks]: the first sequence that may meet each chunk
 };
@@ -209,34 +213,83 @@ __device__ __forceinline__ void grpo_runs(const GrpoArgs& p, GrpoRuns r, int64_t
     }
 }
 
+// Programmatic dependent launch: the fold and the scale pass are launched
+// while their predecessor runs and wait here (griddepcontrol.wait returns
+// once the previous grid has completed and its memory is visible; without
+// the launch attribute it returns at once).  A predecessor lets them launch
+// as soon as each of its CTAs has started.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+// L2 eviction policies (createpolicy): inputs are streamed once and leave
+// L2 first; unscaled gradients that the scale pass re-reads stay longest.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t pol;
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint64_t l2_evict_last() {
+    uint64_t pol;
+    asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ float4 ld_f4_hint(const float* p, uint64_t pol) {
+    float4 v;
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+        : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+        : "l"(p), "l"(pol));
+    return v;
+}
+__device__ __forceinline__ float4 ld_f4_hint_rw(const float* p, uint64_t pol) {   // memory this kernel writes
+    float4 v;
+    asm volatile("ld.global.L1::no_allocate.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p), "l"(pol)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_f4_hint(float* p, float4 v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(v.x), "f"(v.y),
+                 "f"(v.z), "f"(v.w), "l"(pol)
+                 : "memory");
+}
+__device__ __forceinline__ uint32_t ld_u32_hint(const void* p, uint64_t pol) {
+    uint32_t v;
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.u32 %0, [%1], %2;" : "=r"(v) : "l"(p), "l"(pol));
+    return v;
+}
+
 // Token layout of a chunk: lane L holds tokens u = 128 i + 4 L + e (i < 2,
 // e < 4) at index q = 4 i + e, so each 16-byte access of the warp covers 512
 // contiguous bytes.  kVec: the arrays are 16-byte aligned (the mask 4-byte),
 // whole groups of 4 use vector accesses; otherwise every access is scalar.
-template <bool kVec>
-__device__ __forceinline__ void grpo_ld8(const float* base, int lane, int nvalid, float (&v)[kGrpoLaneTokens]) {
+// kRw: the array is written by the same kernel (no read-only path).
+template <bool kVec, bool kRw = false>
+__device__ __forceinline__ void grpo_ld8(const float* base, int lane, int nvalid, float (&v)[kGrpoLaneTokens],
+                                         uint64_t pol) {
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
         const int u = 128 * i + 4 * lane;
         if (kVec && u + 4 <= nvalid) {
-            const float4 x = __ldg(reinterpret_cast<const float4*>(base + u));
+            const float4 x = kRw ? ld_f4_hint_rw(base + u, pol) : ld_f4_hint(base + u, pol);
             v[4 * i] = x.x;
             v[4 * i + 1] = x.y;
             v[4 * i + 2] = x.z;
             v[4 * i + 3] = x.w;
         } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) v[4 * i + e] = u + e < nvalid ? __ldg(base + u + e) : 0.f;
+            for (int e = 0; e < 4; ++e) v[4 * i + e] = u + e < nvalid ? (kRw ? base[u + e] : __ldg(base + u + e)) : 0.f;
         }
     }
 }
 template <bool kVec>
-__device__ __forceinline__ void grpo_st8(float* base, int lane, int nvalid, const float (&v)[kGrpoLaneTokens]) {
+__device__ __forceinline__ void grpo_st8(float* base, int lane, int nvalid, const float (&v)[kGrpoLaneTokens],
+                                         uint64_t pol) {
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
         const int u = 128 * i + 4 * lane;
         if (kVec && u + 4 <= nvalid) {
-            *reinterpret_cast<float4*>(base + u) = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            st_f4_hint(base + u, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]), pol);
         } else {
 #pragma unroll
             for (int e = 0; e < 4; ++e)
@@ -246,7 +299,7 @@ __device__ __forceinline__ void grpo_st8(float* base, int lane, int nvalid, cons
 }
 // Bit q set: token q of the lane exists (u < nvalid) and its mask byte is nonzero.
 template <bool kVec>
-__device__ __forceinline__ uint32_t grpo_active8(const uint8_t* mask, int lane, int nvalid) {
+__device__ __forceinline__ uint32_t grpo_active8(const uint8_t* mask, int lane, int nvalid, uint64_t pol) {
     uint32_t act = 0;
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
@@ -257,7 +310,7 @@ __device__ __forceinline__ uint32_t grpo_active8(const uint8_t* mask, int lane, 
                 if (u + e < nvalid) act |= 1u << (4 * i + e);
         } else if (kVec && u + 4 <= nvalid) {
             // bytes != 0 -> 1 in each byte, then the four bits gathered by a multiply
-            const uint32_t m = __vcmpne4(__ldg(reinterpret_cast<const unsigned int*>(mask + u)), 0u) & 0x01010101u;
+            const uint32_t m = __vcmpne4(ld_u32_hint(mask + u, pol), 0u) & 0x01010101u;
             act |= ((m * 0x01020408u) >> 24) << (4 * i);
         } else {
 #pragma unroll
@@ -284,16 +337,20 @@ __global__ void __launch_bounds__(kGrpoPassThreads, 4) k_grpo_terms(GrpoArgs p, 
     const int64_t nchunks = grpo_chunks(p.n);
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const float clo = 1.f - p.eps_lo, chi = 1.f + p.eps_hi;
+    griddep_launch_dependents();
+    const uint64_t in_pol = l2_evict_first();
+    // the scale pass re-reads the gradients: keep them in L2 (else they are final)
+    const uint64_t g_pol = p.prescale > 0.f ? l2_evict_first() : l2_evict_last();
     if (blockIdx.x == 0 && threadIdx.x == 0) *wk.ticket = 0u;
     for (int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < nchunks; w += nwarps) {
         const int64_t c0 = w * kGrpoChunk;
         const int nv = (int)(p.n - c0 < kGrpoChunk ? p.n - c0 : kGrpoChunk);   // tokens in the chunk
         float lp[kGrpoLaneTokens], od[kGrpoLaneTokens], av[kGrpoLaneTokens], rf[kGrpoLaneTokens];
-        grpo_ld8<kVec>(p.logp + c0, lane, nv, lp);
-        grpo_ld8<kVec>(p.old_logp + c0, lane, nv, od);
-        grpo_ld8<kVec>(p.adv + c0, lane, nv, av);
-        if (p.ref_logp) grpo_ld8<kVec>(p.ref_logp + c0, lane, nv, rf);
-        const uint32_t act = grpo_active8<kVec>(p.mask ? p.mask + c0 : nullptr, lane, nv);
+        grpo_ld8<kVec>(p.logp + c0, lane, nv, lp, in_pol);
+        grpo_ld8<kVec>(p.old_logp + c0, lane, nv, od, in_pol);
+        grpo_ld8<kVec>(p.adv + c0, lane, nv, av, in_pol);
+        if (p.ref_logp) grpo_ld8<kVec>(p.ref_logp + c0, lane, nv, rf, in_pol);
+        const uint32_t act = grpo_active8<kVec>(p.mask ? p.mask + c0 : nullptr, lane, nv, in_pol);
         const GrpoRuns runs = grpo_runs_begin(p, c0, lane);   // overlaps the loads above
         if (p.cu && p.mode == 1 && lane == 0) wk.chunk_first[w] = runs.s;
         float l[kGrpoLaneTokens], dl[kGrpoLaneTokens];
@@ -320,22 +377,25 @@ __global__ void __launch_bounds__(kGrpoPassThreads, 4) k_grpo_terms(GrpoArgs p, 
         int64_t tcnt = 0;
         uint32_t inseq = 0;
         grpo_runs<false>(p, runs, c0, nv, lane, nullptr, [&](int64_t s, int ua, int ub, int64_t) {
-            FF rs{0.f, 0.f};
+            // within the chunk, plain FP32: the lane's tokens in order, then the
+            // xor butterfly (lane 0 holds the result)
+            float rs = 0.f;
             uint32_t in;
             if (ua == 0 && ub == nv) {   // the whole chunk: no membership tests
                 in = 0xffu;
 #pragma unroll
-                for (int q = 0; q < kGrpoLaneTokens; ++q) rs = ff_add(rs, l[q]);
+                for (int q = 0; q < kGrpoLaneTokens; ++q) rs = __fadd_rn(rs, l[q]);
             } else {
                 in = grpo_in8(lane, ua, ub);
 #pragma unroll
-                for (int q = 0; q < kGrpoLaneTokens; ++q) rs = ff_add(rs, ((in >> q) & 1u) ? l[q] : 0.f);
+                for (int q = 0; q < kGrpoLaneTokens; ++q) rs = __fadd_rn(rs, ((in >> q) & 1u) ? l[q] : 0.f);
             }
             inseq |= in;
-            rs = ff_warp_sum(rs);
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) rs = __fadd_rn(rs, __shfl_xor_sync(0xffffffffu, rs, off));
             const int cnt = __reduce_add_sync(0xffffffffu, __popc(in & act));
             if (p.cu && p.mode != 0 && lane == 0) {
-                wk.piece[s + w] = rs;
+                wk.piece[s + w] = FF{rs, 0.f};
                 wk.piece_cnt[s + w] = cnt;
             }
             tot = ff_add(tot, rs);
@@ -353,8 +413,8 @@ __global__ void __launch_bounds__(kGrpoPassThreads, 4) k_grpo_terms(GrpoArgs p, 
 #pragma unroll
             for (int q = 0; q < kGrpoLaneTokens; ++q) dl[q] = __fmul_rn(dl[q], p.prescale);
         }
-        grpo_st8<kVec>(p.grad + c0, lane, nv, dl);
-        if (p.token_loss) grpo_st8<kVec>(p.token_loss + c0, lane, nv, l);
+        grpo_st8<kVec>(p.grad + c0, lane, nv, dl, g_pol);
+        if (p.token_loss) grpo_st8<kVec>(p.token_loss + c0, lane, nv, l, in_pol);
         if (lane == 0) {
             wk.chunk_sum[w] = tot;
             wk.chunk_cnt[w] = tcnt;
@@ -397,81 +457,16 @@ __device__ __forceinline__ FF cta_fold(FF v, int64_t& c, FF* sh_v, int64_t* sh_c
 
 constexpr int64_t kGrpoLongPieces = 64;   // sequences with more pieces are folded by a whole warp
 
-// Per sequence s (sequence normalisers): its active-token count and, for
-// mode 1, its mean, from its chunk pieces (chunks floor(a / 256) ..
-// floor((b - 1) / 256), at slots s + chunk).  One lane per sequence folds up
-// to 64 pieces in piece order; a longer sequence is folded by its whole warp
-// (lane-strided, fixed butterfly).  Which of the two a sequence takes depends
-// only on its length, so the result does not depend on the grid.
-__global__ void __launch_bounds__(kGrpoPassThreads) k_grpo_segments(GrpoArgs p, GrpoWork wk) {
-    const int lane = threadIdx.x & 31;
-    const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t base = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31); base < p.nseq; base += nthreads) {
-        const int64_t s = base + lane;
-        int64_t j0 = 0, j1 = -1;
-        if (s < p.nseq) {
-            const int64_t a = grpo_cu(p, s), e = grpo_cu(p, s + 1);
-            if (e > a) {
-                j0 = s + a / kGrpoChunk;
-                j1 = s + (e - 1) / kGrpoChunk;
-            }
-        }
-        const bool is_long = j1 - j0 + 1 > kGrpoLongPieces;
-        FF sum{0.f, 0.f};
-        int64_t cnt = 0;
-        if (!is_long) {
-            int64_t j = j0;
-            for (; j + 3 <= j1; j += 4) {   // four loads in flight, added in order
-                FF v[4];
-                int64_t c[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    v[u] = wk.piece[j + u];
-                    c[u] = wk.piece_cnt[j + u];
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    sum = ff_add(sum, v[u]);
-                    cnt += c[u];
-                }
-            }
-            for (; j <= j1; ++j) {
-                sum = ff_add(sum, wk.piece[j]);
-                cnt += wk.piece_cnt[j];
-            }
-        }
-        // the warp's long sequences, one at a time in lane order
-        for (uint32_t m = __ballot_sync(0xffffffffu, is_long); m != 0; m &= m - 1) {
-            const int src = __ffs(m) - 1;
-            const int64_t k0 = __shfl_sync(0xffffffffu, j0, src), k1 = __shfl_sync(0xffffffffu, j1, src);
-            FF ws{0.f, 0.f};
-            int64_t wc = 0;
-            for (int64_t j = k0 + lane; j <= k1; j += 32) {
-                ws = ff_add(ws, wk.piece[j]);
-                wc += wk.piece_cnt[j];
-            }
-            ws = ff_warp_sum(ws);
-            wc = warp_sum_i64(wc);
-            const FF w0{__shfl_sync(0xffffffffu, ws.hi, 0), __shfl_sync(0xffffffffu, ws.lo, 0)};
-            wc = __shfl_sync(0xffffffffu, wc, 0);
-            if (lane == src) {
-                sum = w0;
-                cnt = wc;
-            }
-        }
-        if (s < p.nseq) {
-            wk.seg_cnt[s] = cnt;
-            if (p.mode == 1) wk.seg_mean[s] = cnt > 0 ? ff_div_count(sum, cnt) : FF{0.f, 0.f};
-        }
-    }
-}
-
-// The fold of the loss and the normaliser.  kGrpoReduceCtas CTAs (1 when
-// n == 0): CTA b takes the b-th equal share of the chunk totals and,
-// for the sequence normalisers, of the sequences' counts and means.  Each
-// CTA writes its partials; the CTA that finishes last (an atomic ticket, no
-// waiting) folds the partials in CTA order and writes the loss, the
-// normaliser and the uniform weight.
+// The fold of the loss and the normaliser, G CTAs (1 when n == 0).  CTA b
+// takes the b-th equal share of the chunk totals and, for the sequence
+// normalisers, of the sequences: one lane per sequence folds up to 64 of its
+// chunk pieces (chunks floor(a / 256) .. floor((b - 1) / 256), at slots
+// s + chunk) in piece order; a longer sequence is folded by its whole warp
+// (lane-strided, fixed butterfly) -- which of the two depends only on the
+// sequence -- giving its active count (kept for the scale pass) and mean.
+// Each CTA writes its partials; the CTA that finishes last (an atomic
+// ticket, no waiting) folds the partials in CTA order and writes the loss,
+// the normaliser and the uniform weight.
 __global__ void __launch_bounds__(kGrpoReduceThreads) k_grpo_reduce(GrpoArgs p, GrpoWork wk) {
     constexpr int kW = kGrpoReduceThreads / 32;
     __shared__ FF sh_v[kW];
@@ -481,6 +476,16 @@ __global__ void __launch_bounds__(kGrpoReduceThreads) k_grpo_reduce(GrpoArgs p, 
     const int G = gridDim.x, b = blockIdx.x;
     const int64_t nchunks = grpo_chunks(p.n);
     const bool seqs = p.cu != nullptr && p.mode != 0 && p.n > 0;
+    griddep_launch_dependents();
+    // cu_seqlens is the caller's: its first bounds are read before the wait
+    const int64_t qs = seqs ? (p.nseq + G - 1) / G : 0;
+    const int64_t s0 = b * qs, s1 = seqs ? (s0 + qs < p.nseq ? s0 + qs : p.nseq) : 0;
+    int64_t a_first = 0, e_first = 0;
+    if (s0 + 32 * warp + lane < s1) {
+        a_first = grpo_cu(p, s0 + 32 * warp + lane);
+        e_first = grpo_cu(p, s0 + 32 * warp + lane + 1);
+    }
+    griddep_wait();
     // chunk totals [b ps, (b + 1) ps)
     const int64_t ps = (nchunks + G - 1) / G;
     const int64_t k1 = (b + 1) * ps < nchunks ? (b + 1) * ps : nchunks;
@@ -493,13 +498,67 @@ __global__ void __launch_bounds__(kGrpoReduceThreads) k_grpo_reduce(GrpoArgs p, 
     T = cta_fold<kW>(T, C, sh_v, sh_c);
     FF Q{0.f, 0.f};
     int64_t A = 0;
-    if (seqs) {   // the sequences [b qs, (b + 1) qs): counts and means
-        const int64_t qs = (p.nseq + G - 1) / G;
-        const int64_t s1 = (b + 1) * qs < p.nseq ? (b + 1) * qs : p.nseq;
-        for (int64_t s = b * qs + threadIdx.x; s < s1; s += kGrpoReduceThreads) {
-            if (wk.seg_cnt[s] > 0) {
-                ++A;
-                if (p.mode == 1) Q = ff_add(Q, wk.seg_mean[s]);
+    if (seqs) {   // the sequences [s0, s1)
+        for (int64_t base = s0 + 32 * warp; base < s1; base += kGrpoReduceThreads) {   // warp-uniform
+            const int64_t s = base + lane;
+            int64_t j0 = 0, j1 = -1;
+            if (s < s1) {
+                const bool first = base == s0 + 32 * warp;
+                const int64_t a = first ? a_first : grpo_cu(p, s), e = first ? e_first : grpo_cu(p, s + 1);
+                if (e > a) {
+                    j0 = s + a / kGrpoChunk;
+                    j1 = s + (e - 1) / kGrpoChunk;
+                }
+            }
+            const bool is_long = j1 - j0 + 1 > kGrpoLongPieces;
+            FF sum{0.f, 0.f};
+            int64_t cnt = 0;
+            if (!is_long) {
+                int64_t j = j0;
+                for (; j + 3 <= j1; j += 4) {   // four loads in flight, added in order
+                    FF v[4];
+                    int64_t c[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        v[u] = wk.piece[j + u];
+                        c[u] = wk.piece_cnt[j + u];
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        sum = ff_add(sum, v[u]);
+                        cnt += c[u];
+                    }
+                }
+                for (; j <= j1; ++j) {
+                    sum = ff_add(sum, wk.piece[j]);
+                    cnt += wk.piece_cnt[j];
+                }
+            }
+            // the warp's long sequences, one at a time in lane order
+            for (uint32_t m = __ballot_sync(0xffffffffu, is_long); m != 0; m &= m - 1) {
+                const int src = __ffs(m) - 1;
+                const int64_t k0 = __shfl_sync(0xffffffffu, j0, src), kl = __shfl_sync(0xffffffffu, j1, src);
+                FF ws{0.f, 0.f};
+                int64_t wc = 0;
+                for (int64_t j = k0 + lane; j <= kl; j += 32) {
+                    ws = ff_add(ws, wk.piece[j]);
+                    wc += wk.piece_cnt[j];
+                }
+                ws = ff_warp_sum(ws);
+                wc = warp_sum_i64(wc);
+                const FF w0{__shfl_sync(0xffffffffu, ws.hi, 0), __shfl_sync(0xffffffffu, ws.lo, 0)};
+                wc = __shfl_sync(0xffffffffu, wc, 0);
+                if (lane == src) {
+                    sum = w0;
+                    cnt = wc;
+                }
+            }
+            if (s < s1) {
+                wk.seg_cnt[s] = cnt;
+                if (cnt > 0) {
+                    ++A;
+                    if (p.mode == 1) Q = ff_add(Q, ff_div_count(sum, cnt));
+                }
             }
         }
         Q = cta_fold<kW>(Q, A, sh_v, sh_c);
@@ -524,17 +583,17 @@ __global__ void __launch_bounds__(kGrpoReduceThreads) k_grpo_reduce(GrpoArgs p, 
         if (!last) return;
         __threadfence();
     }
-    // the last CTA: thread i takes partial i; the CTA fold combines them (a
-    // fixed butterfly per warp, then warp order)
+    // the last CTA: thread i takes partials i, i + 256, ... in order; the CTA
+    // fold combines them (a fixed butterfly per warp, then warp order)
     FF t{0.f, 0.f}, q{0.f, 0.f};
     int64_t c = 0, a = 0;
-    if ((int)threadIdx.x < G) {
-        const float2 tv = __ldcg(reinterpret_cast<const float2*>(wk.part_t) + threadIdx.x);
-        const float2 qv = __ldcg(reinterpret_cast<const float2*>(wk.part_q) + threadIdx.x);
-        t = FF{tv.x, tv.y};
-        q = FF{qv.x, qv.y};
-        c = __ldcg(reinterpret_cast<const long long*>(wk.part_c) + threadIdx.x);
-        a = __ldcg(reinterpret_cast<const long long*>(wk.part_a) + threadIdx.x);
+    for (int i = threadIdx.x; i < G; i += kGrpoReduceThreads) {
+        const float2 tv = __ldcg(reinterpret_cast<const float2*>(wk.part_t) + i);
+        const float2 qv = __ldcg(reinterpret_cast<const float2*>(wk.part_q) + i);
+        t = ff_add(t, FF{tv.x, tv.y});
+        q = ff_add(q, FF{qv.x, qv.y});
+        c += __ldcg(reinterpret_cast<const long long*>(wk.part_c) + i);
+        a += __ldcg(reinterpret_cast<const long long*>(wk.part_a) + i);
     }
     t = cta_fold<kW>(t, c, sh_v, sh_c);
     q = cta_fold<kW>(q, a, sh_v, sh_c);
@@ -566,21 +625,32 @@ template <bool kVec>
 __global__ void __launch_bounds__(kGrpoPassThreads, 4) k_grpo_scale(GrpoArgs p, GrpoWork wk) {
     const int lane = threadIdx.x & 31;
     const int64_t nchunks = grpo_chunks(p.n);
+    griddep_wait();
     const double den = wk.den[0];
-    if (!(den > 0)) return;   // no active token: every gradient is already 0
+    const bool zero = !(den > 0);   // no active token: the gradients are 0 (rewritten, so that
+                                    // the lines kept in L2 by pass 1 are released)
     const float wu = wk.wt[0];
+    const uint64_t pol = l2_evict_first();
     const bool per_seq = p.mode == 1 && p.cu != nullptr;
     const float denf = (float)den;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    for (int64_t ww = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; ww < nchunks; ww += nwarps) {
+    int64_t ww = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    // the first sequence of the warp's next chunk is fetched one iteration ahead
+    int64_t s_next = per_seq && ww < nchunks ? wk.chunk_first[nchunks - 1 - ww] : 0;
+    for (; ww < nchunks; ww += nwarps) {
         const int64_t w = nchunks - 1 - ww;
+        const int64_t s_cur = s_next;
+        if (per_seq && ww + nwarps < nchunks) s_next = wk.chunk_first[nchunks - 1 - (ww + nwarps)];
         const int64_t c0 = w * kGrpoChunk;
         const int nv = (int)(p.n - c0 < kGrpoChunk ? p.n - c0 : kGrpoChunk);
         float g[kGrpoLaneTokens];
-        grpo_ld8<kVec>(p.grad + c0, lane, nv, g);
-        if (per_seq) {
+        grpo_ld8<kVec, true>(p.grad + c0, lane, nv, g, pol);
+        if (zero) {
+#pragma unroll
+            for (int q = 0; q < kGrpoLaneTokens; ++q) g[q] = 0.f;
+        } else if (per_seq) {
             // the first sequence recorded by pass 1; boundaries and counts in one trip
-            const GrpoRuns runs = grpo_runs_at(p, wk.chunk_first[w], c0, lane, wk.seg_cnt);
+            const GrpoRuns runs = grpo_runs_at(p, s_cur, c0, lane, wk.seg_cnt);
             float wt[kGrpoLaneTokens];
 #pragma unroll
             for (int q = 0; q < kGrpoLaneTokens; ++q) wt[q] = 0.f;
@@ -597,7 +667,7 @@ __global__ void __launch_bounds__(kGrpoPassThreads, 4) k_grpo_scale(GrpoArgs p, 
 #pragma unroll
             for (int q = 0; q < kGrpoLaneTokens; ++q) g[q] = __fmul_rn(g[q], wu);
         }
-        grpo_st8<kVec>(p.grad + c0, lane, nv, g);
+        grpo_st8<kVec>(p.grad + c0, lane, nv, g, pol);
     }
 }
 

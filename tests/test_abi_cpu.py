@@ -273,13 +273,13 @@ def test_linear_shard_host_checks(lib):
 
 def test_grpo_host_checks(lib):
     b = ctypes.c_int64(0)
-    # 32 bytes of normaliser words, 128 fold partials of 32 bytes, 16 per
-    # 256-token chunk, and with S sequences 16 per piece slot (S + chunks), 16
-    # per sequence and 8 per chunk; rounded up to 256:
-    # 32 + 4096 + 16*128 = 6176 -> 6400;  + 16*228 + 16*100 + 8*128 -> 12544
-    assert lib.logp_grpo_loss_workspace_size(32768, 0, ctypes.byref(b)) == 0 and b.value == 6400
-    assert lib.logp_grpo_loss_workspace_size(32768, 100, ctypes.byref(b)) == 0 and b.value == 12544
-    assert lib.logp_grpo_loss_workspace_size(0, 0, ctypes.byref(b)) == 0 and b.value == 4352
+    # 32 bytes of normaliser words, room for 1024 fold partials of 32 bytes,
+    # 16 per 256-token chunk, and with S sequences 16 per piece slot (S +
+    # chunks), 8 per sequence and 8 per chunk; rounded up to 256:
+    # 32 + 32768 + 16*128 = 34848 -> 35072;  + 16*228 + 8*100 + 8*128 -> 40448
+    assert lib.logp_grpo_loss_workspace_size(32768, 0, ctypes.byref(b)) == 0 and b.value == 35072
+    assert lib.logp_grpo_loss_workspace_size(32768, 100, ctypes.byref(b)) == 0 and b.value == 40448
+    assert lib.logp_grpo_loss_workspace_size(0, 0, ctypes.byref(b)) == 0 and b.value == 33024
     assert lib.logp_grpo_loss_workspace_size(-1, 0, ctypes.byref(b)) == EINVAL
 
     def call(mode=0, ws=1 << 20, ws_bytes=1 << 20, n=1000, eps_lo=0.2):

@@ -76,3 +76,35 @@ def test_linear_forward_replays_bitwise():
     graph.replay()
     torch.cuda.synchronize()
     assert torch.equal(_i(logp), _i(want[0])) and torch.equal(_i(lse), _i(want[1]))
+
+
+def test_grpo_loss_replays_bitwise():
+    """The GRPO loss (its fold and scale kernels are launched as programmatic
+    dependents of their predecessors) captured in a graph replays bitwise."""
+    g = torch.Generator().manual_seed(31)
+    n, nseq = 50000, 77
+    lp = -torch.rand(n, generator=g) * 5
+    old = lp + (torch.rand(n, generator=g) - 0.5)
+    adv = torch.randn(n, generator=g)
+    mask = (torch.rand(n, generator=g) > 0.2).to(torch.uint8)
+    cu = torch.cat([torch.zeros(1, dtype=torch.int64),
+                    torch.sort(torch.randint(0, n + 1, (nseq - 1,), generator=g)).values,
+                    torch.full((1,), n, dtype=torch.int64)])
+    lp, old, adv, mask, cu = (t.to(DEV) for t in (lp, old, adv, mask, cu))
+    ws = torch.empty(flp.logp_grpo_loss_workspace_size(n, nseq), dtype=torch.uint8, device=DEV)
+    for mode in ("token_mean", "seq_mean_token_mean"):
+        kw = dict(ref_logp=old, active_mask=mask, cu_seqlens=cu, mode=mode, beta=0.02, workspace=ws)
+        want = flp.logp_grpo_loss(lp, old, adv, **kw)
+        torch.cuda.synchronize()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(graph, stream=s):
+                got = flp.logp_grpo_loss(lp, old, adv, **kw)
+        torch.cuda.current_stream().wait_stream(s)
+        for _ in range(2):
+            graph.replay()
+        torch.cuda.synchronize()
+        for u, v in zip(got, want):
+            assert torch.equal(u.view(torch.int32), v.view(torch.int32)), mode
