@@ -622,7 +622,7 @@ __global__ void __launch_bounds__(kGrpoReduceThreads) k_grpo_reduce(GrpoArgs p, 
 // tokens (formed in FP32: den n_s rounded, then its correctly rounded
 // reciprocal).
 template <bool kVec>
-__global__ void __launch_bounds__(kGrpoPassThreads, 4) k_grpo_scale(GrpoArgs p, GrpoWork wk) {
+__global__ void __launch_bounds__(kGrpoPassThreads, 5) k_grpo_scale(GrpoArgs p, GrpoWork wk) {
     const int lane = threadIdx.x & 31;
     const int64_t nchunks = grpo_chunks(p.n);
     griddep_wait();
@@ -651,18 +651,14 @@ __global__ void __launch_bounds__(kGrpoPassThreads, 4) k_grpo_scale(GrpoArgs p, 
         } else if (per_seq) {
             // the first sequence recorded by pass 1; boundaries and counts in one trip
             const GrpoRuns runs = grpo_runs_at(p, s_cur, c0, lane, wk.seg_cnt);
-            float wt[kGrpoLaneTokens];
-#pragma unroll
-            for (int q = 0; q < kGrpoLaneTokens; ++q) wt[q] = 0.f;
+            // each run's tokens times its weight; tokens in no sequence hold 0 already
             grpo_runs<true>(p, runs, c0, nv, lane, wk.seg_cnt, [&](int64_t, int ua, int ub, int64_t c) {
                 const float ws = c > 0 ? __frcp_rn(__fmul_rn(denf, (float)c)) : 0.f;
-                const uint32_t in = grpo_in8(lane, ua, ub);
+                const uint32_t in = (ua == 0 && ub == nv) ? 0xffu : grpo_in8(lane, ua, ub);
 #pragma unroll
                 for (int q = 0; q < kGrpoLaneTokens; ++q)
-                    if ((in >> q) & 1u) wt[q] = ws;
+                    if ((in >> q) & 1u) g[q] = __fmul_rn(g[q], ws);
             });
-#pragma unroll
-            for (int q = 0; q < kGrpoLaneTokens; ++q) g[q] = __fmul_rn(g[q], wt[q]);
         } else {
 #pragma unroll
             for (int q = 0; q < kGrpoLaneTokens; ++q) g[q] = __fmul_rn(g[q], wu);
