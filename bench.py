@@ -450,16 +450,18 @@ def run_grpo(args):
         return flp.logp_grpo_loss(lp, old, adv, **kw)
 
     stream = torch.cuda.current_stream(dev)
-    w0 = torch.cuda.Event(enable_timing=True)
-    w1 = torch.cuda.Event(enable_timing=True)
-    w0.record(stream)
     for _ in range(args.warmup):
         step()
-    w1.record(stream)
     torch.cuda.synchronize(dev)
     # a call takes well under a millisecond: time at least a second of them so
-    # that the clock sampler (every 200 ms) sees the timed region
-    steps = max(args.steps, int(1.0 / max(w0.elapsed_time(w1) / max(args.warmup, 1) * 1e-3, 1e-6)))
+    # that the clock sampler (every 200 ms) sees the timed region (the count
+    # comes from the wall time of 20 calls, host overhead included)
+    t_probe = time.perf_counter()
+    for _ in range(20):
+        step()
+    torch.cuda.synchronize(dev)
+    per_call = (time.perf_counter() - t_probe) / 20
+    steps = max(args.steps, int(1.0 / max(per_call, 1e-6)))
     sampler = ClockSampler(local)
     with sampler:
         t0 = torch.cuda.Event(enable_timing=True)
