@@ -1131,17 +1131,19 @@ flp_status logp_grpo_loss(const float* logp, const float* old_logp, const float*
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int sms = sm_count(dev);
     if (sms <= 0) return fail(FLP_ECUDA, "cannot read the SM count of device %d", dev);
-    const int64_t cap = (int64_t)sms * 8;
     const int64_t tok_ctas = ceil_div(nchunks, flp::kGrpoPassThreads / 32);
-    const int tok_grid = (int)(tok_ctas < cap ? (tok_ctas < 1 ? 1 : tok_ctas) : cap);
     auto al = [](const void* q, uintptr_t m) { return (reinterpret_cast<uintptr_t>(q) & (m - 1)) == 0; };
     const bool vec = al(logp, 16) && al(old_logp, 16) && al(advantages, 16) && al(grad, 16) && al(ref_logp, 16) &&
                      al(token_loss, 16) && al(active_mask, 4);
     if (n > 0) {
+        // pass 1: one wave (4 CTAs per SM at its 64 registers), each warp a
+        // contiguous range of chunks
+        const int64_t wave = (int64_t)sms * 4;
+        const int terms_grid = (int)(tok_ctas < wave ? (tok_ctas < 1 ? 1 : tok_ctas) : wave);
         if (vec)
-            flp::k_grpo_terms<true><<<tok_grid, flp::kGrpoPassThreads, 0, s>>>(a, wk);
+            flp::k_grpo_terms<true><<<terms_grid, flp::kGrpoPassThreads, 0, s>>>(a, wk);
         else
-            flp::k_grpo_terms<false><<<tok_grid, flp::kGrpoPassThreads, 0, s>>>(a, wk);
+            flp::k_grpo_terms<false><<<terms_grid, flp::kGrpoPassThreads, 0, s>>>(a, wk);
         if ((st = check_launch("grpo terms")) != FLP_OK) return st;
     }
     // the fold's first level: a CTA count fixed by the sequence count (its
@@ -1155,8 +1157,10 @@ flp_status logp_grpo_loss(const float* logp, const float* old_logp, const float*
                                flp::kGrpoReduceThreads, s, a, wk)) != FLP_OK)
         return st;
     if (n > 0 && prescale == 0.f) {
+        const int64_t wave = (int64_t)sms * 5;   // 5 CTAs per SM at its 48 registers
+        const int scale_grid = (int)(tok_ctas < wave ? (tok_ctas < 1 ? 1 : tok_ctas) : wave);
         if ((st = launch_dependent("grpo scale", vec ? flp::k_grpo_scale<true> : flp::k_grpo_scale<false>,
-                                   tok_grid, flp::kGrpoPassThreads, s, a, wk)) != FLP_OK)
+                                   scale_grid, flp::kGrpoPassThreads, s, a, wk)) != FLP_OK)
             return st;
     }
     return ok();

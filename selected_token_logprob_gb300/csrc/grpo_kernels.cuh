@@ -17,10 +17,11 @@
 // The batch is cut into fixed chunks of 256 tokens (one warp each),
 // independent of the sequence layout, so the work per warp is the same
 // whatever the sequence lengths:
-//   1. k_grpo_terms: a warp loads its chunk (8 tokens per lane in two
-//      groups of 4, 16-byte accesses when the arrays allow), finds the
-//      sequences that cross it (a 32-ary search over cu_seqlens, overlapped
-//      with the loads), and for each such run (sequence s within chunk w)
+//   1. k_grpo_terms: each warp takes a contiguous range of chunks; it loads a
+//      chunk (8 tokens per lane in two groups of 4, 16-byte accesses when the
+//      arrays allow) and finds the sequences that cross it (for its first
+//      chunk a 32-ary search over cu_seqlens, later resuming at the last
+//      sequence seen; overlapped with the loads), and for each such run (sequence s within chunk w)
 //      sums l and counts the active tokens; the run's sums go to piece slot
 //      s + w (slots of distinct runs never collide: a later sequence only
 //      meets later chunks).  Each token's unnormalised gradient (or, when
@@ -30,9 +31,8 @@
 //      fixed share of the chunk totals and of the sequences (each sequence's
 //      pieces give its active count and mean); the CTA that finishes last
 //      folds the G partials in order into the loss and the weight;
-//   3. k_grpo_scale (when the weight was not known up front): the chunks, in
-//      reverse order (the gradients written last are the likeliest still in
-//      L2), multiply each token's gradient by its sequence's weight.
+//   3. k_grpo_scale (when the weight was not known up front): each token's
+//      gradient, kept in L2 by pass 1, times its sequence's weight.
 // Within a 256-token chunk the sums are plain FP32 (each lane's 8 tokens in
 // order, then the xor butterfly: an error of at most about 12 u times the
 // chunk's sum of |l|); from the chunk level up they are two-float (hi + lo)
@@ -342,7 +342,12 @@ __global__ void __launch_bounds__(kGrpoPassThreads, 4) k_grpo_terms(GrpoArgs p, 
     // the scale pass re-reads the gradients: keep them in L2 (else they are final)
     const uint64_t g_pol = p.prescale > 0.f ? l2_evict_first() : l2_evict_last();
     if (blockIdx.x == 0 && threadIdx.x == 0) *wk.ticket = 0u;
-    for (int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; w < nchunks; w += nwarps) {
+    // each warp takes a contiguous range of chunks: only its first chunk needs
+    // the search, later ones resume the run walk at the last sequence seen
+    const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t w_end = (gw + 1) * nchunks / nwarps;
+    int64_t s_resume = -1;
+    for (int64_t w = gw * nchunks / nwarps; w < w_end; ++w) {
         const int64_t c0 = w * kGrpoChunk;
         const int nv = (int)(p.n - c0 < kGrpoChunk ? p.n - c0 : kGrpoChunk);   // tokens in the chunk
         float lp[kGrpoLaneTokens], od[kGrpoLaneTokens], av[kGrpoLaneTokens], rf[kGrpoLaneTokens];
@@ -351,7 +356,10 @@ __global__ void __launch_bounds__(kGrpoPassThreads, 4) k_grpo_terms(GrpoArgs p, 
         grpo_ld8<kVec>(p.adv + c0, lane, nv, av, in_pol);
         if (p.ref_logp) grpo_ld8<kVec>(p.ref_logp + c0, lane, nv, rf, in_pol);
         const uint32_t act = grpo_active8<kVec>(p.mask ? p.mask + c0 : nullptr, lane, nv, in_pol);
-        const GrpoRuns runs = grpo_runs_begin(p, c0, lane);   // overlaps the loads above
+        // overlaps the loads above
+        const GrpoRuns runs = (s_resume < 0 || p.cu == nullptr) ? grpo_runs_begin(p, c0, lane)
+                                                                 : grpo_runs_at(p, s_resume, c0, lane, nullptr);
+        int64_t s_last = runs.s;
         if (p.cu && p.mode == 1 && lane == 0) wk.chunk_first[w] = runs.s;
         float l[kGrpoLaneTokens], dl[kGrpoLaneTokens];
 #pragma unroll
@@ -377,6 +385,7 @@ __global__ void __launch_bounds__(kGrpoPassThreads, 4) k_grpo_terms(GrpoArgs p, 
         int64_t tcnt = 0;
         uint32_t inseq = 0;
         grpo_runs<false>(p, runs, c0, nv, lane, nullptr, [&](int64_t s, int ua, int ub, int64_t) {
+            s_last = s;
             // within the chunk, plain FP32: the lane's tokens in order, then the
             // xor butterfly (lane 0 holds the result)
             float rs = 0.f;
@@ -419,6 +428,7 @@ __global__ void __launch_bounds__(kGrpoPassThreads, 4) k_grpo_terms(GrpoArgs p, 
             wk.chunk_sum[w] = tot;
             wk.chunk_cnt[w] = tcnt;
         }
+        s_resume = s_last;   // no later chunk meets an earlier sequence
     }
 }
 
@@ -620,45 +630,44 @@ __global__ void __launch_bounds__(kGrpoReduceThreads) k_grpo_reduce(GrpoArgs p, 
 // Each token's gradient times its weight: 1 / den, or for the sequence mean
 // of token means with sequences 1 / (den n_s), n_s the sequence's active
 // tokens (formed in FP32: den n_s rounded, then its correctly rounded
-// reciprocal).
+// reciprocal).  Each warp takes a contiguous range of chunks (as in pass 1):
+// the range's first sequence was recorded by pass 1, later chunks resume at
+// the last sequence seen.
 template <bool kVec>
 __global__ void __launch_bounds__(kGrpoPassThreads, 5) k_grpo_scale(GrpoArgs p, GrpoWork wk) {
     const int lane = threadIdx.x & 31;
     const int64_t nchunks = grpo_chunks(p.n);
     griddep_wait();
     const double den = wk.den[0];
-    const bool zero = !(den > 0);   // no active token: the gradients are 0 (rewritten, so that
-                                    // the lines kept in L2 by pass 1 are released)
-    const float wu = wk.wt[0];
+    const bool zero = !(den > 0);   // no active token: every gradient is 0 already (rewritten,
+                                    // so that the lines kept in L2 by pass 1 are released)
+    const float wu = zero ? 0.f : wk.wt[0];
     const uint64_t pol = l2_evict_first();
-    const bool per_seq = p.mode == 1 && p.cu != nullptr;
+    const bool per_seq = !zero && p.mode == 1 && p.cu != nullptr;
     const float denf = (float)den;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    int64_t ww = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    // the first sequence of the warp's next chunk is fetched one iteration ahead
-    int64_t s_next = per_seq && ww < nchunks ? wk.chunk_first[nchunks - 1 - ww] : 0;
-    for (; ww < nchunks; ww += nwarps) {
-        const int64_t w = nchunks - 1 - ww;
-        const int64_t s_cur = s_next;
-        if (per_seq && ww + nwarps < nchunks) s_next = wk.chunk_first[nchunks - 1 - (ww + nwarps)];
+    const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t w_end = (gw + 1) * nchunks / nwarps;
+    int64_t w = gw * nchunks / nwarps;
+    int64_t s_resume = per_seq && w < w_end ? wk.chunk_first[w] : 0;
+    for (; w < w_end; ++w) {
         const int64_t c0 = w * kGrpoChunk;
         const int nv = (int)(p.n - c0 < kGrpoChunk ? p.n - c0 : kGrpoChunk);
         float g[kGrpoLaneTokens];
         grpo_ld8<kVec, true>(p.grad + c0, lane, nv, g, pol);
-        if (zero) {
-#pragma unroll
-            for (int q = 0; q < kGrpoLaneTokens; ++q) g[q] = 0.f;
-        } else if (per_seq) {
-            // the first sequence recorded by pass 1; boundaries and counts in one trip
-            const GrpoRuns runs = grpo_runs_at(p, s_cur, c0, lane, wk.seg_cnt);
+        if (per_seq) {
+            const GrpoRuns runs = grpo_runs_at(p, s_resume, c0, lane, wk.seg_cnt);
+            int64_t s_last = runs.s;
             // each run's tokens times its weight; tokens in no sequence hold 0 already
-            grpo_runs<true>(p, runs, c0, nv, lane, wk.seg_cnt, [&](int64_t, int ua, int ub, int64_t c) {
+            grpo_runs<true>(p, runs, c0, nv, lane, wk.seg_cnt, [&](int64_t s, int ua, int ub, int64_t c) {
+                s_last = s;
                 const float ws = c > 0 ? __frcp_rn(__fmul_rn(denf, (float)c)) : 0.f;
                 const uint32_t in = (ua == 0 && ub == nv) ? 0xffu : grpo_in8(lane, ua, ub);
 #pragma unroll
                 for (int q = 0; q < kGrpoLaneTokens; ++q)
                     if ((in >> q) & 1u) g[q] = __fmul_rn(g[q], ws);
             });
+            s_resume = s_last;
         } else {
 #pragma unroll
             for (int q = 0; q < kGrpoLaneTokens; ++q) g[q] = __fmul_rn(g[q], wu);
