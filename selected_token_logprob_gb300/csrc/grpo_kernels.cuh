@@ -297,29 +297,37 @@ __device__ __forceinline__ void grpo_st8(float* base, int lane, int nvalid, cons
         }
     }
 }
-// Bit q set: token q of the lane exists (u < nvalid) and its mask byte is nonzero.
+// Bit q set: token q of the lane exists (u < nvalid) and its mask byte is
+// nonzero.  Both groups' mask words are loaded before either is decoded.
 template <bool kVec>
 __device__ __forceinline__ uint32_t grpo_active8(const uint8_t* mask, int lane, int nvalid, uint64_t pol) {
+    const int u0 = 4 * lane, u1 = 128 + 4 * lane;
+    if (mask == nullptr) {
+        uint32_t act = 0;
+#pragma unroll
+        for (int q = 0; q < kGrpoLaneTokens; ++q)
+            if ((q < 4 ? u0 : u1) + (q & 3) < nvalid) act |= 1u << q;
+        return act;
+    }
+    if (kVec && u1 + 4 <= nvalid) {   // both groups whole (every group of a full chunk)
+        const uint32_t m0 = ld_u32_hint(mask + u0, pol), m1 = ld_u32_hint(mask + u1, pol);
+        // bytes != 0 -> 1 in each byte, then the four bits gathered by a multiply
+        const uint32_t b0 = __vcmpne4(m0, 0u) & 0x01010101u, b1 = __vcmpne4(m1, 0u) & 0x01010101u;
+        return ((b0 * 0x01020408u) >> 24) | (((b1 * 0x01020408u) >> 24) << 4);
+    }
+    uint8_t m[kGrpoLaneTokens];
+#pragma unroll
+    for (int q = 0; q < kGrpoLaneTokens; ++q) {
+        const int u = (q < 4 ? u0 : u1) + (q & 3);
+        m[q] = u < nvalid ? __ldg(mask + u) : 0;
+    }
     uint32_t act = 0;
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int u = 128 * i + 4 * lane;
-        if (mask == nullptr) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (u + e < nvalid) act |= 1u << (4 * i + e);
-        } else if (kVec && u + 4 <= nvalid) {
-            // bytes != 0 -> 1 in each byte, then the four bits gathered by a multiply
-            const uint32_t m = __vcmpne4(ld_u32_hint(mask + u, pol), 0u) & 0x01010101u;
-            act |= ((m * 0x01020408u) >> 24) << (4 * i);
-        } else {
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (u + e < nvalid && __ldg(mask + u + e) != 0) act |= 1u << (4 * i + e);
-        }
-    }
+    for (int q = 0; q < kGrpoLaneTokens; ++q)
+        if (m[q] != 0) act |= 1u << q;
     return act;
 }
+
 // Bits of the lane's tokens with chunk index u in [ua, ub).
 __device__ __forceinline__ uint32_t grpo_in8(int lane, int ua, int ub) {
     uint32_t in = 0;
