@@ -504,16 +504,13 @@ __global__ void __launch_bounds__(kGrpoReduceThreads) k_grpo_reduce(GrpoArgs p, 
         e_first = grpo_cu(p, s0 + 32 * warp + lane + 1);
     }
     griddep_wait();
-    // chunk totals [b ps, (b + 1) ps)
+    // chunk totals [b ps, (b + 1) ps): the thread's first one is loaded now,
+    // with the sequences' first pieces below, and added first
     const int64_t ps = (nchunks + G - 1) / G;
     const int64_t k1 = (b + 1) * ps < nchunks ? (b + 1) * ps : nchunks;
-    FF T{0.f, 0.f};
-    int64_t C = 0;
-    for (int64_t k = b * ps + threadIdx.x; k < k1; k += kGrpoReduceThreads) {
-        T = ff_add(T, wk.chunk_sum[k]);
-        C += wk.chunk_cnt[k];
-    }
-    T = cta_fold<kW>(T, C, sh_v, sh_c);
+    const int64_t kf = b * ps + threadIdx.x;
+    const FF t_first = kf < k1 ? wk.chunk_sum[kf] : FF{0.f, 0.f};
+    const int64_t c_first = kf < k1 ? wk.chunk_cnt[kf] : 0;
     FF Q{0.f, 0.f};
     int64_t A = 0;
     if (seqs) {   // the sequences [s0, s1)
@@ -531,25 +528,22 @@ __global__ void __launch_bounds__(kGrpoReduceThreads) k_grpo_reduce(GrpoArgs p, 
             const bool is_long = j1 - j0 + 1 > kGrpoLongPieces;
             FF sum{0.f, 0.f};
             int64_t cnt = 0;
-            if (!is_long) {
-                int64_t j = j0;
-                for (; j + 3 <= j1; j += 4) {   // four loads in flight, added in order
-                    FF v[4];
-                    int64_t c[4];
+            if (!is_long) {   // up to 8 pieces per round, all loaded before they are added in order
+                for (int64_t j = j0; j <= j1; j += 8) {
+                    FF v[8];
+                    int64_t c[8];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        v[u] = wk.piece[j + u];
-                        c[u] = wk.piece_cnt[j + u];
+                    for (int u = 0; u < 8; ++u) {
+                        v[u] = j + u <= j1 ? wk.piece[j + u] : FF{0.f, 0.f};
+                        c[u] = j + u <= j1 ? wk.piece_cnt[j + u] : 0;
                     }
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        sum = ff_add(sum, v[u]);
-                        cnt += c[u];
+                    for (int u = 0; u < 8; ++u) {
+                        if (j + u <= j1) {
+                            sum = ff_add(sum, v[u]);
+                            cnt += c[u];
+                        }
                     }
-                }
-                for (; j <= j1; ++j) {
-                    sum = ff_add(sum, wk.piece[j]);
-                    cnt += wk.piece_cnt[j];
                 }
             }
             // the warp's long sequences, one at a time in lane order
@@ -579,8 +573,15 @@ __global__ void __launch_bounds__(kGrpoReduceThreads) k_grpo_reduce(GrpoArgs p, 
                 }
             }
         }
-        Q = cta_fold<kW>(Q, A, sh_v, sh_c);
     }
+    FF T = t_first;
+    int64_t C = c_first;
+    for (int64_t k = kf + kGrpoReduceThreads; k < k1; k += kGrpoReduceThreads) {
+        T = ff_add(T, wk.chunk_sum[k]);
+        C += wk.chunk_cnt[k];
+    }
+    T = cta_fold<kW>(T, C, sh_v, sh_c);
+    if (seqs) Q = cta_fold<kW>(Q, A, sh_v, sh_c);
     if (G == 1) {
         if (threadIdx.x == 0) {
             wk.part_t[0] = T;
