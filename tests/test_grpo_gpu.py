@@ -253,3 +253,23 @@ def test_grpo_unaligned_arrays_bitwise_equal():
         assert views[0].data_ptr() % 16 == 4
         for u, v in zip(a, b):
             assert torch.equal(u.view(torch.int32), v.view(torch.int32)), mode
+
+
+def test_grpo_bench_size_against_oracle():
+    """The bench's workload and launch shape: 16,777,216 tokens in 16,384
+    sequences, sequence mean of token means with KL; every loss and gradient
+    value against the FP64 oracle, and a second call bitwise equal."""
+    n, nseq = 1 << 24, 16384
+    lp, old, ref, adv, mask, cu = _case(n, 41, nseq=nseq)
+    kw = dict(mode="seq_mean_token_mean", eps_lo=0.2, eps_hi=0.28, beta=0.04)
+    args = _dev(lp, old, adv)
+    dk = dict(ref_logp=_dev(ref)[0], active_mask=_dev(mask)[0], cu_seqlens=_dev(cu)[0], **kw)
+    loss, grad = flp.logp_grpo_loss(*args, **dk)
+    want_l, want_g = oracle.grpo_loss(lp.double().numpy(), old.double().numpy(), adv.double().numpy(),
+                                      ref_logp=ref.double().numpy(), mask=mask.numpy(), cu_seqlens=cu.numpy(), **kw)
+    got_g = grad.double().cpu().numpy()
+    assert abs(loss.item() - want_l) <= 1e-5 * abs(want_l) + 1e-7, (loss.item(), want_l)
+    assert np.max(np.abs(got_g - want_g)) <= 1e-5 * np.max(np.abs(want_g))
+    again = flp.logp_grpo_loss(*args, **dk)
+    assert torch.equal(again[0].view(torch.int32), loss.view(torch.int32))
+    assert torch.equal(again[1].view(torch.int32), grad.view(torch.int32))
