@@ -13,6 +13,7 @@ import torch
 import oracle
 import selected_token_logprob_gb300 as flp
 import workloads
+from grpo_checks import _assert_grad, _token_weights
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -154,7 +155,9 @@ def test_grpo_many_segments_against_oracle(mode):
                                           cu_seqlens=None if cuv is None else cuv.numpy(), **kw)
         got_g = grad.double().cpu().numpy()
         assert abs(loss.item() - want_l) <= 1e-5 * abs(want_l) + 1e-7, (loss.item(), want_l)
-        assert np.max(np.abs(got_g - want_g)) <= 1e-5 * np.max(np.abs(want_g))
+        w = _token_weights(n, mask.numpy(), None if cuv is None else cuv.numpy(), mode)
+        _assert_grad(got_g, want_g, lp.double().numpy(), old.double().numpy(), adv.double().numpy(),
+                     ref.double().numpy(), kw["beta"], kw["eps_lo"], kw["eps_hi"], w)
         again = flp.logp_grpo_loss(*_dev(lp, old, adv), ref_logp=_dev(ref)[0], active_mask=_dev(mask)[0],
                                    cu_seqlens=None if cuv is None else _dev(cuv)[0], **kw)
         assert torch.equal(again[0].view(torch.int32), loss.view(torch.int32))
@@ -269,7 +272,9 @@ def test_grpo_bench_size_against_oracle():
                                       ref_logp=ref.double().numpy(), mask=mask.numpy(), cu_seqlens=cu.numpy(), **kw)
     got_g = grad.double().cpu().numpy()
     assert abs(loss.item() - want_l) <= 1e-5 * abs(want_l) + 1e-7, (loss.item(), want_l)
-    assert np.max(np.abs(got_g - want_g)) <= 1e-5 * np.max(np.abs(want_g))
+    w = _token_weights(n, mask.numpy(), cu.numpy(), kw["mode"])
+    _assert_grad(got_g, want_g, lp.double().numpy(), old.double().numpy(), adv.double().numpy(),
+                 ref.double().numpy(), kw["beta"], kw["eps_lo"], kw["eps_hi"], w)
     again = flp.logp_grpo_loss(*args, **dk)
     assert torch.equal(again[0].view(torch.int32), loss.view(torch.int32))
     assert torch.equal(again[1].view(torch.int32), grad.view(torch.int32))
