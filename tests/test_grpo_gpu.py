@@ -278,3 +278,22 @@ def test_grpo_bench_size_against_oracle():
     again = flp.logp_grpo_loss(*args, **dk)
     assert torch.equal(again[0].view(torch.int32), loss.view(torch.int32))
     assert torch.equal(again[1].view(torch.int32), grad.view(torch.int32))
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_grpo_300k_short_sequences(mode):
+    """2,097,152 tokens in 300,000 sequences (about 7 tokens each): the folds
+    run at their largest shape (1024 CTAs, sequence shares of 293 that loop,
+    the last CTA folding 4 partials per thread), and a 256-token chunk meets
+    about 37 sequences (boundary windows reloaded in both token passes)."""
+    n, nseq = 1 << 21, 300000
+    lp, old, ref, adv, mask, cu = _case(n, 51, nseq=nseq)
+    kw = dict(mode=mode, eps_lo=0.2, eps_hi=0.28, beta=0.03)
+    loss, grad = flp.logp_grpo_loss(*_dev(lp, old, adv), ref_logp=_dev(ref)[0], active_mask=_dev(mask)[0],
+                                    cu_seqlens=_dev(cu)[0], **kw)
+    want_l, want_g = oracle.grpo_loss(lp.double().numpy(), old.double().numpy(), adv.double().numpy(),
+                                      ref_logp=ref.double().numpy(), mask=mask.numpy(), cu_seqlens=cu.numpy(), **kw)
+    assert abs(loss.item() - want_l) <= 1e-5 * abs(want_l) + 1e-7, (loss.item(), want_l)
+    w = _token_weights(n, mask.numpy(), cu.numpy(), mode)
+    _assert_grad(grad.double().cpu().numpy(), want_g, lp.double().numpy(), old.double().numpy(),
+                 adv.double().numpy(), ref.double().numpy(), kw["beta"], kw["eps_lo"], kw["eps_hi"], w)
