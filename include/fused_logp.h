@@ -388,8 +388,8 @@ flp_status fused_linear_logp_forward_noalloc(const void* hidden, int64_t n, int6
  *              needed: 32 bytes of normaliser words, 32 KB for the fold's
  *              partials, a two-float sum and a count per 256-token chunk,
  *              and with sequences the same per (sequence, chunk) piece slot
- *              (num_seqs + ceil(n / 256) slots), a count per sequence and a
- *              sequence index per chunk; rounded up to 256 bytes.  One
+ *              (num_seqs + ceil(n / 256) slots), a sequence index per chunk
+ *              and a float per sequence; rounded up to 256 bytes.  One
  *              workspace serves one call at a time.
  * Tokens outside every sequence (before cu_seqlens[0] or from
  * cu_seqlens[num_seqs] on) are inactive: l = 0, grad 0.  cu_seqlens must be

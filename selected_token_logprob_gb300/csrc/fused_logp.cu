@@ -533,11 +533,11 @@ flp_status launch_dependent(const char* what, void (*kern)(Args...), int grid, i
 // GRPO workspace: 32 bytes of normaliser words and the fold's ticket, room
 // for the fold's per-CTA partials (32 bytes each, up to 1024 CTAs), per
 // 256-token chunk a two-float sum and a count, and with sequences per
-// (sequence, chunk) piece slot the same, per sequence a count and per chunk
-// its first sequence; rounded up to 256 bytes.
+// (sequence, chunk) piece slot the same, per chunk its first sequence and
+// per sequence the reciprocal of its active count; rounded up to 256 bytes.
 int64_t grpo_workspace_bytes(int64_t n, int64_t nseq) {
     const int64_t nchunks = ceil_div(n, flp::kGrpoChunk);
-    const int64_t seq_part = nseq > 0 ? 16 * (nseq + nchunks) + 8 * nseq + 8 * nchunks : 0;
+    const int64_t seq_part = nseq > 0 ? 16 * (nseq + nchunks) + 8 * nchunks + 4 * nseq : 0;
     return ceil_div(32 + 32 * flp::kGrpoFoldMaxCtas + 16 * nchunks + seq_part, 256) * 256;
 }
 
@@ -1126,8 +1126,8 @@ flp_status logp_grpo_loss(const float* logp, const float* old_logp, const float*
     wk.chunk_cnt = reinterpret_cast<int64_t*>(wk.chunk_sum + nchunks);
     wk.piece = reinterpret_cast<flp::FF*>(wk.chunk_cnt + nchunks);
     wk.piece_cnt = reinterpret_cast<int64_t*>(wk.piece + slots);
-    wk.seg_cnt = wk.piece_cnt + slots;
-    wk.chunk_first = wk.seg_cnt + (nseq > 0 ? nseq : 0);
+    wk.chunk_first = wk.piece_cnt + slots;
+    wk.seg_inv = reinterpret_cast<float*>(wk.chunk_first + (nseq > 0 ? nchunks : 0));
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int sms = sm_count(dev);
     if (sms <= 0) return fail(FLP_ECUDA, "cannot read the SM count of device %d", dev);

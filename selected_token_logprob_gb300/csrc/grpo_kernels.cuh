@@ -133,8 +133,8 @@ struct GrpoWork {
     int64_t* chunk_cnt;   // [nchunks]: its active tokens
     FF* piece;            // [nseq + nchunks]: loss sum of sequence s within chunk w, at s + w
     int64_t* piece_cnt;
-    int64_t* seg_cnt;     // [nseq]: active tokens of each sequence
     int64_t* chunk_first; // [nchunks]: the first sequence that may meet each chunk
+    float* seg_inv;       // [nseq]: 1 / (active tokens of each sequence), 0 for none
 };
 
 __device__ __forceinline__ int64_t grpo_chunks(int64_t n) { return (n + kGrpoChunk - 1) / kGrpoChunk; }
@@ -171,12 +171,12 @@ __device__ __forceinline__ int64_t grpo_find(const GrpoArgs& p, int64_t x, int l
 struct GrpoRuns {
     int64_t s;     // the first sequence that may meet the chunk
     int bnd;       // lane j: cu[s + j] - c0 clamped to [0, 256] (256 past cu[nseq])
-    int64_t aux;   // lane j: aux[s + j] when an aux array is given (s + j < nseq), else 0
+    float aux;     // lane j: aux[s + j] when an aux array is given (s + j < nseq), else 0
 };
 
 __device__ __forceinline__ GrpoRuns grpo_runs_at(const GrpoArgs& p, int64_t s, int64_t c0, int lane,
-                                                 const int64_t* aux) {
-    GrpoRuns r{s < 0 ? 0 : s, (int)kGrpoChunk, 0};
+                                                 const float* aux) {
+    GrpoRuns r{s < 0 ? 0 : s, (int)kGrpoChunk, 0.f};
     const int64_t idx = r.s + lane;
     if (idx <= p.nseq) {
         const int64_t d = grpo_cu(p, idx) - c0;
@@ -186,7 +186,7 @@ __device__ __forceinline__ GrpoRuns grpo_runs_at(const GrpoArgs& p, int64_t s, i
     return r;
 }
 __device__ __forceinline__ GrpoRuns grpo_runs_begin(const GrpoArgs& p, int64_t c0, int lane) {
-    if (p.cu == nullptr) return GrpoRuns{0, 0, 0};
+    if (p.cu == nullptr) return GrpoRuns{0, 0, 0.f};
     return grpo_runs_at(p, grpo_find(p, c0, lane), c0, lane, nullptr);
 }
 
@@ -196,17 +196,24 @@ __device__ __forceinline__ GrpoRuns grpo_runs_begin(const GrpoArgs& p, int64_t c
 // fetched 32 at a time.  kAux: pass the aux value (else 0, no shuffle).
 template <bool kAux, class F>
 __device__ __forceinline__ void grpo_runs(const GrpoArgs& p, GrpoRuns r, int64_t c0, int nv, int lane,
-                                          const int64_t* aux, F&& f) {
+                                          const float* aux, F&& f) {
     if (p.cu == nullptr) {
-        f((int64_t)0, 0, nv, (int64_t)0);   // one sequence: the whole batch
+        f((int64_t)0, 0, nv, 0.f);   // one sequence: the whole batch
         return;
+    }
+    if (r.s < p.nseq) {   // the common case: the chunk lies inside sequence r.s
+        const int a0 = __shfl_sync(0xffffffffu, r.bnd, 0), b0 = __shfl_sync(0xffffffffu, r.bnd, 1);
+        if (a0 == 0 && b0 >= nv) {
+            f(r.s, 0, nv, kAux ? __shfl_sync(0xffffffffu, r.aux, 0) : 0.f);
+            return;
+        }
     }
     while (r.s < p.nseq) {
         for (int j = 0; j < 31; ++j) {
             const int a = __shfl_sync(0xffffffffu, r.bnd, j);
             if (r.s + j >= p.nseq || a >= nv) return;
             const int b = min(__shfl_sync(0xffffffffu, r.bnd, j + 1), nv);
-            const int64_t x = kAux ? __shfl_sync(0xffffffffu, r.aux, j) : 0;
+            const float x = kAux ? __shfl_sync(0xffffffffu, r.aux, j) : 0.f;
             if (a < b) f(r.s + j, a, b, x);
         }
         r = grpo_runs_at(p, r.s + 31, c0, lane, aux);
@@ -392,7 +399,7 @@ __global__ void __launch_bounds__(kGrpoPassThreads, 4) k_grpo_terms(GrpoArgs p, 
         FF tot{0.f, 0.f};
         int64_t tcnt = 0;
         uint32_t inseq = 0;
-        grpo_runs<false>(p, runs, c0, nv, lane, nullptr, [&](int64_t s, int ua, int ub, int64_t) {
+        grpo_runs<false>(p, runs, c0, nv, lane, nullptr, [&](int64_t s, int ua, int ub, float) {
             s_last = s;
             // within the chunk, plain FP32: the lane's tokens in order, then the
             // xor butterfly (lane 0 holds the result)
@@ -566,7 +573,7 @@ __global__ void __launch_bounds__(kGrpoReduceThreads) k_grpo_reduce(GrpoArgs p, 
                 }
             }
             if (s < s1) {
-                wk.seg_cnt[s] = cnt;
+                wk.seg_inv[s] = cnt > 0 ? __frcp_rn((float)cnt) : 0.f;
                 if (cnt > 0) {
                     ++A;
                     if (p.mode == 1) Q = ff_add(Q, ff_div_count(sum, cnt));
@@ -638,8 +645,8 @@ __global__ void __launch_bounds__(kGrpoReduceThreads) k_grpo_reduce(GrpoArgs p, 
 
 // Each token's gradient times its weight: 1 / den, or for the sequence mean
 // of token means with sequences 1 / (den n_s), n_s the sequence's active
-// tokens (formed in FP32: den n_s rounded, then its correctly rounded
-// reciprocal).  Each warp takes a contiguous range of chunks (as in pass 1):
+// tokens (formed in FP32 as the product of the correctly rounded 1 / den and
+// 1 / n_s, the latter kept per sequence by the fold).  Each warp takes a contiguous range of chunks (as in pass 1):
 // the range's first sequence was recorded by pass 1, later chunks resume at
 // the last sequence seen.
 template <bool kVec>
@@ -659,18 +666,19 @@ __global__ void __launch_bounds__(kGrpoPassThreads, 5) k_grpo_scale(GrpoArgs p, 
     const int64_t w_end = (gw + 1) * nchunks / nwarps;
     int64_t w = gw * nchunks / nwarps;
     int64_t s_resume = per_seq && w < w_end ? wk.chunk_first[w] : 0;
+    const float inv_den = zero ? 0.f : __frcp_rn(denf);
     for (; w < w_end; ++w) {
         const int64_t c0 = w * kGrpoChunk;
         const int nv = (int)(p.n - c0 < kGrpoChunk ? p.n - c0 : kGrpoChunk);
         float g[kGrpoLaneTokens];
         grpo_ld8<kVec, true>(p.grad + c0, lane, nv, g, pol);
         if (per_seq) {
-            const GrpoRuns runs = grpo_runs_at(p, s_resume, c0, lane, wk.seg_cnt);
+            const GrpoRuns runs = grpo_runs_at(p, s_resume, c0, lane, wk.seg_inv);
             int64_t s_last = runs.s;
             // each run's tokens times its weight; tokens in no sequence hold 0 already
-            grpo_runs<true>(p, runs, c0, nv, lane, wk.seg_cnt, [&](int64_t s, int ua, int ub, int64_t c) {
+            grpo_runs<true>(p, runs, c0, nv, lane, wk.seg_inv, [&](int64_t s, int ua, int ub, float inv_cnt) {
                 s_last = s;
-                const float ws = c > 0 ? __frcp_rn(__fmul_rn(denf, (float)c)) : 0.f;
+                const float ws = __fmul_rn(inv_den, inv_cnt);
                 const uint32_t in = (ua == 0 && ub == nv) ? 0xffu : grpo_in8(lane, ua, ub);
 #pragma unroll
                 for (int q = 0; q < kGrpoLaneTokens; ++q)

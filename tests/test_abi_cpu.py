@@ -275,10 +275,10 @@ def test_grpo_host_checks(lib):
     b = ctypes.c_int64(0)
     # 32 bytes of normaliser words, room for 1024 fold partials of 32 bytes,
     # 16 per 256-token chunk, and with S sequences 16 per piece slot (S +
-    # chunks), 8 per sequence and 8 per chunk; rounded up to 256:
-    # 32 + 32768 + 16*128 = 34848 -> 35072;  + 16*228 + 8*100 + 8*128 -> 40448
+    # chunks), 8 per chunk and 4 per sequence; rounded up to 256:
+    # 32 + 32768 + 16*128 = 34848 -> 35072;  + 16*228 + 8*128 + 4*100 -> 39936
     assert lib.logp_grpo_loss_workspace_size(32768, 0, ctypes.byref(b)) == 0 and b.value == 35072
-    assert lib.logp_grpo_loss_workspace_size(32768, 100, ctypes.byref(b)) == 0 and b.value == 40448
+    assert lib.logp_grpo_loss_workspace_size(32768, 100, ctypes.byref(b)) == 0 and b.value == 39936
     assert lib.logp_grpo_loss_workspace_size(0, 0, ctypes.byref(b)) == 0 and b.value == 33024
     assert lib.logp_grpo_loss_workspace_size(-1, 0, ctypes.byref(b)) == EINVAL
 
