@@ -12,6 +12,11 @@
       d = g (onehot - p),  p = e^0 / (H (1 + e)) below, e / (H (1 + e)) above.
   (Random logits this wide are outside the accuracy envelope of binary32
   per-lane sums; the two-level row checks the indexing, not the rounding.)
+* The GRPO loss over more than 2^31 tokens (n = 2^31 + 777, sequences whose
+  bounds straddle 2^31): with logp == old_logp the ratio is exactly 1 and
+  each gradient is exactly -A times the token's FP32 weight (the KL = 0
+  identity of PR 5), checked bitwise at positions on both sides of 2^31 and
+  at the ragged end; the loss against an FP64 sum on the device.
 """
 
 import math
@@ -76,4 +81,35 @@ def test_row_wider_than_2_31_elements():
     for a, b in ((0, h), (h, v - 1)):
         mn, mx = torch.aminmax(dl[0, a:b])
         assert mn.item() == mx.item(), (a, b, mn.item(), mx.item())
+    assert flp.flp_device_error(0) == 0
+
+
+def test_grpo_beyond_2_31_tokens():
+    n = (1 << 31) + 777
+    free = torch.cuda.mem_get_info()[0]
+    if free < 5 * n * 4:
+        pytest.skip("needs about 43 GB of free device memory")
+    gen = torch.Generator(device=DEV).manual_seed(61)
+    lp = torch.empty(n, device=DEV).uniform_(-5.0, -0.1, generator=gen)
+    adv = torch.randn(n, device=DEV, generator=gen)
+    b1, b2 = 1000, (1 << 31) - 5
+    cu = torch.tensor([0, b1, b2, n], dtype=torch.int64, device=DEV)
+    lens = np.array([b1, b2 - b1, n - b2], dtype=np.float64)
+    ws = torch.empty(flp.logp_grpo_loss_workspace_size(n, 3), dtype=torch.uint8, device=DEV)
+    idx = [0, 1, b1 - 1, b1, 123456789, b2 - 1, b2, (1 << 31) - 1, 1 << 31, (1 << 31) + 1, n - 2, n - 1]
+    seq = np.searchsorted(np.array([0, b1, b2, n]), np.array(idx), side="right") - 1
+    a_s = adv[torch.tensor(idx, device=DEV)].cpu().numpy().astype(np.float32)
+    sums = [float(adv[lo_:hi_].double().sum().item()) for lo_, hi_ in ((0, b1), (b1, b2), (b2, n))]
+    for mode in ("token_mean", "seq_mean_token_mean"):
+        loss, grad = flp.logp_grpo_loss(lp, lp, adv, cu_seqlens=cu, mode=mode, workspace=ws)
+        got = grad[torch.tensor(idx, device=DEV)].cpu().numpy()
+        if mode == "token_mean":
+            w = np.full(len(idx), np.float32(1.0 / n), np.float32)     # the weight rounded once from 1/n
+            want_loss = -sum(sums) / n
+        else:                                                       # (1/den)(1/n_s), each rounded
+            w = np.float32(1.0) / np.float32(3.0) * (np.float32(1.0) / lens[seq].astype(np.float32))
+            want_loss = -np.mean([sums[k] / lens[k] for k in range(3)])
+        want = (-a_s) * w.astype(np.float32)
+        assert np.array_equal(got.view(np.int32), want.view(np.int32)), (mode, got, want)
+        assert abs(loss.item() - want_loss) <= 1e-5 * abs(want_loss) + 1e-7, (mode, loss.item(), want_loss)
     assert flp.flp_device_error(0) == 0
