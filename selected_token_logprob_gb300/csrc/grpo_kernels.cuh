@@ -17,16 +17,17 @@
 // The batch is cut into fixed chunks of 256 tokens (one warp each),
 // independent of the sequence layout, so the work per warp is the same
 // whatever the sequence lengths:
-//   1. k_grpo_terms: each warp takes a contiguous range of chunks; it loads a
-//      chunk (8 tokens per lane in two groups of 4, 16-byte accesses when the
-//      arrays allow) and finds the sequences that cross it (for its first
+//   1. k_grpo_terms: each warp takes a contiguous range of chunks.  It loads
+//      a chunk (8 tokens per lane in two groups of 4, 16-byte accesses when
+//      the arrays allow) and finds the sequences that cross it (for its first
 //      chunk a 32-ary search over cu_seqlens, later resuming at the last
-//      sequence seen; overlapped with the loads), and for each such run (sequence s within chunk w)
-//      sums l and counts the active tokens; the run's sums go to piece slot
-//      s + w (slots of distinct runs never collide: a later sequence only
-//      meets later chunks).  Each token's unnormalised gradient (or, when
-//      the weight is uniform and known up front, the final one) and loss are
-//      written, with the chunk's loss sum, active count and first sequence;
+//      sequence seen; overlapped with the loads).  For each such run
+//      (sequence s within chunk w) it sums l and counts the active tokens;
+//      the run's sums go to piece slot s + w (slots of distinct runs never
+//      collide: a later sequence only meets later chunks).  Each token's
+//      unnormalised gradient (or, when the weight is uniform and known up
+//      front, the final one) and loss are written, with the chunk's loss
+//      sum, active count and first sequence;
 //   2. k_grpo_reduce: G CTAs (G fixed by the sequence count) each fold a
 //      fixed share of the chunk totals and of the sequences (each sequence's
 //      pieces give its active count and mean); the CTA that finishes last
@@ -39,16 +40,14 @@
 // compensated sums in FP32 (Knuth's TwoSum per addition; the pair carries
 // about 44 significant bits), so the error does not grow with the batch: the
 // FP64 unit of this GPU is far too slow to accumulate per token.  Token
-// counts are integers.  Every fold has an order fixed by the token positions and the
-// sequence layout, never by the grid or by timing.
+// counts are integers.  Every fold has an order fixed by the token positions
+// and the sequence layout, never by the grid or by timing.
 #pragma once
 
 #include "logp_prims.cuh"
 
 namespace flp {
 
-constexpr int kGrpoThreads = 1024;                                   // the single-CTA fold
-constexpr int kGrpoWarps = kGrpoThreads / 32;
 constexpr int kGrpoPassThreads = 256;                                // token passes: 8 warps per CTA
 constexpr int kGrpoLaneTokens = 8;
 constexpr int64_t kGrpoChunk = 32 * kGrpoLaneTokens;                 // 256 tokens per warp
