@@ -833,6 +833,8 @@ def run_reference(args):
     oracle.build()
     if args.path == "linear":
         return _run_reference_linear(args, world)
+    if args.path == "grpo":
+        return _run_reference_grpo(args, world)
     wl = workloads.WORKLOADS[args.workload]
     rows = args.ref_rows
     x, y, g = workloads.make(wl, n=rows)   # same recipe, a bounded row sample, on the host
@@ -895,6 +897,48 @@ def _run_reference_linear(args, world):
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 5), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _run_reference_grpo(args, world):
+    """The FP64 oracle of the GRPO loss on a bounded sample of the GRPO
+    workload: the sequences that lie in its first --ref-rows x 8192 tokens."""
+    import oracle
+
+    n, nseq = args.grpo_n, args.grpo_seqs
+    lp, old, ref, adv, mask, cu = _grpo_inputs(n, nseq, 1, "cpu")
+    rows = min(n, max(1, args.ref_rows) * 8192)
+    cut = cu.numpy()
+    cut = np.concatenate([cut[cut < rows], [rows]])
+    hl = [t[:rows].double().numpy() for t in (lp, old, ref, adv)]
+    hm = mask[:rows].numpy()
+    kw = dict(ref_logp=hl[2], mask=hm, cu_seqlens=cut, mode="seq_mean_token_mean", eps_lo=0.2, eps_hi=0.28,
+              beta=0.04)
+    for _ in range(min(args.warmup, 1)):
+        oracle.grpo_loss(hl[0], hl[1], hl[3], **kw)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.grpo_loss(hl[0], hl[1], hl[3], **kw)
+        times.append(time.perf_counter() - t0)
+    sec = statistics.mean(times)
+    bpt = 4 * 4 + 1 + 4
+    value = rows * bpt / sec / 1e9
+    sample = f"the first {rows} tokens of the GRPO workload per step (FP64 loss and gradient); same 21 B/token"
+    metric = GRPO_METRIC if (n, nseq) == (16777216, 16384) else f"GRPO loss GB/s at N={n}, {nseq} sequences"
+    line = {
+        "metric": metric, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": f"GRPO clipped surrogate + k3 KL (beta 0.04), seq_mean_token_mean, {n} tokens in "
+                               f"{nseq} packed sequences of random lengths, 10% inactive (synthetic)",
+                   "n": n, "num_seqs": nseq, "tokens_per_step": rows},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
     print(json.dumps(line), flush=True)

@@ -28,6 +28,16 @@ def test_reference_arm_json_line():
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
 
 
+def test_reference_arm_grpo_json_line():
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        bench.main(["--impl", "reference", "--path", "grpo", "--grpo-n", "65536", "--grpo-seqs", "64",
+                    "--steps", "1", "--warmup", "1", "--ref-rows", "2"])
+    line = json.loads(buf.getvalue().strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
+    assert line["config"]["tokens_per_step"] == 16384 and line["cpu_baseline"]["kind"] == "oracle"
+
+
 def test_clock_summary_parsing():
     s = bench.ClockSampler(0)
     s.out = ("2026/12/02 10:00:00.100, 0, 1500, 2070, 300.0, 0x0, Not Active, Not Active, Not Active, Not Active\n"
