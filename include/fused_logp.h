@@ -398,7 +398,7 @@ flp_status fused_linear_logp_forward_noalloc(const void* hidden, int64_t n, int6
  * Deterministic: the batch is cut into fixed 256-token chunks (one warp
  * each) whatever the sequence lengths; each sequence's sums are a fold of its
  * chunk pieces in a fixed order, and the fold of the chunk totals has a shape
- * fixed by the sequence count (G shares, then the shares in order); the
+ * fixed by the problem's shape (G shares, then the shares in order); the
  * weights are applied last (by the first pass when normalizer > 0 makes the
  * weight uniform).  Sums are plain FP32 within a 256-token chunk and
  * compensated two-float sums in FP32 from there on.  The result does not

@@ -1146,11 +1146,11 @@ flp_status logp_grpo_loss(const float* logp, const float* old_logp, const float*
             flp::k_grpo_terms<false><<<terms_grid, flp::kGrpoPassThreads, 0, s>>>(a, wk);
         if ((st = check_launch("grpo terms")) != FLP_OK) return st;
     }
-    // the fold's first level: a CTA count fixed by the sequence count (its
-    // order depends on it); with no tokens one CTA writes the result
-    int64_t fold_ctas = ceil_div(nseq, 256);
-    fold_ctas = fold_ctas < flp::kGrpoFoldMinCtas ? flp::kGrpoFoldMinCtas
-                                                   : (fold_ctas > flp::kGrpoFoldMaxCtas ? flp::kGrpoFoldMaxCtas : fold_ctas);
+    // the fold's first level: a CTA count fixed by the shape (its order
+    // depends on it), one round of sequences and of chunk totals per CTA up
+    // to 1024 CTAs; with no tokens one CTA writes the result
+    int64_t fold_ctas = ceil_div(nseq > nchunks ? nseq : nchunks, flp::kGrpoReduceThreads);
+    fold_ctas = fold_ctas < 1 ? 1 : (fold_ctas > flp::kGrpoFoldMaxCtas ? flp::kGrpoFoldMaxCtas : fold_ctas);
     // the fold and the scale pass overlap their launch with the predecessor
     // (programmatic dependent launch; they wait for it on the device)
     if ((st = launch_dependent("grpo reduce", flp::k_grpo_reduce, n > 0 ? (int)fold_ctas : 1,

@@ -28,7 +28,7 @@
 //      unnormalised gradient (or, when the weight is uniform and known up
 //      front, the final one) and loss are written, with the chunk's loss
 //      sum, active count and first sequence;
-//   2. k_grpo_reduce: G CTAs (G fixed by the sequence count) each fold a
+//   2. k_grpo_reduce: G CTAs (G fixed by the shape) each fold a
 //      fixed share of the chunk totals and of the sequences (each sequence's
 //      pieces give its active count and mean); the CTA that finishes last
 //      folds the G partials in order into the loss and the weight;
@@ -108,10 +108,9 @@ __device__ __forceinline__ int64_t warp_sum_i64(int64_t v) {
     return v;
 }
 
-// The fold's first level has G CTAs, G a function of the sequence count
-// only (so the fold order is fixed by the layout): about 256 sequences per
-// CTA, at least 256 and at most 1024 CTAs.
-constexpr int kGrpoFoldMinCtas = 256;
+// The fold's first level has G CTAs, G a function of the shape only (so
+// the fold order is fixed by the layout): max(sequences, chunks) / 256
+// rounded up, at least 1 and at most 1024.
 constexpr int kGrpoFoldMaxCtas = 1024;
 constexpr int kGrpoReduceThreads = 256;
 
