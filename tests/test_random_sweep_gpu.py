@@ -1,0 +1,81 @@
+"""A seeded random sweep of the logits path: 24 configurations, each drawing
+at once the row count, a ragged vocabulary size, the logits dtype, the
+temperature, the row stride and the base alignment, an explicit active mask,
+the ignore fraction and the logit spread.  Each is checked against the FP64
+oracle with the bars of the fixed-shape tests:
+- logp within 1e-4;
+- LSE within 1e-4 plus one binary32 ulp;
+- 16-bit gradients no worse than max(2e-3 max|d|, the correctly rounded
+  result's own gap), and at most 1e-4 of the elements (rounded up: one miss
+  is allowed on small samples) not correctly rounded.  Near a 16-bit
+  rounding midpoint the FP32 arithmetic's ~1e-7 relative error decides the
+  side at a rate of about 1e-4, so a sample of a few thousand elements can
+  hold one such element;
+- FP32 gradients within 1e-6 max|d|."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import selected_token_logprob_gb300 as flp
+import workloads
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+DTYPES = [torch.bfloat16, torch.float16, torch.float32]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    flp._lib.load(build_if_missing=True)
+
+
+def _configs():
+    rng = np.random.default_rng(20261202)
+    out = []
+    for k in range(24):
+        n = int(rng.integers(1, 300))
+        v = int([rng.integers(1, 64), rng.integers(64, 5000), rng.integers(5000, 40000)][k % 3 if k < 12 else int(rng.integers(0, 3))])
+        out.append(dict(k=k, n=n, v=v, dtype=DTYPES[(k // 3) % 3], temp=float(rng.choice([1.0, 0.7, 1.3, 0.5])),
+                        pad=int(rng.choice([0, 0, 1, 7, 8, 17])), offset=int(rng.choice([0, 0, 1, 3])),
+                        masked=bool(rng.random() < 0.5), ignore=float(rng.choice([0.0, 0.05, 0.3])),
+                        sigma=float(rng.choice([1.0, 2.0, 4.0]))))
+    return out
+
+
+@pytest.mark.parametrize("c", _configs(), ids=lambda c: f"c{c['k']}-n{c['n']}-v{c['v']}")
+def test_random_configuration_against_oracle(c):
+    n, v, dtype, temp = c["n"], c["v"], c["dtype"], c["temp"]
+    wl = workloads.Workload(f"r{c['k']}", n, v, c["sigma"], 8.0 if c["k"] % 2 else 0.0, c["ignore"], "normal",
+                            seed=100 + c["k"])
+    x0, y, g = workloads.make(wl, device=DEV, dtype=dtype)
+    # the same values in a padded, possibly misaligned row layout
+    ld = v + c["pad"]
+    big = torch.zeros(n * ld + c["offset"] + 8, dtype=dtype, device=DEV)
+    x = big[c["offset"]:c["offset"] + n * ld].view(n, ld)[:, :v]
+    x.copy_(x0)
+    mask = None
+    if c["masked"]:
+        mask = (torch.rand(n, generator=torch.Generator().manual_seed(c["k"])) > 0.3).to(DEV)
+    logp, lse, lo = flp.fused_logp_forward(x, y, with_lse_lo=True, temperature=temp, active_mask=mask)
+    d = flp.fused_logp_backward(x, y, lse, g, lse_lo=lo, temperature=temp, active_mask=mask)
+    torch.cuda.synchronize()
+    assert flp.flp_device_error(0) == 0
+
+    scale = 1.0 if temp == 1.0 else float(np.float32(1.0 / temp))   # the binary32 1/T the library uses
+    xa, dt = workloads.host_array(x0)
+    yn, gn = y.cpu().numpy(), g.cpu().numpy()
+    mk = None if mask is None else mask.cpu().numpy().astype(np.uint8)
+    ref_logp, ref_lse = oracle.forward(xa, yn, dtype=dt, scale=scale, mask=mk)
+    assert np.max(np.abs(logp.double().cpu().numpy() - ref_logp)) <= 1e-4, c
+    lse_tol = 1e-4 + np.spacing(np.abs(ref_lse).astype(np.float32)).astype(np.float64)
+    assert np.all(np.abs(lse.double().cpu().numpy() - ref_lse) <= lse_tol), c
+    da, _ = workloads.host_array(d)
+    st = oracle.backward_compare(xa, yn, gn, da, dtype=dt, scale=scale, mask=mk)
+    assert st["n_nonfinite"] == 0, (c, st)
+    if dt == "f32":
+        assert st["max_abs_diff"] <= 1e-6 * st["max_abs_d"] + 1e-30, (c, st)
+    else:
+        assert st["max_abs_diff"] <= max(2e-3 * st["max_abs_d"], st["max_rounding_gap"]) + 1e-30, (c, st)
+        assert st["n_not_correctly_rounded"] <= int(np.ceil(1e-4 * st["n_compared"])), (c, st)
