@@ -1,4 +1,4 @@
-"""A seeded random sweep of the logits path: 24 configurations, each drawing
+"""Seeded random sweeps.  The logits path: 24 configurations, each drawing
 at once the row count, a ragged vocabulary size, the logits dtype, the
 temperature, the row stride and the base alignment, an explicit active mask,
 the ignore fraction and the logit spread.  Each is checked against the FP64
@@ -11,7 +11,10 @@ oracle with the bars of the fixed-shape tests:
   rounding midpoint the FP32 arithmetic's ~1e-7 relative error decides the
   side at a rate of about 1e-4, so a sample of a few thousand elements can
   hold one such element;
-- FP32 gradients within 1e-6 max|d|."""
+- FP32 gradients within 1e-6 max|d|.
+The fused LM-head forward: 12 configurations of shape, row strides,
+temperature and mask, with the tolerance derived from its tensor-core
+arithmetic."""
 
 import numpy as np
 import pytest
@@ -79,3 +82,35 @@ def test_random_configuration_against_oracle(c):
     else:
         assert st["max_abs_diff"] <= max(2e-3 * st["max_abs_d"], st["max_rounding_gap"]) + 1e-30, (c, st)
         assert st["n_not_correctly_rounded"] <= int(np.ceil(1e-4 * st["n_compared"])), (c, st)
+
+
+def _linear_configs():
+    rng = np.random.default_rng(20261203)
+    out = []
+    for k in range(12):
+        out.append(dict(k=k, n=int(rng.integers(1, 700)), d=8 * int(rng.integers(1, 257)),
+                        v=int([rng.integers(1, 300), rng.integers(300, 5000), rng.integers(5000, 30000)][k % 3]),
+                        temp=float(rng.choice([1.0, 0.7, 1.3])), pad_h=8 * int(rng.choice([0, 0, 1, 3])),
+                        pad_w=8 * int(rng.choice([0, 0, 2])), masked=bool(rng.random() < 0.5)))
+    return out
+
+
+@pytest.mark.parametrize("c", _linear_configs(), ids=lambda c: f"c{c['k']}-n{c['n']}-d{c['d']}-v{c['v']}")
+def test_random_linear_configuration_against_oracle(c):
+    """The fused LM-head forward over random shapes (D a multiple of 8, row
+    strides padded by multiples of 8), temperatures and masks, against the
+    FP64 oracle with the tolerance derived from the tensor-core arithmetic."""
+    from test_linear_gpu import _check, _padded
+
+    n, d, v = c["n"], c["d"], c["v"]
+    h, w, y = workloads.linear(n, d, v, seed=200 + c["k"], device=DEV)
+    hp = _padded(h, d + c["pad_h"], 7.0) if c["pad_h"] else h
+    wp = _padded(w, d + c["pad_w"], -3.0) if c["pad_w"] else w
+    mask = None
+    if c["masked"]:
+        mask = (torch.rand(n, generator=torch.Generator().manual_seed(50 + c["k"])) > 0.25).to(DEV)
+    logp, lse = flp.fused_linear_logp_forward(hp, wp, y, temperature=c["temp"], active_mask=mask)
+    torch.cuda.synchronize()
+    assert flp.flp_device_error(0) == 0
+    s = 1.0 if c["temp"] == 1.0 else float(np.float32(1.0 / c["temp"]))
+    _check(h, w, y, d, logp, lse, s=s, mask=mask, label=str(c))
