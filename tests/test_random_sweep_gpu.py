@@ -14,7 +14,8 @@ oracle with the bars of the fixed-shape tests:
 - FP32 gradients within 1e-6 max|d|.
 The fused LM-head forward: 12 configurations of shape, row strides,
 temperature and mask, with the tolerance derived from its tensor-core
-arithmetic."""
+arithmetic.  The GRPO loss: 12 configurations of token and sequence counts,
+mode, KL, mask, normaliser, clip range and alignment."""
 
 import numpy as np
 import pytest
@@ -114,3 +115,56 @@ def test_random_linear_configuration_against_oracle(c):
     assert flp.flp_device_error(0) == 0
     s = 1.0 if c["temp"] == 1.0 else float(np.float32(1.0 / c["temp"]))
     _check(h, w, y, d, logp, lse, s=s, mask=mask, label=str(c))
+
+
+def _grpo_configs():
+    rng = np.random.default_rng(20261204)
+    modes = ["token_mean", "seq_mean_token_mean", "seq_mean_token_sum"]
+    out = []
+    for k in range(12):
+        n = int([rng.integers(1, 300), rng.integers(300, 20000), rng.integers(20000, 400000)][k % 3])
+        out.append(dict(k=k, n=n, nseq=int(rng.integers(1, max(2, n // int(rng.choice([1, 8, 200]))) + 1)),
+                        mode=modes[(k // 3) % 3], kl=bool(rng.random() < 0.6), masked=bool(rng.random() < 0.6),
+                        norm=float(rng.choice([0.0, 0.0, 1234.0])), eps_lo=float(rng.choice([0.1, 0.2])),
+                        eps_hi=float(rng.choice([0.2, 0.28, 0.5])), offset=int(rng.choice([0, 0, 1]))))
+    return out
+
+
+@pytest.mark.parametrize("c", _grpo_configs(), ids=lambda c: f"c{c['k']}-n{c['n']}-s{c['nseq']}")
+def test_random_grpo_configuration_against_oracle(c):
+    """The GRPO loss over random token and sequence counts, modes, KL, mask,
+    normaliser, clip range and array alignment, against the FP64 oracle
+    (gradients compared with either branch accepted at a clip bound)."""
+    from grpo_checks import _assert_grad, _token_weights
+
+    n, nseq = c["n"], c["nseq"]
+    gen = torch.Generator().manual_seed(300 + c["k"])
+    lp = -torch.rand(n, generator=gen) * 6 - 0.05
+    old = lp + (torch.rand(n, generator=gen) - 0.5) * 1.2
+    ref = lp + (torch.rand(n, generator=gen) - 0.5) * 1.0
+    adv = torch.randn(n, generator=gen)
+    mask = (torch.rand(n, generator=gen) > 0.15).to(torch.uint8)
+    cuts = torch.sort(torch.randint(0, n + 1, (nseq - 1,), generator=gen)).values
+    cu = torch.cat([torch.zeros(1, dtype=torch.int64), cuts, torch.full((1,), n, dtype=torch.int64)])
+
+    def dev(t):   # optionally 4 bytes past an alignment boundary
+        if not c["offset"]:
+            return t.to(DEV)
+        b = torch.empty(t.numel() + 1, dtype=t.dtype, device=DEV)
+        b[1:].copy_(t)
+        return b[1:]
+
+    kw = dict(mode=c["mode"], eps_lo=c["eps_lo"], eps_hi=c["eps_hi"], beta=0.03 if c["kl"] else 0.0,
+              normalizer=c["norm"])
+    loss, grad = flp.logp_grpo_loss(dev(lp), dev(old), dev(adv), ref_logp=dev(ref) if c["kl"] else None,
+                                    active_mask=dev(mask) if c["masked"] else None, cu_seqlens=cu.to(DEV), **kw)
+    torch.cuda.synchronize()
+    mk = mask.numpy() if c["masked"] else None
+    want_l, want_g = oracle.grpo_loss(lp.double().numpy(), old.double().numpy(), adv.double().numpy(),
+                                      ref_logp=ref.double().numpy() if c["kl"] else None, mask=mk,
+                                      cu_seqlens=cu.numpy(), **kw)
+    assert abs(loss.item() - want_l) <= 1e-5 * abs(want_l) + 1e-7, (c, loss.item(), want_l)
+    w = _token_weights(n, mk, cu.numpy(), c["mode"], c["norm"])
+    _assert_grad(grad.double().cpu().numpy(), want_g, lp.double().numpy(), old.double().numpy(),
+                 adv.double().numpy(), ref.double().numpy() if c["kl"] else None, kw["beta"], c["eps_lo"],
+                 c["eps_hi"], w)
