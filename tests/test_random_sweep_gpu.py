@@ -12,8 +12,8 @@ oracle with the bars of the fixed-shape tests:
   side at a rate of about 1e-4, so a sample of a few thousand elements can
   hold one such element;
 - FP32 gradients within 1e-6 max|d|.
-The fused LM-head forward: 12 configurations of shape, row strides,
-temperature and mask, with the tolerance derived from its tensor-core
+The fused LM-head forward (12 configurations) and backward (6) over shape,
+row strides, temperature and mask, with the tolerances derived from their
 arithmetic.  The GRPO loss: 12 configurations of token and sequence counts,
 mode, KL, mask, normaliser, clip range and alignment."""
 
@@ -168,3 +168,39 @@ def test_random_grpo_configuration_against_oracle(c):
     _assert_grad(grad.double().cpu().numpy(), want_g, lp.double().numpy(), old.double().numpy(),
                  adv.double().numpy(), ref.double().numpy() if c["kl"] else None, kw["beta"], c["eps_lo"],
                  c["eps_hi"], w)
+
+
+def _linear_backward_configs():
+    rng = np.random.default_rng(20261205)
+    out = []
+    for k in range(6):
+        two_chunks = k == 5   # a second, partial 4096-row chunk
+        out.append(dict(k=k, n=int(rng.integers(4097, 4400) if two_chunks else rng.integers(1, 1500)),
+                        d=8 * int(rng.integers(1, 9) if two_chunks else rng.integers(1, 33)),
+                        v=int(rng.integers(1, 1500) if two_chunks else rng.integers(1, 4000)),
+                        temp=float(rng.choice([1.0, 0.7])), masked=bool(rng.random() < 0.5),
+                        pad=8 * int(rng.choice([0, 1]))))
+    return out
+
+
+@pytest.mark.parametrize("c", _linear_backward_configs(), ids=lambda c: f"c{c['k']}-n{c['n']}-d{c['d']}-v{c['v']}")
+def test_random_linear_backward_against_oracle(c):
+    """The fused LM-head backward (dhidden, dweight) over random shapes (one
+    with a second 4096-row chunk), temperatures, masks and padded strides,
+    against the FP64 oracle with the tolerance derived from its arithmetic."""
+    from test_linear_gpu import _backward_case, _grad_tol
+
+    n, d, v = c["n"], c["d"], c["v"]
+    mask = None
+    if c["masked"]:
+        mask = (torch.rand(n, generator=torch.Generator().manual_seed(70 + c["k"])) > 0.2).to(DEV)
+    h, w, y, g, dh, dw, _ = _backward_case(n, d, v, 400 + c["k"], c["temp"], mask=mask, pad=c["pad"])
+    assert flp.flp_device_error(0) == 0
+    hb, wb = workloads.bf16_bits(h), workloads.bf16_bits(w)
+    s = float(np.float32(1.0 / c["temp"]))
+    mk = None if mask is None else mask.cpu().numpy().astype(np.uint8)
+    ref_dh, ref_dw, ref_dz = oracle.linear_backward(hb, wb, y.cpu().numpy(), g.cpu().numpy(), d=d, scale=s,
+                                                    mask=mk, with_dz=True)
+    hd, wd = oracle.bf16_to_f64(hb)[:, :d], oracle.bf16_to_f64(wb)[:, :d]
+    assert np.all(np.abs(dh.double().cpu().numpy() - ref_dh) <= _grad_tol(ref_dz, wd, v)), c
+    assert np.all(np.abs(dw.double().cpu().numpy() - ref_dw) <= _grad_tol(ref_dz.T, hd, n)), c
