@@ -283,6 +283,8 @@ def logp_grpo_loss(logp: torch.Tensor, old_logp: torch.Tensor, advantages: torch
     ``grad`` is the upstream gradient for ``fused_logp_backward``.
     ``workspace`` (a CUDA byte tensor of logp_grpo_loss_workspace_size(N, S)
     bytes) is allocated when not given."""
+    if mode not in GRPO_MODES:
+        raise ValueError(f"mode must be one of {sorted(GRPO_MODES)} (got {mode!r})")
     n = logp.shape[0] if logp.dim() == 1 else -1
     for name, t in (("logp", logp), ("old_logp", old_logp), ("advantages", advantages)):
         _vec(t, name, n, torch.float32)

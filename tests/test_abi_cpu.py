@@ -271,6 +271,14 @@ def test_linear_shard_host_checks(lib):
                                        None, None) == EINVAL   # workspace too small
 
 
+def test_grpo_binding_rejects_an_unknown_mode():
+    import selected_token_logprob_gb300 as flp
+
+    t = torch.zeros(4)
+    with pytest.raises(ValueError, match="mode must be one of"):
+        flp.logp_grpo_loss(t, t, t, mode="seq_sum_token_mean")
+
+
 def test_grpo_host_checks(lib):
     b = ctypes.c_int64(0)
     # 32 bytes of normaliser words, room for 1024 fold partials of 32 bytes,
