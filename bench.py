@@ -20,8 +20,10 @@ measured bf16 tensor peak.
 
 --impl reference times the FP64 CPU oracle on the host cores (a bounded
 sample of rows per step) on the same metric; under torchrun only rank 0 runs
-it.  For N > 1 (torchrun) every rank runs its own replica of the workload on
-its own GPU (weak scaling, no collective on the data path).
+it.  For N > 1 (torchrun) the ranks split the rows of one global batch of
+N x 32768 rows (rank r's block drawn from seed r): rows are independent and
+each row's bits are batch-invariant, so every rank runs the same kernels on
+its own rows with no collective on the data path (weak scaling).
 """
 
 from __future__ import annotations
@@ -113,25 +115,86 @@ def _profiled_traffic(kernel: str):
 
 
 class ClockSampler:
-    """nvidia-smi samples (every 200 ms) kept only when their timestamp falls
-    inside the timed region (mark() is called at its start and end)."""
+    """SM clock, its maximum, power and the clock-event reasons during the
+    timed region (mark() is called at its start and end).
+
+    Read-only queries.  Preferred: NVML through ctypes, polled every 10 ms in
+    a thread, so that even a timed region of a few tens of milliseconds holds
+    several samples.  Fallback: `nvidia-smi -lms 200`.  Only samples whose
+    time stamp falls inside the marked window are summarised."""
 
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clock-event reason bits (nvml.h: nvmlClocksEventReason*)
+    REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                   0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+    PERIOD_S = 0.010
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, uuid: str | None = None):
         self.gpu = gpu_index
+        self.uuid = uuid
         self.proc = None
         self.out = ""
         self.window = None
+        self.samples = []          # (time, sm_mhz, sm_max_mhz, set of reasons, watts)
+        self.source = None
+        self._thread = None
+        self._stop = None
+
+    # ---- NVML
+    def _nvml_start(self) -> bool:
+        import ctypes
+        import threading
+
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return False
+        if nv.nvmlInit_v2() != 0:
+            return False
+        h = ctypes.c_void_p()
+        ok = False
+        if self.uuid:
+            ok = nv.nvmlDeviceGetHandleByUUID(self.uuid.encode(), ctypes.byref(h)) == 0
+        if not ok:
+            ok = nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.gpu), ctypes.byref(h)) == 0
+        if not ok:
+            return False
+        reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        self._stop = threading.Event()
+
+        def loop():
+            mhz, mx, pw = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint()
+            rs = ctypes.c_ulonglong()
+            while not self._stop.is_set():
+                t = time.time()
+                a = nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz))          # NVML_CLOCK_SM
+                b = nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+                c = reasons_fn(h, ctypes.byref(rs))
+                d = nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw))
+                if a == 0 and b == 0 and c == 0:
+                    names = {n for bit, n in self.REASON_BITS.items() if rs.value & bit}
+                    self.samples.append((t, float(mhz.value), float(mx.value), names,
+                                         pw.value / 1000.0 if d == 0 else None))
+                self._stop.wait(self.PERIOD_S)
+
+        self._thread = threading.Thread(target=loop, daemon=True)
+        self._thread.start()
+        self.source = "nvml, every 10 ms"
+        return True
 
     def __enter__(self):
+        if self._nvml_start():
+            time.sleep(0.05)
+            return self
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi, every 200 ms"
             time.sleep(0.5)                  # let it start sampling before the timed region
         except (OSError, ValueError):
             self.proc = None
@@ -143,6 +206,9 @@ class ClockSampler:
         self.window = (now, None) if self.window is None or self.window[1] is not None else (self.window[0], now)
 
     def __exit__(self, *exc):
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(2)
         self.out = ""
         if self.proc is not None:
             self.proc.terminate()
@@ -162,23 +228,48 @@ class ClockSampler:
         except ValueError:
             return None
 
+    def _smi_samples(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        out = []
+        for r in csv.reader(io.StringIO(self.out or "")):
+            if len(r) < 10:
+                continue
+            ts = self._stamp(r[0])
+            num = lambda x: float(x) if x.strip().replace(".", "").isdigit() else None  # noqa: E731
+            reasons = {names[i] for i in range(4) if "Active" in r[6 + i] and "Not" not in r[6 + i]}
+            out.append((ts, num(r[2]), num(r[3]), reasons, num(r[4])))
+        return out
+
     def summary(self):
-        rows = [r for r in csv.reader(io.StringIO(self.out or "")) if len(r) >= 10]
+        rows = list(self.samples) if self.samples else self._smi_samples()
         if self.window and self.window[1] is not None:
             t0, t1 = self.window
-            inside = [r for r in rows if (ts := self._stamp(r[0])) is not None and t0 <= ts <= t1]
+            inside = [r for r in rows if r[0] is not None and t0 <= r[0] <= t1]
         else:
             inside = rows
         if not inside:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
-        sm = [float(r[2]) for r in inside if r[2].strip().replace(".", "").isdigit()]
-        smax = [float(r[3]) for r in inside if r[3].strip().replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in inside for i in range(4) if "Active" in r[6 + i]
-                          and "Not" not in r[6 + i]})
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0,
+                    "source": self.source}
+        sm = [r[1] for r in inside if r[1] is not None]
+        smax = [r[2] for r in inside if r[2] is not None]
+        pw = [r[4] for r in inside if r[4] is not None]
+        reasons = sorted(set().union(*[r[3] for r in inside]))
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "reasons": reasons, "samples": len(inside)}
+                "power_w_max": round(max(pw), 1) if pw else None,
+                "reasons": reasons, "samples": len(inside), "source": self.source}
+
+
+def _gpu_uuid(dev) -> str | None:
+    """The CUDA device's UUID as NVML names it ("GPU-..."), if torch exposes it."""
+    import torch
+
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+    except (AttributeError, RuntimeError):
+        return None
+    return u if u.startswith("GPU-") else f"GPU-{u}"
+
 
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -253,7 +344,7 @@ def run_ours(args):
                       "step_extra = max_memory_allocated during one step minus memory_allocated before it"}
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(local, _gpu_uuid(dev))
     _barrier(world)
     torch.cuda.synchronize(dev)
     with sampler:
@@ -296,7 +387,9 @@ def run_ours(args):
         "dtype": "f32", "data": "synthetic",
         "config": {"workload": WORKLOAD_DESC if args.workload == "long" else args.workload,
                    "n": n, "v": v, "logits_dtype": args.dtype, "temperature": temp,
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "parallelism": (f"rows x{world}: rank r computes rows [r*{n}, (r+1)*{n}) of one global "
+                                   f"batch of {world * n} rows (row block r drawn from seed r), no collective "
+                                   f"on the data path" if world > 1 else "single GPU"),
                    "l2": "inputs (9.96 GB) exceed the 129 MB L2; no flush"},
         "fwd_ms": round(fwd_avg, 4), "bwd_ms": round(bwd_avg, 4),
         "fwd_gbs": round(logits_per_rank * FWD_BYTES_PER_LOGIT * ebytes // 2 / (fwd_avg * 1e-3) / 1e9, 1),
@@ -355,7 +448,7 @@ def run_linear(args):
         step()
     torch.cuda.synchronize(dev)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(local, _gpu_uuid(dev))
     _barrier(world)
     torch.cuda.synchronize(dev)
     with sampler:
@@ -462,7 +555,7 @@ def run_grpo(args):
     torch.cuda.synchronize(dev)
     per_call = (time.perf_counter() - t_probe) / 20
     steps = max(args.steps, int(1.0 / max(per_call, 1e-6)))
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(local, _gpu_uuid(dev))
     with sampler:
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)

@@ -197,6 +197,66 @@ flp_status logp_merge_partials_ex(const float* part_max, const float* part_sum, 
                                   flp_stream_t stream);
 
 /*
+ * Backward of one vocabulary shard (PR #314 "Deterministic config option":
+ * the vocab-parallel logprob op is an autograd function over the local shard,
+ * whose backward each rank runs on its own columns with the merged LSE; the
+ * method's backward, PR #495 Summary item 2).  The shard holds global columns
+ * [vocab_start, vocab_start + real_width) of a v_total-column vocabulary in
+ * shard_logits[n, ld_shard].  For c in [0, real_width):
+ *   dshard[t, c] = s g_t (onehot(y_t)[vocab_start + c] - exp(s x[t, c] - LSE_t))
+ * with lse (+ lse_lo) the merged, global values.  A row is active by its
+ * global target (0 <= y_t < v_total, not ignore_index, mask byte nonzero);
+ * the one-hot term appears only in the shard that holds y_t.  Inactive rows
+ * get +0.  Elementwise, with the unsharded backward's arithmetic: the shards'
+ * outputs side by side are bitwise the unsharded dlogits, for any split (the
+ * bounds need not lie on the tile grid).  dshard may alias shard_logits
+ * exactly (in place); other overlap is FLP_EINVAL.  Other arguments and
+ * errors as for fused_logp_backward_ex; FLP_EINVAL if the shard is not inside
+ * [0, v_total).
+ */
+flp_status logp_shard_backward(const void* shard_logits, int64_t n, int64_t ld_shard, int64_t vocab_start,
+                               int64_t real_width, int64_t v_total, const int64_t* targets,
+                               int64_t ignore_index, const float* lse, const float* lse_lo,
+                               const float* grad, void* dshard, int64_t ld_out, flp_stream_t stream);
+flp_status logp_shard_backward_ex(const void* shard_logits, int dtype, int64_t n, int64_t ld_shard,
+                                  int64_t vocab_start, int64_t real_width, int64_t v_total,
+                                  const int64_t* targets, int64_t ignore_index, const uint8_t* active_mask,
+                                  float inv_temperature, const float* lse, const float* lse_lo,
+                                  const float* grad, void* dshard, int64_t ld_out, flp_stream_t stream);
+
+/*
+ * Merge of partials gathered from the ranks of a vocabulary-parallel group
+ * (issue #241 PR 3 bullets: per-shard (max, sumexp) partials, the collective
+ * only transports them, one merge in fixed index order; PR 6: each rank emits
+ * (max, sumexp, selected_logit); PR #314 Tensor Parallel section: the tile
+ * partials are all-gathered and every rank runs the same merge).
+ *   gathered     device FP32; rank r's block starts at gathered + r *
+ *                rank_stride and holds, in this order, its tile maxima
+ *                [n, 16], tile sums [n, 16] and selected logits [n] (33 n
+ *                floats), as logp_shard_partials_ex writes them into
+ *                part_max = block, part_sum = block + 16 n, sel = block + 32 n.
+ *                An all-gather of each rank's block is the whole exchange.
+ *   rank_stride  floats between consecutive ranks' blocks (>= 33 n when
+ *                world > 1; ignored when world == 1)
+ *   world        ranks, 1 ..16
+ *   vocab_starts, real_widths  HOST arrays [world]: rank r's shard is
+ *                [vocab_starts[r], vocab_starts[r] + real_widths[r]); each on
+ *                the tile grid (as logp_shard_partials requires), together
+ *                covering every tile of [0, v_total) exactly once, else
+ *                FLP_EUNSUPPORTED (off the grid) or FLP_EINVAL (gap, overlap).
+ * Tile k's partial is read from the rank holding it; row t's selected logit
+ * from the rank holding column y_t.  Other bytes of the blocks are never
+ * read.  Then as logp_merge_partials_ex: the result is bitwise equal to
+ * fused_logp_forward_ex on the unsharded logits, for any world and split.
+ */
+flp_status logp_merge_gathered_partials_ex(const float* gathered, int64_t rank_stride, int64_t world,
+                                           const int64_t* vocab_starts, const int64_t* real_widths,
+                                           const int64_t* targets, int64_t ignore_index,
+                                           const uint8_t* active_mask, int64_t n, int64_t v_total,
+                                           float inv_temperature, float* logp, float* lse, float* lse_lo,
+                                           flp_stream_t stream);
+
+/*
  * Fused LM head + logp (linear_logp, named in RL-Kernel PR #495 Summary; the
  * pages give no formula or design).  The logits z = H W^T of BF16 hidden
  * states and BF16 LM-head weight rows are formed on the tensor cores and
@@ -343,8 +403,10 @@ flp_status fused_linear_logp_shard_backward(const void* hidden, int64_t n, int64
  *   Memory: every GPU that loads the library holds the 16 MiB until the
  *   process exits.
  *   First call per device: looks up the array's device address
- *   (cudaGetSymbolAddress) and caches it; make that first call before any
- *   stream capture.
+ *   (cudaGetSymbolAddress, with that device current) and caches it; make
+ *   that first call before any stream capture.  The cached address belongs
+ *   to the device's context: after cudaDeviceReset it is stale, so do not
+ *   call this entry point again in a process that has reset the device.
  *   Sharing: all calls in the process use the same array.  Calls whose work
  *   can overlap on a GPU (different streams, or different host threads
  *   without ordering) race on it and give wrong results; order them, e.g. on

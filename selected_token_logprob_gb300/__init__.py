@@ -64,7 +64,9 @@ __all__ = [
     "fused_linear_logp_workspace_size",
     "logp_grpo_loss",
     "logp_grpo_loss_workspace_size",
+    "logp_merge_gathered_partials",
     "logp_merge_partials",
+    "logp_shard_backward",
     "logp_shard_partials",
 ]
 GRPO_MODES = {"token_mean": 0, "seq_mean_token_mean": 1, "seq_mean_token_sum": 2}
@@ -269,6 +271,102 @@ def logp_merge_partials(part_max: torch.Tensor, part_sum: torch.Tensor, sel: tor
                                                 logp.data_ptr(), lse.data_ptr(), _opt_ptr(lse_lo),
                                                 _stream(targets))
         _lib.check("logp_merge_partials", st)
+    return (logp, lse, lse_lo) if want_lo else (logp, lse)
+
+
+def logp_shard_backward(shard_logits: torch.Tensor, vocab_start: int, real_width: int, v_total: int,
+                        targets: torch.Tensor, lse: torch.Tensor, grad: torch.Tensor,
+                        ignore_index: int = IGNORE_INDEX, dshard: torch.Tensor | None = None,
+                        lse_lo: torch.Tensor | None = None, temperature: float = 1.0,
+                        active_mask: torch.Tensor | None = None) -> torch.Tensor:
+    """Gradient [N, real_width] (the shard's dtype) of one vocabulary shard
+    holding global columns [vocab_start, vocab_start + real_width) of a
+    v_total-column vocabulary, from the merged (global) lse / lse_lo.  The
+    shards' outputs side by side are the unsharded fused_logp_backward
+    bitwise.  ``dshard`` may be the shard's own columns (in place)."""
+    n, wpad, ld = _rows(shard_logits, "shard_logits")
+    dt = _dtype(shard_logits, "shard_logits")
+    inv_t = _inv_temperature(temperature)
+    if not 0 < real_width <= wpad:
+        raise ValueError(f"real_width {real_width} must be in [1, {wpad}]")
+    _vec(targets, "targets", n, torch.int64)
+    _vec(lse, "lse", n, torch.float32)
+    _vec(grad, "grad", n, torch.float32)
+    if lse_lo is not None:
+        _vec(lse_lo, "lse_lo", n, torch.float32)
+        _cuda(lse_lo)
+    if dshard is None:
+        dshard = torch.empty((n, real_width), dtype=shard_logits.dtype, device=shard_logits.device)
+    if dshard.dtype != shard_logits.dtype or tuple(dshard.shape) != (n, real_width):
+        raise ValueError(f"dshard must be a [{n}, {real_width}] tensor of the shard's dtype")
+    _, _, ld_out = _rows(dshard, "dshard")
+    _cuda(shard_logits, targets, lse, grad, dshard)
+    mp = _mask(active_mask, n)
+    if n == 0:
+        return dshard
+    st = _lib.load().logp_shard_backward_ex(shard_logits.data_ptr(), dt, n, ld, int(vocab_start),
+                                            int(real_width), int(v_total), targets.data_ptr(),
+                                            int(ignore_index), mp, inv_t, lse.data_ptr(), _opt_ptr(lse_lo),
+                                            grad.data_ptr(), dshard.data_ptr(), ld_out,
+                                            _stream(shard_logits))
+    _lib.check("logp_shard_backward", st)
+    return dshard
+
+
+def partials_block(n: int, device) -> torch.Tensor:
+    """One rank's exchange block for the vocabulary-parallel merge: FP32
+    [33 n] = tile maxima [n, 16], tile sums [n, 16], selected logits [n]."""
+    return torch.empty((2 * NUM_TILES + 1) * n, dtype=torch.float32, device=device)
+
+
+def partials_views(block: torch.Tensor, n: int):
+    """(part_max [n, 16], part_sum [n, 16], sel [n]) views of an exchange
+    block, in the layout logp_merge_gathered_partials reads."""
+    k = NUM_TILES * n
+    return block[:k].view(n, NUM_TILES), block[k:2 * k].view(n, NUM_TILES), block[2 * k:2 * k + n]
+
+
+def logp_merge_gathered_partials(gathered: torch.Tensor, vocab_starts, real_widths, targets: torch.Tensor,
+                                 v_total: int, ignore_index: int = IGNORE_INDEX,
+                                 logp: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                                 lse_lo: torch.Tensor | None = None, with_lse_lo: bool = False,
+                                 temperature: float = 1.0, active_mask: torch.Tensor | None = None):
+    """(logp, lse[, lse_lo]) from the exchange blocks of every rank of a
+    vocabulary-parallel group, gathered as FP32 [world, 33 N] (rank r's block
+    in row r; see ``partials_block``).  ``vocab_starts`` / ``real_widths`` give
+    each rank's shard; the result is bitwise the unsharded forward."""
+    import ctypes
+
+    inv_t = _inv_temperature(temperature)
+    n = targets.shape[0] if targets.dim() == 1 else -1
+    _vec(targets, "targets", n, torch.int64)
+    world = len(vocab_starts)
+    if len(real_widths) != world:
+        raise ValueError("vocab_starts and real_widths must have one entry per rank")
+    block = (2 * NUM_TILES + 1) * n
+    if (gathered.dtype != torch.float32 or gathered.dim() != 2 or gathered.shape[0] != world
+            or gathered.shape[1] < block or gathered.stride(1) != 1):
+        raise ValueError(f"gathered must be FP32 [{world}, >= {block}] with contiguous rows")
+    dev = targets.device
+    logp = torch.empty(n, dtype=torch.float32, device=dev) if logp is None else logp
+    lse = torch.empty(n, dtype=torch.float32, device=dev) if lse is None else lse
+    want_lo = with_lse_lo or lse_lo is not None
+    if want_lo and lse_lo is None:
+        lse_lo = torch.empty(n, dtype=torch.float32, device=dev)
+    _vec(logp, "logp", n, torch.float32)
+    _vec(lse, "lse", n, torch.float32)
+    _cuda(gathered, targets, logp, lse)
+    if want_lo:
+        _vec(lse_lo, "lse_lo", n, torch.float32)
+        _cuda(lse_lo)
+    mp = _mask(active_mask, n)
+    starts = (ctypes.c_int64 * max(1, world))(*[int(a) for a in vocab_starts])
+    widths = (ctypes.c_int64 * max(1, world))(*[int(w) for w in real_widths])
+    st = _lib.load().logp_merge_gathered_partials_ex(
+        gathered.data_ptr(), gathered.stride(0) if world > 1 else 0, world, starts, widths, targets.data_ptr(),
+        int(ignore_index), mp, n, int(v_total), inv_t, logp.data_ptr(), lse.data_ptr(), _opt_ptr(lse_lo),
+        _stream(targets))
+    _lib.check("logp_merge_gathered_partials", st)
     return (logp, lse, lse_lo) if want_lo else (logp, lse)
 
 

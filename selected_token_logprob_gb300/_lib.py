@@ -38,6 +38,13 @@ SIGNATURES = {
                                               ctypes.c_float, _P, _P, _P, _P, _P]),
     "logp_merge_partials_ex": (ctypes.c_int, [_P, _P, _P, _P, _I64, _P, _I64, _I64,
                                               ctypes.c_float, _P, _P, _P, _P]),
+    "logp_shard_backward": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _I64, _P, _I64, _P, _P, _P, _P,
+                                           _I64, _P]),
+    "logp_shard_backward_ex": (ctypes.c_int, [_P, ctypes.c_int, _I64, _I64, _I64, _I64, _I64, _P, _I64, _P,
+                                              ctypes.c_float, _P, _P, _P, _P, _I64, _P]),
+    "logp_merge_gathered_partials_ex": (ctypes.c_int, [_P, _I64, _I64, ctypes.POINTER(_I64),
+                                                       ctypes.POINTER(_I64), _P, _I64, _P, _I64, _I64,
+                                                       ctypes.c_float, _P, _P, _P, _P]),
     "logp_grpo_loss_workspace_size": (ctypes.c_int, [_I64, _I64, ctypes.POINTER(_I64)]),
     "logp_grpo_loss": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, ctypes.c_int,
                                       ctypes.c_float, ctypes.c_float, ctypes.c_float,

@@ -5,6 +5,8 @@
 #include <cublasLt.h>
 #include <cuda_runtime.h>
 #include <math.h>
+
+#include <atomic>
 #include <stdarg.h>
 #include <stdint.h>
 #include <stdio.h>
@@ -158,27 +160,29 @@ flp::Scale make_scale(float s) {
     return flp::Scale{s, hi, lo};
 }
 
+// Per-device caches below are atomics: host threads may call in
+// concurrently; every writer stores the same value, so the first one wins.
 int sm_count(int dev) {
-    static int count[kMaxDevices];
-    if (count[dev] == 0) {
-        int c = 0;
+    static std::atomic<int> count[kMaxDevices];
+    int c = count[dev].load(std::memory_order_acquire);
+    if (c == 0) {
         if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        count[dev] = c;
+        count[dev].store(c, std::memory_order_release);
     }
-    return count[dev];
+    return c;
 }
 
 // Once per device and kernel: allow the bulk-copy forward its dynamic shared
-// memory (idempotent, so a race between threads is harmless).
+// memory (idempotent, so two threads doing it at once is harmless).
 template <flp::Dt D, bool kScaled>
 flp_status bulk_setup(int dev) {
-    static bool ready[kMaxDevices];
-    if (!ready[dev]) {
+    static std::atomic<bool> ready[kMaxDevices];
+    if (!ready[dev].load(std::memory_order_acquire)) {
         const cudaError_t e = cudaFuncSetAttribute(flp::k_logp_fwd_bulk<D, kScaled>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    flp::kFwdSmemBytes<D>);
         if (e != cudaSuccess) return fail(FLP_ECUDA, "forward setup: %s", cudaGetErrorString(e));
-        ready[dev] = true;
+        ready[dev].store(true, std::memory_order_release);
     }
     return FLP_OK;
 }
@@ -233,12 +237,14 @@ struct BwdArgs {
     int64_t ld_out;
     cudaStream_t st;
     bool vin, vout, in_place;
+    int64_t y_off, v_total;   // the buffer's first global column; the whole vocabulary
 };
 
 template <flp::Dt D, bool VI, bool VO, bool IP>
 void launch_bwd(const BwdArgs& a, dim3 grid) {
     flp::k_logp_bwd<D, VI, VO, IP><<<grid, flp::kBwdThreads, 0, a.st>>>(
-        a.x, a.n, a.v, a.ld, a.y, a.ii, a.mask, a.s, a.inv_s, a.lse, a.lse_lo, a.g, a.dx, a.ld_out);
+        a.x, a.n, a.v, a.ld, a.y, a.ii, a.mask, a.s, a.inv_s, a.lse, a.lse_lo, a.g, a.dx, a.ld_out, a.y_off,
+        a.v_total);
 }
 
 template <flp::Dt D>
@@ -320,15 +326,15 @@ flp_status make_tmap_bf16(CUtensorMap* m, const void* ptr, int64_t rows, int64_t
 }
 
 flp_status linear_setup(int dev) {
-    static bool ready[kMaxDevices];
-    if (!ready[dev]) {
+    static std::atomic<bool> ready[kMaxDevices];
+    if (!ready[dev].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(flp::k_linear_logp_tiles<false>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)flp::kLinSmemBytes);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(flp::k_linear_logp_tiles<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)flp::kLinSmemBytes);
         if (e != cudaSuccess) return fail(FLP_ECUDA, "linear logp setup: %s", cudaGetErrorString(e));
-        ready[dev] = true;
+        ready[dev].store(true, std::memory_order_release);
     }
     return FLP_OK;
 }
@@ -430,19 +436,22 @@ bool linear_workspace_bytes(int64_t n, int64_t v, int64_t* out) {
 }
 
 // Device address of g_linear_noalloc_scratch on `dev` (which must be
-// current), looked up on the first call for that device and cached.
+// current), looked up on the first call for that device and cached (an
+// atomic per device: concurrent first calls each look it up and store the
+// same address).  The cached address belongs to the device's current
+// context; after cudaDeviceReset it is stale.
 flp_status noalloc_scratch_address(int dev, void** out) {
-    static void* addr[kMaxDevices];
-    if (addr[dev] == nullptr) {
-        void* p = nullptr;
+    static std::atomic<void*> addr[kMaxDevices];
+    void* p = addr[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
         const cudaError_t e = cudaGetSymbolAddress(&p, g_linear_noalloc_scratch);
         if (e != cudaSuccess || p == nullptr) {
             (void)cudaGetLastError();
             return fail(FLP_ECUDA, "address of the static scratch on device %d: %s", dev, cudaGetErrorString(e));
         }
-        addr[dev] = p;
+        addr[dev].store(p, std::memory_order_release);
     }
-    *out = addr[dev];
+    *out = p;
     return FLP_OK;
 }
 
@@ -590,16 +599,25 @@ flp_status fused_logp_forward(const void* logits, int64_t n, int64_t v, int64_t 
                                  1.f, logp, lse, lse_lo, stream);
 }
 
-flp_status fused_logp_backward_ex(const void* logits, int dtype, int64_t n, int64_t v, int64_t ld,
-                                  const int64_t* targets, int64_t ignore_index,
-                                  const uint8_t* active_mask, float inv_temperature,
-                                  const float* lse, const float* lse_lo, const float* grad,
-                                  void* dlogits, int64_t ld_out, flp_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The backward over a buffer of columns [y_off, y_off + v) of a
+// v_total-column vocabulary (unsharded: 0 and v).
+flp_status backward_impl(const void* logits, int dtype, int64_t n, int64_t v, int64_t ld, int64_t y_off,
+                         int64_t v_total, const int64_t* targets, int64_t ignore_index,
+                         const uint8_t* active_mask, float inv_temperature, const float* lse,
+                         const float* lse_lo, const float* grad, void* dlogits, int64_t ld_out,
+                         flp_stream_t stream) {
     flp_status st;
     if ((st = check_dtype(dtype)) != FLP_OK) return st;
     if ((st = check_scale(inv_temperature)) != FLP_OK) return st;
     if (n < 0) return fail(FLP_EINVAL, "n must be >= 0 (got %lld)", (long long)n);
     if (v < 1) return fail(FLP_EINVAL, "v must be >= 1 (got %lld)", (long long)v);
+    if (y_off < 0 || y_off > v_total - v)
+        return fail(FLP_EINVAL, "the columns [%lld, %lld) must lie inside the vocabulary [0, %lld)",
+                    (long long)y_off, (long long)(y_off + v), (long long)v_total);
     if (ld < v) return fail(FLP_EINVAL, "ld (%lld) must be >= v (%lld)", (long long)ld, (long long)v);
     if (ld_out < v)
         return fail(FLP_EINVAL, "ld_out (%lld) must be >= v (%lld)", (long long)ld_out, (long long)v);
@@ -628,12 +646,130 @@ flp_status fused_logp_backward_ex(const void* logits, int dtype, int64_t n, int6
     const BwdArgs a{logits, n, v, ld, targets, ignore_index, active_mask, inv_temperature,
                     1.f / inv_temperature, lse, lse_lo, grad, dlogits, ld_out,
                     reinterpret_cast<cudaStream_t>(stream), rows_aligned16(logits, ld, dtype),
-                    rows_aligned16(dlogits, ld_out, dtype), in_place};
+                    rows_aligned16(dlogits, ld_out, dtype), in_place, y_off, v_total};
     const dim3 grid((unsigned)segs, (unsigned)(n < 65535 ? n : 65535));
     if (dtype == FLP_DTYPE_BF16) launch_backward_d<flp::Dt::BF16>(a, grid);
     else if (dtype == FLP_DTYPE_F16) launch_backward_d<flp::Dt::F16>(a, grid);
     else launch_backward_d<flp::Dt::F32>(a, grid);
     return check_launch("backward");
+}
+
+// Tile -> rank table of a vocabulary-parallel group: 4 bits per tile.  Every
+// rank's shard must lie on the tile grid, and together they must cover each
+// of the ceil(v_total / W) tiles exactly once.
+flp_status tile_rank_table(int64_t world, const int64_t* starts, const int64_t* widths, int64_t v_total,
+                           uint64_t* table) {
+    if (world < 1 || world > flp::kTiles)
+        return fail(FLP_EINVAL, "world must be in [1, %d] (got %lld)", flp::kTiles, (long long)world);
+    if (starts == nullptr || widths == nullptr) return fail(FLP_EINVAL, "vocab_starts and real_widths are null");
+    const int64_t W = tile_width(v_total);
+    const int64_t n_tiles = ceil_div(v_total, W);
+    int owner[flp::kTiles];
+    for (int k = 0; k < flp::kTiles; ++k) owner[k] = -1;
+    for (int64_t r = 0; r < world; ++r) {
+        const int64_t a = starts[r], w = widths[r];
+        if (w < 1 || a < 0 || a > v_total - w)
+            return fail(FLP_EINVAL, "rank %lld: shard [%lld, %lld) is not inside [0, %lld)", (long long)r,
+                        (long long)a, (long long)(a + w), (long long)v_total);
+        if (a % W != 0 || (a + w != v_total && w % W != 0))
+            return fail(FLP_EUNSUPPORTED, "rank %lld: shard [%lld, %lld) is off the %lld-column tile grid",
+                        (long long)r, (long long)a, (long long)(a + w), (long long)W);
+        for (int64_t k = a / W; k < ceil_div(a + w, W); ++k) {
+            if (owner[k] >= 0)
+                return fail(FLP_EINVAL, "tile %lld is held by rank %d and rank %lld", (long long)k, owner[k],
+                            (long long)r);
+            owner[k] = (int)r;
+        }
+    }
+    uint64_t t = 0;
+    for (int64_t k = 0; k < n_tiles; ++k) {
+        if (owner[k] < 0)
+            return fail(FLP_EINVAL, "tile %lld (columns [%lld, %lld)) is held by no rank", (long long)k,
+                        (long long)(k * W), (long long)((k + 1) * W < v_total ? (k + 1) * W : v_total));
+        t |= (uint64_t)owner[k] << (4 * k);
+    }
+    *table = t;
+    return FLP_OK;
+}
+
+flp_status merge_impl(const float* part_max, const float* part_sum, const float* sel, int64_t rank_stride,
+                      uint64_t tile_rank, const int64_t* targets, int64_t ignore_index,
+                      const uint8_t* active_mask, int64_t n, int64_t v_total, float inv_temperature, float* logp,
+                      float* lse, float* lse_lo, flp_stream_t stream) {
+    const void* ptrs[] = {part_max, part_sum, sel, targets, logp, lse, lse_lo, active_mask};
+    const char* names[] = {"part_max", "part_sum", "sel", "targets", "logp", "lse", "lse_lo", "active_mask"};
+    const bool optional[] = {false, false, false, false, false, false, true, true};
+    int dev;
+    flp_status st;
+    if ((st = common_device(8, ptrs, names, optional, &dev)) != FLP_OK) return st;
+    DeviceGuard guard;
+    if ((st = guard.enter(dev)) != FLP_OK) return st;
+
+    const int64_t W = tile_width(v_total);
+    const int n_tiles = (int)ceil_div(v_total, W);
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t rows_per_block = 256 / 16;
+    flp::k_logp_merge<<<grid_for(ceil_div(n, rows_per_block)), 256, 0, s>>>(
+        part_max, part_sum, sel, targets, ignore_index, active_mask, n, v_total, n_tiles, inv_temperature, logp,
+        lse, lse_lo, rank_stride, tile_rank, W);
+    return check_launch("merge");
+}
+
+}  // namespace
+
+extern "C" {
+
+flp_status fused_logp_backward_ex(const void* logits, int dtype, int64_t n, int64_t v, int64_t ld,
+                                  const int64_t* targets, int64_t ignore_index,
+                                  const uint8_t* active_mask, float inv_temperature,
+                                  const float* lse, const float* lse_lo, const float* grad,
+                                  void* dlogits, int64_t ld_out, flp_stream_t stream) {
+    return backward_impl(logits, dtype, n, v, ld, 0, v, targets, ignore_index, active_mask, inv_temperature, lse,
+                         lse_lo, grad, dlogits, ld_out, stream);
+}
+
+flp_status logp_shard_backward_ex(const void* shard_logits, int dtype, int64_t n, int64_t ld_shard,
+                                  int64_t vocab_start, int64_t real_width, int64_t v_total,
+                                  const int64_t* targets, int64_t ignore_index, const uint8_t* active_mask,
+                                  float inv_temperature, const float* lse, const float* lse_lo,
+                                  const float* grad, void* dshard, int64_t ld_out, flp_stream_t stream) {
+    if (v_total < 1) return fail(FLP_EINVAL, "v_total must be >= 1 (got %lld)", (long long)v_total);
+    if (real_width < 1) return fail(FLP_EINVAL, "real_width must be >= 1 (got %lld)", (long long)real_width);
+    return backward_impl(shard_logits, dtype, n, real_width, ld_shard, vocab_start, v_total, targets,
+                         ignore_index, active_mask, inv_temperature, lse, lse_lo, grad, dshard, ld_out, stream);
+}
+
+flp_status logp_shard_backward(const void* shard_logits, int64_t n, int64_t ld_shard, int64_t vocab_start,
+                               int64_t real_width, int64_t v_total, const int64_t* targets, int64_t ignore_index,
+                               const float* lse, const float* lse_lo, const float* grad, void* dshard,
+                               int64_t ld_out, flp_stream_t stream) {
+    return logp_shard_backward_ex(shard_logits, FLP_DTYPE_BF16, n, ld_shard, vocab_start, real_width, v_total,
+                                  targets, ignore_index, nullptr, 1.f, lse, lse_lo, grad, dshard, ld_out, stream);
+}
+
+flp_status logp_merge_gathered_partials_ex(const float* gathered, int64_t rank_stride, int64_t world,
+                                           const int64_t* vocab_starts, const int64_t* real_widths,
+                                           const int64_t* targets, int64_t ignore_index,
+                                           const uint8_t* active_mask, int64_t n, int64_t v_total,
+                                           float inv_temperature, float* logp, float* lse, float* lse_lo,
+                                           flp_stream_t stream) {
+    flp_status st;
+    if ((st = check_scale(inv_temperature)) != FLP_OK) return st;
+    if (n < 0) return fail(FLP_EINVAL, "n must be >= 0 (got %lld)", (long long)n);
+    if (v_total < 1) return fail(FLP_EINVAL, "v_total must be >= 1");
+    uint64_t table = 0;
+    if ((st = tile_rank_table(world, vocab_starts, real_widths, v_total, &table)) != FLP_OK) return st;
+    int64_t block;
+    if (__builtin_mul_overflow(n, (int64_t)(2 * flp::kTiles + 1), &block))
+        return fail(FLP_EINVAL, "partials extent overflows int64");
+    if (world > 1 && rank_stride < block)
+        return fail(FLP_EINVAL, "rank_stride (%lld) is below one rank's %lld floats of partials",
+                    (long long)rank_stride, (long long)block);
+    if (world == 1) rank_stride = 0;
+    if (n == 0) return ok();
+    if (gathered == nullptr) return fail(FLP_EINVAL, "gathered is a null pointer");
+    return merge_impl(gathered, gathered + flp::kTiles * n, gathered + 2 * flp::kTiles * n, rank_stride, table,
+                      targets, ignore_index, active_mask, n, v_total, inv_temperature, logp, lse, lse_lo, stream);
 }
 
 flp_status fused_logp_backward(const void* logits, int64_t n, int64_t v, int64_t ld,
@@ -705,22 +841,8 @@ flp_status logp_merge_partials_ex(const float* part_max, const float* part_sum, 
     if (n < 0) return fail(FLP_EINVAL, "n must be >= 0 (got %lld)", (long long)n);
     if (v_total < 1) return fail(FLP_EINVAL, "v_total must be >= 1");
     if (n == 0) return ok();
-    const void* ptrs[] = {part_max, part_sum, sel, targets, logp, lse, lse_lo, active_mask};
-    const char* names[] = {"part_max", "part_sum", "sel", "targets", "logp", "lse", "lse_lo", "active_mask"};
-    const bool optional[] = {false, false, false, false, false, false, true, true};
-    int dev;
-    if ((st = common_device(8, ptrs, names, optional, &dev)) != FLP_OK) return st;
-    DeviceGuard guard;
-    if ((st = guard.enter(dev)) != FLP_OK) return st;
-
-    const int64_t W = tile_width(v_total);
-    const int n_tiles = (int)ceil_div(v_total, W);
-    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int64_t rows_per_block = 256 / 16;
-    flp::k_logp_merge<<<grid_for(ceil_div(n, rows_per_block)), 256, 0, s>>>(
-        part_max, part_sum, sel, targets, ignore_index, active_mask, n, v_total, n_tiles,
-        inv_temperature, logp, lse, lse_lo);
-    return check_launch("merge");
+    return merge_impl(part_max, part_sum, sel, 0, 0, targets, ignore_index, active_mask, n, v_total,
+                      inv_temperature, logp, lse, lse_lo, stream);
 }
 
 flp_status logp_merge_partials(const float* part_max, const float* part_sum, const float* sel,

@@ -561,28 +561,37 @@ k_logp_partials(const void* __restrict__ xs, int64_t n, int64_t ld, int64_t real
 }
 
 // Merge of tile partials: one half warp per row, the same tile_fold16 and
-// finalize_row as the forward.
+// finalize_row as the forward.  The partials may come from several ranks of
+// a vocabulary-parallel group, gathered side by side: rank r's [n, 16] maxima,
+// [n, 16] sums and [n] selected logits start rank_stride floats after rank
+// r - 1's, and tile k is read from rank (tile_rank >> 4k) & 15, the rank that
+// reduced it; the selected logit of row t from the rank owning the tile of
+// its target, y_t / W.  On one GPU (all shards writing one buffer) the stride
+// and the table are 0.  Only transport differs, so the bits are the same.
 __global__ void __launch_bounds__(256)
 k_logp_merge(const float* __restrict__ pm, const float* __restrict__ ps,
              const float* __restrict__ sel, const int64_t* __restrict__ y, int64_t ignore_index,
              const uint8_t* __restrict__ mask, int64_t n, int64_t v, int n_tiles, float s,
-             float* __restrict__ logp, float* __restrict__ lse, float* __restrict__ lse_lo) {
+             float* __restrict__ logp, float* __restrict__ lse, float* __restrict__ lse_lo,
+             int64_t rank_stride, uint64_t tile_rank, int64_t W) {
     const int lane = threadIdx.x & 31, k = lane & 15;
     const int64_t warp_g = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int64_t my_off = (int64_t)((tile_rank >> (4 * k)) & 15u) * rank_stride;
     for (int64_t pair = warp_g; 2 * pair < n; pair += n_warps) {
         const int64_t t = 2 * pair + (lane >> 4);
         const bool valid = t < n;
         MS p{-INFINITY, 0.f};
         if (valid && k < n_tiles) {
-            p.m = __ldg(pm + t * kTiles + k);
-            p.s = __ldg(ps + t * kTiles + k);
+            p.m = __ldg(pm + my_off + t * kTiles + k);
+            p.s = __ldg(ps + my_off + t * kTiles + k);
         }
         const MS f = tile_fold16(p, s);
         if (valid && k == 0) {
             const int64_t yt = __ldg(y + t);
             const bool act = row_active(mask, t, yt, v, ignore_index);
-            const float x_y = act ? __ldg(sel + t) : 0.f;
+            const int64_t owner = act ? (int64_t)((tile_rank >> (4 * (int)(yt / W))) & 15u) : 0;
+            const float x_y = act ? __ldg(sel + owner * rank_stride + t) : 0.f;
             finalize_row(f, act, x_y, s, logp + t, lse + t, lse_lo ? lse_lo + t : nullptr);
         }
     }
@@ -736,12 +745,19 @@ __device__ __forceinline__ void bwd_store(char* dr, int64_t col, int64_t v,
 // without cancellation.  Values below 2^-126 flush to zero.  Each thread loads
 // its eight units before computing any, so eight (FP32: sixteen) 16-byte loads
 // are in flight per thread.
+//
+// Vocabulary shards: the buffer holds global columns [y_off, y_off + v) of a
+// v_total-column vocabulary (unsharded: y_off = 0, v_total = v).  A row is
+// active by its global target (in [0, v_total)); the one-hot term lands on
+// local column y_t - y_off only when that lies in [0, v).  Every element is
+// computed from the same per-row constants as in the unsharded call, so the
+// shards' outputs side by side are the unsharded gradient bit for bit.
 template <Dt D, bool kVecIn, bool kVecOut, bool kInPlace>
 __global__ void __launch_bounds__(kBwdThreads, kBwdMinBlocks<D>)
 k_logp_bwd(const void* x, int64_t n, int64_t v, int64_t ld, const int64_t* __restrict__ y,
            int64_t ignore_index, const uint8_t* __restrict__ mask, float s, float inv_s,
            const float* __restrict__ lse, const float* __restrict__ lse_lo,
-           const float* __restrict__ g, void* dx, int64_t ld_out) {
+           const float* __restrict__ g, void* dx, int64_t ld_out, int64_t y_off, int64_t v_total) {
     constexpr int EB = Unit<D>::kElemBytes;
     constexpr int NW = Unit<D>::kWords;
     // grid: x = segment of the row, y = row (strided when n > gridDim.y)
@@ -752,7 +768,7 @@ k_logp_bwd(const void* x, int64_t n, int64_t v, int64_t ld, const int64_t* __res
         char* dr = reinterpret_cast<char*>(dx) + t * ld_out * EB;
         const int64_t yt = __ldg(y + t);
         const int64_t cs = (int64_t)kBwdThreads * 8;
-        if (!row_active(mask, t, yt, v, ignore_index)) {
+        if (!row_active(mask, t, yt, v_total, ignore_index)) {
             uint32_t z[NW];
 #pragma unroll
             for (int k = 0; k < NW; ++k) z[k] = 0u;
@@ -789,7 +805,7 @@ k_logp_bwd(const void* x, int64_t n, int64_t v, int64_t ld, const int64_t* __res
         for (int u = 0; u < kBwdUnitsPerThread; ++u) {
             if (col0 + u * cs < v) {
                 uint32_t o[NW];
-                bwd_unit<D>(w[u], r, yt - (col0 + u * cs), o);
+                bwd_unit<D>(w[u], r, yt - y_off - (col0 + u * cs), o);
                 bwd_store<D, kVecOut>(dr, col0 + u * cs, v, o);
             }
         }

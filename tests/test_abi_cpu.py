@@ -299,3 +299,39 @@ def test_grpo_host_checks(lib):
     assert call(ws_bytes=8) == EINVAL and b"workspace" in lib.flp_last_error()
     assert call(ws=(1 << 20) + 8) == EINVAL
     assert call() == EINVAL                            # host pointers are not device memory
+
+
+def test_gathered_merge_validates_the_rank_layout_on_the_host(lib):
+    """The tile -> rank table of a vocabulary-parallel merge is checked before
+    any device access: shards off the tile grid, a gap, an overlap, too many
+    ranks, a short rank stride."""
+    v, w = 151936, 9496
+    I64 = ctypes.c_int64
+
+    def call(starts, widths, n=4, stride=None, world=None):
+        k = len(starts)
+        a = (I64 * max(1, k))(*starts)
+        b = (I64 * max(1, k))(*widths)
+        return lib.logp_merge_gathered_partials_ex(None, 33 * n if stride is None else stride,
+                                                   k if world is None else world, a, b, None, -100, None, n, v,
+                                                   1.0, None, None, None, None)
+
+    assert call([0, 8 * w + 8], [8 * w + 8, v - 8 * w - 8]) == EUNSUP
+    assert b"tile grid" in lib.flp_last_error()
+    assert call([0, 9 * w], [8 * w, v - 9 * w]) == EINVAL
+    assert b"held by no rank" in lib.flp_last_error()
+    assert call([0, 7 * w], [8 * w, v - 7 * w]) == EINVAL
+    assert b"held by rank 0 and rank 1" in lib.flp_last_error()
+    assert call([k * w for k in range(16)] + [0], [w] * 17) == EINVAL
+    assert call([0, 8 * w], [8 * w, v - 8 * w], stride=33 * 4 - 1) == EINVAL
+    assert b"rank_stride" in lib.flp_last_error()
+    # a correct layout with n == 0 returns before touching the device
+    assert call([0, 8 * w], [8 * w, v - 8 * w], n=0) == 0
+
+
+def test_shard_backward_validates_the_shard_on_the_host(lib):
+    st = lib.logp_shard_backward(None, 4, 100, 151900, 100, 151936, None, -100, None, None, None, None, 100,
+                                 None)
+    assert st == EINVAL and b"inside the vocabulary" in lib.flp_last_error()
+    assert lib.logp_shard_backward(None, 0, 100, 0, 100, 151936, None, -100, None, None, None, None, 100,
+                                   None) == 0

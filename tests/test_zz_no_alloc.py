@@ -63,3 +63,46 @@ def test_noalloc_refuses_more_than_its_scratch():
     assert b"16777216" in lib.flp_last_error()
     with pytest.raises(flp.FusedLogpError, match="scratch"):
         flp.fused_linear_logp_forward_noalloc(h, w, y, outs[0], outs[1])
+
+
+def test_noalloc_largest_accepted_call_matches_workspace_entry_point():
+    """3527 rows at V = 151936 need 16,774,656 of the array's 16,777,216
+    bytes, so the last rows' partials sit at its end; two calls in a row give
+    the workspace entry point's bits."""
+    lib = _lib.load(build_if_missing=True)
+    n, d, v = 3527, 256, workloads.QWEN3_VOCAB
+    assert flp.fused_linear_logp_workspace_size(n, v) <= 16 << 20 < flp.fused_linear_logp_workspace_size(n + 1, v)
+    h, w, y = workloads.linear(n, d, v, seed=13, device=DEV)
+    for _ in range(2):
+        outs = [torch.full((n,), float("nan"), device=DEV) for _ in range(3)]
+        assert _call_noalloc(lib, h, w, y, outs, 1.0) == 0, lib.flp_last_error()
+        ref = flp.fused_linear_logp_forward(h, w, y, with_lse_lo=True)
+        torch.cuda.synchronize()
+        for got, want in zip(outs, ref):
+            assert torch.equal(got.view(torch.int32), want.view(torch.int32))
+    assert flp.flp_device_error(0) == 0
+
+
+def test_noalloc_calls_leave_device_memory_unchanged():
+    """After one warm-up call per shape (which loads the kernels), further
+    calls of several shapes change neither the device's free memory nor
+    torch's allocated bytes."""
+    lib = _lib.load(build_if_missing=True)
+    shapes = [(1000, 512, workloads.QWEN3_VOCAB), (77, 64, 3000), (2048, 128, 20000)]
+    cases = []
+    for k, (n, d, v) in enumerate(shapes):
+        h, w, y = workloads.linear(n, d, v, seed=40 + k, device=DEV)
+        outs = [torch.empty(n, device=DEV) for _ in range(3)]
+        cases.append((h, w, y, outs))
+    for h, w, y, outs in cases:
+        assert _call_noalloc(lib, h, w, y, outs, 1.0) == 0
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    alloc0 = torch.cuda.memory_allocated()
+    for _ in range(3):
+        for h, w, y, outs in cases:
+            assert _call_noalloc(lib, h, w, y, outs, 0.8) == 0
+            flp.fused_linear_logp_forward_noalloc(h, w, y, outs[0], outs[1], lse_lo=outs[2])
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert torch.cuda.memory_allocated() == alloc0
