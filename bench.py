@@ -682,8 +682,9 @@ def run_grpo(args):
 
 def _linear_backward_timing(args, flp, h, w, y, lse, lse_lo, dev, stream):
     """The fused LM-head backward (dZ recomputed on the tensor cores per
-    4096-row chunk, dH and dW as two library GEMMs): 3 contractions of 2 N V D
-    FLOP each, timed separately from the forward's metric."""
+    4096-row chunk, then dH = dZ W and dW = dZ^T H on the library's own
+    tensor-core contraction kernel): 3 contractions of 2 N V D FLOP each,
+    timed separately from the forward's metric."""
     import torch
 
     n, d = h.shape
@@ -713,7 +714,8 @@ def _linear_backward_timing(args, flp, h, w, y, lse, lse_lo, dev, stream):
     return {"ms": round(ms, 3), "tflops": round(tf, 1), "frac": round(tf / burst, 4),
             "frac_of_sustained": round(tf / sustained, 4), "steps": args.linear_bwd_steps,
             "flop_per_call": 3 * 2.0 * n * v * d,
-            "kernels": "k_linear_logp_tiles<grad> (dZ, BF16) + 2 library GEMMs per 4096-row chunk"}
+            "kernels": "per 4096-row chunk: k_linear_logp_tiles<grad> (dZ, BF16), k_gemm_bf16 (dH, 5 K splits) + "
+                        "k_gemm_split_sum, k_gemm_bf16 (dW)"}
 
 
 def _linear_e2e(args, flp, h, w, y, ws, dev, stream, world):

@@ -330,26 +330,30 @@ flp_status fused_linear_logp_merge(const void* workspace, int64_t workspace_byte
  * with dZ recomputed on the tensor cores from hidden and weight and the
  * forward's lse (+ lse_lo) and written in BF16 (as the method writes dlogits)
  * one chunk of 4096 rows at a time into the workspace, never as an [n, v]
- * tensor; the two products are plain GEMMs on the GPU's GEMM library (FP32
- * accumulation, no atomic split-K reduction: deterministic).
+ * tensor.  The two products run on this library's own tensor-core kernels,
+ * reading dZ, W and H where they lie (FP32 accumulation): dhidden in
+ * S = ceil(ceil(v / 64) / 512) fixed splits of the vocabulary added in split
+ * order, dweight added chunk after chunk in row order.  No atomics:
+ * deterministic.
  *   hidden, weight, targets, ignore_index, active_mask, inv_temperature: as
  *             for fused_linear_logp_forward (the same call's arguments)
  *   lse       [n] FP32, lse_lo [n] FP32 or NULL: the forward's outputs
  *   grad      [n] FP32 d loss / d logp (0 for inactive rows by definition)
  *   workspace device scratch of fused_linear_logp_backward_workspace_size
  *             bytes (256-byte aligned), caller-owned: dZ [4096, ceil(v/8)*8]
- *             BF16, a [4096, d] FP32 block, 32 MiB for the GEMM library
+ *             BF16 and, when S > 1, the splits' partial dhidden
+ *             [S, 4096, d] FP32
  *   dhidden   [n, ld_dh] FP32 out
  *   dweight   [v, ld_dw] FP32: overwritten with dZ^T H when
  *             accumulate_dweight == 0 (all zero when n == 0), or with
  *             dweight + dZ^T H when it is nonzero (gradient accumulation over
  *             micro-batches; unchanged when n == 0).  With n == 0 only dweight
  *             is touched and the workspace may be NULL.
- * Every chunk has the same shape (the last one padded with zero-gradient
- * rows), so a row's dhidden does not depend on n or on its position.
+ * Each element of dhidden is a tensor-core dot product over the vocabulary
+ * with split points fixed by v, whatever else the chunk holds, so a row's
+ * dhidden does not depend on n or on its position.
  * Requirements and errors as for the forward, plus ld_dh, ld_dw >= d.
- * Asynchronous on `stream`; the library allocates no device memory (the GEMM
- * library's handle is created once per device).
+ * Asynchronous on `stream`; the library allocates nothing.
  */
 flp_status fused_linear_logp_backward_workspace_size(int64_t d, int64_t v, int64_t* bytes);
 flp_status fused_linear_logp_backward(const void* hidden, int64_t n, int64_t d, int64_t ld_h, const void* weight,

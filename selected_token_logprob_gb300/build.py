@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libfused_logp.so")
 SOURCES = [os.path.join(CSRC, "fused_logp.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("logp_kernels.cuh", "logp_prims.cuh",
-                                                  "grpo_kernels.cuh", "linear_logp.cuh")] + [os.path.join(INCLUDE, "fused_logp.h")]
+                                                  "grpo_kernels.cuh", "linear_logp.cuh", "gemm_bf16.cuh")] + [os.path.join(INCLUDE, "fused_logp.h")]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 
@@ -31,7 +31,7 @@ def nvcc() -> str:
 
 def command(out: str) -> list[str]:
     return [nvcc(), ARCH, "-lineinfo", "-O3", "-std=c++17", "-Xptxas", "-v",
-            "-I" + INCLUDE, "-Xcompiler", "-fPIC", "-shared", *SOURCES, "-o", out, "-lcublasLt"]
+            "-I" + INCLUDE, "-Xcompiler", "-fPIC", "-shared", *SOURCES, "-o", out]
 
 
 def stale() -> bool:

@@ -2,7 +2,6 @@
 // configuration and the extern "C" entry points declared in
 // include/fused_logp.h.  All checks run on the host before any launch and
 // report through the return code (no device-side traps).
-#include <cublasLt.h>
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -12,6 +11,7 @@
 #include <stdio.h>
 
 #include "fused_logp.h"
+#include "gemm_bf16.cuh"
 #include "grpo_kernels.cuh"
 #include "linear_logp.cuh"
 #include "logp_kernels.cuh"
@@ -339,86 +339,75 @@ flp_status linear_setup(int dev) {
     return FLP_OK;
 }
 
-// ---- fused LM head backward: row chunks and the two plain GEMMs
+// ---- fused LM head backward: row chunks and the two tensor-core products
 
-// Rows per chunk of the backward: every chunk (the last one padded with zero
-// gradient rows) has this shape, so a row's dH does not depend on the batch.
+// Rows per chunk of the backward: dZ is materialised for one chunk at a time.
+// Every row's dZ and dH are computed the same way whatever the chunk holds.
 constexpr int64_t kLinGradChunk = 4096;
-constexpr int64_t kLtWorkspaceBytes = (int64_t)32 << 20;
+// K blocks of 64 per split of the dH product (K = the vocabulary): enough
+// splits that the (split, tile) units fill the SMs in near-whole waves.
+constexpr int64_t kGemmSplitKBlocks = 512;
 
 int64_t align256(int64_t b) { return ceil_div(b, 256) * 256; }
 
-// Backward workspace: dZ [chunk, ld_dz] BF16, a dH chunk [chunk, d] FP32 for
-// the last (padded) chunk, and the GEMM library's workspace.
-bool linear_grad_workspace(int64_t d, int64_t v, int64_t* ld_dz, int64_t* off_dh, int64_t* off_lt,
-                           int64_t* total) {
+// K splits of dH = dZ W for a v-column vocabulary: a function of v only.
+int dh_splits(int64_t v) {
+    const int64_t s = ceil_div(ceil_div(v, flp::kGemmBK), kGemmSplitKBlocks);
+    return (int)(s < 1 ? 1 : s);
+}
+
+// Backward workspace: dZ [chunk, ld_dz] BF16, then (with more than one K
+// split) the splits' partial dH [splits, chunk, d] FP32.
+bool linear_grad_workspace(int64_t d, int64_t v, int64_t* ld_dz, int64_t* off_dh, int64_t* total) {
     const int64_t ld = ceil_div(v, 8) * 8;
-    int64_t a, b;
+    const int64_t splits = dh_splits(v);
+    int64_t a, b = 0;
     if (__builtin_mul_overflow(kLinGradChunk, ld, &a) || __builtin_mul_overflow(a, (int64_t)2, &a)) return false;
-    if (__builtin_mul_overflow(kLinGradChunk, d, &b) || __builtin_mul_overflow(b, (int64_t)4, &b)) return false;
+    if (splits > 1 && (__builtin_mul_overflow(kLinGradChunk, d, &b) || __builtin_mul_overflow(b, splits * 4, &b)))
+        return false;
     *ld_dz = ld;
     *off_dh = align256(a);
-    *off_lt = *off_dh + align256(b);
-    *total = *off_lt + kLtWorkspaceBytes;
+    *total = *off_dh + align256(b);
     return true;
 }
 
-cublasLtHandle_t lt_handle(int dev) {
-    static cublasLtHandle_t handles[kMaxDevices];
-    if (handles[dev] == nullptr) {
-        cublasLtHandle_t h = nullptr;
-        if (cublasLtCreate(&h) != CUBLAS_STATUS_SUCCESS) return nullptr;
-        handles[dev] = h;
+flp_status gemm_setup(int dev) {
+    static std::atomic<bool> ready[kMaxDevices];
+    if (!ready[dev].load(std::memory_order_acquire)) {
+        cudaError_t e = cudaFuncSetAttribute(flp::k_gemm_bf16<false, true>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)flp::kGemmSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(flp::k_gemm_bf16<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)flp::kGemmSmemBytes);
+        if (e != cudaSuccess) return fail(FLP_ECUDA, "contraction setup: %s", cudaGetErrorString(e));
+        ready[dev].store(true, std::memory_order_release);
     }
-    return handles[dev];
+    return FLP_OK;
 }
 
-// C (m x n, FP32, column-major, ldc) = op(A) op(B) + beta C with A, B BF16
-// column-major: a plain GEMM on the library, FP32 accumulation, no in-place
-// (atomic) split-K reduction, so the result is deterministic.
-flp_status lt_gemm(cublasLtHandle_t lt, cublasOperation_t opa, cublasOperation_t opb, int64_t m, int64_t n,
-                   int64_t k, const void* A, int64_t lda, const void* B, int64_t ldb, float beta, float* C,
-                   int64_t ldc, void* ws, cudaStream_t stream, const char* what) {
-    cublasLtMatmulDesc_t op = nullptr;
-    cublasLtMatrixLayout_t la = nullptr, lb = nullptr, lc = nullptr;
-    cublasLtMatmulPreference_t pref = nullptr;
-    cublasStatus_t st = cublasLtMatmulDescCreate(&op, CUBLAS_COMPUTE_32F, CUDA_R_32F);
-    if (st == CUBLAS_STATUS_SUCCESS)
-        st = cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSA, &opa, sizeof opa);
-    if (st == CUBLAS_STATUS_SUCCESS)
-        st = cublasLtMatmulDescSetAttribute(op, CUBLASLT_MATMUL_DESC_TRANSB, &opb, sizeof opb);
-    if (st == CUBLAS_STATUS_SUCCESS)
-        st = cublasLtMatrixLayoutCreate(&la, CUDA_R_16BF, opa == CUBLAS_OP_N ? m : k, opa == CUBLAS_OP_N ? k : m,
-                                        lda);
-    if (st == CUBLAS_STATUS_SUCCESS)
-        st = cublasLtMatrixLayoutCreate(&lb, CUDA_R_16BF, opb == CUBLAS_OP_N ? k : n, opb == CUBLAS_OP_N ? n : k,
-                                        ldb);
-    if (st == CUBLAS_STATUS_SUCCESS) st = cublasLtMatrixLayoutCreate(&lc, CUDA_R_32F, m, n, ldc);
-    if (st == CUBLAS_STATUS_SUCCESS) st = cublasLtMatmulPreferenceCreate(&pref);
-    const uint64_t wsb = (uint64_t)kLtWorkspaceBytes;
-    const uint32_t schemes = CUBLASLT_REDUCTION_SCHEME_NONE | CUBLASLT_REDUCTION_SCHEME_COMPUTE_TYPE |
-                             CUBLASLT_REDUCTION_SCHEME_OUTPUT_TYPE;
-    if (st == CUBLAS_STATUS_SUCCESS)
-        st = cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES, &wsb, sizeof wsb);
-    if (st == CUBLAS_STATUS_SUCCESS)
-        st = cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_REDUCTION_SCHEME_MASK, &schemes,
-                                                  sizeof schemes);
-    cublasLtMatmulHeuristicResult_t heur{};
-    int found = 0;
-    if (st == CUBLAS_STATUS_SUCCESS)
-        st = cublasLtMatmulAlgoGetHeuristic(lt, op, la, lb, lc, lc, pref, 1, &heur, &found);
-    if (st == CUBLAS_STATUS_SUCCESS && found < 1) st = CUBLAS_STATUS_NOT_SUPPORTED;
-    const float alpha = 1.f;
-    if (st == CUBLAS_STATUS_SUCCESS)
-        st = cublasLtMatmul(lt, op, &alpha, A, la, B, lb, &beta, C, lc, C, lc, &heur.algo, ws, kLtWorkspaceBytes,
-                            stream);
-    if (pref) cublasLtMatmulPreferenceDestroy(pref);
-    if (lc) cublasLtMatrixLayoutDestroy(lc);
-    if (lb) cublasLtMatrixLayoutDestroy(lb);
-    if (la) cublasLtMatrixLayoutDestroy(la);
-    if (op) cublasLtMatmulDescDestroy(op);
-    if (st != CUBLAS_STATUS_SUCCESS) return fail(FLP_ECUDA, "%s: GEMM library status %d", what, (int)st);
-    return FLP_OK;
+// C (+)= A B on the tensor cores: M x N output, K-extent k, `splits` K splits
+// written split_stride floats apart.  A is K-major (kAmn = false) or MN-major,
+// B is MN-major; the tensor maps carry the operands' layouts.
+template <bool kAmn>
+flp_status gemm_launch(int sms, const CUtensorMap& tm_a, const CUtensorMap& tm_b, int64_t m, int64_t n, int64_t k,
+                       int splits, float* c, int64_t ldc, int64_t split_stride, bool accumulate, cudaStream_t s,
+                       const char* what) {
+    flp::GemmArgs g;
+    g.M = m;
+    g.N = n;
+    g.nmb = (int)ceil_div(m, flp::kGemmBM);
+    g.nnb = (int)ceil_div(n, flp::kGemmBN);
+    g.nkb = (int)ceil_div(k, flp::kGemmBK);
+    g.splits = splits;
+    g.C = c;
+    g.ldc = ldc;
+    g.split_stride = split_stride;
+    g.accumulate = accumulate ? 1 : 0;
+    g.vec = (aligned16(c) && ldc % 4 == 0 && split_stride % 4 == 0) ? 1 : 0;
+    const int64_t units = (int64_t)g.nmb * g.nnb * splits;
+    const int grid = (int)(units < sms ? units : sms);
+    flp::k_gemm_bf16<kAmn, true><<<grid, flp::kGemmThreads, flp::kGemmSmemBytes, s>>>(tm_a, tm_b, g);
+    return check_launch(what);
 }
 
 int64_t linear_vocab_tiles(int64_t v) { return ceil_div(v, flp::kLinBN); }
@@ -981,8 +970,8 @@ flp_status fused_linear_logp_merge(const void* workspace, int64_t workspace_byte
 flp_status fused_linear_logp_backward_workspace_size(int64_t d, int64_t v, int64_t* bytes) {
     if (bytes == nullptr) return fail(FLP_EINVAL, "bytes is a null pointer");
     if (d < 1 || v < 1) return fail(FLP_EINVAL, "d and v must be >= 1");
-    int64_t ld, off_dh, off_lt;
-    if (!linear_grad_workspace(d, v, &ld, &off_dh, &off_lt, bytes))
+    int64_t ld, off_dh;
+    if (!linear_grad_workspace(d, v, &ld, &off_dh, bytes))
         return fail(FLP_EINVAL, "workspace size overflows int64");
     return ok();
 }
@@ -1035,8 +1024,8 @@ flp_status linear_backward_impl(const void* hidden, int64_t n, int64_t d, int64_
         if (e != cudaSuccess) return fail(FLP_ECUDA, "clearing dweight: %s", cudaGetErrorString(e));
         return ok();
     }
-    int64_t ld_dz, off_dh, off_lt, need;
-    if (!linear_grad_workspace(d, v, &ld_dz, &off_dh, &off_lt, &need))
+    int64_t ld_dz, off_dh, need;
+    if (!linear_grad_workspace(d, v, &ld_dz, &off_dh, &need))
         return fail(FLP_EINVAL, "workspace size overflows int64");
     if (workspace_bytes < need)
         return fail(FLP_EINVAL, "workspace_bytes (%lld) is below the %lld bytes needed", (long long)workspace_bytes,
@@ -1054,29 +1043,33 @@ flp_status linear_backward_impl(const void* hidden, int64_t n, int64_t d, int64_
     if ((st = guard.enter(dev)) != FLP_OK) return st;
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if ((st = linear_setup(dev)) != FLP_OK) return st;
-    cublasLtHandle_t lt = lt_handle(dev);
-    if (lt == nullptr) return fail(FLP_ECUDA, "cannot create a GEMM library handle on device %d", dev);
+    if ((st = gemm_setup(dev)) != FLP_OK) return st;
     const int sms = sm_count(dev);
     if (sms <= 0) return fail(FLP_ECUDA, "cannot read the SM count of device %d", dev);
 
-    CUtensorMap tm_w;
+    // the weight as the dZ kernel's K-major operand and as dH's MN-major B
+    CUtensorMap tm_w, tm_w_mn;
     if ((st = make_tmap_bf16(&tm_w, weight, v, d, ld_w, flp::kLinBN, "weight")) != FLP_OK) return st;
+    if ((st = make_tmap_bf16(&tm_w_mn, weight, v, d, ld_w, 64, "weight")) != FLP_OK) return st;
     char* ws = static_cast<char*>(workspace);
     uint16_t* dz = reinterpret_cast<uint16_t*>(ws);
-    float* dh_pad = reinterpret_cast<float*>(ws + off_dh);
-    void* lt_ws = ws + off_lt;
+    float* dh_parts = reinterpret_cast<float*>(ws + off_dh);
+    const int splits = dh_splits(v);
     const int64_t nvt = linear_vocab_tiles(v);
-    const int64_t nrb = kLinGradChunk / flp::kLinBM;
-    const int64_t ntiles = nrb * nvt;
-    const int grid = (int)(ntiles < sms ? ntiles : sms);
     const char* hb = static_cast<const char*>(hidden);
     for (int64_t start = 0; start < n; start += kLinGradChunk) {
         const int64_t rows = (n - start < kLinGradChunk) ? n - start : kLinGradChunk;
         const void* h_chunk = hb + start * ld_h * 2;
-        CUtensorMap tm_h;
+        // dZ of the chunk's rows, in BF16, recomputed on the tensor cores
+        CUtensorMap tm_h, tm_h_mn, tm_dz, tm_dz_mn;
         if ((st = make_tmap_bf16(&tm_h, h_chunk, rows, d, ld_h, flp::kLinBM, "hidden")) != FLP_OK) return st;
+        if ((st = make_tmap_bf16(&tm_h_mn, h_chunk, rows, d, ld_h, 64, "hidden")) != FLP_OK) return st;
+        if ((st = make_tmap_bf16(&tm_dz, dz, rows, v, ld_dz, flp::kGemmBM, "dZ")) != FLP_OK) return st;
+        if ((st = make_tmap_bf16(&tm_dz_mn, dz, rows, v, ld_dz, 64, "dZ")) != FLP_OK) return st;
+        const int64_t nrb = ceil_div(rows, flp::kLinBM);
+        const int64_t ntiles = nrb * nvt;
         flp::LinArgs a;
-        a.n = kLinGradChunk;
+        a.n = rows;
         a.v = v;
         a.nrb = (int)nrb;
         a.nvt = (int)nvt;
@@ -1097,27 +1090,28 @@ flp_status linear_backward_impl(const void* hidden, int64_t n, int64_t d, int64_
         a.inv_s = 1.f / inv_temperature;
         a.dz = dz;
         a.ld_dz = ld_dz;
-        flp::k_linear_logp_tiles<true><<<grid, flp::kLinThreads, flp::kLinSmemBytes, s>>>(tm_h, tm_w, a);
+        flp::k_linear_logp_tiles<true><<<(int)(ntiles < sms ? ntiles : sms), flp::kLinThreads, flp::kLinSmemBytes,
+                                          s>>>(tm_h, tm_w, a);
         if ((st = check_launch("linear logp gradient tiles")) != FLP_OK) return st;
-        // dH rows = dZ W: column-major dH^T [d x chunk] = W^T [d x v] dZ^T [v x chunk], always a full chunk
-        // (a padded last chunk goes through a scratch block), or added to dhidden when accumulating
-        const bool full = rows == kLinGradChunk;
-        const bool direct = full || accumulate_dhidden;
-        float* dh_out = direct ? dhidden + start * ld_dh : dh_pad;
-        if ((st = lt_gemm(lt, CUBLAS_OP_N, CUBLAS_OP_N, d, direct ? rows : kLinGradChunk, v, weight, ld_w, dz,
-                          ld_dz, accumulate_dhidden ? 1.f : 0.f, dh_out, direct ? ld_dh : d, lt_ws, s,
-                          "dhidden")) != FLP_OK)
-            return st;
-        if (!direct) {
-            const cudaError_t e = cudaMemcpy2DAsync(dhidden + start * ld_dh, (size_t)ld_dh * 4, dh_pad,
-                                                    (size_t)d * 4, (size_t)d * 4, (size_t)rows,
-                                                    cudaMemcpyDeviceToDevice, s);
-            if (e != cudaSuccess) return fail(FLP_ECUDA, "copying dhidden: %s", cudaGetErrorString(e));
+        // dH rows = dZ W (K = the vocabulary), in fixed K splits summed in split order
+        float* dh_rows = dhidden + start * ld_dh;
+        if (splits == 1) {
+            if ((st = gemm_launch<false>(sms, tm_dz, tm_w_mn, rows, d, v, 1, dh_rows, ld_dh, 0, accumulate_dhidden != 0,
+                                         s, "dhidden product")) != FLP_OK)
+                return st;
+        } else {
+            const int64_t stride = kLinGradChunk * d;
+            if ((st = gemm_launch<false>(sms, tm_dz, tm_w_mn, rows, d, v, splits, dh_parts, d, stride, false, s,
+                                         "dhidden product")) != FLP_OK)
+                return st;
+            const int64_t blocks = ceil_div(rows * d, 256);
+            flp::k_gemm_split_sum<<<(int)(blocks < (int64_t)sms * 8 ? blocks : (int64_t)sms * 8), 256, 0, s>>>(
+                dh_parts, splits, stride, d, rows, d, dh_rows, ld_dh, accumulate_dhidden);
+            if ((st = check_launch("dhidden split sum")) != FLP_OK) return st;
         }
-        // dW (+)= dZ^T H: column-major dW^T [d x v] = H^T [d x rows] (dZ^T [v x rows])^T
-        if ((st = lt_gemm(lt, CUBLAS_OP_N, CUBLAS_OP_T, d, v, rows, h_chunk, ld_h, dz, ld_dz,
-                          (start == 0 && !accumulate_dweight) ? 0.f : 1.f, dweight, ld_dw, lt_ws, s,
-                          "dweight")) != FLP_OK)
+        // dW (+)= dZ^T H (K = the chunk's rows), added chunk after chunk in row order
+        if ((st = gemm_launch<true>(sms, tm_dz_mn, tm_h_mn, v, d, rows, 1, dweight, ld_dw, 0,
+                                    start > 0 || accumulate_dweight, s, "dweight product")) != FLP_OK)
             return st;
     }
     return ok();
