@@ -325,6 +325,22 @@ flp_status make_tmap_bf16(CUtensorMap* m, const void* ptr, int64_t rows, int64_t
     return FLP_OK;
 }
 
+// Tensor map of an FP32 row-major [rows, ld] output matrix whose first `cols`
+// columns are written: boxes of 32 x 32 with 128-byte swizzle (the layout the
+// contraction's epilogue stages).  False when the layout does not allow one
+// (base not 16-byte aligned, row stride not a multiple of 16 bytes).
+bool make_tmap_f32_out(CUtensorMap* m, void* ptr, int64_t rows, int64_t cols, int64_t ld) {
+    const EncodeTiledFn fn = encode_tiled();
+    if (!fn || !aligned16(ptr) || (ld * 4) % 16 != 0 || rows < 1 || cols < 1) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld * 4};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 flp_status linear_setup(int dev) {
     static std::atomic<bool> ready[kMaxDevices];
     if (!ready[dev].load(std::memory_order_acquire)) {
@@ -379,6 +395,18 @@ flp_status gemm_setup(int dev) {
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(flp::k_gemm_bf16<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)flp::kGemmSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(flp::k_gemm_bf16_pair<false, true, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)flp::kPairSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(flp::k_gemm_bf16_pair<true, true, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)flp::kPairSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(flp::k_gemm_bf16_pair<false, true, false>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)flp::kPairSmemBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(flp::k_gemm_bf16_pair<true, true, false>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)flp::kPairSmemBytes);
         if (e != cudaSuccess) return fail(FLP_ECUDA, "contraction setup: %s", cudaGetErrorString(e));
         ready[dev].store(true, std::memory_order_release);
     }
@@ -386,12 +414,40 @@ flp_status gemm_setup(int dev) {
 }
 
 // C (+)= A B on the tensor cores: M x N output, K-extent k, `splits` K splits
-// written split_stride floats apart.  A is K-major (kAmn = false) or MN-major,
+// written split_stride floats apart.  CTA pairs (tcgen05 cta_group::2) when a
+// pair fits on the device, else one CTA per 128 x 256 tile (same bits).  A is K-major (kAmn = false) or MN-major,
 // B is MN-major; the tensor maps carry the operands' layouts.
+// Clusters of the pair kernel that can be resident at once on `dev` (cached).
 template <bool kAmn>
-flp_status gemm_launch(int sms, const CUtensorMap& tm_a, const CUtensorMap& tm_b, int64_t m, int64_t n, int64_t k,
-                       int splits, float* c, int64_t ldc, int64_t split_stride, bool accumulate, cudaStream_t s,
-                       const char* what) {
+int pair_clusters(int dev) {
+    static std::atomic<int> count[kMaxDevices];
+    int c = count[dev].load(std::memory_order_acquire);
+    if (c == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2);
+        cfg.blockDim = dim3(flp::kGemmThreads);
+        cfg.dynamicSmemBytes = flp::kPairSmemBytes;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&c, (void*)flp::k_gemm_bf16_pair<kAmn, true, true>, &cfg) !=
+            cudaSuccess) {
+            (void)cudaGetLastError();
+            return 0;
+        }
+        count[dev].store(c, std::memory_order_release);
+    }
+    return c;
+}
+
+template <bool kAmn>
+flp_status gemm_launch(int dev, int sms, const CUtensorMap& tm_a, const CUtensorMap& tm_b, int64_t m, int64_t n,
+                       int64_t k, int splits, float* c, int64_t ldc, int64_t split_stride, int64_t c_rows,
+                       bool accumulate, cudaStream_t s, const char* what) {
     flp::GemmArgs g;
     g.M = m;
     g.N = n;
@@ -404,6 +460,25 @@ flp_status gemm_launch(int sms, const CUtensorMap& tm_a, const CUtensorMap& tm_b
     g.split_stride = split_stride;
     g.accumulate = accumulate ? 1 : 0;
     g.vec = (aligned16(c) && ldc % 4 == 0 && split_stride % 4 == 0) ? 1 : 0;
+    g.c_split_rows = (splits > 1 && ldc > 0) ? split_stride / ldc : 0;
+    g.group = 0;
+    const int fit = pair_clusters<kAmn>(dev);
+    if (fit > 0) {
+        // CTA pairs: a 256 x 256 tile per pair, as many pairs as fit at once; the
+        // output leaves through a tensor map of C (all splits' rows) when C allows one
+        const int64_t units = ceil_div(m, 256) * g.nnb * splits;
+        const int64_t pairs = units < fit ? units : fit;
+        CUtensorMap tm_c;
+        const bool tma_c = (splits == 1 || split_stride % ldc == 0) &&
+                           make_tmap_f32_out(&tm_c, c, splits > 1 ? g.c_split_rows * splits : c_rows, n, ldc);
+        if (tma_c)
+            flp::k_gemm_bf16_pair<kAmn, true, true><<<(int)(2 * pairs), flp::kGemmThreads, flp::kPairSmemBytes, s>>>(
+                tm_a, tm_b, tm_c, g);
+        else
+            flp::k_gemm_bf16_pair<kAmn, true, false><<<(int)(2 * pairs), flp::kGemmThreads, flp::kPairSmemBytes, s>>>(
+                tm_a, tm_b, tm_a, g);
+        return check_launch(what);
+    }
     const int64_t units = (int64_t)g.nmb * g.nnb * splits;
     const int grid = (int)(units < sms ? units : sms);
     flp::k_gemm_bf16<kAmn, true><<<grid, flp::kGemmThreads, flp::kGemmSmemBytes, s>>>(tm_a, tm_b, g);
@@ -1096,13 +1171,13 @@ flp_status linear_backward_impl(const void* hidden, int64_t n, int64_t d, int64_
         // dH rows = dZ W (K = the vocabulary), in fixed K splits summed in split order
         float* dh_rows = dhidden + start * ld_dh;
         if (splits == 1) {
-            if ((st = gemm_launch<false>(sms, tm_dz, tm_w_mn, rows, d, v, 1, dh_rows, ld_dh, 0, accumulate_dhidden != 0,
-                                         s, "dhidden product")) != FLP_OK)
+            if ((st = gemm_launch<false>(dev, sms, tm_dz, tm_w_mn, rows, d, v, 1, dh_rows, ld_dh, 0, rows,
+                                         accumulate_dhidden != 0, s, "dhidden product")) != FLP_OK)
                 return st;
         } else {
             const int64_t stride = kLinGradChunk * d;
-            if ((st = gemm_launch<false>(sms, tm_dz, tm_w_mn, rows, d, v, splits, dh_parts, d, stride, false, s,
-                                         "dhidden product")) != FLP_OK)
+            if ((st = gemm_launch<false>(dev, sms, tm_dz, tm_w_mn, rows, d, v, splits, dh_parts, d, stride, 0, false,
+                                         s, "dhidden product")) != FLP_OK)
                 return st;
             const int64_t blocks = ceil_div(rows * d, 256);
             flp::k_gemm_split_sum<<<(int)(blocks < (int64_t)sms * 8 ? blocks : (int64_t)sms * 8), 256, 0, s>>>(
@@ -1110,7 +1185,7 @@ flp_status linear_backward_impl(const void* hidden, int64_t n, int64_t d, int64_
             if ((st = check_launch("dhidden split sum")) != FLP_OK) return st;
         }
         // dW (+)= dZ^T H (K = the chunk's rows), added chunk after chunk in row order
-        if ((st = gemm_launch<true>(sms, tm_dz_mn, tm_h_mn, v, d, rows, 1, dweight, ld_dw, 0,
+        if ((st = gemm_launch<true>(dev, sms, tm_dz_mn, tm_h_mn, v, d, rows, 1, dweight, ld_dw, 0, v,
                                     start > 0 || accumulate_dweight, s, "dweight product")) != FLP_OK)
             return st;
     }

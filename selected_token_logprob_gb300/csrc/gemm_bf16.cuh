@@ -72,6 +72,8 @@ struct GemmArgs {
     int64_t ldc, split_stride;
     int accumulate;           // 1: C = C + A B (one rounding per element)
     int vec;                  // C rows 16-byte aligned (base and ldc)
+    int64_t c_split_rows;     // tensor-map output: rows between consecutive splits
+    int group;                // pair kernel: 0 = N blocks fastest; g > 0 = groups of g 256-row blocks, row block fastest
 };
 
 struct GemmUnit {
@@ -311,6 +313,427 @@ k_gemm_split_sum(const float* __restrict__ parts, int splits, int64_t split_stri
         float acc = __ldg(pp);
         for (int k = 1; k < splits; ++k) acc = __fadd_rn(acc, __ldg(pp + (int64_t)k * split_stride));
         out[r * ldo + c] = accumulate ? __fadd_rn(s, acc) : acc;
+    }
+}
+
+// ---------------------------------------------------------------- CTA pairs
+
+// The same contraction on CTA pairs (a cluster of 2) with tcgen05.mma
+// cta_group::2: a pair computes a 256 x 256 tile, each CTA holding 128 rows of
+// A and 128 columns of B per K block (32 KB per stage instead of 48 KB, for
+// the same FLOPs per SM), in a 6-stage ring.  Each CTA's producer copies its
+// own halves of a stage into its own shared memory, completing on the even
+// CTA's (rank 0) stage barrier, which expects both CTAs' bytes; the even CTA's
+// MMA lane issues M = 256 MMAs that read both CTAs' halves, the accumulator
+// rows split between the CTAs' TMEM, and each CTA's four epilogue warps read
+// their 128 rows.  The MMA lane commits each released stage and each ready
+// accumulator to the barriers of both CTAs (one commit per CTA); both CTAs'
+// epilogue warps release an accumulator on the even CTA's barrier.  Every
+// cross-CTA access is a barrier signal inside the pair.  (Forwarding the
+// even CTA's signals to the peer through a waiting thread instead measured
+// 2.4 times slower: the hand-off latency exceeds what 6 stages cover.)
+constexpr int kPairStages = 6;
+constexpr uint32_t kPairABytes = 128 * kGemmBK * 2;          // 16 KB: this CTA's A rows
+constexpr uint32_t kPairBBytes = 128 * kGemmBK * 2;          // 16 KB: this CTA's B columns
+constexpr uint32_t kPairStageBytes = kPairABytes + kPairBBytes;
+// epilogue staging: per epilogue warp two 32 x 32 FP32 boxes (128-byte swizzle)
+constexpr uint32_t kPairStageOutBytes = 32 * 32 * 4;
+constexpr size_t kPairSmemBytes =
+    1024 + (size_t)kPairStages * kPairStageBytes + 1024 + 4 * 2 * (size_t)kPairStageOutBytes;
+static_assert(kPairSmemBytes <= 232448, "shared memory per CTA");
+
+template <bool kAmn, bool kBmn>
+__host__ __device__ constexpr uint32_t pair_idesc() {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((kAmn ? 1u : 0u) << 15) | ((kBmn ? 1u : 0u) << 16) |
+           ((uint32_t)(256 >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_count_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+// The shared::cluster address of `addr` (a shared::cta address of this CTA)
+// in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+// Bounded wait (cluster-scope acquire) that also gives up on the abort flag.
+__device__ __forceinline__ bool pair_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_cluster(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_cluster(bar, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (*abort_flag) return false;
+            if (clock64() - t0 > kWaitLimitCycles) {
+                *abort_flag = 1;
+                atomicExch(&g_device_error, 1);
+                return false;
+            }
+        }
+    }
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                                 uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// Tensor-map store of a shared-memory box to global memory, or its addition
+// to what global memory holds (the add is done where the data lives, one
+// rounding per element); completion is tracked as a bulk group of this thread.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int32_t x, int32_t y, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, int32_t x, int32_t y, uint32_t src) {
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// At most N of this thread's bulk groups still reading shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void sts_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// Loads of one K block of this pair's A (or B) half for CTA `rank` into its
+// stage at `dst` (a shared::cluster address): 128 rows (K-major box) or two
+// MN-major 64 x 64 boxes.
+template <bool kMN>
+__device__ __forceinline__ void pair_load(uint32_t dst, const CUtensorMap* map, int mn0, int k0, uint32_t bar) {
+    if constexpr (kMN) {
+        tma_load_2d_pair(dst, map, mn0, k0, bar);
+        tma_load_2d_pair(dst + kGemmBoxBytes, map, mn0 + 64, k0, bar);
+    } else {
+        tma_load_2d_pair(dst, map, k0, mn0, bar);
+    }
+}
+
+// kTmaC: the output goes out through tm_c (FP32 [rows, N], boxes of 32 x 32,
+// 128-byte swizzle; split s at rows s * c_split_rows + m): each epilogue warp
+// stages a 32 x 32 box in shared memory and one lane stores it, or adds it in
+// place when accumulating, as whole lines.  Otherwise each thread writes its
+// row's values itself.
+template <bool kAmn, bool kBmn, bool kTmaC>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+k_gemm_bf16_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                 const __grid_constant__ CUtensorMap tm_c, GemmArgs p) {
+    extern __shared__ __align__(1024) unsigned char pair_smem_raw[];
+    const uint32_t raw = smem_u32(pair_smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;   // the same offset in both CTAs
+    const uint32_t bars = base + kPairStages * kPairStageBytes;
+    const uint32_t full0 = bars, empty0 = bars + 8 * kPairStages;
+    const uint32_t tfull0 = bars + 16 * kPairStages, tempty0 = tfull0 + 16;
+    const uint32_t drain = tempty0 + 16;
+    const uint32_t slot = drain + 8;
+    unsigned char* slot_gen = pair_smem_raw + (slot - raw);
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(slot_gen);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(slot_gen + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    const int64_t cid = cluster_id_x(), ncl = cluster_count_x();
+    // this pair's units: (split, 256-row block, 256-column block), N fastest
+    const int64_t nmb2 = (p.M + 255) / 256, nnb = p.nnb;
+    const int64_t nunits = nmb2 * nnb * p.splits;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kPairStages; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull0 + 8 * a, 1);
+            mbar_init(tempty0 + 8 * a, 8);     // 4 epilogue warps per CTA, both CTAs
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tm_a);
+        prefetch_tmap(&tm_b);
+        if (kTmaC) prefetch_tmap(&tm_c);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(slot, 2 * kGemmBN);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync_all();   // both CTAs' barriers initialised and TMEM allocated
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    auto unit_of = [&](int64_t u, int& s, int64_t& mb, int64_t& nb) {
+        const int64_t per = nmb2 * nnb;
+        s = (int)(u / per);
+        const int64_t t = u - (int64_t)s * per;
+        if (p.group > 0) {   // groups of `group` row blocks: inside a group the row block is the fast index
+            const int64_t gsz = (int64_t)p.group * nnb;
+            const int64_t g = t / gsz, r = t - g * gsz;
+            const int64_t rows = (g + 1) * p.group <= nmb2 ? p.group : nmb2 - g * p.group;
+            mb = g * p.group + r % rows;
+            nb = r / rows;
+        } else {
+            mb = t / nnb;
+            nb = t - mb * nnb;
+        }
+    };
+
+    if (warp == 0) {
+        // ---------------- producers: each CTA copies its own halves of a stage;
+        // every copy completes on the even CTA's stage barrier, which expects
+        // both CTAs' bytes.  Each CTA's stage is released to its producer by
+        // an MMA commit on its own barrier.
+        if (lane == 0) {
+            const uint32_t full_leader = map_to_rank(full0, 0);
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, last_par = 0;
+            bool ok = true;
+            for (int64_t u = cid; ok && u < nunits; u += ncl) {
+                int s;
+                int64_t mb, nb;
+                unit_of(u, s, mb, nb);
+                const int kb0 = (int)((int64_t)s * p.nkb / p.splits);
+                const int kb1 = (int)((int64_t)(s + 1) * p.nkb / p.splits);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!lin_wait(empty0 + 8 * stage, phase ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t off = stage * kPairStageBytes;
+                    const uint32_t bar = full_leader + 8 * stage;
+                    if (leader) mbar_arrive_expect_tx(full0 + 8 * stage, 2 * kPairStageBytes);
+                    const int k0 = kb * kGemmBK;
+                    const int m0 = (int)(mb * 256) + (int)rank * 128, n0 = (int)(nb * 256) + (int)rank * 128;
+                    pair_load<kAmn>(base + off, &tm_a, m0, k0, bar);
+                    pair_load<kBmn>(base + off + kPairABytes, &tm_b, n0, k0, bar);
+                    issued |= 1u << stage;
+                    last_par = (last_par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == kPairStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok && leader) {
+                for (int s = 0; s < kPairStages; ++s)
+                    if (issued & (1u << s)) mbar_wait(full0 + 8 * s, (last_par >> s) & 1u, kWaitLimitCycles);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------- MMA issuer (even CTA): each commit is issued once
+        // for this CTA's barrier and once for the peer's
+        if (leader && lane == 0) {
+            constexpr uint32_t idesc = pair_idesc<kAmn, kBmn>();
+            const uint32_t empty_peer = map_to_rank(empty0, 1), tfull_peer = map_to_rank(tfull0, 1);
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int64_t u = cid; ok && u < nunits; u += ncl) {
+                int s;
+                int64_t mb, nb;
+                unit_of(u, s, mb, nb);
+                const int kb0 = (int)((int64_t)s * p.nkb / p.splits);
+                const int kb1 = (int)((int64_t)(s + 1) * p.nkb / p.splits);
+                // both CTAs' epilogues have released this accumulator
+                if (!pair_wait(tempty0 + 8 * acc, acc_phase ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + (uint32_t)(acc * kGemmBN);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!lin_wait(full0 + 8 * stage, phase, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = base + stage * kPairStageBytes;
+                    const uint64_t a_desc = gemm_desc<kAmn>(a_addr);
+                    const uint64_t b_desc = gemm_desc<kBmn>(a_addr + kPairABytes);
+#pragma unroll
+                    for (int k = 0; k < kGemmBK / 16; ++k)
+                        umma_bf16_pair(d_tmem, a_desc + gemm_kstep<kAmn>() * k, b_desc + gemm_kstep<kBmn>() * k,
+                                       idesc, (kb != kb0 || k != 0) ? 1u : 0u);
+                    umma_commit_pair(empty0 + 8 * stage);
+                    umma_commit_pair(empty_peer + 8 * stage);
+                    if (++stage == kPairStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit_pair(tfull0 + 8 * acc);
+                umma_commit_pair(tfull_peer + 8 * acc);
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            umma_commit_pair(drain);
+            mbar_wait(drain, 0, kWaitLimitCycles);
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue: this CTA's 128 rows of the pair's tile
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
+        const uint32_t tempty_leader = map_to_rank(tempty0, 0);
+        const uint32_t stg = bars + 1024 + (uint32_t)q * 2 * kPairStageOutBytes;   // this warp's two boxes
+        int acc = 0, nbuf = 0;
+        uint32_t acc_phase = 0;
+        for (int64_t u = cid; u < nunits; u += ncl) {
+            int s;
+            int64_t mb, nb;
+            unit_of(u, s, mb, nb);
+            if (!lin_wait(tfull0 + 8 * acc, acc_phase, abort_flag)) break;
+            tc_fence_after();
+            const int64_t m_warp = mb * 256 + (int64_t)rank * 128 + q * 32;   // first row of this warp
+            const int64_t m = m_warp + lane;
+            const int64_t n0 = nb * kGemmBN;
+            float* crow = p.C + (int64_t)s * p.split_stride + m * p.ldc;
+#pragma unroll 1
+            for (int c = 0; c < kGemmBN / 32; ++c) {
+                const int64_t c0 = n0 + c * 32;
+                if (c0 >= p.N) break;   // uniform over the CTA
+                __syncwarp();
+                if constexpr (kTmaC) {
+                    uint32_t r[32];
+                    tmem_ld32(lane_addr + (uint32_t)(acc * kGemmBN + c * 32), r);
+                    if (m_warp >= p.M) continue;   // the whole box lies past the last row
+                    const uint32_t box = stg + (uint32_t)(nbuf & 1) * kPairStageOutBytes;
+                    if (lane == 0) bulk_wait_read<1>();   // the store that last used this box has read it
+                    __syncwarp();
+                    // row `lane` of the box, 16-byte chunk j at position j ^ (lane mod 8)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        sts_v4(box + (uint32_t)lane * 128 + (uint32_t)((j ^ (lane & 7)) * 16), r[4 * j], r[4 * j + 1],
+                               r[4 * j + 2], r[4 * j + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const int32_t y = (int32_t)((int64_t)s * p.c_split_rows + m_warp);
+                        if (p.accumulate) tma_reduce_add_2d(&tm_c, (int32_t)c0, y, box);
+                        else tma_store_2d(&tm_c, (int32_t)c0, y, box);
+                        bulk_commit_group();
+                    }
+                    ++nbuf;
+                } else {
+                    const bool vec = p.vec && c0 + 32 <= p.N && m < p.M;
+                    float4 old[8];
+                    if (vec && p.accumulate) {
+                        const float4* src = reinterpret_cast<const float4*>(crow + c0);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) old[j] = src[j];
+                    }
+                    uint32_t r[32];
+                    tmem_ld32(lane_addr + (uint32_t)(acc * kGemmBN + c * 32), r);
+                    if (vec) {
+                        float4* dst = reinterpret_cast<float4*>(crow + c0);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            float4 v = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                                   __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                            if (p.accumulate) {
+                                v.x = __fadd_rn(old[j].x, v.x);
+                                v.y = __fadd_rn(old[j].y, v.y);
+                                v.z = __fadd_rn(old[j].z, v.z);
+                                v.w = __fadd_rn(old[j].w, v.w);
+                            }
+                            dst[j] = v;
+                        }
+                    } else if (m < p.M) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            if (c0 + j < p.N) {
+                                const float v = __uint_as_float(r[j]);
+                                crow[c0 + j] = p.accumulate ? __fadd_rn(crow[c0 + j], v) : v;
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tempty_leader + 8 * acc);
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+        if (kTmaC && lane == 0) bulk_wait_read<0>();   // shared memory is read before the CTA exits
+        __syncwarp();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();   // no copy, arrive or MMA of the pair still targets either CTA
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, 2 * kGemmBN);
     }
 }
 
