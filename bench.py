@@ -100,9 +100,10 @@ def _kernel_hash(kernel: str = "k_logp_bwd") -> str:
     return h.hexdigest()[:16]
 
 
-def _profiled_traffic(kernel: str):
+def _profiled_traffic(kernel: str, parts: bool = False):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, if it
-    was taken on the current kernel source; else None."""
+    was taken on the current kernel source; else None.  With parts: a dict of
+    the read, write and total bytes (and the method's bytes, when recorded)."""
     p = os.path.join(ROOT, "profiles", f"{kernel}_long.md")
     if not os.path.exists(p):
         return None
@@ -111,7 +112,14 @@ def _profiled_traffic(kernel: str):
     m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
     if not m_hash or not m_bytes or m_hash.group(1) != _kernel_hash(kernel):
         return None
-    return float(m_bytes.group(1))
+    if not parts:
+        return float(m_bytes.group(1))
+    out = {"total": float(m_bytes.group(1))}
+    for key, name in (("read", "dram_read_bytes_per_launch"), ("write", "dram_write_bytes_per_launch"),
+                      ("algorithmic_active", "algorithmic_bytes_active")):
+        m = re.search(name + r":\s*([0-9.eE+]+)", txt)
+        out[key] = float(m.group(1)) if m else None
+    return out
 
 
 class ClockSampler:
@@ -378,6 +386,8 @@ def run_ours(args):
     fwd_avg = statistics.mean(fwd_ms)
     achieved = logits_per_rank * BWD_BYTES_PER_LOGIT * ebytes // 2 / (bwd_avg * 1e-3) / 1e9
     clocks = sampler.summary()
+    prof = (_profiled_traffic("k_logp_bwd", parts=True)
+            if args.dtype == "bf16" and args.workload == "long" else None)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
@@ -397,8 +407,14 @@ def run_ours(args):
         "roofline": {"kernel": "k_logp_bwd", "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": peak_src,
-                     "traffic": _profiled_traffic("k_logp_bwd")
-                     if args.dtype == "bf16" and args.workload == "long" else None,
+                     "traffic": prof["total"] if prof else None,
+                     "traffic_read": prof["read"] if prof else None,
+                     "traffic_write": prof["write"] if prof else None,
+                     "algorithmic_bytes": logits_per_rank * BWD_BYTES_PER_LOGIT * ebytes // 2,
+                     "algorithmic_bytes_active": prof["algorithmic_active"] if prof else None,
+                     "traffic_note": "ncu dram__bytes_read/write.sum of a full launch (one-pass capture of this "
+                                     "command, profiles/k_logp_bwd_long.md); inactive rows are not read, the "
+                                     "writes still dirty in L2 at the kernel's end are not counted",
                      "fwd_frac": round(logits_per_rank * FWD_BYTES_PER_LOGIT * ebytes // 2
                                        / (fwd_avg * 1e-3) / 1e9 / peak, 4),
                      "step_frac": round(value / world / peak, 4)},
