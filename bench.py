@@ -426,6 +426,11 @@ def run_ours(args):
     }
     if rank == 0:
         line["cpu_baseline"] = cpu_baseline(args, x, y, g, v)
+    if world == 1 and args.side_paths != "none":
+        del x, g, dl
+        torch.cuda.empty_cache()
+        line["side_paths"] = _side_paths(args)
+    if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -433,9 +438,39 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_linear(args):
+def _side_paths(args):
+    """The two other paths of the library, device-timed on the same GPU after
+    the logits path's line is complete (its timed region is over): the fused
+    LM-head forward (and its backward) at N = 32768, D = 4096, V = 151936, and
+    the GRPO loss over 16.8M tokens.  Each keeps its own clock record; its own
+    `--path` run adds the end-to-end leg and the oracle."""
+    import copy
+
+    out = {}
+    for name in args.side_paths.split(","):
+        sub = copy.copy(args)
+        sub.warmup = 3
+        if name == "linear":
+            sub.steps, sub.linear_bwd_steps = 10, 3
+            line = run_linear(sub, side=True)
+            keep = ("metric", "value", "unit", "steps", "ms_per_step", "config", "roofline", "backward",
+                    "gpu_launches", "clocks")
+        elif name == "grpo":
+            sub.steps = 20
+            line = run_grpo(sub, side=True)
+            keep = ("metric", "value", "unit", "steps", "ms_per_step", "config", "roofline",
+                    "token_mean_with_normalizer", "small_call_us", "gpu_launches", "clocks")
+        else:
+            raise SystemExit(f"--side-paths: unknown path {name!r}")
+        out[name] = {k: line[k] for k in keep}
+    return out
+
+
+def run_linear(args, side=False):
     """The fused LM-head forward: one step = one fused_linear_logp_forward
-    call (contraction kernel + partial merge) over the whole batch."""
+    call (contraction kernel + partial merge) over the whole batch.  With
+    `side` (one GPU, called after the logits path's measurement) only the
+    device-timed forward and backward are taken and the line is returned."""
     import torch
 
     import selected_token_logprob_gb300 as flp
@@ -444,7 +479,7 @@ def run_linear(args):
     world, rank, local = _dist()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    if world > 1:
+    if world > 1 and not side:
         import torch.distributed as dist
 
         dist.init_process_group("nccl", device_id=dev)
@@ -487,7 +522,7 @@ def run_linear(args):
     call_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     achieved = flops / (call_ms * 1e-3) / 1e12
     burst, sustained, src = _tensor_peaks()
-    e2e = _linear_e2e(args, flp, h, w, y, ws, dev, stream, world)
+    e2e = None if side else _linear_e2e(args, flp, h, w, y, ws, dev, stream, world)
     bwd = _linear_backward_timing(args, flp, h, w, y, lse, lse_lo, dev, stream)
     line = {
         "metric": LIN_METRIC if (n, d) == (32768, 4096) else f"fused LM-head + logp forward TFLOP/s "
@@ -509,6 +544,8 @@ def run_linear(args):
         "clocks": sampler.summary(),
         "backward": bwd,
     }
+    if side:
+        return line
     if rank == 0:
         line["cpu_baseline"] = _linear_cpu_baseline(args, h, w, y, v, d)
         print(json.dumps(line), flush=True)
@@ -537,10 +574,11 @@ def _grpo_inputs(n, nseq, seed, device):
     return [t.to(device) for t in (lp, old, ref, adv, mask, cu)]
 
 
-def run_grpo(args):
+def run_grpo(args, side=False):
     """The GRPO loss on the logp path over a large RL batch: one call = the
     per-token terms with per-chunk sums, the fixed-order fold (with the
-    sequences' folds), the per-sequence weights."""
+    sequences' folds), the per-sequence weights.  With `side` the end-to-end
+    leg and the oracle are skipped and the line is returned."""
     import torch
 
     import selected_token_logprob_gb300 as flp
@@ -630,28 +668,10 @@ def run_grpo(args):
     b.record(stream)
     torch.cuda.synchronize(dev)
     small_us = a.elapsed_time(b) / 100 * 1e3
-    # end to end: the step's inputs from pinned host memory, the loss read back
-    host = [t.cpu().pin_memory() for t in (lp, old, ref, adv, mask, cu)]
-    devs = [torch.empty_like(t) for t in (lp, old, ref, adv, mask, cu)]
-    hloss = torch.empty(1, dtype=torch.float32).pin_memory()
-
-    def e2e_step():
-        for d_, h_ in zip(devs, host):
-            d_.copy_(h_, non_blocking=True)
-        loss, _ = flp.logp_grpo_loss(devs[0], devs[1], devs[3], ref_logp=devs[2], active_mask=devs[4],
-                                     cu_seqlens=devs[5], mode="seq_mean_token_mean", eps_lo=0.2, eps_hi=0.28,
-                                     beta=0.04, workspace=ws)
-        hloss.copy_(loss, non_blocking=True)
-
-    e2e_step()
-    torch.cuda.synchronize(dev)
-    a.record(stream)
-    for _ in range(max(1, args.e2e_steps)):
-        e2e_step()
-    b.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = a.elapsed_time(b) / max(1, args.e2e_steps)
-    h2d = sum(t.numel() * t.element_size() for t in host)
+    if side:
+        e2e_ms = None
+    else:
+        e2e_ms, h2d = _grpo_e2e(args, flp, (lp, old, ref, adv, mask, cu), ws, dev, stream)
     line = {
         "metric": GRPO_METRIC if (n, nseq) == (16777216, 16384) else f"GRPO loss GB/s at N={n}, {nseq} sequences",
         "value": round(gbs, 1), "unit": "GB/s", "n_gpus": 1, "steps": steps, "warmup": args.warmup,
@@ -669,11 +689,14 @@ def run_grpo(args):
         "token_mean_with_normalizer": {"ms_per_step": round(tm_ms, 4),
                                        "GB/s": round(alg / (tm_ms * 1e-3) / 1e9, 1),
                                        "frac": round(alg / (tm_ms * 1e-3) / 1e9 / peak, 4)},
-        "e2e": {"value": round(alg / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 3),
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4},
+        "e2e": None if e2e_ms is None else
+        {"value": round(alg / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 3),
+         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4},
         "gpu_launches": 3 * steps,
         "clocks": sampler.summary(),
     }
+    if side:
+        return line
     if rank == 0 and args.cpu_seconds > 0:
         import oracle
 
@@ -694,6 +717,35 @@ def run_grpo(args):
                                 "cores": oracle.num_threads(), "kind": "oracle",
                                 "sample": f"{done} x {rows} tokens (the first {rows} of the batch), FP64, {el:.1f} s"}
     print(json.dumps(line), flush=True)
+
+
+def _grpo_e2e(args, flp, inputs, ws, dev, stream):
+    """End to end: the step's inputs copied from pinned host memory, the loss
+    read back; returns (ms per step, host-to-device bytes per step)."""
+    import torch
+
+    host = [t.cpu().pin_memory() for t in inputs]
+    devs = [torch.empty_like(t) for t in inputs]
+    hloss = torch.empty(1, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        for d_, h_ in zip(devs, host):
+            d_.copy_(h_, non_blocking=True)
+        loss, _ = flp.logp_grpo_loss(devs[0], devs[1], devs[3], ref_logp=devs[2], active_mask=devs[4],
+                                     cu_seqlens=devs[5], mode="seq_mean_token_mean", eps_lo=0.2, eps_hi=0.28,
+                                     beta=0.04, workspace=ws)
+        hloss.copy_(loss, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(max(1, args.e2e_steps)):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    return a.elapsed_time(b) / max(1, args.e2e_steps), sum(t.numel() * t.element_size() for t in host)
 
 
 def _linear_backward_timing(args, flp, h, w, y, lse, lse_lo, dev, stream):
@@ -730,8 +782,8 @@ def _linear_backward_timing(args, flp, h, w, y, lse, lse_lo, dev, stream):
     return {"ms": round(ms, 3), "tflops": round(tf, 1), "frac": round(tf / burst, 4),
             "frac_of_sustained": round(tf / sustained, 4), "steps": args.linear_bwd_steps,
             "flop_per_call": 3 * 2.0 * n * v * d,
-            "kernels": "per 4096-row chunk: k_linear_logp_tiles<grad> (dZ, BF16), k_gemm_bf16 (dH, 5 K splits) + "
-                        "k_gemm_split_sum, k_gemm_bf16 (dW)"}
+            "kernels": "per 4096-row chunk: k_linear_logp_tiles<grad> (dZ, BF16), k_gemm_bf16_pair (dH, 5 K splits) + "
+                        "k_gemm_split_sum, k_gemm_bf16_pair (dW, added over the chunks)"}
 
 
 def _linear_e2e(args, flp, h, w, y, ws, dev, stream, world):
@@ -1074,6 +1126,9 @@ def main(argv=None):
     ap.add_argument("--path", choices=["logits", "linear", "grpo"], default="logits",
                     help="logits: logp fwd+bwd over BF16 logits (the headline); "
                          "linear: fused LM head + logp forward")
+    ap.add_argument("--side-paths", default="linear,grpo",
+                    help="with the logits path on one GPU: also device-time these paths after its line is "
+                         "complete and attach them under side_paths ('none' to skip)")
     ap.add_argument("--linear-n", type=int, default=32768)
     ap.add_argument("--linear-d", type=int, default=4096)
     ap.add_argument("--grpo-n", type=int, default=16777216)

@@ -603,15 +603,15 @@ flp_status launch_dependent(const char* what, void (*kern)(Args...), int grid, i
     return ok();
 }
 
-// GRPO workspace: 32 bytes of normaliser words and the fold's ticket, room
-// for the fold's per-CTA partials (32 bytes each, up to 1024 CTAs), per
-// 256-token chunk a two-float sum and a count, and with sequences per
-// (sequence, chunk) piece slot the same, per chunk its first sequence and
-// per sequence the reciprocal of its active count; rounded up to 256 bytes.
+// GRPO workspace: 32 bytes for the active-token count and the fold's
+// ticket, two two-float sums per CTA of the token pass (608 CTAs), a count
+// per CTA of the sequences' counts (1024) and per count range (1024), and
+// with sequences two floats per sequence and a 32-bit word prefix per 16
+// tokens; rounded up to 256 bytes.
 int64_t grpo_workspace_bytes(int64_t n, int64_t nseq) {
-    const int64_t nchunks = ceil_div(n, flp::kGrpoChunk);
-    const int64_t seq_part = nseq > 0 ? 16 * (nseq + nchunks) + 8 * nchunks + 4 * nseq : 0;
-    return ceil_div(32 + 32 * flp::kGrpoFoldMaxCtas + 16 * nchunks + seq_part, 256) * 256;
+    const int64_t seq_part = nseq > 0 ? 8 * nseq + 4 * ceil_div(n, 16) : 0;
+    return ceil_div(32 + 16 * flp::kGrpoPassCtas + 8 * flp::kGrpoFixMaxCtas + 8 * flp::kGrpoCountMaxCtas + seq_part,
+                    256) * 256;
 }
 
 }  // namespace
@@ -1297,61 +1297,65 @@ flp_status logp_grpo_loss(const float* logp, const float* old_logp, const float*
     DeviceGuard guard;
     if ((st = guard.enter(dev)) != FLP_OK) return st;
     // with a caller's normaliser the token mean and the sequence mean of sums
-    // have one weight known now: pass 1 applies it and the scale pass is skipped
+    // have one weight known now: the token pass applies it and nothing is counted
     const float prescale =
         (normalizer > 0.f && mode != FLP_GRPO_SEQ_MEAN_TOKEN_MEAN) ? (float)(1.0 / (double)normalizer) : 0.f;
     const flp::GrpoArgs a{logp, old_logp, ref_logp, advantages, active_mask, cu_seqlens, nseq, n, mode,
                           eps_lo, eps_hi, beta, normalizer, prescale, loss, grad, token_loss};
     const int64_t nchunks = ceil_div(n, flp::kGrpoChunk);
-    const int64_t slots = nseq > 0 ? nseq + nchunks : 0;
     char* base = static_cast<char*>(workspace);
     flp::GrpoWork wk;
-    wk.den = reinterpret_cast<double*>(base);
-    wk.wt = reinterpret_cast<float*>(base + 16);
-    wk.ticket = reinterpret_cast<unsigned*>(base + 20);
+    wk.dcnt = reinterpret_cast<int64_t*>(base);
+    wk.ticket = reinterpret_cast<unsigned*>(base + 8);
     wk.part_t = reinterpret_cast<flp::FF*>(base + 32);
-    wk.part_q = wk.part_t + flp::kGrpoFoldMaxCtas;
-    wk.part_c = reinterpret_cast<int64_t*>(wk.part_q + flp::kGrpoFoldMaxCtas);
-    wk.part_a = wk.part_c + flp::kGrpoFoldMaxCtas;
-    wk.chunk_sum = reinterpret_cast<flp::FF*>(wk.part_a + flp::kGrpoFoldMaxCtas);
-    wk.chunk_cnt = reinterpret_cast<int64_t*>(wk.chunk_sum + nchunks);
-    wk.piece = reinterpret_cast<flp::FF*>(wk.chunk_cnt + nchunks);
-    wk.piece_cnt = reinterpret_cast<int64_t*>(wk.piece + slots);
-    wk.chunk_first = wk.piece_cnt + slots;
-    wk.seg_inv = reinterpret_cast<float*>(wk.chunk_first + (nseq > 0 ? nchunks : 0));
+    wk.part_q = wk.part_t + flp::kGrpoPassCtas;
+    wk.a_part = reinterpret_cast<int64_t*>(wk.part_q + flp::kGrpoPassCtas);
+    wk.range_cnt = wk.a_part + flp::kGrpoFixMaxCtas;
+    wk.seg_cnt = reinterpret_cast<float2*>(wk.range_cnt + flp::kGrpoCountMaxCtas);
+    wk.word_pre = reinterpret_cast<uint32_t*>(wk.seg_cnt + nseq);
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int sms = sm_count(dev);
-    if (sms <= 0) return fail(FLP_ECUDA, "cannot read the SM count of device %d", dev);
-    const int64_t tok_ctas = ceil_div(nchunks, flp::kGrpoPassThreads / 32);
     auto al = [](const void* q, uintptr_t m) { return (reinterpret_cast<uintptr_t>(q) & (m - 1)) == 0; };
     const bool vec = al(logp, 16) && al(old_logp, 16) && al(advantages, 16) && al(grad, 16) && al(ref_logp, 16) &&
                      al(token_loss, 16) && al(active_mask, 4);
-    if (n > 0) {
-        // pass 1: one wave (4 CTAs per SM at its 64 registers), each warp a
-        // contiguous range of chunks
-        const int64_t wave = (int64_t)sms * 4;
-        const int terms_grid = (int)(tok_ctas < wave ? (tok_ctas < 1 ? 1 : tok_ctas) : wave);
-        if (vec)
-            flp::k_grpo_terms<true><<<terms_grid, flp::kGrpoPassThreads, 0, s>>>(a, wk);
+    // 1. the mask's counts, when a weight depends on them (any weight but the
+    //    caller's uniform one); ranges of R tokens (a multiple of 16), at most
+    //    1024 of them, a function of n only
+    int64_t range = 0;
+    int nranges = 0;
+    if (n > 0 && prescale == 0.f && active_mask != nullptr) {
+        int64_t g = ceil_div(n, flp::kGrpoCountRound);
+        g = g < 1 ? 1 : (g > flp::kGrpoCountMaxCtas ? flp::kGrpoCountMaxCtas : g);
+        range = ceil_div(ceil_div(n, g), 16) * 16;
+        nranges = (int)ceil_div(n, range);
+        if (al(active_mask, 16))
+            flp::k_grpo_count<true><<<nranges, flp::kGrpoCountThreads, 0, s>>>(a, wk, range);
         else
-            flp::k_grpo_terms<false><<<terms_grid, flp::kGrpoPassThreads, 0, s>>>(a, wk);
-        if ((st = check_launch("grpo terms")) != FLP_OK) return st;
+            flp::k_grpo_count<false><<<nranges, flp::kGrpoCountThreads, 0, s>>>(a, wk, range);
+        if ((st = check_launch("grpo count")) != FLP_OK) return st;
     }
-    // the fold's first level: a CTA count fixed by the shape (its order
-    // depends on it), one round of sequences and of chunk totals per CTA up
-    // to 1024 CTAs; with no tokens one CTA writes the result
-    int64_t fold_ctas = ceil_div(nseq > nchunks ? nseq : nchunks, flp::kGrpoReduceThreads);
-    fold_ctas = fold_ctas < 1 ? 1 : (fold_ctas > flp::kGrpoFoldMaxCtas ? flp::kGrpoFoldMaxCtas : fold_ctas);
-    // the fold and the scale pass overlap their launch with the predecessor
-    // (programmatic dependent launch; they wait for it on the device)
-    if ((st = launch_dependent("grpo reduce", flp::k_grpo_reduce, n > 0 ? (int)fold_ctas : 1,
-                               flp::kGrpoReduceThreads, s, a, wk)) != FLP_OK)
-        return st;
-    if (n > 0 && prescale == 0.f) {
-        const int64_t wave = (int64_t)sms * 5;   // 5 CTAs per SM at its 48 registers
-        const int scale_grid = (int)(tok_ctas < wave ? (tok_ctas < 1 ? 1 : tok_ctas) : wave);
-        if ((st = launch_dependent("grpo scale", vec ? flp::k_grpo_scale<true> : flp::k_grpo_scale<false>,
-                                   scale_grid, flp::kGrpoPassThreads, s, a, wk)) != FLP_OK)
+    // 2. the sequences' counts (a sequence per thread); it waits for the
+    //    count on the device when that ran before it
+    int64_t nfix = (cu_seqlens != nullptr && n > 0 && mode != FLP_GRPO_TOKEN_MEAN)
+                       ? ceil_div(nseq, flp::kGrpoFixThreads) : 1;
+    nfix = nfix < 1 ? 1 : (nfix > flp::kGrpoFixMaxCtas ? flp::kGrpoFixMaxCtas : nfix);
+    auto fix = al(active_mask, 16) ? flp::k_grpo_fix<true> : flp::k_grpo_fix<false>;
+    if (nranges > 0) {
+        if ((st = launch_dependent("grpo counts", fix, (int)nfix, flp::kGrpoFixThreads, s, a, wk, range, nranges)) !=
+            FLP_OK)
+            return st;
+    } else {
+        fix<<<(int)nfix, flp::kGrpoFixThreads, 0, s>>>(a, wk, range, nranges);
+        if ((st = check_launch("grpo counts")) != FLP_OK) return st;
+    }
+    // 3. the token pass, launched while the fix kernel runs: final gradients
+    //    and the loss; its grid is fixed by n (the fold's shape depends on it)
+    if (n > 0) {
+        int64_t grid = ceil_div(nchunks, flp::kGrpoPassThreads / 32);
+        grid = grid < 1 ? 1 : (grid > flp::kGrpoPassCtas ? flp::kGrpoPassCtas : grid);
+        const bool per_seq = cu_seqlens != nullptr && mode == FLP_GRPO_SEQ_MEAN_TOKEN_MEAN;
+        auto kern = vec ? (per_seq ? flp::k_grpo_pass<true, true> : flp::k_grpo_pass<true, false>)
+                        : (per_seq ? flp::k_grpo_pass<false, true> : flp::k_grpo_pass<false, false>);
+        if ((st = launch_dependent("grpo pass", kern, (int)grid, flp::kGrpoPassThreads, s, a, wk, (int)nfix)) != FLP_OK)
             return st;
     }
     return ok();

@@ -14,34 +14,40 @@
 // number of non-empty sequences.  Tokens outside every sequence count as
 // inactive (l = 0, gradient 0).
 //
-// The batch is cut into fixed chunks of 256 tokens (one warp each),
-// independent of the sequence layout, so the work per warp is the same
-// whatever the sequence lengths:
-//   1. k_grpo_terms: each warp takes a contiguous range of chunks.  It loads
-//      a chunk (8 tokens per lane in two groups of 4, 16-byte accesses when
-//      the arrays allow) and finds the sequences that cross it (for its first
-//      chunk a 32-ary search over cu_seqlens, later resuming at the last
-//      sequence seen; overlapped with the loads).  For each such run
-//      (sequence s within chunk w) it sums l and counts the active tokens;
-//      the run's sums go to piece slot s + w (slots of distinct runs never
-//      collide: a later sequence only meets later chunks).  Each token's
-//      unnormalised gradient (or, when the weight is uniform and known up
-//      front, the final one) and loss are written, with the chunk's loss
-//      sum, active count and first sequence;
-//   2. k_grpo_reduce: G CTAs (G fixed by the shape) each fold a
-//      fixed share of the chunk totals and of the sequences (each sequence's
-//      pieces give its active count and mean); the CTA that finishes last
-//      folds the G partials in order into the loss and the weight;
-//   3. k_grpo_scale (when the weight was not known up front): each token's
-//      gradient, kept in L2 by pass 1, times its sequence's weight.
-// Within a 256-token chunk the sums are plain FP32 (each lane's 8 tokens in
-// order, then the xor butterfly: an error of at most about 12 u times the
-// chunk's sum of |l|); from the chunk level up they are two-float (hi + lo)
-// compensated sums in FP32 (Knuth's TwoSum per addition; the pair carries
-// about 44 significant bits), so the error does not grow with the batch: the
-// FP64 unit of this GPU is far too slow to accumulate per token.  Token
-// counts are integers.  Every fold has an order fixed by the token positions
-// and the sequence layout, never by the grid or by timing.
+// Every normaliser weight depends on the mask and the sequence layout only,
+// so the counts come first and the token pass writes final gradients:
+//   1. k_grpo_count (when there is a mask and the weight is not the
+//      caller's): CTA b takes tokens [b R, (b + 1) R) in rounds of 32768,
+//      counts the active tokens of each 16-token mask word, scans them in
+//      token order and writes, with sequences, each word's prefix within the
+//      range, and the range's total.  Integer counts: exact in any order.
+//   2. k_grpo_fix: the ranges' exclusive prefix, a word's prefix and the
+//      bits of the word below x give P(x), the active tokens before x, for
+//      every sequence start x = cu_seqlens[s]: hence each sequence's count
+//      n_s = P(cu[s + 1]) - P(cu[s]), per CTA the number of sequences with an
+//      active token, and the active tokens D inside the sequences; it also
+//      zeroes the ticket of pass 3's fold.  Pass 3's warps form the
+//      normaliser and the weight from these.
+//   3. k_grpo_pass: the batch is cut into fixed chunks of 256 tokens (one
+//      warp each), independent of the sequence layout; each warp takes a
+//      contiguous range of chunks.  It loads a chunk (8 tokens per lane in
+//      two groups of 4, 16-byte accesses when the arrays allow) and finds
+//      the sequences that cross it (for its first chunk a 32-ary search over
+//      cu_seqlens, later resuming at the last sequence seen), overlapped with
+//      the loads.  Each token's gradient is written once, with its weight
+//      (1 / den, or 1 / (den n_s) for the sequence mean of token means);
+//      each run (sequence s within the chunk) adds its loss sum (or, for the
+//      sequence mean of means, that sum over n_s) to the warp's total.  The
+//      CTA folds its warps in order; the CTA that finishes last (an atomic
+//      ticket) folds the CTAs' sums in order into the loss.
+// The grid of pass 3 and so every fold's shape are fixed by the problem's
+// shape.  Within a 256-token chunk the sums are plain FP32 (each lane's 8
+// tokens in order, then the xor butterfly: an error of at most about 12 u
+// times the chunk's sum of |l|); from the chunk level up they are two-float
+// (hi + lo) compensated sums in FP32 (Knuth's TwoSum per addition; the pair
+// carries about 44 significant bits), so the error does not grow with the
+// batch: the FP64 unit of this GPU is far too slow to accumulate per token.
+// No fold's order depends on timing.
 #pragma once
 
 #include "logp_prims.cuh"
@@ -108,11 +114,19 @@ __device__ __forceinline__ int64_t warp_sum_i64(int64_t v) {
     return v;
 }
 
-// The fold's first level has G CTAs, G a function of the shape only (so
-// the fold order is fixed by the layout): max(sequences, chunks) / 256
-// rounded up, at least 1 and at most 1024.
-constexpr int kGrpoFoldMaxCtas = 1024;
-constexpr int kGrpoReduceThreads = 256;
+// Pass 3's grid for a large batch: one wave of 4 CTAs per SM on a 152-SM
+// GB300, a constant so that the fold's shape depends on the problem only.
+constexpr int kGrpoPassCtas = 608;
+// The count: 256 threads, 8 mask words of 16 tokens per thread per round,
+// at most 1024 ranges (the fix kernel scans them in one CTA of 1024 threads).
+constexpr int kGrpoCountThreads = 256;
+constexpr int kGrpoCountWords = 8;
+constexpr int64_t kGrpoCountRound = 16 * kGrpoCountWords * kGrpoCountThreads;   // 32768 tokens
+constexpr int kGrpoCountMaxCtas = 1024;
+// The sequences' counts: one sequence per thread and step, at most 1024
+// CTAs of 256 threads.
+constexpr int kGrpoFixThreads = 256;
+constexpr int kGrpoFixMaxCtas = 1024;
 
 // e^x as 2^(x log2 e), the power of two from the special-function unit
 // (ex2.approx, flushing subnormal results to 0): within a few ulp for
@@ -120,19 +134,14 @@ constexpr int kGrpoReduceThreads = 256;
 __device__ __forceinline__ float grpo_exp(float x) { return ex2_ftz(__fmul_rn(x, 1.4426950408889634f)); }
 
 struct GrpoWork {
-    double* den;          // [2]: the normaliser, the number of active tokens
-    float* wt;            // [1]: the uniform weight (token mean, sequence mean of sums, or one sequence)
-    unsigned* ticket;     // [1]: CTAs of the fold that are done (zeroed by pass 1, reset by the last CTA)
-    FF* part_t;           // [kGrpoFoldMaxCtas]: per fold CTA, loss sum
-    FF* part_q;           //   sum of sequence means
-    int64_t* part_c;      //   active tokens
-    int64_t* part_a;      //   sequences with an active token
-    FF* chunk_sum;        // [nchunks]: loss sum of each 256-token chunk
-    int64_t* chunk_cnt;   // [nchunks]: its active tokens
-    FF* piece;            // [nseq + nchunks]: loss sum of sequence s within chunk w, at s + w
-    int64_t* piece_cnt;
-    int64_t* chunk_first; // [nchunks]: the first sequence that may meet each chunk
-    float* seg_inv;       // [nseq]: 1 / (active tokens of each sequence), 0 for none
+    int64_t* dcnt;        // [1]: active tokens inside the sequences (or in the batch)
+    unsigned* ticket;     // [1]: CTAs of pass 3 that are done (zeroed by the fix kernel, counted by pass 3)
+    FF* part_t;           // [kGrpoPassCtas]: per CTA of pass 3, its loss sum
+    FF* part_q;           //   its sum of sequence means' pieces
+    int64_t* a_part;      // [kGrpoFixMaxCtas]: per CTA of the fix kernel, its sequences with an active token
+    int64_t* range_cnt;   // [kGrpoCountMaxCtas]: active tokens of each count range
+    uint32_t* word_pre;   // [ceil(n / 16)] with sequences: active tokens of a word's range before the word
+    float2* seg_cnt;      // [nseq]: active tokens of each sequence n_s and 1 / n_s (0 for none), FP32
 };
 
 __device__ __forceinline__ int64_t grpo_chunks(int64_t n) { return (n + kGrpoChunk - 1) / kGrpoChunk; }
@@ -169,12 +178,12 @@ __device__ __forceinline__ int64_t grpo_find(const GrpoArgs& p, int64_t x, int l
 struct GrpoRuns {
     int64_t s;     // the first sequence that may meet the chunk
     int bnd;       // lane j: cu[s + j] - c0 clamped to [0, 256] (256 past cu[nseq])
-    float aux;     // lane j: aux[s + j] when an aux array is given (s + j < nseq), else 0
+    float2 aux;    // lane j: aux[s + j] when an aux array is given (s + j < nseq), else 0
 };
 
 __device__ __forceinline__ GrpoRuns grpo_runs_at(const GrpoArgs& p, int64_t s, int64_t c0, int lane,
-                                                 const float* aux) {
-    GrpoRuns r{s < 0 ? 0 : s, (int)kGrpoChunk, 0.f};
+                                                 const float2* aux) {
+    GrpoRuns r{s < 0 ? 0 : s, (int)kGrpoChunk, make_float2(0.f, 0.f)};
     const int64_t idx = r.s + lane;
     if (idx <= p.nseq) {
         const int64_t d = grpo_cu(p, idx) - c0;
@@ -184,8 +193,12 @@ __device__ __forceinline__ GrpoRuns grpo_runs_at(const GrpoArgs& p, int64_t s, i
     return r;
 }
 __device__ __forceinline__ GrpoRuns grpo_runs_begin(const GrpoArgs& p, int64_t c0, int lane) {
-    if (p.cu == nullptr) return GrpoRuns{0, 0, 0.f};
+    if (p.cu == nullptr) return GrpoRuns{0, 0, make_float2(0.f, 0.f)};
     return grpo_runs_at(p, grpo_find(p, c0, lane), c0, lane, nullptr);
+}
+
+__device__ __forceinline__ float2 shfl_f2(float2 v, int src) {
+    return make_float2(__shfl_sync(0xffffffffu, v.x, src), __shfl_sync(0xffffffffu, v.y, src));
 }
 
 // Calls f(s, ua, ub, aux_s) for each sequence s whose tokens meet the chunk
@@ -194,15 +207,15 @@ __device__ __forceinline__ GrpoRuns grpo_runs_begin(const GrpoArgs& p, int64_t c
 // fetched 32 at a time.  kAux: pass the aux value (else 0, no shuffle).
 template <bool kAux, class F>
 __device__ __forceinline__ void grpo_runs(const GrpoArgs& p, GrpoRuns r, int64_t c0, int nv, int lane,
-                                          const float* aux, F&& f) {
+                                          const float2* aux, F&& f) {
     if (p.cu == nullptr) {
-        f((int64_t)0, 0, nv, 0.f);   // one sequence: the whole batch
+        f((int64_t)0, 0, nv, make_float2(0.f, 0.f));   // one sequence: the whole batch
         return;
     }
     if (r.s < p.nseq) {   // the common case: the chunk lies inside sequence r.s
         const int a0 = __shfl_sync(0xffffffffu, r.bnd, 0), b0 = __shfl_sync(0xffffffffu, r.bnd, 1);
         if (a0 == 0 && b0 >= nv) {
-            f(r.s, 0, nv, kAux ? __shfl_sync(0xffffffffu, r.aux, 0) : 0.f);
+            f(r.s, 0, nv, kAux ? shfl_f2(r.aux, 0) : make_float2(0.f, 0.f));
             return;
         }
     }
@@ -211,7 +224,7 @@ __device__ __forceinline__ void grpo_runs(const GrpoArgs& p, GrpoRuns r, int64_t
             const int a = __shfl_sync(0xffffffffu, r.bnd, j);
             if (r.s + j >= p.nseq || a >= nv) return;
             const int b = min(__shfl_sync(0xffffffffu, r.bnd, j + 1), nv);
-            const float x = kAux ? __shfl_sync(0xffffffffu, r.aux, j) : 0.f;
+            const float2 x = kAux ? shfl_f2(r.aux, j) : make_float2(0.f, 0.f);
             if (a < b) f(r.s + j, a, b, x);
         }
         r = grpo_runs_at(p, r.s + 31, c0, lane, aux);
@@ -257,6 +270,9 @@ __device__ __forceinline__ void st_f4_hint(float* p, float4 v, uint64_t pol) {
     asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(v.x), "f"(v.y),
                  "f"(v.z), "f"(v.w), "l"(pol)
                  : "memory");
+}
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p));
 }
 __device__ __forceinline__ uint32_t ld_u32_hint(const void* p, uint64_t pol) {
     uint32_t v;
@@ -344,36 +360,332 @@ __device__ __forceinline__ uint32_t grpo_in8(int lane, int ua, int ub) {
     return in;
 }
 
+// Bits of the 16 mask bytes from token u (those at or past `end` left 0):
+// bit i set when byte u + i is nonzero.  kVec: one 16-byte load (the mask
+// 16-byte aligned, u a multiple of 16); it keeps the default L2 policy, so
+// that pass 3's read of the same bytes may still find them there.
 template <bool kVec>
-__global__ void __launch_bounds__(kGrpoPassThreads, 4) k_grpo_terms(GrpoArgs p, GrpoWork wk) {
-    const int lane = threadIdx.x & 31;
+__device__ __forceinline__ uint32_t grpo_mask_bits16(const uint8_t* mask, int64_t u, int64_t end) {
+    if (kVec && u + 16 <= end) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(mask + u));
+        const uint32_t x[4] = {w.x, w.y, w.z, w.w};
+        uint32_t b = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) b |= (((__vcmpne4(x[i], 0u) & 0x01010101u) * 0x01020408u) >> 24) << (4 * i);
+        return b;
+    }
+    uint32_t b = 0;
+    for (int i = 0; i < 16; ++i)
+        if (u + i < end && __ldg(mask + u + i) != 0) b |= 1u << i;
+    return b;
+}
+
+// Pass 1: the active tokens of each range of `range` tokens (a multiple of
+// 16) and, when there are sequences, of each 16-token word's range before
+// the word.  A round's word counts go through shared memory so that thread
+// t scans words [8 t, 8 t + 8) after the CTA's exclusive scan of the
+// threads' sums: the prefix runs in token order.
+template <bool kVec>
+__global__ void __launch_bounds__(kGrpoCountThreads) k_grpo_count(GrpoArgs p, GrpoWork wk, int64_t range) {
+    constexpr int kWords = kGrpoCountWords * kGrpoCountThreads;
+    __shared__ uint8_t sh_cnt[kWords];
+    __shared__ uint32_t sh_pre[kWords];
+    __shared__ uint32_t sh_wsum[kGrpoCountThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t t0 = (int64_t)blockIdx.x * range;
+    const int64_t t1 = t0 + range < p.n ? t0 + range : p.n;
+    griddep_launch_dependents();
+    int64_t base = 0;   // active tokens in [t0, r0)
+    for (int64_t r0 = t0; r0 < t1; r0 += kGrpoCountRound) {
+        const int64_t r1 = r0 + kGrpoCountRound < t1 ? r0 + kGrpoCountRound : t1;
+        uint32_t bits[kGrpoCountWords];
+        if (kVec) {   // every whole word's load first (predicated, no branch), then the bits
+            uint4 wv[kGrpoCountWords];
+#pragma unroll
+            for (int k = 0; k < kGrpoCountWords; ++k) {
+                const int64_t u = r0 + 16 * (int64_t)(k * kGrpoCountThreads + tid);
+                wv[k] = u + 16 <= r1 ? __ldg(reinterpret_cast<const uint4*>(p.mask + u)) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int k = 0; k < kGrpoCountWords; ++k) {
+                const int64_t u = r0 + 16 * (int64_t)(k * kGrpoCountThreads + tid);
+                const uint32_t x[4] = {wv[k].x, wv[k].y, wv[k].z, wv[k].w};
+                uint32_t b = 0;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) b |= (((__vcmpne4(x[i], 0u) & 0x01010101u) * 0x01020408u) >> 24) << (4 * i);
+                bits[k] = (u < r1 && u + 16 > r1) ? grpo_mask_bits16<false>(p.mask, u, r1) : b;   // the ragged end
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < kGrpoCountWords; ++k) {
+                const int64_t u = r0 + 16 * (int64_t)(k * kGrpoCountThreads + tid);
+                bits[k] = u < r1 ? grpo_mask_bits16<false>(p.mask, u, r1) : 0u;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kGrpoCountWords; ++k) sh_cnt[k * kGrpoCountThreads + tid] = (uint8_t)__popc(bits[k]);
+        __syncthreads();
+        uint32_t c[kGrpoCountWords], sum = 0;
+#pragma unroll
+        for (int i = 0; i < kGrpoCountWords; ++i) {
+            c[i] = sh_cnt[kGrpoCountWords * tid + i];
+            sum += c[i];
+        }
+        uint32_t incl = sum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        if (lane == 31) sh_wsum[warp] = incl;
+        __syncthreads();
+        uint32_t run = incl - sum, total = 0;
+#pragma unroll
+        for (int w = 0; w < kGrpoCountThreads / 32; ++w) {
+            const uint32_t x = sh_wsum[w];
+            run += w < warp ? x : 0u;
+            total += x;
+        }
+        if (p.cu != nullptr) {   // through shared memory, so that the stores are coalesced
+#pragma unroll
+            for (int i = 0; i < kGrpoCountWords; ++i) {
+                sh_pre[kGrpoCountWords * tid + i] = (uint32_t)base + run;
+                run += c[i];
+            }
+            __syncthreads();
+            const int64_t wn = ((r1 + 15) >> 4) - (r0 >> 4);   // words of the round
+#pragma unroll
+            for (int k = 0; k < kGrpoCountWords; ++k) {
+                const int j = k * kGrpoCountThreads + tid;
+                if (j < wn) wk.word_pre[(r0 >> 4) + j] = sh_pre[j];
+            }
+        }
+        base += total;
+        __syncthreads();   // the next round rewrites the shared arrays
+    }
+    if (tid == 0) wk.range_cnt[blockIdx.x] = base;
+}
+
+// Pass 2: thread t of CTA b takes sequence s = 256 b + t (then s + 256 G,
+// ...).  Its two bounds are loaded first; while they are in flight the CTA
+// scans the ranges' counts (with a mask; else every token is active); then
+// the word prefix and the mask word at each bound are loaded together, and
+// P(x) = the ranges before x + the word's prefix in its range + the word's
+// active tokens below x.  n_s = P(cu[s + 1]) - P(cu[s]) and its correctly
+// rounded reciprocal are written for the sequence mean of token means; each CTA writes its number of sequences
+// with an active token (not needed for the token mean).  CTA 0 writes the
+// active tokens D inside the sequences (or in the batch), zeroes pass 3's
+// ticket and writes the loss when there are no tokens.
+template <bool kVec>
+__global__ void __launch_bounds__(kGrpoFixThreads) k_grpo_fix(GrpoArgs p, GrpoWork wk, int64_t range, int nranges) {
+    constexpr int kW = kGrpoFixThreads / 32;
+    constexpr int kPer = kGrpoCountMaxCtas / kGrpoFixThreads;     // ranges per thread in the scan
+    __shared__ int64_t sh_pre[kGrpoCountMaxCtas];
+    __shared__ int64_t sh_w[kW];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    griddep_launch_dependents();
+    griddep_wait();
+    const bool counted = p.mask != nullptr && nranges > 0;
+    const bool per_seq = p.cu != nullptr && p.n > 0 && p.mode != 0;   // with no tokens cu_seqlens is not read
+    const int64_t step = (int64_t)gridDim.x * kGrpoFixThreads;
+    int64_t s = (int64_t)blockIdx.x * kGrpoFixThreads + tid;
+    int64_t xa = p.n, xb = p.n;
+    if (per_seq && s < p.nseq) {
+        xa = grpo_cu(p, s);
+        xb = grpo_cu(p, s + 1);
+    }
+    int64_t total = p.n;
+    if (counted) {   // thread t scans ranges [kPer t, kPer t + kPer)
+        int64_t v[kPer], sum = 0;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int r = kPer * tid + i;
+            v[i] = r < nranges ? __ldcg(reinterpret_cast<const long long*>(wk.range_cnt) + r) : 0;
+            sum += v[i];
+        }
+        int64_t incl = sum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int64_t y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += y;
+        }
+        if (lane == 31) sh_w[warp] = incl;
+        __syncthreads();
+        int64_t run = incl - sum;
+        total = 0;
+        for (int w = 0; w < kW; ++w) {
+            const int64_t x = sh_w[w];
+            run += w < warp ? x : 0;
+            total += x;
+        }
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            sh_pre[kPer * tid + i] = run;
+            run += v[i];
+        }
+        __syncthreads();
+    }
+    // the two loads of P(x) (none without a mask or at the end of the batch)
+    auto loads_at = [&](int64_t x, uint32_t& wpre, uint32_t& wbits) {
+        wpre = 0;
+        wbits = 0;
+        if (counted && x < p.n) {
+            wpre = __ldcg(wk.word_pre + (x >> 4));
+            wbits = grpo_mask_bits16<kVec>(p.mask, x & ~(int64_t)15, p.n);
+        }
+    };
+    auto active_before = [&](int64_t x, uint32_t wpre, uint32_t wbits) -> int64_t {
+        if (!counted) return x;
+        if (x >= p.n) return total;
+        return sh_pre[x / range] + (int64_t)wpre + __popc(wbits & ((1u << (x & 15)) - 1u));
+    };
+    int64_t A = 0;
+    while (per_seq && s < p.nseq) {
+        uint32_t pa, ba, pb, bb;
+        loads_at(xa, pa, ba);
+        loads_at(xb, pb, bb);
+        int64_t c = active_before(xb, pb, bb) - active_before(xa, pa, ba);
+        c = c < 0 ? 0 : c;
+        if (p.mode == 1) {
+            const float cf = (float)c;
+            wk.seg_cnt[s] = make_float2(cf, c > 0 ? __frcp_rn(cf) : 0.f);
+        }
+        A += c > 0 ? 1 : 0;
+        s += step;
+        if (s < p.nseq) {
+            xa = grpo_cu(p, s);
+            xb = grpo_cu(p, s + 1);
+        }
+    }
+    A = warp_sum_i64(A);
+    __syncthreads();   // sh_w is reused
+    if (lane == 0) sh_w[warp] = A;
+    __syncthreads();
+    if (tid == 0) {
+        A = 0;
+        for (int w = 0; w < kW; ++w) A += sh_w[w];
+        wk.a_part[blockIdx.x] = A;
+        if (blockIdx.x == 0) {
+            int64_t D = total;
+            if (p.cu != nullptr && p.n > 0) {
+                const int64_t x0 = grpo_cu(p, 0), x1 = grpo_cu(p, p.nseq);
+                uint32_t pa, ba, pb, bb;
+                loads_at(x0, pa, ba);
+                loads_at(x1, pb, bb);
+                D = active_before(x1, pb, bb) - active_before(x0, pa, ba);
+                D = D < 0 ? 0 : D;
+            }
+            *wk.dcnt = D;
+            *wk.ticket = 0u;
+            if (p.n == 0) p.loss[0] = 0.f;
+        }
+    }
+}
+
+// The normaliser and the uniform weight from the active tokens D and the
+// number A of sequences with an active token.
+struct GrpoNorm {
+    double den, cnt;
+    float wt;
+};
+__device__ __forceinline__ GrpoNorm grpo_norm(const GrpoArgs& p, int64_t A, int64_t D) {
+    const bool seqs = p.cu != nullptr && p.mode != 0 && p.n > 0;
+    const double cnt = (double)D;
+    const double aa = seqs ? (double)A : (D > 0 ? 1.0 : 0.0);
+    double den = (p.mode == 0) ? cnt : aa;
+    if (p.normalizer > 0.f) den = (double)p.normalizer;
+    double w = 0.0;
+    if (den > 0) w = (p.mode == 1 && p.cu == nullptr) ? (D > 0 ? 1.0 / (den * cnt) : 0.0) : 1.0 / den;
+    return {den, cnt, __double2float_rn(w)};
+}
+// The same on every lane of a warp: the fix kernel's A partials summed.
+__device__ __forceinline__ GrpoNorm grpo_norm_warp(const GrpoArgs& p, const GrpoWork& wk, int nfix, int lane) {
+    int64_t A = 0;
+    for (int i = lane; i < nfix; i += 32) A += __ldcg(reinterpret_cast<const long long*>(wk.a_part) + i);
+    A = warp_sum_i64(A);
+    return grpo_norm(p, A, __ldcg(reinterpret_cast<const long long*>(wk.dcnt)));
+}
+
+// A sequence's piece s over its active count c as two floats, from the
+// correctly rounded reciprocal inv = 1 / c: q = s inv, and the residual
+// s - q c (one rounding, by the fused multiply-add) times inv as the low
+// part, so that q + lo carries s / c to about 2^-46 relative.
+__device__ __forceinline__ FF ff_div_countf(float s, float c, float inv) {
+    const float q = __fmul_rn(s, inv);
+    const float r = __fmaf_rn(-q, c, s);
+    return {q, __fmul_rn(r, inv)};
+}
+
+// Folds v over the CTA: the fixed butterfly in each warp, then warp order
+// (thread 0 gets the result; every thread must call it).
+template <int kWarps>
+__device__ __forceinline__ FF cta_fold(FF v, FF* sh_v) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    v = ff_warp_sum(v);
+    __syncthreads();   // the shared slots may still be read by a previous fold
+    if (lane == 0) sh_v[warp] = v;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        v = FF{0.f, 0.f};
+        for (int w = 0; w < kWarps; ++w) v = ff_add(v, sh_v[w]);
+    }
+    return v;
+}
+
+// Pass 3 (see the top of this file).  kSeq: the sequence mean of token
+// means with sequences, i.e. a weight per sequence.  The weight is the
+// caller's (p.prescale > 0: the fix kernel is waited for only before the
+// ticket) or the fix kernel's (waited for first).
+template <bool kVec, bool kSeq>
+__global__ void __launch_bounds__(kGrpoPassThreads, 4) k_grpo_pass(GrpoArgs p, GrpoWork wk, int nfix) {
+    constexpr int kW = kGrpoPassThreads / 32;
+    __shared__ FF sh_t[kW], sh_q[kW];
+    __shared__ bool last;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t nchunks = grpo_chunks(p.n);
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const float clo = 1.f - p.eps_lo, chi = 1.f + p.eps_hi;
     griddep_launch_dependents();
-    const uint64_t in_pol = l2_evict_first();
-    // the scale pass re-reads the gradients: keep them in L2 (else they are final)
-    const uint64_t g_pol = p.prescale > 0.f ? l2_evict_first() : l2_evict_last();
-    if (blockIdx.x == 0 && threadIdx.x == 0) *wk.ticket = 0u;
-    // each warp takes a contiguous range of chunks: only its first chunk needs
-    // the search, later ones resume the run walk at the last sequence seen
+    const uint64_t pol = l2_evict_first();
+    const bool known = p.prescale > 0.f;
+    float wu = p.prescale, inv_den = 0.f;
     const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t w_end = (gw + 1) * nchunks / nwarps;
+    if (!known) {   // the counts and the weight
+        // while they are formed, the warp's first two chunks go to L2
+        const int64_t w0 = gw * nchunks / nwarps;
+        for (int64_t w = w0; w < w0 + 2 && w < w_end; ++w) {
+            const int64_t c0 = w * kGrpoChunk;
+            const int nv = (int)(p.n - c0 < kGrpoChunk ? p.n - c0 : kGrpoChunk);
+            const int line = lane & 7;   // 8 lines of 128 bytes per array and chunk
+            if (32 * line < nv) {
+                const float* arr = lane < 8 ? p.logp : lane < 16 ? p.old_logp : lane < 24 ? p.adv : p.ref_logp;
+                if (arr) prefetch_l2(arr + c0 + 32 * line);
+            }
+            if (p.mask && lane < 2 && 128 * lane < nv) prefetch_l2(p.mask + c0 + 128 * lane);
+        }
+        griddep_wait();
+        const GrpoNorm nm = grpo_norm_warp(p, wk, nfix, lane);
+        wu = nm.wt;
+        inv_den = nm.den > 0 ? __frcp_rn((float)nm.den) : 0.f;
+    }
+    FF T{0.f, 0.f}, Q{0.f, 0.f};
     int64_t s_resume = -1;
     for (int64_t w = gw * nchunks / nwarps; w < w_end; ++w) {
         const int64_t c0 = w * kGrpoChunk;
         const int nv = (int)(p.n - c0 < kGrpoChunk ? p.n - c0 : kGrpoChunk);   // tokens in the chunk
         float lp[kGrpoLaneTokens], od[kGrpoLaneTokens], av[kGrpoLaneTokens], rf[kGrpoLaneTokens];
-        grpo_ld8<kVec>(p.logp + c0, lane, nv, lp, in_pol);
-        grpo_ld8<kVec>(p.old_logp + c0, lane, nv, od, in_pol);
-        grpo_ld8<kVec>(p.adv + c0, lane, nv, av, in_pol);
-        if (p.ref_logp) grpo_ld8<kVec>(p.ref_logp + c0, lane, nv, rf, in_pol);
-        const uint32_t act = grpo_active8<kVec>(p.mask ? p.mask + c0 : nullptr, lane, nv, in_pol);
+        grpo_ld8<kVec>(p.logp + c0, lane, nv, lp, pol);
+        grpo_ld8<kVec>(p.old_logp + c0, lane, nv, od, pol);
+        grpo_ld8<kVec>(p.adv + c0, lane, nv, av, pol);
+        if (p.ref_logp) grpo_ld8<kVec>(p.ref_logp + c0, lane, nv, rf, pol);
+        const uint32_t act = grpo_active8<kVec>(p.mask ? p.mask + c0 : nullptr, lane, nv, pol);
         // overlaps the loads above
-        const GrpoRuns runs = (s_resume < 0 || p.cu == nullptr) ? grpo_runs_begin(p, c0, lane)
-                                                                 : grpo_runs_at(p, s_resume, c0, lane, nullptr);
+        const GrpoRuns runs = (s_resume < 0 || p.cu == nullptr)
+                                  ? (kSeq ? grpo_runs_at(p, grpo_find(p, c0, lane), c0, lane, wk.seg_cnt)
+                                          : grpo_runs_begin(p, c0, lane))
+                                  : grpo_runs_at(p, s_resume, c0, lane, kSeq ? wk.seg_cnt : nullptr);
         int64_t s_last = runs.s;
-        if (p.cu && p.mode == 1 && lane == 0) wk.chunk_first[w] = runs.s;
         float l[kGrpoLaneTokens], dl[kGrpoLaneTokens];
 #pragma unroll
         for (int q = 0; q < kGrpoLaneTokens; ++q) {
@@ -395,12 +707,12 @@ __global__ void __launch_bounds__(kGrpoPassThreads, 4) k_grpo_terms(GrpoArgs p, 
             dl[q] = on ? dl[q] : 0.f;
         }
         FF tot{0.f, 0.f};
-        int64_t tcnt = 0;
         uint32_t inseq = 0;
-        grpo_runs<false>(p, runs, c0, nv, lane, nullptr, [&](int64_t s, int ua, int ub, float) {
+        grpo_runs<kSeq>(p, runs, c0, nv, lane, kSeq ? wk.seg_cnt : nullptr,
+                        [&](int64_t s, int ua, int ub, float2 cnt_s) {
             s_last = s;
             // within the chunk, plain FP32: the lane's tokens in order, then the
-            // xor butterfly (lane 0 holds the result)
+            // xor butterfly (every lane holds the result)
             float rs = 0.f;
             uint32_t in;
             if (ua == 0 && ub == nv) {   // the whole chunk: no membership tests
@@ -415,13 +727,21 @@ __global__ void __launch_bounds__(kGrpoPassThreads, 4) k_grpo_terms(GrpoArgs p, 
             inseq |= in;
 #pragma unroll
             for (int off = 16; off >= 1; off >>= 1) rs = __fadd_rn(rs, __shfl_xor_sync(0xffffffffu, rs, off));
-            const int cnt = __reduce_add_sync(0xffffffffu, __popc(in & act));
-            if (p.cu && p.mode != 0 && lane == 0) {
-                wk.piece[s + w] = FF{rs, 0.f};
-                wk.piece_cnt[s + w] = cnt;
+            if (kSeq && p.cu) {
+                // the run's tokens times 1 / (den n_s): the product of the correctly
+                // rounded 1 / den and 1 / n_s
+                const float ws = __fmul_rn(inv_den, cnt_s.y);
+                if (in == 0xffu) {
+#pragma unroll
+                    for (int q = 0; q < kGrpoLaneTokens; ++q) dl[q] = __fmul_rn(dl[q], ws);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < kGrpoLaneTokens; ++q)
+                        if ((in >> q) & 1u) dl[q] = __fmul_rn(dl[q], ws);
+                }
+                if (cnt_s.x > 0.f) Q = ff_add(Q, ff_div_countf(rs, cnt_s.x, cnt_s.y));
             }
             tot = ff_add(tot, rs);
-            tcnt += cnt;
         });
         if (p.cu && inseq != 0xffu) {   // tokens outside every sequence
 #pragma unroll
@@ -431,263 +751,54 @@ __global__ void __launch_bounds__(kGrpoPassThreads, 4) k_grpo_terms(GrpoArgs p, 
                 dl[q] = in ? dl[q] : 0.f;
             }
         }
-        if (p.prescale > 0.f) {
+        if (!(kSeq && p.cu)) {   // one weight for every token
 #pragma unroll
-            for (int q = 0; q < kGrpoLaneTokens; ++q) dl[q] = __fmul_rn(dl[q], p.prescale);
+            for (int q = 0; q < kGrpoLaneTokens; ++q) dl[q] = __fmul_rn(dl[q], wu);
         }
-        grpo_st8<kVec>(p.grad + c0, lane, nv, dl, g_pol);
-        if (p.token_loss) grpo_st8<kVec>(p.token_loss + c0, lane, nv, l, in_pol);
-        if (lane == 0) {
-            wk.chunk_sum[w] = tot;
-            wk.chunk_cnt[w] = tcnt;
-        }
+        grpo_st8<kVec>(p.grad + c0, lane, nv, dl, pol);
+        if (p.token_loss) grpo_st8<kVec>(p.token_loss + c0, lane, nv, l, pol);
+        T = ff_add(T, tot);
         s_resume = s_last;   // no later chunk meets an earlier sequence
     }
-}
-
-// The mean of a sequence as two floats: sum / cnt, with the remainder of the
-// high quotient carried into the low part.
-__device__ __forceinline__ FF ff_div_count(FF s, int64_t cnt) {
-    const float c = (float)cnt;
-    const float q = __fdiv_rn(s.hi, c);
-    const float r = __fmaf_rn(-q, c, s.hi);   // s.hi - q c, exact for a correctly rounded q (c < 2^24)
-    return {q, __fdiv_rn(__fadd_rn(r, s.lo), c)};
-}
-
-// Folds v over the CTA: the fixed butterfly in each warp, then warp order
-// (thread 0 gets the result; every thread must call it).
-template <int kWarps>
-__device__ __forceinline__ FF cta_fold(FF v, int64_t& c, FF* sh_v, int64_t* sh_c) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    v = ff_warp_sum(v);
-    c = warp_sum_i64(c);
-    __syncthreads();   // the shared slots may still be read by a previous fold
+    if (known) griddep_wait();   // the ticket and the normaliser
+    // the CTA's sums (every lane of a warp holds its warp's), warps in order
     if (lane == 0) {
-        sh_v[warp] = v;
-        sh_c[warp] = c;
+        sh_t[warp] = T;
+        sh_q[warp] = Q;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        v = FF{0.f, 0.f};
-        c = 0;
-        for (int w = 0; w < kWarps; ++w) {
-            v = ff_add(v, sh_v[w]);
-            c += sh_c[w];
+        FF t{0.f, 0.f}, q{0.f, 0.f};
+        for (int i = 0; i < kW; ++i) {
+            t = ff_add(t, sh_t[i]);
+            q = ff_add(q, sh_q[i]);
         }
-    }
-    return v;
-}
-
-constexpr int64_t kGrpoLongPieces = 64;   // sequences with more pieces are folded by a whole warp
-
-// The fold of the loss and the normaliser, G CTAs (1 when n == 0).  CTA b
-// takes the b-th equal share of the chunk totals and, for the sequence
-// normalisers, of the sequences: one lane per sequence folds up to 64 of its
-// chunk pieces (chunks floor(a / 256) .. floor((b - 1) / 256), at slots
-// s + chunk) in piece order; a longer sequence is folded by its whole warp
-// (lane-strided, fixed butterfly) -- which of the two depends only on the
-// sequence -- giving its active count (kept for the scale pass) and mean.
-// Each CTA writes its partials; the CTA that finishes last (an atomic
-// ticket, no waiting) folds the partials in CTA order and writes the loss,
-// the normaliser and the uniform weight.
-__global__ void __launch_bounds__(kGrpoReduceThreads) k_grpo_reduce(GrpoArgs p, GrpoWork wk) {
-    constexpr int kW = kGrpoReduceThreads / 32;
-    __shared__ FF sh_v[kW];
-    __shared__ int64_t sh_c[kW];
-    __shared__ bool last;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int G = gridDim.x, b = blockIdx.x;
-    const int64_t nchunks = grpo_chunks(p.n);
-    const bool seqs = p.cu != nullptr && p.mode != 0 && p.n > 0;
-    griddep_launch_dependents();
-    // cu_seqlens is the caller's: its first bounds are read before the wait
-    const int64_t qs = seqs ? (p.nseq + G - 1) / G : 0;
-    const int64_t s0 = b * qs, s1 = seqs ? (s0 + qs < p.nseq ? s0 + qs : p.nseq) : 0;
-    int64_t a_first = 0, e_first = 0;
-    if (s0 + 32 * warp + lane < s1) {
-        a_first = grpo_cu(p, s0 + 32 * warp + lane);
-        e_first = grpo_cu(p, s0 + 32 * warp + lane + 1);
-    }
-    griddep_wait();
-    // chunk totals [b ps, (b + 1) ps): the thread's first one is loaded now,
-    // with the sequences' first pieces below, and added first
-    const int64_t ps = (nchunks + G - 1) / G;
-    const int64_t k1 = (b + 1) * ps < nchunks ? (b + 1) * ps : nchunks;
-    const int64_t kf = b * ps + threadIdx.x;
-    const FF t_first = kf < k1 ? wk.chunk_sum[kf] : FF{0.f, 0.f};
-    const int64_t c_first = kf < k1 ? wk.chunk_cnt[kf] : 0;
-    FF Q{0.f, 0.f};
-    int64_t A = 0;
-    if (seqs) {   // the sequences [s0, s1)
-        for (int64_t base = s0 + 32 * warp; base < s1; base += kGrpoReduceThreads) {   // warp-uniform
-            const int64_t s = base + lane;
-            int64_t j0 = 0, j1 = -1;
-            if (s < s1) {
-                const bool first = base == s0 + 32 * warp;
-                const int64_t a = first ? a_first : grpo_cu(p, s), e = first ? e_first : grpo_cu(p, s + 1);
-                if (e > a) {
-                    j0 = s + a / kGrpoChunk;
-                    j1 = s + (e - 1) / kGrpoChunk;
-                }
-            }
-            const bool is_long = j1 - j0 + 1 > kGrpoLongPieces;
-            FF sum{0.f, 0.f};
-            int64_t cnt = 0;
-            if (!is_long) {   // up to 8 pieces per round, all loaded before they are added in order
-                for (int64_t j = j0; j <= j1; j += 8) {
-                    FF v[8];
-                    int64_t c[8];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        v[u] = j + u <= j1 ? wk.piece[j + u] : FF{0.f, 0.f};
-                        c[u] = j + u <= j1 ? wk.piece_cnt[j + u] : 0;
-                    }
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        if (j + u <= j1) {
-                            sum = ff_add(sum, v[u]);
-                            cnt += c[u];
-                        }
-                    }
-                }
-            }
-            // the warp's long sequences, one at a time in lane order
-            for (uint32_t m = __ballot_sync(0xffffffffu, is_long); m != 0; m &= m - 1) {
-                const int src = __ffs(m) - 1;
-                const int64_t k0 = __shfl_sync(0xffffffffu, j0, src), kl = __shfl_sync(0xffffffffu, j1, src);
-                FF ws{0.f, 0.f};
-                int64_t wc = 0;
-                for (int64_t j = k0 + lane; j <= kl; j += 32) {
-                    ws = ff_add(ws, wk.piece[j]);
-                    wc += wk.piece_cnt[j];
-                }
-                ws = ff_warp_sum(ws);
-                wc = warp_sum_i64(wc);
-                const FF w0{__shfl_sync(0xffffffffu, ws.hi, 0), __shfl_sync(0xffffffffu, ws.lo, 0)};
-                wc = __shfl_sync(0xffffffffu, wc, 0);
-                if (lane == src) {
-                    sum = w0;
-                    cnt = wc;
-                }
-            }
-            if (s < s1) {
-                wk.seg_inv[s] = cnt > 0 ? __frcp_rn((float)cnt) : 0.f;
-                if (cnt > 0) {
-                    ++A;
-                    if (p.mode == 1) Q = ff_add(Q, ff_div_count(sum, cnt));
-                }
-            }
-        }
-    }
-    FF T = t_first;
-    int64_t C = c_first;
-    for (int64_t k = kf + kGrpoReduceThreads; k < k1; k += kGrpoReduceThreads) {
-        T = ff_add(T, wk.chunk_sum[k]);
-        C += wk.chunk_cnt[k];
-    }
-    T = cta_fold<kW>(T, C, sh_v, sh_c);
-    if (seqs) Q = cta_fold<kW>(Q, A, sh_v, sh_c);
-    if (G == 1) {
-        if (threadIdx.x == 0) {
-            wk.part_t[0] = T;
-            wk.part_q[0] = Q;
-            wk.part_c[0] = C;
-            wk.part_a[0] = A;
-        }
-    } else {
-        if (threadIdx.x == 0) {
-            wk.part_t[b] = T;
-            wk.part_q[b] = Q;
-            wk.part_c[b] = C;
-            wk.part_a[b] = A;
-            __threadfence();
-            last = atomicAdd(wk.ticket, 1u) == (unsigned)(G - 1);
-        }
-        __syncthreads();
-        if (!last) return;
+        wk.part_t[blockIdx.x] = t;
+        wk.part_q[blockIdx.x] = q;
         __threadfence();
+        last = atomicAdd(wk.ticket, 1u) == gridDim.x - 1;
     }
-    // the last CTA: thread i takes partials i, i + 256, ... in order; the CTA
-    // fold combines them (a fixed butterfly per warp, then warp order)
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    // the last CTA: thread i takes the CTAs i, i + 256, ... in order, then the
+    // CTA fold (a fixed butterfly per warp, then warp order)
     FF t{0.f, 0.f}, q{0.f, 0.f};
-    int64_t c = 0, a = 0;
-    for (int i = threadIdx.x; i < G; i += kGrpoReduceThreads) {
+    for (int i = threadIdx.x; i < (int)gridDim.x; i += kGrpoPassThreads) {
         const float2 tv = __ldcg(reinterpret_cast<const float2*>(wk.part_t) + i);
         const float2 qv = __ldcg(reinterpret_cast<const float2*>(wk.part_q) + i);
         t = ff_add(t, FF{tv.x, tv.y});
         q = ff_add(q, FF{qv.x, qv.y});
-        c += __ldcg(reinterpret_cast<const long long*>(wk.part_c) + i);
-        a += __ldcg(reinterpret_cast<const long long*>(wk.part_a) + i);
     }
-    t = cta_fold<kW>(t, c, sh_v, sh_c);
-    q = cta_fold<kW>(q, a, sh_v, sh_c);
+    t = cta_fold<kW>(t, sh_t);
+    q = cta_fold<kW>(q, sh_q);
+    const GrpoNorm nm = warp == 0 ? grpo_norm_warp(p, wk, nfix, lane) : GrpoNorm{0.0, 0.0, 0.f};
     if (threadIdx.x == 0) {
-        const double tt = ff_value(t), cnt = (double)c;
-        double qq = ff_value(q), aa = (double)a;
-        if (!seqs) {   // the whole batch is one sequence (or token mean)
-            aa = c > 0 ? 1.0 : 0.0;
-            qq = c > 0 ? tt / cnt : 0.0;
-        }
-        double den = (p.mode == 0) ? cnt : aa;
-        if (p.normalizer > 0.f) den = (double)p.normalizer;
-        const double num = (p.mode == 1) ? qq : tt;
+        const double den = nm.den, cnt = nm.cnt;
+        const double tt = ff_value(t);
+        double num = tt;
+        if (p.mode == 1) num = p.cu ? ff_value(q) : (cnt > 0 ? tt / cnt : 0.0);
         p.loss[0] = den > 0 ? __double2float_rn(num / den) : 0.f;
-        wk.den[0] = den;
-        wk.den[1] = cnt;
-        double w = 0.0;
-        if (den > 0) w = (p.mode == 1 && p.cu == nullptr) ? (c > 0 ? 1.0 / (den * cnt) : 0.0) : 1.0 / den;
-        wk.wt[0] = __double2float_rn(w);
-        if (G > 1) *wk.ticket = 0u;
-    }
-}
-
-// Each token's gradient times its weight: 1 / den, or for the sequence mean
-// of token means with sequences 1 / (den n_s), n_s the sequence's active
-// tokens (formed in FP32 as the product of the correctly rounded 1 / den and
-// 1 / n_s, the latter kept per sequence by the fold).  Each warp takes a contiguous range of chunks (as in pass 1):
-// the range's first sequence was recorded by pass 1, later chunks resume at
-// the last sequence seen.
-template <bool kVec>
-__global__ void __launch_bounds__(kGrpoPassThreads, 5) k_grpo_scale(GrpoArgs p, GrpoWork wk) {
-    const int lane = threadIdx.x & 31;
-    const int64_t nchunks = grpo_chunks(p.n);
-    griddep_wait();
-    const double den = wk.den[0];
-    const bool zero = !(den > 0);   // no active token: every gradient is 0 already (rewritten,
-                                    // so that the lines kept in L2 by pass 1 are released)
-    const float wu = zero ? 0.f : wk.wt[0];
-    const uint64_t pol = l2_evict_first();
-    const bool per_seq = !zero && p.mode == 1 && p.cu != nullptr;
-    const float denf = (float)den;
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t w_end = (gw + 1) * nchunks / nwarps;
-    int64_t w = gw * nchunks / nwarps;
-    int64_t s_resume = per_seq && w < w_end ? wk.chunk_first[w] : 0;
-    const float inv_den = zero ? 0.f : __frcp_rn(denf);
-    for (; w < w_end; ++w) {
-        const int64_t c0 = w * kGrpoChunk;
-        const int nv = (int)(p.n - c0 < kGrpoChunk ? p.n - c0 : kGrpoChunk);
-        float g[kGrpoLaneTokens];
-        grpo_ld8<kVec, true>(p.grad + c0, lane, nv, g, pol);
-        if (per_seq) {
-            const GrpoRuns runs = grpo_runs_at(p, s_resume, c0, lane, wk.seg_inv);
-            int64_t s_last = runs.s;
-            // each run's tokens times its weight; tokens in no sequence hold 0 already
-            grpo_runs<true>(p, runs, c0, nv, lane, wk.seg_inv, [&](int64_t s, int ua, int ub, float inv_cnt) {
-                s_last = s;
-                const float ws = __fmul_rn(inv_den, inv_cnt);
-                const uint32_t in = (ua == 0 && ub == nv) ? 0xffu : grpo_in8(lane, ua, ub);
-#pragma unroll
-                for (int q = 0; q < kGrpoLaneTokens; ++q)
-                    if ((in >> q) & 1u) g[q] = __fmul_rn(g[q], ws);
-            });
-            s_resume = s_last;
-        } else {
-#pragma unroll
-            for (int q = 0; q < kGrpoLaneTokens; ++q) g[q] = __fmul_rn(g[q], wu);
-        }
-        grpo_st8<kVec>(p.grad + c0, lane, nv, g, pol);
     }
 }
 

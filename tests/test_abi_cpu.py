@@ -281,13 +281,15 @@ def test_grpo_binding_rejects_an_unknown_mode():
 
 def test_grpo_host_checks(lib):
     b = ctypes.c_int64(0)
-    # 32 bytes of normaliser words, room for 1024 fold partials of 32 bytes,
-    # 16 per 256-token chunk, and with S sequences 16 per piece slot (S +
-    # chunks), 8 per chunk and 4 per sequence; rounded up to 256:
-    # 32 + 32768 + 16*128 = 34848 -> 35072;  + 16*228 + 8*128 + 4*100 -> 39936
-    assert lib.logp_grpo_loss_workspace_size(32768, 0, ctypes.byref(b)) == 0 and b.value == 35072
-    assert lib.logp_grpo_loss_workspace_size(32768, 100, ctypes.byref(b)) == 0 and b.value == 39936
-    assert lib.logp_grpo_loss_workspace_size(0, 0, ctypes.byref(b)) == 0 and b.value == 33024
+    # 32 bytes of count and ticket, two 8-byte sums per CTA of the token pass
+    # (608), 8 bytes per CTA of the sequences' counts (1024) and per count
+    # range (1024), and with S sequences 8 per sequence and 4 per 16 tokens;
+    # rounded up to 256; without sequences n does not enter:
+    # 32 + 9728 + 8192 + 8192 = 26144 -> 26368;  + 8*100 + 4*2048 = 35136 -> 35328
+    assert lib.logp_grpo_loss_workspace_size(32768, 0, ctypes.byref(b)) == 0 and b.value == 26368
+    assert lib.logp_grpo_loss_workspace_size(32768, 100, ctypes.byref(b)) == 0 and b.value == 35328
+    assert lib.logp_grpo_loss_workspace_size(0, 0, ctypes.byref(b)) == 0 and b.value == 26368
+    assert lib.logp_grpo_loss_workspace_size(1 << 31, 0, ctypes.byref(b)) == 0 and b.value == 26368
     assert lib.logp_grpo_loss_workspace_size(-1, 0, ctypes.byref(b)) == EINVAL
 
     def call(mode=0, ws=1 << 20, ws_bytes=1 << 20, n=1000, eps_lo=0.2):

@@ -79,8 +79,9 @@ def test_linear_forward_replays_bitwise():
 
 
 def test_grpo_loss_replays_bitwise():
-    """The GRPO loss (its fold and scale kernels are launched as programmatic
-    dependents of their predecessors) captured in a graph replays bitwise."""
+    """The GRPO loss (its count fix and token pass are launched as
+    programmatic dependents of their predecessors) captured in a graph
+    replays bitwise."""
     g = torch.Generator().manual_seed(31)
     n, nseq = 50000, 77
     lp = -torch.rand(n, generator=g) * 5
