@@ -681,7 +681,7 @@ def run_grpo(args, side=False):
                                f"{nseq} packed sequences of random lengths, 10% inactive (synthetic)",
                    "n": n, "num_seqs": nseq, "parallelism": "single GPU",
                    "l2": f"inputs {n * 17 / 1e6:.0f} MB per step against a 129 MB L2 (no flush)"},
-        "roofline": {"kernel": "k_grpo_terms + k_grpo_reduce + k_grpo_scale (the whole call)",
+        "roofline": {"kernel": "k_grpo_count + k_grpo_fix + k_grpo_pass (the whole call)",
                      "bound": "hbm",
                      "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4),
                      "peak_source": src, "bytes_per_token": bpt, "traffic": None},

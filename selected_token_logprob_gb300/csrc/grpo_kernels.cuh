@@ -271,9 +271,6 @@ __device__ __forceinline__ void st_f4_hint(float* p, float4 v, uint64_t pol) {
                  "f"(v.z), "f"(v.w), "l"(pol)
                  : "memory");
 }
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-    asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p));
-}
 __device__ __forceinline__ uint32_t ld_u32_hint(const void* p, uint64_t pol) {
     uint32_t v;
     asm("ld.global.nc.L1::no_allocate.L2::cache_hint.u32 %0, [%1], %2;" : "=r"(v) : "l"(p), "l"(pol));
@@ -652,18 +649,6 @@ __global__ void __launch_bounds__(kGrpoPassThreads, 4) k_grpo_pass(GrpoArgs p, G
     const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t w_end = (gw + 1) * nchunks / nwarps;
     if (!known) {   // the counts and the weight
-        // while they are formed, the warp's first two chunks go to L2
-        const int64_t w0 = gw * nchunks / nwarps;
-        for (int64_t w = w0; w < w0 + 2 && w < w_end; ++w) {
-            const int64_t c0 = w * kGrpoChunk;
-            const int nv = (int)(p.n - c0 < kGrpoChunk ? p.n - c0 : kGrpoChunk);
-            const int line = lane & 7;   // 8 lines of 128 bytes per array and chunk
-            if (32 * line < nv) {
-                const float* arr = lane < 8 ? p.logp : lane < 16 ? p.old_logp : lane < 24 ? p.adv : p.ref_logp;
-                if (arr) prefetch_l2(arr + c0 + 32 * line);
-            }
-            if (p.mask && lane < 2 && 128 * lane < nv) prefetch_l2(p.mask + c0 + 128 * lane);
-        }
         griddep_wait();
         const GrpoNorm nm = grpo_norm_warp(p, wk, nfix, lane);
         wu = nm.wt;
