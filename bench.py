@@ -626,7 +626,7 @@ def run_grpo(args, side=False):
     gbs = alg / (ms * 1e-3) / 1e9
     peak, src = _peaks()
     # token mean with the caller's normaliser (e.g. a count over all
-    # micro-batches): the weight is known up front, no scale pass
+    # micro-batches): the weight is known up front, nothing is counted
     kw_tm = dict(ref_logp=ref, active_mask=mask, cu_seqlens=cu, mode="token_mean", eps_lo=0.2, eps_hi=0.28,
                  beta=0.04, normalizer=float(n), workspace=ws)
     for _ in range(3):

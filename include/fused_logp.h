@@ -451,25 +451,28 @@ flp_status fused_linear_logp_forward_noalloc(const void* hidden, int64_t n, int6
  *   token_loss [n] FP32 out or NULL: l per token (0 when inactive).
  *   workspace  device scratch of logp_grpo_loss_workspace_size(n, num_seqs)
  *              bytes (16-byte aligned), caller-owned, no initial contents
- *              needed: 32 bytes of normaliser words, 32 KB for the fold's
- *              partials, a two-float sum and a count per 256-token chunk,
- *              and with sequences the same per (sequence, chunk) piece slot
- *              (num_seqs + ceil(n / 256) slots), a sequence index per chunk
- *              and a float per sequence; rounded up to 256 bytes.  One
- *              workspace serves one call at a time.
+ *              needed: 32 bytes for a count and the fold's ticket, 9.5 KB
+ *              for the token pass's per-CTA sums, 16 KB of counts, and with
+ *              sequences 8 bytes per sequence and 4 per 16 tokens; rounded
+ *              up to 256 bytes.  One workspace serves one call at a time.
  * Tokens outside every sequence (before cu_seqlens[0] or from
  * cu_seqlens[num_seqs] on) are inactive: l = 0, grad 0.  cu_seqlens must be
  * non-decreasing; for one that is not, the result is unspecified, but every
  * access stays inside the arrays.
- * Deterministic: the batch is cut into fixed 256-token chunks (one warp
- * each) whatever the sequence lengths; each sequence's sums are a fold of its
- * chunk pieces in a fixed order, and the fold of the chunk totals has a shape
- * fixed by the problem's shape (G shares, then the shares in order); the
- * weights are applied last (by the first pass when normalizer > 0 makes the
- * weight uniform).  Sums are plain FP32 within a 256-token chunk and
- * compensated two-float sums in FP32 from there on.  The result does not
- * depend on the grid or on timing.  With logp == old_logp the ratio is
- * exactly 1 and grad = -A times the weight (the KL = 0 identity of PR 5).
+ * Kernels: when a weight depends on the mask (any normaliser but the
+ * caller's uniform one), a count of the mask's active tokens per 16-token
+ * word and per range, then per sequence its active count, the number of
+ * non-empty sequences and the active tokens; then one token pass that
+ * writes each final gradient once and folds the loss.  Integer counts are
+ * exact.  Deterministic: the batch is cut into fixed 256-token chunks (one
+ * warp each) whatever the sequence lengths; sums are plain FP32 within a
+ * chunk and compensated two-float sums in FP32 from there on, folded per
+ * warp over its contiguous chunks, per CTA in warp order and over the CTAs
+ * in order, a shape fixed by n; the result does not depend on timing.  A
+ * gradient is dl/dlogp times its weight, rounded once: 1 / den, or for the
+ * sequence mean of token means the product of the correctly rounded 1 / den
+ * and 1 / n_s.  With logp == old_logp the ratio is exactly 1 and grad = -A
+ * times the weight (the KL = 0 identity of PR 5).
  * Errors: FLP_EINVAL for a bad mode, eps_lo outside [0, 1), a negative or
  * non-finite eps_hi, beta or normalizer, a sequence mode without sequences,
  * or num_seqs >= 2^31 - 1.

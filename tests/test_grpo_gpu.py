@@ -140,8 +140,9 @@ def test_rl_step_chain_against_fp64():
 
 @pytest.mark.parametrize("mode", MODES)
 def test_grpo_many_segments_against_oracle(mode):
-    """A million tokens in 3000 packed sequences (many CTAs in the terms and
-    scale passes) and the whole-batch form (1024 chunks), against FP64."""
+    """A million tokens in 3000 packed sequences (many CTAs in the mask count,
+    the sequence counts and the token pass) and the whole-batch form (1024
+    chunks), against FP64."""
     n = 1 << 20
     lp, old, ref, adv, mask, cu = _case(n, 11, nseq=3000)
     for cuv in (cu, None):
@@ -203,8 +204,9 @@ def test_grpo_uncovered_tiny_and_long_sequences(mode):
 
 
 def test_grpo_one_long_sequence_mean_of_means():
-    """One sequence of 300000 tokens given by cu_seqlens (its 1172 chunk
-    pieces folded by one warp) equals the whole-batch form."""
+    """One sequence of 300000 tokens given by cu_seqlens (its 1172 chunks on
+    many warps, its count from the word prefixes at its two bounds) equals
+    the whole-batch form."""
     n = 300000
     lp, old, ref, adv, mask, _ = _case(n, 23)
     cu = torch.tensor([0, n], dtype=torch.int64)
@@ -219,10 +221,11 @@ def test_grpo_one_long_sequence_mean_of_means():
         assert np.max(np.abs(grad.double().cpu().numpy() - want_g)) <= 1e-5 * np.max(np.abs(want_g))
 
 
-def test_grpo_first_pass_weight_equals_scale_pass():
-    """A normaliser equal to the active-token count makes the weight known up
-    front (applied by the first pass, no scale pass): loss and gradient are
-    bitwise those of the two-step form that derives the count on the device."""
+def test_grpo_caller_weight_equals_counted_weight():
+    """A normaliser equal to the active-token count (or the number of
+    non-empty sequences) makes the weight the caller's, and nothing is
+    counted: loss and gradient are bitwise those of the form that counts the
+    mask on the device."""
     n = 100000
     lp, old, ref, adv, mask, cu = _case(n, 24, nseq=333)
     d = float(int(mask.sum()))
