@@ -459,7 +459,8 @@ def _side_paths(args):
             sub.steps = 20
             line = run_grpo(sub, side=True)
             keep = ("metric", "value", "unit", "steps", "ms_per_step", "config", "roofline",
-                    "token_mean_with_normalizer", "small_call_us", "gpu_launches", "clocks")
+                    "token_mean_with_normalizer", "counts_taken_beforehand", "small_call_us", "gpu_launches",
+                    "clocks")
         else:
             raise SystemExit(f"--side-paths: unknown path {name!r}")
         out[name] = {k: line[k] for k in keep}
@@ -640,6 +641,19 @@ def run_grpo(args, side=False):
     b_.record(stream)
     torch.cuda.synchronize(dev)
     tm_ms = a_.elapsed_time(b_) / args.steps
+    # the same call with the batch layout's counts taken beforehand (once per
+    # batch, e.g. on a second stream during the logp forward, or reused over
+    # several epochs): the token pass alone
+    flp.logp_grpo_loss_counts(n, active_mask=mask, cu_seqlens=cu, mode="seq_mean_token_mean", workspace=ws)
+    for _ in range(3):
+        flp.logp_grpo_loss(lp, old, adv, counted=True, **kw)
+    torch.cuda.synchronize(dev)
+    a_.record(stream)
+    for _ in range(args.steps):
+        flp.logp_grpo_loss(lp, old, adv, counted=True, **kw)
+    b_.record(stream)
+    torch.cuda.synchronize(dev)
+    counted_ms = a_.elapsed_time(b_) / args.steps
     # GPU time of one call at the logits workloads' size (32768 tokens, 256
     # sequences): 20 calls captured in a CUDA graph and replayed, so that the
     # host's per-call overhead does not show
@@ -689,6 +703,11 @@ def run_grpo(args, side=False):
         "token_mean_with_normalizer": {"ms_per_step": round(tm_ms, 4),
                                        "GB/s": round(alg / (tm_ms * 1e-3) / 1e9, 1),
                                        "frac": round(alg / (tm_ms * 1e-3) / 1e9 / peak, 4)},
+        "counts_taken_beforehand": {"ms_per_step": round(counted_ms, 4),
+                                    "GB/s": round(alg / (counted_ms * 1e-3) / 1e9, 1),
+                                    "frac": round(alg / (counted_ms * 1e-3) / 1e9 / peak, 4),
+                                    "note": "logp_grpo_loss(counted=True) after one logp_grpo_loss_counts for "
+                                            "the batch layout: the token pass alone"},
         "e2e": None if e2e_ms is None else
         {"value": round(alg / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(e2e_ms, 3),
          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4},

@@ -489,6 +489,44 @@ flp_status logp_grpo_loss(const float* logp, const float* old_logp, const float*
                           flp_stream_t stream);
 
 /*
+ * The GRPO loss in two parts, for a batch whose layout (active_mask,
+ * cu_seqlens, n, num_seqs, mode, normalizer) is known before its logp: the
+ * normaliser weights depend on the layout only (issue #241 PR 5's declared
+ * normaliser), so they can be counted once, e.g. on a second stream while
+ * the logp forward runs, or once for several optimisation epochs over the
+ * same batch.
+ *
+ * logp_grpo_loss_counts runs the counting kernels of logp_grpo_loss (the
+ * mask's counts, each sequence's active count, the number of non-empty
+ * sequences) into `workspace` and records a tag of the layout: the mask and
+ * cu_seqlens pointers, n, num_seqs, mode and normalizer.  Arguments as for
+ * logp_grpo_loss; nothing else is read or written.
+ *
+ * logp_grpo_loss_counted is logp_grpo_loss with the counting left out: it
+ * runs the token pass on counts that an earlier logp_grpo_loss_counts (or
+ * logp_grpo_loss) call left in the same workspace, which must have completed
+ * on the device first (same stream, or an event).  Results are bitwise those
+ * of logp_grpo_loss.  The layout arguments must be the ones the counts were
+ * taken for and the mask and cu_seqlens contents unchanged since: the token
+ * pass compares the recorded tag with the call's, and on a mismatch writes
+ * NaN for the loss and for the gradient of every token inside a sequence (the
+ * contents themselves are not compared).  Calls may repeat on the same
+ * counts.  When the weight is the caller's (a normalizer with the token mean
+ * or the sequence mean of token sums) nothing is counted and the call is
+ * logp_grpo_loss.
+ * Errors: as logp_grpo_loss.
+ */
+flp_status logp_grpo_loss_counts(const uint8_t* active_mask, const int64_t* cu_seqlens, int64_t num_seqs,
+                                 int64_t n, int mode, float normalizer, void* workspace, int64_t workspace_bytes,
+                                 flp_stream_t stream);
+flp_status logp_grpo_loss_counted(const float* logp, const float* old_logp, const float* ref_logp,
+                                  const float* advantages, const uint8_t* active_mask,
+                                  const int64_t* cu_seqlens, int64_t num_seqs, int64_t n, int mode,
+                                  float eps_lo, float eps_hi, float beta, float normalizer, void* workspace,
+                                  int64_t workspace_bytes, float* loss, float* grad, float* token_loss,
+                                  flp_stream_t stream);
+
+/*
  * Health of the device side (no counterpart in the pages: a guard of this
  * library's own waits).  The bulk-copy forward waits on its own copies with a
  * bounded wait (about 2 s); if one runs out, the kernel records it in a

@@ -63,6 +63,7 @@ __all__ = [
     "fused_linear_logp_shard_partials",
     "fused_linear_logp_workspace_size",
     "logp_grpo_loss",
+    "logp_grpo_loss_counts",
     "logp_grpo_loss_workspace_size",
     "logp_merge_gathered_partials",
     "logp_merge_partials",
@@ -370,17 +371,31 @@ def logp_merge_gathered_partials(gathered: torch.Tensor, vocab_starts, real_widt
     return (logp, lse, lse_lo) if want_lo else (logp, lse)
 
 
+def _grpo_layout(cu_seqlens):
+    """(cu_seqlens contiguous or None, number of sequences)."""
+    if cu_seqlens is None:
+        return None, 0
+    if cu_seqlens.dtype != torch.int64 or cu_seqlens.dim() != 1 or cu_seqlens.shape[0] < 1:
+        raise ValueError("cu_seqlens must be an int64 [S + 1] tensor")
+    _cuda(cu_seqlens)
+    cu_seqlens = cu_seqlens.contiguous()
+    return cu_seqlens, cu_seqlens.shape[0] - 1
+
+
 def logp_grpo_loss(logp: torch.Tensor, old_logp: torch.Tensor, advantages: torch.Tensor,
                    ref_logp: torch.Tensor | None = None, active_mask: torch.Tensor | None = None,
                    cu_seqlens: torch.Tensor | None = None, mode: str = "token_mean",
                    eps_lo: float = 0.2, eps_hi: float = 0.2, beta: float = 0.0,
                    normalizer: float = 0.0, token_loss: bool = False,
-                   workspace: torch.Tensor | None = None):
+                   workspace: torch.Tensor | None = None, counted: bool = False):
     """GRPO clipped-surrogate loss of per-token logp: (loss FP32 [1], grad
     FP32 [N] = d loss / d logp) [+ per-token loss FP32 [N] if token_loss].
     ``grad`` is the upstream gradient for ``fused_logp_backward``.
     ``workspace`` (a CUDA byte tensor of logp_grpo_loss_workspace_size(N, S)
-    bytes) is allocated when not given."""
+    bytes) is allocated when not given.  With ``counted`` the normaliser
+    counts are not taken again: ``workspace`` must hold the counts of an
+    earlier ``logp_grpo_loss_counts`` (or ``logp_grpo_loss``) call for the
+    same active_mask, cu_seqlens, mode and normalizer tensors and values."""
     if mode not in GRPO_MODES:
         raise ValueError(f"mode must be one of {sorted(GRPO_MODES)} (got {mode!r})")
     n = logp.shape[0] if logp.dim() == 1 else -1
@@ -391,28 +406,53 @@ def logp_grpo_loss(logp: torch.Tensor, old_logp: torch.Tensor, advantages: torch
         _vec(ref_logp, "ref_logp", n, torch.float32)
         _cuda(ref_logp)
     mp = _mask(active_mask, n)
-    nseq = 0
-    if cu_seqlens is not None:
-        if cu_seqlens.dtype != torch.int64 or cu_seqlens.dim() != 1 or cu_seqlens.shape[0] < 1:
-            raise ValueError("cu_seqlens must be an int64 [S + 1] tensor")
-        _cuda(cu_seqlens)
-        cu_seqlens = cu_seqlens.contiguous()
-        nseq = cu_seqlens.shape[0] - 1
+    cu_seqlens, nseq = _grpo_layout(cu_seqlens)
     dev = logp.device
     loss = torch.empty(1, dtype=torch.float32, device=dev)
     grad = torch.empty(n, dtype=torch.float32, device=dev)
     tl = torch.empty(n, dtype=torch.float32, device=dev) if token_loss else None
     if workspace is None:
+        if counted:
+            raise ValueError("counted=True needs the workspace that holds the counts")
         workspace = torch.empty(logp_grpo_loss_workspace_size(n, nseq), dtype=torch.uint8, device=dev)
     _cuda(workspace)
-    st = _lib.load().logp_grpo_loss(logp.data_ptr(), old_logp.data_ptr(), _opt_ptr(ref_logp),
-                                    advantages.data_ptr(), mp, _opt_ptr(cu_seqlens), nseq, n,
-                                    GRPO_MODES[mode], float(eps_lo), float(eps_hi), float(beta),
-                                    float(normalizer), workspace.data_ptr(),
-                                    workspace.numel() * workspace.element_size(), loss.data_ptr(),
-                                    grad.data_ptr(), _opt_ptr(tl), _stream(logp))
-    _lib.check("logp_grpo_loss", st)
+    fn = "logp_grpo_loss_counted" if counted else "logp_grpo_loss"
+    st = getattr(_lib.load(), fn)(logp.data_ptr(), old_logp.data_ptr(), _opt_ptr(ref_logp),
+                                  advantages.data_ptr(), mp, _opt_ptr(cu_seqlens), nseq, n,
+                                  GRPO_MODES[mode], float(eps_lo), float(eps_hi), float(beta),
+                                  float(normalizer), workspace.data_ptr(),
+                                  workspace.numel() * workspace.element_size(), loss.data_ptr(),
+                                  grad.data_ptr(), _opt_ptr(tl), _stream(logp))
+    _lib.check(fn, st)
     return (loss, grad, tl) if token_loss else (loss, grad)
+
+
+def logp_grpo_loss_counts(n: int, active_mask: torch.Tensor | None = None,
+                          cu_seqlens: torch.Tensor | None = None, mode: str = "token_mean",
+                          normalizer: float = 0.0, workspace: torch.Tensor | None = None,
+                          stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """The normaliser counts of a GRPO batch layout (n tokens, the active
+    mask, the sequences, the mode and normalizer) into ``workspace``
+    (allocated when not given on the mask's or cu_seqlens' device), on
+    ``stream`` (default: the current stream); returns the workspace for
+    ``logp_grpo_loss(..., counted=True, workspace=...)``."""
+    if mode not in GRPO_MODES:
+        raise ValueError(f"mode must be one of {sorted(GRPO_MODES)} (got {mode!r})")
+    n = int(n)
+    mp = _mask(active_mask, n)
+    cu_seqlens, nseq = _grpo_layout(cu_seqlens)
+    if workspace is None:
+        ref = active_mask if active_mask is not None else cu_seqlens
+        if ref is None:
+            raise ValueError("give the workspace when there is neither a mask nor cu_seqlens")
+        workspace = torch.empty(logp_grpo_loss_workspace_size(n, nseq), dtype=torch.uint8, device=ref.device)
+    _cuda(workspace)
+    s = stream if stream is not None else torch.cuda.current_stream(workspace.device)
+    st = _lib.load().logp_grpo_loss_counts(mp, _opt_ptr(cu_seqlens), nseq, n, GRPO_MODES[mode],
+                                           float(normalizer), workspace.data_ptr(),
+                                           workspace.numel() * workspace.element_size(), s.cuda_stream)
+    _lib.check("logp_grpo_loss_counts", st)
+    return workspace
 
 
 def logp_grpo_loss_workspace_size(n: int, num_seqs: int = 0) -> int:

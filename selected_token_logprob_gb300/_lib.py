@@ -49,6 +49,10 @@ SIGNATURES = {
     "logp_grpo_loss": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, ctypes.c_int,
                                       ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                       ctypes.c_float, _P, _I64, _P, _P, _P, _P]),
+    "logp_grpo_loss_counts": (ctypes.c_int, [_P, _P, _I64, _I64, ctypes.c_int, ctypes.c_float, _P, _I64, _P]),
+    "logp_grpo_loss_counted": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, ctypes.c_int,
+                                              ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                              ctypes.c_float, _P, _I64, _P, _P, _P, _P]),
     "fused_linear_logp_workspace_size": (ctypes.c_int, [_I64, _I64, ctypes.POINTER(_I64)]),
     "fused_linear_logp_forward": (ctypes.c_int, [_P, _I64, _I64, _I64, _P, _I64, _I64, _P, _I64, _P,
                                                  ctypes.c_float, _P, _I64, _P, _P, _P, _P]),

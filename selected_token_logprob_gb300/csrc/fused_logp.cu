@@ -1260,17 +1260,38 @@ flp_status logp_grpo_loss_workspace_size(int64_t n, int64_t num_seqs, int64_t* b
     return ok();
 }
 
-flp_status logp_grpo_loss(const float* logp, const float* old_logp, const float* ref_logp,
-                          const float* advantages, const uint8_t* active_mask,
-                          const int64_t* cu_seqlens, int64_t num_seqs, int64_t n, int mode,
-                          float eps_lo, float eps_hi, float beta, float normalizer, void* workspace,
-                          int64_t workspace_bytes, float* loss, float* grad, float* token_loss,
-                          flp_stream_t stream) {
+// What a GRPO call runs: everything, only the counts, or only the token pass
+// on counts that an earlier call left in the workspace.
+enum GrpoStage { kGrpoWhole = 0, kGrpoCountsOnly = 1, kGrpoCounted = 2 };
+
+// FNV-1a over the fields that fix the counts: a call that reuses counts
+// must describe the same layout.
+static uint64_t grpo_tag(int64_t n, int64_t nseq, int mode, float normalizer, const void* mask, const void* cu) {
+    uint64_t h = 1469598103934665603ull;
+    auto mix = [&](const void* p, size_t len) {
+        const unsigned char* b = static_cast<const unsigned char*>(p);
+        for (size_t i = 0; i < len; ++i) h = (h ^ b[i]) * 1099511628211ull;
+    };
+    const uintptr_t m = reinterpret_cast<uintptr_t>(mask), c = reinterpret_cast<uintptr_t>(cu);
+    mix(&n, sizeof n);
+    mix(&nseq, sizeof nseq);
+    mix(&mode, sizeof mode);
+    mix(&normalizer, sizeof normalizer);
+    mix(&m, sizeof m);
+    mix(&c, sizeof c);
+    return h;
+}
+
+static flp_status grpo_impl(GrpoStage stage, const float* logp, const float* old_logp, const float* ref_logp,
+                            const float* advantages, const uint8_t* active_mask, const int64_t* cu_seqlens,
+                            int64_t num_seqs, int64_t n, int mode, float eps_lo, float eps_hi, float beta,
+                            float normalizer, void* workspace, int64_t workspace_bytes, float* loss, float* grad,
+                            float* token_loss, flp_stream_t stream) {
     flp_status st;
     if (n < 0) return fail(FLP_EINVAL, "n must be >= 0 (got %lld)", (long long)n);
     if (mode < FLP_GRPO_TOKEN_MEAN || mode > FLP_GRPO_SEQ_MEAN_TOKEN_SUM)
         return fail(FLP_EINVAL, "mode must be 0, 1 or 2 (got %d)", mode);
-    if (!(eps_lo >= 0.f && eps_lo < 1.f) || !(eps_hi >= 0.f) || !isfinite(eps_hi))
+    if (stage != kGrpoCountsOnly && (!(eps_lo >= 0.f && eps_lo < 1.f) || !(eps_hi >= 0.f) || !isfinite(eps_hi)))
         return fail(FLP_EINVAL, "clip range needs 0 <= eps_lo < 1 and finite eps_hi >= 0");
     if (!isfinite(beta) || !isfinite(normalizer) || normalizer < 0.f)
         return fail(FLP_EINVAL, "beta and normalizer must be finite, normalizer >= 0");
@@ -1285,14 +1306,21 @@ flp_status logp_grpo_loss(const float* logp, const float* old_logp, const float*
                     (long long)need);
     if ((reinterpret_cast<uintptr_t>(workspace) & 15u) != 0)
         return fail(FLP_EINVAL, "workspace must start on a 16-byte boundary");
-    const void* ptrs[] = {loss, workspace, logp, old_logp, advantages, grad, ref_logp, active_mask, cu_seqlens,
-                          token_loss};
-    const char* names[] = {"loss", "workspace", "logp", "old_logp", "advantages", "grad", "ref_logp",
-                           "active_mask", "cu_seqlens", "token_loss"};
-    const bool optional[] = {false, false, false, false, false, false, true, true, true, true};
     int dev;
-    // with n == 0 only the loss (and the workspace's two normaliser words) are written
-    if ((st = common_device(n == 0 ? 2 : 10, ptrs, names, optional, &dev)) != FLP_OK) return st;
+    if (stage == kGrpoCountsOnly) {
+        const void* ptrs[] = {workspace, active_mask, cu_seqlens};
+        const char* names[] = {"workspace", "active_mask", "cu_seqlens"};
+        const bool optional[] = {false, true, true};
+        if ((st = common_device(n == 0 ? 1 : 3, ptrs, names, optional, &dev)) != FLP_OK) return st;
+    } else {
+        const void* ptrs[] = {loss, workspace, logp, old_logp, advantages, grad, ref_logp, active_mask, cu_seqlens,
+                              token_loss};
+        const char* names[] = {"loss", "workspace", "logp", "old_logp", "advantages", "grad", "ref_logp",
+                               "active_mask", "cu_seqlens", "token_loss"};
+        const bool optional[] = {false, false, false, false, false, false, true, true, true, true};
+        // with n == 0 only the loss (and the workspace's count words) are written
+        if ((st = common_device(n == 0 ? 2 : 10, ptrs, names, optional, &dev)) != FLP_OK) return st;
+    }
     if (dev < 0 || dev >= kMaxDevices) return fail(FLP_ECUDA, "device index %d out of range", dev);
     DeviceGuard guard;
     if ((st = guard.enter(dev)) != FLP_OK) return st;
@@ -1300,13 +1328,17 @@ flp_status logp_grpo_loss(const float* logp, const float* old_logp, const float*
     // have one weight known now: the token pass applies it and nothing is counted
     const float prescale =
         (normalizer > 0.f && mode != FLP_GRPO_SEQ_MEAN_TOKEN_MEAN) ? (float)(1.0 / (double)normalizer) : 0.f;
+    // counts from an earlier call are used only when a weight depends on them
+    const bool reuse = stage == kGrpoCounted && prescale == 0.f;
     const flp::GrpoArgs a{logp, old_logp, ref_logp, advantages, active_mask, cu_seqlens, nseq, n, mode,
-                          eps_lo, eps_hi, beta, normalizer, prescale, loss, grad, token_loss};
+                          eps_lo, eps_hi, beta, normalizer, prescale, loss, grad, token_loss,
+                          grpo_tag(n, nseq, mode, normalizer, active_mask, cu_seqlens), reuse ? 1 : 0};
     const int64_t nchunks = ceil_div(n, flp::kGrpoChunk);
     char* base = static_cast<char*>(workspace);
     flp::GrpoWork wk;
     wk.dcnt = reinterpret_cast<int64_t*>(base);
     wk.ticket = reinterpret_cast<unsigned*>(base + 8);
+    wk.tag = reinterpret_cast<uint64_t*>(base + 16);
     wk.part_t = reinterpret_cast<flp::FF*>(base + 32);
     wk.part_q = wk.part_t + flp::kGrpoPassCtas;
     wk.a_part = reinterpret_cast<int64_t*>(wk.part_q + flp::kGrpoPassCtas);
@@ -1315,50 +1347,90 @@ flp_status logp_grpo_loss(const float* logp, const float* old_logp, const float*
     wk.word_pre = reinterpret_cast<uint32_t*>(wk.seg_cnt + nseq);
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     auto al = [](const void* q, uintptr_t m) { return (reinterpret_cast<uintptr_t>(q) & (m - 1)) == 0; };
-    const bool vec = al(logp, 16) && al(old_logp, 16) && al(advantages, 16) && al(grad, 16) && al(ref_logp, 16) &&
-                     al(token_loss, 16) && al(active_mask, 4);
-    // 1. the mask's counts, when a weight depends on them (any weight but the
-    //    caller's uniform one); ranges of R tokens (a multiple of 16), at most
-    //    1024 of them, a function of n only
-    int64_t range = 0;
-    int nranges = 0;
-    if (n > 0 && prescale == 0.f && active_mask != nullptr) {
-        int64_t g = ceil_div(n, flp::kGrpoCountRound);
-        g = g < 1 ? 1 : (g > flp::kGrpoCountMaxCtas ? flp::kGrpoCountMaxCtas : g);
-        range = ceil_div(ceil_div(n, g), 16) * 16;
-        nranges = (int)ceil_div(n, range);
-        if (al(active_mask, 16))
-            flp::k_grpo_count<true><<<nranges, flp::kGrpoCountThreads, 0, s>>>(a, wk, range);
-        else
-            flp::k_grpo_count<false><<<nranges, flp::kGrpoCountThreads, 0, s>>>(a, wk, range);
-        if ((st = check_launch("grpo count")) != FLP_OK) return st;
-    }
-    // 2. the sequences' counts (a sequence per thread); it waits for the
-    //    count on the device when that ran before it
     int64_t nfix = (cu_seqlens != nullptr && n > 0 && mode != FLP_GRPO_TOKEN_MEAN)
                        ? ceil_div(nseq, flp::kGrpoFixThreads) : 1;
     nfix = nfix < 1 ? 1 : (nfix > flp::kGrpoFixMaxCtas ? flp::kGrpoFixMaxCtas : nfix);
-    auto fix = al(active_mask, 16) ? flp::k_grpo_fix<true> : flp::k_grpo_fix<false>;
-    if (nranges > 0) {
-        if ((st = launch_dependent("grpo counts", fix, (int)nfix, flp::kGrpoFixThreads, s, a, wk, range, nranges)) !=
-            FLP_OK)
-            return st;
-    } else {
-        fix<<<(int)nfix, flp::kGrpoFixThreads, 0, s>>>(a, wk, range, nranges);
-        if ((st = check_launch("grpo counts")) != FLP_OK) return st;
+    if (!reuse) {
+        // 1. the mask's counts, when a weight depends on them (any weight but
+        //    the caller's uniform one); ranges of R tokens (a multiple of 16),
+        //    at most 1024 of them, a function of n only
+        int64_t range = 0;
+        int nranges = 0;
+        if (n > 0 && prescale == 0.f && active_mask != nullptr) {
+            int64_t g = ceil_div(n, flp::kGrpoCountRound);
+            g = g < 1 ? 1 : (g > flp::kGrpoCountMaxCtas ? flp::kGrpoCountMaxCtas : g);
+            range = ceil_div(ceil_div(n, g), 16) * 16;
+            nranges = (int)ceil_div(n, range);
+            if (al(active_mask, 16))
+                flp::k_grpo_count<true><<<nranges, flp::kGrpoCountThreads, 0, s>>>(a, wk, range);
+            else
+                flp::k_grpo_count<false><<<nranges, flp::kGrpoCountThreads, 0, s>>>(a, wk, range);
+            if ((st = check_launch("grpo count")) != FLP_OK) return st;
+        }
+        // 2. the sequences' counts (a sequence per thread); it waits for the
+        //    count on the device when that ran before it
+        auto fix = al(active_mask, 16) ? flp::k_grpo_fix<true> : flp::k_grpo_fix<false>;
+        if (nranges > 0) {
+            if ((st = launch_dependent("grpo counts", fix, (int)nfix, flp::kGrpoFixThreads, s, a, wk, range,
+                                       nranges)) != FLP_OK)
+                return st;
+        } else {
+            fix<<<(int)nfix, flp::kGrpoFixThreads, 0, s>>>(a, wk, range, nranges);
+            if ((st = check_launch("grpo counts")) != FLP_OK) return st;
+        }
     }
-    // 3. the token pass, launched while the fix kernel runs: final gradients
-    //    and the loss; its grid is fixed by n (the fold's shape depends on it)
+    if (stage == kGrpoCountsOnly) return ok();
+    // 3. the token pass (launched while the fix kernel runs, when it ran in
+    //    this call): final gradients and the loss; its grid is fixed by n (the
+    //    fold's shape depends on it)
     if (n > 0) {
+        const bool vec = al(logp, 16) && al(old_logp, 16) && al(advantages, 16) && al(grad, 16) &&
+                         al(ref_logp, 16) && al(token_loss, 16) && al(active_mask, 4);
         int64_t grid = ceil_div(nchunks, flp::kGrpoPassThreads / 32);
         grid = grid < 1 ? 1 : (grid > flp::kGrpoPassCtas ? flp::kGrpoPassCtas : grid);
         const bool per_seq = cu_seqlens != nullptr && mode == FLP_GRPO_SEQ_MEAN_TOKEN_MEAN;
         auto kern = vec ? (per_seq ? flp::k_grpo_pass<true, true> : flp::k_grpo_pass<true, false>)
                         : (per_seq ? flp::k_grpo_pass<false, true> : flp::k_grpo_pass<false, false>);
-        if ((st = launch_dependent("grpo pass", kern, (int)grid, flp::kGrpoPassThreads, s, a, wk, (int)nfix)) != FLP_OK)
+        if (reuse) {
+            kern<<<(int)grid, flp::kGrpoPassThreads, 0, s>>>(a, wk, (int)nfix);
+            if ((st = check_launch("grpo pass")) != FLP_OK) return st;
+        } else if ((st = launch_dependent("grpo pass", kern, (int)grid, flp::kGrpoPassThreads, s, a, wk,
+                                          (int)nfix)) != FLP_OK) {
             return st;
+        }
+    } else if (reuse) {
+        // no tokens: the loss is 0 and nothing else is written
+        if (cudaMemsetAsync(loss, 0, sizeof(float), s) != cudaSuccess)
+            return fail(FLP_ECUDA, "grpo loss: %s", cudaGetErrorString(cudaGetLastError()));
     }
     return ok();
+}
+
+flp_status logp_grpo_loss(const float* logp, const float* old_logp, const float* ref_logp,
+                          const float* advantages, const uint8_t* active_mask,
+                          const int64_t* cu_seqlens, int64_t num_seqs, int64_t n, int mode,
+                          float eps_lo, float eps_hi, float beta, float normalizer, void* workspace,
+                          int64_t workspace_bytes, float* loss, float* grad, float* token_loss,
+                          flp_stream_t stream) {
+    return grpo_impl(kGrpoWhole, logp, old_logp, ref_logp, advantages, active_mask, cu_seqlens, num_seqs, n, mode,
+                     eps_lo, eps_hi, beta, normalizer, workspace, workspace_bytes, loss, grad, token_loss, stream);
+}
+
+flp_status logp_grpo_loss_counts(const uint8_t* active_mask, const int64_t* cu_seqlens, int64_t num_seqs,
+                                 int64_t n, int mode, float normalizer, void* workspace, int64_t workspace_bytes,
+                                 flp_stream_t stream) {
+    return grpo_impl(kGrpoCountsOnly, nullptr, nullptr, nullptr, nullptr, active_mask, cu_seqlens, num_seqs, n, mode,
+                     0.f, 0.f, 0.f, normalizer, workspace, workspace_bytes, nullptr, nullptr, nullptr, stream);
+}
+
+flp_status logp_grpo_loss_counted(const float* logp, const float* old_logp, const float* ref_logp,
+                                  const float* advantages, const uint8_t* active_mask,
+                                  const int64_t* cu_seqlens, int64_t num_seqs, int64_t n, int mode,
+                                  float eps_lo, float eps_hi, float beta, float normalizer, void* workspace,
+                                  int64_t workspace_bytes, float* loss, float* grad, float* token_loss,
+                                  flp_stream_t stream) {
+    return grpo_impl(kGrpoCounted, logp, old_logp, ref_logp, advantages, active_mask, cu_seqlens, num_seqs, n, mode,
+                     eps_lo, eps_hi, beta, normalizer, workspace, workspace_bytes, loss, grad, token_loss, stream);
 }
 
 flp_status flp_device_error(int device, int* code) {

@@ -72,6 +72,8 @@ struct GrpoArgs {
     float* loss;                // [1]
     float* grad;                // [n]
     float* token_loss;          // nullable [n]
+    uint64_t tag;               // the layout's tag (n, sequences, mode, normaliser, mask, cu_seqlens)
+    int check_tag;              // pass 3: the counts come from an earlier call; check their tag
 };
 
 // Two-float sum: value = hi + lo.
@@ -135,7 +137,9 @@ __device__ __forceinline__ float grpo_exp(float x) { return ex2_ftz(__fmul_rn(x,
 
 struct GrpoWork {
     int64_t* dcnt;        // [1]: active tokens inside the sequences (or in the batch)
-    unsigned* ticket;     // [1]: CTAs of pass 3 that are done (zeroed by the fix kernel, counted by pass 3)
+    unsigned* ticket;     // [1]: CTAs of pass 3 that are done (zeroed by the fix kernel, counted by
+                          //      pass 3, zeroed again by its last CTA)
+    uint64_t* tag;        // [1]: the tag of the layout the counts were taken for
     FF* part_t;           // [kGrpoPassCtas]: per CTA of pass 3, its loss sum
     FF* part_q;           //   its sum of sequence means' pieces
     int64_t* a_part;      // [kGrpoFixMaxCtas]: per CTA of the fix kernel, its sequences with an active token
@@ -574,7 +578,8 @@ __global__ void __launch_bounds__(kGrpoFixThreads) k_grpo_fix(GrpoArgs p, GrpoWo
             }
             *wk.dcnt = D;
             *wk.ticket = 0u;
-            if (p.n == 0) p.loss[0] = 0.f;
+            *wk.tag = p.tag;
+            if (p.n == 0 && p.loss != nullptr) p.loss[0] = 0.f;
         }
     }
 }
@@ -648,11 +653,15 @@ __global__ void __launch_bounds__(kGrpoPassThreads, 4) k_grpo_pass(GrpoArgs p, G
     float wu = p.prescale, inv_den = 0.f;
     const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t w_end = (gw + 1) * nchunks / nwarps;
+    // counts from an earlier call taken for another layout: every gradient
+    // and the loss become NaN
+    bool stale = false;
     if (!known) {   // the counts and the weight
         griddep_wait();
         const GrpoNorm nm = grpo_norm_warp(p, wk, nfix, lane);
-        wu = nm.wt;
-        inv_den = nm.den > 0 ? __frcp_rn((float)nm.den) : 0.f;
+        stale = p.check_tag && __ldcg(reinterpret_cast<const unsigned long long*>(wk.tag)) != p.tag;
+        wu = stale ? __int_as_float(0x7fc00000) : nm.wt;
+        inv_den = stale ? __int_as_float(0x7fc00000) : (nm.den > 0 ? __frcp_rn((float)nm.den) : 0.f);
     }
     FF T{0.f, 0.f}, Q{0.f, 0.f};
     int64_t s_resume = -1;
@@ -783,7 +792,8 @@ __global__ void __launch_bounds__(kGrpoPassThreads, 4) k_grpo_pass(GrpoArgs p, G
         const double tt = ff_value(t);
         double num = tt;
         if (p.mode == 1) num = p.cu ? ff_value(q) : (cnt > 0 ? tt / cnt : 0.0);
-        p.loss[0] = den > 0 ? __double2float_rn(num / den) : 0.f;
+        p.loss[0] = stale ? __int_as_float(0x7fc00000) : (den > 0 ? __double2float_rn(num / den) : 0.f);
+        *wk.ticket = 0u;   // every CTA has counted: ready for a call that reuses the counts
     }
 }
 

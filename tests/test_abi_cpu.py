@@ -302,6 +302,19 @@ def test_grpo_host_checks(lib):
     assert call(ws=(1 << 20) + 8) == EINVAL
     assert call() == EINVAL                            # host pointers are not device memory
 
+    # the two-part form checks the same things before any device access
+    def counts(mode=0, ws=1 << 20, ws_bytes=1 << 20, n=1000, normalizer=0.0):
+        return lib.logp_grpo_loss_counts(None, None, 0, n, mode, normalizer, ws, ws_bytes, None)
+
+    assert counts(mode=-1) == EINVAL and b"mode" in lib.flp_last_error()
+    assert counts(n=-5) == EINVAL
+    assert counts(normalizer=-1.0) == EINVAL
+    assert counts(ws_bytes=64) == EINVAL and b"workspace" in lib.flp_last_error()
+    assert counts(ws=(1 << 20) + 4) == EINVAL
+    assert counts() == EINVAL                          # a host address is not device memory
+    assert lib.logp_grpo_loss_counted(1 << 21, 1 << 22, None, 1 << 23, None, None, 0, 1000, 2, 0.2, 0.2, 0.0,
+                                      0.0, 1 << 20, 1 << 20, 1 << 24, 1 << 25, None, None) == EINVAL
+
 
 def test_gathered_merge_validates_the_rank_layout_on_the_host(lib):
     """The tile -> rank table of a vocabulary-parallel merge is checked before
