@@ -48,6 +48,7 @@ __all__ = [
     "VocabParallelLogp",
     "gather_rows",
     "preflight",
+    "row_parallel_logp_backward",
     "row_parallel_logp_forward",
     "vocab_parallel_logp",
     "vocab_parallel_logp_backward",
