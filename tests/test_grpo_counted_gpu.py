@@ -46,12 +46,14 @@ def _bits(t):
     return t.view(torch.int32)
 
 
-@pytest.mark.parametrize("mode", MODES)
-@pytest.mark.parametrize("with_mask, with_cu, kl", [(True, True, True), (True, True, False), (False, True, True),
-                                                    (True, False, True)])
+# (mode, mask, cu_seqlens, KL); without cu_seqlens only the token mean here (the
+# sequence modes then take the whole batch as one sequence: the next test)
+_CASES = [(m, True, True, True) for m in MODES] + [(m, True, True, False) for m in MODES] + \
+         [(m, False, True, True) for m in MODES] + [("token_mean", True, False, True)]
+
+
+@pytest.mark.parametrize("mode, with_mask, with_cu, kl", _CASES)
 def test_counted_equals_whole_call_bitwise(mode, with_mask, with_cu, kl):
-    if not with_cu and mode != "token_mean":
-        pytest.skip("the sequence modes without cu_seqlens are the whole batch as one sequence: covered below")
     n = 300017                                      # ragged last chunk
     lp, old, ref, adv, mask, cu = _case(n, 41, 1000)
     mask = mask if with_mask else None
