@@ -972,6 +972,7 @@ def _oracle_sample_rate(x_rows_u16, y_np, g_np, v, seconds: float):
     chunk = 64
     rows_done = 0
     t0 = time.perf_counter()
+    t_fwd = t_bwd = 0.0
     i = 0
     nrows = x_rows_u16.shape[0]
     while True:
@@ -979,14 +980,18 @@ def _oracle_sample_rate(x_rows_u16, y_np, g_np, v, seconds: float):
         xb = np.ascontiguousarray(x_rows_u16[a:a + chunk])
         yb = y_np[a:a + chunk]
         gb = g_np[a:a + chunk]
+        ta = time.perf_counter()
         oracle.forward(xb, yb)
+        tb = time.perf_counter()
         oracle.backward(xb, yb, gb)
+        t_fwd += tb - ta
+        t_bwd += time.perf_counter() - tb
         rows_done += xb.shape[0]
         i += 1
         el = time.perf_counter() - t0
         if el >= seconds:
             break
-    return rows_done * v * BYTES_PER_LOGIT / el / 1e9, rows_done, el
+    return rows_done * v * BYTES_PER_LOGIT / el / 1e9, rows_done, el, t_fwd / rows_done, t_bwd / rows_done
 
 
 def cpu_baseline(args, x, y, g, v):
@@ -997,11 +1002,15 @@ def cpu_baseline(args, x, y, g, v):
         return None
     rows = min(512, x.shape[0])
     xs = workloads.bf16_bits(x[:rows])
-    rate, done, el = _oracle_sample_rate(xs, y[:rows].cpu().numpy(), g[:rows].cpu().numpy(), v,
-                                         args.cpu_seconds)
+    rate, done, el, fwd_row, bwd_row = _oracle_sample_rate(xs, y[:rows].cpu().numpy(), g[:rows].cpu().numpy(), v,
+                                                           args.cpu_seconds)
+    n = x.shape[0]
     return {"value": round(rate, 4), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{done} rows of the long-CoT workload (first {rows} rows, cycled), "
-                      f"FP64 forward + dense backward, {el:.1f} s"}
+            "sample": f"{done} rows of the {getattr(args, 'workload', 'long')} workload (first {rows} rows, "
+                      f"cycled), FP64 forward + dense backward, {el:.1f} s",
+            "ms_extrapolated": {"fwd": round(fwd_row * n * 1e3, 1), "bwd": round(bwd_row * n * 1e3, 1),
+                                "total": round((fwd_row + bwd_row) * n * 1e3, 1),
+                                "note": f"per-row time of the sample times N = {n} rows (linear extrapolation)"}}
 
 
 def run_reference(args):
