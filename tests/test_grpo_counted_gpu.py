@@ -152,3 +152,65 @@ def test_counted_with_a_callers_weight_and_empty_batch():
     loss, grad = flp.logp_grpo_loss(e, e, e, active_mask=torch.empty(0, dtype=torch.uint8, device=DEV),
                                     workspace=ws0, counted=True)
     assert loss.item() == 0.0 and grad.numel() == 0
+
+
+def _edge_layout(kind, n, g):
+    """cu_seqlens (host, int64) of a layout kind: empty sequences, tokens
+    outside every sequence, one sequence, many tiny ones."""
+    if kind == "empty_and_outside":
+        cuts = torch.sort(torch.randint(n // 10, n - n // 10, (40,), generator=g)).values
+        cuts = torch.cat([cuts, cuts[5:9]])                                 # repeated bounds: empty sequences
+        return torch.sort(cuts).values.to(torch.int64)
+    if kind == "one":
+        return torch.tensor([0, n], dtype=torch.int64)
+    step = 3                                                                # many tiny sequences
+    return torch.arange(0, n + 1, step, dtype=torch.int64) if n % step == 0 else \
+        torch.cat([torch.arange(0, n, step, dtype=torch.int64), torch.tensor([n])])
+
+
+@pytest.mark.parametrize("seed, n, kind, density, mode, offset", [
+    (1, 100, "one", 0.9, "seq_mean_token_mean", 0),             # a single partial chunk
+    (2, 4099, "empty_and_outside", 0.7, "seq_mean_token_mean", 0),
+    (3, 4099, "empty_and_outside", 0.0, "seq_mean_token_mean", 0),   # no active token: loss 0, grads 0
+    (4, 65537, "tiny", 0.5, "seq_mean_token_sum", 0),
+    (5, 65537, "empty_and_outside", 1.0, "token_mean", 0),
+    (6, 33333, "empty_and_outside", 0.8, "seq_mean_token_mean", 1),  # arrays one element off alignment
+    (7, 33333, "tiny", 0.8, "token_mean", 3),
+])
+def test_counted_edge_layouts_against_whole_call_and_oracle(seed, n, kind, density, mode, offset):
+    import numpy as np
+
+    import oracle
+    from grpo_checks import _assert_grad, _token_weights
+
+    g = torch.Generator().manual_seed(100 + seed)
+    lp = -torch.rand(n, generator=g) * 6 - 0.05
+    old = lp + (torch.rand(n, generator=g) - 0.5) * 1.2
+    ref = lp + (torch.rand(n, generator=g) - 0.5) * 1.0
+    adv = torch.randn(n, generator=g)
+    mask = (torch.rand(n, generator=g) < density).to(torch.uint8)
+    cu = _edge_layout(kind, n, g)
+
+    def dev(t):   # a device view `offset` elements into a larger buffer (off alignment when offset > 0)
+        buf = torch.zeros(n + offset, dtype=t.dtype, device=DEV)
+        buf[offset:] = t.to(DEV)
+        return buf[offset:]
+
+    d_lp, d_old, d_ref, d_adv, d_mask = [dev(t) for t in (lp, old, ref, adv, mask)]
+    d_cu = cu.to(DEV)
+    kw = dict(ref_logp=d_ref, active_mask=d_mask, cu_seqlens=d_cu, mode=mode, eps_lo=0.2, eps_hi=0.28, beta=0.03)
+    want = flp.logp_grpo_loss(d_lp, d_old, d_adv, **kw)
+    ws = flp.logp_grpo_loss_counts(n, active_mask=d_mask, cu_seqlens=d_cu, mode=mode)
+    got = flp.logp_grpo_loss(d_lp, d_old, d_adv, workspace=ws, counted=True, **kw)
+    for u, v in zip(got, want):
+        assert torch.equal(_bits(u), _bits(v))
+    f64 = [t.double().numpy() for t in (lp, old, adv, ref)]
+    want_l, want_g = oracle.grpo_loss(f64[0], f64[1], f64[2], ref_logp=f64[3], mask=mask.numpy(),
+                                      cu_seqlens=cu.numpy(), mode=mode, eps_lo=0.2, eps_hi=0.28, beta=0.03)
+    got_g = got[1].double().cpu().numpy()
+    assert abs(got[0].item() - want_l) <= 1e-5 * abs(want_l) + 1e-7, (got[0].item(), want_l)
+    if density == 0.0:
+        assert got[0].item() == 0.0 and np.all(got_g == 0)
+    else:
+        w = _token_weights(n, mask.numpy(), cu.numpy(), mode)
+        _assert_grad(got_g, want_g, f64[0], f64[1], f64[2], f64[3], 0.03, 0.2, 0.28, w)
