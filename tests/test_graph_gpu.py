@@ -109,3 +109,39 @@ def test_grpo_loss_replays_bitwise():
         torch.cuda.synchronize()
         for u, v in zip(got, want):
             assert torch.equal(u.view(torch.int32), v.view(torch.int32)), mode
+
+
+def test_grpo_counts_and_counted_loss_replay_bitwise():
+    """The two-part GRPO form (the layout's counts, then the token pass on
+    them) captured in one graph replays bit for bit, and equals the one-call
+    loss."""
+    g = torch.Generator().manual_seed(32)
+    n, nseq = 40000, 50
+    lp = -torch.rand(n, generator=g) * 5
+    old = lp + (torch.rand(n, generator=g) - 0.5)
+    adv = torch.randn(n, generator=g)
+    mask = (torch.rand(n, generator=g) > 0.3).to(torch.uint8)
+    cu = torch.cat([torch.zeros(1, dtype=torch.int64),
+                    torch.sort(torch.randint(0, n + 1, (nseq - 1,), generator=g)).values,
+                    torch.full((1,), n, dtype=torch.int64)])
+    lp, old, adv, mask, cu = (t.to(DEV) for t in (lp, old, adv, mask, cu))
+    kw = dict(active_mask=mask, cu_seqlens=cu, mode="seq_mean_token_mean", beta=0.0)
+    want = flp.logp_grpo_loss(lp, old, adv, **kw)
+    ws = torch.empty(flp.logp_grpo_loss_workspace_size(n, nseq), dtype=torch.uint8, device=DEV)
+    flp.logp_grpo_loss_counts(n, active_mask=mask, cu_seqlens=cu, mode="seq_mean_token_mean", workspace=ws)
+    flp.logp_grpo_loss(lp, old, adv, workspace=ws, counted=True, **kw)       # eager first call
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            flp.logp_grpo_loss_counts(n, active_mask=mask, cu_seqlens=cu, mode="seq_mean_token_mean",
+                                      workspace=ws, stream=s)
+            got = flp.logp_grpo_loss(lp, old, adv, workspace=ws, counted=True, **kw)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(3):
+        graph.replay()
+        torch.cuda.synchronize()
+        for u, v in zip(got, want):
+            assert torch.equal(u.view(torch.int32), v.view(torch.int32))
