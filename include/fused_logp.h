@@ -513,7 +513,8 @@ flp_status logp_grpo_loss(const float* logp, const float* old_logp, const float*
  * contents themselves are not compared).  Calls may repeat on the same
  * counts.  When the weight is the caller's (a normalizer with the token mean
  * or the sequence mean of token sums) nothing is counted and the call is
- * logp_grpo_loss.
+ * logp_grpo_loss, which replaces the counts and the tag in the workspace
+ * (a later counted call for the earlier layout then gets NaN: count again).
  * Errors: as logp_grpo_loss.
  */
 flp_status logp_grpo_loss_counts(const uint8_t* active_mask, const int64_t* cu_seqlens, int64_t num_seqs,
