@@ -640,7 +640,6 @@ k_gemm_bf16_pair(const __grid_constant__ CUtensorMap tm_a, const __grid_constant
     } else {
         // ---------------- epilogue: this CTA's 128 rows of the pair's tile
         const int q = warp & 3;
-        const int row = q * 32 + lane;
         const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
         const uint32_t tempty_leader = map_to_rank(tempty0, 0);
         const uint32_t stg = bars + 1024 + (uint32_t)q * 2 * kPairStageOutBytes;   // this warp's two boxes
