@@ -207,3 +207,50 @@ def test_row_parallel_global_batch_matches_one_call_bitwise():
         kind, val = res[rank]
         assert kind == "ok", (rank, val)
         assert all(val.values()), (rank, val)
+
+
+def _vocab_rank_device_transport(rank, world, n):
+    """As _vocab_rank, with the exchange on device tensors the way it runs on
+    NCCL (one all_gather_into_tensor into a rank-major [world, L] buffer).  Two
+    NCCL ranks cannot share one GPU, so gloo stands in for the transport with
+    NCCL's documented semantics (the output is the inputs concatenated in rank
+    order); the library code path is the one a NCCL group takes."""
+    import torch
+    import torch.distributed as dist
+
+    import selected_token_logprob_gb300 as flp
+    from selected_token_logprob_gb300 import distributed as fd
+
+    torch.cuda.set_device(0)
+    calls = []
+
+    def all_gather_into_tensor(out, inp, group=None):
+        assert out.is_cuda and inp.is_cuda and out.numel() == world * inp.numel()
+        parts = [torch.empty_like(inp, device="cpu") for _ in range(world)]
+        dist.all_gather(parts, inp.cpu(), group=group)
+        out.copy_(torch.cat(parts).to(out.device))
+        calls.append(inp.numel())
+
+    real_backend = fd.dist.get_backend
+    fd.dist.get_backend = lambda group=None: "nccl"
+    fd.dist.all_gather_into_tensor = all_gather_into_tensor
+    try:
+        x, y, g = _inputs(n, V, seed=23)
+        logp, lse, lo = flp.fused_logp_forward(x, y, with_lse_lo=True)
+        W = flp.flp_tile_width(V)
+        a, w = _bounds(V, world, W)[rank]
+        shard = _padded_shard(x, a, w)
+        r_logp, r_lse, r_lo = fd.vocab_parallel_logp_forward(shard, y, a, V, real_width=w, with_lse_lo=True)
+        torch.cuda.synchronize()
+        return {"logp": torch.equal(_i(r_logp), _i(logp)), "lse": torch.equal(_i(r_lse), _i(lse)),
+                "lse_lo": torch.equal(_i(r_lo), _i(lo)), "device_transport_used": calls == [33 * n]}
+    finally:
+        fd.dist.get_backend = real_backend
+
+
+def test_vocab_parallel_device_tensor_transport_path():
+    res = run_ranks(_vocab_rank_device_transport, 2, (512,), timeout=600)
+    for rank in range(2):
+        kind, val = res[rank]
+        assert kind == "ok", (rank, val)
+        assert all(val.values()), (rank, val)
