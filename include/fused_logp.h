@@ -426,6 +426,41 @@ flp_status fused_linear_logp_forward_noalloc(const void* hidden, int64_t n, int6
                                              float* lse, float* lse_lo, flp_stream_t stream);
 
 /*
+ * The fused LM head across several processes, one vocabulary slice of the
+ * weight per rank (the tensor-parallel output layer; the exchange is the
+ * tile-partial all-gather of issue #241 PR 3 / PR #314 Tensor Parallel,
+ * transport only, then the same fixed-order merge on every rank).
+ *
+ * fused_linear_logp_merge_gathered: every rank ran
+ * fused_linear_logp_shard_partials on its slice into its own workspace (the
+ * slices on the 256-column tile grid, covering every tile once); `gathered`
+ * holds the world workspaces one after another, rank r's at gathered +
+ * r * rank_stride (floats; rank_stride >= (2 ceil(v_total / 256) + 1) n, e.g.
+ * the workspace's size / 4).  vocab_starts / real_widths are host arrays of
+ * world entries (at most 16).  Tile k is read from the rank that holds it
+ * and row t's selected logit from the rank that holds its target's tile:
+ * logp, lse (and lse_lo) are those of fused_linear_logp_merge over one
+ * workspace that all slices wrote, bit for bit.
+ * Errors: FLP_EINVAL for bad extents, a stride below one block, a slice
+ * outside the vocabulary, a tile held by no rank or by two;
+ * FLP_EUNSUPPORTED for a slice off the tile grid.
+ *
+ * flp_sum_blocks: out[r, c] = ((b_0 + b_1) + b_2) + ... over world FP32
+ * blocks [rows, cols] (row pitch cols) at blocks + k * block_stride, one
+ * rounding per addition in block order -- the sum that the one-GPU sharded
+ * LM-head backward forms when each later shard adds its term of dhidden, so
+ * the ranks' all-gathered terms summed here give its dhidden bit for bit.
+ * out has row pitch ld_out and must not overlap the blocks.
+ */
+flp_status fused_linear_logp_merge_gathered(const float* gathered, int64_t rank_stride, int world,
+                                            const int64_t* vocab_starts, const int64_t* real_widths, int64_t n,
+                                            int64_t v_total, const int64_t* targets, int64_t ignore_index,
+                                            const uint8_t* active_mask, float inv_temperature, float* logp,
+                                            float* lse, float* lse_lo, flp_stream_t stream);
+flp_status flp_sum_blocks(const float* blocks, int64_t block_stride, int world, int64_t rows, int64_t cols,
+                          float* out, int64_t ld_out, flp_stream_t stream);
+
+/*
  * GRPO loss on the logp path (issue #241 PR 5: ratio, clip, KL, advantage,
  * a declared normaliser and a fixed summation order; the pages name these
  * terms, the formulas below are the standard clipped-surrogate form).

@@ -62,6 +62,8 @@ __all__ = [
     "fused_linear_logp_shard_backward",
     "fused_linear_logp_shard_partials",
     "fused_linear_logp_workspace_size",
+    "fused_linear_logp_merge_gathered",
+    "sum_blocks",
     "logp_grpo_loss",
     "logp_grpo_loss_counts",
     "logp_grpo_loss_workspace_size",
@@ -687,6 +689,53 @@ def fused_linear_logp_merge(workspace: torch.Tensor, v_total: int, targets: torc
         _stream(targets))
     _lib.check("fused_linear_logp_merge", st)
     return (logp, lse, lse_lo) if with_lse_lo else (logp, lse)
+
+
+def fused_linear_logp_merge_gathered(gathered: torch.Tensor, vocab_starts, real_widths, targets: torch.Tensor,
+                                     v_total: int, ignore_index: int = IGNORE_INDEX, with_lse_lo: bool = False,
+                                     temperature: float = 1.0, active_mask: torch.Tensor | None = None):
+    """(logp, lse[, lse_lo]) FP32 [N] of a vocabulary-parallel LM head from
+    the ranks' all-gathered workspaces: ``gathered`` FP32 [world, >= block]
+    in rank order, rank r having run ``fused_linear_logp_shard_partials`` on
+    columns [vocab_starts[r], vocab_starts[r] + real_widths[r]) into its own
+    workspace."""
+    import ctypes
+
+    if gathered.dtype != torch.float32 or gathered.dim() != 2 or gathered.stride(1) != 1:
+        raise ValueError("gathered must be an FP32 [world, L] tensor with unit column stride")
+    world = gathered.shape[0]
+    if len(vocab_starts) != world or len(real_widths) != world:
+        raise ValueError("vocab_starts and real_widths need one entry per rank")
+    n = targets.shape[0]
+    _vec(targets, "targets", n, torch.int64)
+    dev = targets.device
+    logp = torch.empty(n, dtype=torch.float32, device=dev)
+    lse = torch.empty(n, dtype=torch.float32, device=dev)
+    lse_lo = torch.empty(n, dtype=torch.float32, device=dev) if with_lse_lo else None
+    _cuda(gathered, targets)
+    mp = _mask(active_mask, n)
+    starts = (ctypes.c_int64 * max(1, world))(*[int(a) for a in vocab_starts])
+    widths = (ctypes.c_int64 * max(1, world))(*[int(w) for w in real_widths])
+    st = _lib.load().fused_linear_logp_merge_gathered(
+        gathered.data_ptr(), gathered.stride(0), world, starts, widths, n, int(v_total), targets.data_ptr(),
+        int(ignore_index), mp, _inv_temperature(temperature), logp.data_ptr(), lse.data_ptr(), _opt_ptr(lse_lo),
+        _stream(targets))
+    _lib.check("fused_linear_logp_merge_gathered", st)
+    return (logp, lse, lse_lo) if with_lse_lo else (logp, lse)
+
+
+def sum_blocks(blocks: torch.Tensor) -> torch.Tensor:
+    """((b_0 + b_1) + b_2) + ... of FP32 blocks [world, rows, cols], one
+    rounding per addition in block order (``flp_sum_blocks``)."""
+    if blocks.dtype != torch.float32 or blocks.dim() != 3 or not blocks[0].is_contiguous():
+        raise ValueError("blocks must be FP32 [world, rows, cols] with contiguous blocks")
+    _cuda(blocks)
+    world, rows, cols = blocks.shape
+    out = torch.empty((rows, cols), dtype=torch.float32, device=blocks.device)
+    st = _lib.load().flp_sum_blocks(blocks.data_ptr(), blocks.stride(0), world, rows, cols, out.data_ptr(), cols,
+                                    _stream(blocks))
+    _lib.check("flp_sum_blocks", st)
+    return out
 
 
 def fused_linear_logp_shard_backward(hidden: torch.Tensor, weight_shard: torch.Tensor, vocab_start: int,

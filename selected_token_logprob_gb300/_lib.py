@@ -49,6 +49,9 @@ SIGNATURES = {
     "logp_grpo_loss": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, ctypes.c_int,
                                       ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                       ctypes.c_float, _P, _I64, _P, _P, _P, _P]),
+    "fused_linear_logp_merge_gathered": (ctypes.c_int, [_P, _I64, ctypes.c_int, _P, _P, _I64, _I64, _P, _I64, _P,
+                                                        ctypes.c_float, _P, _P, _P, _P]),
+    "flp_sum_blocks": (ctypes.c_int, [_P, _I64, ctypes.c_int, _I64, _I64, _P, _I64, _P]),
     "logp_grpo_loss_counts": (ctypes.c_int, [_P, _P, _I64, _I64, ctypes.c_int, ctypes.c_float, _P, _I64, _P]),
     "logp_grpo_loss_counted": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, ctypes.c_int,
                                               ctypes.c_float, ctypes.c_float, ctypes.c_float,

@@ -1042,6 +1042,111 @@ flp_status fused_linear_logp_merge(const void* workspace, int64_t workspace_byte
                                reinterpret_cast<cudaStream_t>(stream));
 }
 
+flp_status fused_linear_logp_merge_gathered(const float* gathered, int64_t rank_stride, int world,
+                                            const int64_t* vocab_starts, const int64_t* real_widths, int64_t n,
+                                            int64_t v_total, const int64_t* targets, int64_t ignore_index,
+                                            const uint8_t* active_mask, float inv_temperature, float* logp,
+                                            float* lse, float* lse_lo, flp_stream_t stream) {
+    flp_status st;
+    if ((st = check_scale(inv_temperature)) != FLP_OK) return st;
+    if (n < 0) return fail(FLP_EINVAL, "n must be >= 0 (got %lld)", (long long)n);
+    if (v_total < 1) return fail(FLP_EINVAL, "v_total must be >= 1 (got %lld)", (long long)v_total);
+    if (world < 1 || world > flp::kLinMaxRanks)
+        return fail(FLP_EINVAL, "world must be in [1, %d] (got %d)", flp::kLinMaxRanks, world);
+    if (vocab_starts == nullptr || real_widths == nullptr)
+        return fail(FLP_EINVAL, "vocab_starts and real_widths are host arrays of world entries");
+    const int64_t nvt = linear_vocab_tiles(v_total);
+    if (nvt > INT32_MAX) return fail(FLP_EINVAL, "too many vocabulary tiles");
+    int64_t need;   // floats of one rank's block: tile maxima and sums [n, nvt] each, selected logits [n]
+    if (__builtin_mul_overflow(2 * nvt + 1, n, &need)) return fail(FLP_EINVAL, "block size overflows int64");
+    if (rank_stride < need)
+        return fail(FLP_EINVAL, "rank_stride (%lld floats) is below one rank's block (%lld floats)",
+                    (long long)rank_stride, (long long)need);
+    // each rank's tiles, on the 256-column grid, covering every tile once
+    flp::LinRankTiles rt;
+    rt.world = world;
+    int order[flp::kLinMaxRanks];
+    for (int r = 0; r < world; ++r) {
+        const int64_t a = vocab_starts[r], w = real_widths[r];
+        if (w < 1 || a < 0 || a > v_total - w)
+            return fail(FLP_EINVAL, "rank %d: columns [%lld, %lld) are not inside the vocabulary [0, %lld)", r,
+                        (long long)a, (long long)(a + w), (long long)v_total);
+        if (a % flp::kLinBN != 0 || (a + w != v_total && w % flp::kLinBN != 0))
+            return fail(FLP_EUNSUPPORTED, "rank %d: columns [%lld, %lld) are off the %d-column tile grid", r,
+                        (long long)a, (long long)(a + w), flp::kLinBN);
+        order[r] = r;
+    }
+    for (int i = 1; i < world; ++i)   // by first column (insertion sort, at most 16)
+        for (int j = i; j > 0 && vocab_starts[order[j]] < vocab_starts[order[j - 1]]; --j) {
+            const int tmp = order[j];
+            order[j] = order[j - 1];
+            order[j - 1] = tmp;
+        }
+    int64_t next = 0;
+    for (int j = 0; j < world; ++j) {
+        const int r = order[j];
+        const int64_t t0 = vocab_starts[r] / flp::kLinBN, t1 = ceil_div(vocab_starts[r] + real_widths[r], flp::kLinBN);
+        if (t0 != next)
+            return fail(FLP_EINVAL, "tile %lld (columns from %lld) is %s", (long long)next,
+                        (long long)(next * flp::kLinBN), t0 > next ? "held by no rank" : "held by two ranks");
+        rt.t0[j] = (int)t0;
+        rt.t1[j] = (int)t1;
+        rt.rank[j] = r;
+        next = t1;
+    }
+    if (next != nvt)
+        return fail(FLP_EINVAL, "tiles from %lld (columns from %lld) are held by no rank", (long long)next,
+                    (long long)(next * flp::kLinBN));
+    for (int j = world; j < flp::kLinMaxRanks; ++j) rt.t0[j] = rt.t1[j] = rt.rank[j] = 0;
+    if (n == 0) return ok();
+    const void* ptrs[] = {gathered, targets, logp, lse, lse_lo, active_mask};
+    const char* names[] = {"gathered", "targets", "logp", "lse", "lse_lo", "active_mask"};
+    const bool optional[] = {false, false, false, false, true, true};
+    int dev;
+    if ((st = common_device(6, ptrs, names, optional, &dev)) != FLP_OK) return st;
+    if (dev < 0 || dev >= kMaxDevices) return fail(FLP_ECUDA, "device index %d out of range", dev);
+    DeviceGuard guard;
+    if ((st = guard.enter(dev)) != FLP_OK) return st;
+    const int sms = sm_count(dev);
+    if (sms <= 0) return fail(FLP_ECUDA, "cannot read the SM count of device %d", dev);
+    const int64_t ctas = ceil_div(n * 32, flp::kLinMergeThreads);
+    flp::k_linear_logp_merge_gathered<<<(int)(ctas < (int64_t)sms * 16 ? ctas : (int64_t)sms * 16),
+                                        flp::kLinMergeThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        gathered, rank_stride, rt, n, (int)nvt, v_total, targets, ignore_index, active_mask, inv_temperature, logp,
+        lse, lse_lo);
+    return check_launch("linear logp gathered merge");
+}
+
+flp_status flp_sum_blocks(const float* blocks, int64_t block_stride, int world, int64_t rows, int64_t cols,
+                          float* out, int64_t ld_out, flp_stream_t stream) {
+    flp_status st;
+    if (world < 1) return fail(FLP_EINVAL, "world must be >= 1 (got %d)", world);
+    if (rows < 0 || cols < 0) return fail(FLP_EINVAL, "rows and cols must be >= 0");
+    if (ld_out < cols) return fail(FLP_EINVAL, "ld_out (%lld) must be >= cols (%lld)", (long long)ld_out,
+                                   (long long)cols);
+    int64_t total;
+    if (__builtin_mul_overflow(rows, cols, &total)) return fail(FLP_EINVAL, "rows * cols overflows int64");
+    if (world > 1 && block_stride < total)
+        return fail(FLP_EINVAL, "block_stride (%lld) is below one block (%lld floats)", (long long)block_stride,
+                    (long long)total);
+    if (total == 0) return ok();
+    const void* ptrs[] = {blocks, out};
+    const char* names[] = {"blocks", "out"};
+    const bool optional[] = {false, false};
+    int dev;
+    if ((st = common_device(2, ptrs, names, optional, &dev)) != FLP_OK) return st;
+    if (dev < 0 || dev >= kMaxDevices) return fail(FLP_ECUDA, "device index %d out of range", dev);
+    DeviceGuard guard;
+    if ((st = guard.enter(dev)) != FLP_OK) return st;
+    const int sms = sm_count(dev);
+    if (sms <= 0) return fail(FLP_ECUDA, "cannot read the SM count of device %d", dev);
+    const int64_t blocks_n = ceil_div(total, 256);
+    flp::k_sum_blocks_ordered<<<(int)(blocks_n < (int64_t)sms * 8 ? blocks_n : (int64_t)sms * 8), 256, 0,
+                                reinterpret_cast<cudaStream_t>(stream)>>>(blocks, block_stride, world, rows, cols,
+                                                                           out, ld_out);
+    return check_launch("ordered block sum");
+}
+
 flp_status fused_linear_logp_backward_workspace_size(int64_t d, int64_t v, int64_t* bytes) {
     if (bytes == nullptr) return fail(FLP_EINVAL, "bytes is a null pointer");
     if (d < 1 || v < 1) return fail(FLP_EINVAL, "d and v must be >= 1");

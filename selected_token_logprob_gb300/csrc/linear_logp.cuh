@@ -550,4 +550,79 @@ k_linear_logp_merge(const float* __restrict__ pm, const float* __restrict__ ps, 
     }
 }
 
+// The ranks of a vocabulary-parallel LM head, in the order of their first
+// tile: rank rank[j] holds tiles [t0[j], t1[j]) of the 256-column grid.
+constexpr int kLinMaxRanks = 16;
+struct LinRankTiles {
+    int world;
+    int t0[kLinMaxRanks], t1[kLinMaxRanks], rank[kLinMaxRanks];
+};
+
+// The merge of k_linear_logp_merge over the ranks' all-gathered workspaces
+// (rank r's at gathered + r * stride, laid out as the one-buffer workspace):
+// tile k is read from the rank that holds it, the selected logit from the
+// rank that holds the target's tile.  Each lane visits the same tiles in the
+// same order with the same arithmetic, so the result is the one-buffer
+// merge's bit for bit.
+__global__ void __launch_bounds__(kLinMergeThreads)
+k_linear_logp_merge_gathered(const float* __restrict__ gathered, int64_t stride, LinRankTiles rt, int64_t n, int nvt,
+                             int64_t v, const int64_t* __restrict__ y, int64_t ignore_index,
+                             const uint8_t* __restrict__ mask, float s, float* __restrict__ logp,
+                             float* __restrict__ lse, float* __restrict__ lse_lo) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int64_t ps_off = (int64_t)nvt * n, sel_off = 2 * (int64_t)nvt * n;
+    for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < n; t += warps) {
+        float M = -INFINITY;
+        int j = 0;
+        for (int k = lane; k < nvt; k += 32) {
+            while (j + 1 < rt.world && k >= rt.t1[j]) ++j;
+            M = fmaxf(M, __ldg(gathered + rt.rank[j] * stride + t * nvt + k));
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        float S = 0.f;
+        if (M != -INFINITY) {
+            j = 0;
+            for (int k = lane; k < nvt; k += 32) {
+                while (j + 1 < rt.world && k >= rt.t1[j]) ++j;
+                const float* blk = gathered + rt.rank[j] * stride;
+                const float mk = __ldg(blk + t * nvt + k);
+                if (mk != -INFINITY) S = __fmaf_rn(__ldg(blk + ps_off + t * nvt + k), expf(__fmul_rn(s, __fsub_rn(mk, M))), S);
+            }
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) S = __fadd_rn(S, __shfl_xor_sync(0xffffffffu, S, off));
+        if (lane == 0) {
+            const int64_t yt = __ldg(y + t);
+            const bool act = row_active(mask, t, yt, v, ignore_index);
+            float x_y = 0.f;
+            if (act) {
+                const int tile = (int)(yt / kLinBN);
+                int o = 0;
+                while (o + 1 < rt.world && tile >= rt.t1[o]) ++o;
+                x_y = __ldg(gathered + rt.rank[o] * stride + sel_off + t);
+            }
+            finalize_row(MS{M, S}, act, x_y, s, logp + t, lse + t, lse_lo ? lse_lo + t : nullptr);
+        }
+    }
+}
+
+// out = ((b_0 + b_1) + b_2) + ... of `world` [rows, cols] FP32 blocks at
+// blocks + r * stride (row pitch cols), one rounding per addition, in rank
+// order: the sum the one-GPU sharded backward forms when each later shard
+// adds its term of dhidden.
+__global__ void __launch_bounds__(256) k_sum_blocks_ordered(const float* __restrict__ blocks, int64_t stride,
+                                                            int world, int64_t rows, int64_t cols,
+                                                            float* __restrict__ out, int64_t ldo) {
+    const int64_t total = rows * cols;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / cols, c = i - r * cols;
+        float acc = __ldg(blocks + i);
+        for (int k = 1; k < world; ++k) acc = __fadd_rn(acc, __ldg(blocks + (int64_t)k * stride + i));
+        out[r * ldo + c] = acc;
+    }
+}
+
 }  // namespace flp

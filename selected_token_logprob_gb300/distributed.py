@@ -28,6 +28,16 @@ rows are independent and each row's bits do not depend on the batch, so each
 rank runs the ordinary forward and backward on its rows; ``gather_rows``
 assembles per-row results in global row order when a caller wants them.
 
+The fused LM head in the same vocabulary-parallel layout (the
+tensor-parallel output layer: each rank holds a slice of the weight's rows
+on the 256-column tile grid, the hidden states on every rank): each rank
+writes its tiles' partials into its own workspace, one all-gather of the
+workspaces, the same merge on every rank (``fused_linear_logp_merge_gathered``)
+-- bitwise the one-GPU result.  Its backward: each rank's slice gives its
+dweight rows and its term of dhidden; the terms are all-gathered and summed
+in rank order by the library (``sum_blocks``), the sum the one-GPU sharded
+backward forms, so every rank has the same dhidden.
+
 Nothing here computes: the arithmetic is in the library's kernels; this
 module checks agreement, moves bytes and calls the C ABI.
 """
@@ -39,17 +49,24 @@ from dataclasses import asdict, dataclass
 import torch
 import torch.distributed as dist
 
-from . import (IGNORE_INDEX, NUM_TILES, flp_tile_width, fused_logp_backward, fused_logp_forward,
-               logp_merge_gathered_partials, logp_shard_backward, logp_shard_partials, partials_block,
-               partials_views)
+from . import (IGNORE_INDEX, NUM_TILES, flp_tile_width, fused_linear_logp_merge_gathered,
+               fused_linear_logp_shard_backward, fused_linear_logp_shard_partials, fused_linear_logp_workspace_size,
+               fused_logp_backward, fused_logp_forward, logp_merge_gathered_partials, logp_shard_backward,
+               logp_shard_partials, partials_block, partials_views, sum_blocks)
+
+LINEAR_TILE = 256   # vocabulary columns per tile of the fused LM head
 
 __all__ = [
     "PreflightError",
+    "VocabParallelLinearLogp",
     "VocabParallelLogp",
     "gather_rows",
     "preflight",
     "row_parallel_logp_backward",
     "row_parallel_logp_forward",
+    "vocab_parallel_linear_logp",
+    "vocab_parallel_linear_logp_backward",
+    "vocab_parallel_linear_logp_forward",
     "vocab_parallel_logp",
     "vocab_parallel_logp_backward",
     "vocab_parallel_logp_forward",
@@ -71,6 +88,7 @@ class _Spec:
     temperature: float
     ignore_index: int
     masked: bool
+    d: int = 0          # hidden size (the fused LM head)
 
 
 def _world(group) -> tuple[int, int]:
@@ -84,8 +102,10 @@ def _check_specs(specs: list[dict]) -> tuple[list[int], list[int]]:
     Returns the ranks' (vocab_starts, real_widths)."""
     first = specs[0]
     same = ["mode", "v_total", "dtype", "temperature", "ignore_index", "masked"]
-    if first["mode"] == "vocab":
+    if first["mode"] in ("vocab", "linear"):
         same.insert(1, "n")
+    if first["mode"] == "linear":
+        same.insert(2, "d")
     for key in same:
         vals = [s[key] for s in specs]
         if any(v != vals[0] for v in vals):
@@ -93,12 +113,12 @@ def _check_specs(specs: list[dict]) -> tuple[list[int], list[int]]:
                                  ", ".join(f"rank {r}: {v!r}" for r, v in enumerate(vals)))
     starts = [s["vocab_start"] for s in specs]
     widths = [s["real_width"] for s in specs]
-    if first["mode"] != "vocab":
+    if first["mode"] not in ("vocab", "linear"):
         return starts, widths
     v_total = first["v_total"]
     if len(specs) > NUM_TILES:
         raise PreflightError(f"a vocabulary-parallel group has at most {NUM_TILES} ranks (got {len(specs)})")
-    w = flp_tile_width(v_total)
+    w = flp_tile_width(v_total) if first["mode"] == "vocab" else LINEAR_TILE
     n_tiles = -(-v_total // w)
     owner = [-1] * n_tiles
     for r, (a, b) in enumerate(zip(starts, widths)):
@@ -118,15 +138,18 @@ def _check_specs(specs: list[dict]) -> tuple[list[int], list[int]]:
 
 
 def preflight(mode: str, n: int, v_total: int, vocab_start: int, real_width: int, dtype: torch.dtype,
-              temperature: float, ignore_index: int, masked: bool, group=None) -> tuple[list[int], list[int]]:
+              temperature: float, ignore_index: int, masked: bool, group=None,
+              d: int = 0) -> tuple[list[int], list[int]]:
     """All ranks publish their call and check that they agree; on a mismatch
     every rank raises the same PreflightError, before any exchange of
     tensors.  mode "vocab": the same N, vocabulary, dtype, temperature,
     ignore_index and mask use, and shards on the tile grid covering every
-    tile exactly once.  mode "rows": the same vocabulary and mode (row
-    counts may differ).  Returns every rank's (vocab_start, real_width)."""
+    tile exactly once; mode "linear" (the fused LM head): the same, with the
+    hidden size d, on the 256-column grid.  mode "rows": the same vocabulary
+    and mode (row counts may differ).  Returns every rank's (vocab_start,
+    real_width)."""
     spec = asdict(_Spec(mode, int(n), int(v_total), int(vocab_start), int(real_width), str(dtype),
-                        float(temperature), int(ignore_index), bool(masked)))
+                        float(temperature), int(ignore_index), bool(masked), int(d)))
     world, _ = _world(group)
     specs = [spec]
     if world > 1:
@@ -226,6 +249,92 @@ def vocab_parallel_logp(shard_logits: torch.Tensor, targets: torch.Tensor, vocab
     buffer's width)."""
     return VocabParallelLogp.apply(shard_logits, targets, vocab_start, v_total, real_width, group,
                                    ignore_index, temperature, active_mask)
+
+
+def vocab_parallel_linear_logp_forward(hidden: torch.Tensor, weight_shard: torch.Tensor, targets: torch.Tensor,
+                                       vocab_start: int, v_total: int, group=None, ignore_index: int = IGNORE_INDEX,
+                                       temperature: float = 1.0, active_mask: torch.Tensor | None = None,
+                                       with_lse_lo: bool = False):
+    """(logp, lse[, lse_lo]) FP32 [N] of hidden [N, D] @ weight.T over the
+    whole vocabulary, on every rank, from this rank's weight rows
+    weight_shard [w, D] (global columns [vocab_start, vocab_start + w));
+    bitwise the one-GPU fused LM head."""
+    n, d = hidden.shape
+    w = weight_shard.shape[0]
+    starts, widths = preflight("linear", n, v_total, vocab_start, w, hidden.dtype, temperature, ignore_index,
+                               active_mask is not None, group, d=d)
+    ws = torch.empty(fused_linear_logp_workspace_size(n, v_total), dtype=torch.uint8, device=hidden.device)
+    if n > 0:
+        fused_linear_logp_shard_partials(hidden, weight_shard, vocab_start, v_total, targets, ws,
+                                         temperature=temperature)
+    gathered = _all_gather_flat(ws.view(torch.float32), group)
+    return fused_linear_logp_merge_gathered(gathered, starts, widths, targets, v_total, ignore_index,
+                                            with_lse_lo=with_lse_lo, temperature=temperature,
+                                            active_mask=active_mask)
+
+
+def vocab_parallel_linear_logp_backward(hidden: torch.Tensor, weight_shard: torch.Tensor, targets: torch.Tensor,
+                                        vocab_start: int, v_total: int, lse: torch.Tensor, grad: torch.Tensor,
+                                        group=None, lse_lo: torch.Tensor | None = None,
+                                        ignore_index: int = IGNORE_INDEX, temperature: float = 1.0,
+                                        active_mask: torch.Tensor | None = None):
+    """(dhidden [N, D] FP32, the same on every rank; this rank's dweight
+    rows [w, D] FP32) of Σ_t g_t logp_t.  Each rank computes its slice's
+    term of dhidden; the terms are all-gathered and summed in rank order, the
+    order in which the one-GPU sharded backward adds its shards' terms when
+    the ranks hold increasing slices."""
+    n, d = hidden.shape
+    term = torch.empty((n, d), dtype=torch.float32, device=hidden.device)
+    dw = fused_linear_logp_shard_backward(hidden, weight_shard, vocab_start, v_total, targets, lse, grad, term,
+                                          False, ignore_index, lse_lo=lse_lo, temperature=temperature,
+                                          active_mask=active_mask)
+    world, _ = _world(group)
+    if world == 1:
+        return term, dw
+    gathered = _all_gather_flat(term.view(-1), group)
+    return sum_blocks(gathered.view(world, n, d)), dw
+
+
+class VocabParallelLinearLogp(torch.autograd.Function):
+    """logp = VocabParallelLinearLogp.apply(hidden, weight_shard, targets,
+    vocab_start, v_total, group, ignore_index, temperature, active_mask): the
+    fused LM head with the weight's vocabulary rows split across the group's
+    ranks.  Saves the O(N) merged LSE; the backward returns dhidden (the same
+    on every rank) and this rank's dweight rows, in the dtypes of hidden and
+    weight_shard."""
+
+    @staticmethod
+    def forward(ctx, hidden, weight_shard, targets, vocab_start, v_total, group=None, ignore_index=IGNORE_INDEX,
+                temperature=1.0, active_mask=None):
+        logp, lse, lse_lo = vocab_parallel_linear_logp_forward(hidden, weight_shard, targets, vocab_start, v_total,
+                                                               group=group, ignore_index=ignore_index,
+                                                               temperature=temperature, active_mask=active_mask,
+                                                               with_lse_lo=True)
+        ctx.save_for_backward(hidden, weight_shard, targets, lse, lse_lo, active_mask)
+        ctx.args = (int(vocab_start), int(v_total), group, int(ignore_index), float(temperature))
+        return logp
+
+    @staticmethod
+    def backward(ctx, grad_logp):
+        hidden, weight_shard, targets, lse, lse_lo, active_mask = ctx.saved_tensors
+        vocab_start, v_total, group, ignore_index, temperature = ctx.args
+        g = grad_logp.to(torch.float32).contiguous()
+        dh, dw = vocab_parallel_linear_logp_backward(hidden, weight_shard, targets, vocab_start, v_total, lse, g,
+                                                     group=group, lse_lo=lse_lo, ignore_index=ignore_index,
+                                                     temperature=temperature, active_mask=active_mask)
+        dh = dh if hidden.dtype == torch.float32 else dh.to(hidden.dtype)
+        dw = dw if weight_shard.dtype == torch.float32 else dw.to(weight_shard.dtype)
+        return dh, dw, None, None, None, None, None, None, None
+
+
+def vocab_parallel_linear_logp(hidden: torch.Tensor, weight_shard: torch.Tensor, targets: torch.Tensor,
+                               vocab_start: int, v_total: int, group=None, ignore_index: int = IGNORE_INDEX,
+                               temperature: float = 1.0, active_mask: torch.Tensor | None = None) -> torch.Tensor:
+    """Autograd-aware vocabulary-parallel fused LM head + selected-token logp
+    (FP32 [N]) of hidden [N, D] @ weight.T, this rank holding weight rows
+    [vocab_start, vocab_start + weight_shard.shape[0])."""
+    return VocabParallelLinearLogp.apply(hidden, weight_shard, targets, vocab_start, v_total, group, ignore_index,
+                                         temperature, active_mask)
 
 
 def gather_rows(t: torch.Tensor, group=None) -> torch.Tensor:

@@ -350,3 +350,31 @@ def test_shard_backward_validates_the_shard_on_the_host(lib):
     assert st == EINVAL and b"inside the vocabulary" in lib.flp_last_error()
     assert lib.logp_shard_backward(None, 0, 100, 0, 100, 151936, None, -100, None, None, None, None, 100,
                                    None) == 0
+
+
+def test_vocab_parallel_lm_head_host_checks(lib):
+    """The gathered LM-head merge and the ordered block sum validate the rank
+    layout and the extents on the host, before any device access."""
+    I64 = ctypes.c_int64
+    v, n = 20000, 16
+    block = (2 * ((v + 255) // 256) + 1) * n
+
+    def merge(starts, widths, stride=block, world=None):
+        k = len(starts)
+        a = (I64 * max(1, k))(*starts)
+        b = (I64 * max(1, k))(*widths)
+        return lib.fused_linear_logp_merge_gathered(None, stride, k if world is None else world, a, b, n, v, None,
+                                                    -100, None, 1.0, None, None, None, None)
+
+    assert merge([0, 10240], [10240, 9760], world=0) == EINVAL
+    assert merge([0, 10240], [10240, 9760], world=17) == EINVAL
+    assert merge([0, 10240], [10240, 9760], stride=block - 1) == EINVAL and b"rank_stride" in lib.flp_last_error()
+    assert merge([0, 10000], [10000, 10000]) == EUNSUP and b"tile grid" in lib.flp_last_error()
+    assert merge([0, 10496], [10240, 9504]) == EINVAL and b"held by no rank" in lib.flp_last_error()
+    assert merge([0, 9984], [10240, 10016]) == EINVAL and b"held by two ranks" in lib.flp_last_error()
+    assert merge([0, 10240], [10240, 9800]) == EINVAL and b"not inside" in lib.flp_last_error()
+    assert merge([0, 10240], [10240, 9760]) == EINVAL              # the layout is fine; host pointers are not
+    assert lib.flp_sum_blocks(None, 10, 0, 2, 5, None, 5, None) == EINVAL
+    assert lib.flp_sum_blocks(None, 10, 2, 2, 5, None, 4, None) == EINVAL and b"ld_out" in lib.flp_last_error()
+    assert lib.flp_sum_blocks(None, 9, 2, 2, 5, None, 5, None) == EINVAL and b"block_stride" in lib.flp_last_error()
+    assert lib.flp_sum_blocks(None, 10, 2, 0, 5, None, 5, None) == 0   # nothing to sum

@@ -137,3 +137,26 @@ def test_gather_rows_uneven_counts():
         kind, got = res[rank]
         assert kind == "ok", got
         assert torch.equal(torch.from_numpy(got), want)
+
+
+def _lspec(**kw):
+    base = _spec(mode="linear", d=512, v_total=20000)
+    base.update(kw)
+    return base
+
+
+def test_linear_mode_checks_the_256_grid_and_the_hidden_size():
+    """The fused LM head's vocabulary-parallel preflight: slices on the
+    256-column grid of the fused kernel (not the logits path's tile width),
+    covering every tile once, and the same hidden size on every rank."""
+    v = 20000
+    fd._check_specs([_lspec(vocab_start=0, real_width=10240), _lspec(vocab_start=10240, real_width=v - 10240)])
+    fd._check_specs([_lspec(vocab_start=19968, real_width=32), _lspec(vocab_start=0, real_width=19968)])
+    with pytest.raises(fd.PreflightError, match="256-column tile grid"):
+        fd._check_specs([_lspec(vocab_start=0, real_width=10000), _lspec(vocab_start=10000, real_width=10000)])
+    with pytest.raises(fd.PreflightError, match="held by no rank"):
+        fd._check_specs([_lspec(vocab_start=0, real_width=9984), _lspec(vocab_start=10240, real_width=v - 10240)])
+    specs = [_lspec(vocab_start=0, real_width=10240), _lspec(vocab_start=10240, real_width=v - 10240)]
+    specs[1]["d"] = 1024
+    with pytest.raises(fd.PreflightError, match="ranks disagree on d"):
+        fd._check_specs(specs)

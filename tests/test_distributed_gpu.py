@@ -254,3 +254,82 @@ def test_vocab_parallel_device_tensor_transport_path():
         kind, val = res[rank]
         assert kind == "ok", (rank, val)
         assert all(val.values()), (rank, val)
+
+
+# ---------------------------------------------------------------- the fused LM head, vocabulary parallel
+
+@pytest.mark.parametrize("bounds", [(0, 10240, 20000), (0, 5120, 12800, 20000), (0, 256, 512, 19968, 20000)])
+def test_linear_gathered_merge_equals_unsharded_bitwise(bounds):
+    """Each slice of the LM-head weight writes its tiles' partials into its
+    own workspace; the merge over the stacked workspaces (ranks listed in any
+    order) gives the one-GPU forward's logp, lse and lse_lo bit for bit, with
+    temperature and a mask."""
+    n, d, v = 300, 512, 20000
+    h, w, y = workloads.linear(n, d, v, seed=91, device=DEV)
+    mask = (torch.arange(n, device=DEV) % 7 != 3)
+    ref = flp.fused_linear_logp_forward(h, w, y, with_lse_lo=True, temperature=0.7, active_mask=mask)
+    nbytes = flp.fused_linear_logp_workspace_size(n, v)
+    slices = list(zip(bounds[:-1], bounds[1:]))
+    blocks = torch.full((len(slices), nbytes // 4 + 5), float("nan"), device=DEV)   # a stride wider than a block
+    for r, (a, b) in enumerate(slices):
+        ws = torch.full((nbytes,), 0xFF, dtype=torch.uint8, device=DEV)            # other ranks' tiles: garbage
+        flp.fused_linear_logp_shard_partials(h, w[a:b].clone(), a, v, y, ws, temperature=0.7)
+        blocks[r, :nbytes // 4] = ws.view(torch.float32)
+    perm = list(range(len(slices)))[::-1]
+    out = flp.fused_linear_logp_merge_gathered(blocks[perm], [slices[r][0] for r in perm],
+                                               [slices[r][1] - slices[r][0] for r in perm], y, v,
+                                               with_lse_lo=True, temperature=0.7, active_mask=mask)
+    for r, o in zip(ref, out):
+        assert torch.equal(_i(r), _i(o))
+
+
+def test_sum_blocks_is_the_rank_order_sum():
+    g = torch.Generator(device=DEV).manual_seed(3)
+    blocks = torch.randn((4, 333, 257), generator=g, device=DEV) * torch.tensor([1.0, 1e4, 1e-4, 1.0],
+                                                                               device=DEV).view(4, 1, 1)
+    want = ((blocks[0] + blocks[1]) + blocks[2]) + blocks[3]          # the same IEEE additions, in order
+    assert torch.equal(_i(flp.sum_blocks(blocks)), _i(want))
+    assert torch.equal(_i(flp.sum_blocks(blocks[:1])), _i(blocks[0]))
+
+
+def _linear_rank(rank, world, n, d, v, cut):
+    import torch
+
+    import selected_token_logprob_gb300 as flp
+    from selected_token_logprob_gb300 import distributed as fd
+
+    torch.cuda.set_device(0)
+    h, w, y = workloads.linear(n, d, v, seed=97, device=DEV)        # every rank: the same hidden states
+    mask = (torch.arange(n, device=DEV) % 5 != 2)
+    g = torch.randn(n, generator=torch.Generator().manual_seed(98)).to(DEV)
+    bounds = [(0, cut), (cut, v)]
+    # the one-GPU references: the unsharded forward, the sharded backward in slice order
+    ref = flp.fused_linear_logp_forward(h, w, y, with_lse_lo=True, temperature=0.7, active_mask=mask)
+    dh_ref = torch.empty((n, d), device=DEV)
+    dw_ref = [flp.fused_linear_logp_shard_backward(h, w[a:b].clone(), a, v, y, ref[1], g, dh_ref, k > 0,
+                                                   lse_lo=ref[2], temperature=0.7, active_mask=mask)
+              for k, (a, b) in enumerate(bounds)]
+    dh_all, _ = flp.fused_linear_logp_backward(h, w, y, ref[1], g, lse_lo=ref[2], temperature=0.7,
+                                               active_mask=mask)
+    a, b = bounds[rank]
+    hh = h.clone().requires_grad_(True)
+    ws = w[a:b].clone().requires_grad_(True)
+    logp = fd.vocab_parallel_linear_logp(hh, ws, y, a, v, temperature=0.7, active_mask=mask)
+    (logp * g).sum().backward()
+    torch.cuda.synchronize()
+    rel = (torch.max(torch.abs(hh.grad.float() - dh_all)) / torch.max(torch.abs(dh_all))).item()
+    return {"logp": torch.equal(_i(logp.detach()), _i(ref[0])),
+            # autograd returns dhidden in hidden's dtype (BF16): compare with the reference cast the same way
+            "dhidden_sharded_bits": torch.equal(hh.grad.view(torch.int16), dh_ref.to(torch.bfloat16).view(torch.int16)),
+            "dweight_rows_bits": torch.equal(ws.grad.view(torch.int16), dw_ref[rank].to(torch.bfloat16).view(torch.int16)),
+            "dhidden_close_to_unsharded": rel <= 1e-2,
+            "device_error": flp.flp_device_error(0)}
+
+
+def test_vocab_parallel_lm_head_two_ranks_match_one_gpu():
+    res = run_ranks(_linear_rank, 2, (300, 512, 20000, 10240), timeout=600)
+    for rank in range(2):
+        kind, val = res[rank]
+        assert kind == "ok", (rank, val)
+        assert all(v is True for k, v in val.items() if k != "device_error"), (rank, val)
+        assert val["device_error"] == 0
